@@ -1,0 +1,127 @@
+/*
+ * fca.h - formal-concept enumeration (Close-by-One with saturation pruning)
+ * on one GB300 GPU (sm_103a). Plain C ABI: no C++ or framework types.
+ *
+ * A formal context is a binary table of N objects x M attributes. For an
+ * object set X, X' is the set of attributes shared by every object of X; for
+ * an attribute set Y, Y' is the set of objects having every attribute of Y.
+ * A concept is a pair (A, B) with A' = B and B' = A; B is its intent
+ * (FCbO-to-CUDA page, sections 1.1-1.2; Parallel FCBO page, section 1.1).
+ * fca_enumerate outputs every intent exactly once, found by the Close-by-One
+ * search with the canonical prefix test and the saturation skip
+ * (FCbO-to-CUDA page, sections 2.1-2.3 and 4.3; Parallel FCBO page,
+ * sections 1.2-1.3 and 2.1).
+ *
+ * Bit layout (FCbO-to-CUDA page, section 4.3; Parallel FCBO page, section
+ * 3.1): attribute a of a row is bit (a & 31) of 32-bit word (a >> 5), least
+ * significant bit first. A row / intent is W_M = ceil(M/32) words.
+ *
+ * Error behaviour: every call returns a status; nothing aborts the process.
+ * A CUDA error is reported as FCA_ERR_CUDA and its text is kept in the
+ * context (fca_last_error). The library never falls back to the CPU.
+ */
+#ifndef FCA_H
+#define FCA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct fca_ctx fca_ctx; /* opaque; owns the device copies and work pools */
+
+typedef enum {
+    FCA_OK = 0,
+    FCA_ERR_INVALID = 1,  /* bad argument (NULL pointer, N < 1, M < 1, sizes beyond limits) */
+    FCA_ERR_OOM = 2,      /* a device or host allocation failed */
+    FCA_ERR_CAPACITY = 3, /* more concepts than `capacity`; *out_count holds the true total */
+    FCA_ERR_CUDA = 4      /* a CUDA runtime call or kernel failed; see fca_last_error */
+} fca_status;
+
+/* Statistics of the last fca_enumerate call on a context. */
+typedef struct {
+    uint64_t concepts;        /* intents found (= *out_count) */
+    uint64_t closures;        /* candidates (A, B, j) evaluated: j >= cursor, j not in B */
+    uint64_t large_parents;   /* search nodes expanded by the bitmap-extent kernel */
+    uint64_t small_roots;     /* subtrees handed to the object-list kernel (extent <= 32) */
+    uint64_t launches;        /* kernels launched by the call */
+    uint64_t levels;          /* deepest bitmap-frontier level used, plus one */
+    uint64_t max_frontier;    /* largest number of bitmap entries held by one level */
+    uint64_t frontier_bytes;  /* device bytes held by frontier and queue buffers */
+} fca_stats;
+
+/*
+ * Build a context: device copies of the object rows (ctxRows, N x W_M words)
+ * and of their transpose, the attribute columns (ctxCols, M x W_N words with
+ * W_N = ceil(N/32), each column padded to a 16-byte multiple), plus the top
+ * intent G' (AND of all rows). This is the dual row/column layout of the
+ * FCbO-to-CUDA page, section 3.1, and the Parallel FCBO page, section 2.3;
+ * the transpose is built on the GPU (Parallel FCBO page, section 3.1).
+ *
+ *   rows       N x W_M uint32 words, row-major, LSB-first. Host or device
+ *              pointer (copied with cudaMemcpyDefault, read once, not kept).
+ *              Padding bits past M are ignored.
+ *   n_objects  N >= 1.
+ *   n_attrs    1 <= M <= 8192.
+ *   out_ctx    receives the new context (NULL on failure).
+ * Runs on the legacy default stream and returns after it completes.
+ * Uses the current CUDA device; the context must be used on that device.
+ */
+fca_status fca_context_create(const uint32_t *rows, int64_t n_objects, int32_t n_attrs,
+                              fca_ctx **out_ctx);
+
+/*
+ * Enumerate every intent of the context.
+ *
+ *   out        device pointer, capacity x W_M uint32 words, caller-owned.
+ *              Row r receives one intent. Output order is unspecified; the
+ *              top intent G' is row 0 when capacity >= 1. Padding bits are 0.
+ *   capacity   rows available in `out` (0 allowed: count only).
+ *   out_count  host pointer; receives the total number of intents, also when
+ *              it exceeds `capacity`.
+ *   stream     cudaStream_t to run on (NULL = legacy default stream).
+ * Returns FCA_OK, or FCA_ERR_CAPACITY when the total exceeds `capacity`
+ * (the first `capacity` rows are written, the count is exact: retry with a
+ * larger buffer). The call returns after the work on `stream` completes.
+ * One context serves one caller at a time.
+ */
+fca_status fca_enumerate(fca_ctx *ctx, uint32_t *out, uint64_t capacity, uint64_t *out_count,
+                         void *stream);
+
+/*
+ * Like fca_enumerate, but `out_host` is a host pointer (pinned or pageable,
+ * capacity x W_M words). The intents are produced in a device buffer held
+ * by the context and copied back before return.
+ */
+fca_status fca_enumerate_host(fca_ctx *ctx, uint32_t *out_host, uint64_t capacity,
+                              uint64_t *out_count, void *stream);
+
+/* Statistics of the last enumerate call (zeros before the first). */
+fca_status fca_get_stats(const fca_ctx *ctx, fca_stats *out);
+
+/* N and M of the context. */
+fca_status fca_context_dims(const fca_ctx *ctx, int64_t *n_objects, int32_t *n_attrs);
+
+/*
+ * Copy the context's device row or column bitmap into `dst` (host or device
+ * pointer): which = 0 -> rows (N x W_M words), 1 -> columns (M x W_Np words,
+ * W_Np = W_N rounded up to a multiple of 4), 2 -> top intent (W_M words).
+ * `dst_words` is the room in `dst`; FCA_ERR_INVALID if too small.
+ */
+fca_status fca_context_copy(const fca_ctx *ctx, int which, uint32_t *dst, uint64_t dst_words);
+
+/* Text of the last error on this context ("" when none). Valid until the next call. */
+const char *fca_last_error(const fca_ctx *ctx);
+
+/* Release the context and everything it holds. NULL is ignored. */
+void fca_free(fca_ctx *ctx);
+
+/* Static description of a status code. */
+const char *fca_status_string(fca_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FCA_H */
