@@ -1,0 +1,412 @@
+#!/usr/bin/env python
+"""Throughput of full formal-concept enumeration on GB300.
+
+One step = one pass of the whole hot path over one synthetic context: load the
+rows into the context (row copy, padding mask, transpose to columns, top
+intent) and enumerate every intent (bitmap-tier expansion, object-list
+subtrees, compaction into the output buffer). Inputs are resident in device
+memory when the timed region starts; L2 is flushed between timed steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Prints one JSON line (rank 0). With N > 1 (torchrun), every rank enumerates its
+own copy of the workload (independent replicas, no collective on the data
+path); value = concepts of all ranks / slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from closed_set_enumeration_gb300 import contexts as cx  # noqa: E402
+
+METRIC = "concepts/sec (closures/sec) per GB300; fraction of bitwise INT/L2 roofline"
+UNIT = "concepts/s"
+DEFAULT_WORKLOAD = "sparse"
+L2_FLUSH_BYTES = 512 << 20
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+INT_LANES_PER_SM = 64        # 32-bit logical-op results per SM per clock (checked by the LOP3 probe)
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(cx.WORKLOADS))
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="budget of the CPU oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- distributed
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- CPU oracle baseline
+
+def cpu_oracle_rate(rows, w, budget_s: float, threads: int):
+    """Concepts/s of the CPU oracle on a bounded sample of the workload (test-infrastructure code)."""
+    import oracle
+    oracle.cbo(cx.random_context(40, 12, 0.3, 0), 40, 12)   # build/load outside the timing
+    concepts = 0
+    t0 = time.perf_counter()
+    runs = 0
+    limit = 0
+    # full enumerations while they are cheap; a per-thread intent limit otherwise
+    while True:
+        t1 = time.perf_counter()
+        r = oracle.cbo(rows, w.n_objects, w.n_attrs, threads=threads, limit=limit)
+        dt = time.perf_counter() - t1
+        concepts += int(r["intents"].shape[0])
+        runs += 1
+        elapsed = time.perf_counter() - t0
+        if elapsed >= budget_s:
+            break
+        if dt > budget_s / 2 and limit == 0:
+            break
+    sample = (f"{runs} full enumeration(s) of the workload" if limit == 0 else
+              f"{runs} runs limited to {limit} intents per thread")
+    return concepts / elapsed, sample, elapsed
+
+
+def cpu_oracle_limited_rate(rows, w, budget_s: float, threads: int):
+    """Like cpu_oracle_rate, for workloads too large to enumerate on the host in the budget."""
+    import oracle
+    limit = 20000
+    while True:
+        t1 = time.perf_counter()
+        r = oracle.cbo(rows, w.n_objects, w.n_attrs, threads=threads, limit=limit)
+        dt = time.perf_counter() - t1
+        if dt >= budget_s / 4 or limit >= 1 << 26:
+            return int(r["intents"].shape[0]) / dt, \
+                f"search stopped after {limit} intents per thread ({int(r['intents'].shape[0])} intents)", dt
+        limit *= 4
+
+
+def cpu_baseline(rows, w, budget_s: float):
+    threads = os.cpu_count() or 1
+    digests = os.path.join(ROOT, "tests", "golden", "workload_digests.json")
+    full_s = None
+    if os.path.exists(digests):
+        d = json.load(open(digests)).get(w.name)
+        if d:
+            full_s = d.get("oracle_seconds")
+    if full_s is not None and full_s > budget_s:
+        rate, sample, dt = cpu_oracle_limited_rate(rows, w, budget_s, threads)
+    else:
+        rate, sample, dt = cpu_oracle_rate(rows, w, budget_s, threads)
+    return {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample,
+            "seconds": round(dt, 2)}
+
+
+# ----------------------------------------------------------------------------- roofline helpers
+
+def load_peaks():
+    try:
+        return json.load(open(PEAKS_FILE))
+    except (OSError, ValueError):
+        return None
+
+
+def probe_peaks():
+    """LOP3 issue rate and L2 read bandwidth measured on this GPU by the probe library."""
+    import ctypes
+    path = os.path.join(ROOT, "closed_set_enumeration_gb300", "libfca_probe.so")
+    lib = ctypes.CDLL(path)
+    lib.fca_probe_lop3.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double)]
+    lib.fca_probe_read_bw.argtypes = [ctypes.c_uint64, ctypes.c_int, ctypes.POINTER(ctypes.c_double)]
+    ops, ms, l2 = ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
+    out = {}
+    if lib.fca_probe_lop3(ctypes.byref(ops), ctypes.byref(ms)) == 0:
+        out["lop3_gops"] = ops.value / 1e9
+    if lib.fca_probe_read_bw(48 << 20, 5, ctypes.byref(l2)) == 0:
+        out["l2_read_gbs"] = l2.value
+    return out
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args, world, rank, local):
+    import torch
+    from closed_set_enumeration_gb300 import build as fbuild
+    from closed_set_enumeration_gb300 import fca
+
+    fbuild.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = cx.WORKLOADS[args.workload]
+    rows = w.rows()
+    wm = (w.n_attrs + 31) // 32
+    rows_dev = torch.from_numpy(rows.view(np.int32)).to(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    ctx = fca.Context(rows_dev, w.n_objects, w.n_attrs)
+    # one untimed counting pass: the algorithmic work of each kernel, and the exact output size
+    ctx.set_option(fca.FCA_OPT_COUNT_WORK, 1)
+    first = ctx.enumerate(stream=stream)
+    counted = ctx.stats()
+    ctx.set_option(fca.FCA_OPT_COUNT_WORK, 0)
+    concepts = int(first.shape[0])
+    del first
+    out = torch.empty((concepts, wm), dtype=torch.int32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    table_kernels = 2 + (1 if w.n_attrs % 32 else 0)
+
+    def step():
+        ctx.load(rows_dev, stream=stream)
+        st, cnt = ctx.enumerate_into(out, concepts, stream=stream)
+        if st != fca.FCA_OK or cnt != concepts:
+            raise RuntimeError(f"enumeration returned status {st}, count {cnt} (expected {concepts})")
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize(dev)
+
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    step_ms, sub_ms, exp_ms, launches = [], 0.0, 0.0, 0
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    for _ in range(args.steps):
+        flush.zero_()                         # L2 flush between timed steps (outside the events)
+        ev0.record(stream)
+        step()
+        ev1.record(stream)
+        ev1.synchronize()
+        step_ms.append(ev0.elapsed_time(ev1))
+        s = ctx.stats()
+        sub_ms += s["subtree_ms"]
+        exp_ms += s["expand_ms"]
+        launches += s["launches"] + table_kernels
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    last = ctx.stats()
+
+    total_s = max_over_ranks(sum(step_ms) / 1e3, world)
+    value = concepts * args.steps * world / total_s
+    closures_per_s = last["closures"] * args.steps * world / total_s
+
+    # ---- end to end through the C ABI with host buffers: H2D of the rows, D2H of the intents
+    pin_rows = torch.from_numpy(rows.view(np.int32)).pin_memory()
+    pin_out = torch.empty((concepts, wm), dtype=torch.int32).pin_memory()
+    pin_out_np = pin_out.numpy().view(np.uint32)
+    e2e_steps = max(1, args.e2e_steps)
+    for _ in range(2):
+        ctx.load(pin_rows, stream=stream)
+        ctx.enumerate_host(pin_out_np, stream=stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        ctx.load(pin_rows, stream=stream)
+        st, cnt = ctx.enumerate_host(pin_out_np, stream=stream)
+        if cnt != concepts:
+            raise RuntimeError("end-to-end count mismatch")
+    torch.cuda.synchronize(dev)
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    barrier(world)
+
+    # ---- roofline of the dominant kernel
+    probes = probe_peaks() if rank == 0 else {}
+    peaks = load_peaks() or {}
+    sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
+    sm_max = float(peaks.get("sm_max_mhz", 2070.0))
+    steps = args.steps
+    if sub_ms >= exp_ms:
+        per_launch_ops = counted["subtree_word_ops"] / max(1, counted["subtree_launches"])
+        avg_ms = sub_ms / max(1, steps * max(1, last["subtree_launches"]))
+        achieved = per_launch_ops / (avg_ms * 1e-3) / 1e9
+        peak = sm_count * INT_LANES_PER_SM * sm_max * 1e6 / 1e9
+        roofline = {"kernel": "subtree_kernel", "bound": "alu", "achieved": achieved, "peak": peak,
+                    "unit": "Gop/s", "frac": achieved / peak, "traffic": None,
+                    "peak_basis": f"{sm_count} SMs x {INT_LANES_PER_SM} int32 lanes x {sm_max:.0f} MHz",
+                    "probe_lop3_gops": probes.get("lop3_gops"),
+                    "word_ops_per_launch": per_launch_ops, "avg_launch_ms": avg_ms}
+    else:
+        per_launch = counted["expand_bytes"] / max(1, counted["expand_launches"])
+        avg_ms = exp_ms / max(1, steps * max(1, last["expand_launches"]))
+        achieved = per_launch / (avg_ms * 1e-3) / 1e9
+        peak = probes.get("l2_read_gbs") or float(peaks.get("hbm_gbs", 6800.0))
+        roofline = {"kernel": "expand_bitmap_kernel", "bound": "l2", "achieved": achieved, "peak": peak,
+                    "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                    "peak_basis": "L2 read probe (48 MiB buffer) in this run" if probes.get("l2_read_gbs")
+                    else "measured HBM copy bandwidth",
+                    "bytes_per_launch": per_launch, "avg_launch_ms": avg_ms}
+
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
+        "warmup": args.warmup, "ms_per_step": total_s * 1e3 / steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u32", "data": "synthetic",
+        "config": {"workload": w.name, "n_objects": w.n_objects, "n_attrs": w.n_attrs, "seed": w.seed,
+                   "description": w.description, "concepts": concepts, "closures": last["closures"],
+                   "l2": "flushed between timed steps (512 MiB write)",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "closures_per_s": closures_per_s,
+        "e2e": {"value": concepts * e2e_steps * world / e2e_s, "unit": UNIT,
+                "h2d_bytes_per_step": int(rows.nbytes), "d2h_bytes_per_step": int(concepts * wm * 4)},
+        "gpu_launches": launches,
+        "kernel_ms_per_step": {"subtree_kernel": sub_ms / steps, "expand_bitmap_kernel": exp_ms / steps},
+        "roofline": roofline,
+        "clocks": clocks,
+        "probes": probes,
+    }
+    ctx.close()
+    return result
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The CPU oracle as the reference arm: same workload, metric and unit."""
+    w = cx.WORKLOADS[args.workload]
+    rows = w.rows()
+    threads = os.cpu_count() or 1
+    budget = max(1.0, min(args.cpu_seconds, 20.0))
+    rates = []
+    cb = None
+    for _ in range(max(args.warmup, 0)):
+        pass
+    for _ in range(max(1, args.steps)):
+        cb = cpu_baseline(rows, w, budget / max(1, args.steps) if args.steps > 3 else budget)
+        rates.append(cb["value"])
+        if sum(1 for _ in rates) * budget > 240:
+            break
+    value = statistics.median(rates)
+    cb["value"] = value
+    return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
+            "steps": len(rates), "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "u64", "data": "synthetic",
+            "config": {"workload": w.name, "n_objects": w.n_objects, "n_attrs": w.n_attrs, "seed": w.seed},
+            "cpu_baseline": cb,
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse_args()
+    world, rank, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    result = run_ours(args, world, rank, local)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            w = cx.WORKLOADS[args.workload]
+            result["cpu_baseline"] = cpu_baseline(w.rows(), w, args.cpu_seconds)
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

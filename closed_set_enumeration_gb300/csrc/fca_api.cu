@@ -1,0 +1,614 @@
+// C ABI and host driver of libfca.
+//
+// The driver runs the Close-by-One search level by level (Parallel FCBO page,
+// section 2.1: a level is expanded in one launch over all its (parent, j)
+// pairs, and the loop ends when no level holds work), but it never keeps a
+// whole level: each level is expanded in chunks whose worst-case output fits
+// the next level's buffer, and a full buffer is drained depth first before
+// its producer continues. Extent storage therefore stays bounded (the memory
+// concern of the FCbO-to-CUDA page, sections 3.4 and 6.1), and no global
+// dedupe is needed because the canonical test is local (section 2.2).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "fca.h"
+#include "fca_internal.cuh"
+
+using namespace fca;
+
+struct fca_ctx {
+    int device = 0;
+    int sm_count = 0;
+    Dims d{};
+    uint32_t *rows = nullptr;      // n x wm
+    uint32_t *cols = nullptr;      // m x wnp
+    uint32_t *top = nullptr;       // wm
+    uint32_t *full_mask = nullptr; // wm: every attribute (the bottom intent)
+    uint32_t *root_ext = nullptr;  // wnp: every object
+    bool full_row_exists = false;
+    uint32_t *flag_host = nullptr; // pinned: full-row flag readback
+
+    // work pools, allocated on first use and kept for later calls
+    std::vector<Level> levels;
+    std::vector<uint64_t> level_count;
+    std::vector<uint64_t> level_cands;   // candidates held by the entries of each level
+    Queue q[2]{};
+    uint64_t q_count[2]{0, 0};
+    uint64_t level_cap = 0, queue_cap = 0;
+    Counters *ctr = nullptr;        // device
+    Counters *ctr_host = nullptr;   // pinned host mirror
+    uint32_t *stage = nullptr;      // pinned host staging (root entry)
+
+    uint32_t *host_out_dev = nullptr;   // device buffer behind fca_enumerate_host
+    uint64_t host_out_rows = 0;
+
+    size_t pool_bytes = 0;
+    uint64_t level_bytes = 0, queue_entries = 0;   // requested pool sizes
+    int count_work = 0;
+    uint64_t table_launches = 0;   // kernels launched by the last table load
+
+    // device timing of kernel launches: event pairs recorded around each launch
+    std::vector<cudaEvent_t> events;
+    std::vector<int> event_kind;     // per pair: 0 = expand, 1 = subtree
+    size_t pairs_used = 0;
+
+    fca_stats stats{};
+    std::string err;
+};
+
+namespace {
+
+const char *kStatus[] = {"ok", "invalid argument", "out of memory", "capacity exceeded",
+                         "CUDA error"};
+
+fca_status cuda_fail(fca_ctx *c, cudaError_t e, const char *what)
+{
+    if (c) {
+        char buf[256];
+        snprintf(buf, sizeof buf, "%s: %s (%d)", what, cudaGetErrorString(e), (int)e);
+        c->err = buf;
+    }
+    return e == cudaErrorMemoryAllocation ? FCA_ERR_OOM : FCA_ERR_CUDA;
+}
+
+#define CK(call, what)                                      \
+    do {                                                    \
+        cudaError_t e_ = (call);                            \
+        if (e_ != cudaSuccess) return cuda_fail(c, e_, what); \
+    } while (0)
+
+uint64_t env_u64(const char *name, uint64_t dflt)
+{
+    const char *v = getenv(name);
+    if (!v || !*v) return dflt;
+    char *end = nullptr;
+    unsigned long long x = strtoull(v, &end, 10);
+    return (end && *end == 0 && x > 0) ? (uint64_t)x : dflt;
+}
+
+fca_status alloc_dev(fca_ctx *c, void **p, size_t bytes, const char *what)
+{
+    cudaError_t e = cudaMalloc(p, bytes ? bytes : 16);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        c->err = std::string("cudaMalloc failed for ") + what;
+        return FCA_ERR_OOM;
+    }
+    c->pool_bytes += bytes;
+    return FCA_OK;
+}
+
+void size_pools(fca_ctx *c)
+{
+    const Dims &d = c->d;
+    const uint64_t entry = ((uint64_t)d.wnp + d.wm + 1) * 4;
+    const uint64_t M = (uint64_t)d.m;
+    c->level_cap = std::max<uint64_t>(4 * M, c->level_bytes / entry);
+    c->queue_cap = std::max<uint64_t>(4 * M, c->queue_entries);
+}
+
+void free_pools(fca_ctx *c)
+{
+    for (Level &L : c->levels) { cudaFree(L.ext); cudaFree(L.itt); cudaFree(L.y); }
+    c->levels.clear();
+    c->level_count.clear();
+    c->level_cands.clear();
+    for (Queue &Q : c->q) { cudaFree(Q.ids); cudaFree(Q.itt); cudaFree(Q.y); cudaFree(Q.n); Q = Queue{}; }
+    c->pool_bytes = 0;
+}
+
+fca_status ensure_level(fca_ctx *c, size_t idx)
+{
+    while (c->levels.size() <= idx) {
+        Level L{};
+        L.cap = c->level_cap;
+        fca_status s;
+        if ((s = alloc_dev(c, (void **)&L.ext, L.cap * c->d.wnp * 4, "frontier extents")) != FCA_OK) return s;
+        if ((s = alloc_dev(c, (void **)&L.itt, L.cap * c->d.wm * 4, "frontier intents")) != FCA_OK) return s;
+        if ((s = alloc_dev(c, (void **)&L.y, L.cap * 4, "frontier cursors")) != FCA_OK) return s;
+        c->levels.push_back(L);
+        c->level_count.push_back(0);
+        c->level_cands.push_back(0);
+    }
+    return FCA_OK;
+}
+
+fca_status ensure_queues(fca_ctx *c)
+{
+    if (c->q[0].ids) return FCA_OK;
+    for (int i = 0; i < 2; ++i) {
+        Queue &Q = c->q[i];
+        const int per = 32 * (i + 1);
+        Q.cap = c->queue_cap;
+        fca_status s;
+        if ((s = alloc_dev(c, (void **)&Q.ids, Q.cap * per * 4, "queue ids")) != FCA_OK) return s;
+        if ((s = alloc_dev(c, (void **)&Q.itt, Q.cap * c->d.wm * 4, "queue intents")) != FCA_OK) return s;
+        if ((s = alloc_dev(c, (void **)&Q.y, Q.cap * 4, "queue cursors")) != FCA_OK) return s;
+        if ((s = alloc_dev(c, (void **)&Q.n, Q.cap * 4, "queue sizes")) != FCA_OK) return s;
+    }
+    return FCA_OK;
+}
+
+struct Run {
+    fca_ctx *c;
+    uint32_t *out;
+    uint64_t capacity;
+    cudaStream_t st;
+};
+
+// Record the start event of a timed launch; returns the pair index.
+fca_status time_begin(Run &r, int kind, size_t *pair)
+{
+    fca_ctx *c = r.c;
+    if (c->pairs_used == c->event_kind.size()) {
+        cudaEvent_t e0, e1;
+        CK(cudaEventCreate(&e0), "cudaEventCreate");
+        CK(cudaEventCreate(&e1), "cudaEventCreate");
+        c->events.push_back(e0);
+        c->events.push_back(e1);
+        c->event_kind.push_back(0);
+    }
+    *pair = c->pairs_used++;
+    c->event_kind[*pair] = kind;
+    CK(cudaEventRecord(c->events[2 * *pair], r.st), "cudaEventRecord");
+    return FCA_OK;
+}
+
+fca_status time_end(Run &r, size_t pair)
+{
+    fca_ctx *c = r.c;
+    CK(cudaEventRecord(c->events[2 * pair + 1], r.st), "cudaEventRecord");
+    return FCA_OK;
+}
+
+// After the stream is idle: add the recorded launch times to the statistics.
+fca_status time_collect(fca_ctx *c)
+{
+    for (size_t i = 0; i < c->pairs_used; ++i) {
+        float ms = 0.f;
+        CK(cudaEventElapsedTime(&ms, c->events[2 * i], c->events[2 * i + 1]), "cudaEventElapsedTime");
+        if (c->event_kind[i] == 0) c->stats.expand_ms += ms;
+        else c->stats.subtree_ms += ms;
+    }
+    c->pairs_used = 0;
+    return FCA_OK;
+}
+
+fca_status read_counters(Run &r)
+{
+    fca_ctx *c = r.c;
+    CK(cudaMemcpyAsync(c->ctr_host, c->ctr, sizeof(Counters), cudaMemcpyDeviceToHost, r.st),
+       "counter readback");
+    CK(cudaStreamSynchronize(r.st), "stream synchronize");
+    if (c->ctr_host->error) {
+        c->err = "internal work-buffer capacity check failed";
+        return FCA_ERR_CUDA;
+    }
+    return FCA_OK;
+}
+
+// Process every root waiting in object-list queue qi, then empty it.
+fca_status run_subtree(Run &r, int qi)
+{
+    fca_ctx *c = r.c;
+    if (c->q_count[qi] == 0) return FCA_OK;
+    SubtreeArgs a{};
+    a.d = c->d;
+    a.rows = c->rows;
+    a.q = c->q[qi];
+    a.q_count = c->q_count[qi];
+    a.q_index = qi;
+    a.out = r.out;
+    a.capacity = r.capacity;
+    a.ctr = c->ctr;
+    a.count_work = c->count_work;
+    size_t pair = 0;
+    fca_status s;
+    if ((s = time_begin(r, 1, &pair)) != FCA_OK) return s;
+    CK((cudaError_t)launch_subtree(a, qi + 1, c->sm_count, r.st), "subtree kernel launch");
+    if ((s = time_end(r, pair)) != FCA_OK) return s;
+    c->stats.launches++;
+    c->stats.subtree_launches++;
+    c->stats.small_roots += c->q_count[qi];
+    // reset the queue: its append counter and its work cursor
+    CK(cudaMemsetAsync(&c->ctr->q_count[qi], 0, sizeof(unsigned long long), r.st), "queue reset");
+    CK(cudaMemsetAsync(&c->ctr->q_head[qi], 0, sizeof(unsigned long long), r.st), "queue reset");
+    c->q_count[qi] = 0;
+    return FCA_OK;
+}
+
+// Expand every entry of bitmap level `lv`, depth first over chunks.
+fca_status drain(Run &r, size_t lv)
+{
+    fca_ctx *c = r.c;
+    const uint64_t M = (uint64_t)c->d.m;
+    fca_status s;
+    while (c->level_count[lv] > 0) {
+        if ((s = ensure_level(c, lv + 1)) != FCA_OK) return s;
+        const uint64_t free_next = c->levels[lv + 1].cap - c->level_count[lv + 1];
+        if (free_next < M) {
+            if ((s = drain(r, lv + 1)) != FCA_OK) return s;
+            continue;
+        }
+        bool flushed = false;
+        for (int qi = 0; qi < 2; ++qi)
+            if (c->q[qi].cap - c->q_count[qi] < M) {
+                if ((s = run_subtree(r, qi)) != FCA_OK) return s;
+                flushed = true;
+            }
+        if (flushed) continue;
+        const uint64_t room = std::min({free_next, c->q[0].cap - c->q_count[0], c->q[1].cap - c->q_count[1]});
+        const uint64_t have = c->level_count[lv];
+        // each candidate yields at most one child, so the whole level fits when its candidates do
+        uint64_t k = c->level_cands[lv] <= room ? have : std::min<uint64_t>(have, std::max<uint64_t>(1, room / M));
+        const uint64_t begin = have - k;
+
+        // the next level's append counter starts from its current fill
+        c->ctr_host->next_count = c->level_count[lv + 1];
+        CK(cudaMemcpyAsync(&c->ctr->next_count, &c->ctr_host->next_count, sizeof(unsigned long long),
+                           cudaMemcpyHostToDevice, r.st), "counter set");
+        CK(cudaMemsetAsync(&c->ctr->next_cands, 0, sizeof(unsigned long long), r.st), "counter set");
+        CK(cudaMemsetAsync(&c->ctr->chunk_closures, 0, sizeof(unsigned long long), r.st), "counter set");
+
+        ExpandArgs a{};
+        a.d = c->d;
+        a.rows = c->rows;
+        a.cols = c->cols;
+        a.in = c->levels[lv];
+        a.p_begin = begin;
+        a.p_count = k;
+        a.next = c->levels[lv + 1];
+        a.q1 = c->q[0];
+        a.q2 = c->q[1];
+        a.out = r.out;
+        a.capacity = r.capacity;
+        a.ctr = c->ctr;
+        a.count_work = c->count_work;
+        size_t pair = 0;
+        if ((s = time_begin(r, 0, &pair)) != FCA_OK) return s;
+        CK((cudaError_t)launch_expand(a, c->sm_count, r.st), "expand kernel launch");
+        if ((s = time_end(r, pair)) != FCA_OK) return s;
+        c->stats.launches++;
+        c->stats.expand_launches++;
+        c->stats.large_parents += k;
+        if ((s = read_counters(r)) != FCA_OK) return s;
+
+        const uint64_t used = c->ctr_host->chunk_closures;   // candidates of the chunk
+        c->level_cands[lv] = c->level_cands[lv] > used ? c->level_cands[lv] - used : 0;
+        c->level_count[lv] = begin;
+        c->level_count[lv + 1] = c->ctr_host->next_count;
+        c->level_cands[lv + 1] += c->ctr_host->next_cands;
+        c->q_count[0] = c->ctr_host->q_count[0];
+        c->q_count[1] = c->ctr_host->q_count[1];
+        c->stats.levels = std::max<uint64_t>(c->stats.levels, lv + 2);
+        c->stats.max_frontier = std::max<uint64_t>(c->stats.max_frontier, c->level_count[lv + 1]);
+    }
+    c->level_cands[lv] = 0;
+    if (lv + 1 < c->levels.size() && c->level_count[lv + 1] > 0) return drain(r, lv + 1);
+    return FCA_OK;
+}
+
+// Copy the rows in (host or device source), clear padding bits, rebuild the columns (transpose),
+// the top intent and the full-row flag. Everything on stream `st`; returns after it completes.
+fca_status load_table(fca_ctx *c, const uint32_t *rows, cudaStream_t st)
+{
+    const Dims &d = c->d;
+    CK(cudaSetDevice(c->device), "cudaSetDevice");
+    CK(cudaMemcpyAsync(c->rows, rows, (size_t)d.n * d.wm * 4, cudaMemcpyDefault, st), "row copy");
+    CK(cudaMemsetAsync(c->cols, 0, (size_t)d.m * d.wnp * 4, st), "column clear");
+    CK(cudaMemcpyAsync(c->top, c->full_mask, d.wm * 4, cudaMemcpyDeviceToDevice, st), "top reset");
+    CK(cudaMemsetAsync(c->ctr, 0, sizeof(Counters), st), "counter clear");
+    CK((cudaError_t)launch_mask_rows(c->rows, d, st), "padding mask kernel");
+    CK((cudaError_t)launch_transpose(c->rows, c->cols, d, st), "transpose kernel");
+    CK((cudaError_t)launch_top(c->rows, c->top, &c->ctr->error, d, st), "top kernel");
+    CK(cudaMemcpyAsync(c->flag_host, &c->ctr->error, 4, cudaMemcpyDeviceToHost, st), "flag readback");
+    CK(cudaMemsetAsync(c->ctr, 0, sizeof(Counters), st), "counter clear");
+    CK(cudaStreamSynchronize(st), "stream synchronize");
+    c->full_row_exists = *c->flag_host != 0;
+    c->table_launches = 2 + ((d.m & 31) ? 1 : 0);
+    return FCA_OK;
+}
+
+fca_status enumerate_impl(fca_ctx *c, uint32_t *out, uint64_t capacity, uint64_t *out_count,
+                          cudaStream_t st)
+{
+    CK(cudaSetDevice(c->device), "cudaSetDevice");
+    fca_status s;
+    c->stats = fca_stats{};
+    c->pairs_used = 0;
+    if ((s = ensure_queues(c)) != FCA_OK) return s;
+    if ((s = ensure_level(c, 0)) != FCA_OK) return s;
+    for (size_t i = 0; i < c->levels.size(); ++i) { c->level_count[i] = 0; c->level_cands[i] = 0; }
+    c->q_count[0] = c->q_count[1] = 0;
+
+    Run r{c, out, capacity, st};
+    const Dims &d = c->d;
+    // counters: the top intent already occupies output row 0
+    memset(c->ctr_host, 0, sizeof(Counters));
+    c->ctr_host->out_count = 1;
+    if (capacity >= 1)
+        CK(cudaMemcpyAsync(out, c->top, d.wm * 4, cudaMemcpyDeviceToDevice, st), "top intent copy");
+
+    // the root node (G, G', 0)
+    if (d.n <= SMALL_MAX) {
+        const int qi = d.n <= 32 ? 0 : 1;
+        const int per = 32 * (qi + 1);
+        uint32_t *ids = c->stage;
+        for (int i = 0; i < per; ++i) ids[i] = i < d.n ? (uint32_t)i : 0u;
+        int32_t *meta = reinterpret_cast<int32_t *>(c->stage + per);
+        meta[0] = 0;
+        meta[1] = (int32_t)d.n;
+        Queue &Q = c->q[qi];
+        CK(cudaMemcpyAsync(Q.ids, ids, per * 4, cudaMemcpyHostToDevice, st), "root entry");
+        CK(cudaMemcpyAsync(Q.itt, c->top, d.wm * 4, cudaMemcpyDeviceToDevice, st), "root entry");
+        CK(cudaMemcpyAsync(Q.y, &meta[0], 4, cudaMemcpyHostToDevice, st), "root entry");
+        CK(cudaMemcpyAsync(Q.n, &meta[1], 4, cudaMemcpyHostToDevice, st), "root entry");
+        c->ctr_host->q_count[qi] = 1;
+        c->q_count[qi] = 1;
+    } else {
+        Level &L = c->levels[0];
+        int32_t *meta = reinterpret_cast<int32_t *>(c->stage);
+        meta[0] = 0;
+        CK(cudaMemcpyAsync(L.ext, c->root_ext, d.wnp * 4, cudaMemcpyDeviceToDevice, st), "root entry");
+        CK(cudaMemcpyAsync(L.itt, c->top, d.wm * 4, cudaMemcpyDeviceToDevice, st), "root entry");
+        CK(cudaMemcpyAsync(L.y, &meta[0], 4, cudaMemcpyHostToDevice, st), "root entry");
+        c->level_count[0] = 1;
+        c->level_cands[0] = (uint64_t)d.m;   // an upper bound is enough here
+    }
+    CK(cudaMemcpyAsync(c->ctr, c->ctr_host, sizeof(Counters), cudaMemcpyHostToDevice, st), "counters");
+    CK(cudaStreamSynchronize(st), "stream synchronize");
+
+    if ((s = drain(r, 0)) != FCA_OK) return s;
+    if ((s = run_subtree(r, 0)) != FCA_OK) return s;
+    if ((s = run_subtree(r, 1)) != FCA_OK) return s;
+    if ((s = read_counters(r)) != FCA_OK) return s;
+
+    uint64_t total = c->ctr_host->out_count;
+    // The bottom concept (M', M). When some object holds every attribute its extent is not empty and
+    // the search reaches it. Otherwise only empty candidate extents close to it; the search skips
+    // those, and it is added here (a concept is output exactly once either way).
+    if (!c->full_row_exists) {
+        if (total < capacity)
+            CK(cudaMemcpyAsync(out + total * d.wm, c->full_mask, d.wm * 4, cudaMemcpyDeviceToDevice, st),
+               "bottom intent copy");
+        total += 1;
+        CK(cudaStreamSynchronize(st), "stream synchronize");
+    }
+    c->stats.concepts = total;
+    c->stats.closures = c->ctr_host->closures;
+    c->stats.frontier_bytes = c->pool_bytes;
+    c->stats.subtree_word_ops = c->ctr_host->word_ops;
+    c->stats.expand_bytes = c->ctr_host->bytes;
+    if ((s = time_collect(c)) != FCA_OK) return s;
+    *out_count = total;
+    return total > capacity ? FCA_ERR_CAPACITY : FCA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *fca_status_string(fca_status s)
+{
+    int i = (int)s;
+    return (i >= 0 && i < 5) ? kStatus[i] : "unknown status";
+}
+
+const char *fca_last_error(const fca_ctx *ctx) { return ctx ? ctx->err.c_str() : ""; }
+
+void fca_free(fca_ctx *ctx)
+{
+    if (!ctx) return;
+    cudaSetDevice(ctx->device);
+    cudaFree(ctx->rows);
+    cudaFree(ctx->cols);
+    cudaFree(ctx->top);
+    cudaFree(ctx->full_mask);
+    cudaFree(ctx->root_ext);
+    free_pools(ctx);
+    for (cudaEvent_t e : ctx->events) cudaEventDestroy(e);
+    cudaFree(ctx->ctr);
+    cudaFree(ctx->host_out_dev);
+    cudaFreeHost(ctx->ctr_host);
+    cudaFreeHost(ctx->stage);
+    cudaFreeHost(ctx->flag_host);
+    delete ctx;
+}
+
+fca_status fca_context_create(const uint32_t *rows, int64_t n_objects, int32_t n_attrs,
+                              fca_ctx **out_ctx)
+{
+    if (out_ctx) *out_ctx = nullptr;
+    if (!rows || !out_ctx || n_objects < 1 || n_attrs < 1 || n_attrs > MAX_ATTRS ||
+        n_objects > ((int64_t)1 << 31) - 64)
+        return FCA_ERR_INVALID;
+    fca_ctx *c = new fca_ctx();
+    auto fail = [&](fca_status s) {
+        *out_ctx = nullptr;
+        std::string e = c->err;
+        fca_free(c);
+        (void)e;
+        return s;
+    };
+    cudaError_t e = cudaGetDevice(&c->device);
+    if (e != cudaSuccess) { cuda_fail(c, e, "cudaGetDevice"); return fail(FCA_ERR_CUDA); }
+    e = cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, c->device);
+    if (e != cudaSuccess) { cuda_fail(c, e, "device query"); return fail(FCA_ERR_CUDA); }
+    Dims &d = c->d;
+    d.n = n_objects;
+    d.m = n_attrs;
+    d.wm = (n_attrs + 31) / 32;
+    d.wn = (n_objects + 31) / 32;
+    d.wnp = (d.wn + 3) & ~(int64_t)3;
+    // the expand kernel stages one extent per warp in shared memory
+    if (expand_smem_per_warp(d) > 200 * 1024) return fail(FCA_ERR_INVALID);
+
+    fca_status s;
+    if ((s = alloc_dev(c, (void **)&c->rows, (size_t)d.n * d.wm * 4, "rows")) != FCA_OK) return fail(s);
+    if ((s = alloc_dev(c, (void **)&c->cols, (size_t)d.m * d.wnp * 4, "columns")) != FCA_OK) return fail(s);
+    if ((s = alloc_dev(c, (void **)&c->top, (size_t)d.wm * 4, "top")) != FCA_OK) return fail(s);
+    if ((s = alloc_dev(c, (void **)&c->full_mask, (size_t)d.wm * 4, "mask")) != FCA_OK) return fail(s);
+    if ((s = alloc_dev(c, (void **)&c->root_ext, (size_t)d.wnp * 4, "root extent")) != FCA_OK) return fail(s);
+    if ((s = alloc_dev(c, (void **)&c->ctr, sizeof(Counters), "counters")) != FCA_OK) return fail(s);
+    c->pool_bytes = 0;
+    if (cudaMallocHost((void **)&c->ctr_host, sizeof(Counters)) != cudaSuccess ||
+        cudaMallocHost((void **)&c->stage, 4096) != cudaSuccess) {
+        cudaGetLastError();
+        c->err = "pinned host allocation failed";
+        return fail(FCA_ERR_OOM);
+    }
+
+    // host-side constants: the all-attribute intent and the all-object extent
+    std::vector<uint32_t> mask(d.wm, 0xffffffffu), ext(d.wnp, 0u);
+    if (cudaMallocHost((void **)&c->flag_host, 4) != cudaSuccess) {
+        cudaGetLastError();
+        c->err = "pinned host allocation failed";
+        return fail(FCA_ERR_OOM);
+    }
+    if (d.m & 31) mask[d.wm - 1] = (1u << (d.m & 31)) - 1u;
+    for (int64_t w = 0; w < d.wn; ++w) ext[w] = 0xffffffffu;
+    if (d.n & 31) ext[d.wn - 1] = (1u << (d.n & 31)) - 1u;
+
+    if ((e = cudaMemcpy(c->full_mask, mask.data(), d.wm * 4, cudaMemcpyHostToDevice)) != cudaSuccess ||
+        (e = cudaMemcpy(c->root_ext, ext.data(), d.wnp * 4, cudaMemcpyHostToDevice)) != cudaSuccess) {
+        cuda_fail(c, e, "context set-up");
+        return fail(FCA_ERR_CUDA);
+    }
+    if ((s = load_table(c, rows, 0)) != FCA_OK) return fail(s);
+
+    // work-pool sizes (bytes per bitmap level and entries per object-list queue)
+    c->level_bytes = env_u64("FCA_LEVEL_BYTES", 256ull << 20);
+    c->queue_entries = env_u64("FCA_QUEUE_ENTRIES", 1ull << 20);
+    size_pools(c);
+    *out_ctx = c;
+    return FCA_OK;
+}
+
+fca_status fca_enumerate(fca_ctx *ctx, uint32_t *out, uint64_t capacity, uint64_t *out_count, void *stream)
+{
+    if (!ctx || !out_count || (capacity > 0 && !out)) return FCA_ERR_INVALID;
+    ctx->err.clear();
+    return enumerate_impl(ctx, out, capacity, out_count, (cudaStream_t)stream);
+}
+
+fca_status fca_enumerate_host(fca_ctx *ctx, uint32_t *out_host, uint64_t capacity, uint64_t *out_count,
+                              void *stream)
+{
+    if (!ctx || !out_count || (capacity > 0 && !out_host)) return FCA_ERR_INVALID;
+    fca_ctx *c = ctx;
+    c->err.clear();
+    CK(cudaSetDevice(c->device), "cudaSetDevice");
+    if (capacity > c->host_out_rows) {
+        cudaFree(c->host_out_dev);
+        c->host_out_dev = nullptr;
+        c->host_out_rows = 0;
+        void *p = nullptr;
+        if (cudaMalloc(&p, capacity * c->d.wm * 4) != cudaSuccess) {
+            cudaGetLastError();
+            c->err = "cudaMalloc failed for the output buffer";
+            return FCA_ERR_OOM;
+        }
+        c->host_out_dev = (uint32_t *)p;
+        c->host_out_rows = capacity;
+    }
+    cudaStream_t st = (cudaStream_t)stream;
+    fca_status s = enumerate_impl(c, c->host_out_dev, capacity, out_count, st);
+    if (s != FCA_OK && s != FCA_ERR_CAPACITY) return s;
+    const uint64_t rows = std::min<uint64_t>(*out_count, capacity);
+    if (rows) {
+        CK(cudaMemcpyAsync(out_host, c->host_out_dev, rows * c->d.wm * 4, cudaMemcpyDeviceToHost, st),
+           "output copy");
+        CK(cudaStreamSynchronize(st), "stream synchronize");
+    }
+    return s;
+}
+
+fca_status fca_context_load(fca_ctx *ctx, const uint32_t *rows, void *stream)
+{
+    if (!ctx || !rows) return FCA_ERR_INVALID;
+    ctx->err.clear();
+    return load_table(ctx, rows, (cudaStream_t)stream);
+}
+
+fca_status fca_set_option(fca_ctx *ctx, int option, int64_t value)
+{
+    if (!ctx || value < 0) return FCA_ERR_INVALID;
+    fca_ctx *c = ctx;
+    switch (option) {
+    case FCA_OPT_COUNT_WORK:
+        c->count_work = value != 0;
+        return FCA_OK;
+    case FCA_OPT_LEVEL_BYTES:
+    case FCA_OPT_QUEUE_ENTRIES:
+        CK(cudaSetDevice(c->device), "cudaSetDevice");
+        CK(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
+        free_pools(c);
+        if (option == FCA_OPT_LEVEL_BYTES) c->level_bytes = (uint64_t)value;
+        else c->queue_entries = (uint64_t)value;
+        size_pools(c);
+        return FCA_OK;
+    default:
+        return FCA_ERR_INVALID;
+    }
+}
+
+fca_status fca_get_stats(const fca_ctx *ctx, fca_stats *out)
+{
+    if (!ctx || !out) return FCA_ERR_INVALID;
+    *out = ctx->stats;
+    return FCA_OK;
+}
+
+fca_status fca_context_dims(const fca_ctx *ctx, int64_t *n_objects, int32_t *n_attrs)
+{
+    if (!ctx || !n_objects || !n_attrs) return FCA_ERR_INVALID;
+    *n_objects = ctx->d.n;
+    *n_attrs = ctx->d.m;
+    return FCA_OK;
+}
+
+fca_status fca_context_copy(const fca_ctx *ctx, int which, uint32_t *dst, uint64_t dst_words)
+{
+    if (!ctx || !dst) return FCA_ERR_INVALID;
+    const uint32_t *src = nullptr;
+    uint64_t words = 0;
+    switch (which) {
+    case 0: src = ctx->rows; words = (uint64_t)ctx->d.n * ctx->d.wm; break;
+    case 1: src = ctx->cols; words = (uint64_t)ctx->d.m * ctx->d.wnp; break;
+    case 2: src = ctx->top; words = (uint64_t)ctx->d.wm; break;
+    default: return FCA_ERR_INVALID;
+    }
+    if (dst_words < words) return FCA_ERR_INVALID;
+    fca_ctx *c = const_cast<fca_ctx *>(ctx);
+    CK(cudaSetDevice(c->device), "cudaSetDevice");
+    CK(cudaMemcpy(dst, src, words * 4, cudaMemcpyDefault), "context copy");
+    return FCA_OK;
+}
+
+}  // extern "C"

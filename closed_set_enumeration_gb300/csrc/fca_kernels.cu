@@ -1,0 +1,647 @@
+// Kernels of libfca (sm_103a). Bitwise set algebra only: no tensor cores.
+//
+//  transpose_kernel      ctxRows -> ctxCols, 32x32 bit tiles by warp ballots
+//                        (Parallel FCBO page, section 3.1 builds the same
+//                        column bitmaps with one atomicOr per set bit).
+//  top_kernel            top intent G' = AND of all rows, and whether some
+//                        row holds every attribute (then the bottom concept
+//                        has a non-empty extent and the search reaches it).
+//  expand_bitmap_kernel  bitmap tier: one warp per (parent, j) candidate:
+//                        extent intersection, closure, canonical test,
+//                        compaction of the child (FCbO-to-CUDA page, sections
+//                        2.1-2.3, 4.2-4.4; Parallel FCBO page, sections 2.1,
+//                        3.2).
+//  subtree_kernel<NW>    object-list tier: one warp runs a whole subtree whose
+//                        root extent holds at most 32*NW objects.
+#include <cuda_runtime.h>
+
+#include "fca_internal.cuh"
+
+namespace fca {
+namespace {
+
+constexpr unsigned FULL = 0xffffffffu;
+constexpr int OUTBUF = 16;          // intents buffered per warp before one atomicAdd
+
+__device__ __forceinline__ unsigned popc4(const uint4 &x)
+{
+    return __popc(x.x) + __popc(x.y) + __popc(x.z) + __popc(x.w);
+}
+
+// Bits >= b of 32-bit word `w` of a bitset (b is a bit index of the whole set).
+__device__ __forceinline__ uint32_t ge_mask(int w, int b)
+{
+    const int bw = b >> 5;
+    if (w < bw) return 0u;
+    if (w > bw) return FULL;
+    return FULL << (b & 31);
+}
+
+// Bits < b of word `w`.
+__device__ __forceinline__ uint32_t lt_mask(int w, int b) { return ~ge_mask(w, b); }
+
+// ------------------------------------------------------------------ context build
+
+// Clear the padding bits past M in the last word of every row (they are ignored on input).
+__global__ void mask_rows_kernel(uint32_t *rows, Dims d)
+{
+    const long long o = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (o < d.n) rows[o * d.wm + d.wm - 1] &= (1u << (d.m & 31)) - 1u;
+}
+
+__global__ void transpose_kernel(const uint32_t *__restrict__ rows, uint32_t *__restrict__ cols,
+                                 Dims d)
+{
+    const int wpb = blockDim.x >> 5;
+    const long long tile = (long long)blockIdx.x * wpb + (threadIdx.x >> 5);
+    if (tile >= d.wn * (long long)d.wm) return;  // uniform per warp
+    const unsigned lane = threadIdx.x & 31;
+    const long long ot = tile / d.wm;             // 32 objects
+    const int aw = (int)(tile % d.wm);            // 32 attributes
+    const long long o = ot * 32 + lane;
+    uint32_t v = (o < d.n) ? rows[o * d.wm + aw] : 0u;
+    const int valid = d.m - aw * 32;
+    if (valid < 32) v &= (1u << valid) - 1u;      // ignore padding bits
+    uint32_t mine = 0;
+#pragma unroll
+    for (int b = 0; b < 32; ++b) {
+        const uint32_t bal = __ballot_sync(FULL, (v >> b) & 1u);
+        if (lane == (unsigned)b) mine = bal;
+    }
+    const int a = aw * 32 + (int)lane;
+    if (a < d.m) cols[(size_t)a * d.wnp + ot] = mine;
+}
+
+__global__ void top_kernel(const uint32_t *__restrict__ rows, uint32_t *top, uint32_t *flag, Dims d)
+{
+    __shared__ uint32_t red[32];
+    const long long o = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const bool valid = o < d.n;
+    bool full_row = valid;
+    for (int w = 0; w < d.wm; ++w) {
+        const int vb = d.m - w * 32;
+        const uint32_t mask = vb >= 32 ? FULL : ((1u << vb) - 1u);
+        uint32_t v = valid ? (rows[o * d.wm + w] & mask) : FULL;
+        if (valid && v != mask) full_row = false;
+        v = __reduce_and_sync(FULL, v);
+        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+        __syncthreads();
+        if (threadIdx.x < 32) {
+            uint32_t x = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : FULL;
+            x = __reduce_and_sync(FULL, x);
+            if (threadIdx.x == 0) atomicAnd(&top[w], x);
+        }
+        __syncthreads();
+    }
+    if (full_row) atomicOr(flag, 1u);
+}
+
+// ------------------------------------------------------------------ bitmap tier
+
+// C subset of column K? Early exit at the first block of 64 uint4 that disagrees.
+// `loads` counts the column uint4 read (non-zero uint4 of C in the blocks examined).
+__device__ __forceinline__ bool subset_of_column(const uint4 *C, const uint4 *__restrict__ K, int wq,
+                                                 unsigned lane, unsigned &loads)
+{
+    for (int base = 0; base < wq; base += 64) {
+        bool bad = false;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int q = base + h * 32 + (int)lane;
+            if (q < wq) {
+                const uint4 c = C[q];
+                if (c.x | c.y | c.z | c.w) {
+                    const uint4 k = __ldg(K + q);
+                    ++loads;
+                    bad |= ((c.x & ~k.x) | (c.y & ~k.y) | (c.z & ~k.z) | (c.w & ~k.w)) != 0u;
+                }
+            }
+        }
+        if (__any_sync(FULL, bad)) return false;
+    }
+    return true;
+}
+
+template <bool COUNT>
+__global__ void __launch_bounds__(256) expand_bitmap_kernel(ExpandArgs a)
+{
+    extern __shared__ uint4 smem4[];
+    const Dims d = a.d;
+    const int wq = (int)(d.wnp >> 2);
+    const unsigned lane = threadIdx.x & 31;
+    const int wib = threadIdx.x >> 5;
+    const int wpb = blockDim.x >> 5;
+    uint4 *Csm = smem4 + (size_t)wib * (wq + SMALL_MAX / 4);
+    uint32_t *ids = reinterpret_cast<uint32_t *>(Csm + wq);
+    const uint4 *cols4 = reinterpret_cast<const uint4 *>(a.cols);
+    const uint4 *ext4 = reinterpret_cast<const uint4 *>(a.in.ext);
+
+    unsigned long long my_closures = 0, my_next_cands = 0, my_bytes = 0;
+    unsigned loads = 0;   // uint4 loads of columns by this lane (counting only)
+    const unsigned long long total = a.p_count * (unsigned long long)d.m;
+    const unsigned long long nwarps = (unsigned long long)gridDim.x * wpb;
+    for (unsigned long long idx = (unsigned long long)blockIdx.x * wpb + wib; idx < total;
+         idx += nwarps) {
+        const unsigned long long p = a.p_begin + idx / (unsigned)d.m;
+        const int j = (int)(idx % (unsigned)d.m);
+        if (j < a.in.y[p]) continue;
+        const uint32_t *B = a.in.itt + p * d.wm;
+        if ((B[j >> 5] >> (j & 31)) & 1u) continue;      // saturation: A inside column j
+        ++my_closures;
+
+        // C = A & column j, staged in shared memory; |C| by popcount
+        const uint4 *A4 = ext4 + p * wq;
+        const uint4 *J4 = cols4 + (size_t)j * wq;
+        unsigned cnt = 0;
+        for (int q = (int)lane; q < wq; q += 32) {
+            uint4 x = A4[q];
+            if (x.x | x.y | x.z | x.w) {
+                const uint4 c = __ldg(J4 + q);
+                x.x &= c.x; x.y &= c.y; x.z &= c.z; x.w &= c.w;
+                if (COUNT) ++loads;
+            }
+            Csm[q] = x;
+            cnt += popc4(x);
+        }
+        cnt = __reduce_add_sync(FULL, cnt);
+        if (COUNT && lane == 0) my_bytes += (unsigned long long)d.wnp * 4;   // the parent extent
+        if (cnt == 0) continue;   // empty extent: its closure is the bottom, added by the host
+        __syncwarp();
+
+        // object ids of C in ascending order: all of them when |C| <= SMALL_MAX, else the first 32
+        const unsigned need = cnt <= (unsigned)SMALL_MAX ? cnt : 32u;
+        unsigned got = 0;
+        for (int base = 0; base < wq && got < need; base += 32) {
+            const int q = base + (int)lane;
+            const uint4 x = q < wq ? Csm[q] : make_uint4(0u, 0u, 0u, 0u);
+            const unsigned pc = popc4(x);
+            unsigned incl = pc;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const unsigned t = __shfl_up_sync(FULL, incl, off);
+                if (lane >= (unsigned)off) incl += t;
+            }
+            unsigned pos = got + incl - pc;
+            const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                uint32_t bits = w4[t];
+                while (bits && pos < need) {
+                    const int b = __ffs(bits) - 1;
+                    bits &= bits - 1u;
+                    ids[pos++] = (uint32_t)((4 * q + t) * 32 + b);
+                }
+            }
+            got += __shfl_sync(FULL, incl, 31);
+        }
+        __syncwarp();
+
+        // U = AND of the rows of those objects (exact D when |C| <= SMALL_MAX). Lane w: word w.
+        uint32_t U = FULL, Bw = 0;
+        if (lane < (unsigned)d.wm) {
+            for (unsigned i = 0; i < need; ++i) U &= __ldg(a.rows + (size_t)ids[i] * d.wm + lane);
+            Bw = B[lane];
+        } else {
+            U = 0;
+        }
+        if (COUNT && lane == 0) my_bytes += (unsigned long long)need * d.wm * 4;   // rows read
+        const int ju = j >> 5;
+        const uint32_t jbit = 1u << (j & 31);
+        const uint32_t pm = lt_mask((int)lane, j);   // attributes below j
+        uint32_t Dw;
+        bool canon = true;
+        if (cnt <= (unsigned)SMALL_MAX) {
+            Dw = U;
+            canon = !__any_sync(FULL, (U & ~Bw & pm) != 0u);
+        } else {
+            // attributes that may still join: in U, not in B, not j. Test each against the columns,
+            // in ascending order, so a violation below j ends the candidate early.
+            uint32_t X = U & ~Bw;
+            if ((int)lane == ju) X &= ~jbit;
+            Dw = Bw | ((int)lane == ju ? jbit : 0u);
+            for (;;) {
+                const unsigned bal = __ballot_sync(FULL, X != 0u);
+                if (!bal) break;
+                const int u = __ffs(bal) - 1;
+                const uint32_t xw = __shfl_sync(FULL, X, u);
+                const int b = __ffs(xw) - 1;
+                const int k = u * 32 + b;
+                if ((int)lane == u) X &= ~(1u << b);
+                if (subset_of_column(Csm, cols4 + (size_t)k * wq, wq, lane, loads)) {
+                    if (k < j) { canon = false; break; }
+                    if ((int)lane == u) Dw |= 1u << b;
+                }
+            }
+        }
+        if (!canon) continue;
+
+        if (COUNT && lane == 0) {   // the intent row and the child entry written
+            my_bytes += (unsigned long long)d.wm * 4;
+            my_bytes += cnt <= (unsigned)SMALL_MAX
+                            ? (unsigned long long)(4 * (cnt <= 32u ? 32 : 64) + 4 * d.wm + 8)
+                            : (unsigned long long)(4 * d.wnp + 4 * d.wm + 4);
+        }
+        // emit the intent
+        unsigned long long slot = 0;
+        if (lane == 0) slot = atomicAdd(&a.ctr->out_count, 1ull);
+        slot = __shfl_sync(FULL, slot, 0);
+        if (slot < a.capacity && lane < (unsigned)d.wm) a.out[slot * d.wm + lane] = Dw;
+
+        // the child (C, D, j+1)
+        if (cnt <= (unsigned)SMALL_MAX) {
+            const int qi = cnt <= 32u ? 0 : 1;
+            const Queue &Q = qi == 0 ? a.q1 : a.q2;
+            const int per = qi == 0 ? 32 : 64;
+            unsigned long long s = 0;
+            if (lane == 0) s = atomicAdd(&a.ctr->q_count[qi], 1ull);
+            s = __shfl_sync(FULL, s, 0);
+            if (s >= Q.cap) {
+                if (lane == 0) atomicOr(&a.ctr->error, 1u);
+                continue;
+            }
+            for (int i = (int)lane; i < per; i += 32) Q.ids[s * per + i] = i < (int)cnt ? ids[i] : 0u;
+            if (lane < (unsigned)d.wm) Q.itt[s * d.wm + lane] = Dw;
+            if (lane == 0) { Q.y[s] = j + 1; Q.n[s] = (int)cnt; }
+        } else {
+            unsigned long long s = 0;
+            if (lane == 0) s = atomicAdd(&a.ctr->next_count, 1ull);
+            s = __shfl_sync(FULL, s, 0);
+            if (s >= a.next.cap) {
+                if (lane == 0) atomicOr(&a.ctr->error, 2u);
+                continue;
+            }
+            uint4 *dst = reinterpret_cast<uint4 *>(a.next.ext) + s * wq;
+            for (int q = (int)lane; q < wq; q += 32) dst[q] = Csm[q];
+            if (lane < (unsigned)d.wm) a.next.itt[s * d.wm + lane] = Dw;
+            if (lane == 0) a.next.y[s] = j + 1;
+            // candidates of the child: attributes > j not in D
+            unsigned c = lane < (unsigned)d.wm ? __popc(Dw & ge_mask((int)lane, j + 1)) : 0u;
+            c = __reduce_add_sync(FULL, c);
+            my_next_cands += (unsigned long long)(d.m - j - 1 - (int)c);
+        }
+        __syncwarp();
+    }
+    if (COUNT) {
+        const unsigned tl = __reduce_add_sync(FULL, loads);
+        if (lane == 0) atomicAdd(&a.ctr->bytes, my_bytes + 16ull * tl);
+    }
+    if (lane == 0) {
+        if (my_closures) {
+            atomicAdd(&a.ctr->closures, my_closures);
+            atomicAdd(&a.ctr->chunk_closures, my_closures);
+        }
+        if (my_next_cands) atomicAdd(&a.ctr->next_cands, my_next_cands);
+    }
+}
+
+// ------------------------------------------------------------------ object-list tier
+
+struct SubtreeLayout {
+    int mp, wm, fr, fs;
+    size_t o_rmap, o_rootb, o_rm, o_rlo, o_sufb, o_stack, o_outbuf, words;
+    __host__ __device__ SubtreeLayout(const Dims &d, int nw)
+    {
+        mp = (d.m + 31) & ~31;
+        wm = d.wm;
+        fr = (32 * nw < d.m ? 32 * nw : d.m) + 1;     // depth <= |extent| and <= |R|
+        fs = nw + 1 + wm;                             // frame: extent mask, cursor, intent
+        o_rmap = (size_t)nw * mp;
+        o_rootb = o_rmap + mp / 2;
+        o_rm = o_rootb + 32;
+        o_rlo = o_rm + 32;
+        o_sufb = o_rlo + 34;
+        o_stack = o_sufb + 32;
+        o_outbuf = o_stack + (size_t)fr * fs;
+        words = o_outbuf + (size_t)OUTBUF * wm;
+        words = (words + 3) & ~(size_t)3;
+    }
+};
+
+template <int NW, bool COUNT>
+__global__ void __launch_bounds__(256) subtree_kernel(SubtreeArgs a)
+{
+    extern __shared__ uint32_t smw[];
+    const Dims d = a.d;
+    const SubtreeLayout L(d, NW);
+    const unsigned lane = threadIdx.x & 31;
+    uint32_t *base = smw + (size_t)(threadIdx.x >> 5) * L.words;
+    uint32_t *cR = base;                                         // NW planes x mp
+    uint16_t *rmap = reinterpret_cast<uint16_t *>(base + L.o_rmap);
+    uint32_t *rootB = base + L.o_rootb;
+    uint32_t *Rm = base + L.o_rm;
+    uint32_t *rlo = base + L.o_rlo;
+    uint32_t *sufB = base + L.o_sufb;
+    uint32_t *stk = base + L.o_stack;
+    uint32_t *ob = base + L.o_outbuf;
+    const int mp = L.mp, WM = d.wm, FS = L.fs, PER = 32 * NW;
+
+    unsigned long long my_closures = 0, my_ops = 0;
+    int nb = 0;   // intents waiting in the output buffer
+
+    auto flush = [&]() {
+        unsigned long long b0 = 0;
+        if (lane == 0) b0 = atomicAdd(&a.ctr->out_count, (unsigned long long)nb);
+        b0 = __shfl_sync(FULL, b0, 0);
+        __syncwarp();
+        for (int i = (int)lane; i < nb * WM; i += 32)
+            if (b0 + (unsigned long long)(i / WM) < a.capacity) a.out[b0 * WM + i] = ob[i];
+        __syncwarp();
+        nb = 0;
+    };
+
+    for (;;) {
+        unsigned long long r = 0;
+        if (lane == 0) r = atomicAdd(&a.ctr->q_head[a.q_index], 1ull);
+        r = __shfl_sync(FULL, r, 0);
+        if (r >= a.q_count) break;
+
+        // ---- root: object ids, intent, cursor
+        const int n = a.q.n[r];
+        const int y0 = a.q.y[r];
+        uint32_t id[NW];
+#pragma unroll
+        for (int t = 0; t < NW; ++t) {
+            const int o = 32 * t + (int)lane;
+            id[t] = o < n ? a.q.ids[r * PER + o] : 0u;
+        }
+        const uint32_t myRootB = lane < (unsigned)WM ? a.q.itt[r * WM + lane] : 0u;
+        rootB[lane] = myRootB;
+
+        // ---- relevant attributes R (held by some but not all objects), compact index order = attribute
+        //      order, and the columns restricted to the subtree's objects (one ballot per attribute)
+        int R = 0;
+        for (int w = 0; w < WM; ++w) {
+            uint32_t rw[NW];
+            uint32_t uni = 0;
+#pragma unroll
+            for (int t = 0; t < NW; ++t) {
+                rw[t] = (32 * t + (int)lane < n) ? __ldg(a.rows + (size_t)id[t] * WM + w) : 0u;
+                uni |= rw[t];
+            }
+            uni = __reduce_or_sync(FULL, uni);
+            const uint32_t rm = uni & ~__shfl_sync(FULL, myRootB, w);
+            if (lane == 0) { Rm[w] = rm; rlo[w] = (uint32_t)R; }
+            uint32_t bits = rm;
+            while (bits) {
+                const int b = __ffs(bits) - 1;
+                bits &= bits - 1u;
+#pragma unroll
+                for (int t = 0; t < NW; ++t) {
+                    const uint32_t bal = __ballot_sync(FULL, (rw[t] >> b) & 1u);
+                    if (lane == 0) cR[t * mp + R] = bal;
+                }
+                if (lane == 0) rmap[R] = (uint16_t)(32 * w + b);
+                ++R;
+            }
+        }
+        if (lane == 0) rlo[WM] = (uint32_t)R;
+        {
+            // sufB[w] = number of root-intent attributes in words above w
+            const unsigned pc = lane < (unsigned)WM ? __popc(myRootB) : 0u;
+            unsigned incl = pc;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const unsigned t = __shfl_up_sync(FULL, incl, off);
+                if (lane >= (unsigned)off) incl += t;
+            }
+            const unsigned tot = __shfl_sync(FULL, incl, 31);
+            sufB[lane] = tot - incl;
+        }
+        __syncwarp();
+
+        // ---- candidates of the root: attributes >= y0 outside its intent
+        {
+            unsigned c = lane < (unsigned)WM ? __popc(myRootB & ge_mask((int)lane, y0)) : 0u;
+            c = __reduce_add_sync(FULL, c);
+            if (lane == 0) my_closures += (unsigned long long)(d.m - y0 - (int)c);
+        }
+        int jn;   // compact cursor: relevant attributes below y0 are not candidates
+        {
+            const unsigned c = lane < (unsigned)WM ? __popc(Rm[lane] & lt_mask((int)lane, y0)) : 0u;
+            jn = (int)__reduce_add_sync(FULL, c);
+        }
+
+        // ---- depth-first search of the subtree
+        const uint32_t validR = ge_mask((int)lane, 0) & lt_mask((int)lane, R);
+        uint32_t myB = 0;          // compact intent of the current node, word `lane`
+        uint32_t ext[NW];          // current extent as a mask over the n objects
+#pragma unroll
+        for (int t = 0; t < NW; ++t) {
+            const int k = n - 32 * t;
+            ext[t] = k >= 32 ? FULL : (k > 0 ? ((1u << k) - 1u) : 0u);
+        }
+        int depth = 0;
+        for (;;) {
+            const uint32_t cw = ~myB & validR & ge_mask((int)lane, jn);
+            const unsigned bal = __ballot_sync(FULL, cw != 0u);
+            if (bal == 0u) {
+                if (depth == 0) break;
+                --depth;
+                const uint32_t *f = stk + (size_t)depth * FS;
+#pragma unroll
+                for (int t = 0; t < NW; ++t) ext[t] = f[t];
+                jn = (int)f[NW];
+                myB = lane < (unsigned)WM ? f[NW + 1 + lane] : 0u;
+                __syncwarp();
+                continue;
+            }
+            const int u0 = __ffs(bal) - 1;
+            const uint32_t cwu = __shfl_sync(FULL, cw, u0);
+            const int j = u0 * 32 + __ffs(cwu) - 1;
+            jn = j + 1;
+
+            uint32_t C[NW];
+            bool nonempty = false;
+#pragma unroll
+            for (int t = 0; t < NW; ++t) {
+                C[t] = ext[t] & cR[t * mp + j];
+                nonempty |= C[t] != 0u;
+            }
+            if (COUNT) my_ops += NW;      // the extent intersection
+            if (!nonempty) continue;      // empty extent: bottom concept, added by the host
+
+            // closure over the relevant attributes, canonical prefix first
+            const int ju = j >> 5;
+            const uint32_t jm = (1u << (j & 31)) - 1u;
+            const int WR = (R + 31) >> 5;
+            bool canon = true;
+            uint32_t myD = 0;
+            for (int u = 0; u < WR; ++u) {
+                const int k = u * 32 + (int)lane;
+                bool in = k < R;
+                if (in) {
+#pragma unroll
+                    for (int t = 0; t < NW; ++t) in = in && ((C[t] & ~cR[t * mp + k]) == 0u);
+                }
+                const uint32_t Du = __ballot_sync(FULL, in);
+                if (COUNT) my_ops += 2ull * NW * (unsigned)min(32, R - 32 * u) + (u <= ju ? 2 : 0);
+                if (u <= ju) {
+                    const uint32_t Bu = __shfl_sync(FULL, myB, u);
+                    const uint32_t pm = u < ju ? FULL : jm;
+                    if (Du & ~Bu & pm) { canon = false; break; }
+                }
+                if ((int)lane == u) myD = Du;
+            }
+            if (!canon) continue;
+
+            // ---- canonical child (C, D, j+1): write its full intent = root intent + D mapped back
+            {
+                const int w = lane < (unsigned)WM ? (int)lane : 0;
+                const int lo = (int)rlo[w], hi = (int)rlo[w + 1];
+                const int su = (lo >> 5) & 31, sh = lo & 31;
+                const uint32_t s0 = __shfl_sync(FULL, myD, su);
+                const uint32_t s1 = __shfl_sync(FULL, myD, (su + 1) & 31);
+                if (lane < (unsigned)WM) {
+                    uint32_t seg = sh ? ((s0 >> sh) | (s1 << (32 - sh))) : s0;
+                    const int len = hi - lo;
+                    if (len < 32) seg &= (1u << len) - 1u;
+                    uint32_t rmw = Rm[w], res = rootB[w];
+                    int i = 0;
+                    while (rmw) {
+                        const int b = __ffs(rmw) - 1;
+                        rmw &= rmw - 1u;
+                        if ((seg >> i) & 1u) res |= 1u << b;
+                        ++i;
+                    }
+                    ob[nb * WM + w] = res;
+                }
+                ++nb;
+                if (COUNT) my_ops += (unsigned)WM;   // the intent words written
+                __syncwarp();
+                if (nb == OUTBUF) flush();
+            }
+            {
+                // candidates of the child: attributes after rmap[j] outside its intent
+                const int rj = rmap[j];
+                const int rw = rj >> 5, rb = rj & 31;
+                const uint32_t above = rb == 31 ? 0u : (rootB[rw] >> (rb + 1));
+                unsigned c = __popc(myD & ge_mask((int)lane, j + 1) & validR);
+                c = __reduce_add_sync(FULL, c);
+                if (lane == 0)
+                    my_closures += (unsigned long long)(d.m - rj - 1 - (int)sufB[rw] - __popc(above) -
+                                                        (int)c);
+            }
+            // push the current node, descend
+            {
+                uint32_t *f = stk + (size_t)depth * FS;
+#pragma unroll
+                for (int t = 0; t < NW; ++t)
+                    if ((int)lane == t) f[t] = ext[t];
+                if (lane == 0) f[NW] = (uint32_t)jn;
+                if (lane < (unsigned)WM) f[NW + 1 + lane] = myB;
+                __syncwarp();
+                ++depth;
+#pragma unroll
+                for (int t = 0; t < NW; ++t) ext[t] = C[t];
+                myB = myD;
+            }
+        }
+        __syncwarp();
+    }
+    if (nb) flush();
+    if (lane == 0 && my_closures) atomicAdd(&a.ctr->closures, my_closures);
+    if (COUNT && lane == 0 && my_ops) atomicAdd(&a.ctr->word_ops, my_ops);
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ launch wrappers
+
+int launch_mask_rows(uint32_t *rows, const Dims &d, void *stream)
+{
+    if ((d.m & 31) == 0) return (int)cudaSuccess;
+    const int tpb = 256;
+    mask_rows_kernel<<<(unsigned)((d.n + tpb - 1) / tpb), tpb, 0, (cudaStream_t)stream>>>(rows, d);
+    return (int)cudaGetLastError();
+}
+
+int launch_transpose(const uint32_t *rows, uint32_t *cols, const Dims &d, void *stream)
+{
+    const long long tiles = d.wn * (long long)d.wm;
+    const int wpb = 8;
+    const long long blocks = (tiles + wpb - 1) / wpb;
+    transpose_kernel<<<(unsigned)blocks, wpb * 32, 0, (cudaStream_t)stream>>>(rows, cols, d);
+    return (int)cudaGetLastError();
+}
+
+int launch_top(const uint32_t *rows, uint32_t *top, uint32_t *flag, const Dims &d, void *stream)
+{
+    const int tpb = 256;
+    const long long blocks = (d.n + tpb - 1) / tpb;
+    top_kernel<<<(unsigned)blocks, tpb, 0, (cudaStream_t)stream>>>(rows, top, flag, d);
+    return (int)cudaGetLastError();
+}
+
+size_t expand_smem_per_warp(const Dims &d)
+{
+    return ((size_t)(d.wnp / 4) + SMALL_MAX / 4) * sizeof(uint4);
+}
+
+size_t subtree_smem_per_warp(const Dims &d, int nw) { return SubtreeLayout(d, nw).words * 4; }
+
+static int warps_for(size_t per_warp)
+{
+    const size_t budget = 200 * 1024;
+    int w = 8;
+    while (w > 1 && (size_t)w * per_warp > budget) --w;
+    return w;
+}
+
+template <bool COUNT>
+static int launch_expand_t(const ExpandArgs &a, int sm_count, void *stream)
+{
+    const size_t pw = expand_smem_per_warp(a.d);
+    const int wpb = warps_for(pw);
+    const size_t smem = pw * wpb;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(expand_bitmap_kernel<COUNT>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return (int)e;
+    }
+    int per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, expand_bitmap_kernel<COUNT>, wpb * 32, smem);
+    if (per_sm < 1) per_sm = 1;
+    const unsigned long long total = a.p_count * (unsigned long long)a.d.m;
+    unsigned long long blocks = (total + wpb - 1) / wpb;
+    const unsigned long long cap = (unsigned long long)sm_count * per_sm * 4;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    expand_bitmap_kernel<COUNT><<<(unsigned)blocks, wpb * 32, smem, (cudaStream_t)stream>>>(a);
+    return (int)cudaGetLastError();
+}
+
+int launch_expand(const ExpandArgs &a, int sm_count, void *stream)
+{
+    return a.count_work ? launch_expand_t<true>(a, sm_count, stream) : launch_expand_t<false>(a, sm_count, stream);
+}
+
+template <int NW, bool COUNT>
+static int launch_subtree_nw(const SubtreeArgs &a, int sm_count, void *stream)
+{
+    const size_t pw = subtree_smem_per_warp(a.d, NW);
+    const int wpb = warps_for(pw);
+    const size_t smem = pw * wpb;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(subtree_kernel<NW, COUNT>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return (int)e;
+    }
+    int per_sm = 0;
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, subtree_kernel<NW, COUNT>, wpb * 32, smem);
+    if (per_sm < 1) per_sm = 1;
+    unsigned long long blocks = (a.q_count + wpb - 1) / wpb;
+    const unsigned long long cap = (unsigned long long)sm_count * per_sm;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    subtree_kernel<NW, COUNT><<<(unsigned)blocks, wpb * 32, smem, (cudaStream_t)stream>>>(a);
+    return (int)cudaGetLastError();
+}
+
+int launch_subtree(const SubtreeArgs &a, int nw, int sm_count, void *stream)
+{
+    if (a.count_work)
+        return nw == 1 ? launch_subtree_nw<1, true>(a, sm_count, stream) : launch_subtree_nw<2, true>(a, sm_count, stream);
+    return nw == 1 ? launch_subtree_nw<1, false>(a, sm_count, stream) : launch_subtree_nw<2, false>(a, sm_count, stream);
+}
+
+}  // namespace fca

@@ -41,15 +41,28 @@ typedef enum {
 
 /* Statistics of the last fca_enumerate call on a context. */
 typedef struct {
-    uint64_t concepts;        /* intents found (= *out_count) */
-    uint64_t closures;        /* candidates (A, B, j) evaluated: j >= cursor, j not in B */
-    uint64_t large_parents;   /* search nodes expanded by the bitmap-extent kernel */
-    uint64_t small_roots;     /* subtrees handed to the object-list kernel (extent <= 32) */
-    uint64_t launches;        /* kernels launched by the call */
-    uint64_t levels;          /* deepest bitmap-frontier level used, plus one */
-    uint64_t max_frontier;    /* largest number of bitmap entries held by one level */
-    uint64_t frontier_bytes;  /* device bytes held by frontier and queue buffers */
+    uint64_t concepts;         /* intents found (= *out_count) */
+    uint64_t closures;         /* candidates (A, B, j) evaluated: j >= cursor, j not in B */
+    uint64_t large_parents;    /* search nodes expanded by the bitmap-extent kernel */
+    uint64_t small_roots;      /* subtrees handed to the object-list kernel (extent <= 64) */
+    uint64_t launches;         /* kernels launched by the call */
+    uint64_t levels;           /* deepest bitmap-frontier level used, plus one */
+    uint64_t max_frontier;     /* largest number of bitmap entries held by one level */
+    uint64_t frontier_bytes;   /* device bytes held by frontier and queue buffers */
+    uint64_t expand_launches;  /* launches of the bitmap-extent kernel */
+    uint64_t subtree_launches; /* launches of the object-list kernels */
+    uint64_t subtree_word_ops; /* counted work of the object-list tier (FCA_OPT_COUNT_WORK) */
+    uint64_t expand_bytes;     /* counted bytes moved by the bitmap tier (FCA_OPT_COUNT_WORK) */
+    double expand_ms;          /* device time of the bitmap-extent kernel launches */
+    double subtree_ms;         /* device time of the object-list kernel launches */
 } fca_stats;
+
+/* Options for fca_set_option. */
+typedef enum {
+    FCA_OPT_COUNT_WORK = 1,    /* 0/1: count the algorithmic work of each kernel (slower) */
+    FCA_OPT_LEVEL_BYTES = 2,   /* bytes of one bitmap-frontier level buffer (default 512 MiB) */
+    FCA_OPT_QUEUE_ENTRIES = 3  /* entries of each object-list queue (default 2^21) */
+} fca_option;
 
 /*
  * Build a context: device copies of the object rows (ctxRows, N x W_M words)
@@ -63,13 +76,22 @@ typedef struct {
  *              pointer (copied with cudaMemcpyDefault, read once, not kept).
  *              Padding bits past M are ignored.
  *   n_objects  N >= 1.
- *   n_attrs    1 <= M <= 8192.
+ *   n_attrs    1 <= M <= 1024.
  *   out_ctx    receives the new context (NULL on failure).
  * Runs on the legacy default stream and returns after it completes.
  * Uses the current CUDA device; the context must be used on that device.
  */
 fca_status fca_context_create(const uint32_t *rows, int64_t n_objects, int32_t n_attrs,
                               fca_ctx **out_ctx);
+
+/*
+ * Replace the context's table with new rows of the same N x M and rebuild
+ * its columns and top intent, reusing every allocation (a new batch of the
+ * same shape). `rows` as for fca_context_create (host or device pointer);
+ * the work runs on `stream` (cudaStream_t, NULL = legacy default stream) and
+ * the call returns after it completes.
+ */
+fca_status fca_context_load(fca_ctx *ctx, const uint32_t *rows, void *stream);
 
 /*
  * Enumerate every intent of the context.
@@ -96,6 +118,14 @@ fca_status fca_enumerate(fca_ctx *ctx, uint32_t *out, uint64_t capacity, uint64_
  */
 fca_status fca_enumerate_host(fca_ctx *ctx, uint32_t *out_host, uint64_t capacity,
                               uint64_t *out_count, void *stream);
+
+/*
+ * Set an option of a context (fca_option). The two pool sizes are rounded up
+ * to hold at least 4*M entries; changing them frees the pools, which are
+ * allocated again by the next enumerate call. FCA_ERR_INVALID for an unknown
+ * option or a negative value.
+ */
+fca_status fca_set_option(fca_ctx *ctx, int option, int64_t value);
 
 /* Statistics of the last enumerate call (zeros before the first). */
 fca_status fca_get_stats(const fca_ctx *ctx, fca_stats *out);

@@ -64,6 +64,7 @@ typedef struct {
     uint64_t *depth_counts; /* m + 2 entries */
     int want_extents;
     int oom;
+    uint64_t limit;      /* stop descending once this many intents are output (0 = no limit) */
 } osink;
 
 static int bit_of(const uint64_t *set, int64_t i) { return (int)((set[i >> 6] >> (i & 63)) & 1u); }
@@ -124,6 +125,7 @@ static void visit(const octx *c, osink *s, oframe *stack, const uint64_t *a, con
                   int32_t y, int depth)
 {
     sink_emit(c, s, a, b, depth);
+    if (s->limit && s->count >= s->limit) return;   /* bounded sample (timing only) */
     uint64_t *cc = stack[depth + 1].ext;
     uint64_t *dd = stack[depth + 1].itt;
     for (int32_t j = y; j < c->m; ++j) {
@@ -202,6 +204,7 @@ static void *worker_main(void *arg)
         int32_t j = (*wk->next_j)++;
         pthread_mutex_unlock(wk->lock);
         if (j >= c->m) break;
+        if (wk->sink.limit && wk->sink.count >= wk->sink.limit) break;
         if (bit_of(wk->top_int, j)) continue;
         wk->sink.closures += 1;
         uint64_t *cc = stack[1].ext, *dd = stack[1].itt;
@@ -232,10 +235,24 @@ static void to_words32(const uint64_t *src, uint64_t count, int32_t wm64, int64_
  * Outputs (malloc'd, free with oracle_free): intents count x ceil(m/32),
  * extents count x ceil(n/32) or NULL; closures; depth_counts[m+2] (caller array).
  * Returns 0, or -1 on bad arguments / allocation failure.
+ * `limit` > 0 stops each thread once it has output `limit` intents: a bounded
+ * sample of the search for timing; the result is then incomplete.
  */
+int oracle_cbo_limited(const uint32_t *rows32, int64_t n, int32_t m, int threads, int want_extents,
+                       uint64_t limit, uint32_t **out_intents, uint32_t **out_extents,
+                       uint64_t *out_count, uint64_t *out_closures, uint64_t *depth_counts);
+
 int oracle_cbo(const uint32_t *rows32, int64_t n, int32_t m, int threads, int want_extents,
                uint32_t **out_intents, uint32_t **out_extents, uint64_t *out_count,
                uint64_t *out_closures, uint64_t *depth_counts)
+{
+    return oracle_cbo_limited(rows32, n, m, threads, want_extents, 0, out_intents, out_extents,
+                              out_count, out_closures, depth_counts);
+}
+
+int oracle_cbo_limited(const uint32_t *rows32, int64_t n, int32_t m, int threads, int want_extents,
+                       uint64_t limit, uint32_t **out_intents, uint32_t **out_extents,
+                       uint64_t *out_count, uint64_t *out_closures, uint64_t *depth_counts)
 {
     if (!rows32 || n < 1 || m < 1 || !out_intents || !out_count || !out_closures || !depth_counts)
         return -1;
@@ -254,6 +271,7 @@ int oracle_cbo(const uint32_t *rows32, int64_t n, int32_t m, int threads, int wa
     if (!wks) { free(top_ext); free(top_int); free_ctx(&c); return -1; }
     for (int t = 0; t < nthr; ++t) {
         wks[t].sink.want_extents = want_extents;
+        wks[t].sink.limit = limit;
         wks[t].sink.depth_counts = (uint64_t *)calloc((size_t)(m + 2), sizeof(uint64_t));
     }
     int rc = 0;

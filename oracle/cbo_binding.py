@@ -51,19 +51,26 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         ctypes.c_void_p,
     ]
     lib.oracle_cbo.restype = ctypes.c_int
+    lib.oracle_cbo_limited.argtypes = [
+        ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int, ctypes.c_int, ctypes.c_uint64,
+        u32pp, u32pp, ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64),
+        ctypes.c_void_p,
+    ]
+    lib.oracle_cbo_limited.restype = ctypes.c_int
     lib.oracle_free.argtypes = [ctypes.c_void_p]
     lib.oracle_free.restype = None
     return lib
 
 
 def cbo(rows: np.ndarray, n_objects: int, n_attrs: int, threads: int = 1,
-        want_extents: bool = False, lib: Optional[ctypes.CDLL] = None) -> dict:
+        want_extents: bool = False, lib: Optional[ctypes.CDLL] = None, limit: int = 0) -> dict:
     """Run the recursive CbO oracle.
 
     ``rows``: ``(N, ceil(M/32))`` uint32 packed rows. Returns a dict with
     ``intents`` (K x ceil(M/32) uint32, output order of the search), ``extents``
     (K x ceil(N/32) uint32 or None), ``closures`` (candidates evaluated),
-    ``depth_counts`` (concepts per search depth, length M+2).
+    ``depth_counts`` (concepts per search depth, length M+2). ``limit`` > 0
+    stops each thread after that many intents (a bounded timing sample).
     """
     lib = lib or load()
     rows = np.ascontiguousarray(rows, dtype=np.uint32)
@@ -76,9 +83,14 @@ def cbo(rows: np.ndarray, n_objects: int, n_attrs: int, threads: int = 1,
     count = ctypes.c_uint64(0)
     closures = ctypes.c_uint64(0)
     depth = np.zeros(n_attrs + 2, dtype=np.uint64)
-    rc = lib.oracle_cbo(rows.ctypes.data, n_objects, n_attrs, int(threads), int(want_extents),
-                        ctypes.byref(p_int), ctypes.byref(p_ext), ctypes.byref(count),
-                        ctypes.byref(closures), depth.ctypes.data)
+    if limit:
+        rc = lib.oracle_cbo_limited(rows.ctypes.data, n_objects, n_attrs, int(threads), int(want_extents),
+                                    int(limit), ctypes.byref(p_int), ctypes.byref(p_ext),
+                                    ctypes.byref(count), ctypes.byref(closures), depth.ctypes.data)
+    else:
+        rc = lib.oracle_cbo(rows.ctypes.data, n_objects, n_attrs, int(threads), int(want_extents),
+                            ctypes.byref(p_int), ctypes.byref(p_ext), ctypes.byref(count),
+                            ctypes.byref(closures), depth.ctypes.data)
     if rc != 0:
         raise RuntimeError("oracle_cbo failed (bad arguments or out of memory)")
     k = int(count.value)

@@ -1,0 +1,63 @@
+"""Write tests/golden/workload_digests.json from the CPU oracle (and nothing else).
+
+For each named synthetic workload it records the number of intents, the
+number of closures (candidates evaluated by Close-by-One), the concepts per
+search depth and a SHA-256 digest of the intents sorted as big integers
+(last 32-bit word most significant), so that full-size GPU runs can be
+checked bit-exactly without re-running the oracle.
+
+usage: python tests/golden/make_workload_digests.py [workload ...] [--threads T]
+"""
+import argparse
+import hashlib
+import json
+import os
+import sys
+import time
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(os.path.dirname(HERE))
+sys.path.insert(0, ROOT)
+
+import oracle  # noqa: E402
+from closed_set_enumeration_gb300 import contexts as cx  # noqa: E402
+
+OUT = os.path.join(HERE, "workload_digests.json")
+
+
+def digest(intents: np.ndarray) -> str:
+    rows = np.ascontiguousarray(intents, dtype="<u4")
+    rows = rows[np.lexsort(rows.T)] if rows.shape[0] else rows
+    return hashlib.sha256(np.ascontiguousarray(rows).tobytes()).hexdigest()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("names", nargs="*", default=list(cx.WORKLOADS))
+    ap.add_argument("--threads", type=int, default=os.cpu_count() or 1)
+    args = ap.parse_args()
+    data = json.load(open(OUT)) if os.path.exists(OUT) else {}
+    for name in args.names:
+        w = cx.WORKLOADS[name]
+        rows = w.rows()
+        t0 = time.time()
+        r = oracle.cbo(rows, w.n_objects, w.n_attrs, threads=args.threads)
+        dt = time.time() - t0
+        depth = [int(x) for x in r["depth_counts"]]
+        while depth and depth[-1] == 0:
+            depth.pop()
+        data[name] = {
+            "n_objects": w.n_objects, "n_attrs": w.n_attrs, "seed": w.seed,
+            "concepts": int(r["intents"].shape[0]), "closures": int(r["closures"]),
+            "depth_counts": depth, "sha256_sorted_intents": digest(r["intents"]),
+            "oracle_seconds": round(dt, 1), "oracle_threads": args.threads,
+        }
+        print(name, data[name]["concepts"], data[name]["closures"], f"{dt:.1f}s", flush=True)
+        with open(OUT, "w") as f:
+            json.dump(data, f, indent=1, sort_keys=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,229 @@
+"""GPU parity: the CUDA library against the CPU oracle, through the C ABI.
+
+The intent set must be bit-exact (compared as a sorted set; output order is
+unspecified), the number of closures evaluated must equal the oracle's, and
+no intent may appear twice.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+
+import oracle
+from closed_set_enumeration_gb300 import build as fbuild
+from closed_set_enumeration_gb300 import contexts as cx
+from tests._util import (GOLDEN, attrs_to_row, golden_names, has_duplicates, load_golden,
+                         same_set, sort_rows)
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    fbuild.build()
+
+
+def gpu_run(rows, n, m, capacity=None):
+    from closed_set_enumeration_gb300 import fca
+    with fca.Context(rows, n, m) as ctx:
+        out = ctx.enumerate(capacity=capacity)
+        got = out.cpu().numpy().view(np.uint32).reshape(-1, (m + 31) // 32)
+        return got, ctx.stats()
+
+
+def check_against_oracle(rows, n, m, threads=1):
+    got, st = gpu_run(rows, n, m)
+    ref = oracle.cbo(rows, n, m, threads=threads)
+    assert not has_duplicates(got)
+    assert same_set(got, ref["intents"])
+    assert st["concepts"] == ref["intents"].shape[0]
+    assert st["closures"] == ref["closures"]
+    return got, st
+
+
+@pytest.mark.parametrize("name", golden_names())
+def test_golden(name):
+    n, m, rows, expected = load_golden(name)
+    got, _ = gpu_run(rows, n, m)
+    assert same_set(got, expected)
+
+
+CASES = [(n, m, d, s)
+         for (n, m) in [(1, 1), (1, 40), (2, 3), (31, 7), (32, 33), (33, 31), (63, 64), (64, 65),
+                        (65, 20), (96, 100), (130, 64), (257, 45), (600, 96), (1500, 40)]
+         for (d, s) in [(0.15, 0), (0.45, 1)]]
+
+
+@pytest.mark.parametrize("n,m,density,seed", CASES)
+def test_random_contexts(n, m, density, seed):
+    rows = cx.random_context(n, m, density, seed)
+    check_against_oracle(rows, n, m)
+
+
+@pytest.mark.parametrize("n,m,density,seed", [(3000, 128, 0.08, 3), (2000, 300, 0.03, 4),
+                                              (5000, 1024, 0.004, 5), (800, 1000, 0.02, 6)])
+def test_larger_random_contexts(n, m, density, seed):
+    rows = cx.random_context(n, m, density, seed)
+    check_against_oracle(rows, n, m, threads=8)
+
+
+@pytest.mark.parametrize("n", [5, 16, 20, 40, 70])
+def test_contranominal(n):
+    got, st = gpu_run(cx.contranominal(n), n, n) if n <= 20 else (None, None)
+    if n <= 20:
+        assert got.shape[0] == 2 ** n and not has_duplicates(got)
+        assert st["closures"] == 2 ** n - 1
+    else:
+        # 2^n concepts do not fit; the count must still be exact with a small buffer
+        pytest.skip("2^n too large to enumerate")
+
+
+@pytest.mark.parametrize("n", [2, 33, 64, 65, 200, 1024])
+def test_identity(n):
+    got, st = gpu_run(cx.identity(n), n, n)
+    expected = [attrs_to_row([], n), attrs_to_row(range(n), n)] + [attrs_to_row([j], n) for j in range(n)]
+    assert same_set(got, np.stack(expected))
+    assert st["closures"] == n + n * (n - 1) // 2
+
+
+@pytest.mark.parametrize("n,m", [(1, 1), (40, 33), (70, 64), (100, 100)])
+def test_all_zero_and_all_ones(n, m):
+    w = (m + 31) // 32
+    zero = np.zeros((n, w), dtype=np.uint32)
+    got, st = gpu_run(zero, n, m)
+    assert same_set(got, np.stack([attrs_to_row([], m), attrs_to_row(range(m), m)]))
+    assert st["closures"] == m
+    ones = np.tile(attrs_to_row(range(m), m), (n, 1))
+    got, st = gpu_run(ones, n, m)
+    assert same_set(got, attrs_to_row(range(m), m)[None, :])
+    assert st["closures"] == 0
+
+
+def test_full_row_object_reaches_bottom_through_search():
+    # one object holds every attribute, so the bottom concept has a non-empty extent
+    rows = cx.random_context(300, 70, 0.2, 9)
+    rows[17] = attrs_to_row(range(70), 70)
+    check_against_oracle(rows, 300, 70)
+
+
+def test_padding_bits_ignored():
+    rows = cx.random_context(200, 37, 0.3, 2)
+    dirty = rows.copy()
+    dirty[:, -1] |= np.uint32(0xFFFFFFE0)
+    got, _ = gpu_run(dirty, 200, 37)
+    assert same_set(got, oracle.cbo(rows, 200, 37)["intents"])
+    assert not np.any(got[:, -1] & np.uint32(0xFFFFFFE0))
+
+
+def test_device_rows_input():
+    from closed_set_enumeration_gb300 import fca
+    rows = cx.random_context(500, 50, 0.2, 4)
+    dev = torch.from_numpy(rows.view(np.int32)).cuda()
+    with fca.Context(dev, 500, 50) as ctx:
+        got = ctx.enumerate().cpu().numpy().view(np.uint32)
+        assert np.array_equal(ctx.copy_layout("rows"), rows)
+    assert same_set(got, oracle.cbo(rows, 500, 50)["intents"])
+
+
+def test_column_layout_is_transpose():
+    from closed_set_enumeration_gb300 import fca
+    n, m = 1000, 70
+    rows = cx.random_context(n, m, 0.3, 1)
+    with fca.Context(rows, n, m) as ctx:
+        cols = ctx.copy_layout("cols")
+        top = ctx.copy_layout("top")
+    cells = cx.unpack_rows(rows, m)
+    wn = (n + 31) // 32
+    expect = cx.pack_rows(cells.T)
+    assert np.array_equal(cols[:, :wn], expect)
+    assert not np.any(cols[:, wn:])
+    assert np.array_equal(top, oracle.derive_intent(rows, np.ones(n, bool), m))
+
+
+def test_capacity_contract():
+    from closed_set_enumeration_gb300 import fca
+    rows = cx.random_context(300, 40, 0.3, 5)
+    ref = oracle.cbo(rows, 300, 40)["intents"]
+    total = ref.shape[0]
+    with fca.Context(rows, 300, 40) as ctx:
+        st, cnt = ctx.enumerate_into(torch.empty((0, 2), dtype=torch.int32, device="cuda"), 0)
+        assert st == fca.FCA_ERR_CAPACITY and cnt == total
+        small = torch.full((10, 2), -1, dtype=torch.int32, device="cuda")
+        st, cnt = ctx.enumerate_into(small, 10)
+        assert st == fca.FCA_ERR_CAPACITY and cnt == total
+        part = small.cpu().numpy().view(np.uint32)
+        refset = set(map(tuple, ref))
+        assert all(tuple(r) in refset for r in part)           # only true intents written
+        assert np.array_equal(part[0], oracle.derive_intent(rows, np.ones(300, bool), 40))
+        exact = torch.empty((total, 2), dtype=torch.int32, device="cuda")
+        st, cnt = ctx.enumerate_into(exact, total)
+        assert st == fca.FCA_OK and cnt == total
+        assert same_set(exact.cpu().numpy().view(np.uint32), ref)
+
+
+def test_enumerate_host_and_reuse():
+    from closed_set_enumeration_gb300 import fca
+    rows = cx.random_context(400, 64, 0.25, 8)
+    ref = oracle.cbo(rows, 400, 64)["intents"]
+    with fca.Context(rows, 400, 64) as ctx:
+        host = np.zeros((ref.shape[0] + 5, 2), dtype=np.uint32)
+        st, cnt = ctx.enumerate_host(host)
+        assert st == fca.FCA_OK and cnt == ref.shape[0]
+        assert same_set(host[:cnt], ref)
+        for _ in range(2):   # pools are reused across calls
+            got = ctx.enumerate().cpu().numpy().view(np.uint32)
+            assert same_set(got, ref)
+
+
+def test_bounded_pools_force_chunking(monkeypatch):
+    # tiny work pools: levels are expanded in many chunks, depth first, and queues drain early
+    n, m = 4000, 60
+    rows = cx.random_context(n, m, 0.12, 12)
+    rows[: n // 4, 0] |= np.uint32(0x00FF00FF)      # dense block -> large extents and deep bitmap levels
+    ref = oracle.cbo(rows, n, m, threads=8)
+    monkeypatch.setenv("FCA_LEVEL_BYTES", "1")       # floor: 4*M entries per level
+    monkeypatch.setenv("FCA_QUEUE_ENTRIES", "1")     # floor: 4*M entries per queue
+    got, st = gpu_run(rows, n, m)
+    assert same_set(got, ref["intents"])
+    assert st["closures"] == ref["closures"]
+    assert st["launches"] > 10
+
+
+@pytest.mark.parametrize("name", ["tiny", "sparse"])
+def test_workload_full_set(name):
+    w = cx.WORKLOADS[name]
+    check_against_oracle(w.rows(), w.n_objects, w.n_attrs, threads=8)
+
+
+DIGESTS = os.path.join(GOLDEN, "workload_digests.json")
+
+
+def _digest(intents):
+    import hashlib
+    rows = sort_rows(np.ascontiguousarray(intents, dtype="<u4"))
+    return hashlib.sha256(np.ascontiguousarray(rows).tobytes()).hexdigest()
+
+
+@pytest.mark.parametrize("name", ["sparse", "skewed", "zipf", "biclusters"])
+def test_workload_full_size_digest(name):
+    """Full-size workloads against oracle digests written by tests/golden/make_workload_digests.py."""
+    table = json.load(open(DIGESTS)) if os.path.exists(DIGESTS) else {}
+    if name not in table:
+        pytest.skip(f"no oracle digest stored for {name}")
+    ref = table[name]
+    w = cx.WORKLOADS[name]
+    rows = w.rows()
+    got, st = gpu_run(rows, w.n_objects, w.n_attrs, capacity=ref["concepts"])
+    assert got.shape[0] == ref["concepts"]
+    assert st["closures"] == ref["closures"]
+    assert _digest(got) == ref["sha256_sorted_intents"]
+    # sampled fixed points, computed one by one by the oracle's derivation operators
+    rng = np.random.default_rng(0)
+    for i in rng.choice(got.shape[0], 200, replace=False):
+        ext = oracle.derive_extent(rows, got[i])
+        assert np.array_equal(oracle.derive_intent(rows, ext, w.n_attrs), got[i])
