@@ -88,6 +88,7 @@ struct SubtreeArgs {
     Queue q;
     uint64_t q_count;
     int q_index;            // which q_head / q_count counter this queue uses
+    int slices;             // work items per root (set by the launcher)
     uint32_t *out;
     uint64_t capacity;
     Counters *ctr;

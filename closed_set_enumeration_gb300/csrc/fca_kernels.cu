@@ -15,6 +15,8 @@
 //                        root extent holds at most 32*NW objects.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+
 #include "fca_internal.cuh"
 
 namespace fca {
@@ -22,6 +24,8 @@ namespace {
 
 constexpr unsigned FULL = 0xffffffffu;
 constexpr int OUTBUF = 16;          // intents buffered per warp before one atomicAdd
+constexpr int REG_WORDS = 8;        // largest compact intent (x32 attributes) kept in registers
+constexpr int MAX_SLICES = 32;      // most work items one subtree root is split into
 
 __device__ __forceinline__ unsigned popc4(const uint4 &x)
 {
@@ -298,24 +302,291 @@ __global__ void __launch_bounds__(256) expand_bitmap_kernel(ExpandArgs a)
 
 struct SubtreeLayout {
     int mp, wm, fr, fs;
-    size_t o_rmap, o_rootb, o_rm, o_rlo, o_sufb, o_stack, o_outbuf, words;
+    size_t o_rmap, o_rootb, o_rm, o_rlo, o_sufb, o_dsc, o_stack, o_outbuf, words;
     __host__ __device__ SubtreeLayout(const Dims &d, int nw)
     {
         mp = (d.m + 31) & ~31;
         wm = d.wm;
         fr = (32 * nw < d.m ? 32 * nw : d.m) + 1;     // depth <= |extent| and <= |R|
-        fs = nw + 1 + wm;                             // frame: extent mask, cursor, intent
+        fs = nw + 1 + (wm > REG_WORDS ? wm : REG_WORDS);   // frame: extent mask, cursor, intent
         o_rmap = (size_t)nw * mp;
         o_rootb = o_rmap + mp / 2;
         o_rm = o_rootb + 32;
         o_rlo = o_rm + 32;
         o_sufb = o_rlo + 34;
-        o_stack = o_sufb + 32;
+        o_dsc = o_sufb + 32;
+        o_stack = o_dsc + 34;
         o_outbuf = o_stack + (size_t)fr * fs;
         words = o_outbuf + (size_t)OUTBUF * wm;
         words = (words + 3) & ~(size_t)3;
     }
 };
+
+// Per-warp state of the object-list tier: shared-memory areas of the current subtree root,
+// the output buffer and the warp's counters.
+struct SubtreeWarp {
+    uint32_t *cR;       // restricted columns, NW planes x mp (compact attribute index)
+    uint16_t *rmap;     // compact index -> attribute
+    uint32_t *rootB;    // root intent (full attribute space), 32 words
+    uint32_t *Rm;       // relevant attributes per full word
+    uint32_t *rlo;      // first compact index of each full word (wm + 1 entries)
+    uint32_t *sufB;     // root-intent attributes in the words above each word
+    uint32_t *dsc;      // compact intent of the child being written
+    uint32_t *stk;      // search stack
+    uint32_t *ob;       // output buffer, OUTBUF x wm
+    int mp, wm, fs, m;
+    uint32_t *out;
+    unsigned long long capacity;
+    Counters *ctr;
+    int nb;             // intents waiting in the output buffer
+    unsigned long long closures, ops;
+
+    __device__ void flush()
+    {
+        const unsigned lane = threadIdx.x & 31;
+        unsigned long long b0 = 0;
+        if (lane == 0) b0 = atomicAdd(&ctr->out_count, (unsigned long long)nb);
+        b0 = __shfl_sync(FULL, b0, 0);
+        __syncwarp();
+        for (int i = (int)lane; i < nb * wm; i += 32)
+            if (b0 + (unsigned long long)(i / wm) < capacity) out[b0 * wm + i] = ob[i];
+        __syncwarp();
+        nb = 0;
+    }
+
+    // Write the full intent of a canonical child whose compact intent is in dsc[]:
+    // root intent plus the compact bits mapped back to their attributes.
+    template <bool COUNT>
+    __device__ void emit()
+    {
+        const unsigned lane = threadIdx.x & 31;
+        __syncwarp();
+        if (lane < (unsigned)wm) {
+            const int w = (int)lane;
+            const int lo = (int)rlo[w], hi = (int)rlo[w + 1];
+            const int su = lo >> 5, sh = lo & 31;
+            const uint32_t s0 = dsc[su];
+            const uint32_t s1 = sh ? dsc[su + 1] : 0u;
+            uint32_t seg = sh ? ((s0 >> sh) | (s1 << (32 - sh))) : s0;
+            const int len = hi - lo;
+            if (len < 32) seg &= (1u << len) - 1u;
+            uint32_t rmw = Rm[w], res = rootB[w];
+            int i = 0;
+            while (rmw) {
+                const int b = __ffs(rmw) - 1;
+                rmw &= rmw - 1u;
+                if ((seg >> i) & 1u) res |= 1u << b;
+                ++i;
+            }
+            ob[nb * wm + w] = res;
+        }
+        ++nb;
+        if (COUNT) ops += (unsigned)wm;   // the intent words written
+        __syncwarp();
+        if (nb == OUTBUF) flush();
+    }
+
+    // Candidates of a child created at compact candidate j whose compact intent has `above`
+    // attributes after j: the attributes after rmap[j] outside its full intent.
+    __device__ void count_child(int j, int above)
+    {
+        const int rj = rmap[j];
+        const int rw = rj >> 5, rb = rj & 31;
+        const uint32_t hi = rb == 31 ? 0u : (rootB[rw] >> (rb + 1));
+        closures += (unsigned long long)(m - rj - 1 - (int)sufB[rw] - __popc(hi) - above);
+    }
+};
+
+// Depth-first search of one subtree with the restricted columns in registers: lane l holds the
+// columns of compact attributes 32u + l, u < WRT (R <= 32 * WRT). Extent, intent and cursor of
+// the current node are warp-uniform registers; the stack of ancestors is in shared memory.
+template <int NW, int WRT, bool COUNT>
+__device__ void dfs_regs(SubtreeWarp &S, int R, int n, int jn, int slices, int slice)
+{
+    const unsigned lane = threadIdx.x & 31;
+    uint32_t col[WRT][NW];
+#pragma unroll
+    for (int u = 0; u < WRT; ++u) {
+        const int k = 32 * u + (int)lane;
+#pragma unroll
+        for (int t = 0; t < NW; ++t) col[u][t] = k < R ? S.cR[t * S.mp + k] : 0u;
+    }
+    uint32_t valid[WRT], B[WRT];
+#pragma unroll
+    for (int u = 0; u < WRT; ++u) { valid[u] = lt_mask(u, R); B[u] = 0u; }
+    uint32_t ext[NW];
+#pragma unroll
+    for (int t = 0; t < NW; ++t) {
+        const int k = n - 32 * t;
+        ext[t] = k >= 32 ? FULL : (k > 0 ? ((1u << k) - 1u) : 0u);
+    }
+    int depth = 0;
+    for (;;) {
+        int j = -1;
+#pragma unroll
+        for (int u = 0; u < WRT; ++u) {
+            const uint32_t cw = ~B[u] & valid[u] & ge_mask(u, jn);
+            if (j < 0 && cw) j = 32 * u + __ffs(cw) - 1;
+        }
+        if (j >= 0 && depth == 0 && slices > 1 && j % slices != slice) {   // another slice's child
+            jn = j + 1;
+            continue;
+        }
+        if (j < 0) {
+            if (depth == 0) break;
+            --depth;
+            const uint32_t *f = S.stk + (size_t)depth * S.fs;
+#pragma unroll
+            for (int t = 0; t < NW; ++t) ext[t] = f[t];
+            jn = (int)f[NW];
+#pragma unroll
+            for (int u = 0; u < WRT; ++u) B[u] = f[NW + 1 + u];
+            __syncwarp();
+            continue;
+        }
+        jn = j + 1;
+        uint32_t C[NW];
+        bool nonempty = false;
+#pragma unroll
+        for (int t = 0; t < NW; ++t) {
+            C[t] = ext[t] & S.cR[t * S.mp + j];
+            nonempty |= C[t] != 0u;
+        }
+        if (COUNT) S.ops += NW;            // the extent intersection
+        if (!nonempty) continue;           // empty extent: bottom concept, added by the host
+
+        // closure over the relevant attributes, canonical prefix first
+        const int ju = j >> 5;
+        const uint32_t jm = (1u << (j & 31)) - 1u;
+        uint32_t D[WRT];
+        bool canon = true;
+#pragma unroll
+        for (int u = 0; u < WRT; ++u) {
+            bool in = true;
+#pragma unroll
+            for (int t = 0; t < NW; ++t) in = in && ((C[t] & ~col[u][t]) == 0u);
+            D[u] = __ballot_sync(FULL, in);   // columns past R are 0, so those bits stay clear
+            if (COUNT) S.ops += 2ull * NW * (unsigned)max(0, min(32, R - 32 * u)) + (u <= ju ? 2 : 0);
+            if (u <= ju && (D[u] & ~B[u] & (u < ju ? FULL : jm))) { canon = false; break; }
+        }
+        if (!canon) continue;
+
+        // canonical child (C, D, j+1): write its intent, count its candidates, descend
+        if (lane == 0) {
+#pragma unroll
+            for (int u = 0; u < WRT; ++u) S.dsc[u] = D[u];
+            S.dsc[WRT] = 0u;
+        }
+        S.emit<COUNT>();
+        int above = 0;
+#pragma unroll
+        for (int u = 0; u < WRT; ++u) above += __popc(D[u] & ge_mask(u, j + 1));
+        S.count_child(j, above);
+        if (lane == 0) {
+            uint32_t *f = S.stk + (size_t)depth * S.fs;
+#pragma unroll
+            for (int t = 0; t < NW; ++t) f[t] = ext[t];
+            f[NW] = (uint32_t)jn;
+#pragma unroll
+            for (int u = 0; u < WRT; ++u) f[NW + 1 + u] = B[u];
+        }
+        __syncwarp();
+        ++depth;
+#pragma unroll
+        for (int t = 0; t < NW; ++t) ext[t] = C[t];
+#pragma unroll
+        for (int u = 0; u < WRT; ++u) B[u] = D[u];
+    }
+}
+
+// Same search with the restricted columns read from shared memory, for any R <= M: lane u of the
+// warp holds word u of the current compact intent.
+template <int NW, bool COUNT>
+__device__ void dfs_smem(SubtreeWarp &S, int R, int n, int jn, int slices, int slice)
+{
+    const unsigned lane = threadIdx.x & 31;
+    const uint32_t validR = lt_mask((int)lane, R);
+    const int WR = (R + 31) >> 5;
+    uint32_t myB = 0;
+    uint32_t ext[NW];
+#pragma unroll
+    for (int t = 0; t < NW; ++t) {
+        const int k = n - 32 * t;
+        ext[t] = k >= 32 ? FULL : (k > 0 ? ((1u << k) - 1u) : 0u);
+    }
+    int depth = 0;
+    for (;;) {
+        const uint32_t cw = ~myB & validR & ge_mask((int)lane, jn);
+        const unsigned bal = __ballot_sync(FULL, cw != 0u);
+        if (bal == 0u) {
+            if (depth == 0) break;
+            --depth;
+            const uint32_t *f = S.stk + (size_t)depth * S.fs;
+#pragma unroll
+            for (int t = 0; t < NW; ++t) ext[t] = f[t];
+            jn = (int)f[NW];
+            myB = lane < (unsigned)S.wm ? f[NW + 1 + lane] : 0u;
+            __syncwarp();
+            continue;
+        }
+        const int u0 = __ffs(bal) - 1;
+        const uint32_t cwu = __shfl_sync(FULL, cw, u0);
+        const int j = u0 * 32 + __ffs(cwu) - 1;
+        jn = j + 1;
+        if (depth == 0 && slices > 1 && j % slices != slice) continue;   // another slice's child
+
+        uint32_t C[NW];
+        bool nonempty = false;
+#pragma unroll
+        for (int t = 0; t < NW; ++t) {
+            C[t] = ext[t] & S.cR[t * S.mp + j];
+            nonempty |= C[t] != 0u;
+        }
+        if (COUNT) S.ops += NW;
+        if (!nonempty) continue;
+
+        const int ju = j >> 5;
+        const uint32_t jm = (1u << (j & 31)) - 1u;
+        bool canon = true;
+        uint32_t myD = 0;
+        for (int u = 0; u < WR; ++u) {
+            const int k = u * 32 + (int)lane;
+            bool in = k < R;
+            if (in) {
+#pragma unroll
+                for (int t = 0; t < NW; ++t) in = in && ((C[t] & ~S.cR[t * S.mp + k]) == 0u);
+            }
+            const uint32_t Du = __ballot_sync(FULL, in);
+            if (COUNT) S.ops += 2ull * NW * (unsigned)min(32, R - 32 * u) + (u <= ju ? 2 : 0);
+            if (u <= ju) {
+                const uint32_t Bu = __shfl_sync(FULL, myB, u);
+                const uint32_t pm = u < ju ? FULL : jm;
+                if (Du & ~Bu & pm) { canon = false; break; }
+            }
+            if ((int)lane == u) myD = Du;
+        }
+        if (!canon) continue;
+
+        if (lane <= (unsigned)WR) S.dsc[lane] = lane < (unsigned)WR ? myD : 0u;
+        S.emit<COUNT>();
+        unsigned c = __popc(myD & ge_mask((int)lane, j + 1) & validR);
+        c = __reduce_add_sync(FULL, c);
+        S.count_child(j, (int)c);
+        {
+            uint32_t *f = S.stk + (size_t)depth * S.fs;
+#pragma unroll
+            for (int t = 0; t < NW; ++t)
+                if ((int)lane == t) f[t] = ext[t];
+            if (lane == 0) f[NW] = (uint32_t)jn;
+            if (lane < (unsigned)S.wm) f[NW + 1 + lane] = myB;
+            __syncwarp();
+            ++depth;
+#pragma unroll
+            for (int t = 0; t < NW; ++t) ext[t] = C[t];
+            myB = myD;
+        }
+    }
+}
 
 template <int NW, bool COUNT>
 __global__ void __launch_bounds__(256) subtree_kernel(SubtreeArgs a)
@@ -325,35 +596,37 @@ __global__ void __launch_bounds__(256) subtree_kernel(SubtreeArgs a)
     const SubtreeLayout L(d, NW);
     const unsigned lane = threadIdx.x & 31;
     uint32_t *base = smw + (size_t)(threadIdx.x >> 5) * L.words;
-    uint32_t *cR = base;                                         // NW planes x mp
-    uint16_t *rmap = reinterpret_cast<uint16_t *>(base + L.o_rmap);
-    uint32_t *rootB = base + L.o_rootb;
-    uint32_t *Rm = base + L.o_rm;
-    uint32_t *rlo = base + L.o_rlo;
-    uint32_t *sufB = base + L.o_sufb;
-    uint32_t *stk = base + L.o_stack;
-    uint32_t *ob = base + L.o_outbuf;
-    const int mp = L.mp, WM = d.wm, FS = L.fs, PER = 32 * NW;
+    SubtreeWarp S;
+    S.cR = base;
+    S.rmap = reinterpret_cast<uint16_t *>(base + L.o_rmap);
+    S.rootB = base + L.o_rootb;
+    S.Rm = base + L.o_rm;
+    S.rlo = base + L.o_rlo;
+    S.sufB = base + L.o_sufb;
+    S.dsc = base + L.o_dsc;
+    S.stk = base + L.o_stack;
+    S.ob = base + L.o_outbuf;
+    S.mp = L.mp;
+    S.wm = d.wm;
+    S.fs = L.fs;
+    S.m = d.m;
+    S.out = a.out;
+    S.capacity = a.capacity;
+    S.ctr = a.ctr;
+    S.nb = 0;
+    S.closures = 0;
+    S.ops = 0;
+    const int mp = L.mp, WM = d.wm, PER = 32 * NW;
 
-    unsigned long long my_closures = 0, my_ops = 0;
-    int nb = 0;   // intents waiting in the output buffer
-
-    auto flush = [&]() {
-        unsigned long long b0 = 0;
-        if (lane == 0) b0 = atomicAdd(&a.ctr->out_count, (unsigned long long)nb);
-        b0 = __shfl_sync(FULL, b0, 0);
-        __syncwarp();
-        for (int i = (int)lane; i < nb * WM; i += 32)
-            if (b0 + (unsigned long long)(i / WM) < a.capacity) a.out[b0 * WM + i] = ob[i];
-        __syncwarp();
-        nb = 0;
-    };
-
+    const unsigned long long items = a.q_count * (unsigned long long)a.slices;
     for (;;) {
-        unsigned long long r = 0;
-        if (lane == 0) r = atomicAdd(&a.ctr->q_head[a.q_index], 1ull);
-        r = __shfl_sync(FULL, r, 0);
-        if (r >= a.q_count) break;
+        unsigned long long item = 0;
+        if (lane == 0) item = atomicAdd(&a.ctr->q_head[a.q_index], 1ull);
+        item = __shfl_sync(FULL, item, 0);
+        if (item >= items) break;
+        // work item = (root, slice): the slice takes the root's children j with j % slices == slice
+        const unsigned long long r = item / (unsigned)a.slices;
+        const int slice = (int)(item % (unsigned)a.slices);
 
         // ---- root: object ids, intent, cursor
         const int n = a.q.n[r];
@@ -365,10 +638,11 @@ __global__ void __launch_bounds__(256) subtree_kernel(SubtreeArgs a)
             id[t] = o < n ? a.q.ids[r * PER + o] : 0u;
         }
         const uint32_t myRootB = lane < (unsigned)WM ? a.q.itt[r * WM + lane] : 0u;
-        rootB[lane] = myRootB;
+        __syncwarp();
+        S.rootB[lane] = myRootB;
 
-        // ---- relevant attributes R (held by some but not all objects), compact index order = attribute
-        //      order, and the columns restricted to the subtree's objects (one ballot per attribute)
+        // ---- relevant attributes R (held by some but not all objects), compact index order =
+        //      attribute order, and the columns restricted to the subtree's objects
         int R = 0;
         for (int w = 0; w < WM; ++w) {
             uint32_t rw[NW];
@@ -380,7 +654,7 @@ __global__ void __launch_bounds__(256) subtree_kernel(SubtreeArgs a)
             }
             uni = __reduce_or_sync(FULL, uni);
             const uint32_t rm = uni & ~__shfl_sync(FULL, myRootB, w);
-            if (lane == 0) { Rm[w] = rm; rlo[w] = (uint32_t)R; }
+            if (lane == 0) { S.Rm[w] = rm; S.rlo[w] = (uint32_t)R; }
             uint32_t bits = rm;
             while (bits) {
                 const int b = __ffs(bits) - 1;
@@ -388,13 +662,13 @@ __global__ void __launch_bounds__(256) subtree_kernel(SubtreeArgs a)
 #pragma unroll
                 for (int t = 0; t < NW; ++t) {
                     const uint32_t bal = __ballot_sync(FULL, (rw[t] >> b) & 1u);
-                    if (lane == 0) cR[t * mp + R] = bal;
+                    if (lane == 0) S.cR[t * mp + R] = bal;
                 }
-                if (lane == 0) rmap[R] = (uint16_t)(32 * w + b);
+                if (lane == 0) S.rmap[R] = (uint16_t)(32 * w + b);
                 ++R;
             }
         }
-        if (lane == 0) rlo[WM] = (uint32_t)R;
+        if (lane == 0) S.rlo[WM] = (uint32_t)R;
         {
             // sufB[w] = number of root-intent attributes in words above w
             const unsigned pc = lane < (unsigned)WM ? __popc(myRootB) : 0u;
@@ -405,142 +679,34 @@ __global__ void __launch_bounds__(256) subtree_kernel(SubtreeArgs a)
                 if (lane >= (unsigned)off) incl += t;
             }
             const unsigned tot = __shfl_sync(FULL, incl, 31);
-            sufB[lane] = tot - incl;
+            S.sufB[lane] = tot - incl;
         }
         __syncwarp();
 
-        // ---- candidates of the root: attributes >= y0 outside its intent
+        // ---- candidates of the root: attributes >= y0 outside its intent (counted by slice 0)
         {
             unsigned c = lane < (unsigned)WM ? __popc(myRootB & ge_mask((int)lane, y0)) : 0u;
             c = __reduce_add_sync(FULL, c);
-            if (lane == 0) my_closures += (unsigned long long)(d.m - y0 - (int)c);
+            if (slice == 0) S.closures += (unsigned long long)(d.m - y0 - (int)c);
         }
         int jn;   // compact cursor: relevant attributes below y0 are not candidates
         {
-            const unsigned c = lane < (unsigned)WM ? __popc(Rm[lane] & lt_mask((int)lane, y0)) : 0u;
+            const unsigned c = lane < (unsigned)WM ? __popc(S.Rm[lane] & lt_mask((int)lane, y0)) : 0u;
             jn = (int)__reduce_add_sync(FULL, c);
         }
 
         // ---- depth-first search of the subtree
-        const uint32_t validR = ge_mask((int)lane, 0) & lt_mask((int)lane, R);
-        uint32_t myB = 0;          // compact intent of the current node, word `lane`
-        uint32_t ext[NW];          // current extent as a mask over the n objects
-#pragma unroll
-        for (int t = 0; t < NW; ++t) {
-            const int k = n - 32 * t;
-            ext[t] = k >= 32 ? FULL : (k > 0 ? ((1u << k) - 1u) : 0u);
-        }
-        int depth = 0;
-        for (;;) {
-            const uint32_t cw = ~myB & validR & ge_mask((int)lane, jn);
-            const unsigned bal = __ballot_sync(FULL, cw != 0u);
-            if (bal == 0u) {
-                if (depth == 0) break;
-                --depth;
-                const uint32_t *f = stk + (size_t)depth * FS;
-#pragma unroll
-                for (int t = 0; t < NW; ++t) ext[t] = f[t];
-                jn = (int)f[NW];
-                myB = lane < (unsigned)WM ? f[NW + 1 + lane] : 0u;
-                __syncwarp();
-                continue;
-            }
-            const int u0 = __ffs(bal) - 1;
-            const uint32_t cwu = __shfl_sync(FULL, cw, u0);
-            const int j = u0 * 32 + __ffs(cwu) - 1;
-            jn = j + 1;
-
-            uint32_t C[NW];
-            bool nonempty = false;
-#pragma unroll
-            for (int t = 0; t < NW; ++t) {
-                C[t] = ext[t] & cR[t * mp + j];
-                nonempty |= C[t] != 0u;
-            }
-            if (COUNT) my_ops += NW;      // the extent intersection
-            if (!nonempty) continue;      // empty extent: bottom concept, added by the host
-
-            // closure over the relevant attributes, canonical prefix first
-            const int ju = j >> 5;
-            const uint32_t jm = (1u << (j & 31)) - 1u;
-            const int WR = (R + 31) >> 5;
-            bool canon = true;
-            uint32_t myD = 0;
-            for (int u = 0; u < WR; ++u) {
-                const int k = u * 32 + (int)lane;
-                bool in = k < R;
-                if (in) {
-#pragma unroll
-                    for (int t = 0; t < NW; ++t) in = in && ((C[t] & ~cR[t * mp + k]) == 0u);
-                }
-                const uint32_t Du = __ballot_sync(FULL, in);
-                if (COUNT) my_ops += 2ull * NW * (unsigned)min(32, R - 32 * u) + (u <= ju ? 2 : 0);
-                if (u <= ju) {
-                    const uint32_t Bu = __shfl_sync(FULL, myB, u);
-                    const uint32_t pm = u < ju ? FULL : jm;
-                    if (Du & ~Bu & pm) { canon = false; break; }
-                }
-                if ((int)lane == u) myD = Du;
-            }
-            if (!canon) continue;
-
-            // ---- canonical child (C, D, j+1): write its full intent = root intent + D mapped back
-            {
-                const int w = lane < (unsigned)WM ? (int)lane : 0;
-                const int lo = (int)rlo[w], hi = (int)rlo[w + 1];
-                const int su = (lo >> 5) & 31, sh = lo & 31;
-                const uint32_t s0 = __shfl_sync(FULL, myD, su);
-                const uint32_t s1 = __shfl_sync(FULL, myD, (su + 1) & 31);
-                if (lane < (unsigned)WM) {
-                    uint32_t seg = sh ? ((s0 >> sh) | (s1 << (32 - sh))) : s0;
-                    const int len = hi - lo;
-                    if (len < 32) seg &= (1u << len) - 1u;
-                    uint32_t rmw = Rm[w], res = rootB[w];
-                    int i = 0;
-                    while (rmw) {
-                        const int b = __ffs(rmw) - 1;
-                        rmw &= rmw - 1u;
-                        if ((seg >> i) & 1u) res |= 1u << b;
-                        ++i;
-                    }
-                    ob[nb * WM + w] = res;
-                }
-                ++nb;
-                if (COUNT) my_ops += (unsigned)WM;   // the intent words written
-                __syncwarp();
-                if (nb == OUTBUF) flush();
-            }
-            {
-                // candidates of the child: attributes after rmap[j] outside its intent
-                const int rj = rmap[j];
-                const int rw = rj >> 5, rb = rj & 31;
-                const uint32_t above = rb == 31 ? 0u : (rootB[rw] >> (rb + 1));
-                unsigned c = __popc(myD & ge_mask((int)lane, j + 1) & validR);
-                c = __reduce_add_sync(FULL, c);
-                if (lane == 0)
-                    my_closures += (unsigned long long)(d.m - rj - 1 - (int)sufB[rw] - __popc(above) -
-                                                        (int)c);
-            }
-            // push the current node, descend
-            {
-                uint32_t *f = stk + (size_t)depth * FS;
-#pragma unroll
-                for (int t = 0; t < NW; ++t)
-                    if ((int)lane == t) f[t] = ext[t];
-                if (lane == 0) f[NW] = (uint32_t)jn;
-                if (lane < (unsigned)WM) f[NW + 1 + lane] = myB;
-                __syncwarp();
-                ++depth;
-#pragma unroll
-                for (int t = 0; t < NW; ++t) ext[t] = C[t];
-                myB = myD;
-            }
-        }
+        const int sl = a.slices;
+        if (R <= 32) dfs_regs<NW, 1, COUNT>(S, R, n, jn, sl, slice);
+        else if (R <= 64) dfs_regs<NW, 2, COUNT>(S, R, n, jn, sl, slice);
+        else if (R <= 128) dfs_regs<NW, 4, COUNT>(S, R, n, jn, sl, slice);
+        else if (R <= 32 * REG_WORDS) dfs_regs<NW, REG_WORDS, COUNT>(S, R, n, jn, sl, slice);
+        else dfs_smem<NW, COUNT>(S, R, n, jn, sl, slice);
         __syncwarp();
     }
-    if (nb) flush();
-    if (lane == 0 && my_closures) atomicAdd(&a.ctr->closures, my_closures);
-    if (COUNT && lane == 0 && my_ops) atomicAdd(&a.ctr->word_ops, my_ops);
+    if (S.nb) S.flush();
+    if (lane == 0 && S.closures) atomicAdd(&a.ctr->closures, S.closures);
+    if (COUNT && lane == 0 && S.ops) atomicAdd(&a.ctr->word_ops, S.ops);
 }
 
 }  // namespace
@@ -629,11 +795,17 @@ static int launch_subtree_nw(const SubtreeArgs &a, int sm_count, void *stream)
     int per_sm = 0;
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, subtree_kernel<NW, COUNT>, wpb * 32, smem);
     if (per_sm < 1) per_sm = 1;
-    unsigned long long blocks = (a.q_count + wpb - 1) / wpb;
+    // split roots into slices when there are too few roots to keep every resident warp busy
+    SubtreeArgs b = a;
+    const unsigned long long resident = (unsigned long long)sm_count * per_sm * wpb;
+    const unsigned long long want = 16 * resident;
+    b.slices = (int)std::min<unsigned long long>(MAX_SLICES, std::max<unsigned long long>(
+                                                     1, (want + a.q_count - 1) / std::max<unsigned long long>(1, a.q_count)));
+    unsigned long long blocks = (a.q_count * b.slices + wpb - 1) / wpb;
     const unsigned long long cap = (unsigned long long)sm_count * per_sm;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    subtree_kernel<NW, COUNT><<<(unsigned)blocks, wpb * 32, smem, (cudaStream_t)stream>>>(a);
+    subtree_kernel<NW, COUNT><<<(unsigned)blocks, wpb * 32, smem, (cudaStream_t)stream>>>(b);
     return (int)cudaGetLastError();
 }
 

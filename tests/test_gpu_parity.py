@@ -53,10 +53,12 @@ def test_golden(name):
     assert same_set(got, expected)
 
 
+# shapes straddle the word and tier boundaries (32 / 64 objects, 32 / 64 attributes); the
+# densities keep each oracle run well under a second (denser tables explode combinatorially)
 CASES = [(n, m, d, s)
          for (n, m) in [(1, 1), (1, 40), (2, 3), (31, 7), (32, 33), (33, 31), (63, 64), (64, 65),
-                        (65, 20), (96, 100), (130, 64), (257, 45), (600, 96), (1500, 40)]
-         for (d, s) in [(0.15, 0), (0.45, 1)]]
+                        (65, 20), (96, 100), (130, 64), (257, 45), (1500, 40)]
+         for (d, s) in [(0.12, 0), (0.3, 1)]] + [(600, 96, 0.12, 0), (600, 96, 0.2, 1)]
 
 
 @pytest.mark.parametrize("n,m,density,seed", CASES)
@@ -72,15 +74,11 @@ def test_larger_random_contexts(n, m, density, seed):
     check_against_oracle(rows, n, m, threads=8)
 
 
-@pytest.mark.parametrize("n", [5, 16, 20, 40, 70])
+@pytest.mark.parametrize("n", [5, 16, 20])
 def test_contranominal(n):
-    got, st = gpu_run(cx.contranominal(n), n, n) if n <= 20 else (None, None)
-    if n <= 20:
-        assert got.shape[0] == 2 ** n and not has_duplicates(got)
-        assert st["closures"] == 2 ** n - 1
-    else:
-        # 2^n concepts do not fit; the count must still be exact with a small buffer
-        pytest.skip("2^n too large to enumerate")
+    got, st = gpu_run(cx.contranominal(n), n, n)
+    assert got.shape[0] == 2 ** n and not has_duplicates(got)
+    assert st["closures"] == 2 ** n - 1
 
 
 @pytest.mark.parametrize("n", [2, 33, 64, 65, 200, 1024])
