@@ -1,13 +1,16 @@
 // C ABI and host driver of libfca.
 //
-// The driver runs the Close-by-One search level by level (Parallel FCBO page,
-// section 2.1: a level is expanded in one launch over all its (parent, j)
-// pairs, and the loop ends when no level holds work), but it never keeps a
-// whole level: each level is expanded in chunks whose worst-case output fits
-// the next level's buffer, and a full buffer is drained depth first before
-// its producer continues. Extent storage therefore stays bounded (the memory
-// concern of the FCbO-to-CUDA page, sections 3.4 and 6.1), and no global
-// dedupe is needed because the canonical test is local (section 2.2).
+// The driver runs the Close-by-One search level by level (Parallel FCBO
+// article, section 2.1: a level is expanded in one launch over all its
+// (parent, j) pairs, and the loop ends when no level holds work). A level is
+// launched optimistically into the current pools; when a destination turns
+// out too small, the launch is rolled back (the device counters are restored
+// from the copy taken before it, so everything it appended is dropped) and
+// retried after the destination was emptied (queues run, levels drained depth
+// first) or grown, up to a memory limit beyond which the level is split into
+// smaller chunks. Storage therefore stays bounded (the memory concern of the
+// FCbO-to-CUDA article, sections 3.4 and 6.1), and no global dedupe is needed
+// because the canonical test is local (section 2.2).
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -34,28 +37,29 @@ struct fca_ctx {
     bool full_row_exists = false;
     uint32_t *flag_host = nullptr; // pinned: full-row flag readback
 
-    // work pools, allocated on first use and kept for later calls
+    // work pools, allocated on first use, grown on demand and kept for later calls
     std::vector<Level> levels;
     std::vector<uint64_t> level_count;
-    std::vector<uint64_t> level_cands;   // candidates held by the entries of each level
-    Queue q[2]{};
-    uint64_t q_count[2]{0, 0};
-    uint64_t level_cap = 0, queue_cap = 0;
+    Queue q[NQ]{};
+    uint64_t q_count[NQ]{};
+    uint32_t *gstack = nullptr;    // ancestor stacks of the wide object-list kernels
+    size_t gstack_words = 0;
     Counters *ctr = nullptr;        // device
-    Counters *ctr_host = nullptr;   // pinned host mirror
+    Counters *ctr_host = nullptr;   // pinned host mirror, current after every readback
     uint32_t *stage = nullptr;      // pinned host staging (root entry)
 
     uint32_t *host_out_dev = nullptr;   // device buffer behind fca_enumerate_host
     uint64_t host_out_rows = 0;
 
-    size_t pool_bytes = 0;
-    uint64_t level_bytes = 0, queue_entries = 0;   // requested pool sizes
+    size_t pool_bytes = 0;          // bytes held by levels, queues and stacks
+    size_t pool_limit = 0;          // growth stops here; levels are then split into chunks
+    uint64_t level_bytes = 0, queue_entries = 0;   // initial pool sizes
     int count_work = 0;
-    uint64_t table_launches = 0;   // kernels launched by the last table load
+    uint64_t table_launches = 0;    // kernels launched by the last table load
 
     // device timing of kernel launches: event pairs recorded around each launch
     std::vector<cudaEvent_t> events;
-    std::vector<int> event_kind;     // per pair: 0 = expand, 1 = subtree
+    std::vector<int> event_kind;    // per pair: 0 = expand, 1 = subtree
     size_t pairs_used = 0;
 
     fca_stats stats{};
@@ -77,9 +81,9 @@ fca_status cuda_fail(fca_ctx *c, cudaError_t e, const char *what)
     return e == cudaErrorMemoryAllocation ? FCA_ERR_OOM : FCA_ERR_CUDA;
 }
 
-#define CK(call, what)                                      \
-    do {                                                    \
-        cudaError_t e_ = (call);                            \
+#define CK(call, what)                                        \
+    do {                                                      \
+        cudaError_t e_ = (call);                              \
         if (e_ != cudaSuccess) return cuda_fail(c, e_, what); \
     } while (0)
 
@@ -92,66 +96,152 @@ uint64_t env_u64(const char *name, uint64_t dflt)
     return (end && *end == 0 && x > 0) ? (uint64_t)x : dflt;
 }
 
-fca_status alloc_dev(fca_ctx *c, void **p, size_t bytes, const char *what)
+fca_status alloc_raw(fca_ctx *c, void **p, size_t bytes, const char *what)
 {
     cudaError_t e = cudaMalloc(p, bytes ? bytes : 16);
     if (e != cudaSuccess) {
         cudaGetLastError();
+        *p = nullptr;
         c->err = std::string("cudaMalloc failed for ") + what;
         return FCA_ERR_OOM;
     }
-    c->pool_bytes += bytes;
     return FCA_OK;
 }
 
-void size_pools(fca_ctx *c)
+uint64_t level_entry_bytes(const Dims &d) { return ((uint64_t)d.wnp + d.wm + 1) * 4; }
+uint64_t queue_entry_bytes(const Dims &d, int qi) { return ((uint64_t)(32 << qi) + d.wm + 2) * 4; }
+
+uint64_t initial_level_cap(const fca_ctx *c)
 {
-    const Dims &d = c->d;
-    const uint64_t entry = ((uint64_t)d.wnp + d.wm + 1) * 4;
-    const uint64_t M = (uint64_t)d.m;
-    c->level_cap = std::max<uint64_t>(4 * M, c->level_bytes / entry);
-    c->queue_cap = std::max<uint64_t>(4 * M, c->queue_entries);
+    return std::max<uint64_t>(4 * (uint64_t)c->d.m, c->level_bytes / level_entry_bytes(c->d));
+}
+
+uint64_t initial_queue_cap(const fca_ctx *c) { return std::max<uint64_t>(4 * (uint64_t)c->d.m, c->queue_entries); }
+
+void free_level(Level &L)
+{
+    cudaFree(L.ext);
+    cudaFree(L.itt);
+    cudaFree(L.y);
+    L = Level{};
+}
+
+void free_queue(Queue &Q)
+{
+    cudaFree(Q.ids);
+    cudaFree(Q.itt);
+    cudaFree(Q.y);
+    cudaFree(Q.n);
+    Q = Queue{};
 }
 
 void free_pools(fca_ctx *c)
 {
-    for (Level &L : c->levels) { cudaFree(L.ext); cudaFree(L.itt); cudaFree(L.y); }
+    for (Level &L : c->levels) free_level(L);
     c->levels.clear();
     c->level_count.clear();
-    c->level_cands.clear();
-    for (Queue &Q : c->q) { cudaFree(Q.ids); cudaFree(Q.itt); cudaFree(Q.y); cudaFree(Q.n); Q = Queue{}; }
+    for (Queue &Q : c->q) free_queue(Q);
+    cudaFree(c->gstack);
+    c->gstack = nullptr;
+    c->gstack_words = 0;
     c->pool_bytes = 0;
+}
+
+fca_status make_level(fca_ctx *c, Level *L, uint64_t cap)
+{
+    const Dims &d = c->d;
+    Level n{};
+    n.cap = cap;
+    fca_status s;
+    if ((s = alloc_raw(c, (void **)&n.ext, cap * d.wnp * 4, "frontier extents")) != FCA_OK ||
+        (s = alloc_raw(c, (void **)&n.itt, cap * d.wm * 4, "frontier intents")) != FCA_OK ||
+        (s = alloc_raw(c, (void **)&n.y, cap * 4, "frontier cursors")) != FCA_OK) {
+        free_level(n);
+        return s;
+    }
+    *L = n;
+    return FCA_OK;
+}
+
+fca_status make_queue(fca_ctx *c, Queue *Q, int qi, uint64_t cap)
+{
+    const Dims &d = c->d;
+    Queue n{};
+    n.cap = cap;
+    fca_status s;
+    if ((s = alloc_raw(c, (void **)&n.ids, cap * (32 << qi) * 4, "queue ids")) != FCA_OK ||
+        (s = alloc_raw(c, (void **)&n.itt, cap * d.wm * 4, "queue intents")) != FCA_OK ||
+        (s = alloc_raw(c, (void **)&n.y, cap * 4, "queue cursors")) != FCA_OK ||
+        (s = alloc_raw(c, (void **)&n.n, cap * 4, "queue sizes")) != FCA_OK) {
+        free_queue(n);
+        return s;
+    }
+    *Q = n;
+    return FCA_OK;
 }
 
 fca_status ensure_level(fca_ctx *c, size_t idx)
 {
     while (c->levels.size() <= idx) {
+        const uint64_t cap = initial_level_cap(c);
         Level L{};
-        L.cap = c->level_cap;
-        fca_status s;
-        if ((s = alloc_dev(c, (void **)&L.ext, L.cap * c->d.wnp * 4, "frontier extents")) != FCA_OK) return s;
-        if ((s = alloc_dev(c, (void **)&L.itt, L.cap * c->d.wm * 4, "frontier intents")) != FCA_OK) return s;
-        if ((s = alloc_dev(c, (void **)&L.y, L.cap * 4, "frontier cursors")) != FCA_OK) return s;
+        fca_status s = make_level(c, &L, cap);
+        if (s != FCA_OK) return s;
+        c->pool_bytes += cap * level_entry_bytes(c->d);
         c->levels.push_back(L);
         c->level_count.push_back(0);
-        c->level_cands.push_back(0);
     }
     return FCA_OK;
 }
 
 fca_status ensure_queues(fca_ctx *c)
 {
-    if (c->q[0].ids) return FCA_OK;
-    for (int i = 0; i < 2; ++i) {
-        Queue &Q = c->q[i];
-        const int per = 32 * (i + 1);
-        Q.cap = c->queue_cap;
-        fca_status s;
-        if ((s = alloc_dev(c, (void **)&Q.ids, Q.cap * per * 4, "queue ids")) != FCA_OK) return s;
-        if ((s = alloc_dev(c, (void **)&Q.itt, Q.cap * c->d.wm * 4, "queue intents")) != FCA_OK) return s;
-        if ((s = alloc_dev(c, (void **)&Q.y, Q.cap * 4, "queue cursors")) != FCA_OK) return s;
-        if ((s = alloc_dev(c, (void **)&Q.n, Q.cap * 4, "queue sizes")) != FCA_OK) return s;
+    for (int qi = 0; qi < NQ; ++qi) {
+        if (c->q[qi].ids) continue;
+        const uint64_t cap = initial_queue_cap(c);
+        fca_status s = make_queue(c, &c->q[qi], qi, cap);
+        if (s != FCA_OK) return s;
+        c->pool_bytes += cap * queue_entry_bytes(c->d, qi);
     }
+    return FCA_OK;
+}
+
+// Grow level `idx` to hold at least `need` entries, keeping its current entries. Returns
+// FCA_ERR_CAPACITY (nothing changed) when that would pass the pool limit.
+fca_status grow_level(fca_ctx *c, size_t idx, uint64_t need, cudaStream_t st)
+{
+    Level &L = c->levels[idx];
+    const uint64_t cap = std::max<uint64_t>(2 * L.cap, need + need / 4);
+    const uint64_t eb = level_entry_bytes(c->d);
+    if (c->pool_bytes + (cap - L.cap) * eb > c->pool_limit) return FCA_ERR_CAPACITY;
+    Level n{};
+    fca_status s = make_level(c, &n, cap);
+    if (s != FCA_OK) return s;
+    const uint64_t cnt = c->level_count[idx];
+    const Dims &d = c->d;
+    CK(cudaMemcpyAsync(n.ext, L.ext, cnt * d.wnp * 4, cudaMemcpyDeviceToDevice, st), "level grow");
+    CK(cudaMemcpyAsync(n.itt, L.itt, cnt * d.wm * 4, cudaMemcpyDeviceToDevice, st), "level grow");
+    CK(cudaMemcpyAsync(n.y, L.y, cnt * 4, cudaMemcpyDeviceToDevice, st), "level grow");
+    CK(cudaStreamSynchronize(st), "stream synchronize");
+    c->pool_bytes += (cap - L.cap) * eb;
+    free_level(L);
+    L = n;
+    return FCA_OK;
+}
+
+// Grow (empty) queue qi to hold at least `need` entries.
+fca_status grow_queue(fca_ctx *c, int qi, uint64_t need)
+{
+    Queue &Q = c->q[qi];
+    const uint64_t cap = std::max<uint64_t>(2 * Q.cap, need + need / 4);
+    const uint64_t eb = queue_entry_bytes(c->d, qi);
+    if (c->pool_bytes + (cap - Q.cap) * eb > c->pool_limit) return FCA_ERR_CAPACITY;
+    Queue n{};
+    fca_status s = make_queue(c, &n, qi, cap);
+    if (s != FCA_OK) return s;
+    c->pool_bytes += (cap - Q.cap) * eb;
+    free_queue(Q);
+    Q = n;
     return FCA_OK;
 }
 
@@ -206,10 +296,15 @@ fca_status read_counters(Run &r)
     CK(cudaMemcpyAsync(c->ctr_host, c->ctr, sizeof(Counters), cudaMemcpyDeviceToHost, r.st),
        "counter readback");
     CK(cudaStreamSynchronize(r.st), "stream synchronize");
-    if (c->ctr_host->error) {
-        c->err = "internal work-buffer capacity check failed";
-        return FCA_ERR_CUDA;
-    }
+    return FCA_OK;
+}
+
+fca_status write_counters(Run &r, const Counters &v)
+{
+    fca_ctx *c = r.c;
+    *c->ctr_host = v;
+    CK(cudaMemcpyAsync(c->ctr, c->ctr_host, sizeof(Counters), cudaMemcpyHostToDevice, r.st), "counter write");
+    CK(cudaStreamSynchronize(r.st), "stream synchronize");
     return FCA_OK;
 }
 
@@ -218,6 +313,15 @@ fca_status run_subtree(Run &r, int qi)
 {
     fca_ctx *c = r.c;
     if (c->q_count[qi] == 0) return FCA_OK;
+    const int nw = 1 << qi;
+    fca_status s;
+    if (nw >= 4 && !c->gstack) {
+        const size_t words = std::max(subtree_gstack_words(c->d, 4, c->sm_count),
+                                      subtree_gstack_words(c->d, 8, c->sm_count));
+        if ((s = alloc_raw(c, (void **)&c->gstack, words * 4, "subtree stacks")) != FCA_OK) return s;
+        c->gstack_words = words;
+        c->pool_bytes += words * 4;
+    }
     SubtreeArgs a{};
     a.d = c->d;
     a.rows = c->rows;
@@ -227,54 +331,39 @@ fca_status run_subtree(Run &r, int qi)
     a.out = r.out;
     a.capacity = r.capacity;
     a.ctr = c->ctr;
+    a.gstack = c->gstack;
     a.count_work = c->count_work;
     size_t pair = 0;
-    fca_status s;
     if ((s = time_begin(r, 1, &pair)) != FCA_OK) return s;
-    CK((cudaError_t)launch_subtree(a, qi + 1, c->sm_count, r.st), "subtree kernel launch");
+    CK((cudaError_t)launch_subtree(a, nw, c->sm_count, r.st), "subtree kernel launch");
     if ((s = time_end(r, pair)) != FCA_OK) return s;
     c->stats.launches++;
     c->stats.subtree_launches++;
     c->stats.small_roots += c->q_count[qi];
-    // reset the queue: its append counter and its work cursor
+    // empty the queue: its append counter and its work cursor
     CK(cudaMemsetAsync(&c->ctr->q_count[qi], 0, sizeof(unsigned long long), r.st), "queue reset");
     CK(cudaMemsetAsync(&c->ctr->q_head[qi], 0, sizeof(unsigned long long), r.st), "queue reset");
     c->q_count[qi] = 0;
-    return FCA_OK;
+    return read_counters(r);
 }
 
-// Expand every entry of bitmap level `lv`, depth first over chunks.
+// Expand every entry of bitmap level `lv`, depth first.
 fca_status drain(Run &r, size_t lv)
 {
     fca_ctx *c = r.c;
-    const uint64_t M = (uint64_t)c->d.m;
     fca_status s;
+    uint64_t kmax = ~(uint64_t)0;    // chunk limit, lowered only when the pools may not grow
     while (c->level_count[lv] > 0) {
         if ((s = ensure_level(c, lv + 1)) != FCA_OK) return s;
-        const uint64_t free_next = c->levels[lv + 1].cap - c->level_count[lv + 1];
-        if (free_next < M) {
-            if ((s = drain(r, lv + 1)) != FCA_OK) return s;
-            continue;
-        }
-        bool flushed = false;
-        for (int qi = 0; qi < 2; ++qi)
-            if (c->q[qi].cap - c->q_count[qi] < M) {
-                if ((s = run_subtree(r, qi)) != FCA_OK) return s;
-                flushed = true;
-            }
-        if (flushed) continue;
-        const uint64_t room = std::min({free_next, c->q[0].cap - c->q_count[0], c->q[1].cap - c->q_count[1]});
         const uint64_t have = c->level_count[lv];
-        // each candidate yields at most one child, so the whole level fits when its candidates do
-        uint64_t k = c->level_cands[lv] <= room ? have : std::min<uint64_t>(have, std::max<uint64_t>(1, room / M));
+        const uint64_t k = std::min(have, kmax);
         const uint64_t begin = have - k;
 
-        // the next level's append counter starts from its current fill
-        c->ctr_host->next_count = c->level_count[lv + 1];
-        CK(cudaMemcpyAsync(&c->ctr->next_count, &c->ctr_host->next_count, sizeof(unsigned long long),
-                           cudaMemcpyHostToDevice, r.st), "counter set");
-        CK(cudaMemsetAsync(&c->ctr->next_cands, 0, sizeof(unsigned long long), r.st), "counter set");
-        CK(cudaMemsetAsync(&c->ctr->chunk_closures, 0, sizeof(unsigned long long), r.st), "counter set");
+        // counters before the launch: the next level appends after its current fill
+        Counters before = *c->ctr_host;
+        before.next_count = c->level_count[lv + 1];
+        before.error = 0;
+        if ((s = write_counters(r, before)) != FCA_OK) return s;
 
         ExpandArgs a{};
         a.d = c->d;
@@ -284,8 +373,7 @@ fca_status drain(Run &r, size_t lv)
         a.p_begin = begin;
         a.p_count = k;
         a.next = c->levels[lv + 1];
-        a.q1 = c->q[0];
-        a.q2 = c->q[1];
+        for (int qi = 0; qi < NQ; ++qi) a.q[qi] = c->q[qi];
         a.out = r.out;
         a.capacity = r.capacity;
         a.ctr = c->ctr;
@@ -296,20 +384,49 @@ fca_status drain(Run &r, size_t lv)
         if ((s = time_end(r, pair)) != FCA_OK) return s;
         c->stats.launches++;
         c->stats.expand_launches++;
-        c->stats.large_parents += k;
         if ((s = read_counters(r)) != FCA_OK) return s;
+        const Counters after = *c->ctr_host;
 
-        const uint64_t used = c->ctr_host->chunk_closures;   // candidates of the chunk
-        c->level_cands[lv] = c->level_cands[lv] > used ? c->level_cands[lv] - used : 0;
+        if (after.error) {
+            // roll back: drop everything the launch appended, then make room and retry
+            c->stats.retries++;
+            if ((s = write_counters(r, before)) != FCA_OK) return s;
+            bool limited = false;
+            for (int qi = 0; qi < NQ; ++qi) {
+                if (!(after.error & (ERR_QUEUE0 << qi))) continue;
+                const uint64_t need = after.q_count[qi] - before.q_count[qi];
+                if ((s = run_subtree(r, qi)) != FCA_OK) return s;
+                if (need > c->q[qi].cap) {
+                    s = grow_queue(c, qi, need);
+                    if (s == FCA_ERR_CAPACITY) limited = true;
+                    else if (s != FCA_OK) return s;
+                }
+            }
+            if (after.error & ERR_NEXT) {
+                const uint64_t need = after.next_count - before.next_count;
+                if ((s = drain(r, lv + 1)) != FCA_OK) return s;
+                if (need > c->levels[lv + 1].cap) {
+                    s = grow_level(c, lv + 1, need, r.st);
+                    if (s == FCA_ERR_CAPACITY) limited = true;
+                    else if (s != FCA_OK) return s;
+                }
+            }
+            if (limited) {
+                if (k == 1) {
+                    c->err = "work pools too small for one search node (raise FCA_POOL_LIMIT_BYTES)";
+                    return FCA_ERR_OOM;
+                }
+                kmax = std::max<uint64_t>(1, k / 2);
+            }
+            continue;
+        }
         c->level_count[lv] = begin;
-        c->level_count[lv + 1] = c->ctr_host->next_count;
-        c->level_cands[lv + 1] += c->ctr_host->next_cands;
-        c->q_count[0] = c->ctr_host->q_count[0];
-        c->q_count[1] = c->ctr_host->q_count[1];
+        c->level_count[lv + 1] = after.next_count;
+        for (int qi = 0; qi < NQ; ++qi) c->q_count[qi] = after.q_count[qi];
+        c->stats.large_parents += k;
         c->stats.levels = std::max<uint64_t>(c->stats.levels, lv + 2);
         c->stats.max_frontier = std::max<uint64_t>(c->stats.max_frontier, c->level_count[lv + 1]);
     }
-    c->level_cands[lv] = 0;
     if (lv + 1 < c->levels.size() && c->level_count[lv + 1] > 0) return drain(r, lv + 1);
     return FCA_OK;
 }
@@ -344,21 +461,21 @@ fca_status enumerate_impl(fca_ctx *c, uint32_t *out, uint64_t capacity, uint64_t
     c->pairs_used = 0;
     if ((s = ensure_queues(c)) != FCA_OK) return s;
     if ((s = ensure_level(c, 0)) != FCA_OK) return s;
-    for (size_t i = 0; i < c->levels.size(); ++i) { c->level_count[i] = 0; c->level_cands[i] = 0; }
-    c->q_count[0] = c->q_count[1] = 0;
+    for (size_t i = 0; i < c->levels.size(); ++i) c->level_count[i] = 0;
+    for (int qi = 0; qi < NQ; ++qi) c->q_count[qi] = 0;
 
     Run r{c, out, capacity, st};
     const Dims &d = c->d;
     // counters: the top intent already occupies output row 0
-    memset(c->ctr_host, 0, sizeof(Counters));
-    c->ctr_host->out_count = 1;
+    Counters init{};
+    init.out_count = 1;
     if (capacity >= 1)
         CK(cudaMemcpyAsync(out, c->top, d.wm * 4, cudaMemcpyDeviceToDevice, st), "top intent copy");
 
     // the root node (G, G', 0)
     if (d.n <= SMALL_MAX) {
-        const int qi = d.n <= 32 ? 0 : 1;
-        const int per = 32 * (qi + 1);
+        const int qi = d.n <= 32 ? 0 : d.n <= 64 ? 1 : d.n <= 128 ? 2 : 3;
+        const int per = 32 << qi;
         uint32_t *ids = c->stage;
         for (int i = 0; i < per; ++i) ids[i] = i < d.n ? (uint32_t)i : 0u;
         int32_t *meta = reinterpret_cast<int32_t *>(c->stage + per);
@@ -369,7 +486,7 @@ fca_status enumerate_impl(fca_ctx *c, uint32_t *out, uint64_t capacity, uint64_t
         CK(cudaMemcpyAsync(Q.itt, c->top, d.wm * 4, cudaMemcpyDeviceToDevice, st), "root entry");
         CK(cudaMemcpyAsync(Q.y, &meta[0], 4, cudaMemcpyHostToDevice, st), "root entry");
         CK(cudaMemcpyAsync(Q.n, &meta[1], 4, cudaMemcpyHostToDevice, st), "root entry");
-        c->ctr_host->q_count[qi] = 1;
+        init.q_count[qi] = 1;
         c->q_count[qi] = 1;
     } else {
         Level &L = c->levels[0];
@@ -379,14 +496,12 @@ fca_status enumerate_impl(fca_ctx *c, uint32_t *out, uint64_t capacity, uint64_t
         CK(cudaMemcpyAsync(L.itt, c->top, d.wm * 4, cudaMemcpyDeviceToDevice, st), "root entry");
         CK(cudaMemcpyAsync(L.y, &meta[0], 4, cudaMemcpyHostToDevice, st), "root entry");
         c->level_count[0] = 1;
-        c->level_cands[0] = (uint64_t)d.m;   // an upper bound is enough here
     }
-    CK(cudaMemcpyAsync(c->ctr, c->ctr_host, sizeof(Counters), cudaMemcpyHostToDevice, st), "counters");
-    CK(cudaStreamSynchronize(st), "stream synchronize");
+    if ((s = write_counters(r, init)) != FCA_OK) return s;
 
     if ((s = drain(r, 0)) != FCA_OK) return s;
-    if ((s = run_subtree(r, 0)) != FCA_OK) return s;
-    if ((s = run_subtree(r, 1)) != FCA_OK) return s;
+    for (int qi = 0; qi < NQ; ++qi)
+        if ((s = run_subtree(r, qi)) != FCA_OK) return s;
     if ((s = read_counters(r)) != FCA_OK) return s;
 
     uint64_t total = c->ctr_host->out_count;
@@ -451,9 +566,7 @@ fca_status fca_context_create(const uint32_t *rows, int64_t n_objects, int32_t n
     fca_ctx *c = new fca_ctx();
     auto fail = [&](fca_status s) {
         *out_ctx = nullptr;
-        std::string e = c->err;
         fca_free(c);
-        (void)e;
         return s;
     };
     cudaError_t e = cudaGetDevice(&c->device);
@@ -470,15 +583,16 @@ fca_status fca_context_create(const uint32_t *rows, int64_t n_objects, int32_t n
     if (expand_smem_per_warp(d) > 200 * 1024) return fail(FCA_ERR_INVALID);
 
     fca_status s;
-    if ((s = alloc_dev(c, (void **)&c->rows, (size_t)d.n * d.wm * 4, "rows")) != FCA_OK) return fail(s);
-    if ((s = alloc_dev(c, (void **)&c->cols, (size_t)d.m * d.wnp * 4, "columns")) != FCA_OK) return fail(s);
-    if ((s = alloc_dev(c, (void **)&c->top, (size_t)d.wm * 4, "top")) != FCA_OK) return fail(s);
-    if ((s = alloc_dev(c, (void **)&c->full_mask, (size_t)d.wm * 4, "mask")) != FCA_OK) return fail(s);
-    if ((s = alloc_dev(c, (void **)&c->root_ext, (size_t)d.wnp * 4, "root extent")) != FCA_OK) return fail(s);
-    if ((s = alloc_dev(c, (void **)&c->ctr, sizeof(Counters), "counters")) != FCA_OK) return fail(s);
-    c->pool_bytes = 0;
+    if ((s = alloc_raw(c, (void **)&c->rows, (size_t)d.n * d.wm * 4, "rows")) != FCA_OK ||
+        (s = alloc_raw(c, (void **)&c->cols, (size_t)d.m * d.wnp * 4, "columns")) != FCA_OK ||
+        (s = alloc_raw(c, (void **)&c->top, (size_t)d.wm * 4, "top")) != FCA_OK ||
+        (s = alloc_raw(c, (void **)&c->full_mask, (size_t)d.wm * 4, "mask")) != FCA_OK ||
+        (s = alloc_raw(c, (void **)&c->root_ext, (size_t)d.wnp * 4, "root extent")) != FCA_OK ||
+        (s = alloc_raw(c, (void **)&c->ctr, sizeof(Counters), "counters")) != FCA_OK)
+        return fail(s);
     if (cudaMallocHost((void **)&c->ctr_host, sizeof(Counters)) != cudaSuccess ||
-        cudaMallocHost((void **)&c->stage, 4096) != cudaSuccess) {
+        cudaMallocHost((void **)&c->stage, 4096) != cudaSuccess ||
+        cudaMallocHost((void **)&c->flag_host, 4) != cudaSuccess) {
         cudaGetLastError();
         c->err = "pinned host allocation failed";
         return fail(FCA_ERR_OOM);
@@ -486,15 +600,9 @@ fca_status fca_context_create(const uint32_t *rows, int64_t n_objects, int32_t n
 
     // host-side constants: the all-attribute intent and the all-object extent
     std::vector<uint32_t> mask(d.wm, 0xffffffffu), ext(d.wnp, 0u);
-    if (cudaMallocHost((void **)&c->flag_host, 4) != cudaSuccess) {
-        cudaGetLastError();
-        c->err = "pinned host allocation failed";
-        return fail(FCA_ERR_OOM);
-    }
     if (d.m & 31) mask[d.wm - 1] = (1u << (d.m & 31)) - 1u;
     for (int64_t w = 0; w < d.wn; ++w) ext[w] = 0xffffffffu;
     if (d.n & 31) ext[d.wn - 1] = (1u << (d.n & 31)) - 1u;
-
     if ((e = cudaMemcpy(c->full_mask, mask.data(), d.wm * 4, cudaMemcpyHostToDevice)) != cudaSuccess ||
         (e = cudaMemcpy(c->root_ext, ext.data(), d.wnp * 4, cudaMemcpyHostToDevice)) != cudaSuccess) {
         cuda_fail(c, e, "context set-up");
@@ -502,12 +610,24 @@ fca_status fca_context_create(const uint32_t *rows, int64_t n_objects, int32_t n
     }
     if ((s = load_table(c, rows, 0)) != FCA_OK) return fail(s);
 
-    // work-pool sizes (bytes per bitmap level and entries per object-list queue)
-    c->level_bytes = env_u64("FCA_LEVEL_BYTES", 256ull << 20);
-    c->queue_entries = env_u64("FCA_QUEUE_ENTRIES", 1ull << 20);
-    size_pools(c);
+    // work pools: initial sizes and the growth limit (half of the free device memory by default)
+    size_t free_b = 0, total_b = 0;
+    if (cudaMemGetInfo(&free_b, &total_b) != cudaSuccess) {
+        cudaGetLastError();
+        free_b = (size_t)8 << 30;
+    }
+    c->level_bytes = env_u64("FCA_LEVEL_BYTES", 64ull << 20);
+    c->queue_entries = env_u64("FCA_QUEUE_ENTRIES", 1ull << 18);
+    c->pool_limit = (size_t)env_u64("FCA_POOL_LIMIT_BYTES", free_b / 2);
     *out_ctx = c;
     return FCA_OK;
+}
+
+fca_status fca_context_load(fca_ctx *ctx, const uint32_t *rows, void *stream)
+{
+    if (!ctx || !rows) return FCA_ERR_INVALID;
+    ctx->err.clear();
+    return load_table(ctx, rows, (cudaStream_t)stream);
 }
 
 fca_status fca_enumerate(fca_ctx *ctx, uint32_t *out, uint64_t capacity, uint64_t *out_count, void *stream)
@@ -549,13 +669,6 @@ fca_status fca_enumerate_host(fca_ctx *ctx, uint32_t *out_host, uint64_t capacit
     return s;
 }
 
-fca_status fca_context_load(fca_ctx *ctx, const uint32_t *rows, void *stream)
-{
-    if (!ctx || !rows) return FCA_ERR_INVALID;
-    ctx->err.clear();
-    return load_table(ctx, rows, (cudaStream_t)stream);
-}
-
 fca_status fca_set_option(fca_ctx *ctx, int option, int64_t value)
 {
     if (!ctx || value < 0) return FCA_ERR_INVALID;
@@ -566,12 +679,13 @@ fca_status fca_set_option(fca_ctx *ctx, int option, int64_t value)
         return FCA_OK;
     case FCA_OPT_LEVEL_BYTES:
     case FCA_OPT_QUEUE_ENTRIES:
+    case FCA_OPT_POOL_LIMIT_BYTES:
         CK(cudaSetDevice(c->device), "cudaSetDevice");
         CK(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
         free_pools(c);
         if (option == FCA_OPT_LEVEL_BYTES) c->level_bytes = (uint64_t)value;
-        else c->queue_entries = (uint64_t)value;
-        size_pools(c);
+        else if (option == FCA_OPT_QUEUE_ENTRIES) c->queue_entries = (uint64_t)value;
+        else c->pool_limit = (size_t)value;
         return FCA_OK;
     default:
         return FCA_ERR_INVALID;

@@ -1,7 +1,7 @@
 // Internal declarations shared by the host driver and the kernels of libfca.
 //
-// Search model (FCbO-to-CUDA page, sections 2.1-2.4 and 5.3; Parallel FCBO
-// page, sections 1.3 and 2.1): a search node is (A, B, y) with extent A,
+// Search model (FCbO-to-CUDA article, sections 2.1-2.4 and 5.3; Parallel FCBO
+// article, sections 1.3 and 2.1): a search node is (A, B, y) with extent A,
 // intent B = A' and cursor y. Its candidates are the attributes j >= y that
 // are not in B (the saturation skip: j in B <=> A is inside column j). For a
 // candidate, C = A & column j and D = C'; the child (C, D, j+1) exists iff D
@@ -11,36 +11,38 @@
 // Two tiers, chosen by extent size:
 //  * bitmap tier: nodes whose extent has more than SMALL_MAX objects are held
 //    as N-bit bitmaps in level-synchronous frontiers; one warp evaluates one
-//    (parent, j) pair (kernel expand_bitmap_kernel);
-//  * object-list tier: a node with at most 32*NW objects (NW = 1 or 2) is
+//    (parent, j) pair (expand_bitmap_kernel);
+//  * object-list tier: a node with at most 32*NW objects (NW = 1, 2, 4, 8) is
 //    handed over as a list of object ids, and one warp runs its whole subtree
-//    in shared memory, on the columns restricted to those objects
-//    (kernel subtree_kernel<NW>). Every descendant of such a node has a subset
-//    of its objects, so the subtree never needs the bitmaps again; this is
-//    the FCbO-to-CUDA page's section 5.3 rule of finishing small extents
-//    in-block instead of re-enqueueing them.
+//    on the columns restricted to those objects (subtree_kernel<NW>). Every
+//    descendant of such a node has a subset of its objects, so the subtree
+//    never needs the bitmaps again; this is the FCbO-to-CUDA article's
+//    section 5.3 rule of finishing small extents in-block instead of
+//    re-enqueueing them.
 #pragma once
 #include <cstdint>
 
 namespace fca {
 
-constexpr int SMALL_MAX = 64;      // largest extent handed to the object-list tier
+constexpr int SMALL_MAX = 256;     // largest extent handed to the object-list tier
+constexpr int NQ = 4;              // object-list queues: queue q holds extents of <= 32 << q objects
 constexpr int MAX_ATTRS = 1024;    // M limit (intent words fit one per lane)
-constexpr int WARP = 32;
 
-// Device-side counters of one enumerate call (one 128-byte block).
+// Overflow bits of Counters::error (a destination was too small; the driver rolls back and retries).
+constexpr unsigned ERR_NEXT = 1u << 4;     // next bitmap level
+constexpr unsigned ERR_QUEUE0 = 1u;        // queue q sets ERR_QUEUE0 << q
+
+// Device-side counters of one enumerate call.
 struct Counters {
-    unsigned long long out_count;     // intents emitted so far (row index allocator)
-    unsigned long long closures;      // candidates evaluated
-    unsigned long long next_count;    // entries appended to the next bitmap level
-    unsigned long long q_count[2];    // entries appended to the object-list queues
-    unsigned long long next_cands;    // candidates of the entries appended to the next level
-    unsigned long long q_head[2];     // work-distribution cursors of the subtree kernels
-    unsigned long long chunk_closures;// candidates evaluated by the current expand launch
-    unsigned long long word_ops;      // counted object-list-tier word operations (when counting)
-    unsigned long long bytes;         // counted bitmap-tier bytes (when counting)
-    unsigned int error;               // nonzero: an internal capacity check failed
-    unsigned int pad[1];
+    unsigned long long out_count;      // intents emitted so far (row index allocator)
+    unsigned long long closures;       // candidates evaluated
+    unsigned long long next_count;     // entries appended to the next bitmap level
+    unsigned long long q_count[NQ];    // entries appended to the object-list queues
+    unsigned long long q_head[NQ];     // work-distribution cursors of the subtree kernels
+    unsigned long long word_ops;       // counted object-list-tier word operations (when counting)
+    unsigned long long bytes;          // counted bitmap-tier bytes (when counting)
+    unsigned int error;                // overflow bits (ERR_*)
+    unsigned int pad[3];
 };
 
 // A bitmap-tier frontier level (structure of arrays).
@@ -51,7 +53,7 @@ struct Level {
     uint64_t cap;
 };
 
-// An object-list queue of subtree roots for the NW-word tier.
+// A queue of subtree roots for the NW-word object-list tier.
 struct Queue {
     uint32_t *ids;   // cap x (32*NW) object ids, ascending
     uint32_t *itt;   // cap x wm words (intents)
@@ -75,7 +77,7 @@ struct ExpandArgs {
     Level in;               // parents
     uint64_t p_begin, p_count;
     Level next;             // children with more than SMALL_MAX objects
-    Queue q1, q2;           // children with <= 32 / <= 64 objects
+    Queue q[NQ];            // children with <= 32 << q objects
     uint32_t *out;          // capacity x wm
     uint64_t capacity;
     Counters *ctr;
@@ -87,15 +89,16 @@ struct SubtreeArgs {
     const uint32_t *rows;
     Queue q;
     uint64_t q_count;
-    int q_index;            // which q_head / q_count counter this queue uses
+    int q_index;            // which q_head counter this queue uses
     int slices;             // work items per root (set by the launcher)
     uint32_t *out;
     uint64_t capacity;
     Counters *ctr;
+    uint32_t *gstack;       // ancestor stacks in global memory (NW >= 4), per resident warp
     int count_work;         // 1: accumulate Counters::word_ops
 };
 
-// Launch wrappers (defined in fca_kernels.cu). Each returns cudaGetLastError().
+// Launch wrappers (defined in fca_kernels.cu). Each returns a cudaError_t value.
 int launch_mask_rows(uint32_t *rows, const Dims &d, void *stream);
 int launch_transpose(const uint32_t *rows, uint32_t *cols, const Dims &d, void *stream);
 int launch_top(const uint32_t *rows, uint32_t *top, uint32_t *flag_full_row, const Dims &d,
@@ -103,6 +106,8 @@ int launch_top(const uint32_t *rows, uint32_t *top, uint32_t *flag_full_row, con
 int launch_expand(const ExpandArgs &a, int sm_count, void *stream);
 int launch_subtree(const SubtreeArgs &a, int nw, int sm_count, void *stream);
 size_t expand_smem_per_warp(const Dims &d);
-size_t subtree_smem_per_warp(const Dims &d, int nw);
+// Words of global ancestor stack the subtree kernel of width nw needs (0 when it keeps the
+// stack in shared memory), for the grid it launches on this device.
+size_t subtree_gstack_words(const Dims &d, int nw, int sm_count);
 
 }  // namespace fca

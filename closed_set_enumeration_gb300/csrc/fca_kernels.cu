@@ -1,16 +1,17 @@
 // Kernels of libfca (sm_103a). Bitwise set algebra only: no tensor cores.
 //
+//  mask_rows_kernel      clears the padding bits past M of every row.
 //  transpose_kernel      ctxRows -> ctxCols, 32x32 bit tiles by warp ballots
-//                        (Parallel FCBO page, section 3.1 builds the same
-//                        column bitmaps with one atomicOr per set bit).
+//                        (the Parallel FCBO article, section 3.1, builds the
+//                        same column bitmaps with one atomicOr per set bit).
 //  top_kernel            top intent G' = AND of all rows, and whether some
 //                        row holds every attribute (then the bottom concept
 //                        has a non-empty extent and the search reaches it).
 //  expand_bitmap_kernel  bitmap tier: one warp per (parent, j) candidate:
 //                        extent intersection, closure, canonical test,
-//                        compaction of the child (FCbO-to-CUDA page, sections
-//                        2.1-2.3, 4.2-4.4; Parallel FCBO page, sections 2.1,
-//                        3.2).
+//                        compaction of the child (FCbO-to-CUDA article,
+//                        sections 2.1-2.3, 4.2-4.4; Parallel FCBO article,
+//                        sections 2.1, 3.2).
 //  subtree_kernel<NW>    object-list tier: one warp runs a whole subtree whose
 //                        root extent holds at most 32*NW objects.
 #include <cuda_runtime.h>
@@ -24,8 +25,8 @@ namespace {
 
 constexpr unsigned FULL = 0xffffffffu;
 constexpr int OUTBUF = 16;          // intents buffered per warp before one atomicAdd
-constexpr int REG_WORDS = 8;        // largest compact intent (x32 attributes) kept in registers
 constexpr int MAX_SLICES = 32;      // most work items one subtree root is split into
+constexpr int WARPS_PER_BLOCK = 8;
 
 __device__ __forceinline__ unsigned popc4(const uint4 &x)
 {
@@ -43,6 +44,16 @@ __device__ __forceinline__ uint32_t ge_mask(int w, int b)
 
 // Bits < b of word `w`.
 __device__ __forceinline__ uint32_t lt_mask(int w, int b) { return ~ge_mask(w, b); }
+
+// Largest number of restricted-column words (x32 attributes) a lane keeps in registers.
+__host__ __device__ constexpr int reg_words(int nw) { return nw <= 2 ? 8 : 16 / nw; }
+
+// Entry size in 32-bit words of an object-list queue root holding `cnt` objects (counting only).
+__device__ __forceinline__ unsigned queue_entry_words(unsigned cnt, int wm)
+{
+    const unsigned per = cnt <= 32u ? 32u : cnt <= 64u ? 64u : cnt <= 128u ? 128u : 256u;
+    return per + (unsigned)wm + 2u;
+}
 
 // ------------------------------------------------------------------ context build
 
@@ -140,7 +151,7 @@ __global__ void __launch_bounds__(256) expand_bitmap_kernel(ExpandArgs a)
     const uint4 *cols4 = reinterpret_cast<const uint4 *>(a.cols);
     const uint4 *ext4 = reinterpret_cast<const uint4 *>(a.in.ext);
 
-    unsigned long long my_closures = 0, my_next_cands = 0, my_bytes = 0;
+    unsigned long long my_closures = 0, my_bytes = 0;
     unsigned loads = 0;   // uint4 loads of columns by this lane (counting only)
     const unsigned long long total = a.p_count * (unsigned long long)d.m;
     const unsigned long long nwarps = (unsigned long long)gridDim.x * wpb;
@@ -200,15 +211,17 @@ __global__ void __launch_bounds__(256) expand_bitmap_kernel(ExpandArgs a)
         }
         __syncwarp();
 
-        // U = AND of the rows of those objects (exact D when |C| <= SMALL_MAX). Lane w: word w.
-        uint32_t U = FULL, Bw = 0;
-        if (lane < (unsigned)d.wm) {
-            for (unsigned i = 0; i < need; ++i) U &= __ldg(a.rows + (size_t)ids[i] * d.wm + lane);
-            Bw = B[lane];
-        } else {
-            U = 0;
+        // U = AND of the rows of those objects (exact D when |C| <= SMALL_MAX): each lane ANDs the
+        // rows of every 32nd object, then one reduction per word; lane w keeps word w.
+        uint32_t U = 0;
+        for (int w = 0; w < d.wm; ++w) {
+            uint32_t acc = FULL;
+            for (unsigned i = lane; i < need; i += 32) acc &= __ldg(a.rows + (size_t)ids[i] * d.wm + w);
+            acc = __reduce_and_sync(FULL, acc);
+            if ((int)lane == w) U = acc;
         }
         if (COUNT && lane == 0) my_bytes += (unsigned long long)need * d.wm * 4;   // rows read
+        const uint32_t Bw = lane < (unsigned)d.wm ? B[lane] : 0u;
         const int ju = j >> 5;
         const uint32_t jbit = 1u << (j & 31);
         const uint32_t pm = lt_mask((int)lane, j);   // attributes below j
@@ -241,9 +254,8 @@ __global__ void __launch_bounds__(256) expand_bitmap_kernel(ExpandArgs a)
 
         if (COUNT && lane == 0) {   // the intent row and the child entry written
             my_bytes += (unsigned long long)d.wm * 4;
-            my_bytes += cnt <= (unsigned)SMALL_MAX
-                            ? (unsigned long long)(4 * (cnt <= 32u ? 32 : 64) + 4 * d.wm + 8)
-                            : (unsigned long long)(4 * d.wnp + 4 * d.wm + 4);
+            my_bytes += cnt <= (unsigned)SMALL_MAX ? 4ull * queue_entry_words(cnt, d.wm)
+                                                   : (unsigned long long)(4 * d.wnp + 4 * d.wm + 4);
         }
         // emit the intent
         unsigned long long slot = 0;
@@ -251,16 +263,17 @@ __global__ void __launch_bounds__(256) expand_bitmap_kernel(ExpandArgs a)
         slot = __shfl_sync(FULL, slot, 0);
         if (slot < a.capacity && lane < (unsigned)d.wm) a.out[slot * d.wm + lane] = Dw;
 
-        // the child (C, D, j+1)
+        // the child (C, D, j+1): an object-list root, or an entry of the next bitmap level.
+        // A destination that is full only counts; the driver rolls the launch back and retries.
         if (cnt <= (unsigned)SMALL_MAX) {
-            const int qi = cnt <= 32u ? 0 : 1;
-            const Queue &Q = qi == 0 ? a.q1 : a.q2;
-            const int per = qi == 0 ? 32 : 64;
+            const int qi = cnt <= 32u ? 0 : cnt <= 64u ? 1 : cnt <= 128u ? 2 : 3;
+            const Queue &Q = a.q[qi];
+            const int per = 32 << qi;
             unsigned long long s = 0;
             if (lane == 0) s = atomicAdd(&a.ctr->q_count[qi], 1ull);
             s = __shfl_sync(FULL, s, 0);
             if (s >= Q.cap) {
-                if (lane == 0) atomicOr(&a.ctr->error, 1u);
+                if (lane == 0) atomicOr(&a.ctr->error, ERR_QUEUE0 << qi);
                 continue;
             }
             for (int i = (int)lane; i < per; i += 32) Q.ids[s * per + i] = i < (int)cnt ? ids[i] : 0u;
@@ -271,17 +284,13 @@ __global__ void __launch_bounds__(256) expand_bitmap_kernel(ExpandArgs a)
             if (lane == 0) s = atomicAdd(&a.ctr->next_count, 1ull);
             s = __shfl_sync(FULL, s, 0);
             if (s >= a.next.cap) {
-                if (lane == 0) atomicOr(&a.ctr->error, 2u);
+                if (lane == 0) atomicOr(&a.ctr->error, ERR_NEXT);
                 continue;
             }
             uint4 *dst = reinterpret_cast<uint4 *>(a.next.ext) + s * wq;
             for (int q = (int)lane; q < wq; q += 32) dst[q] = Csm[q];
             if (lane < (unsigned)d.wm) a.next.itt[s * d.wm + lane] = Dw;
             if (lane == 0) a.next.y[s] = j + 1;
-            // candidates of the child: attributes > j not in D
-            unsigned c = lane < (unsigned)d.wm ? __popc(Dw & ge_mask((int)lane, j + 1)) : 0u;
-            c = __reduce_add_sync(FULL, c);
-            my_next_cands += (unsigned long long)(d.m - j - 1 - (int)c);
         }
         __syncwarp();
     }
@@ -289,26 +298,24 @@ __global__ void __launch_bounds__(256) expand_bitmap_kernel(ExpandArgs a)
         const unsigned tl = __reduce_add_sync(FULL, loads);
         if (lane == 0) atomicAdd(&a.ctr->bytes, my_bytes + 16ull * tl);
     }
-    if (lane == 0) {
-        if (my_closures) {
-            atomicAdd(&a.ctr->closures, my_closures);
-            atomicAdd(&a.ctr->chunk_closures, my_closures);
-        }
-        if (my_next_cands) atomicAdd(&a.ctr->next_cands, my_next_cands);
-    }
+    if (lane == 0 && my_closures) atomicAdd(&a.ctr->closures, my_closures);
 }
 
 // ------------------------------------------------------------------ object-list tier
 
+// Shared-memory layout of one warp of subtree_kernel<NW> (32-bit words).
 struct SubtreeLayout {
     int mp, wm, fr, fs;
+    bool gstack;
     size_t o_rmap, o_rootb, o_rm, o_rlo, o_sufb, o_dsc, o_stack, o_outbuf, words;
     __host__ __device__ SubtreeLayout(const Dims &d, int nw)
     {
         mp = (d.m + 31) & ~31;
         wm = d.wm;
         fr = (32 * nw < d.m ? 32 * nw : d.m) + 1;     // depth <= |extent| and <= |R|
-        fs = nw + 1 + (wm > REG_WORDS ? wm : REG_WORDS);   // frame: extent mask, cursor, intent
+        const int rw = reg_words(nw);
+        fs = nw + 1 + (wm > rw ? wm : rw);            // frame: extent mask, cursor, intent
+        gstack = nw >= 4;                             // deep stacks live in global memory
         o_rmap = (size_t)nw * mp;
         o_rootb = o_rmap + mp / 2;
         o_rm = o_rootb + 32;
@@ -316,7 +323,7 @@ struct SubtreeLayout {
         o_sufb = o_rlo + 34;
         o_dsc = o_sufb + 32;
         o_stack = o_dsc + 34;
-        o_outbuf = o_stack + (size_t)fr * fs;
+        o_outbuf = o_stack + (gstack ? 0 : (size_t)fr * fs);
         words = o_outbuf + (size_t)OUTBUF * wm;
         words = (words + 3) & ~(size_t)3;
     }
@@ -332,7 +339,7 @@ struct SubtreeWarp {
     uint32_t *rlo;      // first compact index of each full word (wm + 1 entries)
     uint32_t *sufB;     // root-intent attributes in the words above each word
     uint32_t *dsc;      // compact intent of the child being written
-    uint32_t *stk;      // search stack
+    uint32_t *stk;      // search stack (shared or global memory)
     uint32_t *ob;       // output buffer, OUTBUF x wm
     int mp, wm, fs, m;
     uint32_t *out;
@@ -399,7 +406,7 @@ struct SubtreeWarp {
 
 // Depth-first search of one subtree with the restricted columns in registers: lane l holds the
 // columns of compact attributes 32u + l, u < WRT (R <= 32 * WRT). Extent, intent and cursor of
-// the current node are warp-uniform registers; the stack of ancestors is in shared memory.
+// the current node are warp-uniform registers; the stack of ancestors is in memory.
 template <int NW, int WRT, bool COUNT>
 __device__ void dfs_regs(SubtreeWarp &S, int R, int n, int jn, int slices, int slice)
 {
@@ -595,7 +602,8 @@ __global__ void __launch_bounds__(256) subtree_kernel(SubtreeArgs a)
     const Dims d = a.d;
     const SubtreeLayout L(d, NW);
     const unsigned lane = threadIdx.x & 31;
-    uint32_t *base = smw + (size_t)(threadIdx.x >> 5) * L.words;
+    const int wib = threadIdx.x >> 5;
+    uint32_t *base = smw + (size_t)wib * L.words;
     SubtreeWarp S;
     S.cR = base;
     S.rmap = reinterpret_cast<uint16_t *>(base + L.o_rmap);
@@ -604,7 +612,8 @@ __global__ void __launch_bounds__(256) subtree_kernel(SubtreeArgs a)
     S.rlo = base + L.o_rlo;
     S.sufB = base + L.o_sufb;
     S.dsc = base + L.o_dsc;
-    S.stk = base + L.o_stack;
+    S.stk = L.gstack ? a.gstack + ((size_t)blockIdx.x * (blockDim.x >> 5) + wib) * (size_t)L.fr * L.fs
+                     : base + L.o_stack;
     S.ob = base + L.o_outbuf;
     S.mp = L.mp;
     S.wm = d.wm;
@@ -696,11 +705,12 @@ __global__ void __launch_bounds__(256) subtree_kernel(SubtreeArgs a)
         }
 
         // ---- depth-first search of the subtree
+        constexpr int RW = reg_words(NW);
         const int sl = a.slices;
         if (R <= 32) dfs_regs<NW, 1, COUNT>(S, R, n, jn, sl, slice);
         else if (R <= 64) dfs_regs<NW, 2, COUNT>(S, R, n, jn, sl, slice);
-        else if (R <= 128) dfs_regs<NW, 4, COUNT>(S, R, n, jn, sl, slice);
-        else if (R <= 32 * REG_WORDS) dfs_regs<NW, REG_WORDS, COUNT>(S, R, n, jn, sl, slice);
+        else if (RW >= 4 && R <= 128) dfs_regs<NW, (RW >= 4 ? 4 : 1), COUNT>(S, R, n, jn, sl, slice);
+        else if (RW >= 8 && R <= 256) dfs_regs<NW, (RW >= 8 ? 8 : 1), COUNT>(S, R, n, jn, sl, slice);
         else dfs_smem<NW, COUNT>(S, R, n, jn, sl, slice);
         __syncwarp();
     }
@@ -743,12 +753,10 @@ size_t expand_smem_per_warp(const Dims &d)
     return ((size_t)(d.wnp / 4) + SMALL_MAX / 4) * sizeof(uint4);
 }
 
-size_t subtree_smem_per_warp(const Dims &d, int nw) { return SubtreeLayout(d, nw).words * 4; }
-
 static int warps_for(size_t per_warp)
 {
     const size_t budget = 200 * 1024;
-    int w = 8;
+    int w = WARPS_PER_BLOCK;
     while (w > 1 && (size_t)w * per_warp > budget) --w;
     return w;
 }
@@ -781,10 +789,11 @@ int launch_expand(const ExpandArgs &a, int sm_count, void *stream)
     return a.count_work ? launch_expand_t<true>(a, sm_count, stream) : launch_expand_t<false>(a, sm_count, stream);
 }
 
+// Block shape of the subtree kernel (persistent: at most one block per resident slot).
 template <int NW, bool COUNT>
-static int launch_subtree_nw(const SubtreeArgs &a, int sm_count, void *stream)
+static int subtree_shape(const Dims &d, int *wpb_out, size_t *smem_out, int *per_sm_out)
 {
-    const size_t pw = subtree_smem_per_warp(a.d, NW);
+    const size_t pw = SubtreeLayout(d, NW).words * 4;
     const int wpb = warps_for(pw);
     const size_t smem = pw * wpb;
     if (smem > 48 * 1024) {
@@ -793,14 +802,29 @@ static int launch_subtree_nw(const SubtreeArgs &a, int sm_count, void *stream)
         if (e != cudaSuccess) return (int)e;
     }
     int per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, subtree_kernel<NW, COUNT>, wpb * 32, smem);
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, subtree_kernel<NW, COUNT>,
+                                                                  wpb * 32, smem);
+    if (e != cudaSuccess) return (int)e;
     if (per_sm < 1) per_sm = 1;
+    *wpb_out = wpb;
+    *smem_out = smem;
+    *per_sm_out = per_sm;
+    return (int)cudaSuccess;
+}
+
+template <int NW, bool COUNT>
+static int launch_subtree_nw(const SubtreeArgs &a, int sm_count, void *stream)
+{
+    int wpb = 0, per_sm = 0;
+    size_t smem = 0;
+    int e = subtree_shape<NW, COUNT>(a.d, &wpb, &smem, &per_sm);
+    if (e != (int)cudaSuccess) return e;
     // split roots into slices when there are too few roots to keep every resident warp busy
     SubtreeArgs b = a;
     const unsigned long long resident = (unsigned long long)sm_count * per_sm * wpb;
     const unsigned long long want = 16 * resident;
-    b.slices = (int)std::min<unsigned long long>(MAX_SLICES, std::max<unsigned long long>(
-                                                     1, (want + a.q_count - 1) / std::max<unsigned long long>(1, a.q_count)));
+    const unsigned long long qn = std::max<unsigned long long>(1, a.q_count);
+    b.slices = (int)std::min<unsigned long long>(MAX_SLICES, std::max<unsigned long long>(1, (want + qn - 1) / qn));
     unsigned long long blocks = (a.q_count * b.slices + wpb - 1) / wpb;
     const unsigned long long cap = (unsigned long long)sm_count * per_sm;
     if (blocks > cap) blocks = cap;
@@ -809,11 +833,42 @@ static int launch_subtree_nw(const SubtreeArgs &a, int sm_count, void *stream)
     return (int)cudaGetLastError();
 }
 
+template <int NW>
+static size_t gstack_words_nw(const Dims &d, int sm_count)
+{
+    const SubtreeLayout L(d, NW);
+    int wpb = 0, per_sm = 0, wpb2 = 0, per_sm2 = 0;
+    size_t smem = 0;
+    if (subtree_shape<NW, false>(d, &wpb, &smem, &per_sm) != (int)cudaSuccess ||
+        subtree_shape<NW, true>(d, &wpb2, &smem, &per_sm2) != (int)cudaSuccess)
+        return 0;
+    const size_t warps = (size_t)sm_count * (size_t)std::max(per_sm * wpb, per_sm2 * wpb2);
+    return warps * (size_t)L.fr * (size_t)L.fs;
+}
+
+size_t subtree_gstack_words(const Dims &d, int nw, int sm_count)
+{
+    if (nw == 4) return gstack_words_nw<4>(d, sm_count);
+    if (nw == 8) return gstack_words_nw<8>(d, sm_count);
+    return 0;
+}
+
 int launch_subtree(const SubtreeArgs &a, int nw, int sm_count, void *stream)
 {
-    if (a.count_work)
-        return nw == 1 ? launch_subtree_nw<1, true>(a, sm_count, stream) : launch_subtree_nw<2, true>(a, sm_count, stream);
-    return nw == 1 ? launch_subtree_nw<1, false>(a, sm_count, stream) : launch_subtree_nw<2, false>(a, sm_count, stream);
+    if (a.count_work) {
+        switch (nw) {
+        case 1: return launch_subtree_nw<1, true>(a, sm_count, stream);
+        case 2: return launch_subtree_nw<2, true>(a, sm_count, stream);
+        case 4: return launch_subtree_nw<4, true>(a, sm_count, stream);
+        default: return launch_subtree_nw<8, true>(a, sm_count, stream);
+        }
+    }
+    switch (nw) {
+    case 1: return launch_subtree_nw<1, false>(a, sm_count, stream);
+    case 2: return launch_subtree_nw<2, false>(a, sm_count, stream);
+    case 4: return launch_subtree_nw<4, false>(a, sm_count, stream);
+    default: return launch_subtree_nw<8, false>(a, sm_count, stream);
+    }
 }
 
 }  // namespace fca

@@ -25,14 +25,14 @@ EXPORTS = (
 )
 
 
-FCA_OPT_COUNT_WORK, FCA_OPT_LEVEL_BYTES, FCA_OPT_QUEUE_ENTRIES = 1, 2, 3
+FCA_OPT_COUNT_WORK, FCA_OPT_LEVEL_BYTES, FCA_OPT_QUEUE_ENTRIES, FCA_OPT_POOL_LIMIT_BYTES = 1, 2, 3, 4
 
 
 class FcaStats(ctypes.Structure):
     _fields_ = [(name, ctypes.c_uint64) for name in (
         "concepts", "closures", "large_parents", "small_roots", "launches", "levels",
         "max_frontier", "frontier_bytes", "expand_launches", "subtree_launches",
-        "subtree_word_ops", "expand_bytes")] + [("expand_ms", ctypes.c_double),
+        "subtree_word_ops", "expand_bytes", "retries")] + [("expand_ms", ctypes.c_double),
                                                 ("subtree_ms", ctypes.c_double)]
 
     def as_dict(self) -> dict:

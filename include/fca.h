@@ -44,7 +44,7 @@ typedef struct {
     uint64_t concepts;         /* intents found (= *out_count) */
     uint64_t closures;         /* candidates (A, B, j) evaluated: j >= cursor, j not in B */
     uint64_t large_parents;    /* search nodes expanded by the bitmap-extent kernel */
-    uint64_t small_roots;      /* subtrees handed to the object-list kernel (extent <= 64) */
+    uint64_t small_roots;      /* subtrees handed to the object-list kernels (extent <= 256) */
     uint64_t launches;         /* kernels launched by the call */
     uint64_t levels;           /* deepest bitmap-frontier level used, plus one */
     uint64_t max_frontier;     /* largest number of bitmap entries held by one level */
@@ -53,15 +53,17 @@ typedef struct {
     uint64_t subtree_launches; /* launches of the object-list kernels */
     uint64_t subtree_word_ops; /* counted work of the object-list tier (FCA_OPT_COUNT_WORK) */
     uint64_t expand_bytes;     /* counted bytes moved by the bitmap tier (FCA_OPT_COUNT_WORK) */
+    uint64_t retries;          /* bitmap-tier launches rolled back because a work pool was full */
     double expand_ms;          /* device time of the bitmap-extent kernel launches */
     double subtree_ms;         /* device time of the object-list kernel launches */
 } fca_stats;
 
 /* Options for fca_set_option. */
 typedef enum {
-    FCA_OPT_COUNT_WORK = 1,    /* 0/1: count the algorithmic work of each kernel (slower) */
-    FCA_OPT_LEVEL_BYTES = 2,   /* bytes of one bitmap-frontier level buffer (default 512 MiB) */
-    FCA_OPT_QUEUE_ENTRIES = 3  /* entries of each object-list queue (default 2^21) */
+    FCA_OPT_COUNT_WORK = 1,       /* 0/1: count the algorithmic work of each kernel (slower) */
+    FCA_OPT_LEVEL_BYTES = 2,      /* initial bytes of one bitmap-frontier level (default 64 MiB) */
+    FCA_OPT_QUEUE_ENTRIES = 3,    /* initial entries of each object-list queue (default 2^18) */
+    FCA_OPT_POOL_LIMIT_BYTES = 4  /* growth limit of all work pools (default: half the free memory) */
 } fca_option;
 
 /*
@@ -120,10 +122,15 @@ fca_status fca_enumerate_host(fca_ctx *ctx, uint32_t *out_host, uint64_t capacit
                               uint64_t *out_count, void *stream);
 
 /*
- * Set an option of a context (fca_option). The two pool sizes are rounded up
- * to hold at least 4*M entries; changing them frees the pools, which are
- * allocated again by the next enumerate call. FCA_ERR_INVALID for an unknown
- * option or a negative value.
+ * Set an option of a context (fca_option). Pools start at the initial sizes
+ * (rounded up to at least 4*M entries) and grow on demand up to the limit;
+ * past the limit a frontier level is expanded in smaller chunks. Changing a
+ * pool option frees the pools, which are allocated again by the next
+ * enumerate call. The same sizes can be set before creation through the
+ * environment variables FCA_LEVEL_BYTES, FCA_QUEUE_ENTRIES and
+ * FCA_POOL_LIMIT_BYTES. FCA_ERR_INVALID for an unknown option or a negative
+ * value; FCA_ERR_OOM from enumerate when the limit cannot hold the children
+ * of a single search node.
  */
 fca_status fca_set_option(fca_ctx *ctx, int option, int64_t value);
 

@@ -68,7 +68,11 @@ def test_random_contexts(n, m, density, seed):
 
 
 @pytest.mark.parametrize("n,m,density,seed", [(3000, 128, 0.08, 3), (2000, 300, 0.03, 4),
-                                              (5000, 1024, 0.004, 5), (800, 1000, 0.02, 6)])
+                                              (5000, 1024, 0.004, 5), (800, 1000, 0.02, 6),
+                                              # roots of 100-256 objects: the 4- and 8-word object-list
+                                              # tiers, with registers (R <= 128) and shared memory (R > 128)
+                                              (250, 300, 0.1, 2), (200, 128, 0.15, 3), (256, 200, 0.12, 4),
+                                              (120, 300, 0.2, 5), (100, 700, 0.1, 6)])
 def test_larger_random_contexts(n, m, density, seed):
     rows = cx.random_context(n, m, density, seed)
     check_against_oracle(rows, n, m, threads=8)
@@ -178,18 +182,23 @@ def test_enumerate_host_and_reuse():
             assert same_set(got, ref)
 
 
-def test_bounded_pools_force_chunking(monkeypatch):
-    # tiny work pools: levels are expanded in many chunks, depth first, and queues drain early
+@pytest.mark.parametrize("limit", [None, "1"])
+def test_small_pools_roll_back_and_chunk(monkeypatch, limit):
+    # tiny initial pools: launches overflow, are rolled back and retried after the destinations are
+    # emptied or grown; with a 1-byte growth limit, levels are split into ever smaller chunks instead
     n, m = 4000, 60
     rows = cx.random_context(n, m, 0.12, 12)
     rows[: n // 4, 0] |= np.uint32(0x00FF00FF)      # dense block -> large extents and deep bitmap levels
     ref = oracle.cbo(rows, n, m, threads=8)
     monkeypatch.setenv("FCA_LEVEL_BYTES", "1")       # floor: 4*M entries per level
     monkeypatch.setenv("FCA_QUEUE_ENTRIES", "1")     # floor: 4*M entries per queue
+    if limit:
+        monkeypatch.setenv("FCA_POOL_LIMIT_BYTES", limit)
     got, st = gpu_run(rows, n, m)
+    assert not has_duplicates(got)
     assert same_set(got, ref["intents"])
     assert st["closures"] == ref["closures"]
-    assert st["launches"] > 10
+    assert st["retries"] > 0
 
 
 @pytest.mark.parametrize("name", ["tiny", "sparse"])
