@@ -22,6 +22,7 @@ FCA_OK, FCA_ERR_INVALID, FCA_ERR_OOM, FCA_ERR_CAPACITY, FCA_ERR_CUDA = range(5)
 EXPORTS = (
     "fca_context_create", "fca_context_load", "fca_enumerate", "fca_enumerate_host", "fca_set_option",
     "fca_get_stats", "fca_context_dims", "fca_context_copy", "fca_last_error", "fca_free", "fca_status_string",
+    "fca_enumerate_small_noalloc",
 )
 
 
@@ -66,6 +67,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.fca_enumerate.argtypes = [vp, vp, u64, ctypes.POINTER(u64), vp]
         lib.fca_enumerate_host.argtypes = [vp, vp, u64, ctypes.POINTER(u64), vp]
         lib.fca_set_option.argtypes = [vp, ctypes.c_int, i64]
+        lib.fca_enumerate_small_noalloc.argtypes = [vp, i64, i32, vp, u64, ctypes.POINTER(u64), vp]
+        lib.fca_enumerate_small_noalloc.restype = ctypes.c_int
         lib.fca_get_stats.argtypes = [vp, ctypes.POINTER(FcaStats)]
         lib.fca_context_dims.argtypes = [vp, ctypes.POINTER(i64), ctypes.POINTER(i32)]
         lib.fca_context_copy.argtypes = [vp, ctypes.c_int, vp, u64]

@@ -134,6 +134,30 @@ fca_status fca_enumerate_host(fca_ctx *ctx, uint32_t *out_host, uint64_t capacit
  */
 fca_status fca_set_option(fca_ctx *ctx, int option, int64_t value);
 
+/*
+ * Enumerate every intent of a small context without allocating any memory.
+ * The paper has no counterpart: this entry point serves callers that may not
+ * call cudaMalloc/cudaFree while they run, because their device memory is
+ * owned entirely by another allocator (a framework's caching allocator or a
+ * fixed arena reserved at start-up) or because they run on a latency-critical
+ * path where an allocation, which can synchronize the device, is not allowed.
+ *
+ *   rows       N x W_M uint32 words as for fca_context_create (host or device
+ *              pointer); padding bits past M are ignored.
+ *   n_objects  1 <= N <= 64 (the whole search is one object-list subtree).
+ *   n_attrs    1 <= M <= 1024.
+ *   out, capacity, out_count, stream: as for fca_enumerate (out on the device).
+ * Larger sizes return FCA_ERR_INVALID. Its scratch (under 10 KB) is one
+ * file-scope device array, held by every GPU that loads the library until the
+ * process exits; the first call on a device looks up that array's device
+ * address, so make that first call before any stream capture. All calls on a
+ * device share the array and rewrite it: calls whose GPU work overlaps in time
+ * race. The call returns after the work on `stream` completes.
+ */
+fca_status fca_enumerate_small_noalloc(const uint32_t *rows, int64_t n_objects, int32_t n_attrs,
+                                       uint32_t *out, uint64_t capacity, uint64_t *out_count,
+                                       void *stream);
+
 /* Statistics of the last enumerate call (zeros before the first). */
 fca_status fca_get_stats(const fca_ctx *ctx, fca_stats *out);
 
