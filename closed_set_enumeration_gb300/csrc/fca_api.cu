@@ -44,11 +44,6 @@ struct fca_ctx {
     uint64_t q_count[NQ]{};
     uint32_t *gstack = nullptr;    // ancestor stacks of the wide object-list kernels
     size_t gstack_words = 0;
-    uint32_t *pieces[2] = {nullptr, nullptr};   // unfinished subtree nodes, double-buffered
-    uint64_t piece_cap = 0;        // records per buffer (records sized for the widest tier)
-    uint32_t *tables = nullptr;    // restricted-column tables of split subtree roots
-    uint64_t tables_cap = 0;       // words
-    int split_budget = 0;          // candidates a subtree item evaluates before it splits
     Counters *ctr = nullptr;        // device
     Counters *ctr_host = nullptr;   // pinned host mirror, current after every readback
     uint32_t *stage = nullptr;      // pinned host staging (root entry)
@@ -149,10 +144,6 @@ void free_pools(fca_ctx *c)
     cudaFree(c->gstack);
     c->gstack = nullptr;
     c->gstack_words = 0;
-    for (uint32_t *&p : c->pieces) { cudaFree(p); p = nullptr; }
-    cudaFree(c->tables);
-    c->tables = nullptr;
-    c->piece_cap = c->tables_cap = 0;
     c->pool_bytes = 0;
 }
 
@@ -317,27 +308,7 @@ fca_status write_counters(Run &r, const Counters &v)
     return FCA_OK;
 }
 
-// Piece buffers and the table pool of the object-list tier (allocated on first use).
-fca_status ensure_split_pools(fca_ctx *c)
-{
-    if (c->tables || c->split_budget <= 0) return FCA_OK;
-    const uint64_t cap = c->queue_entries;
-    const uint64_t pw = (uint64_t)piece_words(8, c->d.wm);
-    const uint64_t tw = 16 * cap + ((uint64_t)1 << 20);
-    fca_status s;
-    if ((s = alloc_raw(c, (void **)&c->pieces[0], cap * pw * 4, "subtree pieces")) != FCA_OK ||
-        (s = alloc_raw(c, (void **)&c->pieces[1], cap * pw * 4, "subtree pieces")) != FCA_OK ||
-        (s = alloc_raw(c, (void **)&c->tables, tw * 4, "subtree tables")) != FCA_OK)
-        return s;
-    c->piece_cap = cap;
-    c->tables_cap = tw;
-    c->pool_bytes += 2 * cap * pw * 4 + tw * 4;
-    return FCA_OK;
-}
-
-// Process every root waiting in object-list queue qi, then empty it. A subtree search that runs
-// past its candidate budget hands its unfinished nodes over as pieces; launches over the pieces
-// follow until none is left.
+// Process every root waiting in object-list queue qi, then empty it.
 fca_status run_subtree(Run &r, int qi)
 {
     fca_ctx *c = r.c;
@@ -351,11 +322,9 @@ fca_status run_subtree(Run &r, int qi)
         c->gstack_words = words;
         c->pool_bytes += words * 4;
     }
-    if ((s = ensure_split_pools(c)) != FCA_OK) return s;
     SubtreeArgs a{};
     a.d = c->d;
     a.rows = c->rows;
-    a.mode = 0;
     a.q = c->q[qi];
     a.q_count = c->q_count[qi];
     a.q_index = qi;
@@ -364,41 +333,17 @@ fca_status run_subtree(Run &r, int qi)
     a.ctr = c->ctr;
     a.gstack = c->gstack;
     a.count_work = c->count_work;
-    a.tables = c->tables;
-    a.tables_cap = c->tables ? c->tables_cap : 0;
-    a.budget = c->tables ? c->split_budget : 0;
-    int cur = 0;
-    uint64_t pieces = 0;
-    for (int round = 0;; ++round) {
-        a.pout = c->pieces[cur];
-        a.pout_cap = c->tables ? c->piece_cap : 0;
-        size_t pair = 0;
-        if ((s = time_begin(r, 1, &pair)) != FCA_OK) return s;
-        CK((cudaError_t)launch_subtree(a, nw, c->sm_count, r.st), "subtree kernel launch");
-        if ((s = time_end(r, pair)) != FCA_OK) return s;
-        c->stats.launches++;
-        c->stats.subtree_launches++;
-        if (round == 0) {
-            c->stats.small_roots += c->q_count[qi];
-            // empty the queue: its append counter and its work cursor
-            CK(cudaMemsetAsync(&c->ctr->q_count[qi], 0, sizeof(unsigned long long), r.st), "queue reset");
-            CK(cudaMemsetAsync(&c->ctr->q_head[qi], 0, sizeof(unsigned long long), r.st), "queue reset");
-            c->q_count[qi] = 0;
-        }
-        if ((s = read_counters(r)) != FCA_OK) return s;
-        pieces = std::min<uint64_t>(c->ctr_host->piece_count, a.pout_cap);
-        c->stats.pieces += pieces;
-        CK(cudaMemsetAsync(&c->ctr->piece_count, 0, sizeof(unsigned long long), r.st), "piece reset");
-        CK(cudaMemsetAsync(&c->ctr->piece_head, 0, sizeof(unsigned long long), r.st), "piece reset");
-        if (pieces == 0) break;
-        // the next launch runs the pieces just written and writes its own to the other buffer
-        a.mode = 1;
-        a.pin = c->pieces[cur];
-        a.pin_count = pieces;
-        cur ^= 1;
-    }
-    // every piece is done: the tables can be reused
-    CK(cudaMemsetAsync(&c->ctr->table_words, 0, sizeof(unsigned long long), r.st), "table reset");
+    size_t pair = 0;
+    if ((s = time_begin(r, 1, &pair)) != FCA_OK) return s;
+    CK((cudaError_t)launch_subtree(a, nw, c->sm_count, r.st), "subtree kernel launch");
+    if ((s = time_end(r, pair)) != FCA_OK) return s;
+    c->stats.launches++;
+    c->stats.subtree_launches++;
+    c->stats.small_roots += c->q_count[qi];
+    // empty the queue: its append counter and its work cursor
+    CK(cudaMemsetAsync(&c->ctr->q_count[qi], 0, sizeof(unsigned long long), r.st), "queue reset");
+    CK(cudaMemsetAsync(&c->ctr->q_head[qi], 0, sizeof(unsigned long long), r.st), "queue reset");
+    c->q_count[qi] = 0;
     return read_counters(r);
 }
 
@@ -673,7 +618,6 @@ fca_status fca_context_create(const uint32_t *rows, int64_t n_objects, int32_t n
     }
     c->level_bytes = env_u64("FCA_LEVEL_BYTES", 64ull << 20);
     c->queue_entries = env_u64("FCA_QUEUE_ENTRIES", 1ull << 18);
-    c->split_budget = (int)env_u64("FCA_SPLIT_BUDGET", 2048);
     c->pool_limit = (size_t)env_u64("FCA_POOL_LIMIT_BYTES", free_b / 2);
     *out_ctx = c;
     return FCA_OK;

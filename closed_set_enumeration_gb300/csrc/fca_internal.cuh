@@ -41,9 +41,6 @@ struct Counters {
     unsigned long long q_head[NQ];     // work-distribution cursors of the subtree kernels
     unsigned long long word_ops;       // counted object-list-tier word operations (when counting)
     unsigned long long bytes;          // counted bitmap-tier bytes (when counting)
-    unsigned long long piece_count;    // pieces appended by the current subtree launch
-    unsigned long long piece_head;     // work cursor over the input pieces
-    unsigned long long table_words;    // words of the subtree-table pool in use
     unsigned int error;                // overflow bits (ERR_*)
     unsigned int pad[3];
 };
@@ -87,28 +84,13 @@ struct ExpandArgs {
     int count_work;         // 1: accumulate Counters::bytes
 };
 
-// A subtree search that has spent its budget of candidates stops and hands its unfinished nodes
-// (the current node and every ancestor with candidates left) to the next launch as "pieces";
-// the restricted columns of its root are saved once in a table pool that the pieces refer to.
-// Piece record (piece_words(NW, wm) words): table offset, cursor, slice filter, 0, extent mask
-// (NW words), compact intent (wm words).
-__host__ __device__ constexpr int piece_words(int nw, int wm) { return 4 + nw + wm; }
-
 struct SubtreeArgs {
     Dims d;
     const uint32_t *rows;
-    int mode;               // 0: roots from q; 1: pieces from pin
     Queue q;
     uint64_t q_count;
     int q_index;            // which q_head counter this queue uses
     int slices;             // work items per root (set by the launcher)
-    const uint32_t *pin;    // input pieces (mode 1)
-    uint64_t pin_count;
-    uint32_t *pout;         // output pieces
-    uint64_t pout_cap;      // 0: never split
-    uint32_t *tables;       // subtree-table pool
-    uint64_t tables_cap;    // words
-    int budget;             // candidates per item before it splits (0: never)
     uint32_t *out;
     uint64_t capacity;
     Counters *ctr;

@@ -347,11 +347,6 @@ struct SubtreeWarp {
     Counters *ctr;
     int nb;             // intents waiting in the output buffer
     unsigned long long closures, ops;
-    // splitting: where unfinished nodes go, and this item's table (~0u: not saved yet)
-    uint32_t *pout, *tables;
-    unsigned long long pout_cap, tables_cap;
-    uint32_t toff;
-    int n;              // objects of the subtree root
 
     __device__ void flush()
     {
@@ -407,137 +402,13 @@ struct SubtreeWarp {
         const uint32_t hi = rb == 31 ? 0u : (rootB[rw] >> (rb + 1));
         closures += (unsigned long long)(m - rj - 1 - (int)sufB[rw] - __popc(hi) - above);
     }
-
-    // Table of a subtree root in the pool: R, n, 2 spare words, rootB, Rm, rlo (wm + 1), sufB,
-    // one spare word, the NW column planes (Rp = R rounded up to 32 words each), rmap (Rp / 2).
-    __device__ static int table_words(int nw, int wm, int R)
-    {
-        const int rp = (R + 31) & ~31;
-        return 4 + 4 * wm + 2 + nw * rp + rp / 2;
-    }
-
-    // Lane 0 reserves `k` slots of a counter bounded by `cap` without ever passing it (a bounded
-    // number of compare-and-swap attempts; giving up only means the caller does not split).
-    __device__ static bool reserve(unsigned long long *ctr_word, unsigned long long k, unsigned long long cap,
-                                   unsigned long long *at)
-    {
-        const unsigned lane = threadIdx.x & 31;
-        unsigned long long got = ~0ull;
-        if (lane == 0) {
-            unsigned long long old = *(volatile unsigned long long *)ctr_word;
-            for (int it = 0; it < 64 && old + k <= cap; ++it) {
-                const unsigned long long prev = atomicCAS(ctr_word, old, old + k);
-                if (prev == old) { got = old; break; }
-                old = prev;
-            }
-        }
-        got = __shfl_sync(FULL, got, 0);
-        *at = got;
-        return got != ~0ull;
-    }
-
-    // Save this root's table (once per item); false when the pool is full.
-    template <int NW>
-    __device__ bool save_table(int R)
-    {
-        if (toff != ~0u) return true;
-        const unsigned lane = threadIdx.x & 31;
-        const int tw = table_words(NW, wm, R);
-        unsigned long long at = 0;
-        if (!reserve(&ctr->table_words, (unsigned long long)tw, tables_cap, &at)) return false;
-        uint32_t *T = tables + at;
-        const int rp = (R + 31) & ~31;
-        if (lane == 0) { T[0] = (uint32_t)R; T[1] = (uint32_t)n; T[2] = 0u; T[3] = 0u; }
-        for (int i = (int)lane; i < wm; i += 32) {
-            T[4 + i] = rootB[i];
-            T[4 + wm + i] = Rm[i];
-            T[4 + 3 * wm + 1 + i] = sufB[i];
-        }
-        for (int i = (int)lane; i <= wm; i += 32) T[4 + 2 * wm + i] = rlo[i];
-        uint32_t *planes = T + 4 + 4 * wm + 2;
-        for (int t = 0; t < NW; ++t)
-            for (int k = (int)lane; k < rp; k += 32) planes[t * rp + k] = k < R ? cR[t * mp + k] : 0u;
-        const uint32_t *rm32 = reinterpret_cast<const uint32_t *>(rmap);
-        for (int i = (int)lane; i < rp / 2; i += 32) planes[NW * rp + i] = rm32[i];
-        toff = (uint32_t)at;
-        return true;
-    }
-
-    // Load a saved table into this warp's shared memory; returns R and sets n.
-    template <int NW>
-    __device__ int load_table(uint32_t off)
-    {
-        const unsigned lane = threadIdx.x & 31;
-        const uint32_t *T = tables + off;
-        const int R = (int)T[0];
-        n = (int)T[1];
-        const int rp = (R + 31) & ~31;
-        for (int i = (int)lane; i < 32; i += 32) {
-            rootB[i] = i < wm ? T[4 + i] : 0u;
-            Rm[i] = i < wm ? T[4 + wm + i] : 0u;
-            sufB[i] = i < wm ? T[4 + 3 * wm + 1 + i] : 0u;
-        }
-        for (int i = (int)lane; i <= wm; i += 32) rlo[i] = T[4 + 2 * wm + i];
-        const uint32_t *planes = T + 4 + 4 * wm + 2;
-        for (int t = 0; t < NW; ++t)
-            for (int k = (int)lane; k < rp; k += 32) cR[t * mp + k] = planes[t * rp + k];
-        uint32_t *rm32 = reinterpret_cast<uint32_t *>(rmap);
-        for (int i = (int)lane; i < rp / 2; i += 32) rm32[i] = planes[NW * rp + i];
-        toff = off;
-        __syncwarp();
-        return R;
-    }
-
-    // Hand the unfinished nodes over as pieces: frames 0..nframes-1 of the stack (the current node
-    // is the last one). A frame is (extent, cursor, compact intent of WR words). Frame 0 keeps the
-    // item's slice filter. Returns false (nothing written) when a pool is full.
-    template <int NW>
-    __device__ bool split(int nframes, int R, int WR, int slices, int slice)
-    {
-        const unsigned lane = threadIdx.x & 31;
-        const uint32_t validR = lt_mask((int)lane, R);
-        // pieces needed: frames with a candidate left (an attribute >= cursor outside the intent)
-        int k = 0;
-        for (int f = 0; f < nframes; ++f) {
-            const uint32_t *fr = stk + (size_t)f * fs;
-            const int jn = (int)fr[NW];
-            const uint32_t bw = lane < (unsigned)WR ? fr[NW + 1 + lane] : FULL;
-            k += __any_sync(FULL, (~bw & validR & ge_mask((int)lane, jn)) != 0u) ? 1 : 0;
-        }
-        if (k == 0) return true;
-        if (!save_table<NW>(R)) return false;
-        const int pw = piece_words(NW, wm);
-        unsigned long long at = 0;
-        if (!reserve(&ctr->piece_count, (unsigned long long)k, pout_cap, &at)) return false;
-        for (int f = 0; f < nframes; ++f) {
-            const uint32_t *fr = stk + (size_t)f * fs;
-            const int jn = (int)fr[NW];
-            const uint32_t bw = lane < (unsigned)WR ? fr[NW + 1 + lane] : FULL;
-            if (!__any_sync(FULL, (~bw & validR & ge_mask((int)lane, jn)) != 0u)) continue;
-            uint32_t *P = pout + at * pw;
-            for (int i = (int)lane; i < pw; i += 32) {
-                uint32_t v = 0u;
-                if (i == 0) v = toff;
-                else if (i == 1) v = (uint32_t)jn;
-                else if (i == 2) v = f == 0 ? ((uint32_t)slices | ((uint32_t)slice << 16)) : 1u;
-                else if (i >= 4 && i < 4 + NW) v = fr[i - 4];
-                else if (i >= 4 + NW && i - 4 - NW < WR) v = fr[NW + 1 + (i - 4 - NW)];
-                P[i] = v;
-            }
-            ++at;
-        }
-        return true;
-    }
 };
 
 // Depth-first search of one subtree with the restricted columns in registers: lane l holds the
 // columns of compact attributes 32u + l, u < WRT (R <= 32 * WRT). Extent, intent and cursor of
-// the current node are warp-uniform registers; the stack of ancestors is in memory. The search
-// starts at node (ext0, dsc[] compact intent, cursor jn); after `budget` candidates (0: never) it
-// hands its unfinished nodes to the next launch and stops.
+// the current node are warp-uniform registers; the stack of ancestors is in memory.
 template <int NW, int WRT, bool COUNT>
-__device__ void dfs_regs(SubtreeWarp &S, int R, const uint32_t (&ext0)[NW], int jn, int slices, int slice,
-                         int budget)
+__device__ void dfs_regs(SubtreeWarp &S, int R, int n, int jn, int slices, int slice)
 {
     const unsigned lane = threadIdx.x & 31;
     uint32_t col[WRT][NW];
@@ -549,31 +420,15 @@ __device__ void dfs_regs(SubtreeWarp &S, int R, const uint32_t (&ext0)[NW], int 
     }
     uint32_t valid[WRT], B[WRT];
 #pragma unroll
-    for (int u = 0; u < WRT; ++u) {
-        valid[u] = lt_mask(u, R);
-        B[u] = S.dsc[u] & valid[u];
-    }
+    for (int u = 0; u < WRT; ++u) { valid[u] = lt_mask(u, R); B[u] = 0u; }
     uint32_t ext[NW];
 #pragma unroll
-    for (int t = 0; t < NW; ++t) ext[t] = ext0[t];
-    const int WR = (R + 31) >> 5;
-    int depth = 0, visits = 0;
+    for (int t = 0; t < NW; ++t) {
+        const int k = n - 32 * t;
+        ext[t] = k >= 32 ? FULL : (k > 0 ? ((1u << k) - 1u) : 0u);
+    }
+    int depth = 0;
     for (;;) {
-        if (budget > 0 && visits >= budget) {
-            // out of budget: the current node becomes the last frame, and every unfinished node
-            // goes to the next launch (when the pools have room; otherwise keep searching)
-            if (lane == 0) {
-                uint32_t *f = S.stk + (size_t)depth * S.fs;
-#pragma unroll
-                for (int t = 0; t < NW; ++t) f[t] = ext[t];
-                f[NW] = (uint32_t)jn;
-#pragma unroll
-                for (int u = 0; u < WRT; ++u) f[NW + 1 + u] = B[u];
-            }
-            __syncwarp();
-            if (S.split<NW>(depth + 1, R, WR, slices, slice)) return;
-            budget = 0;
-        }
         int j = -1;
 #pragma unroll
         for (int u = 0; u < WRT; ++u) {
@@ -597,7 +452,6 @@ __device__ void dfs_regs(SubtreeWarp &S, int R, const uint32_t (&ext0)[NW], int 
             continue;
         }
         jn = j + 1;
-        ++visits;
         uint32_t C[NW];
         bool nonempty = false;
 #pragma unroll
@@ -625,7 +479,6 @@ __device__ void dfs_regs(SubtreeWarp &S, int R, const uint32_t (&ext0)[NW], int 
         if (!canon) continue;
 
         // canonical child (C, D, j+1): write its intent, count its candidates, descend
-        __syncwarp();
         if (lane == 0) {
 #pragma unroll
             for (int u = 0; u < WRT; ++u) S.dsc[u] = D[u];
@@ -656,29 +509,20 @@ __device__ void dfs_regs(SubtreeWarp &S, int R, const uint32_t (&ext0)[NW], int 
 // Same search with the restricted columns read from shared memory, for any R <= M: lane u of the
 // warp holds word u of the current compact intent.
 template <int NW, bool COUNT>
-__device__ void dfs_smem(SubtreeWarp &S, int R, const uint32_t (&ext0)[NW], int jn, int slices, int slice,
-                         int budget)
+__device__ void dfs_smem(SubtreeWarp &S, int R, int n, int jn, int slices, int slice)
 {
     const unsigned lane = threadIdx.x & 31;
     const uint32_t validR = lt_mask((int)lane, R);
     const int WR = (R + 31) >> 5;
-    uint32_t myB = S.dsc[lane] & validR;
+    uint32_t myB = 0;
     uint32_t ext[NW];
 #pragma unroll
-    for (int t = 0; t < NW; ++t) ext[t] = ext0[t];
-    int depth = 0, visits = 0;
+    for (int t = 0; t < NW; ++t) {
+        const int k = n - 32 * t;
+        ext[t] = k >= 32 ? FULL : (k > 0 ? ((1u << k) - 1u) : 0u);
+    }
+    int depth = 0;
     for (;;) {
-        if (budget > 0 && visits >= budget) {
-            uint32_t *f = S.stk + (size_t)depth * S.fs;
-#pragma unroll
-            for (int t = 0; t < NW; ++t)
-                if ((int)lane == t) f[t] = ext[t];
-            if (lane == 0) f[NW] = (uint32_t)jn;
-            if (lane < (unsigned)S.wm) f[NW + 1 + lane] = myB;
-            __syncwarp();
-            if (S.split<NW>(depth + 1, R, WR, slices, slice)) return;
-            budget = 0;
-        }
         const uint32_t cw = ~myB & validR & ge_mask((int)lane, jn);
         const unsigned bal = __ballot_sync(FULL, cw != 0u);
         if (bal == 0u) {
@@ -697,7 +541,6 @@ __device__ void dfs_smem(SubtreeWarp &S, int R, const uint32_t (&ext0)[NW], int 
         const int j = u0 * 32 + __ffs(cwu) - 1;
         jn = j + 1;
         if (depth == 0 && slices > 1 && j % slices != slice) continue;   // another slice's child
-        ++visits;
 
         uint32_t C[NW];
         bool nonempty = false;
@@ -731,7 +574,6 @@ __device__ void dfs_smem(SubtreeWarp &S, int R, const uint32_t (&ext0)[NW], int 
         }
         if (!canon) continue;
 
-        __syncwarp();
         if (lane <= (unsigned)WR) S.dsc[lane] = lane < (unsigned)WR ? myD : 0u;
         S.emit<COUNT>();
         unsigned c = __popc(myD & ge_mask((int)lane, j + 1) & validR);
@@ -751,18 +593,6 @@ __device__ void dfs_smem(SubtreeWarp &S, int R, const uint32_t (&ext0)[NW], int 
             myB = myD;
         }
     }
-}
-
-template <int NW, bool COUNT>
-__device__ void run_dfs(SubtreeWarp &S, int R, const uint32_t (&ext0)[NW], int jn, int slices, int slice,
-                        int budget)
-{
-    constexpr int RW = reg_words(NW);
-    if (R <= 32) dfs_regs<NW, 1, COUNT>(S, R, ext0, jn, slices, slice, budget);
-    else if (R <= 64) dfs_regs<NW, 2, COUNT>(S, R, ext0, jn, slices, slice, budget);
-    else if (RW >= 4 && R <= 128) dfs_regs<NW, (RW >= 4 ? 4 : 1), COUNT>(S, R, ext0, jn, slices, slice, budget);
-    else if (RW >= 8 && R <= 256) dfs_regs<NW, (RW >= 8 ? 8 : 1), COUNT>(S, R, ext0, jn, slices, slice, budget);
-    else dfs_smem<NW, COUNT>(S, R, ext0, jn, slices, slice, budget);
 }
 
 template <int NW, bool COUNT>
@@ -795,39 +625,14 @@ __global__ void __launch_bounds__(256) subtree_kernel(SubtreeArgs a)
     S.nb = 0;
     S.closures = 0;
     S.ops = 0;
-    S.pout = a.pout;
-    S.pout_cap = a.pout_cap;
-    S.tables = a.tables;
-    S.tables_cap = a.tables_cap;
     const int mp = L.mp, WM = d.wm, PER = 32 * NW;
 
-    const unsigned long long items = a.mode == 0 ? a.q_count * (unsigned long long)a.slices : a.pin_count;
-    unsigned long long *cursor = a.mode == 0 ? &a.ctr->q_head[a.q_index] : &a.ctr->piece_head;
+    const unsigned long long items = a.q_count * (unsigned long long)a.slices;
     for (;;) {
         unsigned long long item = 0;
-        if (lane == 0) item = atomicAdd(cursor, 1ull);
+        if (lane == 0) item = atomicAdd(&a.ctr->q_head[a.q_index], 1ull);
         item = __shfl_sync(FULL, item, 0);
         if (item >= items) break;
-        S.toff = ~0u;
-        __syncwarp();
-
-        if (a.mode == 1) {
-            // ---- a piece: the saved table of its root, then its node
-            const uint32_t *P = a.pin + item * (unsigned long long)piece_words(NW, WM);
-            const uint32_t toff = P[0];
-            const int jn = (int)P[1];
-            const int slices = (int)(P[2] & 0xffffu), slice = (int)(P[2] >> 16);
-            uint32_t ext[NW];
-#pragma unroll
-            for (int t = 0; t < NW; ++t) ext[t] = P[4 + t];
-            S.dsc[lane] = lane < (unsigned)WM ? P[4 + NW + lane] : 0u;
-            if (lane < 2) S.dsc[32 + lane] = 0u;
-            const int R = S.load_table<NW>(toff);
-            run_dfs<NW, COUNT>(S, R, ext, jn, slices, slice, a.budget);
-            __syncwarp();
-            continue;
-        }
-
         // work item = (root, slice): the slice takes the root's children j with j % slices == slice
         const unsigned long long r = item / (unsigned)a.slices;
         const int slice = (int)(item % (unsigned)a.slices);
@@ -835,7 +640,6 @@ __global__ void __launch_bounds__(256) subtree_kernel(SubtreeArgs a)
         // ---- root: object ids, intent, cursor
         const int n = a.q.n[r];
         const int y0 = a.q.y[r];
-        S.n = n;
         uint32_t id[NW];
 #pragma unroll
         for (int t = 0; t < NW; ++t) {
@@ -843,6 +647,7 @@ __global__ void __launch_bounds__(256) subtree_kernel(SubtreeArgs a)
             id[t] = o < n ? a.q.ids[r * PER + o] : 0u;
         }
         const uint32_t myRootB = lane < (unsigned)WM ? a.q.itt[r * WM + lane] : 0u;
+        __syncwarp();
         S.rootB[lane] = myRootB;
 
         // ---- relevant attributes R (held by some but not all objects), compact index order =
@@ -885,8 +690,6 @@ __global__ void __launch_bounds__(256) subtree_kernel(SubtreeArgs a)
             const unsigned tot = __shfl_sync(FULL, incl, 31);
             S.sufB[lane] = tot - incl;
         }
-        S.dsc[lane] = 0u;                  // the root's compact intent is empty
-        if (lane < 2) S.dsc[32 + lane] = 0u;
         __syncwarp();
 
         // ---- candidates of the root: attributes >= y0 outside its intent (counted by slice 0)
@@ -902,13 +705,13 @@ __global__ void __launch_bounds__(256) subtree_kernel(SubtreeArgs a)
         }
 
         // ---- depth-first search of the subtree
-        uint32_t ext[NW];
-#pragma unroll
-        for (int t = 0; t < NW; ++t) {
-            const int k = n - 32 * t;
-            ext[t] = k >= 32 ? FULL : (k > 0 ? ((1u << k) - 1u) : 0u);
-        }
-        run_dfs<NW, COUNT>(S, R, ext, jn, a.slices, slice, a.budget);
+        constexpr int RW = reg_words(NW);
+        const int sl = a.slices;
+        if (R <= 32) dfs_regs<NW, 1, COUNT>(S, R, n, jn, sl, slice);
+        else if (R <= 64) dfs_regs<NW, 2, COUNT>(S, R, n, jn, sl, slice);
+        else if (RW >= 4 && R <= 128) dfs_regs<NW, (RW >= 4 ? 4 : 1), COUNT>(S, R, n, jn, sl, slice);
+        else if (RW >= 8 && R <= 256) dfs_regs<NW, (RW >= 8 ? 8 : 1), COUNT>(S, R, n, jn, sl, slice);
+        else dfs_smem<NW, COUNT>(S, R, n, jn, sl, slice);
         __syncwarp();
     }
     if (S.nb) S.flush();
@@ -1022,9 +825,7 @@ static int launch_subtree_nw(const SubtreeArgs &a, int sm_count, void *stream)
     const unsigned long long want = 16 * resident;
     const unsigned long long qn = std::max<unsigned long long>(1, a.q_count);
     b.slices = (int)std::min<unsigned long long>(MAX_SLICES, std::max<unsigned long long>(1, (want + qn - 1) / qn));
-    if (a.mode != 0) b.slices = 1;   // pieces carry their own slice filter
-    const unsigned long long items = a.mode == 0 ? a.q_count * (unsigned long long)b.slices : a.pin_count;
-    unsigned long long blocks = (items + wpb - 1) / wpb;
+    unsigned long long blocks = (a.q_count * b.slices + wpb - 1) / wpb;
     const unsigned long long cap = (unsigned long long)sm_count * per_sm;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;

@@ -30,9 +30,9 @@ constexpr int STATIC_MAX_WORDS = MAX_ATTRS / 32;       // intent words
 constexpr int MAX_DEVICES = 64;
 
 // Word offsets inside the scratch array.
-constexpr int OFF_CTR = 0;                                             // Counters (144 bytes)
-constexpr int OFF_FLAG = 36;                                           // some row holds every attribute
-constexpr int OFF_ROWS = 40;                                           // rows, padding cleared
+constexpr int OFF_CTR = 0;                                             // Counters (120 bytes)
+constexpr int OFF_FLAG = 30;                                           // some row holds every attribute
+constexpr int OFF_ROWS = 32;                                           // rows, padding cleared
 constexpr int OFF_IDS = OFF_ROWS + STATIC_MAX_OBJECTS * STATIC_MAX_WORDS;
 constexpr int OFF_ITT = OFF_IDS + STATIC_MAX_OBJECTS;                  // root intent = top intent
 constexpr int OFF_Y = OFF_ITT + STATIC_MAX_WORDS;                      // root cursor
@@ -137,10 +137,6 @@ extern "C" fca_status fca_enumerate_small_noalloc(const uint32_t *rows, int64_t 
     a.ctr = reinterpret_cast<Counters *>(s + OFF_CTR);
     a.gstack = nullptr;     // the 1- and 2-word tiers keep their stacks in shared memory
     a.count_work = 0;
-    a.mode = 0;             // no piece or table pool: the single subtree is never split
-    a.pout_cap = 0;
-    a.tables_cap = 0;
-    a.budget = 0;
     if (launch_subtree(a, n <= 32 ? 1 : 2, sms, st) != (int)cudaSuccess) return FCA_ERR_CUDA;
 
     // counters and the full-row flag back to the host (a local variable: no host allocation)

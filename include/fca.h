@@ -54,7 +54,6 @@ typedef struct {
     uint64_t subtree_word_ops; /* counted work of the object-list tier (FCA_OPT_COUNT_WORK) */
     uint64_t expand_bytes;     /* counted bytes moved by the bitmap tier (FCA_OPT_COUNT_WORK) */
     uint64_t retries;          /* bitmap-tier launches rolled back because a work pool was full */
-    uint64_t pieces;           /* unfinished subtree nodes handed from one launch to the next */
     double expand_ms;          /* device time of the bitmap-extent kernel launches */
     double subtree_ms;         /* device time of the object-list kernel launches */
 } fca_stats;

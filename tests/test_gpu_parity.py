@@ -201,25 +201,6 @@ def test_small_pools_roll_back_and_chunk(monkeypatch, limit):
     assert st["retries"] > 0
 
 
-@pytest.mark.parametrize("budget,entries", [("1", None), ("7", None), ("3", "1")])
-def test_subtree_splitting(monkeypatch, budget, entries):
-    # a tiny candidate budget makes every subtree search hand its unfinished nodes to the next
-    # launch (many rounds of pieces); with 1-entry pools most hand-overs find no room and the
-    # searches continue in place
-    monkeypatch.setenv("FCA_SPLIT_BUDGET", budget)
-    if entries:
-        monkeypatch.setenv("FCA_QUEUE_ENTRIES", entries)
-    for (n, m, d, s) in [(250, 300, 0.1, 2), (200, 128, 0.15, 3), (1500, 40, 0.12, 0), (60, 90, 0.3, 7)]:
-        rows = cx.random_context(n, m, d, s)
-        ref = oracle.cbo(rows, n, m, threads=8)
-        got, st = gpu_run(rows, n, m)
-        assert not has_duplicates(got)
-        assert same_set(got, ref["intents"])
-        assert st["closures"] == ref["closures"]
-        if entries is None:
-            assert st["pieces"] > 0
-
-
 @pytest.mark.parametrize("name", ["tiny", "sparse"])
 def test_workload_full_set(name):
     w = cx.WORKLOADS[name]
