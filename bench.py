@@ -148,57 +148,65 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- CPU oracle baseline
 
-def cpu_oracle_rate(rows, w, budget_s: float, threads: int):
-    """Concepts/s of the CPU oracle on a bounded sample of the workload (test-infrastructure code)."""
-    import oracle
-    oracle.cbo(cx.random_context(40, 12, 0.3, 0), 40, 12)   # build/load outside the timing
-    concepts = 0
-    t0 = time.perf_counter()
-    runs = 0
-    limit = 0
-    # full enumerations while they are cheap; a per-thread intent limit otherwise
-    while True:
-        t1 = time.perf_counter()
-        r = oracle.cbo(rows, w.n_objects, w.n_attrs, threads=threads, limit=limit)
-        dt = time.perf_counter() - t1
-        concepts += int(r["intents"].shape[0])
-        runs += 1
-        elapsed = time.perf_counter() - t0
-        if elapsed >= budget_s:
-            break
-        if dt > budget_s / 2 and limit == 0:
-            break
-    sample = (f"{runs} full enumeration(s) of the workload" if limit == 0 else
-              f"{runs} runs limited to {limit} intents per thread")
-    return concepts / elapsed, sample, elapsed
+class OracleSampler:
+    """Concepts/s of the CPU oracle (test infrastructure) on a bounded sample of a workload.
 
+    A sample is either whole enumerations of the workload, repeated until the time budget is
+    used, or - when one enumeration would not fit the budget - one enumeration whose threads stop
+    after a fixed number of intents each (the limit is calibrated once to fit the budget).
+    """
 
-def cpu_oracle_limited_rate(rows, w, budget_s: float, threads: int):
-    """Like cpu_oracle_rate, for workloads too large to enumerate on the host in the budget."""
-    import oracle
-    limit = 20000
-    while True:
-        t1 = time.perf_counter()
-        r = oracle.cbo(rows, w.n_objects, w.n_attrs, threads=threads, limit=limit)
-        dt = time.perf_counter() - t1
-        if dt >= budget_s / 4 or limit >= 1 << 26:
-            return int(r["intents"].shape[0]) / dt, \
-                f"search stopped after {limit} intents per thread ({int(r['intents'].shape[0])} intents)", dt
-        limit *= 4
+    def __init__(self, rows, w, threads: int):
+        import oracle
+        self.oracle = oracle
+        self.rows, self.w, self.threads = rows, w, threads
+        self.limit = None
+        oracle.cbo(cx.random_context(40, 12, 0.3, 0), 40, 12)   # build/load outside any timing
+
+    def _run(self, limit: int):
+        t0 = time.perf_counter()
+        r = self.oracle.cbo(self.rows, self.w.n_objects, self.w.n_attrs, threads=self.threads, limit=limit)
+        return int(r["intents"].shape[0]), time.perf_counter() - t0
+
+    def sample(self, budget_s: float):
+        if self.limit is None:
+            cnt, dt = self._run(0) if self._fits(budget_s) else (None, None)
+            if cnt is not None:
+                self.limit = 0
+            else:
+                lim = 4096
+                while True:
+                    cnt, dt = self._run(lim)
+                    if dt >= budget_s / 4 or lim >= 1 << 28:
+                        break
+                    lim *= 4
+                self.limit = lim
+                return cnt / dt, f"one enumeration stopped after {lim} intents per thread", dt
+        if self.limit:
+            cnt, dt = self._run(self.limit)
+            return cnt / dt, f"one enumeration stopped after {self.limit} intents per thread", dt
+        total, runs, t0 = 0, 0, time.perf_counter()
+        while True:
+            cnt, _ = self._run(0)
+            total += cnt
+            runs += 1
+            el = time.perf_counter() - t0
+            if el >= budget_s:
+                return total / el, f"{runs} whole enumeration(s) of the workload", el
+
+    def _fits(self, budget_s: float) -> bool:
+        digests = os.path.join(ROOT, "tests", "golden", "workload_digests.json")
+        try:
+            d = json.load(open(digests)).get(self.w.name) or {}
+        except (OSError, ValueError):
+            d = {}
+        full_s = d.get("oracle_seconds")
+        return full_s is not None and full_s * d.get("oracle_threads", 1) / max(1, self.threads) < budget_s
 
 
 def cpu_baseline(rows, w, budget_s: float):
     threads = os.cpu_count() or 1
-    digests = os.path.join(ROOT, "tests", "golden", "workload_digests.json")
-    full_s = None
-    if os.path.exists(digests):
-        d = json.load(open(digests)).get(w.name)
-        if d:
-            full_s = d.get("oracle_seconds")
-    if full_s is not None and full_s > budget_s:
-        rate, sample, dt = cpu_oracle_limited_rate(rows, w, budget_s, threads)
-    else:
-        rate, sample, dt = cpu_oracle_rate(rows, w, budget_s, threads)
+    rate, sample, dt = OracleSampler(rows, w, threads).sample(budget_s)
     return {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample,
             "seconds": round(dt, 2)}
 
@@ -366,25 +374,30 @@ def run_ours(args, world, rank, local):
 # ----------------------------------------------------------------------------- reference arm
 
 def run_reference(args):
-    """The CPU oracle as the reference arm: same workload, metric and unit."""
+    """The CPU oracle as the reference arm: same workload, metric and unit, on the host cores.
+
+    Each step is one bounded sample of the workload (the budget split over the steps, so the
+    whole run stays within a few minutes)."""
     w = cx.WORKLOADS[args.workload]
     rows = w.rows()
     threads = os.cpu_count() or 1
-    budget = max(1.0, min(args.cpu_seconds, 20.0))
-    rates = []
-    cb = None
+    sampler = OracleSampler(rows, w, threads)
+    per_step = max(0.5, min(args.cpu_seconds * 6, 120.0) / max(1, args.steps))
     for _ in range(max(args.warmup, 0)):
-        pass
+        sampler.sample(min(per_step, 1.0))
+    rates, samples, seconds = [], [], 0.0
     for _ in range(max(1, args.steps)):
-        cb = cpu_baseline(rows, w, budget / max(1, args.steps) if args.steps > 3 else budget)
-        rates.append(cb["value"])
-        if sum(1 for _ in rates) * budget > 240:
-            break
+        rate, sample, dt = sampler.sample(per_step)
+        rates.append(rate)
+        samples.append(sample)
+        seconds += dt
     value = statistics.median(rates)
-    cb["value"] = value
+    cb = {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": samples[-1],
+          "seconds": round(seconds, 2)}
     return {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1,
-            "steps": len(rates), "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "u64", "data": "synthetic",
+            "steps": len(rates), "warmup": args.warmup, "ms_per_step": seconds * 1e3 / len(rates),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u64",
+            "data": "synthetic",
             "config": {"workload": w.name, "n_objects": w.n_objects, "n_attrs": w.n_attrs, "seed": w.seed},
             "cpu_baseline": cb,
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -399,7 +412,7 @@ def main():
         return
     result = run_ours(args, world, rank, local)
     if rank == 0:
-        if not args.no_cpu_baseline:
+        if not args.no_cpu_baseline and world == 1:
             w = cx.WORKLOADS[args.workload]
             result["cpu_baseline"] = cpu_baseline(w.rows(), w, args.cpu_seconds)
         print(json.dumps(result), flush=True)

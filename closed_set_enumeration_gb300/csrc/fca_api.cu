@@ -42,8 +42,6 @@ struct fca_ctx {
     std::vector<uint64_t> level_count;
     Queue q[NQ]{};
     uint64_t q_count[NQ]{};
-    uint32_t *gstack = nullptr;    // ancestor stacks of the wide object-list kernels
-    size_t gstack_words = 0;
     Counters *ctr = nullptr;        // device
     Counters *ctr_host = nullptr;   // pinned host mirror, current after every readback
     uint32_t *stage = nullptr;      // pinned host staging (root entry)
@@ -51,7 +49,7 @@ struct fca_ctx {
     uint32_t *host_out_dev = nullptr;   // device buffer behind fca_enumerate_host
     uint64_t host_out_rows = 0;
 
-    size_t pool_bytes = 0;          // bytes held by levels, queues and stacks
+    size_t pool_bytes = 0;          // bytes held by levels and queues
     size_t pool_limit = 0;          // growth stops here; levels are then split into chunks
     uint64_t level_bytes = 0, queue_entries = 0;   // initial pool sizes
     int count_work = 0;
@@ -141,9 +139,6 @@ void free_pools(fca_ctx *c)
     c->levels.clear();
     c->level_count.clear();
     for (Queue &Q : c->q) free_queue(Q);
-    cudaFree(c->gstack);
-    c->gstack = nullptr;
-    c->gstack_words = 0;
     c->pool_bytes = 0;
 }
 
@@ -315,13 +310,6 @@ fca_status run_subtree(Run &r, int qi)
     if (c->q_count[qi] == 0) return FCA_OK;
     const int nw = 1 << qi;
     fca_status s;
-    if (nw >= 4 && !c->gstack) {
-        const size_t words = std::max(subtree_gstack_words(c->d, 4, c->sm_count),
-                                      subtree_gstack_words(c->d, 8, c->sm_count));
-        if ((s = alloc_raw(c, (void **)&c->gstack, words * 4, "subtree stacks")) != FCA_OK) return s;
-        c->gstack_words = words;
-        c->pool_bytes += words * 4;
-    }
     SubtreeArgs a{};
     a.d = c->d;
     a.rows = c->rows;
@@ -331,7 +319,6 @@ fca_status run_subtree(Run &r, int qi)
     a.out = r.out;
     a.capacity = r.capacity;
     a.ctr = c->ctr;
-    a.gstack = c->gstack;
     a.count_work = c->count_work;
     size_t pair = 0;
     if ((s = time_begin(r, 1, &pair)) != FCA_OK) return s;
@@ -474,7 +461,7 @@ fca_status enumerate_impl(fca_ctx *c, uint32_t *out, uint64_t capacity, uint64_t
 
     // the root node (G, G', 0)
     if (d.n <= SMALL_MAX) {
-        const int qi = d.n <= 32 ? 0 : d.n <= 64 ? 1 : d.n <= 128 ? 2 : 3;
+        const int qi = d.n <= 32 ? 0 : 1;
         const int per = 32 << qi;
         uint32_t *ids = c->stage;
         for (int i = 0; i < per; ++i) ids[i] = i < d.n ? (uint32_t)i : 0u;

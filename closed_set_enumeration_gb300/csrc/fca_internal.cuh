@@ -12,7 +12,7 @@
 //  * bitmap tier: nodes whose extent has more than SMALL_MAX objects are held
 //    as N-bit bitmaps in level-synchronous frontiers; one warp evaluates one
 //    (parent, j) pair (expand_bitmap_kernel);
-//  * object-list tier: a node with at most 32*NW objects (NW = 1, 2, 4, 8) is
+//  * object-list tier: a node with at most 32*NW objects (NW = 1, 2) is
 //    handed over as a list of object ids, and one warp runs its whole subtree
 //    on the columns restricted to those objects (subtree_kernel<NW>). Every
 //    descendant of such a node has a subset of its objects, so the subtree
@@ -24,8 +24,8 @@
 
 namespace fca {
 
-constexpr int SMALL_MAX = 256;     // largest extent handed to the object-list tier
-constexpr int NQ = 4;              // object-list queues: queue q holds extents of <= 32 << q objects
+constexpr int SMALL_MAX = 64;      // largest extent handed to the object-list tier
+constexpr int NQ = 2;              // object-list queues: queue q holds extents of <= 32 << q objects
 constexpr int MAX_ATTRS = 1024;    // M limit (intent words fit one per lane)
 
 // Overflow bits of Counters::error (a destination was too small; the driver rolls back and retries).
@@ -94,7 +94,6 @@ struct SubtreeArgs {
     uint32_t *out;
     uint64_t capacity;
     Counters *ctr;
-    uint32_t *gstack;       // ancestor stacks in global memory (NW >= 4), per resident warp
     int count_work;         // 1: accumulate Counters::word_ops
 };
 
@@ -106,8 +105,5 @@ int launch_top(const uint32_t *rows, uint32_t *top, uint32_t *flag_full_row, con
 int launch_expand(const ExpandArgs &a, int sm_count, void *stream);
 int launch_subtree(const SubtreeArgs &a, int nw, int sm_count, void *stream);
 size_t expand_smem_per_warp(const Dims &d);
-// Words of global ancestor stack the subtree kernel of width nw needs (0 when it keeps the
-// stack in shared memory), for the grid it launches on this device.
-size_t subtree_gstack_words(const Dims &d, int nw, int sm_count);
 
 }  // namespace fca

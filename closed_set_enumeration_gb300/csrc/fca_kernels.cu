@@ -46,12 +46,12 @@ __device__ __forceinline__ uint32_t ge_mask(int w, int b)
 __device__ __forceinline__ uint32_t lt_mask(int w, int b) { return ~ge_mask(w, b); }
 
 // Largest number of restricted-column words (x32 attributes) a lane keeps in registers.
-__host__ __device__ constexpr int reg_words(int nw) { return nw <= 2 ? 8 : 16 / nw; }
+constexpr int REG_WORDS = 8;
 
 // Entry size in 32-bit words of an object-list queue root holding `cnt` objects (counting only).
 __device__ __forceinline__ unsigned queue_entry_words(unsigned cnt, int wm)
 {
-    const unsigned per = cnt <= 32u ? 32u : cnt <= 64u ? 64u : cnt <= 128u ? 128u : 256u;
+    const unsigned per = cnt <= 32u ? 32u : 64u;
     return per + (unsigned)wm + 2u;
 }
 
@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(256) expand_bitmap_kernel(ExpandArgs a)
         // the child (C, D, j+1): an object-list root, or an entry of the next bitmap level.
         // A destination that is full only counts; the driver rolls the launch back and retries.
         if (cnt <= (unsigned)SMALL_MAX) {
-            const int qi = cnt <= 32u ? 0 : cnt <= 64u ? 1 : cnt <= 128u ? 2 : 3;
+            const int qi = cnt <= 32u ? 0 : 1;
             const Queue &Q = a.q[qi];
             const int per = 32 << qi;
             unsigned long long s = 0;
@@ -306,16 +306,13 @@ __global__ void __launch_bounds__(256) expand_bitmap_kernel(ExpandArgs a)
 // Shared-memory layout of one warp of subtree_kernel<NW> (32-bit words).
 struct SubtreeLayout {
     int mp, wm, fr, fs;
-    bool gstack;
     size_t o_rmap, o_rootb, o_rm, o_rlo, o_sufb, o_dsc, o_stack, o_outbuf, words;
     __host__ __device__ SubtreeLayout(const Dims &d, int nw)
     {
         mp = (d.m + 31) & ~31;
         wm = d.wm;
         fr = (32 * nw < d.m ? 32 * nw : d.m) + 1;     // depth <= |extent| and <= |R|
-        const int rw = reg_words(nw);
-        fs = nw + 1 + (wm > rw ? wm : rw);            // frame: extent mask, cursor, intent
-        gstack = nw >= 4;                             // deep stacks live in global memory
+        fs = nw + 1 + (wm > REG_WORDS ? wm : REG_WORDS);   // frame: extent mask, cursor, intent
         o_rmap = (size_t)nw * mp;
         o_rootb = o_rmap + mp / 2;
         o_rm = o_rootb + 32;
@@ -323,7 +320,7 @@ struct SubtreeLayout {
         o_sufb = o_rlo + 34;
         o_dsc = o_sufb + 32;
         o_stack = o_dsc + 34;
-        o_outbuf = o_stack + (gstack ? 0 : (size_t)fr * fs);
+        o_outbuf = o_stack + (size_t)fr * fs;
         words = o_outbuf + (size_t)OUTBUF * wm;
         words = (words + 3) & ~(size_t)3;
     }
@@ -339,7 +336,7 @@ struct SubtreeWarp {
     uint32_t *rlo;      // first compact index of each full word (wm + 1 entries)
     uint32_t *sufB;     // root-intent attributes in the words above each word
     uint32_t *dsc;      // compact intent of the child being written
-    uint32_t *stk;      // search stack (shared or global memory)
+    uint32_t *stk;      // search stack
     uint32_t *ob;       // output buffer, OUTBUF x wm
     int mp, wm, fs, m;
     uint32_t *out;
@@ -406,7 +403,7 @@ struct SubtreeWarp {
 
 // Depth-first search of one subtree with the restricted columns in registers: lane l holds the
 // columns of compact attributes 32u + l, u < WRT (R <= 32 * WRT). Extent, intent and cursor of
-// the current node are warp-uniform registers; the stack of ancestors is in memory.
+// the current node are warp-uniform registers; the stack of ancestors is in shared memory.
 template <int NW, int WRT, bool COUNT>
 __device__ void dfs_regs(SubtreeWarp &S, int R, int n, int jn, int slices, int slice)
 {
@@ -612,8 +609,7 @@ __global__ void __launch_bounds__(256) subtree_kernel(SubtreeArgs a)
     S.rlo = base + L.o_rlo;
     S.sufB = base + L.o_sufb;
     S.dsc = base + L.o_dsc;
-    S.stk = L.gstack ? a.gstack + ((size_t)blockIdx.x * (blockDim.x >> 5) + wib) * (size_t)L.fr * L.fs
-                     : base + L.o_stack;
+    S.stk = base + L.o_stack;
     S.ob = base + L.o_outbuf;
     S.mp = L.mp;
     S.wm = d.wm;
@@ -705,12 +701,11 @@ __global__ void __launch_bounds__(256) subtree_kernel(SubtreeArgs a)
         }
 
         // ---- depth-first search of the subtree
-        constexpr int RW = reg_words(NW);
         const int sl = a.slices;
         if (R <= 32) dfs_regs<NW, 1, COUNT>(S, R, n, jn, sl, slice);
         else if (R <= 64) dfs_regs<NW, 2, COUNT>(S, R, n, jn, sl, slice);
-        else if (RW >= 4 && R <= 128) dfs_regs<NW, (RW >= 4 ? 4 : 1), COUNT>(S, R, n, jn, sl, slice);
-        else if (RW >= 8 && R <= 256) dfs_regs<NW, (RW >= 8 ? 8 : 1), COUNT>(S, R, n, jn, sl, slice);
+        else if (R <= 128) dfs_regs<NW, 4, COUNT>(S, R, n, jn, sl, slice);
+        else if (R <= 32 * REG_WORDS) dfs_regs<NW, REG_WORDS, COUNT>(S, R, n, jn, sl, slice);
         else dfs_smem<NW, COUNT>(S, R, n, jn, sl, slice);
         __syncwarp();
     }
@@ -833,42 +828,11 @@ static int launch_subtree_nw(const SubtreeArgs &a, int sm_count, void *stream)
     return (int)cudaGetLastError();
 }
 
-template <int NW>
-static size_t gstack_words_nw(const Dims &d, int sm_count)
-{
-    const SubtreeLayout L(d, NW);
-    int wpb = 0, per_sm = 0, wpb2 = 0, per_sm2 = 0;
-    size_t smem = 0;
-    if (subtree_shape<NW, false>(d, &wpb, &smem, &per_sm) != (int)cudaSuccess ||
-        subtree_shape<NW, true>(d, &wpb2, &smem, &per_sm2) != (int)cudaSuccess)
-        return 0;
-    const size_t warps = (size_t)sm_count * (size_t)std::max(per_sm * wpb, per_sm2 * wpb2);
-    return warps * (size_t)L.fr * (size_t)L.fs;
-}
-
-size_t subtree_gstack_words(const Dims &d, int nw, int sm_count)
-{
-    if (nw == 4) return gstack_words_nw<4>(d, sm_count);
-    if (nw == 8) return gstack_words_nw<8>(d, sm_count);
-    return 0;
-}
-
 int launch_subtree(const SubtreeArgs &a, int nw, int sm_count, void *stream)
 {
-    if (a.count_work) {
-        switch (nw) {
-        case 1: return launch_subtree_nw<1, true>(a, sm_count, stream);
-        case 2: return launch_subtree_nw<2, true>(a, sm_count, stream);
-        case 4: return launch_subtree_nw<4, true>(a, sm_count, stream);
-        default: return launch_subtree_nw<8, true>(a, sm_count, stream);
-        }
-    }
-    switch (nw) {
-    case 1: return launch_subtree_nw<1, false>(a, sm_count, stream);
-    case 2: return launch_subtree_nw<2, false>(a, sm_count, stream);
-    case 4: return launch_subtree_nw<4, false>(a, sm_count, stream);
-    default: return launch_subtree_nw<8, false>(a, sm_count, stream);
-    }
+    if (a.count_work)
+        return nw == 1 ? launch_subtree_nw<1, true>(a, sm_count, stream) : launch_subtree_nw<2, true>(a, sm_count, stream);
+    return nw == 1 ? launch_subtree_nw<1, false>(a, sm_count, stream) : launch_subtree_nw<2, false>(a, sm_count, stream);
 }
 
 }  // namespace fca

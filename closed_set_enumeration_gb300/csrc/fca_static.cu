@@ -135,7 +135,6 @@ extern "C" fca_status fca_enumerate_small_noalloc(const uint32_t *rows, int64_t 
     a.out = out;
     a.capacity = capacity;
     a.ctr = reinterpret_cast<Counters *>(s + OFF_CTR);
-    a.gstack = nullptr;     // the 1- and 2-word tiers keep their stacks in shared memory
     a.count_work = 0;
     if (launch_subtree(a, n <= 32 ? 1 : 2, sms, st) != (int)cudaSuccess) return FCA_ERR_CUDA;
 

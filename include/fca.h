@@ -44,7 +44,7 @@ typedef struct {
     uint64_t concepts;         /* intents found (= *out_count) */
     uint64_t closures;         /* candidates (A, B, j) evaluated: j >= cursor, j not in B */
     uint64_t large_parents;    /* search nodes expanded by the bitmap-extent kernel */
-    uint64_t small_roots;      /* subtrees handed to the object-list kernels (extent <= 256) */
+    uint64_t small_roots;      /* subtrees handed to the object-list kernels (extent <= 64) */
     uint64_t launches;         /* kernels launched by the call */
     uint64_t levels;           /* deepest bitmap-frontier level used, plus one */
     uint64_t max_frontier;     /* largest number of bitmap entries held by one level */

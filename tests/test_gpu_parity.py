@@ -69,8 +69,8 @@ def test_random_contexts(n, m, density, seed):
 
 @pytest.mark.parametrize("n,m,density,seed", [(3000, 128, 0.08, 3), (2000, 300, 0.03, 4),
                                               (5000, 1024, 0.004, 5), (800, 1000, 0.02, 6),
-                                              # roots of 100-256 objects: the 4- and 8-word object-list
-                                              # tiers, with registers (R <= 128) and shared memory (R > 128)
+                                              # 100-256 objects with many attributes: bitmap-tier roots,
+                                              # subtrees with many relevant attributes (shared-memory path)
                                               (250, 300, 0.1, 2), (200, 128, 0.15, 3), (256, 200, 0.12, 4),
                                               (120, 300, 0.2, 5), (100, 700, 0.1, 6)])
 def test_larger_random_contexts(n, m, density, seed):
