@@ -566,7 +566,7 @@ fca_status fca_context_create(const uint32_t *rows, int64_t n_objects, int32_t n
     d.wm = (n_attrs + 31) / 32;
     d.wn = (n_objects + 31) / 32;
     d.wnp = (d.wn + 3) & ~(int64_t)3;
-    // the expand kernel stages one extent per warp in shared memory
+    // the expand kernel stages an extent's chunks and one intersection per warp in shared memory
     if (expand_smem_per_warp(d) > 200 * 1024) return fail(FCA_ERR_INVALID);
 
     fca_status s;

@@ -113,20 +113,20 @@ __global__ void top_kernel(const uint32_t *__restrict__ rows, uint32_t *top, uin
 
 // ------------------------------------------------------------------ bitmap tier
 
-// C subset of column K? Early exit at the first block of 64 uint4 that disagrees.
-// `loads` counts the column uint4 read (non-zero uint4 of C in the blocks examined).
-__device__ __forceinline__ bool subset_of_column(const uint4 *C, const uint4 *__restrict__ K, int wq,
-                                                 unsigned lane, unsigned &loads)
+// C subset of column K? C is held as its chunk list (values cv[i] at uint4 index idx[i]); early exit
+// at the first block of 64 chunks that disagrees. `loads` counts the column uint4 read.
+__device__ __forceinline__ bool subset_of_column(const uint4 *cv, const uint32_t *idx, int nnz,
+                                                 const uint4 *__restrict__ K, unsigned lane, unsigned &loads)
 {
-    for (int base = 0; base < wq; base += 64) {
+    for (int base = 0; base < nnz; base += 64) {
         bool bad = false;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-            const int q = base + h * 32 + (int)lane;
-            if (q < wq) {
-                const uint4 c = C[q];
+            const int i = base + h * 32 + (int)lane;
+            if (i < nnz) {
+                const uint4 c = cv[i];
                 if (c.x | c.y | c.z | c.w) {
-                    const uint4 k = __ldg(K + q);
+                    const uint4 k = __ldg(K + idx[i]);
                     ++loads;
                     bad |= ((c.x & ~k.x) | (c.y & ~k.y) | (c.z & ~k.z) | (c.w & ~k.w)) != 0u;
                 }
@@ -137,162 +137,224 @@ __device__ __forceinline__ bool subset_of_column(const uint4 *C, const uint4 *__
     return true;
 }
 
+// Shared memory of expand_bitmap_kernel: the parent's non-zero extent chunks (uint4 index and
+// value, shared by the block) and, per warp, the chunks of its candidate's C and up to SMALL_MAX
+// object ids.
+struct ExpandLayout {
+    size_t o_aidx, o_aval, o_wbase, per_warp, bytes;
+    __host__ __device__ ExpandLayout(const Dims &d, int wpb)
+    {
+        const size_t wq = (size_t)(d.wnp >> 2);
+        o_aval = 0;                                        // wq uint4
+        o_aidx = o_aval + wq * 16;                         // wq uint32
+        o_wbase = (o_aidx + wq * 4 + 15) & ~(size_t)15;
+        per_warp = wq * 16 + SMALL_MAX * 4;                // C chunks, ids
+        bytes = o_wbase + per_warp * wpb + 64;             // + block scratch (parent cursor, counts)
+    }
+};
+
+// Bitmap tier. A work item is (parent, part of the attribute range): the block stages the parent's
+// non-zero extent chunks once, then its warps take the part's candidates j one at a time:
+// C = A & column j over those chunks only (a gather of column j), |C|, the first object ids of C,
+// the AND of their rows (the exact closure for |C| <= SMALL_MAX, else an upper bound whose extra
+// attributes are decided by column subset tests in ascending order, so a violation below j ends
+// the candidate early), the canonical test, and the child.
 template <bool COUNT>
 __global__ void __launch_bounds__(256) expand_bitmap_kernel(ExpandArgs a)
 {
-    extern __shared__ uint4 smem4[];
+    extern __shared__ __align__(16) unsigned char smem[];
     const Dims d = a.d;
     const int wq = (int)(d.wnp >> 2);
     const unsigned lane = threadIdx.x & 31;
     const int wib = threadIdx.x >> 5;
     const int wpb = blockDim.x >> 5;
-    uint4 *Csm = smem4 + (size_t)wib * (wq + SMALL_MAX / 4);
-    uint32_t *ids = reinterpret_cast<uint32_t *>(Csm + wq);
+    const ExpandLayout L(d, wpb);
+    uint4 *aval = reinterpret_cast<uint4 *>(smem + L.o_aval);
+    uint32_t *aidx = reinterpret_cast<uint32_t *>(smem + L.o_aidx);
+    uint4 *cval = reinterpret_cast<uint4 *>(smem + L.o_wbase + L.per_warp * wib);
+    uint32_t *ids = reinterpret_cast<uint32_t *>(cval + wq);
+    int *blk = reinterpret_cast<int *>(smem + L.o_wbase + L.per_warp * wpb);   // [0] nnz, [1..8] warp sums
     const uint4 *cols4 = reinterpret_cast<const uint4 *>(a.cols);
     const uint4 *ext4 = reinterpret_cast<const uint4 *>(a.in.ext);
 
     unsigned long long my_closures = 0, my_bytes = 0;
     unsigned loads = 0;   // uint4 loads of columns by this lane (counting only)
-    const unsigned long long total = a.p_count * (unsigned long long)d.m;
-    const unsigned long long nwarps = (unsigned long long)gridDim.x * wpb;
-    for (unsigned long long idx = (unsigned long long)blockIdx.x * wpb + wib; idx < total;
-         idx += nwarps) {
-        const unsigned long long p = a.p_begin + idx / (unsigned)d.m;
-        const int j = (int)(idx % (unsigned)d.m);
-        if (j < a.in.y[p]) continue;
+    const int parts = a.parts;
+    const int span = (d.m + parts - 1) / parts;
+    const unsigned long long items = a.p_count * (unsigned long long)parts;
+    for (unsigned long long item = blockIdx.x; item < items; item += gridDim.x) {
+        const unsigned long long p = a.p_begin + item / (unsigned)parts;
+        const int part = (int)(item % (unsigned)parts);
+        const int y = a.in.y[p];
+        const int j_lo = max(y, part * span), j_hi = min(d.m, (part + 1) * span);
+        if (j_lo >= j_hi) continue;                       // uniform over the block
         const uint32_t *B = a.in.itt + p * d.wm;
-        if ((B[j >> 5] >> (j & 31)) & 1u) continue;      // saturation: A inside column j
-        ++my_closures;
 
-        // C = A & column j, staged in shared memory; |C| by popcount
+        // ---- stage the non-zero chunks of A in order (block-wide compaction)
         const uint4 *A4 = ext4 + p * wq;
-        const uint4 *J4 = cols4 + (size_t)j * wq;
-        unsigned cnt = 0;
-        for (int q = (int)lane; q < wq; q += 32) {
-            uint4 x = A4[q];
-            if (x.x | x.y | x.z | x.w) {
-                const uint4 c = __ldg(J4 + q);
-                x.x &= c.x; x.y &= c.y; x.z &= c.z; x.w &= c.w;
+        __syncthreads();
+        if (threadIdx.x == 0) blk[0] = 0;
+        __syncthreads();
+        for (int base = 0; base < wq; base += blockDim.x) {
+            const int q = base + (int)threadIdx.x;
+            uint4 x = make_uint4(0u, 0u, 0u, 0u);
+            if (q < wq) x = A4[q];
+            const bool nz = (x.x | x.y | x.z | x.w) != 0u;
+            const unsigned bal = __ballot_sync(FULL, nz);
+            if (lane == 0) blk[1 + wib] = __popc(bal);
+            __syncthreads();
+            int off = blk[0];
+            for (int w = 0; w < wib; ++w) off += blk[1 + w];
+            off += __popc(bal & ((1u << lane) - 1u));
+            if (nz) { aval[off] = x; aidx[off] = (uint32_t)q; }
+            __syncthreads();
+            if (threadIdx.x == 0) {
+                int t = blk[0];
+                for (int w = 0; w < wpb; ++w) t += blk[1 + w];
+                blk[0] = t;
+            }
+            __syncthreads();
+        }
+        const int nnz = blk[0];
+        if (COUNT && threadIdx.x == 0) my_bytes += (unsigned long long)d.wnp * 4;   // the parent extent
+
+        // ---- candidates j of this part, warps in turn
+        for (int j = j_lo + wib; j < j_hi; j += wpb) {
+            if ((B[j >> 5] >> (j & 31)) & 1u) continue;   // saturation: A inside column j
+            ++my_closures;
+
+            // C = A & column j on the chunks of A; |C| by popcount
+            const uint4 *J4 = cols4 + (size_t)j * wq;
+            unsigned cnt = 0;
+            for (int i = (int)lane; i < nnz; i += 32) {
+                uint4 x = aval[i];
+                const uint4 c = __ldg(J4 + aidx[i]);
                 if (COUNT) ++loads;
+                x.x &= c.x; x.y &= c.y; x.z &= c.z; x.w &= c.w;
+                cval[i] = x;
+                cnt += popc4(x);
             }
-            Csm[q] = x;
-            cnt += popc4(x);
-        }
-        cnt = __reduce_add_sync(FULL, cnt);
-        if (COUNT && lane == 0) my_bytes += (unsigned long long)d.wnp * 4;   // the parent extent
-        if (cnt == 0) continue;   // empty extent: its closure is the bottom, added by the host
-        __syncwarp();
+            cnt = __reduce_add_sync(FULL, cnt);
+            if (cnt == 0) continue;   // empty extent: its closure is the bottom, added by the host
+            __syncwarp();
 
-        // object ids of C in ascending order: all of them when |C| <= SMALL_MAX, else the first 32
-        const unsigned need = cnt <= (unsigned)SMALL_MAX ? cnt : 32u;
-        unsigned got = 0;
-        for (int base = 0; base < wq && got < need; base += 32) {
-            const int q = base + (int)lane;
-            const uint4 x = q < wq ? Csm[q] : make_uint4(0u, 0u, 0u, 0u);
-            const unsigned pc = popc4(x);
-            unsigned incl = pc;
+            // object ids of C in ascending order: all of them when |C| <= SMALL_MAX, else the first 32
+            const unsigned need = cnt <= (unsigned)SMALL_MAX ? cnt : 32u;
+            unsigned got = 0;
+            for (int base = 0; base < nnz && got < need; base += 32) {
+                const int i = base + (int)lane;
+                const uint4 x = i < nnz ? cval[i] : make_uint4(0u, 0u, 0u, 0u);
+                const unsigned pc = popc4(x);
+                unsigned incl = pc;
 #pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const unsigned t = __shfl_up_sync(FULL, incl, off);
-                if (lane >= (unsigned)off) incl += t;
+                for (int off = 1; off < 32; off <<= 1) {
+                    const unsigned t = __shfl_up_sync(FULL, incl, off);
+                    if (lane >= (unsigned)off) incl += t;
+                }
+                unsigned pos = got + incl - pc;
+                const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+                const uint32_t q = i < nnz ? aidx[i] : 0u;
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    uint32_t bits = w4[t];
+                    while (bits && pos < need) {
+                        const int b = __ffs(bits) - 1;
+                        bits &= bits - 1u;
+                        ids[pos++] = (uint32_t)((4 * q + t) * 32 + b);
+                    }
+                }
+                got += __shfl_sync(FULL, incl, 31);
             }
-            unsigned pos = got + incl - pc;
-            const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                uint32_t bits = w4[t];
-                while (bits && pos < need) {
-                    const int b = __ffs(bits) - 1;
-                    bits &= bits - 1u;
-                    ids[pos++] = (uint32_t)((4 * q + t) * 32 + b);
+            __syncwarp();
+
+            // U = AND of the rows of those objects (exact D when |C| <= SMALL_MAX): each lane ANDs
+            // the rows of every 32nd object, then one reduction per word; lane w keeps word w.
+            uint32_t U = 0;
+            for (int w = 0; w < d.wm; ++w) {
+                uint32_t acc = FULL;
+                for (unsigned i = lane; i < need; i += 32) acc &= __ldg(a.rows + (size_t)ids[i] * d.wm + w);
+                acc = __reduce_and_sync(FULL, acc);
+                if ((int)lane == w) U = acc;
+            }
+            if (COUNT && lane == 0) my_bytes += (unsigned long long)need * d.wm * 4;   // rows read
+            const uint32_t Bw = lane < (unsigned)d.wm ? B[lane] : 0u;
+            const int ju = j >> 5;
+            const uint32_t jbit = 1u << (j & 31);
+            const uint32_t pm = lt_mask((int)lane, j);   // attributes below j
+            uint32_t Dw;
+            bool canon = true;
+            if (cnt <= (unsigned)SMALL_MAX) {
+                Dw = U;
+                canon = !__any_sync(FULL, (U & ~Bw & pm) != 0u);
+            } else {
+                // attributes that may still join: in U, not in B, not j; tested in ascending order
+                uint32_t X = U & ~Bw;
+                if ((int)lane == ju) X &= ~jbit;
+                Dw = Bw | ((int)lane == ju ? jbit : 0u);
+                for (;;) {
+                    const unsigned bal = __ballot_sync(FULL, X != 0u);
+                    if (!bal) break;
+                    const int u = __ffs(bal) - 1;
+                    const uint32_t xw = __shfl_sync(FULL, X, u);
+                    const int b = __ffs(xw) - 1;
+                    const int k = u * 32 + b;
+                    if ((int)lane == u) X &= ~(1u << b);
+                    if (subset_of_column(cval, aidx, nnz, cols4 + (size_t)k * wq, lane, loads)) {
+                        if (k < j) { canon = false; break; }
+                        if ((int)lane == u) Dw |= 1u << b;
+                    }
                 }
             }
-            got += __shfl_sync(FULL, incl, 31);
-        }
-        __syncwarp();
+            if (!canon) continue;
 
-        // U = AND of the rows of those objects (exact D when |C| <= SMALL_MAX): each lane ANDs the
-        // rows of every 32nd object, then one reduction per word; lane w keeps word w.
-        uint32_t U = 0;
-        for (int w = 0; w < d.wm; ++w) {
-            uint32_t acc = FULL;
-            for (unsigned i = lane; i < need; i += 32) acc &= __ldg(a.rows + (size_t)ids[i] * d.wm + w);
-            acc = __reduce_and_sync(FULL, acc);
-            if ((int)lane == w) U = acc;
-        }
-        if (COUNT && lane == 0) my_bytes += (unsigned long long)need * d.wm * 4;   // rows read
-        const uint32_t Bw = lane < (unsigned)d.wm ? B[lane] : 0u;
-        const int ju = j >> 5;
-        const uint32_t jbit = 1u << (j & 31);
-        const uint32_t pm = lt_mask((int)lane, j);   // attributes below j
-        uint32_t Dw;
-        bool canon = true;
-        if (cnt <= (unsigned)SMALL_MAX) {
-            Dw = U;
-            canon = !__any_sync(FULL, (U & ~Bw & pm) != 0u);
-        } else {
-            // attributes that may still join: in U, not in B, not j. Test each against the columns,
-            // in ascending order, so a violation below j ends the candidate early.
-            uint32_t X = U & ~Bw;
-            if ((int)lane == ju) X &= ~jbit;
-            Dw = Bw | ((int)lane == ju ? jbit : 0u);
-            for (;;) {
-                const unsigned bal = __ballot_sync(FULL, X != 0u);
-                if (!bal) break;
-                const int u = __ffs(bal) - 1;
-                const uint32_t xw = __shfl_sync(FULL, X, u);
-                const int b = __ffs(xw) - 1;
-                const int k = u * 32 + b;
-                if ((int)lane == u) X &= ~(1u << b);
-                if (subset_of_column(Csm, cols4 + (size_t)k * wq, wq, lane, loads)) {
-                    if (k < j) { canon = false; break; }
-                    if ((int)lane == u) Dw |= 1u << b;
+            if (COUNT && lane == 0) {   // the intent row and the child entry written
+                my_bytes += (unsigned long long)d.wm * 4;
+                my_bytes += cnt <= (unsigned)SMALL_MAX ? 4ull * queue_entry_words(cnt, d.wm)
+                                                       : (unsigned long long)(4 * d.wnp + 4 * d.wm + 4);
+            }
+            // emit the intent
+            unsigned long long slot = 0;
+            if (lane == 0) slot = atomicAdd(&a.ctr->out_count, 1ull);
+            slot = __shfl_sync(FULL, slot, 0);
+            if (slot < a.capacity && lane < (unsigned)d.wm) a.out[slot * d.wm + lane] = Dw;
+
+            // the child (C, D, j+1): an object-list root, or an entry of the next bitmap level.
+            // A destination that is full only counts; the driver rolls the launch back and retries.
+            if (cnt <= (unsigned)SMALL_MAX) {
+                const int qi = cnt <= 32u ? 0 : 1;
+                const Queue &Q = a.q[qi];
+                const int per = 32 << qi;
+                unsigned long long s = 0;
+                if (lane == 0) s = atomicAdd(&a.ctr->q_count[qi], 1ull);
+                s = __shfl_sync(FULL, s, 0);
+                if (s >= Q.cap) {
+                    if (lane == 0) atomicOr(&a.ctr->error, ERR_QUEUE0 << qi);
+                    continue;
                 }
+                for (int i = (int)lane; i < per; i += 32) Q.ids[s * per + i] = i < (int)cnt ? ids[i] : 0u;
+                if (lane < (unsigned)d.wm) Q.itt[s * d.wm + lane] = Dw;
+                if (lane == 0) { Q.y[s] = j + 1; Q.n[s] = (int)cnt; }
+            } else {
+                unsigned long long s = 0;
+                if (lane == 0) s = atomicAdd(&a.ctr->next_count, 1ull);
+                s = __shfl_sync(FULL, s, 0);
+                if (s >= a.next.cap) {
+                    if (lane == 0) atomicOr(&a.ctr->error, ERR_NEXT);
+                    continue;
+                }
+                // dense bitmap of C: zeros, then the non-zero chunks
+                uint4 *dst = reinterpret_cast<uint4 *>(a.next.ext) + s * wq;
+                for (int q = (int)lane; q < wq; q += 32) dst[q] = make_uint4(0u, 0u, 0u, 0u);
+                __syncwarp();
+                for (int i = (int)lane; i < nnz; i += 32) {
+                    const uint4 x = cval[i];
+                    if (x.x | x.y | x.z | x.w) dst[aidx[i]] = x;
+                }
+                if (lane < (unsigned)d.wm) a.next.itt[s * d.wm + lane] = Dw;
+                if (lane == 0) a.next.y[s] = j + 1;
             }
+            __syncwarp();
         }
-        if (!canon) continue;
-
-        if (COUNT && lane == 0) {   // the intent row and the child entry written
-            my_bytes += (unsigned long long)d.wm * 4;
-            my_bytes += cnt <= (unsigned)SMALL_MAX ? 4ull * queue_entry_words(cnt, d.wm)
-                                                   : (unsigned long long)(4 * d.wnp + 4 * d.wm + 4);
-        }
-        // emit the intent
-        unsigned long long slot = 0;
-        if (lane == 0) slot = atomicAdd(&a.ctr->out_count, 1ull);
-        slot = __shfl_sync(FULL, slot, 0);
-        if (slot < a.capacity && lane < (unsigned)d.wm) a.out[slot * d.wm + lane] = Dw;
-
-        // the child (C, D, j+1): an object-list root, or an entry of the next bitmap level.
-        // A destination that is full only counts; the driver rolls the launch back and retries.
-        if (cnt <= (unsigned)SMALL_MAX) {
-            const int qi = cnt <= 32u ? 0 : 1;
-            const Queue &Q = a.q[qi];
-            const int per = 32 << qi;
-            unsigned long long s = 0;
-            if (lane == 0) s = atomicAdd(&a.ctr->q_count[qi], 1ull);
-            s = __shfl_sync(FULL, s, 0);
-            if (s >= Q.cap) {
-                if (lane == 0) atomicOr(&a.ctr->error, ERR_QUEUE0 << qi);
-                continue;
-            }
-            for (int i = (int)lane; i < per; i += 32) Q.ids[s * per + i] = i < (int)cnt ? ids[i] : 0u;
-            if (lane < (unsigned)d.wm) Q.itt[s * d.wm + lane] = Dw;
-            if (lane == 0) { Q.y[s] = j + 1; Q.n[s] = (int)cnt; }
-        } else {
-            unsigned long long s = 0;
-            if (lane == 0) s = atomicAdd(&a.ctr->next_count, 1ull);
-            s = __shfl_sync(FULL, s, 0);
-            if (s >= a.next.cap) {
-                if (lane == 0) atomicOr(&a.ctr->error, ERR_NEXT);
-                continue;
-            }
-            uint4 *dst = reinterpret_cast<uint4 *>(a.next.ext) + s * wq;
-            for (int q = (int)lane; q < wq; q += 32) dst[q] = Csm[q];
-            if (lane < (unsigned)d.wm) a.next.itt[s * d.wm + lane] = Dw;
-            if (lane == 0) a.next.y[s] = j + 1;
-        }
-        __syncwarp();
     }
     if (COUNT) {
         const unsigned tl = __reduce_add_sync(FULL, loads);
@@ -312,7 +374,8 @@ struct SubtreeLayout {
         mp = (d.m + 31) & ~31;
         wm = d.wm;
         fr = (32 * nw < d.m ? 32 * nw : d.m) + 1;     // depth <= |extent| and <= |R|
-        fs = nw + 1 + (wm > REG_WORDS ? wm : REG_WORDS);   // frame: extent mask, cursor, intent
+        // frame: extent mask, then cursor + intent (shared-memory search) or candidates + intent
+        fs = nw + (1 + wm > 2 * REG_WORDS ? 1 + wm : 2 * REG_WORDS);
         o_rmap = (size_t)nw * mp;
         o_rootb = o_rmap + mp / 2;
         o_rm = o_rootb + 32;
@@ -402,8 +465,11 @@ struct SubtreeWarp {
 };
 
 // Depth-first search of one subtree with the restricted columns in registers: lane l holds the
-// columns of compact attributes 32u + l, u < WRT (R <= 32 * WRT). Extent, intent and cursor of
-// the current node are warp-uniform registers; the stack of ancestors is in shared memory.
+// columns of compact attributes 32u + l, u < WRT (R <= 32 * WRT). Extent, intent and remaining
+// candidates of the current node are warp-uniform registers; the stack of ancestors is in shared
+// memory. A node's candidates are filtered once, when the node is entered, to the attributes
+// whose column meets its extent (the others give an empty extent, whose closure is the bottom
+// concept the host adds), so the loop only visits candidates with a non-empty C.
 template <int NW, int WRT, bool COUNT>
 __device__ void dfs_regs(SubtreeWarp &S, int R, int n, int jn, int slices, int slice)
 {
@@ -415,52 +481,55 @@ __device__ void dfs_regs(SubtreeWarp &S, int R, int n, int jn, int slices, int s
 #pragma unroll
         for (int t = 0; t < NW; ++t) col[u][t] = k < R ? S.cR[t * S.mp + k] : 0u;
     }
-    uint32_t valid[WRT], B[WRT];
-#pragma unroll
-    for (int u = 0; u < WRT; ++u) { valid[u] = lt_mask(u, R); B[u] = 0u; }
+    uint32_t B[WRT], cand[WRT];
     uint32_t ext[NW];
 #pragma unroll
     for (int t = 0; t < NW; ++t) {
         const int k = n - 32 * t;
         ext[t] = k >= 32 ? FULL : (k > 0 ? ((1u << k) - 1u) : 0u);
     }
+    // the root: empty compact intent; candidates from jn on, in this slice, meeting the extent
+#pragma unroll
+    for (int u = 0; u < WRT; ++u) {
+        bool meets = false;
+#pragma unroll
+        for (int t = 0; t < NW; ++t) meets = meets || (ext[t] & col[u][t]) != 0u;
+        const int k = 32 * u + (int)lane;
+        const bool mine = slices <= 1 || k % slices == slice;
+        cand[u] = __ballot_sync(FULL, meets && mine) & ge_mask(u, jn);
+        B[u] = 0u;
+        if (COUNT) S.ops += 2ull * NW * (unsigned)max(0, min(32, R - 32 * u));
+    }
     int depth = 0;
     for (;;) {
         int j = -1;
 #pragma unroll
-        for (int u = 0; u < WRT; ++u) {
-            const uint32_t cw = ~B[u] & valid[u] & ge_mask(u, jn);
-            if (j < 0 && cw) j = 32 * u + __ffs(cw) - 1;
-        }
-        if (j >= 0 && depth == 0 && slices > 1 && j % slices != slice) {   // another slice's child
-            jn = j + 1;
-            continue;
-        }
+        for (int u = 0; u < WRT; ++u)
+            if (j < 0 && cand[u]) j = 32 * u + __ffs(cand[u]) - 1;
         if (j < 0) {
             if (depth == 0) break;
             --depth;
             const uint32_t *f = S.stk + (size_t)depth * S.fs;
 #pragma unroll
             for (int t = 0; t < NW; ++t) ext[t] = f[t];
-            jn = (int)f[NW];
 #pragma unroll
-            for (int u = 0; u < WRT; ++u) B[u] = f[NW + 1 + u];
+            for (int u = 0; u < WRT; ++u) {
+                cand[u] = f[NW + u];
+                B[u] = f[NW + WRT + u];
+            }
             __syncwarp();
             continue;
         }
-        jn = j + 1;
-        uint32_t C[NW];
-        bool nonempty = false;
+        const int ju = j >> 5;
 #pragma unroll
-        for (int t = 0; t < NW; ++t) {
-            C[t] = ext[t] & S.cR[t * S.mp + j];
-            nonempty |= C[t] != 0u;
-        }
+        for (int u = 0; u < WRT; ++u)
+            if (u == ju) cand[u] &= cand[u] - 1u;     // j is the lowest remaining candidate
+        uint32_t C[NW];
+#pragma unroll
+        for (int t = 0; t < NW; ++t) C[t] = ext[t] & S.cR[t * S.mp + j];
         if (COUNT) S.ops += NW;            // the extent intersection
-        if (!nonempty) continue;           // empty extent: bottom concept, added by the host
 
         // closure over the relevant attributes, canonical prefix first
-        const int ju = j >> 5;
         const uint32_t jm = (1u << (j & 31)) - 1u;
         uint32_t D[WRT];
         bool canon = true;
@@ -490,16 +559,25 @@ __device__ void dfs_regs(SubtreeWarp &S, int R, int n, int jn, int slices, int s
             uint32_t *f = S.stk + (size_t)depth * S.fs;
 #pragma unroll
             for (int t = 0; t < NW; ++t) f[t] = ext[t];
-            f[NW] = (uint32_t)jn;
 #pragma unroll
-            for (int u = 0; u < WRT; ++u) f[NW + 1 + u] = B[u];
+            for (int u = 0; u < WRT; ++u) {
+                f[NW + u] = cand[u];
+                f[NW + WRT + u] = B[u];
+            }
         }
         __syncwarp();
         ++depth;
 #pragma unroll
         for (int t = 0; t < NW; ++t) ext[t] = C[t];
 #pragma unroll
-        for (int u = 0; u < WRT; ++u) B[u] = D[u];
+        for (int u = 0; u < WRT; ++u) {
+            bool meets = false;
+#pragma unroll
+            for (int t = 0; t < NW; ++t) meets = meets || (C[t] & col[u][t]) != 0u;
+            B[u] = D[u];
+            cand[u] = __ballot_sync(FULL, meets) & ~D[u] & ge_mask(u, j + 1);
+            if (COUNT) S.ops += 2ull * NW * (unsigned)max(0, min(32, R - 32 * u));
+        }
     }
 }
 
@@ -593,7 +671,7 @@ __device__ void dfs_smem(SubtreeWarp &S, int R, int n, int jn, int slices, int s
 }
 
 template <int NW, bool COUNT>
-__global__ void __launch_bounds__(256) subtree_kernel(SubtreeArgs a)
+__global__ void __launch_bounds__(256, 3) subtree_kernel(SubtreeArgs a)
 {
     extern __shared__ uint32_t smw[];
     const Dims d = a.d;
@@ -743,10 +821,7 @@ int launch_top(const uint32_t *rows, uint32_t *top, uint32_t *flag, const Dims &
     return (int)cudaGetLastError();
 }
 
-size_t expand_smem_per_warp(const Dims &d)
-{
-    return ((size_t)(d.wnp / 4) + SMALL_MAX / 4) * sizeof(uint4);
-}
+size_t expand_smem_per_warp(const Dims &d) { return ExpandLayout(d, 1).bytes; }
 
 static int warps_for(size_t per_warp)
 {
@@ -759,9 +834,9 @@ static int warps_for(size_t per_warp)
 template <bool COUNT>
 static int launch_expand_t(const ExpandArgs &a, int sm_count, void *stream)
 {
-    const size_t pw = expand_smem_per_warp(a.d);
-    const int wpb = warps_for(pw);
-    const size_t smem = pw * wpb;
+    int wpb = WARPS_PER_BLOCK;
+    while (wpb > 1 && ExpandLayout(a.d, wpb).bytes > 200 * 1024) --wpb;
+    const size_t smem = ExpandLayout(a.d, wpb).bytes;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(expand_bitmap_kernel<COUNT>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -770,12 +845,17 @@ static int launch_expand_t(const ExpandArgs &a, int sm_count, void *stream)
     int per_sm = 0;
     cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, expand_bitmap_kernel<COUNT>, wpb * 32, smem);
     if (per_sm < 1) per_sm = 1;
-    const unsigned long long total = a.p_count * (unsigned long long)a.d.m;
-    unsigned long long blocks = (total + wpb - 1) / wpb;
-    const unsigned long long cap = (unsigned long long)sm_count * per_sm * 4;
-    if (blocks > cap) blocks = cap;
+    // split each parent's attribute range into parts when there are too few parents to fill the GPU
+    // (at least one candidate per warp in every part)
+    ExpandArgs b = a;
+    const unsigned long long resident = (unsigned long long)sm_count * per_sm;
+    const unsigned long long pc = std::max<unsigned long long>(1, a.p_count);
+    const int max_parts = std::max(1, a.d.m / wpb);
+    b.parts = (int)std::min<unsigned long long>(max_parts, std::max<unsigned long long>(1, (2 * resident + pc - 1) / pc));
+    const unsigned long long items = a.p_count * (unsigned long long)b.parts;
+    unsigned long long blocks = std::min<unsigned long long>(items, resident * 2);
     if (blocks < 1) blocks = 1;
-    expand_bitmap_kernel<COUNT><<<(unsigned)blocks, wpb * 32, smem, (cudaStream_t)stream>>>(a);
+    expand_bitmap_kernel<COUNT><<<(unsigned)blocks, wpb * 32, smem, (cudaStream_t)stream>>>(b);
     return (int)cudaGetLastError();
 }
 

@@ -77,7 +77,9 @@ typedef enum {
  *   rows       N x W_M uint32 words, row-major, LSB-first. Host or device
  *              pointer (copied with cudaMemcpyDefault, read once, not kept).
  *              Padding bits past M are ignored.
- *   n_objects  N >= 1.
+ *   n_objects  1 <= N <= about 720 000 (a thread block of the bitmap-extent
+ *              kernel stages one extent and one intersection in shared memory;
+ *              larger N returns FCA_ERR_INVALID).
  *   n_attrs    1 <= M <= 1024.
  *   out_ctx    receives the new context (NULL on failure).
  * Runs on the legacy default stream and returns after it completes.
