@@ -7,6 +7,8 @@ it; it is the independent definition the library is checked against.
 Contents:
   * :func:`cbo`             plain recursive Close-by-One in C (``cbo.c``),
                             single-thread or split over top-level attributes;
+  * :func:`cbo_digest`      the same search keeping only an order-independent
+                            digest of the intents (for sets too large to hold);
   * :func:`brute_force`     closes every attribute subset (M <= 20) and dedupes;
   * :func:`brute_force_by_objects` derives every object subset (N <= 16);
   * :func:`derive_extent`,
@@ -15,5 +17,5 @@ Contents:
 
 Every pin that ties these to the pages' definitions lives in ``tests/``.
 """
-from .cbo_binding import build_oracle, cbo, oracle_library_path  # noqa: F401
+from .cbo_binding import build_oracle, cbo, cbo_digest, oracle_library_path  # noqa: F401
 from .brute import brute_force, brute_force_by_objects, derive_extent, derive_intent  # noqa: F401

@@ -65,7 +65,32 @@ typedef struct {
     int want_extents;
     int oom;
     uint64_t limit;      /* stop descending once this many intents are output (0 = no limit) */
+    int digest_only;     /* keep no intents; accumulate an order-independent digest instead */
+    int32_t words32;     /* 32-bit words of an intent (for the digest) */
+    uint64_t hsum, hxor; /* sum and xor of the per-intent hashes */
 } osink;
+
+/* splitmix64 finaliser (Steele, Lea and Flood, "Fast splittable pseudorandom number generators"). */
+static uint64_t mix64(uint64_t z)
+{
+    z ^= z >> 30;
+    z *= 0xBF58476D1CE4E5B9ull;
+    z ^= z >> 27;
+    z *= 0x94D049BB133111EBull;
+    z ^= z >> 31;
+    return z;
+}
+
+/* Hash of one intent: its 32-bit words folded in order, then the word count. */
+static uint64_t intent_hash(const uint64_t *intent, int32_t words32)
+{
+    uint64_t h = 0x9E3779B97F4A7C15ull;
+    for (int32_t i = 0; i < words32; ++i) {
+        uint64_t w = (intent[i >> 1] >> (32 * (i & 1))) & 0xFFFFFFFFull;
+        h = mix64(h ^ w);
+    }
+    return mix64(h + (uint64_t)words32);
+}
 
 static int bit_of(const uint64_t *set, int64_t i) { return (int)((set[i >> 6] >> (i & 63)) & 1u); }
 
@@ -99,6 +124,14 @@ static void sink_emit(const octx *c, osink *s, const uint64_t *extent, const uin
                       int depth)
 {
     if (s->oom) return;
+    if (s->digest_only) {
+        uint64_t h = intent_hash(intent, s->words32);
+        s->hsum += h;
+        s->hxor ^= h;
+        s->count += 1;
+        s->depth_counts[depth] += 1;
+        return;
+    }
     if (s->count == s->cap) {
         uint64_t ncap = s->cap ? s->cap * 2 : 1024;
         uint64_t *ni = (uint64_t *)realloc(s->intents, ncap * (size_t)c->wm * sizeof(uint64_t));
@@ -242,6 +275,11 @@ int oracle_cbo_limited(const uint32_t *rows32, int64_t n, int32_t m, int threads
                        uint64_t limit, uint32_t **out_intents, uint32_t **out_extents,
                        uint64_t *out_count, uint64_t *out_closures, uint64_t *depth_counts);
 
+static int run_cbo(const uint32_t *rows32, int64_t n, int32_t m, int threads, int want_extents,
+                   uint64_t limit, int digest_only, uint32_t **out_intents, uint32_t **out_extents,
+                   uint64_t *out_count, uint64_t *out_closures, uint64_t *depth_counts,
+                   uint64_t *hsum, uint64_t *hxor);
+
 int oracle_cbo(const uint32_t *rows32, int64_t n, int32_t m, int threads, int want_extents,
                uint32_t **out_intents, uint32_t **out_extents, uint64_t *out_count,
                uint64_t *out_closures, uint64_t *depth_counts)
@@ -254,7 +292,31 @@ int oracle_cbo_limited(const uint32_t *rows32, int64_t n, int32_t m, int threads
                        uint64_t limit, uint32_t **out_intents, uint32_t **out_extents,
                        uint64_t *out_count, uint64_t *out_closures, uint64_t *depth_counts)
 {
-    if (!rows32 || n < 1 || m < 1 || !out_intents || !out_count || !out_closures || !depth_counts)
+    return run_cbo(rows32, n, m, threads, want_extents, limit, 0, out_intents, out_extents, out_count,
+                   out_closures, depth_counts, NULL, NULL);
+}
+
+/*
+ * Same search, keeping no intents: returns their number, the closures, the depth
+ * counts and an order-independent digest of the intent set (the sum and the xor,
+ * modulo 2^64, of one 64-bit hash per intent), for workloads whose intents do not
+ * fit in host memory.
+ */
+int oracle_cbo_digest(const uint32_t *rows32, int64_t n, int32_t m, int threads, uint64_t *out_count,
+                      uint64_t *out_closures, uint64_t *depth_counts, uint64_t *hsum, uint64_t *hxor)
+{
+    if (!hsum || !hxor) return -1;
+    return run_cbo(rows32, n, m, threads, 0, 0, 1, NULL, NULL, out_count, out_closures, depth_counts,
+                   hsum, hxor);
+}
+
+static int run_cbo(const uint32_t *rows32, int64_t n, int32_t m, int threads, int want_extents,
+                   uint64_t limit, int digest_only, uint32_t **out_intents, uint32_t **out_extents,
+                   uint64_t *out_count, uint64_t *out_closures, uint64_t *depth_counts,
+                   uint64_t *hsum, uint64_t *hxor)
+{
+    if (!rows32 || n < 1 || m < 1 || (!digest_only && !out_intents) || !out_count || !out_closures ||
+        !depth_counts)
         return -1;
     octx c;
     if (build_ctx(&c, rows32, n, m) != 0) { free_ctx(&c); return -1; }
@@ -272,6 +334,8 @@ int oracle_cbo_limited(const uint32_t *rows32, int64_t n, int32_t m, int threads
     for (int t = 0; t < nthr; ++t) {
         wks[t].sink.want_extents = want_extents;
         wks[t].sink.limit = limit;
+        wks[t].sink.digest_only = digest_only;
+        wks[t].sink.words32 = (m + 31) / 32;
         wks[t].sink.depth_counts = (uint64_t *)calloc((size_t)(m + 2), sizeof(uint64_t));
     }
     int rc = 0;
@@ -298,15 +362,30 @@ int oracle_cbo_limited(const uint32_t *rows32, int64_t n, int32_t m, int threads
         free(tid);
     }
 
-    uint64_t total = 0, closures = 0;
+    uint64_t total = 0, closures = 0, hs = 0, hx = 0;
     for (int t = 0; t < nthr; ++t) {
         if (wks[t].fail || wks[t].sink.oom) rc = -1;
         total += wks[t].sink.count;
+        hs += wks[t].sink.hsum;
+        hx ^= wks[t].sink.hxor;
         closures += wks[t].sink.closures;
         for (int d = 0; d < m + 2; ++d) depth_counts[d] += wks[t].sink.depth_counts[d];
     }
     int64_t w32m = (m + 31) / 32, w32n = (n + 31) / 32;
     uint32_t *oi = NULL, *oe = NULL;
+    if (digest_only) {
+        for (int t = 0; t < nthr; ++t) free(wks[t].sink.depth_counts);
+        free(wks);
+        free(top_ext);
+        free(top_int);
+        free_ctx(&c);
+        if (rc != 0) return -1;
+        *out_count = total;
+        *out_closures = closures;
+        *hsum = hs;
+        *hxor = hx;
+        return 0;
+    }
     if (rc == 0) {
         oi = (uint32_t *)malloc((size_t)(total ? total : 1) * (size_t)w32m * sizeof(uint32_t));
         if (want_extents)

@@ -57,6 +57,10 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
         ctypes.c_void_p,
     ]
     lib.oracle_cbo_limited.restype = ctypes.c_int
+    u64p = ctypes.POINTER(ctypes.c_uint64)
+    lib.oracle_cbo_digest.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int,
+                                      u64p, u64p, ctypes.c_void_p, u64p, u64p]
+    lib.oracle_cbo_digest.restype = ctypes.c_int
     lib.oracle_free.argtypes = [ctypes.c_void_p]
     lib.oracle_free.restype = None
     return lib
@@ -105,3 +109,23 @@ def cbo(rows: np.ndarray, n_objects: int, n_attrs: int, threads: int = 1,
             lib.oracle_free(ctypes.cast(p_ext, ctypes.c_void_p))
     return {"intents": intents, "extents": extents, "closures": int(closures.value),
             "depth_counts": depth}
+
+
+def cbo_digest(rows: np.ndarray, n_objects: int, n_attrs: int, threads: int = 1,
+               lib: Optional[ctypes.CDLL] = None) -> dict:
+    """The same search keeping no intents: their number, the closures, the depth counts and an
+    order-independent digest of the intent set (sum and xor mod 2^64 of one hash per intent)."""
+    lib = lib or load()
+    rows = np.ascontiguousarray(rows, dtype=np.uint32)
+    if rows.shape != (n_objects, (n_attrs + 31) // 32):
+        raise ValueError("rows shape does not match (N, ceil(M/32))")
+    count, closures = ctypes.c_uint64(0), ctypes.c_uint64(0)
+    hsum, hxor = ctypes.c_uint64(0), ctypes.c_uint64(0)
+    depth = np.zeros(n_attrs + 2, dtype=np.uint64)
+    rc = lib.oracle_cbo_digest(rows.ctypes.data, n_objects, n_attrs, int(threads), ctypes.byref(count),
+                               ctypes.byref(closures), depth.ctypes.data, ctypes.byref(hsum),
+                               ctypes.byref(hxor))
+    if rc != 0:
+        raise RuntimeError("oracle_cbo_digest failed")
+    return {"count": int(count.value), "closures": int(closures.value), "depth_counts": depth,
+            "hsum": int(hsum.value), "hxor": int(hxor.value)}

@@ -61,3 +61,35 @@ def load_golden(name: str) -> Tuple[int, int, np.ndarray, np.ndarray]:
 
 def golden_names() -> List[str]:
     return sorted(f for f in os.listdir(GOLDEN) if f.endswith(".txt"))
+
+
+_M1, _M2 = np.uint64(0xBF58476D1CE4E5B9), np.uint64(0x94D049BB133111EB)
+
+
+def _mix64(z: np.ndarray) -> np.ndarray:
+    z = z ^ (z >> np.uint64(30))
+    z = z * _M1
+    z = z ^ (z >> np.uint64(27))
+    z = z * _M2
+    return z ^ (z >> np.uint64(31))
+
+
+def multiset_digest(intents: np.ndarray, chunk: int = 1 << 22):
+    """Order-independent digest of a set of intents: (sum, xor) mod 2^64 of one hash per row.
+
+    The hash folds the row's 32-bit words in order through the splitmix64 finaliser and then the
+    word count (the same definition as the oracle's digest mode).
+    """
+    rows = np.ascontiguousarray(intents, dtype=np.uint32)
+    k, w = rows.shape
+    hsum, hxor = np.uint64(0), np.uint64(0)
+    with np.errstate(over="ignore"):
+        for lo in range(0, k, chunk):
+            part = rows[lo:lo + chunk].astype(np.uint64)
+            h = np.full(part.shape[0], 0x9E3779B97F4A7C15, dtype=np.uint64)
+            for i in range(w):
+                h = _mix64(h ^ part[:, i])
+            h = _mix64(h + np.uint64(w))
+            hsum = np.uint64(hsum + np.sum(h, dtype=np.uint64))
+            hxor = np.uint64(hxor ^ np.bitwise_xor.reduce(h))
+    return int(hsum), int(hxor)

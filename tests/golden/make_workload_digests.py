@@ -2,11 +2,13 @@
 
 For each named synthetic workload it records the number of intents, the
 number of closures (candidates evaluated by Close-by-One), the concepts per
-search depth and a SHA-256 digest of the intents sorted as big integers
-(last 32-bit word most significant), so that full-size GPU runs can be
-checked bit-exactly without re-running the oracle.
+search depth, an order-independent digest of the intent set (sum and xor mod
+2^64 of one hash per intent, computed by the oracle's digest mode) and, when
+the intents fit in host memory, a SHA-256 digest of the intents sorted as big
+integers (last 32-bit word most significant), so that full-size GPU runs can
+be checked without re-running the oracle.
 
-usage: python tests/golden/make_workload_digests.py [workload ...] [--threads T]
+usage: python tests/golden/make_workload_digests.py [workload ...] [--threads T] [--digest-only]
 """
 import argparse
 import hashlib
@@ -37,23 +39,32 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("names", nargs="*", default=list(cx.WORKLOADS))
     ap.add_argument("--threads", type=int, default=os.cpu_count() or 1)
+    ap.add_argument("--digest-only", action="store_true", help="skip the sorted SHA-256 (large sets)")
     args = ap.parse_args()
     data = json.load(open(OUT)) if os.path.exists(OUT) else {}
     for name in args.names:
         w = cx.WORKLOADS[name]
         rows = w.rows()
         t0 = time.time()
-        r = oracle.cbo(rows, w.n_objects, w.n_attrs, threads=args.threads)
+        g = oracle.cbo_digest(rows, w.n_objects, w.n_attrs, threads=args.threads)
         dt = time.time() - t0
-        depth = [int(x) for x in r["depth_counts"]]
+        depth = [int(x) for x in g["depth_counts"]]
         while depth and depth[-1] == 0:
             depth.pop()
-        data[name] = {
+        entry = (json.load(open(OUT)) if os.path.exists(OUT) else {}).get(name, {})
+        entry.update({
             "n_objects": w.n_objects, "n_attrs": w.n_attrs, "seed": w.seed,
-            "concepts": int(r["intents"].shape[0]), "closures": int(r["closures"]),
-            "depth_counts": depth, "sha256_sorted_intents": digest(r["intents"]),
+            "concepts": g["count"], "closures": g["closures"], "depth_counts": depth,
+            "multiset_hsum": f"{g['hsum']:016x}", "multiset_hxor": f"{g['hxor']:016x}",
             "oracle_seconds": round(dt, 1), "oracle_threads": args.threads,
-        }
+        })
+        if not args.digest_only:
+            r = oracle.cbo(rows, w.n_objects, w.n_attrs, threads=args.threads)
+            assert r["intents"].shape[0] == g["count"] and r["closures"] == g["closures"]
+            entry["sha256_sorted_intents"] = digest(r["intents"])
+        # re-read before writing: several runs (one per workload) may update the file
+        data = json.load(open(OUT)) if os.path.exists(OUT) else {}
+        data[name] = entry
         print(name, data[name]["concepts"], data[name]["closures"], f"{dt:.1f}s", flush=True)
         with open(OUT, "w") as f:
             json.dump(data, f, indent=1, sort_keys=True)

@@ -229,6 +229,24 @@ def test_thread_modes_agree(name, threads):
     assert np.array_equal(a["depth_counts"], b["depth_counts"])
 
 
+@pytest.mark.parametrize("n,m,density,seed,threads", [(300, 33, 0.2, 1, 1), (500, 64, 0.15, 2, 4),
+                                                      (200, 100, 0.1, 3, 3)])
+def test_digest_mode_matches_full_output(n, m, density, seed, threads):
+    from tests._util import multiset_digest
+    rows = cx.random_context(n, m, density, seed)
+    full = oracle.cbo(rows, n, m, threads=threads)
+    dig = oracle.cbo_digest(rows, n, m, threads=threads)
+    assert dig["count"] == full["intents"].shape[0]
+    assert dig["closures"] == full["closures"]
+    assert np.array_equal(dig["depth_counts"], full["depth_counts"])
+    assert (dig["hsum"], dig["hxor"]) == multiset_digest(full["intents"])
+    # the digest tells sets apart: drop one intent, or change one bit of one
+    assert multiset_digest(full["intents"][1:]) != (dig["hsum"], dig["hxor"])
+    changed = full["intents"].copy()
+    changed[3, 0] ^= np.uint32(1)
+    assert multiset_digest(changed) != (dig["hsum"], dig["hxor"])
+
+
 def test_extents_are_derivations():
     rows = cx.random_context(70, 40, 0.3, 9)
     r = oracle.cbo(rows, 70, 40, want_extents=True)
