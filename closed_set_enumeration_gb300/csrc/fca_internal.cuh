@@ -77,6 +77,7 @@ struct ExpandArgs {
     Level in;               // parents
     uint64_t p_begin, p_count;
     int parts;              // work items per parent: parts of the attribute range (set by the launcher)
+    int restrict_max;       // largest extent rebuilt as restricted columns (set by the launcher)
     Level next;             // children with more than SMALL_MAX objects
     Queue q[NQ];            // children with <= 32 << q objects
     uint32_t *out;          // capacity x wm

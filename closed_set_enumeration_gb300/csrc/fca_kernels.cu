@@ -137,28 +137,153 @@ __device__ __forceinline__ bool subset_of_column(const uint4 *cv, const uint32_t
     return true;
 }
 
-// Shared memory of expand_bitmap_kernel: the parent's non-zero extent chunks (uint4 index and
-// value, shared by the block) and, per warp, the chunks of its candidate's C and up to SMALL_MAX
-// object ids.
+// Largest parent extent (objects) whose columns the block rebuilds restricted to its objects,
+// limited by shared memory: M restricted columns of TR/32 words plus the object list.
+constexpr int RESTRICT_CAP = 4096;
+constexpr int RPL = RESTRICT_CAP / 1024;   // restricted-column words per lane
+
+// Shared memory of expand_bitmap_kernel. Both paths first stage the parent's non-zero extent
+// chunks (uint4 index and value). The gather path then keeps, per warp, its candidate's C chunks
+// and up to SMALL_MAX object ids; the restricted path keeps the parent's object list, its columns
+// restricted to those objects (M x TR/32 words) and per-warp object ids.
 struct ExpandLayout {
-    size_t o_aidx, o_aval, o_wbase, per_warp, bytes;
-    __host__ __device__ ExpandLayout(const Dims &d, int wpb)
+    size_t o_aidx, o_aval, o_wbase, per_warp, o_oid, o_colr, o_rids, o_blk, bytes;
+    __host__ __device__ ExpandLayout(const Dims &d, int wpb, int tr)
     {
         const size_t wq = (size_t)(d.wnp >> 2);
         o_aval = 0;                                        // wq uint4
         o_aidx = o_aval + wq * 16;                         // wq uint32
         o_wbase = (o_aidx + wq * 4 + 15) & ~(size_t)15;
         per_warp = wq * 16 + SMALL_MAX * 4;                // C chunks, ids
-        bytes = o_wbase + per_warp * wpb + 64;             // + block scratch (parent cursor, counts)
+        const size_t gather_end = o_wbase + per_warp * wpb;
+        o_oid = o_wbase;                                   // tr uint32
+        o_colr = o_oid + (size_t)tr * 4;                   // m x tr/32 uint32
+        o_rids = o_colr + (size_t)d.m * (size_t)(tr / 32) * 4;
+        const size_t restrict_end = o_rids + (size_t)wpb * SMALL_MAX * 4;
+        o_blk = ((gather_end > restrict_end ? gather_end : restrict_end) + 15) & ~(size_t)15;
+        bytes = o_blk + 32 * 4;                            // block scratch: counts and sums
     }
 };
 
-// Bitmap tier. A work item is (parent, part of the attribute range): the block stages the parent's
-// non-zero extent chunks once, then its warps take the part's candidates j one at a time:
-// C = A & column j over those chunks only (a gather of column j), |C|, the first object ids of C,
-// the AND of their rows (the exact closure for |C| <= SMALL_MAX, else an upper bound whose extra
-// attributes are decided by column subset tests in ascending order, so a violation below j ends
-// the candidate early), the canonical test, and the child.
+// Block-wide exclusive prefix sum of one value per thread (all threads call it); returns the
+// thread's offset and writes the block total to *total. `scratch` holds 2 x 32 ints.
+__device__ __forceinline__ int block_exclusive_sum(int v, int *scratch, int *total)
+{
+    const unsigned lane = threadIdx.x & 31;
+    const int wib = threadIdx.x >> 5, wpb = blockDim.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int t = __shfl_up_sync(FULL, incl, off);
+        if (lane >= (unsigned)off) incl += t;
+    }
+    if (lane == 31) scratch[wib] = incl;
+    __syncthreads();
+    int before = 0, all = 0;
+    for (int w = 0; w < wpb; ++w) {
+        const int s = scratch[w];
+        if (w < wib) before += s;
+        all += s;
+    }
+    __syncthreads();
+    *total = all;
+    return before + incl - v;
+}
+
+// The rest of a candidate once |C| and the first object ids of C are known: the closure (AND of
+// the rows of `need` objects: exact for |C| <= SMALL_MAX, else an upper bound whose extra
+// attributes are decided by `subset(k)` in ascending order, so a violation below j ends the
+// candidate early), the canonical test, the intent and the child. `write_ext(dst)` writes C as a
+// dense bitmap for a child of the next level.
+template <bool COUNT, class Subset, class WriteExt>
+__device__ __forceinline__ void finish_candidate(const ExpandArgs &a, const Dims &d, const uint32_t *B, int j,
+                                                 unsigned cnt, const uint32_t *ids, unsigned need, Subset &&subset,
+                                                 WriteExt &&write_ext, unsigned long long &my_bytes)
+{
+    const unsigned lane = threadIdx.x & 31;
+    uint32_t U = 0;
+    for (int w = 0; w < d.wm; ++w) {
+        uint32_t acc = FULL;
+        for (unsigned i = lane; i < need; i += 32) acc &= __ldg(a.rows + (size_t)ids[i] * d.wm + w);
+        acc = __reduce_and_sync(FULL, acc);
+        if ((int)lane == w) U = acc;
+    }
+    if (COUNT && lane == 0) my_bytes += (unsigned long long)need * d.wm * 4;   // rows read
+    const uint32_t Bw = lane < (unsigned)d.wm ? B[lane] : 0u;
+    const int ju = j >> 5;
+    const uint32_t jbit = 1u << (j & 31);
+    const uint32_t pm = lt_mask((int)lane, j);   // attributes below j
+    uint32_t Dw;
+    if (cnt <= (unsigned)SMALL_MAX) {
+        Dw = U;
+        if (__any_sync(FULL, (U & ~Bw & pm) != 0u)) return;
+    } else {
+        // attributes that may still join: in U, not in B, not j; tested in ascending order
+        uint32_t X = U & ~Bw;
+        if ((int)lane == ju) X &= ~jbit;
+        Dw = Bw | ((int)lane == ju ? jbit : 0u);
+        for (;;) {
+            const unsigned bal = __ballot_sync(FULL, X != 0u);
+            if (!bal) break;
+            const int u = __ffs(bal) - 1;
+            const uint32_t xw = __shfl_sync(FULL, X, u);
+            const int b = __ffs(xw) - 1;
+            const int k = u * 32 + b;
+            if ((int)lane == u) X &= ~(1u << b);
+            if (subset(k)) {
+                if (k < j) return;                      // not canonical
+                if ((int)lane == u) Dw |= 1u << b;
+            }
+        }
+    }
+
+    if (COUNT && lane == 0) {   // the intent row and the child entry written
+        my_bytes += (unsigned long long)d.wm * 4;
+        my_bytes += cnt <= (unsigned)SMALL_MAX ? 4ull * queue_entry_words(cnt, d.wm)
+                                               : (unsigned long long)(4 * d.wnp + 4 * d.wm + 4);
+    }
+    // emit the intent
+    unsigned long long slot = 0;
+    if (lane == 0) slot = atomicAdd(&a.ctr->out_count, 1ull);
+    slot = __shfl_sync(FULL, slot, 0);
+    if (slot < a.capacity && lane < (unsigned)d.wm) a.out[slot * d.wm + lane] = Dw;
+
+    // the child (C, D, j+1): an object-list root, or an entry of the next bitmap level.
+    // A destination that is full only counts; the driver rolls the launch back and retries.
+    if (cnt <= (unsigned)SMALL_MAX) {
+        const int qi = cnt <= 32u ? 0 : 1;
+        const Queue &Q = a.q[qi];
+        const int per = 32 << qi;
+        unsigned long long s = 0;
+        if (lane == 0) s = atomicAdd(&a.ctr->q_count[qi], 1ull);
+        s = __shfl_sync(FULL, s, 0);
+        if (s >= Q.cap) {
+            if (lane == 0) atomicOr(&a.ctr->error, ERR_QUEUE0 << qi);
+            return;
+        }
+        for (int i = (int)lane; i < per; i += 32) Q.ids[s * per + i] = i < (int)cnt ? ids[i] : 0u;
+        if (lane < (unsigned)d.wm) Q.itt[s * d.wm + lane] = Dw;
+        if (lane == 0) { Q.y[s] = j + 1; Q.n[s] = (int)cnt; }
+    } else {
+        unsigned long long s = 0;
+        if (lane == 0) s = atomicAdd(&a.ctr->next_count, 1ull);
+        s = __shfl_sync(FULL, s, 0);
+        if (s >= a.next.cap) {
+            if (lane == 0) atomicOr(&a.ctr->error, ERR_NEXT);
+            return;
+        }
+        write_ext(a.next.ext + s * (size_t)d.wnp);
+        if (lane < (unsigned)d.wm) a.next.itt[s * d.wm + lane] = Dw;
+        if (lane == 0) a.next.y[s] = j + 1;
+    }
+}
+
+// Bitmap tier. A work item is (parent, part of the attribute range). The block stages the parent's
+// non-zero extent chunks once. Extents of at most `a.restrict_max` objects are then turned into an
+// object list, and the rows of those objects are transposed into columns restricted to them (one
+// ballot per attribute and 32 objects); each candidate's C is read from those columns without any
+// global column access. Larger extents keep the chunk list: each warp gathers column j on the
+// parent's non-zero chunks. Either way the warps of the block take the part's candidates j in turn.
 template <bool COUNT>
 __global__ void __launch_bounds__(256) expand_bitmap_kernel(ExpandArgs a)
 {
@@ -168,12 +293,16 @@ __global__ void __launch_bounds__(256) expand_bitmap_kernel(ExpandArgs a)
     const unsigned lane = threadIdx.x & 31;
     const int wib = threadIdx.x >> 5;
     const int wpb = blockDim.x >> 5;
-    const ExpandLayout L(d, wpb);
+    const int tr = a.restrict_max;
+    const ExpandLayout L(d, wpb, tr);
     uint4 *aval = reinterpret_cast<uint4 *>(smem + L.o_aval);
     uint32_t *aidx = reinterpret_cast<uint32_t *>(smem + L.o_aidx);
     uint4 *cval = reinterpret_cast<uint4 *>(smem + L.o_wbase + L.per_warp * wib);
-    uint32_t *ids = reinterpret_cast<uint32_t *>(cval + wq);
-    int *blk = reinterpret_cast<int *>(smem + L.o_wbase + L.per_warp * wpb);   // [0] nnz, [1..8] warp sums
+    uint32_t *gids = reinterpret_cast<uint32_t *>(cval + wq);
+    uint32_t *oid = reinterpret_cast<uint32_t *>(smem + L.o_oid);
+    uint32_t *colr = reinterpret_cast<uint32_t *>(smem + L.o_colr);
+    uint32_t *rids = reinterpret_cast<uint32_t *>(smem + L.o_rids) + (size_t)wib * SMALL_MAX;
+    int *blk = reinterpret_cast<int *>(smem + L.o_blk);   // [0..31] scan scratch
     const uint4 *cols4 = reinterpret_cast<const uint4 *>(a.cols);
     const uint4 *ext4 = reinterpret_cast<const uint4 *>(a.in.ext);
 
@@ -190,35 +319,137 @@ __global__ void __launch_bounds__(256) expand_bitmap_kernel(ExpandArgs a)
         if (j_lo >= j_hi) continue;                       // uniform over the block
         const uint32_t *B = a.in.itt + p * d.wm;
 
-        // ---- stage the non-zero chunks of A in order (block-wide compaction)
+        // ---- stage the non-zero chunks of A in order (block-wide compaction), and |A|
         const uint4 *A4 = ext4 + p * wq;
         __syncthreads();
-        if (threadIdx.x == 0) blk[0] = 0;
-        __syncthreads();
+        int nnz = 0, na = 0;
         for (int base = 0; base < wq; base += blockDim.x) {
             const int q = base + (int)threadIdx.x;
             uint4 x = make_uint4(0u, 0u, 0u, 0u);
             if (q < wq) x = A4[q];
             const bool nz = (x.x | x.y | x.z | x.w) != 0u;
-            const unsigned bal = __ballot_sync(FULL, nz);
-            if (lane == 0) blk[1 + wib] = __popc(bal);
-            __syncthreads();
-            int off = blk[0];
-            for (int w = 0; w < wib; ++w) off += blk[1 + w];
-            off += __popc(bal & ((1u << lane) - 1u));
-            if (nz) { aval[off] = x; aidx[off] = (uint32_t)q; }
-            __syncthreads();
-            if (threadIdx.x == 0) {
-                int t = blk[0];
-                for (int w = 0; w < wpb; ++w) t += blk[1 + w];
-                blk[0] = t;
-            }
-            __syncthreads();
+            int round_nnz = 0, round_na = 0;
+            const int off = block_exclusive_sum(nz ? 1 : 0, blk, &round_nnz);
+            (void)block_exclusive_sum((int)popc4(x), blk, &round_na);
+            if (nz) { aval[nnz + off] = x; aidx[nnz + off] = (uint32_t)q; }
+            nnz += round_nnz;
+            na += round_na;
         }
-        const int nnz = blk[0];
+        __syncthreads();
         if (COUNT && threadIdx.x == 0) my_bytes += (unsigned long long)d.wnp * 4;   // the parent extent
 
-        // ---- candidates j of this part, warps in turn
+        if (na <= tr) {
+            // ---- restricted path: object list, then the columns restricted to these objects
+            int base_id = 0;
+            for (int base = 0; base < nnz; base += blockDim.x) {
+                const int i = base + (int)threadIdx.x;
+                const uint4 x = i < nnz ? aval[i] : make_uint4(0u, 0u, 0u, 0u);
+                int round = 0;
+                int pos = base_id + block_exclusive_sum((int)popc4(x), blk, &round);
+                if (i < nnz) {
+                    const uint32_t q = aidx[i];
+                    const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        uint32_t bits = w4[t];
+                        while (bits) {
+                            const int b = __ffs(bits) - 1;
+                            bits &= bits - 1u;
+                            oid[pos++] = (4 * q + t) * 32 + b;
+                        }
+                    }
+                }
+                base_id += round;
+            }
+            __syncthreads();
+            const int G = (na + 31) >> 5;                  // restricted-column words
+            for (int unit = wib; unit < G * d.wm; unit += wpb) {
+                const int g = unit / d.wm, w = unit % d.wm;
+                const int pidx = 32 * g + (int)lane;
+                const uint32_t v = pidx < na ? __ldg(a.rows + (size_t)oid[pidx] * d.wm + w) : 0u;
+                uint32_t mine = 0;
+#pragma unroll
+                for (int b = 0; b < 32; ++b) {
+                    const uint32_t bal = __ballot_sync(FULL, (v >> b) & 1u);
+                    if (lane == (unsigned)b) mine = bal;
+                }
+                const int k = 32 * w + (int)lane;
+                if (k < d.m) colr[(size_t)k * G + g] = mine;
+            }
+            __syncthreads();
+            if (COUNT && threadIdx.x == 0) my_bytes += (unsigned long long)na * d.wm * 4;   // rows of A
+
+            for (int j = j_lo + wib; j < j_hi; j += wpb) {
+                if ((B[j >> 5] >> (j & 31)) & 1u) continue;   // saturation: A inside column j
+                ++my_closures;
+                uint32_t c[RPL];
+                unsigned cnt = 0;
+#pragma unroll
+                for (int r = 0; r < RPL; ++r) {
+                    const int g = 32 * r + (int)lane;
+                    c[r] = g < G ? colr[(size_t)j * G + g] : 0u;
+                    cnt += __popc(c[r]);
+                }
+                cnt = __reduce_add_sync(FULL, cnt);
+                if (cnt == 0) continue;   // empty extent: its closure is the bottom, added by the host
+
+                // object ids of C in ascending order: all of them when |C| <= SMALL_MAX, else the first 32
+                const unsigned need = cnt <= (unsigned)SMALL_MAX ? cnt : 32u;
+                unsigned got = 0;
+#pragma unroll
+                for (int r = 0; r < RPL; ++r) {
+                    if (got >= need) break;
+                    const unsigned pc = __popc(c[r]);
+                    unsigned incl = pc;
+#pragma unroll
+                    for (int off = 1; off < 32; off <<= 1) {
+                        const unsigned t = __shfl_up_sync(FULL, incl, off);
+                        if (lane >= (unsigned)off) incl += t;
+                    }
+                    unsigned pos = got + incl - pc;
+                    uint32_t bits = c[r];
+                    const int g = 32 * r + (int)lane;
+                    while (bits && pos < need) {
+                        const int b = __ffs(bits) - 1;
+                        bits &= bits - 1u;
+                        rids[pos++] = oid[32 * g + b];
+                    }
+                    got += __shfl_sync(FULL, incl, 31);
+                }
+                __syncwarp();
+                finish_candidate<COUNT>(
+                    a, d, B, j, cnt, rids, need,
+                    [&](int k) {
+                        bool bad = false;
+#pragma unroll
+                        for (int r = 0; r < RPL; ++r) {
+                            const int g = 32 * r + (int)lane;
+                            if (g < G) bad |= (c[r] & ~colr[(size_t)k * G + g]) != 0u;
+                        }
+                        return !__any_sync(FULL, bad);
+                    },
+                    [&](uint32_t *dst) {
+                        for (int q = (int)lane; q < (int)d.wnp; q += 32) dst[q] = 0u;
+                        __syncwarp();
+#pragma unroll
+                        for (int r = 0; r < RPL; ++r) {
+                            uint32_t bits = c[r];
+                            const int g = 32 * r + (int)lane;
+                            while (bits) {
+                                const int b = __ffs(bits) - 1;
+                                bits &= bits - 1u;
+                                const uint32_t o = oid[32 * g + b];
+                                atomicOr(dst + (o >> 5), 1u << (o & 31));
+                            }
+                        }
+                    },
+                    my_bytes);
+                __syncwarp();
+            }
+            continue;
+        }
+
+        // ---- gather path: candidates j of this part, warps in turn
         for (int j = j_lo + wib; j < j_hi; j += wpb) {
             if ((B[j >> 5] >> (j & 31)) & 1u) continue;   // saturation: A inside column j
             ++my_closures;
@@ -228,9 +459,9 @@ __global__ void __launch_bounds__(256) expand_bitmap_kernel(ExpandArgs a)
             unsigned cnt = 0;
             for (int i = (int)lane; i < nnz; i += 32) {
                 uint4 x = aval[i];
-                const uint4 c = __ldg(J4 + aidx[i]);
+                const uint4 cc = __ldg(J4 + aidx[i]);
                 if (COUNT) ++loads;
-                x.x &= c.x; x.y &= c.y; x.z &= c.z; x.w &= c.w;
+                x.x &= cc.x; x.y &= cc.y; x.z &= cc.z; x.w &= cc.w;
                 cval[i] = x;
                 cnt += popc4(x);
             }
@@ -260,99 +491,25 @@ __global__ void __launch_bounds__(256) expand_bitmap_kernel(ExpandArgs a)
                     while (bits && pos < need) {
                         const int b = __ffs(bits) - 1;
                         bits &= bits - 1u;
-                        ids[pos++] = (uint32_t)((4 * q + t) * 32 + b);
+                        gids[pos++] = (uint32_t)((4 * q + t) * 32 + b);
                     }
                 }
                 got += __shfl_sync(FULL, incl, 31);
             }
             __syncwarp();
-
-            // U = AND of the rows of those objects (exact D when |C| <= SMALL_MAX): each lane ANDs
-            // the rows of every 32nd object, then one reduction per word; lane w keeps word w.
-            uint32_t U = 0;
-            for (int w = 0; w < d.wm; ++w) {
-                uint32_t acc = FULL;
-                for (unsigned i = lane; i < need; i += 32) acc &= __ldg(a.rows + (size_t)ids[i] * d.wm + w);
-                acc = __reduce_and_sync(FULL, acc);
-                if ((int)lane == w) U = acc;
-            }
-            if (COUNT && lane == 0) my_bytes += (unsigned long long)need * d.wm * 4;   // rows read
-            const uint32_t Bw = lane < (unsigned)d.wm ? B[lane] : 0u;
-            const int ju = j >> 5;
-            const uint32_t jbit = 1u << (j & 31);
-            const uint32_t pm = lt_mask((int)lane, j);   // attributes below j
-            uint32_t Dw;
-            bool canon = true;
-            if (cnt <= (unsigned)SMALL_MAX) {
-                Dw = U;
-                canon = !__any_sync(FULL, (U & ~Bw & pm) != 0u);
-            } else {
-                // attributes that may still join: in U, not in B, not j; tested in ascending order
-                uint32_t X = U & ~Bw;
-                if ((int)lane == ju) X &= ~jbit;
-                Dw = Bw | ((int)lane == ju ? jbit : 0u);
-                for (;;) {
-                    const unsigned bal = __ballot_sync(FULL, X != 0u);
-                    if (!bal) break;
-                    const int u = __ffs(bal) - 1;
-                    const uint32_t xw = __shfl_sync(FULL, X, u);
-                    const int b = __ffs(xw) - 1;
-                    const int k = u * 32 + b;
-                    if ((int)lane == u) X &= ~(1u << b);
-                    if (subset_of_column(cval, aidx, nnz, cols4 + (size_t)k * wq, lane, loads)) {
-                        if (k < j) { canon = false; break; }
-                        if ((int)lane == u) Dw |= 1u << b;
+            finish_candidate<COUNT>(
+                a, d, B, j, cnt, gids, need,
+                [&](int k) { return subset_of_column(cval, aidx, nnz, cols4 + (size_t)k * wq, lane, loads); },
+                [&](uint32_t *dst) {
+                    uint4 *dst4 = reinterpret_cast<uint4 *>(dst);
+                    for (int q = (int)lane; q < wq; q += 32) dst4[q] = make_uint4(0u, 0u, 0u, 0u);
+                    __syncwarp();
+                    for (int i = (int)lane; i < nnz; i += 32) {
+                        const uint4 x = cval[i];
+                        if (x.x | x.y | x.z | x.w) dst4[aidx[i]] = x;
                     }
-                }
-            }
-            if (!canon) continue;
-
-            if (COUNT && lane == 0) {   // the intent row and the child entry written
-                my_bytes += (unsigned long long)d.wm * 4;
-                my_bytes += cnt <= (unsigned)SMALL_MAX ? 4ull * queue_entry_words(cnt, d.wm)
-                                                       : (unsigned long long)(4 * d.wnp + 4 * d.wm + 4);
-            }
-            // emit the intent
-            unsigned long long slot = 0;
-            if (lane == 0) slot = atomicAdd(&a.ctr->out_count, 1ull);
-            slot = __shfl_sync(FULL, slot, 0);
-            if (slot < a.capacity && lane < (unsigned)d.wm) a.out[slot * d.wm + lane] = Dw;
-
-            // the child (C, D, j+1): an object-list root, or an entry of the next bitmap level.
-            // A destination that is full only counts; the driver rolls the launch back and retries.
-            if (cnt <= (unsigned)SMALL_MAX) {
-                const int qi = cnt <= 32u ? 0 : 1;
-                const Queue &Q = a.q[qi];
-                const int per = 32 << qi;
-                unsigned long long s = 0;
-                if (lane == 0) s = atomicAdd(&a.ctr->q_count[qi], 1ull);
-                s = __shfl_sync(FULL, s, 0);
-                if (s >= Q.cap) {
-                    if (lane == 0) atomicOr(&a.ctr->error, ERR_QUEUE0 << qi);
-                    continue;
-                }
-                for (int i = (int)lane; i < per; i += 32) Q.ids[s * per + i] = i < (int)cnt ? ids[i] : 0u;
-                if (lane < (unsigned)d.wm) Q.itt[s * d.wm + lane] = Dw;
-                if (lane == 0) { Q.y[s] = j + 1; Q.n[s] = (int)cnt; }
-            } else {
-                unsigned long long s = 0;
-                if (lane == 0) s = atomicAdd(&a.ctr->next_count, 1ull);
-                s = __shfl_sync(FULL, s, 0);
-                if (s >= a.next.cap) {
-                    if (lane == 0) atomicOr(&a.ctr->error, ERR_NEXT);
-                    continue;
-                }
-                // dense bitmap of C: zeros, then the non-zero chunks
-                uint4 *dst = reinterpret_cast<uint4 *>(a.next.ext) + s * wq;
-                for (int q = (int)lane; q < wq; q += 32) dst[q] = make_uint4(0u, 0u, 0u, 0u);
-                __syncwarp();
-                for (int i = (int)lane; i < nnz; i += 32) {
-                    const uint4 x = cval[i];
-                    if (x.x | x.y | x.z | x.w) dst[aidx[i]] = x;
-                }
-                if (lane < (unsigned)d.wm) a.next.itt[s * d.wm + lane] = Dw;
-                if (lane == 0) a.next.y[s] = j + 1;
-            }
+                },
+                my_bytes);
             __syncwarp();
         }
     }
@@ -821,7 +978,7 @@ int launch_top(const uint32_t *rows, uint32_t *top, uint32_t *flag, const Dims &
     return (int)cudaGetLastError();
 }
 
-size_t expand_smem_per_warp(const Dims &d) { return ExpandLayout(d, 1).bytes; }
+size_t expand_smem_per_warp(const Dims &d) { return ExpandLayout(d, 1, 0).bytes; }
 
 static int warps_for(size_t per_warp)
 {
@@ -835,8 +992,13 @@ template <bool COUNT>
 static int launch_expand_t(const ExpandArgs &a, int sm_count, void *stream)
 {
     int wpb = WARPS_PER_BLOCK;
-    while (wpb > 1 && ExpandLayout(a.d, wpb).bytes > 200 * 1024) --wpb;
-    const size_t smem = ExpandLayout(a.d, wpb).bytes;
+    while (wpb > 1 && ExpandLayout(a.d, wpb, 0).bytes > 200 * 1024) --wpb;
+    // the largest restricted extent whose columns fit next to the gather path's shared memory
+    // (at least 112 KiB, two blocks per SM)
+    const size_t budget = std::max<size_t>(ExpandLayout(a.d, wpb, 0).bytes, 112 * 1024);
+    int tr = RESTRICT_CAP;
+    while (tr > 0 && ExpandLayout(a.d, wpb, tr).bytes > budget) tr -= 32;
+    const size_t smem = ExpandLayout(a.d, wpb, tr).bytes;
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(expand_bitmap_kernel<COUNT>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -848,6 +1010,7 @@ static int launch_expand_t(const ExpandArgs &a, int sm_count, void *stream)
     // split each parent's attribute range into parts when there are too few parents to fill the GPU
     // (at least one candidate per warp in every part)
     ExpandArgs b = a;
+    b.restrict_max = tr;
     const unsigned long long resident = (unsigned long long)sm_count * per_sm;
     const unsigned long long pc = std::max<unsigned long long>(1, a.p_count);
     const int max_parts = std::max(1, a.d.m / wpb);

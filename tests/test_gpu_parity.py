@@ -72,7 +72,10 @@ def test_random_contexts(n, m, density, seed):
                                               # 100-256 objects with many attributes: bitmap-tier roots,
                                               # subtrees with many relevant attributes (shared-memory path)
                                               (250, 300, 0.1, 2), (200, 128, 0.15, 3), (256, 200, 0.12, 4),
-                                              (120, 300, 0.2, 5), (100, 700, 0.1, 6)])
+                                              (120, 300, 0.2, 5), (100, 700, 0.1, 6),
+                                              # parents above and below the restricted-column limit:
+                                              # both paths of the bitmap tier
+                                              (9000, 24, 0.25, 2), (12000, 40, 0.2, 3)])
 def test_larger_random_contexts(n, m, density, seed):
     rows = cx.random_context(n, m, density, seed)
     check_against_oracle(rows, n, m, threads=8)
