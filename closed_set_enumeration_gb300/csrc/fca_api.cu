@@ -43,7 +43,8 @@ struct fca_ctx {
     Queue q[NQ]{};
     uint64_t q_count[NQ]{};
     Counters *ctr = nullptr;        // device
-    Counters *ctr_host = nullptr;   // pinned host mirror, current after every readback
+    Counters *ctr_snap = nullptr;   // device copy taken before each bitmap-tier launch (rollback)
+    Counters *ctr_host = nullptr;   // pinned host copy, read after each bitmap-tier launch
     uint32_t *stage = nullptr;      // pinned host staging (root entry)
 
     uint32_t *host_out_dev = nullptr;   // device buffer behind fca_enumerate_host
@@ -106,7 +107,7 @@ fca_status alloc_raw(fca_ctx *c, void **p, size_t bytes, const char *what)
     return FCA_OK;
 }
 
-uint64_t level_entry_bytes(const Dims &d) { return ((uint64_t)d.wnp + d.wm + 1) * 4; }
+uint64_t level_entry_bytes(const Dims &d) { return ((uint64_t)d.wnp + d.wm + 2) * 4; }
 uint64_t queue_entry_bytes(const Dims &d, int qi) { return ((uint64_t)(32 << qi) + d.wm + 2) * 4; }
 
 uint64_t initial_level_cap(const fca_ctx *c)
@@ -121,6 +122,7 @@ void free_level(Level &L)
     cudaFree(L.ext);
     cudaFree(L.itt);
     cudaFree(L.y);
+    cudaFree(L.n);
     L = Level{};
 }
 
@@ -150,7 +152,8 @@ fca_status make_level(fca_ctx *c, Level *L, uint64_t cap)
     fca_status s;
     if ((s = alloc_raw(c, (void **)&n.ext, cap * d.wnp * 4, "frontier extents")) != FCA_OK ||
         (s = alloc_raw(c, (void **)&n.itt, cap * d.wm * 4, "frontier intents")) != FCA_OK ||
-        (s = alloc_raw(c, (void **)&n.y, cap * 4, "frontier cursors")) != FCA_OK) {
+        (s = alloc_raw(c, (void **)&n.y, cap * 4, "frontier cursors")) != FCA_OK ||
+        (s = alloc_raw(c, (void **)&n.n, cap * 4, "frontier sizes")) != FCA_OK) {
         free_level(n);
         return s;
     }
@@ -217,6 +220,7 @@ fca_status grow_level(fca_ctx *c, size_t idx, uint64_t need, cudaStream_t st)
     CK(cudaMemcpyAsync(n.ext, L.ext, cnt * d.wnp * 4, cudaMemcpyDeviceToDevice, st), "level grow");
     CK(cudaMemcpyAsync(n.itt, L.itt, cnt * d.wm * 4, cudaMemcpyDeviceToDevice, st), "level grow");
     CK(cudaMemcpyAsync(n.y, L.y, cnt * 4, cudaMemcpyDeviceToDevice, st), "level grow");
+    CK(cudaMemcpyAsync(n.n, L.n, cnt * 4, cudaMemcpyDeviceToDevice, st), "level grow");
     CK(cudaStreamSynchronize(st), "stream synchronize");
     c->pool_bytes += (cap - L.cap) * eb;
     free_level(L);
@@ -331,7 +335,7 @@ fca_status run_subtree(Run &r, int qi)
     CK(cudaMemsetAsync(&c->ctr->q_count[qi], 0, sizeof(unsigned long long), r.st), "queue reset");
     CK(cudaMemsetAsync(&c->ctr->q_head[qi], 0, sizeof(unsigned long long), r.st), "queue reset");
     c->q_count[qi] = 0;
-    return read_counters(r);
+    return FCA_OK;
 }
 
 // Expand every entry of bitmap level `lv`, depth first.
@@ -346,11 +350,15 @@ fca_status drain(Run &r, size_t lv)
         const uint64_t k = std::min(have, kmax);
         const uint64_t begin = have - k;
 
-        // counters before the launch: the next level appends after its current fill
-        Counters before = *c->ctr_host;
-        before.next_count = c->level_count[lv + 1];
-        before.error = 0;
-        if ((s = write_counters(r, before)) != FCA_OK) return s;
+        // the next level appends after its current fill; the counters as they are now are kept on
+        // the device, to be restored if the launch has to be rolled back
+        uint64_t *next_fill = reinterpret_cast<uint64_t *>(c->stage + 1000);
+        *next_fill = c->level_count[lv + 1];
+        CK(cudaMemcpyAsync(&c->ctr->next_count, next_fill, sizeof(uint64_t), cudaMemcpyHostToDevice, r.st),
+           "counter set");
+        CK(cudaMemsetAsync(&c->ctr->error, 0, sizeof(unsigned int), r.st), "counter set");
+        CK(cudaMemcpyAsync(c->ctr_snap, c->ctr, sizeof(Counters), cudaMemcpyDeviceToDevice, r.st),
+           "counter snapshot");
 
         ExpandArgs a{};
         a.d = c->d;
@@ -377,11 +385,12 @@ fca_status drain(Run &r, size_t lv)
         if (after.error) {
             // roll back: drop everything the launch appended, then make room and retry
             c->stats.retries++;
-            if ((s = write_counters(r, before)) != FCA_OK) return s;
+            CK(cudaMemcpyAsync(c->ctr, c->ctr_snap, sizeof(Counters), cudaMemcpyDeviceToDevice, r.st),
+               "counter restore");
             bool limited = false;
             for (int qi = 0; qi < NQ; ++qi) {
                 if (!(after.error & (ERR_QUEUE0 << qi))) continue;
-                const uint64_t need = after.q_count[qi] - before.q_count[qi];
+                const uint64_t need = after.q_count[qi] - c->q_count[qi];
                 if ((s = run_subtree(r, qi)) != FCA_OK) return s;
                 if (need > c->q[qi].cap) {
                     s = grow_queue(c, qi, need);
@@ -390,7 +399,7 @@ fca_status drain(Run &r, size_t lv)
                 }
             }
             if (after.error & ERR_NEXT) {
-                const uint64_t need = after.next_count - before.next_count;
+                const uint64_t need = after.next_count - c->level_count[lv + 1];
                 if ((s = drain(r, lv + 1)) != FCA_OK) return s;
                 if (need > c->levels[lv + 1].cap) {
                     s = grow_level(c, lv + 1, need, r.st);
@@ -479,9 +488,11 @@ fca_status enumerate_impl(fca_ctx *c, uint32_t *out, uint64_t capacity, uint64_t
         Level &L = c->levels[0];
         int32_t *meta = reinterpret_cast<int32_t *>(c->stage);
         meta[0] = 0;
+        meta[1] = (int32_t)d.n;
         CK(cudaMemcpyAsync(L.ext, c->root_ext, d.wnp * 4, cudaMemcpyDeviceToDevice, st), "root entry");
         CK(cudaMemcpyAsync(L.itt, c->top, d.wm * 4, cudaMemcpyDeviceToDevice, st), "root entry");
         CK(cudaMemcpyAsync(L.y, &meta[0], 4, cudaMemcpyHostToDevice, st), "root entry");
+        CK(cudaMemcpyAsync(L.n, &meta[1], 4, cudaMemcpyHostToDevice, st), "root entry");
         c->level_count[0] = 1;
     }
     if ((s = write_counters(r, init)) != FCA_OK) return s;
@@ -536,6 +547,7 @@ void fca_free(fca_ctx *ctx)
     free_pools(ctx);
     for (cudaEvent_t e : ctx->events) cudaEventDestroy(e);
     cudaFree(ctx->ctr);
+    cudaFree(ctx->ctr_snap);
     cudaFree(ctx->host_out_dev);
     cudaFreeHost(ctx->ctr_host);
     cudaFreeHost(ctx->stage);
@@ -575,7 +587,8 @@ fca_status fca_context_create(const uint32_t *rows, int64_t n_objects, int32_t n
         (s = alloc_raw(c, (void **)&c->top, (size_t)d.wm * 4, "top")) != FCA_OK ||
         (s = alloc_raw(c, (void **)&c->full_mask, (size_t)d.wm * 4, "mask")) != FCA_OK ||
         (s = alloc_raw(c, (void **)&c->root_ext, (size_t)d.wnp * 4, "root extent")) != FCA_OK ||
-        (s = alloc_raw(c, (void **)&c->ctr, sizeof(Counters), "counters")) != FCA_OK)
+        (s = alloc_raw(c, (void **)&c->ctr, sizeof(Counters), "counters")) != FCA_OK ||
+        (s = alloc_raw(c, (void **)&c->ctr_snap, sizeof(Counters), "counter snapshot")) != FCA_OK)
         return fail(s);
     if (cudaMallocHost((void **)&c->ctr_host, sizeof(Counters)) != cudaSuccess ||
         cudaMallocHost((void **)&c->stage, 4096) != cudaSuccess ||

@@ -50,6 +50,7 @@ struct Level {
     uint32_t *ext;   // cap x wnp words (bitmap extents, 16-byte aligned rows)
     uint32_t *itt;   // cap x wm words (intents)
     int32_t *y;      // cap cursors
+    int32_t *n;      // cap extent sizes (objects)
     uint64_t cap;
 };
 

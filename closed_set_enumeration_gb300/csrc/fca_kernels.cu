@@ -141,6 +141,7 @@ __device__ __forceinline__ bool subset_of_column(const uint4 *cv, const uint32_t
 // limited by shared memory: M restricted columns of TR/32 words plus the object list.
 constexpr int RESTRICT_CAP = 4096;
 constexpr int RPL = RESTRICT_CAP / 1024;   // restricted-column words per lane
+constexpr int ROW_BOUND = 8;               // rows ANDed for the closure's upper bound (restricted path)
 
 // Shared memory of expand_bitmap_kernel. Both paths first stage the parent's non-zero extent
 // chunks (uint4 index and value). The gather path then keeps, per warp, its candidate's C chunks
@@ -190,15 +191,16 @@ __device__ __forceinline__ int block_exclusive_sum(int v, int *scratch, int *tot
     return before + incl - v;
 }
 
-// The rest of a candidate once |C| and the first object ids of C are known: the closure (AND of
-// the rows of `need` objects: exact for |C| <= SMALL_MAX, else an upper bound whose extra
-// attributes are decided by `subset(k)` in ascending order, so a violation below j ends the
-// candidate early), the canonical test, the intent and the child. `write_ext(dst)` writes C as a
-// dense bitmap for a child of the next level.
-template <bool COUNT, class Subset, class WriteExt>
+// The rest of a candidate once |C| and the first `need` object ids of C are known: the closure
+// (the AND of their rows: exact when need == |C|, else an upper bound whose extra attributes are
+// decided by `subset(k)` in ascending order, so a violation below j ends the candidate early),
+// the canonical test, the intent and the child. `write_ext(dst)` writes C as a dense bitmap for a
+// child of the next level; `all_ids()` completes the id list of a small child (need < |C|).
+template <bool COUNT, class Subset, class WriteExt, class AllIds>
 __device__ __forceinline__ void finish_candidate(const ExpandArgs &a, const Dims &d, const uint32_t *B, int j,
                                                  unsigned cnt, const uint32_t *ids, unsigned need, Subset &&subset,
-                                                 WriteExt &&write_ext, unsigned long long &my_bytes)
+                                                 WriteExt &&write_ext, AllIds &&all_ids,
+                                                 unsigned long long &my_bytes)
 {
     const unsigned lane = threadIdx.x & 31;
     uint32_t U = 0;
@@ -214,7 +216,7 @@ __device__ __forceinline__ void finish_candidate(const ExpandArgs &a, const Dims
     const uint32_t jbit = 1u << (j & 31);
     const uint32_t pm = lt_mask((int)lane, j);   // attributes below j
     uint32_t Dw;
-    if (cnt <= (unsigned)SMALL_MAX) {
+    if (need == cnt) {
         Dw = U;
         if (__any_sync(FULL, (U & ~Bw & pm) != 0u)) return;
     } else {
@@ -261,6 +263,8 @@ __device__ __forceinline__ void finish_candidate(const ExpandArgs &a, const Dims
             if (lane == 0) atomicOr(&a.ctr->error, ERR_QUEUE0 << qi);
             return;
         }
+        if (need < cnt) all_ids();
+        __syncwarp();
         for (int i = (int)lane; i < per; i += 32) Q.ids[s * per + i] = i < (int)cnt ? ids[i] : 0u;
         if (lane < (unsigned)d.wm) Q.itt[s * d.wm + lane] = Dw;
         if (lane == 0) { Q.y[s] = j + 1; Q.n[s] = (int)cnt; }
@@ -274,7 +278,7 @@ __device__ __forceinline__ void finish_candidate(const ExpandArgs &a, const Dims
         }
         write_ext(a.next.ext + s * (size_t)d.wnp);
         if (lane < (unsigned)d.wm) a.next.itt[s * d.wm + lane] = Dw;
-        if (lane == 0) a.next.y[s] = j + 1;
+        if (lane == 0) { a.next.y[s] = j + 1; a.next.n[s] = (int)cnt; }
     }
 }
 
@@ -315,7 +319,14 @@ __global__ void __launch_bounds__(256) expand_bitmap_kernel(ExpandArgs a)
         const unsigned long long p = a.p_begin + item / (unsigned)parts;
         const int part = (int)(item % (unsigned)parts);
         const int y = a.in.y[p];
-        const int j_lo = max(y, part * span), j_hi = min(d.m, (part + 1) * span);
+        // a parent small enough for restricted columns is expanded whole by its first part (the
+        // transposition is paid once), when its candidates make that cheaper than gathering
+        const int np = a.in.n[p];
+        const int gw = (np + 31) >> 5;
+        const bool restricted = np <= tr && (long long)(d.m - y) * min(wq, np) >= 4ll * gw * d.wm;
+        if (restricted && part > 0) continue;
+        const int j_lo = restricted ? y : max(y, part * span);
+        const int j_hi = restricted ? d.m : min(d.m, (part + 1) * span);
         if (j_lo >= j_hi) continue;                       // uniform over the block
         const uint32_t *B = a.in.itt + p * d.wm;
 
@@ -338,7 +349,7 @@ __global__ void __launch_bounds__(256) expand_bitmap_kernel(ExpandArgs a)
         __syncthreads();
         if (COUNT && threadIdx.x == 0) my_bytes += (unsigned long long)d.wnp * 4;   // the parent extent
 
-        if (na <= tr) {
+        if (restricted) {
             // ---- restricted path: object list, then the columns restricted to these objects
             int base_id = 0;
             for (int base = 0; base < nnz; base += blockDim.x) {
@@ -393,29 +404,33 @@ __global__ void __launch_bounds__(256) expand_bitmap_kernel(ExpandArgs a)
                 cnt = __reduce_add_sync(FULL, cnt);
                 if (cnt == 0) continue;   // empty extent: its closure is the bottom, added by the host
 
-                // object ids of C in ascending order: all of them when |C| <= SMALL_MAX, else the first 32
-                const unsigned need = cnt <= (unsigned)SMALL_MAX ? cnt : 32u;
-                unsigned got = 0;
+                // the first object ids of C in ascending order: the closure is bounded by their rows and
+                // completed on the restricted columns
+                auto collect = [&](unsigned want) {
+                    unsigned got = 0;
 #pragma unroll
-                for (int r = 0; r < RPL; ++r) {
-                    if (got >= need) break;
-                    const unsigned pc = __popc(c[r]);
-                    unsigned incl = pc;
+                    for (int r = 0; r < RPL; ++r) {
+                        if (got >= want) break;
+                        const unsigned pc = __popc(c[r]);
+                        unsigned incl = pc;
 #pragma unroll
-                    for (int off = 1; off < 32; off <<= 1) {
-                        const unsigned t = __shfl_up_sync(FULL, incl, off);
-                        if (lane >= (unsigned)off) incl += t;
+                        for (int off = 1; off < 32; off <<= 1) {
+                            const unsigned t = __shfl_up_sync(FULL, incl, off);
+                            if (lane >= (unsigned)off) incl += t;
+                        }
+                        unsigned pos = got + incl - pc;
+                        uint32_t bits = c[r];
+                        const int g = 32 * r + (int)lane;
+                        while (bits && pos < want) {
+                            const int b = __ffs(bits) - 1;
+                            bits &= bits - 1u;
+                            rids[pos++] = oid[32 * g + b];
+                        }
+                        got += __shfl_sync(FULL, incl, 31);
                     }
-                    unsigned pos = got + incl - pc;
-                    uint32_t bits = c[r];
-                    const int g = 32 * r + (int)lane;
-                    while (bits && pos < need) {
-                        const int b = __ffs(bits) - 1;
-                        bits &= bits - 1u;
-                        rids[pos++] = oid[32 * g + b];
-                    }
-                    got += __shfl_sync(FULL, incl, 31);
-                }
+                };
+                const unsigned need = cnt < (unsigned)ROW_BOUND ? cnt : (unsigned)ROW_BOUND;
+                collect(need);
                 __syncwarp();
                 finish_candidate<COUNT>(
                     a, d, B, j, cnt, rids, need,
@@ -443,6 +458,7 @@ __global__ void __launch_bounds__(256) expand_bitmap_kernel(ExpandArgs a)
                             }
                         }
                     },
+                    [&]() { collect(cnt); },
                     my_bytes);
                 __syncwarp();
             }
@@ -509,6 +525,7 @@ __global__ void __launch_bounds__(256) expand_bitmap_kernel(ExpandArgs a)
                         if (x.x | x.y | x.z | x.w) dst4[aidx[i]] = x;
                     }
                 },
+                [&]() {},
                 my_bytes);
             __syncwarp();
         }
