@@ -113,10 +113,12 @@ __global__ void top_kernel(const uint32_t *__restrict__ rows, uint32_t *top, uin
 
 // ------------------------------------------------------------------ bitmap tier
 
-// C subset of column K? C is held as its chunk list (values cv[i] at uint4 index idx[i]); early exit
-// at the first block of 64 chunks that disagrees. `loads` counts the column uint4 read.
-__device__ __forceinline__ bool subset_of_column(const uint4 *cv, const uint32_t *idx, int nnz,
-                                                 const uint4 *__restrict__ K, unsigned lane, unsigned &loads)
+// C subset of column K, with C = A & J on the staged chunks of A (values av[i] at uint4 index
+// idx[i]) and J the candidate's column: early exit at the first block of 64 chunks that disagrees.
+// `loads` counts the column uint4 read.
+__device__ __forceinline__ bool subset_of_column(const uint4 *av, const uint32_t *idx, int nnz,
+                                                 const uint4 *__restrict__ J, const uint4 *__restrict__ K,
+                                                 unsigned lane, unsigned &loads)
 {
     for (int base = 0; base < nnz; base += 64) {
         bool bad = false;
@@ -124,7 +126,9 @@ __device__ __forceinline__ bool subset_of_column(const uint4 *cv, const uint32_t
         for (int h = 0; h < 2; ++h) {
             const int i = base + h * 32 + (int)lane;
             if (i < nnz) {
-                const uint4 c = cv[i];
+                const uint4 a4 = av[i], j4 = __ldg(J + idx[i]);
+                const uint4 c = make_uint4(a4.x & j4.x, a4.y & j4.y, a4.z & j4.z, a4.w & j4.w);
+                loads += 1;
                 if (c.x | c.y | c.z | c.w) {
                     const uint4 k = __ldg(K + idx[i]);
                     ++loads;
@@ -144,9 +148,10 @@ constexpr int RPL = RESTRICT_CAP / 1024;   // restricted-column words per lane
 constexpr int ROW_BOUND = 8;               // rows ANDed for the closure's upper bound (restricted path)
 
 // Shared memory of expand_bitmap_kernel. Both paths first stage the parent's non-zero extent
-// chunks (uint4 index and value). The gather path then keeps, per warp, its candidate's C chunks
-// and up to SMALL_MAX object ids; the restricted path keeps the parent's object list, its columns
-// restricted to those objects (M x TR/32 words) and per-warp object ids.
+// chunks (uint4 index and value). The gather path then keeps, per warp, up to SMALL_MAX object
+// ids (C itself is recomputed from the staged chunks and column j when needed); the restricted
+// path keeps the parent's object list, its columns restricted to those objects (M x TR/32 words)
+// and per-warp object ids.
 struct ExpandLayout {
     size_t o_aidx, o_aval, o_wbase, per_warp, o_oid, o_colr, o_rids, o_blk, bytes;
     __host__ __device__ ExpandLayout(const Dims &d, int wpb, int tr)
@@ -155,7 +160,7 @@ struct ExpandLayout {
         o_aval = 0;                                        // wq uint4
         o_aidx = o_aval + wq * 16;                         // wq uint32
         o_wbase = (o_aidx + wq * 4 + 15) & ~(size_t)15;
-        per_warp = wq * 16 + SMALL_MAX * 4;                // C chunks, ids
+        per_warp = SMALL_MAX * 4;                          // ids
         const size_t gather_end = o_wbase + per_warp * wpb;
         o_oid = o_wbase;                                   // tr uint32
         o_colr = o_oid + (size_t)tr * 4;                   // m x tr/32 uint32
@@ -301,8 +306,7 @@ __global__ void __launch_bounds__(256) expand_bitmap_kernel(ExpandArgs a)
     const ExpandLayout L(d, wpb, tr);
     uint4 *aval = reinterpret_cast<uint4 *>(smem + L.o_aval);
     uint32_t *aidx = reinterpret_cast<uint32_t *>(smem + L.o_aidx);
-    uint4 *cval = reinterpret_cast<uint4 *>(smem + L.o_wbase + L.per_warp * wib);
-    uint32_t *gids = reinterpret_cast<uint32_t *>(cval + wq);
+    uint32_t *gids = reinterpret_cast<uint32_t *>(smem + L.o_wbase + L.per_warp * wib);
     uint32_t *oid = reinterpret_cast<uint32_t *>(smem + L.o_oid);
     uint32_t *colr = reinterpret_cast<uint32_t *>(smem + L.o_colr);
     uint32_t *rids = reinterpret_cast<uint32_t *>(smem + L.o_rids) + (size_t)wib * SMALL_MAX;
@@ -470,27 +474,31 @@ __global__ void __launch_bounds__(256) expand_bitmap_kernel(ExpandArgs a)
             if ((B[j >> 5] >> (j & 31)) & 1u) continue;   // saturation: A inside column j
             ++my_closures;
 
-            // C = A & column j on the chunks of A; |C| by popcount
+            // |C| for C = A & column j on the chunks of A (C itself is recomputed when needed)
             const uint4 *J4 = cols4 + (size_t)j * wq;
             unsigned cnt = 0;
             for (int i = (int)lane; i < nnz; i += 32) {
-                uint4 x = aval[i];
-                const uint4 cc = __ldg(J4 + aidx[i]);
+                const uint4 x = aval[i], cc = __ldg(J4 + aidx[i]);
                 if (COUNT) ++loads;
-                x.x &= cc.x; x.y &= cc.y; x.z &= cc.z; x.w &= cc.w;
-                cval[i] = x;
-                cnt += popc4(x);
+                cnt += __popc(x.x & cc.x) + __popc(x.y & cc.y) + __popc(x.z & cc.z) + __popc(x.w & cc.w);
             }
             cnt = __reduce_add_sync(FULL, cnt);
             if (cnt == 0) continue;   // empty extent: its closure is the bottom, added by the host
-            __syncwarp();
 
             // object ids of C in ascending order: all of them when |C| <= SMALL_MAX, else the first 32
             const unsigned need = cnt <= (unsigned)SMALL_MAX ? cnt : 32u;
             unsigned got = 0;
             for (int base = 0; base < nnz && got < need; base += 32) {
                 const int i = base + (int)lane;
-                const uint4 x = i < nnz ? cval[i] : make_uint4(0u, 0u, 0u, 0u);
+                uint4 x = make_uint4(0u, 0u, 0u, 0u);
+                uint32_t q = 0u;
+                if (i < nnz) {
+                    const uint4 av = aval[i];
+                    q = aidx[i];
+                    const uint4 cc = __ldg(J4 + q);
+                    if (COUNT) ++loads;
+                    x = make_uint4(av.x & cc.x, av.y & cc.y, av.z & cc.z, av.w & cc.w);
+                }
                 const unsigned pc = popc4(x);
                 unsigned incl = pc;
 #pragma unroll
@@ -500,7 +508,6 @@ __global__ void __launch_bounds__(256) expand_bitmap_kernel(ExpandArgs a)
                 }
                 unsigned pos = got + incl - pc;
                 const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
-                const uint32_t q = i < nnz ? aidx[i] : 0u;
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
                     uint32_t bits = w4[t];
@@ -515,13 +522,14 @@ __global__ void __launch_bounds__(256) expand_bitmap_kernel(ExpandArgs a)
             __syncwarp();
             finish_candidate<COUNT>(
                 a, d, B, j, cnt, gids, need,
-                [&](int k) { return subset_of_column(cval, aidx, nnz, cols4 + (size_t)k * wq, lane, loads); },
+                [&](int k) { return subset_of_column(aval, aidx, nnz, J4, cols4 + (size_t)k * wq, lane, loads); },
                 [&](uint32_t *dst) {
                     uint4 *dst4 = reinterpret_cast<uint4 *>(dst);
                     for (int q = (int)lane; q < wq; q += 32) dst4[q] = make_uint4(0u, 0u, 0u, 0u);
                     __syncwarp();
                     for (int i = (int)lane; i < nnz; i += 32) {
-                        const uint4 x = cval[i];
+                        const uint4 av = aval[i], cc = __ldg(J4 + aidx[i]);
+                        const uint4 x = make_uint4(av.x & cc.x, av.y & cc.y, av.z & cc.z, av.w & cc.w);
                         if (x.x | x.y | x.z | x.w) dst4[aidx[i]] = x;
                     }
                 },
@@ -1010,9 +1018,9 @@ static int launch_expand_t(const ExpandArgs &a, int sm_count, void *stream)
 {
     int wpb = WARPS_PER_BLOCK;
     while (wpb > 1 && ExpandLayout(a.d, wpb, 0).bytes > 200 * 1024) --wpb;
-    // the largest restricted extent whose columns fit next to the gather path's shared memory
-    // (at least 112 KiB, two blocks per SM)
-    const size_t budget = std::max<size_t>(ExpandLayout(a.d, wpb, 0).bytes, 112 * 1024);
+    // the largest restricted extent whose columns fit in the shared memory of three blocks per SM
+    // (or next to the gather path's own, when that is larger)
+    const size_t budget = std::max<size_t>(ExpandLayout(a.d, wpb, 0).bytes, 72 * 1024);
     int tr = RESTRICT_CAP;
     while (tr > 0 && ExpandLayout(a.d, wpb, tr).bytes > budget) tr -= 32;
     const size_t smem = ExpandLayout(a.d, wpb, tr).bytes;

@@ -221,7 +221,11 @@ def _digest(intents):
 
 @pytest.mark.parametrize("name", ["sparse", "skewed", "zipf", "biclusters"])
 def test_workload_full_size_digest(name):
-    """Full-size workloads against oracle digests written by tests/golden/make_workload_digests.py."""
+    """Full-size workloads against oracle digests written by tests/golden/make_workload_digests.py:
+    exact count and closures, the order-independent multiset digest of the intent set, the SHA-256
+    of the sorted set where recorded, and fixed points B'' = B of sampled intents computed one by
+    one by the oracle's derivation operators."""
+    from tests._util import multiset_digest
     table = json.load(open(DIGESTS)) if os.path.exists(DIGESTS) else {}
     if name not in table:
         pytest.skip(f"no oracle digest stored for {name}")
@@ -231,8 +235,10 @@ def test_workload_full_size_digest(name):
     got, st = gpu_run(rows, w.n_objects, w.n_attrs, capacity=ref["concepts"])
     assert got.shape[0] == ref["concepts"]
     assert st["closures"] == ref["closures"]
-    assert _digest(got) == ref["sha256_sorted_intents"]
-    # sampled fixed points, computed one by one by the oracle's derivation operators
+    if "multiset_hsum" in ref:
+        assert multiset_digest(got) == (int(ref["multiset_hsum"], 16), int(ref["multiset_hxor"], 16))
+    if "sha256_sorted_intents" in ref:
+        assert _digest(got) == ref["sha256_sorted_intents"]
     rng = np.random.default_rng(0)
     for i in rng.choice(got.shape[0], 200, replace=False):
         ext = oracle.derive_extent(rows, got[i])
