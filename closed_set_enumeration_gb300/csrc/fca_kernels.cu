@@ -46,7 +46,7 @@ __device__ __forceinline__ uint32_t ge_mask(int w, int b)
 __device__ __forceinline__ uint32_t lt_mask(int w, int b) { return ~ge_mask(w, b); }
 
 // Largest number of restricted-column words (x32 attributes) a lane keeps in registers.
-constexpr int REG_WORDS = 8;
+constexpr int REG_WORDS = 4;
 
 // Entry size in 32-bit words of an object-list queue root holding `cnt` objects (counting only).
 __device__ __forceinline__ unsigned queue_entry_words(unsigned cnt, int wm)
@@ -619,13 +619,11 @@ struct SubtreeWarp {
             uint32_t seg = sh ? ((s0 >> sh) | (s1 << (32 - sh))) : s0;
             const int len = hi - lo;
             if (len < 32) seg &= (1u << len) - 1u;
-            uint32_t rmw = Rm[w], res = rootB[w];
-            int i = 0;
-            while (rmw) {
-                const int b = __ffs(rmw) - 1;
-                rmw &= rmw - 1u;
-                if ((seg >> i) & 1u) res |= 1u << b;
-                ++i;
+            uint32_t res = rootB[w];
+            while (seg) {                      // each compact attribute of D in this word
+                const int i = __ffs(seg) - 1;
+                seg &= seg - 1u;
+                res |= 1u << (rmap[lo + i] & 31);
             }
             ob[nb * wm + w] = res;
         }
@@ -853,7 +851,7 @@ __device__ void dfs_smem(SubtreeWarp &S, int R, int n, int jn, int slices, int s
 }
 
 template <int NW, bool COUNT>
-__global__ void __launch_bounds__(256, 3) subtree_kernel(SubtreeArgs a)
+__global__ void __launch_bounds__(256, 4) subtree_kernel(SubtreeArgs a)
 {
     extern __shared__ uint32_t smw[];
     const Dims d = a.d;
@@ -1085,7 +1083,7 @@ static int launch_subtree_nw(const SubtreeArgs &a, int sm_count, void *stream)
     // split roots into slices when there are too few roots to keep every resident warp busy
     SubtreeArgs b = a;
     const unsigned long long resident = (unsigned long long)sm_count * per_sm * wpb;
-    const unsigned long long want = 16 * resident;
+    const unsigned long long want = 4 * resident;
     const unsigned long long qn = std::max<unsigned long long>(1, a.q_count);
     b.slices = (int)std::min<unsigned long long>(MAX_SLICES, std::max<unsigned long long>(1, (want + qn - 1) / qn));
     unsigned long long blocks = (a.q_count * b.slices + wpb - 1) / wpb;
