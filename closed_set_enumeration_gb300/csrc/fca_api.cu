@@ -34,8 +34,7 @@ struct fca_ctx {
     uint32_t *top = nullptr;       // wm
     uint32_t *full_mask = nullptr; // wm: every attribute (the bottom intent)
     uint32_t *root_ext = nullptr;  // wnp: every object
-    bool full_row_exists = false;
-    uint32_t *flag_host = nullptr; // pinned: full-row flag readback
+    uint32_t *flag_dev = nullptr;  // device: some row holds every attribute
 
     // work pools, allocated on first use, grown on demand and kept for later calls
     std::vector<Level> levels;
@@ -298,15 +297,6 @@ fca_status read_counters(Run &r)
     return FCA_OK;
 }
 
-fca_status write_counters(Run &r, const Counters &v)
-{
-    fca_ctx *c = r.c;
-    *c->ctr_host = v;
-    CK(cudaMemcpyAsync(c->ctr, c->ctr_host, sizeof(Counters), cudaMemcpyHostToDevice, r.st), "counter write");
-    CK(cudaStreamSynchronize(r.st), "stream synchronize");
-    return FCA_OK;
-}
-
 // Process every root waiting in object-list queue qi, then empty it.
 fca_status run_subtree(Run &r, int qi)
 {
@@ -436,14 +426,10 @@ fca_status load_table(fca_ctx *c, const uint32_t *rows, cudaStream_t st)
     CK(cudaMemcpyAsync(c->rows, rows, (size_t)d.n * d.wm * 4, cudaMemcpyDefault, st), "row copy");
     CK(cudaMemsetAsync(c->cols, 0, (size_t)d.m * d.wnp * 4, st), "column clear");
     CK(cudaMemcpyAsync(c->top, c->full_mask, d.wm * 4, cudaMemcpyDeviceToDevice, st), "top reset");
-    CK(cudaMemsetAsync(c->ctr, 0, sizeof(Counters), st), "counter clear");
+    CK(cudaMemsetAsync(c->flag_dev, 0, sizeof(uint32_t), st), "flag clear");
     CK((cudaError_t)launch_mask_rows(c->rows, d, st), "padding mask kernel");
     CK((cudaError_t)launch_transpose(c->rows, c->cols, d, st), "transpose kernel");
-    CK((cudaError_t)launch_top(c->rows, c->top, &c->ctr->error, d, st), "top kernel");
-    CK(cudaMemcpyAsync(c->flag_host, &c->ctr->error, 4, cudaMemcpyDeviceToHost, st), "flag readback");
-    CK(cudaMemsetAsync(c->ctr, 0, sizeof(Counters), st), "counter clear");
-    CK(cudaStreamSynchronize(st), "stream synchronize");
-    c->full_row_exists = *c->flag_host != 0;
+    CK((cudaError_t)launch_top(c->rows, c->top, c->flag_dev, d, st), "top kernel");
     c->table_launches = 2 + ((d.m & 31) ? 1 : 0);
     return FCA_OK;
 }
@@ -495,24 +481,20 @@ fca_status enumerate_impl(fca_ctx *c, uint32_t *out, uint64_t capacity, uint64_t
         CK(cudaMemcpyAsync(L.n, &meta[1], 4, cudaMemcpyHostToDevice, st), "root entry");
         c->level_count[0] = 1;
     }
-    if ((s = write_counters(r, init)) != FCA_OK) return s;
+    *c->ctr_host = init;
+    CK(cudaMemcpyAsync(c->ctr, c->ctr_host, sizeof(Counters), cudaMemcpyHostToDevice, st), "counter write");
 
     if ((s = drain(r, 0)) != FCA_OK) return s;
     for (int qi = 0; qi < NQ; ++qi)
         if ((s = run_subtree(r, qi)) != FCA_OK) return s;
-    if ((s = read_counters(r)) != FCA_OK) return s;
-
-    uint64_t total = c->ctr_host->out_count;
     // The bottom concept (M', M). When some object holds every attribute its extent is not empty and
     // the search reaches it. Otherwise only empty candidate extents close to it; the search skips
-    // those, and it is added here (a concept is output exactly once either way).
-    if (!c->full_row_exists) {
-        if (total < capacity)
-            CK(cudaMemcpyAsync(out + total * d.wm, c->full_mask, d.wm * 4, cudaMemcpyDeviceToDevice, st),
-               "bottom intent copy");
-        total += 1;
-        CK(cudaStreamSynchronize(st), "stream synchronize");
-    }
+    // those, and it is appended here (a concept is output exactly once either way).
+    CK((cudaError_t)launch_append_bottom(c->flag_dev, c->full_mask, out, capacity, c->ctr, d, st),
+       "bottom kernel");
+    c->stats.launches++;
+    if ((s = read_counters(r)) != FCA_OK) return s;
+    const uint64_t total = c->ctr_host->out_count;
     c->stats.concepts = total;
     c->stats.closures = c->ctr_host->closures;
     c->stats.frontier_bytes = c->pool_bytes;
@@ -551,7 +533,7 @@ void fca_free(fca_ctx *ctx)
     cudaFree(ctx->host_out_dev);
     cudaFreeHost(ctx->ctr_host);
     cudaFreeHost(ctx->stage);
-    cudaFreeHost(ctx->flag_host);
+    cudaFree(ctx->flag_dev);
     delete ctx;
 }
 
@@ -590,9 +572,9 @@ fca_status fca_context_create(const uint32_t *rows, int64_t n_objects, int32_t n
         (s = alloc_raw(c, (void **)&c->ctr, sizeof(Counters), "counters")) != FCA_OK ||
         (s = alloc_raw(c, (void **)&c->ctr_snap, sizeof(Counters), "counter snapshot")) != FCA_OK)
         return fail(s);
+    if ((s = alloc_raw(c, (void **)&c->flag_dev, sizeof(uint32_t), "flag")) != FCA_OK) return fail(s);
     if (cudaMallocHost((void **)&c->ctr_host, sizeof(Counters)) != cudaSuccess ||
-        cudaMallocHost((void **)&c->stage, 4096) != cudaSuccess ||
-        cudaMallocHost((void **)&c->flag_host, 4) != cudaSuccess) {
+        cudaMallocHost((void **)&c->stage, 4096) != cudaSuccess) {
         cudaGetLastError();
         c->err = "pinned host allocation failed";
         return fail(FCA_ERR_OOM);
@@ -609,6 +591,10 @@ fca_status fca_context_create(const uint32_t *rows, int64_t n_objects, int32_t n
         return fail(FCA_ERR_CUDA);
     }
     if ((s = load_table(c, rows, 0)) != FCA_OK) return fail(s);
+    if ((e = cudaStreamSynchronize(0)) != cudaSuccess) {
+        cuda_fail(c, e, "context set-up");
+        return fail(FCA_ERR_CUDA);
+    }
 
     // work pools: initial sizes and the growth limit (half of the free device memory by default)
     size_t free_b = 0, total_b = 0;

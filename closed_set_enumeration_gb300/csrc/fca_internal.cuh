@@ -106,6 +106,9 @@ int launch_transpose(const uint32_t *rows, uint32_t *cols, const Dims &d, void *
 int launch_top(const uint32_t *rows, uint32_t *top, uint32_t *flag_full_row, const Dims &d,
                void *stream);
 int launch_expand(const ExpandArgs &a, int sm_count, void *stream);
+// Append the all-attribute intent when *flag_full_row is 0 (one slot from Counters::out_count).
+int launch_append_bottom(const uint32_t *flag_full_row, const uint32_t *full_mask, uint32_t *out,
+                         uint64_t capacity, Counters *ctr, const Dims &d, void *stream);
 int launch_subtree(const SubtreeArgs &a, int nw, int sm_count, void *stream);
 size_t expand_smem_per_warp(const Dims &d);
 

@@ -45,8 +45,10 @@ __device__ __forceinline__ uint32_t ge_mask(int w, int b)
 // Bits < b of word `w`.
 __device__ __forceinline__ uint32_t lt_mask(int w, int b) { return ~ge_mask(w, b); }
 
-// Largest number of restricted-column words (x32 attributes) a lane keeps in registers.
-constexpr int REG_WORDS = 4;
+// Largest number of restricted-column words (x32 attributes) a lane keeps in registers: 8 (up to
+// 256 relevant attributes) when M > 128, else 4, which keeps the kernel within 64 registers.
+constexpr int REG_WORDS_MAX = 8;
+constexpr int reg_words_for(int m) { return m > 128 ? 8 : 4; }
 
 // Entry size in 32-bit words of an object-list queue root holding `cnt` objects (counting only).
 __device__ __forceinline__ unsigned queue_entry_words(unsigned cnt, int wm)
@@ -109,6 +111,19 @@ __global__ void top_kernel(const uint32_t *__restrict__ rows, uint32_t *top, uin
         __syncthreads();
     }
     if (full_row) atomicOr(flag, 1u);
+}
+
+// The bottom concept when its extent is empty (no row holds every attribute): one more row.
+__global__ void append_bottom_kernel(const uint32_t *flag, const uint32_t *full_mask, uint32_t *out,
+                                     unsigned long long capacity, Counters *ctr, int wm)
+{
+    if (*flag) return;   // some object holds every attribute: the search has output it
+    const unsigned lane = threadIdx.x & 31;
+    unsigned long long slot = 0;
+    if (lane == 0) slot = atomicAdd(&ctr->out_count, 1ull);
+    slot = __shfl_sync(FULL, slot, 0);
+    if (slot < capacity)
+        for (int w = (int)lane; w < wm; w += 32) out[slot * wm + w] = full_mask[w];
 }
 
 // ------------------------------------------------------------------ bitmap tier
@@ -557,7 +572,7 @@ struct SubtreeLayout {
         wm = d.wm;
         fr = (32 * nw < d.m ? 32 * nw : d.m) + 1;     // depth <= |extent| and <= |R|
         // frame: extent mask, then cursor + intent (shared-memory search) or candidates + intent
-        fs = nw + (1 + wm > 2 * REG_WORDS ? 1 + wm : 2 * REG_WORDS);
+        fs = nw + (1 + wm > 2 * REG_WORDS_MAX ? 1 + wm : 2 * REG_WORDS_MAX);
         o_rmap = (size_t)nw * mp;
         o_rootb = o_rmap + mp / 2;
         o_rm = o_rootb + 32;
@@ -850,8 +865,8 @@ __device__ void dfs_smem(SubtreeWarp &S, int R, int n, int jn, int slices, int s
     }
 }
 
-template <int NW, bool COUNT>
-__global__ void __launch_bounds__(256, 4) subtree_kernel(SubtreeArgs a)
+template <int NW, bool COUNT, int RW>
+__global__ void __launch_bounds__(256, RW > 4 ? 3 : 4) subtree_kernel(SubtreeArgs a)
 {
     extern __shared__ uint32_t smw[];
     const Dims d = a.d;
@@ -963,7 +978,7 @@ __global__ void __launch_bounds__(256, 4) subtree_kernel(SubtreeArgs a)
         if (R <= 32) dfs_regs<NW, 1, COUNT>(S, R, n, jn, sl, slice);
         else if (R <= 64) dfs_regs<NW, 2, COUNT>(S, R, n, jn, sl, slice);
         else if (R <= 128) dfs_regs<NW, 4, COUNT>(S, R, n, jn, sl, slice);
-        else if (R <= 32 * REG_WORDS) dfs_regs<NW, REG_WORDS, COUNT>(S, R, n, jn, sl, slice);
+        else if (RW > 4 && R <= 32 * RW) dfs_regs<NW, RW, COUNT>(S, R, n, jn, sl, slice);
         else dfs_smem<NW, COUNT>(S, R, n, jn, sl, slice);
         __syncwarp();
     }
@@ -993,6 +1008,13 @@ int launch_transpose(const uint32_t *rows, uint32_t *cols, const Dims &d, void *
     return (int)cudaGetLastError();
 }
 
+int launch_append_bottom(const uint32_t *flag, const uint32_t *full_mask, uint32_t *out, uint64_t capacity,
+                         Counters *ctr, const Dims &d, void *stream)
+{
+    append_bottom_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(flag, full_mask, out, capacity, ctr, d.wm);
+    return (int)cudaGetLastError();
+}
+
 int launch_top(const uint32_t *rows, uint32_t *top, uint32_t *flag, const Dims &d, void *stream)
 {
     const int tpb = 256;
@@ -1002,6 +1024,14 @@ int launch_top(const uint32_t *rows, uint32_t *top, uint32_t *flag, const Dims &
 }
 
 size_t expand_smem_per_warp(const Dims &d) { return ExpandLayout(d, 1, 0).bytes; }
+
+// A launch shape computed once per device and shared-memory size.
+struct ShapeCache {
+    int dev = -1;
+    size_t smem = 0;
+    int wpb = 0;
+    int per_sm = 1;
+};
 
 static int warps_for(size_t per_warp)
 {
@@ -1022,14 +1052,21 @@ static int launch_expand_t(const ExpandArgs &a, int sm_count, void *stream)
     int tr = RESTRICT_CAP;
     while (tr > 0 && ExpandLayout(a.d, wpb, tr).bytes > budget) tr -= 32;
     const size_t smem = ExpandLayout(a.d, wpb, tr).bytes;
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(expand_bitmap_kernel<COUNT>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return (int)e;
+    // the shared-memory attribute and the occupancy query, once per device and size (per thread)
+    static thread_local ShapeCache cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cache.dev != dev || cache.smem != smem || cache.wpb != wpb) {
+        if (smem > 48 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(expand_bitmap_kernel<COUNT>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return (int)e;
+        }
+        int ps = 0;
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ps, expand_bitmap_kernel<COUNT>, wpb * 32, smem);
+        cache = ShapeCache{dev, smem, wpb, ps < 1 ? 1 : ps};
     }
-    int per_sm = 0;
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, expand_bitmap_kernel<COUNT>, wpb * 32, smem);
-    if (per_sm < 1) per_sm = 1;
+    const int per_sm = cache.per_sm;
     // split each parent's attribute range into parts when there are too few parents to fill the GPU
     // (at least one candidate per warp in every part)
     ExpandArgs b = a;
@@ -1051,34 +1088,38 @@ int launch_expand(const ExpandArgs &a, int sm_count, void *stream)
 }
 
 // Block shape of the subtree kernel (persistent: at most one block per resident slot).
-template <int NW, bool COUNT>
+template <int NW, bool COUNT, int RW>
 static int subtree_shape(const Dims &d, int *wpb_out, size_t *smem_out, int *per_sm_out)
 {
     const size_t pw = SubtreeLayout(d, NW).words * 4;
     const int wpb = warps_for(pw);
     const size_t smem = pw * wpb;
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(subtree_kernel<NW, COUNT>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    static thread_local ShapeCache cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cache.dev != dev || cache.smem != smem || cache.wpb != wpb) {
+        if (smem > 48 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(subtree_kernel<NW, COUNT, RW>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return (int)e;
+        }
+        int ps = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ps, subtree_kernel<NW, COUNT, RW>, wpb * 32, smem);
         if (e != cudaSuccess) return (int)e;
+        cache = ShapeCache{dev, smem, wpb, ps < 1 ? 1 : ps};
     }
-    int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, subtree_kernel<NW, COUNT>,
-                                                                  wpb * 32, smem);
-    if (e != cudaSuccess) return (int)e;
-    if (per_sm < 1) per_sm = 1;
     *wpb_out = wpb;
     *smem_out = smem;
-    *per_sm_out = per_sm;
+    *per_sm_out = cache.per_sm;
     return (int)cudaSuccess;
 }
 
-template <int NW, bool COUNT>
+template <int NW, bool COUNT, int RW>
 static int launch_subtree_nw(const SubtreeArgs &a, int sm_count, void *stream)
 {
     int wpb = 0, per_sm = 0;
     size_t smem = 0;
-    int e = subtree_shape<NW, COUNT>(a.d, &wpb, &smem, &per_sm);
+    int e = subtree_shape<NW, COUNT, RW>(a.d, &wpb, &smem, &per_sm);
     if (e != (int)cudaSuccess) return e;
     // split roots into slices when there are too few roots to keep every resident warp busy
     SubtreeArgs b = a;
@@ -1090,15 +1131,21 @@ static int launch_subtree_nw(const SubtreeArgs &a, int sm_count, void *stream)
     const unsigned long long cap = (unsigned long long)sm_count * per_sm;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    subtree_kernel<NW, COUNT><<<(unsigned)blocks, wpb * 32, smem, (cudaStream_t)stream>>>(b);
+    subtree_kernel<NW, COUNT, RW><<<(unsigned)blocks, wpb * 32, smem, (cudaStream_t)stream>>>(b);
     return (int)cudaGetLastError();
 }
 
 int launch_subtree(const SubtreeArgs &a, int nw, int sm_count, void *stream)
 {
-    if (a.count_work)
-        return nw == 1 ? launch_subtree_nw<1, true>(a, sm_count, stream) : launch_subtree_nw<2, true>(a, sm_count, stream);
-    return nw == 1 ? launch_subtree_nw<1, false>(a, sm_count, stream) : launch_subtree_nw<2, false>(a, sm_count, stream);
+    const bool wide = reg_words_for(a.d.m) > 4;
+    if (a.count_work) {
+        if (wide) return nw == 1 ? launch_subtree_nw<1, true, 8>(a, sm_count, stream)
+                                 : launch_subtree_nw<2, true, 8>(a, sm_count, stream);
+        return nw == 1 ? launch_subtree_nw<1, true, 4>(a, sm_count, stream) : launch_subtree_nw<2, true, 4>(a, sm_count, stream);
+    }
+    if (wide) return nw == 1 ? launch_subtree_nw<1, false, 8>(a, sm_count, stream)
+                             : launch_subtree_nw<2, false, 8>(a, sm_count, stream);
+    return nw == 1 ? launch_subtree_nw<1, false, 4>(a, sm_count, stream) : launch_subtree_nw<2, false, 4>(a, sm_count, stream);
 }
 
 }  // namespace fca

@@ -91,9 +91,11 @@ fca_status fca_context_create(const uint32_t *rows, int64_t n_objects, int32_t n
 /*
  * Replace the context's table with new rows of the same N x M and rebuild
  * its columns and top intent, reusing every allocation (a new batch of the
- * same shape). `rows` as for fca_context_create (host or device pointer);
- * the work runs on `stream` (cudaStream_t, NULL = legacy default stream) and
- * the call returns after it completes.
+ * same shape). `rows` as for fca_context_create (host or device pointer).
+ * The work is enqueued on `stream` (cudaStream_t, NULL = legacy default
+ * stream) and the call returns without waiting for it: `rows` must stay
+ * valid until it has run, and a later fca_enumerate must be ordered after it
+ * (the same stream does that).
  */
 fca_status fca_context_load(fca_ctx *ctx, const uint32_t *rows, void *stream);
 
