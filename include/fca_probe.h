@@ -25,9 +25,10 @@ extern "C" {
 int fca_probe_lop3(double *ops_per_s, double *ms);
 
 /*
- * Read bandwidth of a device buffer of `bytes` bytes (uint4 loads, all SMs),
- * best of `reps` launches after one warm-up launch. With bytes well below the
- * L2 size this is the L2 read bandwidth.
+ * Read bandwidth of a device buffer of `bytes` bytes (uint4 loads that skip
+ * L1, all SMs, the buffer read 8 times per launch), best of `reps` launches
+ * after one warm-up launch. With bytes well below the L2 size this is the L2
+ * read bandwidth.
  *   gbps       receives bytes read per second / 1e9
  * Returns 0, or a CUDA error code (the buffer is allocated and freed inside).
  */
