@@ -213,6 +213,10 @@ def cpu_baseline(rows, w, budget_s: float):
 
 # ----------------------------------------------------------------------------- roofline helpers
 
+# The source file of each kernel a roofline is reported for.
+KERNEL_SOURCES = {"subtree_kernel": "fca_subtree.cu", "expand_bitmap_kernel": "fca_expand.cu"}
+
+
 def profile_traffic(kernel: str, workload: str):
     """DRAM bytes per launch of `kernel` on `workload` from the committed ncu summary, or None.
 
@@ -221,7 +225,7 @@ def profile_traffic(kernel: str, workload: str):
     """
     import hashlib
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
-    src = os.path.join(ROOT, "closed_set_enumeration_gb300", "csrc", "fca_kernels.cu")
+    src = os.path.join(ROOT, "closed_set_enumeration_gb300", "csrc", KERNEL_SOURCES[kernel])
     try:
         text = open(path).read()
         sha = hashlib.sha256(open(src, "rb").read()).hexdigest()

@@ -1,0 +1,53 @@
+// Device helpers shared by the kernels of libfca: bitset masks, popcounts, queue entry sizes and
+// the per-device cache of a kernel's launch shape.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "fca_internal.cuh"
+
+namespace fca {
+
+constexpr unsigned FULL = 0xffffffffu;
+constexpr int OUTBUF = 16;          // intents buffered per warp before one atomicAdd
+constexpr int MAX_SLICES = 32;      // most work items one subtree root is split into
+constexpr int WARPS_PER_BLOCK = 8;
+
+__device__ __forceinline__ unsigned popc4(const uint4 &x)
+{
+    return __popc(x.x) + __popc(x.y) + __popc(x.z) + __popc(x.w);
+}
+
+// Bits >= b of 32-bit word `w` of a bitset (b is a bit index of the whole set).
+__device__ __forceinline__ uint32_t ge_mask(int w, int b)
+{
+    const int bw = b >> 5;
+    if (w < bw) return 0u;
+    if (w > bw) return FULL;
+    return FULL << (b & 31);
+}
+
+// Bits < b of word `w`.
+__device__ __forceinline__ uint32_t lt_mask(int w, int b) { return ~ge_mask(w, b); }
+
+// Largest number of restricted-column words (x32 attributes) a lane keeps in registers: 8 (up to
+// 256 relevant attributes) when M > 128, else 4, which keeps the kernel within 64 registers.
+constexpr int REG_WORDS_MAX = 8;
+constexpr int reg_words_for(int m) { return m > 128 ? 8 : 4; }
+
+// Entry size in 32-bit words of an object-list queue root holding `cnt` objects (counting only).
+__device__ __forceinline__ unsigned queue_entry_words(unsigned cnt, int wm)
+{
+    const unsigned per = cnt <= 32u ? 32u : 64u;
+    return per + (unsigned)wm + 2u;
+}
+
+// A launch shape computed once per device and shared-memory size.
+struct ShapeCache {
+    int dev = -1;
+    size_t smem = 0;
+    int wpb = 0;
+    int per_sm = 1;
+};
+
+}  // namespace fca

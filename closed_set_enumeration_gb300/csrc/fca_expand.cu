@@ -1,0 +1,501 @@
+// Bitmap tier of libfca (sm_103a): expand_bitmap_kernel expands the concepts of one level whose
+// extents hold more than 64 objects. Per (parent, j) candidate it forms the extent intersection,
+// the closure, the canonical test and the child (FCbO-to-CUDA article, sections 2.1-2.3, 4.2-4.4;
+// Parallel FCBO article, sections 2.1, 3.2). Bitwise set algebra only: no tensor cores.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "fca_device.cuh"
+
+namespace fca {
+namespace {
+
+
+// C subset of column K, with C = A & J on the staged chunks of A (values av[i] at uint4 index
+// idx[i]) and J the candidate's column: early exit at the first block of 64 chunks that disagrees.
+// `loads` counts the column uint4 read.
+__device__ __forceinline__ bool subset_of_column(const uint4 *av, const uint32_t *idx, int nnz,
+                                                 const uint4 *__restrict__ J, const uint4 *__restrict__ K,
+                                                 unsigned lane, unsigned &loads)
+{
+    for (int base = 0; base < nnz; base += 64) {
+        bool bad = false;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int i = base + h * 32 + (int)lane;
+            if (i < nnz) {
+                const uint4 a4 = av[i], j4 = __ldg(J + idx[i]);
+                const uint4 c = make_uint4(a4.x & j4.x, a4.y & j4.y, a4.z & j4.z, a4.w & j4.w);
+                loads += 1;
+                if (c.x | c.y | c.z | c.w) {
+                    const uint4 k = __ldg(K + idx[i]);
+                    ++loads;
+                    bad |= ((c.x & ~k.x) | (c.y & ~k.y) | (c.z & ~k.z) | (c.w & ~k.w)) != 0u;
+                }
+            }
+        }
+        if (__any_sync(FULL, bad)) return false;
+    }
+    return true;
+}
+
+// Largest parent extent (objects) whose columns the block rebuilds restricted to its objects,
+// limited by shared memory: M restricted columns of TR/32 words plus the object list.
+constexpr int RESTRICT_CAP = 4096;
+constexpr int RPL = RESTRICT_CAP / 1024;   // restricted-column words per lane
+constexpr int ROW_BOUND = 8;               // rows ANDed for the closure's upper bound (restricted path)
+
+// Shared memory of expand_bitmap_kernel. Both paths first stage the parent's non-zero extent
+// chunks (uint4 index and value). The gather path then keeps, per warp, up to SMALL_MAX object
+// ids (C itself is recomputed from the staged chunks and column j when needed); the restricted
+// path keeps the parent's object list, its columns restricted to those objects (M x TR/32 words)
+// and per-warp object ids.
+struct ExpandLayout {
+    size_t o_aidx, o_aval, o_wbase, per_warp, o_oid, o_colr, o_rids, o_blk, bytes;
+    __host__ __device__ ExpandLayout(const Dims &d, int wpb, int tr)
+    {
+        const size_t wq = (size_t)(d.wnp >> 2);
+        o_aval = 0;                                        // wq uint4
+        o_aidx = o_aval + wq * 16;                         // wq uint32
+        o_wbase = (o_aidx + wq * 4 + 15) & ~(size_t)15;
+        per_warp = SMALL_MAX * 4;                          // ids
+        const size_t gather_end = o_wbase + per_warp * wpb;
+        o_oid = o_wbase;                                   // tr uint32
+        o_colr = o_oid + (size_t)tr * 4;                   // m x tr/32 uint32
+        o_rids = o_colr + (size_t)d.m * (size_t)(tr / 32) * 4;
+        const size_t restrict_end = o_rids + (size_t)wpb * SMALL_MAX * 4;
+        o_blk = ((gather_end > restrict_end ? gather_end : restrict_end) + 15) & ~(size_t)15;
+        bytes = o_blk + 32 * 4;                            // block scratch: counts and sums
+    }
+};
+
+// Block-wide exclusive prefix sum of one value per thread (all threads call it); returns the
+// thread's offset and writes the block total to *total. `scratch` holds 2 x 32 ints.
+__device__ __forceinline__ int block_exclusive_sum(int v, int *scratch, int *total)
+{
+    const unsigned lane = threadIdx.x & 31;
+    const int wib = threadIdx.x >> 5, wpb = blockDim.x >> 5;
+    int incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int t = __shfl_up_sync(FULL, incl, off);
+        if (lane >= (unsigned)off) incl += t;
+    }
+    if (lane == 31) scratch[wib] = incl;
+    __syncthreads();
+    int before = 0, all = 0;
+    for (int w = 0; w < wpb; ++w) {
+        const int s = scratch[w];
+        if (w < wib) before += s;
+        all += s;
+    }
+    __syncthreads();
+    *total = all;
+    return before + incl - v;
+}
+
+// The rest of a candidate once |C| and the first `need` object ids of C are known: the closure
+// (the AND of their rows: exact when need == |C|, else an upper bound whose extra attributes are
+// decided by `subset(k)` in ascending order, so a violation below j ends the candidate early),
+// the canonical test, the intent and the child. `write_ext(dst)` writes C as a dense bitmap for a
+// child of the next level; `all_ids()` completes the id list of a small child (need < |C|).
+template <bool COUNT, class Subset, class WriteExt, class AllIds>
+__device__ __forceinline__ void finish_candidate(const ExpandArgs &a, const Dims &d, const uint32_t *B, int j,
+                                                 unsigned cnt, const uint32_t *ids, unsigned need, Subset &&subset,
+                                                 WriteExt &&write_ext, AllIds &&all_ids,
+                                                 unsigned long long &my_bytes)
+{
+    const unsigned lane = threadIdx.x & 31;
+    // AND of the rows: lanes take (object, word) pairs with the words padded to a power of two W2
+    // (so a lane always holds the same word), issue all their loads at once, then AND across the
+    // lanes holding the same word; lane w ends with word w.
+    const int w2 = d.wm <= 1 ? 1 : 1 << (32 - __clz(d.wm - 1));
+    const int my_w = (int)lane & (w2 - 1);
+    uint32_t U = FULL;
+    if (my_w < d.wm)
+        for (unsigned pidx = lane; pidx < need * (unsigned)w2; pidx += 32)
+            U &= __ldg(a.rows + (size_t)ids[pidx / (unsigned)w2] * d.wm + my_w);
+    for (int sft = w2; sft < 32; sft <<= 1) U &= __shfl_xor_sync(FULL, U, sft);
+    if ((int)lane >= d.wm) U = 0u;
+    if (COUNT && lane == 0) my_bytes += (unsigned long long)need * d.wm * 4;   // rows read
+    const uint32_t Bw = lane < (unsigned)d.wm ? B[lane] : 0u;
+    const int ju = j >> 5;
+    const uint32_t jbit = 1u << (j & 31);
+    const uint32_t pm = lt_mask((int)lane, j);   // attributes below j
+    uint32_t Dw;
+    if (need == cnt) {
+        Dw = U;
+        if (__any_sync(FULL, (U & ~Bw & pm) != 0u)) return;
+    } else {
+        // attributes that may still join: in U, not in B, not j; tested in ascending order
+        uint32_t X = U & ~Bw;
+        if ((int)lane == ju) X &= ~jbit;
+        Dw = Bw | ((int)lane == ju ? jbit : 0u);
+        for (;;) {
+            const unsigned bal = __ballot_sync(FULL, X != 0u);
+            if (!bal) break;
+            const int u = __ffs(bal) - 1;
+            const uint32_t xw = __shfl_sync(FULL, X, u);
+            const int b = __ffs(xw) - 1;
+            const int k = u * 32 + b;
+            if ((int)lane == u) X &= ~(1u << b);
+            if (subset(k)) {
+                if (k < j) return;                      // not canonical
+                if ((int)lane == u) Dw |= 1u << b;
+            }
+        }
+    }
+
+    if (COUNT && lane == 0) {   // the intent row and the child entry written
+        my_bytes += (unsigned long long)d.wm * 4;
+        my_bytes += cnt <= (unsigned)SMALL_MAX ? 4ull * queue_entry_words(cnt, d.wm)
+                                               : (unsigned long long)(4 * d.wnp + 4 * d.wm + 4);
+    }
+    // emit the intent
+    unsigned long long slot = 0;
+    if (lane == 0) slot = atomicAdd(&a.ctr->out_count, 1ull);
+    slot = __shfl_sync(FULL, slot, 0);
+    if (slot < a.capacity && lane < (unsigned)d.wm) a.out[slot * d.wm + lane] = Dw;
+
+    // the child (C, D, j+1): an object-list root, or an entry of the next bitmap level.
+    // A destination that is full only counts; the driver rolls the launch back and retries.
+    if (cnt <= (unsigned)SMALL_MAX) {
+        const int qi = cnt <= 32u ? 0 : 1;
+        const Queue &Q = a.q[qi];
+        const int per = 32 << qi;
+        unsigned long long s = 0;
+        if (lane == 0) s = atomicAdd(&a.ctr->q_count[qi], 1ull);
+        s = __shfl_sync(FULL, s, 0);
+        if (s >= Q.cap) {
+            if (lane == 0) atomicOr(&a.ctr->error, ERR_QUEUE0 << qi);
+            return;
+        }
+        if (need < cnt) all_ids();
+        __syncwarp();
+        for (int i = (int)lane; i < per; i += 32) Q.ids[s * per + i] = i < (int)cnt ? ids[i] : 0u;
+        if (lane < (unsigned)d.wm) Q.itt[s * d.wm + lane] = Dw;
+        if (lane == 0) { Q.y[s] = j + 1; Q.n[s] = (int)cnt; }
+    } else {
+        unsigned long long s = 0;
+        if (lane == 0) s = atomicAdd(&a.ctr->next_count, 1ull);
+        s = __shfl_sync(FULL, s, 0);
+        if (s >= a.next.cap) {
+            if (lane == 0) atomicOr(&a.ctr->error, ERR_NEXT);
+            return;
+        }
+        write_ext(a.next.ext + s * (size_t)d.wnp);
+        if (lane < (unsigned)d.wm) a.next.itt[s * d.wm + lane] = Dw;
+        if (lane == 0) { a.next.y[s] = j + 1; a.next.n[s] = (int)cnt; }
+    }
+}
+
+// Bitmap tier. A work item is (parent, part of the attribute range). The block stages the parent's
+// non-zero extent chunks once. Extents of at most `a.restrict_max` objects are then turned into an
+// object list, and the rows of those objects are transposed into columns restricted to them (one
+// ballot per attribute and 32 objects); each candidate's C is read from those columns without any
+// global column access. Larger extents keep the chunk list: each warp gathers column j on the
+// parent's non-zero chunks. Either way the warps of the block take the part's candidates j in turn.
+template <bool COUNT>
+__global__ void __launch_bounds__(256) expand_bitmap_kernel(ExpandArgs a)
+{
+    extern __shared__ __align__(16) unsigned char smem[];
+    const Dims d = a.d;
+    const int wq = (int)(d.wnp >> 2);
+    const unsigned lane = threadIdx.x & 31;
+    const int wib = threadIdx.x >> 5;
+    const int wpb = blockDim.x >> 5;
+    const int tr = a.restrict_max;
+    const ExpandLayout L(d, wpb, tr);
+    uint4 *aval = reinterpret_cast<uint4 *>(smem + L.o_aval);
+    uint32_t *aidx = reinterpret_cast<uint32_t *>(smem + L.o_aidx);
+    uint32_t *gids = reinterpret_cast<uint32_t *>(smem + L.o_wbase + L.per_warp * wib);
+    uint32_t *oid = reinterpret_cast<uint32_t *>(smem + L.o_oid);
+    uint32_t *colr = reinterpret_cast<uint32_t *>(smem + L.o_colr);
+    uint32_t *rids = reinterpret_cast<uint32_t *>(smem + L.o_rids) + (size_t)wib * SMALL_MAX;
+    int *blk = reinterpret_cast<int *>(smem + L.o_blk);   // [0..31] scan scratch
+    const uint4 *cols4 = reinterpret_cast<const uint4 *>(a.cols);
+    const uint4 *ext4 = reinterpret_cast<const uint4 *>(a.in.ext);
+
+    unsigned long long my_closures = 0, my_bytes = 0;
+    unsigned loads = 0;   // uint4 loads of columns by this lane (counting only)
+    const int parts = a.parts;
+    const int span = (d.m + parts - 1) / parts;
+    const unsigned long long items = a.p_count * (unsigned long long)parts;
+    for (unsigned long long item = blockIdx.x; item < items; item += gridDim.x) {
+        const unsigned long long p = a.p_begin + item / (unsigned)parts;
+        const int part = (int)(item % (unsigned)parts);
+        const int y = a.in.y[p];
+        // a parent small enough for restricted columns is expanded whole by its first part (the
+        // transposition is paid once), when its candidates make that cheaper than gathering
+        const int np = a.in.n[p];
+        const int gw = (np + 31) >> 5;
+        const bool restricted = np <= tr && (long long)(d.m - y) * min(wq, np) >= 4ll * gw * d.wm;
+        if (restricted && part > 0) continue;
+        const int j_lo = restricted ? y : max(y, part * span);
+        const int j_hi = restricted ? d.m : min(d.m, (part + 1) * span);
+        if (j_lo >= j_hi) continue;                       // uniform over the block
+        const uint32_t *B = a.in.itt + p * d.wm;
+
+        // ---- stage the non-zero chunks of A in order (block-wide compaction), and |A|
+        const uint4 *A4 = ext4 + p * wq;
+        __syncthreads();
+        int nnz = 0, na = 0;
+        for (int base = 0; base < wq; base += blockDim.x) {
+            const int q = base + (int)threadIdx.x;
+            uint4 x = make_uint4(0u, 0u, 0u, 0u);
+            if (q < wq) x = A4[q];
+            const bool nz = (x.x | x.y | x.z | x.w) != 0u;
+            int round_nnz = 0, round_na = 0;
+            const int off = block_exclusive_sum(nz ? 1 : 0, blk, &round_nnz);
+            (void)block_exclusive_sum((int)popc4(x), blk, &round_na);
+            if (nz) { aval[nnz + off] = x; aidx[nnz + off] = (uint32_t)q; }
+            nnz += round_nnz;
+            na += round_na;
+        }
+        __syncthreads();
+        if (COUNT && threadIdx.x == 0) my_bytes += (unsigned long long)d.wnp * 4;   // the parent extent
+
+        if (restricted) {
+            // ---- restricted path: object list, then the columns restricted to these objects
+            int base_id = 0;
+            for (int base = 0; base < nnz; base += blockDim.x) {
+                const int i = base + (int)threadIdx.x;
+                const uint4 x = i < nnz ? aval[i] : make_uint4(0u, 0u, 0u, 0u);
+                int round = 0;
+                int pos = base_id + block_exclusive_sum((int)popc4(x), blk, &round);
+                if (i < nnz) {
+                    const uint32_t q = aidx[i];
+                    const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        uint32_t bits = w4[t];
+                        while (bits) {
+                            const int b = __ffs(bits) - 1;
+                            bits &= bits - 1u;
+                            oid[pos++] = (4 * q + t) * 32 + b;
+                        }
+                    }
+                }
+                base_id += round;
+            }
+            __syncthreads();
+            const int G = (na + 31) >> 5;                  // restricted-column words
+            for (int unit = wib; unit < G * d.wm; unit += wpb) {
+                const int g = unit / d.wm, w = unit % d.wm;
+                const int pidx = 32 * g + (int)lane;
+                const uint32_t v = pidx < na ? __ldg(a.rows + (size_t)oid[pidx] * d.wm + w) : 0u;
+                uint32_t mine = 0;
+#pragma unroll
+                for (int b = 0; b < 32; ++b) {
+                    const uint32_t bal = __ballot_sync(FULL, (v >> b) & 1u);
+                    if (lane == (unsigned)b) mine = bal;
+                }
+                const int k = 32 * w + (int)lane;
+                if (k < d.m) colr[(size_t)k * G + g] = mine;
+            }
+            __syncthreads();
+            if (COUNT && threadIdx.x == 0) my_bytes += (unsigned long long)na * d.wm * 4;   // rows of A
+
+            for (int j = j_lo + wib; j < j_hi; j += wpb) {
+                if ((B[j >> 5] >> (j & 31)) & 1u) continue;   // saturation: A inside column j
+                ++my_closures;
+                uint32_t c[RPL];
+                unsigned cnt = 0;
+#pragma unroll
+                for (int r = 0; r < RPL; ++r) {
+                    const int g = 32 * r + (int)lane;
+                    c[r] = g < G ? colr[(size_t)j * G + g] : 0u;
+                    cnt += __popc(c[r]);
+                }
+                cnt = __reduce_add_sync(FULL, cnt);
+                if (cnt == 0) continue;   // empty extent: its closure is the bottom, added by the host
+
+                // the first object ids of C in ascending order: the closure is bounded by their rows and
+                // completed on the restricted columns
+                auto collect = [&](unsigned want) {
+                    unsigned got = 0;
+#pragma unroll
+                    for (int r = 0; r < RPL; ++r) {
+                        if (got >= want) break;
+                        const unsigned pc = __popc(c[r]);
+                        unsigned incl = pc;
+#pragma unroll
+                        for (int off = 1; off < 32; off <<= 1) {
+                            const unsigned t = __shfl_up_sync(FULL, incl, off);
+                            if (lane >= (unsigned)off) incl += t;
+                        }
+                        unsigned pos = got + incl - pc;
+                        uint32_t bits = c[r];
+                        const int g = 32 * r + (int)lane;
+                        while (bits && pos < want) {
+                            const int b = __ffs(bits) - 1;
+                            bits &= bits - 1u;
+                            rids[pos++] = oid[32 * g + b];
+                        }
+                        got += __shfl_sync(FULL, incl, 31);
+                    }
+                };
+                const unsigned need = cnt < (unsigned)ROW_BOUND ? cnt : (unsigned)ROW_BOUND;
+                collect(need);
+                __syncwarp();
+                finish_candidate<COUNT>(
+                    a, d, B, j, cnt, rids, need,
+                    [&](int k) {
+                        bool bad = false;
+#pragma unroll
+                        for (int r = 0; r < RPL; ++r) {
+                            const int g = 32 * r + (int)lane;
+                            if (g < G) bad |= (c[r] & ~colr[(size_t)k * G + g]) != 0u;
+                        }
+                        return !__any_sync(FULL, bad);
+                    },
+                    [&](uint32_t *dst) {
+                        for (int q = (int)lane; q < (int)d.wnp; q += 32) dst[q] = 0u;
+                        __syncwarp();
+#pragma unroll
+                        for (int r = 0; r < RPL; ++r) {
+                            uint32_t bits = c[r];
+                            const int g = 32 * r + (int)lane;
+                            while (bits) {
+                                const int b = __ffs(bits) - 1;
+                                bits &= bits - 1u;
+                                const uint32_t o = oid[32 * g + b];
+                                atomicOr(dst + (o >> 5), 1u << (o & 31));
+                            }
+                        }
+                    },
+                    [&]() { collect(cnt); },
+                    my_bytes);
+                __syncwarp();
+            }
+            continue;
+        }
+
+        // ---- gather path: candidates j of this part, warps in turn
+        for (int j = j_lo + wib; j < j_hi; j += wpb) {
+            if ((B[j >> 5] >> (j & 31)) & 1u) continue;   // saturation: A inside column j
+            ++my_closures;
+
+            // |C| for C = A & column j on the chunks of A (C itself is recomputed when needed)
+            const uint4 *J4 = cols4 + (size_t)j * wq;
+            unsigned cnt = 0;
+            for (int i = (int)lane; i < nnz; i += 32) {
+                const uint4 x = aval[i], cc = __ldg(J4 + aidx[i]);
+                if (COUNT) ++loads;
+                cnt += __popc(x.x & cc.x) + __popc(x.y & cc.y) + __popc(x.z & cc.z) + __popc(x.w & cc.w);
+            }
+            cnt = __reduce_add_sync(FULL, cnt);
+            if (cnt == 0) continue;   // empty extent: its closure is the bottom, added by the host
+
+            // object ids of C in ascending order: all of them when |C| <= SMALL_MAX, else the first 32
+            const unsigned need = cnt <= (unsigned)SMALL_MAX ? cnt : 32u;
+            unsigned got = 0;
+            for (int base = 0; base < nnz && got < need; base += 32) {
+                const int i = base + (int)lane;
+                uint4 x = make_uint4(0u, 0u, 0u, 0u);
+                uint32_t q = 0u;
+                if (i < nnz) {
+                    const uint4 av = aval[i];
+                    q = aidx[i];
+                    const uint4 cc = __ldg(J4 + q);
+                    if (COUNT) ++loads;
+                    x = make_uint4(av.x & cc.x, av.y & cc.y, av.z & cc.z, av.w & cc.w);
+                }
+                const unsigned pc = popc4(x);
+                unsigned incl = pc;
+#pragma unroll
+                for (int off = 1; off < 32; off <<= 1) {
+                    const unsigned t = __shfl_up_sync(FULL, incl, off);
+                    if (lane >= (unsigned)off) incl += t;
+                }
+                unsigned pos = got + incl - pc;
+                const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    uint32_t bits = w4[t];
+                    while (bits && pos < need) {
+                        const int b = __ffs(bits) - 1;
+                        bits &= bits - 1u;
+                        gids[pos++] = (uint32_t)((4 * q + t) * 32 + b);
+                    }
+                }
+                got += __shfl_sync(FULL, incl, 31);
+            }
+            __syncwarp();
+            finish_candidate<COUNT>(
+                a, d, B, j, cnt, gids, need,
+                [&](int k) { return subset_of_column(aval, aidx, nnz, J4, cols4 + (size_t)k * wq, lane, loads); },
+                [&](uint32_t *dst) {
+                    uint4 *dst4 = reinterpret_cast<uint4 *>(dst);
+                    for (int q = (int)lane; q < wq; q += 32) dst4[q] = make_uint4(0u, 0u, 0u, 0u);
+                    __syncwarp();
+                    for (int i = (int)lane; i < nnz; i += 32) {
+                        const uint4 av = aval[i], cc = __ldg(J4 + aidx[i]);
+                        const uint4 x = make_uint4(av.x & cc.x, av.y & cc.y, av.z & cc.z, av.w & cc.w);
+                        if (x.x | x.y | x.z | x.w) dst4[aidx[i]] = x;
+                    }
+                },
+                [&]() {},
+                my_bytes);
+            __syncwarp();
+        }
+    }
+    if (COUNT) {
+        const unsigned tl = __reduce_add_sync(FULL, loads);
+        if (lane == 0) atomicAdd(&a.ctr->bytes, my_bytes + 16ull * tl);
+    }
+    if (lane == 0 && my_closures) atomicAdd(&a.ctr->closures, my_closures);
+}
+
+}  // namespace
+
+size_t expand_smem_per_warp(const Dims &d) { return ExpandLayout(d, 1, 0).bytes; }
+
+template <bool COUNT>
+static int launch_expand_t(const ExpandArgs &a, int sm_count, void *stream)
+{
+    int wpb = WARPS_PER_BLOCK;
+    while (wpb > 1 && ExpandLayout(a.d, wpb, 0).bytes > 200 * 1024) --wpb;
+    // the largest restricted extent whose columns fit in the shared memory of three blocks per SM
+    // (or next to the gather path's own, when that is larger)
+    const size_t budget = std::max<size_t>(ExpandLayout(a.d, wpb, 0).bytes, 72 * 1024);
+    int tr = RESTRICT_CAP;
+    while (tr > 0 && ExpandLayout(a.d, wpb, tr).bytes > budget) tr -= 32;
+    const size_t smem = ExpandLayout(a.d, wpb, tr).bytes;
+    // the shared-memory attribute and the occupancy query, once per device and size (per thread)
+    static thread_local ShapeCache cache;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cache.dev != dev || cache.smem != smem || cache.wpb != wpb) {
+        if (smem > 48 * 1024) {
+            cudaError_t e = cudaFuncSetAttribute(expand_bitmap_kernel<COUNT>,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return (int)e;
+        }
+        int ps = 0;
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ps, expand_bitmap_kernel<COUNT>, wpb * 32, smem);
+        cache = ShapeCache{dev, smem, wpb, ps < 1 ? 1 : ps};
+    }
+    const int per_sm = cache.per_sm;
+    // split each parent's attribute range into parts when there are too few parents to fill the GPU
+    // (at least one candidate per warp in every part)
+    ExpandArgs b = a;
+    b.restrict_max = tr;
+    const unsigned long long resident = (unsigned long long)sm_count * per_sm;
+    const unsigned long long pc = std::max<unsigned long long>(1, a.p_count);
+    const int max_parts = std::max(1, a.d.m / wpb);
+    b.parts = (int)std::min<unsigned long long>(max_parts, std::max<unsigned long long>(1, (2 * resident + pc - 1) / pc));
+    const unsigned long long items = a.p_count * (unsigned long long)b.parts;
+    unsigned long long blocks = std::min<unsigned long long>(items, resident * 2);
+    if (blocks < 1) blocks = 1;
+    expand_bitmap_kernel<COUNT><<<(unsigned)blocks, wpb * 32, smem, (cudaStream_t)stream>>>(b);
+    return (int)cudaGetLastError();
+}
+
+int launch_expand(const ExpandArgs &a, int sm_count, void *stream)
+{
+    return a.count_work ? launch_expand_t<true>(a, sm_count, stream) : launch_expand_t<false>(a, sm_count, stream);
+}
+
+}  // namespace fca

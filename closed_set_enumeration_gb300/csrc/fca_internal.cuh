@@ -100,7 +100,8 @@ struct SubtreeArgs {
     int count_work;         // 1: accumulate Counters::word_ops
 };
 
-// Launch wrappers (defined in fca_kernels.cu). Each returns a cudaError_t value.
+// Launch wrappers (defined in fca_context.cu, fca_expand.cu and fca_subtree.cu). Each returns a
+// cudaError_t value.
 int launch_mask_rows(uint32_t *rows, const Dims &d, void *stream);
 int launch_transpose(const uint32_t *rows, uint32_t *cols, const Dims &d, void *stream);
 int launch_top(const uint32_t *rows, uint32_t *top, uint32_t *flag_full_row, const Dims &d,
