@@ -14,6 +14,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cstddef>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -342,9 +343,12 @@ fca_status drain(Run &r, size_t lv)
 
         // the next level appends after its current fill; the counters as they are now are kept on
         // the device, to be restored if the launch has to be rolled back
+        // (next_count and the launch's work cursor are adjacent: one copy sets both)
         uint64_t *next_fill = reinterpret_cast<uint64_t *>(c->stage + 1000);
-        *next_fill = c->level_count[lv + 1];
-        CK(cudaMemcpyAsync(&c->ctr->next_count, next_fill, sizeof(uint64_t), cudaMemcpyHostToDevice, r.st),
+        next_fill[0] = c->level_count[lv + 1];
+        next_fill[1] = 0;
+        static_assert(offsetof(Counters, work_head) == offsetof(Counters, next_count) + 8, "counter order");
+        CK(cudaMemcpyAsync(&c->ctr->next_count, next_fill, 2 * sizeof(uint64_t), cudaMemcpyHostToDevice, r.st),
            "counter set");
         CK(cudaMemsetAsync(&c->ctr->error, 0, sizeof(unsigned int), r.st), "counter set");
         CK(cudaMemcpyAsync(c->ctr_snap, c->ctr, sizeof(Counters), cudaMemcpyDeviceToDevice, r.st),

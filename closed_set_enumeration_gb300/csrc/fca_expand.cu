@@ -222,7 +222,15 @@ __global__ void __launch_bounds__(256) expand_bitmap_kernel(ExpandArgs a)
     const int parts = a.parts;
     const int span = (d.m + parts - 1) / parts;
     const unsigned long long items = a.p_count * (unsigned long long)parts;
-    for (unsigned long long item = blockIdx.x; item < items; item += gridDim.x) {
+    __shared__ unsigned long long next_item;
+    for (;;) {
+        // work items are dealt one at a time from a launch-wide cursor, so the blocks that draw
+        // large parents do not hold back the rest
+        __syncthreads();
+        if (threadIdx.x == 0) next_item = atomicAdd(&a.ctr->work_head, 1ull);
+        __syncthreads();
+        const unsigned long long item = next_item;
+        if (item >= items) break;
         const unsigned long long p = a.p_begin + item / (unsigned)parts;
         const int part = (int)(item % (unsigned)parts);
         const int y = a.in.y[p];
@@ -487,7 +495,7 @@ static int launch_expand_t(const ExpandArgs &a, int sm_count, void *stream)
     const int max_parts = std::max(1, a.d.m / wpb);
     b.parts = (int)std::min<unsigned long long>(max_parts, std::max<unsigned long long>(1, (2 * resident + pc - 1) / pc));
     const unsigned long long items = a.p_count * (unsigned long long)b.parts;
-    unsigned long long blocks = std::min<unsigned long long>(items, resident * 2);
+    unsigned long long blocks = std::min<unsigned long long>(items, resident);
     if (blocks < 1) blocks = 1;
     expand_bitmap_kernel<COUNT><<<(unsigned)blocks, wpb * 32, smem, (cudaStream_t)stream>>>(b);
     return (int)cudaGetLastError();

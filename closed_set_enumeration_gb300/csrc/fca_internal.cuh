@@ -37,6 +37,7 @@ struct Counters {
     unsigned long long out_count;      // intents emitted so far (row index allocator)
     unsigned long long closures;       // candidates evaluated
     unsigned long long next_count;     // entries appended to the next bitmap level
+    unsigned long long work_head;      // work-distribution cursor of the bitmap-tier launch
     unsigned long long q_count[NQ];    // entries appended to the object-list queues
     unsigned long long q_head[NQ];     // work-distribution cursors of the subtree kernels
     unsigned long long word_ops;       // counted object-list-tier word operations (when counting)
