@@ -56,6 +56,10 @@ struct fca_ctx {
     int count_work = 0;
     uint64_t table_launches = 0;    // kernels launched by the last table load
 
+    // a second stream for the object-list launch that runs beside the other one
+    cudaStream_t side = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+
     // device timing of kernel launches: event pairs recorded around each launch
     std::vector<cudaEvent_t> events;
     std::vector<int> event_kind;    // per pair: 0 = expand, 1 = subtree
@@ -252,7 +256,7 @@ struct Run {
 };
 
 // Record the start event of a timed launch; returns the pair index.
-fca_status time_begin(Run &r, int kind, size_t *pair)
+fca_status time_begin(Run &r, int kind, size_t *pair, cudaStream_t st)
 {
     fca_ctx *c = r.c;
     if (c->pairs_used == c->event_kind.size()) {
@@ -265,14 +269,14 @@ fca_status time_begin(Run &r, int kind, size_t *pair)
     }
     *pair = c->pairs_used++;
     c->event_kind[*pair] = kind;
-    CK(cudaEventRecord(c->events[2 * *pair], r.st), "cudaEventRecord");
+    CK(cudaEventRecord(c->events[2 * *pair], st), "cudaEventRecord");
     return FCA_OK;
 }
 
-fca_status time_end(Run &r, size_t pair)
+fca_status time_end(Run &r, size_t pair, cudaStream_t st)
 {
     fca_ctx *c = r.c;
-    CK(cudaEventRecord(c->events[2 * pair + 1], r.st), "cudaEventRecord");
+    CK(cudaEventRecord(c->events[2 * pair + 1], st), "cudaEventRecord");
     return FCA_OK;
 }
 
@@ -298,8 +302,8 @@ fca_status read_counters(Run &r)
     return FCA_OK;
 }
 
-// Process every root waiting in object-list queue qi, then empty it.
-fca_status run_subtree(Run &r, int qi)
+// Process every root waiting in object-list queue qi, then empty it; all on stream `st`.
+fca_status run_subtree(Run &r, int qi, cudaStream_t st)
 {
     fca_ctx *c = r.c;
     if (c->q_count[qi] == 0) return FCA_OK;
@@ -316,15 +320,15 @@ fca_status run_subtree(Run &r, int qi)
     a.ctr = c->ctr;
     a.count_work = c->count_work;
     size_t pair = 0;
-    if ((s = time_begin(r, 1, &pair)) != FCA_OK) return s;
-    CK((cudaError_t)launch_subtree(a, nw, c->sm_count, r.st), "subtree kernel launch");
-    if ((s = time_end(r, pair)) != FCA_OK) return s;
+    if ((s = time_begin(r, 1, &pair, st)) != FCA_OK) return s;
+    CK((cudaError_t)launch_subtree(a, nw, c->sm_count, st), "subtree kernel launch");
+    if ((s = time_end(r, pair, st)) != FCA_OK) return s;
     c->stats.launches++;
     c->stats.subtree_launches++;
     c->stats.small_roots += c->q_count[qi];
     // empty the queue: its append counter and its work cursor
-    CK(cudaMemsetAsync(&c->ctr->q_count[qi], 0, sizeof(unsigned long long), r.st), "queue reset");
-    CK(cudaMemsetAsync(&c->ctr->q_head[qi], 0, sizeof(unsigned long long), r.st), "queue reset");
+    CK(cudaMemsetAsync(&c->ctr->q_count[qi], 0, sizeof(unsigned long long), st), "queue reset");
+    CK(cudaMemsetAsync(&c->ctr->q_head[qi], 0, sizeof(unsigned long long), st), "queue reset");
     c->q_count[qi] = 0;
     return FCA_OK;
 }
@@ -368,9 +372,9 @@ fca_status drain(Run &r, size_t lv)
         a.ctr = c->ctr;
         a.count_work = c->count_work;
         size_t pair = 0;
-        if ((s = time_begin(r, 0, &pair)) != FCA_OK) return s;
+        if ((s = time_begin(r, 0, &pair, r.st)) != FCA_OK) return s;
         CK((cudaError_t)launch_expand(a, c->sm_count, r.st), "expand kernel launch");
-        if ((s = time_end(r, pair)) != FCA_OK) return s;
+        if ((s = time_end(r, pair, r.st)) != FCA_OK) return s;
         c->stats.launches++;
         c->stats.expand_launches++;
         if ((s = read_counters(r)) != FCA_OK) return s;
@@ -385,7 +389,7 @@ fca_status drain(Run &r, size_t lv)
             for (int qi = 0; qi < NQ; ++qi) {
                 if (!(after.error & (ERR_QUEUE0 << qi))) continue;
                 const uint64_t need = after.q_count[qi] - c->q_count[qi];
-                if ((s = run_subtree(r, qi)) != FCA_OK) return s;
+                if ((s = run_subtree(r, qi, r.st)) != FCA_OK) return s;
                 if (need > c->q[qi].cap) {
                     s = grow_queue(c, qi, need);
                     if (s == FCA_ERR_CAPACITY) limited = true;
@@ -489,8 +493,20 @@ fca_status enumerate_impl(fca_ctx *c, uint32_t *out, uint64_t capacity, uint64_t
     CK(cudaMemcpyAsync(c->ctr, c->ctr_host, sizeof(Counters), cudaMemcpyHostToDevice, st), "counter write");
 
     if ((s = drain(r, 0)) != FCA_OK) return s;
-    for (int qi = 0; qi < NQ; ++qi)
-        if ((s = run_subtree(r, qi)) != FCA_OK) return s;
+    // The two queues are independent. The larger extents run first on the caller's stream; the
+    // smaller ones on a side stream, so their blocks take the SMs that the last long subtrees of the
+    // first launch leave idle. The caller's stream waits for both.
+    if (c->q_count[0] > 0 && c->q_count[1] > 0) {
+        CK(cudaEventRecord(c->fork, st), "cudaEventRecord");
+        CK(cudaStreamWaitEvent(c->side, c->fork, 0), "cudaStreamWaitEvent");
+        if ((s = run_subtree(r, 1, st)) != FCA_OK) return s;
+        if ((s = run_subtree(r, 0, c->side)) != FCA_OK) return s;
+        CK(cudaEventRecord(c->join, c->side), "cudaEventRecord");
+        CK(cudaStreamWaitEvent(st, c->join, 0), "cudaStreamWaitEvent");
+    } else {
+        for (int qi = NQ - 1; qi >= 0; --qi)
+            if ((s = run_subtree(r, qi, st)) != FCA_OK) return s;
+    }
     // The bottom concept (M', M). When some object holds every attribute its extent is not empty and
     // the search reaches it. Otherwise only empty candidate extents close to it; the search skips
     // those, and it is appended here (a concept is output exactly once either way).
@@ -532,6 +548,9 @@ void fca_free(fca_ctx *ctx)
     cudaFree(ctx->root_ext);
     free_pools(ctx);
     for (cudaEvent_t e : ctx->events) cudaEventDestroy(e);
+    if (ctx->fork) cudaEventDestroy(ctx->fork);
+    if (ctx->join) cudaEventDestroy(ctx->join);
+    if (ctx->side) cudaStreamDestroy(ctx->side);
     cudaFree(ctx->ctr);
     cudaFree(ctx->ctr_snap);
     cudaFree(ctx->host_out_dev);
@@ -582,6 +601,12 @@ fca_status fca_context_create(const uint32_t *rows, int64_t n_objects, int32_t n
         cudaGetLastError();
         c->err = "pinned host allocation failed";
         return fail(FCA_ERR_OOM);
+    }
+    if ((e = cudaStreamCreateWithFlags(&c->side, cudaStreamNonBlocking)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&c->fork, cudaEventDisableTiming)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&c->join, cudaEventDisableTiming)) != cudaSuccess) {
+        cuda_fail(c, e, "stream set-up");
+        return fail(FCA_ERR_CUDA);
     }
 
     // host-side constants: the all-attribute intent and the all-object extent

@@ -243,7 +243,10 @@ __global__ void __launch_bounds__(256) expand_bitmap_kernel(ExpandArgs a)
         const int j_lo = restricted ? y : max(y, part * span);
         const int j_hi = restricted ? d.m : min(d.m, (part + 1) * span);
         if (j_lo >= j_hi) continue;                       // uniform over the block
-        const uint32_t *B = a.in.itt + p * d.wm;
+        // the parent intent, read by every candidate, in shared memory
+        __shared__ uint32_t sB[MAX_ATTRS / 32];
+        if ((int)threadIdx.x < d.wm) sB[threadIdx.x] = a.in.itt[p * d.wm + threadIdx.x];
+        const uint32_t *B = sB;
 
         // ---- stage the non-zero chunks of A in order (block-wide compaction), and |A|
         const uint4 *A4 = ext4 + p * wq;

@@ -347,11 +347,24 @@ __global__ void __launch_bounds__(256, RW > 4 ? 3 : 4) subtree_kernel(SubtreeArg
     const int mp = L.mp, WM = d.wm, PER = 32 * NW;
 
     const unsigned long long items = a.q_count * (unsigned long long)a.slices;
+    // Guided self-scheduling: a warp claims a run of consecutive items with one atomic, a quarter of
+    // its share of what was left at its last claim (so claims shrink to single items near the end),
+    // which keeps the launch-wide cursor from becoming a hot spot when items are short.
+    const unsigned long long nwarps = (unsigned long long)gridDim.x * (blockDim.x >> 5);
+    unsigned long long next = 0, end = 0, seen = 0;
     for (;;) {
-        unsigned long long item = 0;
-        if (lane == 0) item = atomicAdd(&a.ctr->q_head[a.q_index], 1ull);
-        item = __shfl_sync(FULL, item, 0);
-        if (item >= items) break;
+        if (next >= end) {
+            unsigned long long base = 0;
+            const unsigned long long left = items > seen ? items - seen : 0;
+            const unsigned long long k = min(32ull, max(1ull, left / (4 * nwarps)));
+            if (lane == 0) base = atomicAdd(&a.ctr->q_head[a.q_index], k);
+            base = __shfl_sync(FULL, base, 0);
+            if (base >= items) break;
+            next = base;
+            end = min(items, base + k);
+            seen = base + k;
+        }
+        const unsigned long long item = next++;
         // work item = (root, slice): the slice takes the root's children j with j % slices == slice
         const unsigned long long r = item / (unsigned)a.slices;
         const int slice = (int)(item % (unsigned)a.slices);
