@@ -268,6 +268,86 @@ def probe_peaks():
     return out
 
 
+WORK_FILE = os.path.join(ROOT, "tests", "golden", "work_counts.json")
+
+
+def load_work_counts(workload: str):
+    """Per-tier algorithmic work of a workload, written by tests/golden/make_work_counts.py."""
+    try:
+        return json.load(open(WORK_FILE))[workload]["tiers"]
+    except (OSError, ValueError, KeyError):
+        return None
+
+
+def roofline_of(workload, sub_ms, exp_ms, last, counted, probes, peaks, sm_count, sm_max):
+    """Roofline of the kernel with the larger device time per step.
+
+    The numerator is the algorithmic work of that kernel's tier (parents of at most 64 objects run
+    in subtree_kernel, larger ones in expand_bitmap_kernel), counted exactly by the CPU counting
+    pass: HBM words (extent reads, frontier and output writes), L2 words (extent intersections and
+    the cheaper closure route) and word operations. The bound is the slowest of HBM bytes at the
+    measured copy bandwidth, HBM + L2 bytes at the L2 read bandwidth probed in this run, and word
+    operations at the int32 issue rate (SMs x 64 lanes x maximum SM clock). achieved / peak is the
+    bound's time over the measured kernel time. Without stored counts for the workload, the kernel's
+    own counted work (the counting launch) stands in, and `basis` says so.
+    """
+    sub = sub_ms >= exp_ms
+    kernel = "subtree_kernel" if sub else "expand_bitmap_kernel"
+    tier = "list" if sub else "bitmap"
+    kms = sub_ms if sub else exp_ms
+    nl = max(1, last["subtree_launches"] if sub else last["expand_launches"])
+    avg_ms = kms / nl
+    hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
+    hbm_basis = "MEASURED_PEAKS.json hbm_gbs" if "hbm_gbs" in peaks else "fallback 6.8 TB/s"
+    l2_peak = probes.get("l2_read_gbs") or hbm_peak
+    int_peak = sm_count * INT_LANES_PER_SM * sm_max * 1e6 / 1e9   # Gop/s
+    out = {"kernel": kernel, "avg_launch_ms": avg_ms, "launches_per_step": nl,
+           "traffic": profile_traffic(kernel, workload)}
+    work = load_work_counts(workload)
+    if work is not None:
+        t = work[tier]
+        hbm_b = 4.0 * t["hbm_words"]
+        l2_b = 4.0 * (t["isect_words"] + t["closure_words"])
+        ops = t["isect_words"] + t["closure_words"] + t["canon_words"]
+        times = {"hbm": hbm_b / (hbm_peak * 1e9), "l2": (hbm_b + l2_b) / (l2_peak * 1e9),
+                 "alu": ops / (int_peak * 1e9)}
+        bound = max(times, key=times.get)
+        if bound == "alu":
+            per_launch, unit, peak, basis = ops / nl, "Gop/s", int_peak, \
+                f"{sm_count} SMs x {INT_LANES_PER_SM} int32 lanes x {sm_max:.0f} MHz"
+        elif bound == "hbm":
+            per_launch, unit, peak, basis = hbm_b / nl, "GB/s", hbm_peak, hbm_basis
+        else:
+            per_launch, unit, peak, basis = (hbm_b + l2_b) / nl, "GB/s", l2_peak, \
+                "L2 read probe in this run (16 MiB buffer re-read)"
+        achieved = per_launch / (avg_ms * 1e-3) / 1e9
+        out.update({"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
+                    "frac": achieved / peak, "peak_basis": basis,
+                    "per_launch": per_launch, "basis": "algorithmic work of the tier (oracle/workcount.c)",
+                    "units_per_step": {"parents": t["parents"], "closures": t["closures"],
+                                       "children": t["children"]},
+                    "bound_ms": {k: v * 1e3 for k, v in times.items()}})
+    elif sub:
+        per_launch = counted["subtree_word_ops"] / max(1, counted["subtree_launches"])
+        achieved = per_launch / (avg_ms * 1e-3) / 1e9
+        out.update({"bound": "alu", "achieved": achieved, "peak": int_peak, "unit": "Gop/s",
+                    "frac": achieved / int_peak, "per_launch": per_launch,
+                    "peak_basis": f"{sm_count} SMs x {INT_LANES_PER_SM} int32 lanes x {sm_max:.0f} MHz",
+                    "basis": "word operations counted by the kernel (counting launch)"})
+    else:
+        per_launch = counted["expand_bytes"] / max(1, counted["expand_launches"])
+        achieved = per_launch / (avg_ms * 1e-3) / 1e9
+        out.update({"bound": "l2", "achieved": achieved, "peak": l2_peak, "unit": "GB/s",
+                    "frac": achieved / l2_peak, "per_launch": per_launch,
+                    "peak_basis": "L2 read probe in this run (16 MiB buffer re-read)",
+                    "basis": "bytes counted by the kernel (counting launch)"})
+    # the kernel's own counted work, for reference
+    out["kernel_counted"] = {"subtree_word_ops": counted["subtree_word_ops"],
+                             "expand_bytes": counted["expand_bytes"]}
+    out["probe_lop3_gops"] = probes.get("lop3_gops")
+    return out
+
+
 # ----------------------------------------------------------------------------- our arm
 
 def run_ours(args, world, rank, local):
@@ -361,27 +441,7 @@ def run_ours(args, world, rank, local):
     sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
     sm_max = float(peaks.get("sm_max_mhz", 2070.0))
     steps = args.steps
-    if sub_ms >= exp_ms:
-        per_launch_ops = counted["subtree_word_ops"] / max(1, counted["subtree_launches"])
-        avg_ms = sub_ms / max(1, steps * max(1, last["subtree_launches"]))
-        achieved = per_launch_ops / (avg_ms * 1e-3) / 1e9
-        peak = sm_count * INT_LANES_PER_SM * sm_max * 1e6 / 1e9
-        roofline = {"kernel": "subtree_kernel", "bound": "alu", "achieved": achieved, "peak": peak,
-                    "unit": "Gop/s", "frac": achieved / peak, "traffic": profile_traffic("subtree_kernel", w.name),
-                    "peak_basis": f"{sm_count} SMs x {INT_LANES_PER_SM} int32 lanes x {sm_max:.0f} MHz",
-                    "probe_lop3_gops": probes.get("lop3_gops"),
-                    "word_ops_per_launch": per_launch_ops, "avg_launch_ms": avg_ms}
-    else:
-        per_launch = counted["expand_bytes"] / max(1, counted["expand_launches"])
-        avg_ms = exp_ms / max(1, steps * max(1, last["expand_launches"]))
-        achieved = per_launch / (avg_ms * 1e-3) / 1e9
-        peak = probes.get("l2_read_gbs") or float(peaks.get("hbm_gbs", 6800.0))
-        roofline = {"kernel": "expand_bitmap_kernel", "bound": "l2", "achieved": achieved, "peak": peak,
-                    "unit": "GB/s", "frac": achieved / peak,
-                    "traffic": profile_traffic("expand_bitmap_kernel", w.name),
-                    "peak_basis": "L2 read probe (16 MiB buffer read 8 times) in this run" if probes.get("l2_read_gbs")
-                    else "measured HBM copy bandwidth",
-                    "bytes_per_launch": per_launch, "avg_launch_ms": avg_ms}
+    roofline = roofline_of(w.name, sub_ms / steps, exp_ms / steps, last, counted, probes, peaks, sm_count, sm_max)
 
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,

@@ -13,7 +13,11 @@ Contents:
   * :func:`brute_force_by_objects` derives every object subset (N <= 16);
   * :func:`derive_extent`,
     :func:`derive_intent`   the two derivation operators on packed bitmaps,
-                            written with numpy for spot checks at any size.
+                            written with numpy for spot checks at any size;
+  * ``workcount``           a separate counting pass (``workcount.c``) that counts
+                            the algorithmic work of the enumeration in 32-bit
+                            words, the numerator of the benchmark's roofline
+                            (read from the stored ``tests/golden/work_counts.json``).
 
 Every pin that ties these to the pages' definitions lives in ``tests/``.
 """

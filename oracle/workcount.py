@@ -1,0 +1,64 @@
+"""ctypes binding of the work-counting pass in ``workcount.c`` (test and measurement infrastructure).
+
+``workcount(rows, n, m)`` returns, per tier, the algorithmic work of enumerating the context in
+32-bit words: the units and the per-unit counts that the roofline uses (see the header of
+``workcount.c``). Tier ``"list"`` holds the parents with at most 64 objects, tier ``"bitmap"`` the
+larger ones.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from typing import Dict, Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "workcount.c")
+_LIB_PATH = os.path.join(_HERE, "libworkcount.so")
+_lock = threading.Lock()
+_lib: Optional[ctypes.CDLL] = None
+
+FIELDS = ("parents", "closures", "children", "isect_words", "closure_words", "canon_words", "hbm_words")
+TIERS = ("list", "bitmap")
+
+
+def build(force: bool = False) -> str:
+    """Compile ``workcount.c`` with gcc into a shared library (portable flags only)."""
+    if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", _SRC, "-o", tmp], check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load() -> ctypes.CDLL:
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB_PATH)
+            lib.workcount.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int,
+                                      ctypes.POINTER(ctypes.c_uint64)]
+            lib.workcount.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def workcount(rows: np.ndarray, n_objects: int, n_attrs: int, threads: int = 1) -> Dict[str, Dict[str, int]]:
+    """Per-tier work counts of enumerating ``rows`` (``N x ceil(M/32)`` uint32, LSB-first)."""
+    rows = np.ascontiguousarray(rows, dtype=np.uint32)
+    out = (ctypes.c_uint64 * 14)()
+    st = _load().workcount(rows.ctypes.data, int(n_objects), int(n_attrs), int(threads), out)
+    if st != 0:
+        raise RuntimeError("workcount failed")
+    return {t: {f: int(out[7 * i + k]) for k, f in enumerate(FIELDS)} for i, t in enumerate(TIERS)}
+
+
+def derived(counts: Dict[str, int]) -> Dict[str, int]:
+    """Words read from L2 (intersection and closure), word operations, and HBM words of one tier."""
+    l2 = counts["isect_words"] + counts["closure_words"]
+    return {"l2_words": l2, "ops": l2 + counts["canon_words"], "hbm_words": counts["hbm_words"]}
