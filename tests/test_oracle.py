@@ -325,3 +325,23 @@ def test_planted_mistake_is_caught(mutant):
         assert _quick_pins(lib) is not None, f"mutant {mutant} passed every pin"
     finally:
         shutil.rmtree(tmp, ignore_errors=True)
+
+
+@pytest.mark.parametrize("n,m,p,seed", [(60, 10, 0.35, 3), (120, 14, 0.3, 4), (200, 9, 0.5, 5)])
+def test_slice_identity_behind_the_full_size_checks(n, m, p, seed):
+    """The intents containing S are the intents of the sub-context of the objects holding S (the
+    identity the full-size slice checks rest on), on contexts small enough to enumerate whole."""
+    rows = cx.random_context(n, m, p, seed)
+    whole = oracle.cbo(rows, n, m)["intents"]
+    for a in range(m):
+        for b in (a, (a + 3) % m):
+            mask = np.zeros(1, dtype=np.uint32)
+            mask[0] = (1 << a) | (1 << b)
+            inside = whole[(whole[:, 0] & mask[0]) == mask[0]]
+            ext = oracle.derive_extent(rows, mask)
+            sub = np.ascontiguousarray(rows[ext])
+            if sub.shape[0] == 0:
+                assert inside.shape[0] == 1      # only the bottom (every attribute) contains S
+                continue
+            ref = oracle.cbo(sub, sub.shape[0], m)["intents"]
+            assert same_set(inside, ref)
