@@ -45,14 +45,17 @@ __device__ __forceinline__ bool subset_of_column(const uint4 *av, const uint32_t
 constexpr int RESTRICT_CAP = 4096;
 constexpr int RPL = RESTRICT_CAP / 1024;   // restricted-column words per lane
 constexpr int ROW_BOUND = 8;               // rows ANDed for the closure's upper bound (restricted path)
+constexpr int ROWS_KEPT = 256;             // restricted extents up to this size keep their rows in shared memory
 
 // Shared memory of expand_bitmap_kernel. Both paths first stage the parent's non-zero extent
 // chunks (uint4 index and value). The gather path then keeps, per warp, up to SMALL_MAX object
 // ids (C itself is recomputed from the staged chunks and column j when needed); the restricted
 // path keeps the parent's object list, its columns restricted to those objects (M x TR/32 words)
-// and per-warp object ids.
+// and per-warp positions in that list; parents of at most min(TR, ROWS_KEPT) objects also keep
+// their rows (positions x W_M words).
 struct ExpandLayout {
-    size_t o_aidx, o_aval, o_wbase, per_warp, o_oid, o_colr, o_rids, o_blk, bytes;
+    size_t o_aidx, o_aval, o_wbase, per_warp, o_oid, o_colr, o_rowr, o_rids, o_blk, bytes;
+    int rk;   // rows kept: largest restricted extent whose rows are in shared memory
     __host__ __device__ ExpandLayout(const Dims &d, int wpb, int tr)
     {
         const size_t wq = (size_t)(d.wnp >> 2);
@@ -63,7 +66,9 @@ struct ExpandLayout {
         const size_t gather_end = o_wbase + per_warp * wpb;
         o_oid = o_wbase;                                   // tr uint32
         o_colr = o_oid + (size_t)tr * 4;                   // m x tr/32 uint32
-        o_rids = o_colr + (size_t)d.m * (size_t)(tr / 32) * 4;
+        rk = tr < ROWS_KEPT ? tr : ROWS_KEPT;
+        o_rowr = o_colr + (size_t)d.m * (size_t)(tr / 32) * 4;     // rk x wm uint32
+        o_rids = o_rowr + (size_t)rk * (size_t)d.wm * 4;
         const size_t restrict_end = o_rids + (size_t)wpb * SMALL_MAX * 4;
         o_blk = ((gather_end > restrict_end ? gather_end : restrict_end) + 15) & ~(size_t)15;
         bytes = o_blk + 32 * 4;                            // block scratch: counts and sums
@@ -95,15 +100,16 @@ __device__ __forceinline__ int block_exclusive_sum(int v, int *scratch, int *tot
     return before + incl - v;
 }
 
-// The rest of a candidate once |C| and the first `need` object ids of C are known: the closure
+// The rest of a candidate once |C| and the first `need` objects of C are known: the closure
 // (the AND of their rows: exact when need == |C|, else an upper bound whose extra attributes are
 // decided by `subset(k)` in ascending order, so a violation below j ends the candidate early),
-// the canonical test, the intent and the child. `write_ext(dst)` writes C as a dense bitmap for a
-// child of the next level; `all_ids()` completes the id list of a small child (need < |C|).
-template <bool COUNT, class Subset, class WriteExt, class AllIds>
+// the canonical test, the intent and the child. `row_word(i, w)` is word w of the row of the i-th
+// object of C and `obj_id(i)` its object id; `write_ext(dst)` writes C as a dense bitmap for a
+// child of the next level; `all_ids()` completes the list of a small child (need < |C|).
+template <bool COUNT, class RowWord, class ObjId, class Subset, class WriteExt, class AllIds>
 __device__ __forceinline__ void finish_candidate(const ExpandArgs &a, const Dims &d, const uint32_t *B, int j,
-                                                 unsigned cnt, const uint32_t *ids, unsigned need, Subset &&subset,
-                                                 WriteExt &&write_ext, AllIds &&all_ids,
+                                                 unsigned cnt, unsigned need, RowWord &&row_word, ObjId &&obj_id,
+                                                 Subset &&subset, WriteExt &&write_ext, AllIds &&all_ids,
                                                  unsigned long long &my_bytes)
 {
     const unsigned lane = threadIdx.x & 31;
@@ -115,7 +121,7 @@ __device__ __forceinline__ void finish_candidate(const ExpandArgs &a, const Dims
     uint32_t U = FULL;
     if (my_w < d.wm)
         for (unsigned pidx = lane; pidx < need * (unsigned)w2; pidx += 32)
-            U &= __ldg(a.rows + (size_t)ids[pidx / (unsigned)w2] * d.wm + my_w);
+            U &= row_word(pidx / (unsigned)w2, my_w);
     for (int sft = w2; sft < 32; sft <<= 1) U &= __shfl_xor_sync(FULL, U, sft);
     if ((int)lane >= d.wm) U = 0u;
     if (COUNT && lane == 0) my_bytes += (unsigned long long)need * d.wm * 4;   // rows read
@@ -173,7 +179,7 @@ __device__ __forceinline__ void finish_candidate(const ExpandArgs &a, const Dims
         }
         if (need < cnt) all_ids();
         __syncwarp();
-        for (int i = (int)lane; i < per; i += 32) Q.ids[s * per + i] = i < (int)cnt ? ids[i] : 0u;
+        for (int i = (int)lane; i < per; i += 32) Q.ids[s * per + i] = i < (int)cnt ? obj_id((unsigned)i) : 0u;
         if (lane < (unsigned)d.wm) Q.itt[s * d.wm + lane] = Dw;
         if (lane == 0) { Q.y[s] = j + 1; Q.n[s] = (int)cnt; }
     } else {
@@ -197,7 +203,7 @@ __device__ __forceinline__ void finish_candidate(const ExpandArgs &a, const Dims
 // global column access. Larger extents keep the chunk list: each warp gathers column j on the
 // parent's non-zero chunks. Either way the warps of the block take the part's candidates j in turn.
 template <bool COUNT>
-__global__ void __launch_bounds__(256) expand_bitmap_kernel(ExpandArgs a)
+__global__ void __launch_bounds__(256, 3) expand_bitmap_kernel(ExpandArgs a)
 {
     extern __shared__ __align__(16) unsigned char smem[];
     const Dims d = a.d;
@@ -212,6 +218,7 @@ __global__ void __launch_bounds__(256) expand_bitmap_kernel(ExpandArgs a)
     uint32_t *gids = reinterpret_cast<uint32_t *>(smem + L.o_wbase + L.per_warp * wib);
     uint32_t *oid = reinterpret_cast<uint32_t *>(smem + L.o_oid);
     uint32_t *colr = reinterpret_cast<uint32_t *>(smem + L.o_colr);
+    uint32_t *rowr = reinterpret_cast<uint32_t *>(smem + L.o_rowr);
     uint32_t *rids = reinterpret_cast<uint32_t *>(smem + L.o_rids) + (size_t)wib * SMALL_MAX;
     int *blk = reinterpret_cast<int *>(smem + L.o_blk);   // [0..31] scan scratch
     const uint4 *cols4 = reinterpret_cast<const uint4 *>(a.cols);
@@ -292,10 +299,12 @@ __global__ void __launch_bounds__(256) expand_bitmap_kernel(ExpandArgs a)
             }
             __syncthreads();
             const int G = (na + 31) >> 5;                  // restricted-column words
+            const bool keep_rows = na <= L.rk;
             for (int unit = wib; unit < G * d.wm; unit += wpb) {
                 const int g = unit / d.wm, w = unit % d.wm;
                 const int pidx = 32 * g + (int)lane;
                 const uint32_t v = pidx < na ? __ldg(a.rows + (size_t)oid[pidx] * d.wm + w) : 0u;
+                if (keep_rows && pidx < na) rowr[(size_t)pidx * d.wm + w] = v;
                 uint32_t mine = 0;
 #pragma unroll
                 for (int b = 0; b < 32; ++b) {
@@ -322,8 +331,8 @@ __global__ void __launch_bounds__(256) expand_bitmap_kernel(ExpandArgs a)
                 cnt = __reduce_add_sync(FULL, cnt);
                 if (cnt == 0) continue;   // empty extent: its closure is the bottom, added by the host
 
-                // the first object ids of C in ascending order: the closure is bounded by their rows and
-                // completed on the restricted columns
+                // the positions (in the object list) of the first objects of C in ascending order: the
+                // closure is bounded by their rows and completed on the restricted columns
                 auto collect = [&](unsigned want) {
                     unsigned got = 0;
 #pragma unroll
@@ -342,7 +351,7 @@ __global__ void __launch_bounds__(256) expand_bitmap_kernel(ExpandArgs a)
                         while (bits && pos < want) {
                             const int b = __ffs(bits) - 1;
                             bits &= bits - 1u;
-                            rids[pos++] = oid[32 * g + b];
+                            rids[pos++] = (uint32_t)(32 * g + b);
                         }
                         got += __shfl_sync(FULL, incl, 31);
                     }
@@ -351,7 +360,12 @@ __global__ void __launch_bounds__(256) expand_bitmap_kernel(ExpandArgs a)
                 collect(need);
                 __syncwarp();
                 finish_candidate<COUNT>(
-                    a, d, B, j, cnt, rids, need,
+                    a, d, B, j, cnt, need,
+                    [&](unsigned i, int w) {
+                        const uint32_t p = rids[i];
+                        return keep_rows ? rowr[(size_t)p * d.wm + w] : __ldg(a.rows + (size_t)oid[p] * d.wm + w);
+                    },
+                    [&](unsigned i) { return oid[rids[i]]; },
                     [&](int k) {
                         bool bad = false;
 #pragma unroll
@@ -435,7 +449,9 @@ __global__ void __launch_bounds__(256) expand_bitmap_kernel(ExpandArgs a)
             }
             __syncwarp();
             finish_candidate<COUNT>(
-                a, d, B, j, cnt, gids, need,
+                a, d, B, j, cnt, need,
+                [&](unsigned i, int w) { return __ldg(a.rows + (size_t)gids[i] * d.wm + w); },
+                [&](unsigned i) { return gids[i]; },
                 [&](int k) { return subset_of_column(aval, aidx, nnz, J4, cols4 + (size_t)k * wq, lane, loads); },
                 [&](uint32_t *dst) {
                     uint4 *dst4 = reinterpret_cast<uint4 *>(dst);
