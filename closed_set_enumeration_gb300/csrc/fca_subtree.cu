@@ -109,6 +109,57 @@ struct SubtreeWarp {
     }
 };
 
+// Candidate screening for dfs_regs (R <= 64): drops, from the remaining candidates of a node, those
+// whose closure adds an attribute below j (not canonical), evaluating 32 candidates at once: lane l
+// takes candidate j = 32u + l, forms C = ext & c_j from its own column, and ANDs the compact rows of
+// the objects of C (broadcast by shuffles, one object of the extent at a time) into D. A word of
+// candidates is screened only when that costs fewer instructions than evaluating its candidates one
+// by one (about 2 WRT + 2 per object of the extent against about 40 per candidate).
+constexpr int SCREEN_PER_CAND = 40;
+
+template <int NW, int WRT, bool COUNT>
+__device__ __forceinline__ void screen(SubtreeWarp &S, uint32_t (&cand)[WRT], const uint32_t (&ext)[NW],
+                                       const uint32_t (&B)[WRT], const uint32_t (&col)[WRT][NW],
+                                       const uint32_t (&rowc)[NW][WRT])
+{
+    const unsigned lane = threadIdx.x & 31;
+    int ne = 0;
+#pragma unroll
+    for (int t = 0; t < NW; ++t) ne += __popc(ext[t]);
+#pragma unroll
+    for (int u = 0; u < WRT; ++u) {
+        if (ne * (2 * WRT + 2) >= SCREEN_PER_CAND * __popc(cand[u])) continue;   // uniform
+        uint32_t C[NW], D[WRT];
+#pragma unroll
+        for (int t = 0; t < NW; ++t) C[t] = ext[t] & col[u][t];
+#pragma unroll
+        for (int w = 0; w < WRT; ++w) D[w] = FULL;
+#pragma unroll
+        for (int t = 0; t < NW; ++t) {
+            uint32_t e = ext[t];
+            while (e) {
+                const int o = __ffs(e) - 1;
+                e &= e - 1u;
+                const bool in = (C[t] >> o) & 1u;
+#pragma unroll
+                for (int w = 0; w < WRT; ++w) {
+                    const uint32_t r = __shfl_sync(FULL, rowc[t][w], o);
+                    if (in) D[w] &= r;
+                }
+            }
+        }
+        // canonical iff D adds no attribute below j = 32u + lane to B
+        bool ok = true;
+#pragma unroll
+        for (int w = 0; w < WRT; ++w) {
+            const uint32_t below = w < u ? FULL : (w == u ? (1u << lane) - 1u : 0u);
+            ok = ok && (D[w] & ~B[w] & below) == 0u;
+        }
+        cand[u] &= __ballot_sync(FULL, ok);
+        if (COUNT) S.ops += (unsigned long long)ne * 2 * WRT;
+    }
+}
+
 // Depth-first search of one subtree with the restricted columns in registers: lane l holds the
 // columns of compact attributes 32u + l, u < WRT (R <= 32 * WRT). Extent, intent and remaining
 // candidates of the current node are warp-uniform registers; the stack of ancestors is in shared
@@ -126,6 +177,24 @@ __device__ void dfs_regs(SubtreeWarp &S, int R, int n, int jn, int slices, int s
 #pragma unroll
         for (int t = 0; t < NW; ++t) col[u][t] = k < R ? S.cR[t * S.mp + k] : 0u;
     }
+    // compact rows of the root's objects (lane l holds object 32t + l), for candidate screening:
+    // the transpose of the restricted columns, 32 ballots per word
+    constexpr bool SCREEN = WRT <= 2;
+    uint32_t rowc[NW][WRT];
+#pragma unroll
+    for (int t = 0; t < NW; ++t)
+#pragma unroll
+        for (int w = 0; w < WRT; ++w) {
+            uint32_t mine = 0;
+            if (SCREEN) {
+#pragma unroll
+                for (int b = 0; b < 32; ++b) {
+                    const uint32_t bal = __ballot_sync(FULL, (col[w][t] >> b) & 1u);
+                    if (lane == (unsigned)b) mine = bal;
+                }
+            }
+            rowc[t][w] = mine;
+        }
     uint32_t B[WRT], cand[WRT];
     uint32_t ext[NW];
 #pragma unroll
@@ -145,6 +214,7 @@ __device__ void dfs_regs(SubtreeWarp &S, int R, int n, int jn, int slices, int s
         B[u] = 0u;
         if (COUNT) S.ops += 2ull * NW * (unsigned)max(0, min(32, R - 32 * u));
     }
+    if (SCREEN) screen<NW, WRT, COUNT>(S, cand, ext, B, col, rowc);
     int depth = 0;
     for (;;) {
         int j = -1;
@@ -223,6 +293,7 @@ __device__ void dfs_regs(SubtreeWarp &S, int R, int n, int jn, int slices, int s
             cand[u] = __ballot_sync(FULL, meets) & ~D[u] & ge_mask(u, j + 1);
             if (COUNT) S.ops += 2ull * NW * (unsigned)max(0, min(32, R - 32 * u));
         }
+        if (SCREEN) screen<NW, WRT, COUNT>(S, cand, ext, B, col, rowc);
     }
 }
 
