@@ -30,10 +30,11 @@ __device__ __forceinline__ uint32_t ge_mask(int w, int b)
 // Bits < b of word `w`.
 __device__ __forceinline__ uint32_t lt_mask(int w, int b) { return ~ge_mask(w, b); }
 
-// Largest number of restricted-column words (x32 attributes) a lane keeps in registers: 8 (up to
-// 256 relevant attributes) when M > 128, else 4, which keeps the kernel within 64 registers.
+// Largest number of restricted-column words (x32 attributes) a lane keeps in registers, by M: 8 (up
+// to 256 relevant attributes) when M > 128, 4 when M > 64, else 2 (R <= M). The narrower kernels
+// stay within 64 registers.
 constexpr int REG_WORDS_MAX = 8;
-constexpr int reg_words_for(int m) { return m > 128 ? 8 : 4; }
+constexpr int reg_words_for(int m) { return m > 128 ? 8 : (m > 64 ? 4 : 2); }
 
 // Entry size in 32-bit words of an object-list queue root holding `cnt` objects (counting only).
 __device__ __forceinline__ unsigned queue_entry_words(unsigned cnt, int wm)

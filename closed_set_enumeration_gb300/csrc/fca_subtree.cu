@@ -128,7 +128,7 @@ __device__ __forceinline__ void screen(SubtreeWarp &S, uint32_t (&cand)[WRT], co
     for (int t = 0; t < NW; ++t) ne += __popc(ext[t]);
 #pragma unroll
     for (int u = 0; u < WRT; ++u) {
-        if (ne * (2 * WRT + 2) >= SCREEN_PER_CAND * __popc(cand[u])) continue;   // uniform
+        if (ne * (2 * WRT + 2) >= (SCREEN_PER_CAND + 6 * WRT) * __popc(cand[u])) continue;   // uniform
         uint32_t C[NW], D[WRT];
 #pragma unroll
         for (int t = 0; t < NW; ++t) C[t] = ext[t] & col[u][t];
@@ -179,7 +179,7 @@ __device__ void dfs_regs(SubtreeWarp &S, int R, int n, int jn, int slices, int s
     }
     // compact rows of the root's objects (lane l holds object 32t + l), for candidate screening:
     // the transpose of the restricted columns, 32 ballots per word
-    constexpr bool SCREEN = WRT <= 2;
+    constexpr bool SCREEN = WRT <= 4;
     uint32_t rowc[NW][WRT];
 #pragma unroll
     for (int t = 0; t < NW; ++t)
@@ -511,7 +511,7 @@ __global__ void __launch_bounds__(256, RW > 4 ? 3 : 4) subtree_kernel(SubtreeArg
         const int sl = a.slices;
         if (R <= 32) dfs_regs<NW, 1, COUNT>(S, R, n, jn, sl, slice);
         else if (R <= 64) dfs_regs<NW, 2, COUNT>(S, R, n, jn, sl, slice);
-        else if (R <= 128) dfs_regs<NW, 4, COUNT>(S, R, n, jn, sl, slice);
+        else if (RW >= 4 && R <= 128) dfs_regs<NW, 4, COUNT>(S, R, n, jn, sl, slice);
         else if (RW > 4 && R <= 32 * RW) dfs_regs<NW, RW, COUNT>(S, R, n, jn, sl, slice);
         else dfs_smem<NW, COUNT>(S, R, n, jn, sl, slice);
         __syncwarp();
@@ -581,15 +581,16 @@ static int launch_subtree_nw(const SubtreeArgs &a, int sm_count, void *stream)
 
 int launch_subtree(const SubtreeArgs &a, int nw, int sm_count, void *stream)
 {
-    const bool wide = reg_words_for(a.d.m) > 4;
-    if (a.count_work) {
-        if (wide) return nw == 1 ? launch_subtree_nw<1, true, 8>(a, sm_count, stream)
-                                 : launch_subtree_nw<2, true, 8>(a, sm_count, stream);
-        return nw == 1 ? launch_subtree_nw<1, true, 4>(a, sm_count, stream) : launch_subtree_nw<2, true, 4>(a, sm_count, stream);
-    }
-    if (wide) return nw == 1 ? launch_subtree_nw<1, false, 8>(a, sm_count, stream)
-                             : launch_subtree_nw<2, false, 8>(a, sm_count, stream);
-    return nw == 1 ? launch_subtree_nw<1, false, 4>(a, sm_count, stream) : launch_subtree_nw<2, false, 4>(a, sm_count, stream);
+    // register-resident search width by M: R <= M relevant attributes, so M <= 64 never needs more
+    // than two words per lane (a kernel without the wider paths keeps more registers free)
+    const int rw = reg_words_for(a.d.m);
+#define FCA_SUBTREE(NWV, CNT)                                                                   \
+    (rw == 2   ? launch_subtree_nw<NWV, CNT, 2>(a, sm_count, stream)                            \
+     : rw == 4 ? launch_subtree_nw<NWV, CNT, 4>(a, sm_count, stream)                            \
+               : launch_subtree_nw<NWV, CNT, 8>(a, sm_count, stream))
+    if (a.count_work) return nw == 1 ? FCA_SUBTREE(1, true) : FCA_SUBTREE(2, true);
+    return nw == 1 ? FCA_SUBTREE(1, false) : FCA_SUBTREE(2, false);
+#undef FCA_SUBTREE
 }
 
 }  // namespace fca
