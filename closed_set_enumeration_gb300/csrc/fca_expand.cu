@@ -45,6 +45,23 @@ __device__ __forceinline__ bool subset_of_column(const uint4 *av, const uint32_t
 constexpr int RESTRICT_CAP = 4096;
 constexpr int RPL = RESTRICT_CAP / 1024;   // restricted-column words per lane
 constexpr int ROW_BOUND = 8;               // rows ANDed for the closure's upper bound (restricted path)
+// Two block shapes. The warps of a block share one parent's staged extent, restricted columns and
+// rows. With many attributes (many candidates per parent) blocks of 16 warps, two per SM, hide more
+// latency per byte of shared memory, and so do levels with too few parents to fill the GPU; on
+// large levels with fewer attributes the per-parent set-up dominates and blocks of 8 warps, three per
+// SM, keep more parents in flight. Measured with 16 warps throughout: zipf (M = 400) 2.95 -> 2.35 ms
+// per enumeration, sparse (small levels) 0.095 -> 0.073 ms; skewed (M = 128) 94 -> 107 ms and
+// biclusters (M = 256) 3.3 -> 4.2 s.
+constexpr int WIDE_EXPAND_MIN_ATTRS = 320;
+template <int WARPS> struct ExpandShape;
+template <> struct ExpandShape<8> {
+    static constexpr int blocks_per_sm = 3;
+    static constexpr size_t smem_budget = 72 * 1024;
+};
+template <> struct ExpandShape<16> {
+    static constexpr int blocks_per_sm = 2;
+    static constexpr size_t smem_budget = 108 * 1024;
+};
 constexpr int ROWS_KEPT = 256;             // restricted extents up to this size keep their rows in shared memory
 
 // Shared memory of expand_bitmap_kernel. Both paths first stage the parent's non-zero extent
@@ -202,8 +219,8 @@ __device__ __forceinline__ void finish_candidate(const ExpandArgs &a, const Dims
 // ballot per attribute and 32 objects); each candidate's C is read from those columns without any
 // global column access. Larger extents keep the chunk list: each warp gathers column j on the
 // parent's non-zero chunks. Either way the warps of the block take the part's candidates j in turn.
-template <bool COUNT>
-__global__ void __launch_bounds__(256, 3) expand_bitmap_kernel(ExpandArgs a)
+template <bool COUNT, int WARPS>
+__global__ void __launch_bounds__(32 * WARPS, ExpandShape<WARPS>::blocks_per_sm) expand_bitmap_kernel(ExpandArgs a)
 {
     extern __shared__ __align__(16) unsigned char smem[];
     const Dims d = a.d;
@@ -479,14 +496,14 @@ __global__ void __launch_bounds__(256, 3) expand_bitmap_kernel(ExpandArgs a)
 
 size_t expand_smem_per_warp(const Dims &d) { return ExpandLayout(d, 1, 0).bytes; }
 
-template <bool COUNT>
+template <bool COUNT, int WARPS>
 static int launch_expand_t(const ExpandArgs &a, int sm_count, void *stream)
 {
-    int wpb = WARPS_PER_BLOCK;
+    int wpb = WARPS;
     while (wpb > 1 && ExpandLayout(a.d, wpb, 0).bytes > 200 * 1024) --wpb;
-    // the largest restricted extent whose columns fit in the shared memory of three blocks per SM
-    // (or next to the gather path's own, when that is larger)
-    const size_t budget = std::max<size_t>(ExpandLayout(a.d, wpb, 0).bytes, 72 * 1024);
+    // the largest restricted extent whose columns fit in the shared memory of the shape's blocks per
+    // SM (or next to the gather path's own, when that is larger)
+    const size_t budget = std::max<size_t>(ExpandLayout(a.d, wpb, 0).bytes, ExpandShape<WARPS>::smem_budget);
     int tr = RESTRICT_CAP;
     while (tr > 0 && ExpandLayout(a.d, wpb, tr).bytes > budget) tr -= 32;
     const size_t smem = ExpandLayout(a.d, wpb, tr).bytes;
@@ -496,12 +513,12 @@ static int launch_expand_t(const ExpandArgs &a, int sm_count, void *stream)
     cudaGetDevice(&dev);
     if (cache.dev != dev || cache.smem != smem || cache.wpb != wpb) {
         if (smem > 48 * 1024) {
-            cudaError_t e = cudaFuncSetAttribute(expand_bitmap_kernel<COUNT>,
+            cudaError_t e = cudaFuncSetAttribute(expand_bitmap_kernel<COUNT, WARPS>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) return (int)e;
         }
         int ps = 0;
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ps, expand_bitmap_kernel<COUNT>, wpb * 32, smem);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ps, expand_bitmap_kernel<COUNT, WARPS>, wpb * 32, smem);
         cache = ShapeCache{dev, smem, wpb, ps < 1 ? 1 : ps};
     }
     const int per_sm = cache.per_sm;
@@ -516,13 +533,16 @@ static int launch_expand_t(const ExpandArgs &a, int sm_count, void *stream)
     const unsigned long long items = a.p_count * (unsigned long long)b.parts;
     unsigned long long blocks = std::min<unsigned long long>(items, resident);
     if (blocks < 1) blocks = 1;
-    expand_bitmap_kernel<COUNT><<<(unsigned)blocks, wpb * 32, smem, (cudaStream_t)stream>>>(b);
+    expand_bitmap_kernel<COUNT, WARPS><<<(unsigned)blocks, wpb * 32, smem, (cudaStream_t)stream>>>(b);
     return (int)cudaGetLastError();
 }
 
 int launch_expand(const ExpandArgs &a, int sm_count, void *stream)
 {
-    return a.count_work ? launch_expand_t<true>(a, sm_count, stream) : launch_expand_t<false>(a, sm_count, stream);
+    // wide blocks for many attributes, or for levels too small to fill the GPU with narrow blocks
+    if (a.d.m >= WIDE_EXPAND_MIN_ATTRS || a.p_count < 2ull * 3 * (unsigned long long)sm_count)
+        return a.count_work ? launch_expand_t<true, 16>(a, sm_count, stream) : launch_expand_t<false, 16>(a, sm_count, stream);
+    return a.count_work ? launch_expand_t<true, 8>(a, sm_count, stream) : launch_expand_t<false, 8>(a, sm_count, stream);
 }
 
 }  // namespace fca
