@@ -233,7 +233,7 @@ fca_status grow_level(fca_ctx *c, size_t idx, uint64_t need, cudaStream_t st)
 }
 
 // Grow (empty) queue qi to hold at least `need` entries.
-fca_status grow_queue(fca_ctx *c, int qi, uint64_t need)
+fca_status grow_queue(fca_ctx *c, int qi, uint64_t need, cudaStream_t st)
 {
     Queue &Q = c->q[qi];
     const uint64_t cap = std::max<uint64_t>(2 * Q.cap, need + need / 4);
@@ -242,6 +242,16 @@ fca_status grow_queue(fca_ctx *c, int qi, uint64_t need)
     Queue n{};
     fca_status s = make_queue(c, &n, qi, cap);
     if (s != FCA_OK) return s;
+    // keep the roots waiting in the queue
+    const uint64_t cnt = c->q_count[qi];
+    if (cnt) {
+        const Dims &d = c->d;
+        CK(cudaMemcpyAsync(n.ids, Q.ids, cnt * (32u << qi) * 4, cudaMemcpyDeviceToDevice, st), "queue grow");
+        CK(cudaMemcpyAsync(n.itt, Q.itt, cnt * d.wm * 4, cudaMemcpyDeviceToDevice, st), "queue grow");
+        CK(cudaMemcpyAsync(n.y, Q.y, cnt * 4, cudaMemcpyDeviceToDevice, st), "queue grow");
+        CK(cudaMemcpyAsync(n.n, Q.n, cnt * 4, cudaMemcpyDeviceToDevice, st), "queue grow");
+        CK(cudaStreamSynchronize(st), "stream synchronize");
+    }
     c->pool_bytes += (cap - Q.cap) * eb;
     free_queue(Q);
     Q = n;
@@ -385,24 +395,35 @@ fca_status drain(Run &r, size_t lv)
             c->stats.retries++;
             CK(cudaMemcpyAsync(c->ctr, c->ctr_snap, sizeof(Counters), cudaMemcpyDeviceToDevice, r.st),
                "counter restore");
+            // A full destination is first grown to hold what the launch wanted, keeping what waits
+            // in it (the pools are kept for later calls, so a workload stops overflowing once they
+            // have grown); past the pool limit it is emptied instead (its subtrees searched, or the
+            // next level drained) and grown only if one launch alone needs more.
             bool limited = false;
             for (int qi = 0; qi < NQ; ++qi) {
                 if (!(after.error & (ERR_QUEUE0 << qi))) continue;
                 const uint64_t need = after.q_count[qi] - c->q_count[qi];
+                s = grow_queue(c, qi, after.q_count[qi], r.st);
+                if (s == FCA_OK) continue;
+                if (s != FCA_ERR_CAPACITY) return s;
                 if ((s = run_subtree(r, qi, r.st)) != FCA_OK) return s;
                 if (need > c->q[qi].cap) {
-                    s = grow_queue(c, qi, need);
+                    s = grow_queue(c, qi, need, r.st);
                     if (s == FCA_ERR_CAPACITY) limited = true;
                     else if (s != FCA_OK) return s;
                 }
             }
             if (after.error & ERR_NEXT) {
                 const uint64_t need = after.next_count - c->level_count[lv + 1];
-                if ((s = drain(r, lv + 1)) != FCA_OK) return s;
-                if (need > c->levels[lv + 1].cap) {
-                    s = grow_level(c, lv + 1, need, r.st);
-                    if (s == FCA_ERR_CAPACITY) limited = true;
-                    else if (s != FCA_OK) return s;
+                s = grow_level(c, lv + 1, after.next_count, r.st);
+                if (s != FCA_OK && s != FCA_ERR_CAPACITY) return s;
+                if (s == FCA_ERR_CAPACITY) {
+                    if ((s = drain(r, lv + 1)) != FCA_OK) return s;
+                    if (need > c->levels[lv + 1].cap) {
+                        s = grow_level(c, lv + 1, need, r.st);
+                        if (s == FCA_ERR_CAPACITY) limited = true;
+                        else if (s != FCA_OK) return s;
+                    }
                 }
             }
             if (limited) {

@@ -197,7 +197,9 @@ def test_small_pools_roll_back_and_chunk(monkeypatch, limit):
     monkeypatch.setenv("FCA_QUEUE_ENTRIES", "1")     # floor: 4*M entries per queue
     if limit:
         monkeypatch.setenv("FCA_POOL_LIMIT_BYTES", limit)
-    got, st = gpu_run(rows, n, m)
+    # output sized up front: a capacity miss would re-run the enumeration on the pools the first
+    # run grew, and the statistics would describe that second run
+    got, st = gpu_run(rows, n, m, capacity=ref["intents"].shape[0] + 1)
     assert not has_duplicates(got)
     assert same_set(got, ref["intents"])
     assert st["closures"] == ref["closures"]
