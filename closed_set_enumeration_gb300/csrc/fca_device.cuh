@@ -30,6 +30,24 @@ __device__ __forceinline__ uint32_t ge_mask(int w, int b)
 // Bits < b of word `w`.
 __device__ __forceinline__ uint32_t lt_mask(int w, int b) { return ~ge_mask(w, b); }
 
+// Transpose of a 32 x 32 bit matrix held one row per lane (bit j of lane i is entry (i, j)): on
+// return bit i of lane j is entry (i, j). Five exchange rounds: the two off-diagonal 16 x 16 blocks
+// trade places, then the off-diagonal 8 x 8 blocks inside each diagonal block, and so on down to
+// single bits; each round is one shuffle and a masked merge.
+__device__ __forceinline__ uint32_t warp_transpose32(uint32_t x)
+{
+    const unsigned lane = threadIdx.x & 31;
+    constexpr uint32_t lo[5] = {0x0000ffffu, 0x00ff00ffu, 0x0f0f0f0fu, 0x33333333u, 0x55555555u};
+#pragma unroll
+    for (int r = 0; r < 5; ++r) {
+        const int s = 16 >> r;
+        const uint32_t m = lo[r];
+        const uint32_t y = __shfl_xor_sync(FULL, x, s);
+        x = (lane & (unsigned)s) ? ((x & ~m) | ((y >> s) & m)) : ((x & m) | ((y & m) << s));
+    }
+    return x;
+}
+
 // Largest number of restricted-column words (x32 attributes) a lane keeps in registers, by M: 8 (up
 // to 256 relevant attributes) when M > 128, 4 when M > 64, else 2 (R <= M). The narrower kernels
 // stay within 64 registers.

@@ -98,6 +98,34 @@ struct SubtreeWarp {
         if (nb == OUTBUF) flush();
     }
 
+    // Same for a compact intent held in warp-uniform registers (dfs_regs): lane l owns compact
+    // attribute 32u + l of word u, and lane w collects full word w. Each full word that D touches
+    // takes one OR-reduction of the bits of the lanes whose attribute lies in it.
+    template <int WRT, bool COUNT>
+    __device__ void emit_regs(const uint32_t (&D)[WRT])
+    {
+        const unsigned lane = threadIdx.x & 31;
+        uint32_t acc = lane < (unsigned)wm ? rootB[lane] : 0u;
+#pragma unroll
+        for (int u = 0; u < WRT; ++u) {
+            uint32_t pend = D[u];
+            if (pend == 0u) continue;
+            const int a = ((pend >> lane) & 1u) ? (int)rmap[32 * u + (int)lane] : -1;
+            while (pend) {
+                const int w = __shfl_sync(FULL, a, __ffs(pend) - 1) >> 5;
+                const bool in = a >= 0 && (a >> 5) == w;
+                const uint32_t v = __reduce_or_sync(FULL, in ? (1u << (a & 31)) : 0u);
+                if (lane == (unsigned)w) acc |= v;
+                pend &= ~__ballot_sync(FULL, in);
+            }
+        }
+        if (lane < (unsigned)wm) ob[nb * wm + (int)lane] = acc;
+        ++nb;
+        if (COUNT) ops += (unsigned)wm;   // the intent words written
+        __syncwarp();
+        if (nb == OUTBUF) flush();
+    }
+
     // Candidates of a child created at compact candidate j whose compact intent has `above`
     // attributes after j: the attributes after rmap[j] outside its full intent.
     __device__ void count_child(int j, int above)
@@ -178,23 +206,13 @@ __device__ void dfs_regs(SubtreeWarp &S, int R, int n, int jn, int slices, int s
         for (int t = 0; t < NW; ++t) col[u][t] = k < R ? S.cR[t * S.mp + k] : 0u;
     }
     // compact rows of the root's objects (lane l holds object 32t + l), for candidate screening:
-    // the transpose of the restricted columns, 32 ballots per word
+    // the transpose of the restricted columns, one 32 x 32 register transpose per word
     constexpr bool SCREEN = WRT <= 4;
     uint32_t rowc[NW][WRT];
 #pragma unroll
     for (int t = 0; t < NW; ++t)
 #pragma unroll
-        for (int w = 0; w < WRT; ++w) {
-            uint32_t mine = 0;
-            if (SCREEN) {
-#pragma unroll
-                for (int b = 0; b < 32; ++b) {
-                    const uint32_t bal = __ballot_sync(FULL, (col[w][t] >> b) & 1u);
-                    if (lane == (unsigned)b) mine = bal;
-                }
-            }
-            rowc[t][w] = mine;
-        }
+        for (int w = 0; w < WRT; ++w) rowc[t][w] = SCREEN ? warp_transpose32(col[w][t]) : 0u;
     uint32_t B[WRT], cand[WRT];
     uint32_t ext[NW];
 #pragma unroll
@@ -260,12 +278,7 @@ __device__ void dfs_regs(SubtreeWarp &S, int R, int n, int jn, int slices, int s
         if (!canon) continue;
 
         // canonical child (C, D, j+1): write its intent, count its candidates, descend
-        if (lane == 0) {
-#pragma unroll
-            for (int u = 0; u < WRT; ++u) S.dsc[u] = D[u];
-            S.dsc[WRT] = 0u;
-        }
-        S.emit<COUNT>();
+        S.emit_regs<WRT, COUNT>(D);
         int above = 0;
 #pragma unroll
         for (int u = 0; u < WRT; ++u) above += __popc(D[u] & ge_mask(u, j + 1));
@@ -454,30 +467,40 @@ __global__ void __launch_bounds__(256, RW > 4 ? 3 : 4) subtree_kernel(SubtreeArg
         S.rootB[lane] = myRootB;
 
         // ---- relevant attributes R (held by some but not all objects), compact index order =
-        //      attribute order, and the columns restricted to the subtree's objects
+        //      attribute order, and the columns restricted to the subtree's objects. Lane l holds
+        //      the rows of objects 32t + l, loaded CH words at a time (independent loads); each
+        //      32 x 32 block of a word is transposed in registers, so lane b then holds the column of
+        //      attribute 32w + b, and the relevant lanes store theirs at their compact index.
+        constexpr int CH = RW < 8 ? RW : 8;
         int R = 0;
-        for (int w = 0; w < WM; ++w) {
-            uint32_t rw[NW];
-            uint32_t uni = 0;
+        for (int w0 = 0; w0 < WM; w0 += CH) {
+            uint32_t rw[NW][CH];
 #pragma unroll
-            for (int t = 0; t < NW; ++t) {
-                rw[t] = (32 * t + (int)lane < n) ? __ldg(a.rows + (size_t)id[t] * WM + w) : 0u;
-                uni |= rw[t];
-            }
-            uni = __reduce_or_sync(FULL, uni);
-            const uint32_t rm = uni & ~__shfl_sync(FULL, myRootB, w);
-            if (lane == 0) { S.Rm[w] = rm; S.rlo[w] = (uint32_t)R; }
-            uint32_t bits = rm;
-            while (bits) {
-                const int b = __ffs(bits) - 1;
-                bits &= bits - 1u;
+            for (int t = 0; t < NW; ++t)
+#pragma unroll
+                for (int i = 0; i < CH; ++i)
+                    rw[t][i] = (w0 + i < WM && 32 * t + (int)lane < n)
+                                   ? __ldg(a.rows + (size_t)id[t] * WM + w0 + i) : 0u;
+#pragma unroll
+            for (int i = 0; i < CH; ++i) {
+                const int w = w0 + i;
+                if (w >= WM) break;
+                uint32_t uni = 0;
+#pragma unroll
+                for (int t = 0; t < NW; ++t) uni |= rw[t][i];
+                uni = __reduce_or_sync(FULL, uni);
+                const uint32_t rm = uni & ~__shfl_sync(FULL, myRootB, w);
+                if (lane == 0) { S.Rm[w] = rm; S.rlo[w] = (uint32_t)R; }
+                if (rm == 0u) continue;
+                const bool mine = (rm >> lane) & 1u;
+                const int k = R + __popc(rm & ((1u << lane) - 1u));
 #pragma unroll
                 for (int t = 0; t < NW; ++t) {
-                    const uint32_t bal = __ballot_sync(FULL, (rw[t] >> b) & 1u);
-                    if (lane == 0) S.cR[t * mp + R] = bal;
+                    const uint32_t c = warp_transpose32(rw[t][i]);
+                    if (mine) S.cR[t * mp + k] = c;
                 }
-                if (lane == 0) S.rmap[R] = (uint16_t)(32 * w + b);
-                ++R;
+                if (mine) S.rmap[k] = (uint16_t)(32 * w + (int)lane);
+                R += __popc(rm);
             }
         }
         if (lane == 0) S.rlo[WM] = (uint32_t)R;
