@@ -214,7 +214,7 @@ def cpu_baseline(rows, w, budget_s: float):
 # ----------------------------------------------------------------------------- roofline helpers
 
 # The source file of each kernel a roofline is reported for.
-KERNEL_SOURCES = {"subtree_kernel": "fca_subtree.cu", "expand_bitmap_kernel": "fca_expand.cu"}
+KERNEL_SOURCES = {"subtree_kernel": "fca_subtree.cuh", "expand_bitmap_kernel": "fca_expand.cu"}
 
 
 def profile_traffic(kernel: str, workload: str):

@@ -312,8 +312,9 @@ fca_status read_counters(Run &r)
     return FCA_OK;
 }
 
-// Process every root waiting in object-list queue qi, then empty it; all on stream `st`.
-fca_status run_subtree(Run &r, int qi, cudaStream_t st)
+// Process every root waiting in object-list queue qi, then empty it; all on stream `st`. `share`
+// allows the launch to hand work between the warps of a block (see subtree_kernel).
+fca_status run_subtree(Run &r, int qi, cudaStream_t st, bool share = true)
 {
     fca_ctx *c = r.c;
     if (c->q_count[qi] == 0) return FCA_OK;
@@ -329,6 +330,7 @@ fca_status run_subtree(Run &r, int qi, cudaStream_t st)
     a.capacity = r.capacity;
     a.ctr = c->ctr;
     a.count_work = c->count_work;
+    a.share = share ? 1 : 0;
     size_t pair = 0;
     if ((s = time_begin(r, 1, &pair, st)) != FCA_OK) return s;
     CK((cudaError_t)launch_subtree(a, nw, c->sm_count, st), "subtree kernel launch");
@@ -516,12 +518,15 @@ fca_status enumerate_impl(fca_ctx *c, uint32_t *out, uint64_t capacity, uint64_t
     if ((s = drain(r, 0)) != FCA_OK) return s;
     // The two queues are independent. The larger extents run first on the caller's stream; the
     // smaller ones on a side stream, so their blocks take the SMs that the last long subtrees of the
-    // first launch leave idle. The caller's stream waits for both.
+    // first launch leave idle. The caller's stream waits for both. Only the heavier launch (a root
+    // of the wider queue counted as four) may hand work between warps: helpers kept busy in the
+    // lighter one would take issue slots from the heavier one, which ends the call.
     if (c->q_count[0] > 0 && c->q_count[1] > 0) {
         CK(cudaEventRecord(c->fork, st), "cudaEventRecord");
         CK(cudaStreamWaitEvent(c->side, c->fork, 0), "cudaStreamWaitEvent");
-        if ((s = run_subtree(r, 1, st)) != FCA_OK) return s;
-        if ((s = run_subtree(r, 0, c->side)) != FCA_OK) return s;
+        const bool wide_heavier = 4 * c->q_count[1] >= c->q_count[0];
+        if ((s = run_subtree(r, 1, st, wide_heavier)) != FCA_OK) return s;
+        if ((s = run_subtree(r, 0, c->side, !wide_heavier)) != FCA_OK) return s;
         CK(cudaEventRecord(c->join, c->side), "cudaEventRecord");
         CK(cudaStreamWaitEvent(st, c->join, 0), "cudaStreamWaitEvent");
     } else {
@@ -535,6 +540,10 @@ fca_status enumerate_impl(fca_ctx *c, uint32_t *out, uint64_t capacity, uint64_t
        "bottom kernel");
     c->stats.launches++;
     if ((s = read_counters(r)) != FCA_OK) return s;
+    if (c->ctr_host->fault & FAULT_WAIT) {
+        c->err = "object-list kernel: a warp waited past its limit for work from its block";
+        return FCA_ERR_CUDA;
+    }
     const uint64_t total = c->ctr_host->out_count;
     c->stats.concepts = total;
     c->stats.closures = c->ctr_host->closures;

@@ -31,6 +31,8 @@ constexpr int MAX_ATTRS = 1024;    // M limit (intent words fit one per lane)
 // Overflow bits of Counters::error (a destination was too small; the driver rolls back and retries).
 constexpr unsigned ERR_NEXT = 1u << 4;     // next bitmap level
 constexpr unsigned ERR_QUEUE0 = 1u;        // queue q sets ERR_QUEUE0 << q
+// Bits of Counters::fault (the call fails with FCA_ERR_CUDA).
+constexpr unsigned FAULT_WAIT = 1u;        // an object-list warp waited too long for its block
 
 // Device-side counters of one enumerate call.
 struct Counters {
@@ -43,7 +45,8 @@ struct Counters {
     unsigned long long word_ops;       // counted object-list-tier word operations (when counting)
     unsigned long long bytes;          // counted bitmap-tier bytes (when counting)
     unsigned int error;                // overflow bits (ERR_*)
-    unsigned int pad[3];
+    unsigned int fault;                // FAULT_* bits: a bounded wait inside a kernel ran out
+    unsigned int pad[2];
 };
 
 // A bitmap-tier frontier level (structure of arrays).
@@ -95,6 +98,8 @@ struct SubtreeArgs {
     uint64_t q_count;
     int q_index;            // which q_head counter this queue uses
     int slices;             // work items per root (set by the launcher)
+    int share;              // 1: warps may hand work to idle warps of their block (the launcher
+                            // keeps it only for launches with few items per warp)
     uint32_t *out;
     uint64_t capacity;
     Counters *ctr;
@@ -112,6 +117,9 @@ int launch_expand(const ExpandArgs &a, int sm_count, void *stream);
 int launch_append_bottom(const uint32_t *flag_full_row, const uint32_t *full_mask, uint32_t *out,
                          uint64_t capacity, Counters *ctr, const Dims &d, void *stream);
 int launch_subtree(const SubtreeArgs &a, int nw, int sm_count, void *stream);
+// The same with work sharing inside blocks, for a launch whose slices are already set in `b`
+// (called by launch_subtree; rw = register words of the search, 2, 4 or 8).
+int launch_subtree_shared(const SubtreeArgs &b, int nw, int rw, int sm_count, void *stream);
 size_t expand_smem_per_warp(const Dims &d);
 
 }  // namespace fca

@@ -145,6 +145,7 @@ extern "C" fca_status fca_enumerate_small_noalloc(const uint32_t *rows, int64_t 
         return FCA_ERR_CUDA;
     Counters ctr;
     memcpy(&ctr, head + OFF_CTR, sizeof ctr);
+    if (ctr.fault) return FCA_ERR_CUDA;
     uint64_t total = ctr.out_count;
     // the bottom concept, when no object holds every attribute (its extent is then empty)
     if (head[OFF_FLAG] == 0u) {

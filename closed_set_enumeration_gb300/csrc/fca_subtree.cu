@@ -1,592 +1,15 @@
-// Object-list tier of libfca (sm_103a): subtree_kernel<NW> runs whole Close-by-One subtrees whose
-// root extent holds at most 32*NW objects, one warp per subtree, on the context's columns
-// restricted to the root's objects (the recursive Close-by-One search of the FCbO-to-CUDA article,
-// sections 2.1-2.3). Bitwise set algebra only: no tensor cores.
-#include <cuda_runtime.h>
-
-#include <algorithm>
-
-#include "fca_device.cuh"
+// Object-list tier of libfca (sm_103a): launches without work sharing, and the choice of slices
+// and of work sharing per launch. The device code is in fca_subtree.cuh.
+#include "fca_subtree.cuh"
 
 namespace fca {
-namespace {
-
-
-// Shared-memory layout of one warp of subtree_kernel<NW> (32-bit words).
-struct SubtreeLayout {
-    int mp, wm, fr, fs;
-    size_t o_rmap, o_rootb, o_rm, o_rlo, o_sufb, o_dsc, o_stack, o_outbuf, words;
-    __host__ __device__ SubtreeLayout(const Dims &d, int nw)
-    {
-        mp = (d.m + 31) & ~31;
-        wm = d.wm;
-        fr = (32 * nw < d.m ? 32 * nw : d.m) + 1;     // depth <= |extent| and <= |R|
-        // frame: extent mask, then cursor + intent (shared-memory search) or candidates + intent
-        fs = nw + (1 + wm > 2 * REG_WORDS_MAX ? 1 + wm : 2 * REG_WORDS_MAX);
-        o_rmap = (size_t)nw * mp;
-        o_rootb = o_rmap + mp / 2;
-        o_rm = o_rootb + 32;
-        o_rlo = o_rm + 32;
-        o_sufb = o_rlo + 34;
-        o_dsc = o_sufb + 32;
-        o_stack = o_dsc + 34;
-        o_outbuf = o_stack + (size_t)fr * fs;
-        words = o_outbuf + (size_t)OUTBUF * wm;
-        words = (words + 3) & ~(size_t)3;
-    }
-};
-
-// Per-warp state of the object-list tier: shared-memory areas of the current subtree root,
-// the output buffer and the warp's counters.
-struct SubtreeWarp {
-    uint32_t *cR;       // restricted columns, NW planes x mp (compact attribute index)
-    uint16_t *rmap;     // compact index -> attribute
-    uint32_t *rootB;    // root intent (full attribute space), 32 words
-    uint32_t *Rm;       // relevant attributes per full word
-    uint32_t *rlo;      // first compact index of each full word (wm + 1 entries)
-    uint32_t *sufB;     // root-intent attributes in the words above each word
-    uint32_t *dsc;      // compact intent of the child being written
-    uint32_t *stk;      // search stack
-    uint32_t *ob;       // output buffer, OUTBUF x wm
-    int mp, wm, fs, m;
-    uint32_t *out;
-    unsigned long long capacity;
-    Counters *ctr;
-    int nb;             // intents waiting in the output buffer
-    unsigned long long closures, ops;
-
-    __device__ void flush()
-    {
-        const unsigned lane = threadIdx.x & 31;
-        unsigned long long b0 = 0;
-        if (lane == 0) b0 = atomicAdd(&ctr->out_count, (unsigned long long)nb);
-        b0 = __shfl_sync(FULL, b0, 0);
-        __syncwarp();
-        for (int i = (int)lane; i < nb * wm; i += 32)
-            if (b0 + (unsigned long long)(i / wm) < capacity) out[b0 * wm + i] = ob[i];
-        __syncwarp();
-        nb = 0;
-    }
-
-    // Write the full intent of a canonical child whose compact intent is in dsc[]:
-    // root intent plus the compact bits mapped back to their attributes.
-    template <bool COUNT>
-    __device__ void emit()
-    {
-        const unsigned lane = threadIdx.x & 31;
-        __syncwarp();
-        if (lane < (unsigned)wm) {
-            const int w = (int)lane;
-            const int lo = (int)rlo[w], hi = (int)rlo[w + 1];
-            const int su = lo >> 5, sh = lo & 31;
-            const uint32_t s0 = dsc[su];
-            const uint32_t s1 = sh ? dsc[su + 1] : 0u;
-            uint32_t seg = sh ? ((s0 >> sh) | (s1 << (32 - sh))) : s0;
-            const int len = hi - lo;
-            if (len < 32) seg &= (1u << len) - 1u;
-            uint32_t res = rootB[w];
-            while (seg) {                      // each compact attribute of D in this word
-                const int i = __ffs(seg) - 1;
-                seg &= seg - 1u;
-                res |= 1u << (rmap[lo + i] & 31);
-            }
-            ob[nb * wm + w] = res;
-        }
-        ++nb;
-        if (COUNT) ops += (unsigned)wm;   // the intent words written
-        __syncwarp();
-        if (nb == OUTBUF) flush();
-    }
-
-    // Same for a compact intent held in warp-uniform registers (dfs_regs): lane l owns compact
-    // attribute 32u + l of word u, and lane w collects full word w. Each full word that D touches
-    // takes one OR-reduction of the bits of the lanes whose attribute lies in it.
-    template <int WRT, bool COUNT>
-    __device__ void emit_regs(const uint32_t (&D)[WRT])
-    {
-        const unsigned lane = threadIdx.x & 31;
-        uint32_t acc = lane < (unsigned)wm ? rootB[lane] : 0u;
-#pragma unroll
-        for (int u = 0; u < WRT; ++u) {
-            uint32_t pend = D[u];
-            if (pend == 0u) continue;
-            const int a = ((pend >> lane) & 1u) ? (int)rmap[32 * u + (int)lane] : -1;
-            while (pend) {
-                const int w = __shfl_sync(FULL, a, __ffs(pend) - 1) >> 5;
-                const bool in = a >= 0 && (a >> 5) == w;
-                const uint32_t v = __reduce_or_sync(FULL, in ? (1u << (a & 31)) : 0u);
-                if (lane == (unsigned)w) acc |= v;
-                pend &= ~__ballot_sync(FULL, in);
-            }
-        }
-        if (lane < (unsigned)wm) ob[nb * wm + (int)lane] = acc;
-        ++nb;
-        if (COUNT) ops += (unsigned)wm;   // the intent words written
-        __syncwarp();
-        if (nb == OUTBUF) flush();
-    }
-
-    // Candidates of a child created at compact candidate j whose compact intent has `above`
-    // attributes after j: the attributes after rmap[j] outside its full intent.
-    __device__ void count_child(int j, int above)
-    {
-        const int rj = rmap[j];
-        const int rw = rj >> 5, rb = rj & 31;
-        const uint32_t hi = rb == 31 ? 0u : (rootB[rw] >> (rb + 1));
-        closures += (unsigned long long)(m - rj - 1 - (int)sufB[rw] - __popc(hi) - above);
-    }
-};
-
-// Candidate screening for dfs_regs (R <= 64): drops, from the remaining candidates of a node, those
-// whose closure adds an attribute below j (not canonical), evaluating 32 candidates at once: lane l
-// takes candidate j = 32u + l, forms C = ext & c_j from its own column, and ANDs the compact rows of
-// the objects of C (broadcast by shuffles, one object of the extent at a time) into D. A word of
-// candidates is screened only when that costs fewer instructions than evaluating its candidates one
-// by one (about 2 WRT + 2 per object of the extent against about 40 per candidate).
-constexpr int SCREEN_PER_CAND = 40;
-
-template <int NW, int WRT, bool COUNT>
-__device__ __forceinline__ void screen(SubtreeWarp &S, uint32_t (&cand)[WRT], const uint32_t (&ext)[NW],
-                                       const uint32_t (&B)[WRT], const uint32_t (&col)[WRT][NW],
-                                       const uint32_t (&rowc)[NW][WRT])
-{
-    const unsigned lane = threadIdx.x & 31;
-    int ne = 0;
-#pragma unroll
-    for (int t = 0; t < NW; ++t) ne += __popc(ext[t]);
-#pragma unroll
-    for (int u = 0; u < WRT; ++u) {
-        if (ne * (2 * WRT + 2) >= (SCREEN_PER_CAND + 6 * WRT) * __popc(cand[u])) continue;   // uniform
-        uint32_t C[NW], D[WRT];
-#pragma unroll
-        for (int t = 0; t < NW; ++t) C[t] = ext[t] & col[u][t];
-#pragma unroll
-        for (int w = 0; w < WRT; ++w) D[w] = FULL;
-#pragma unroll
-        for (int t = 0; t < NW; ++t) {
-            uint32_t e = ext[t];
-            while (e) {
-                const int o = __ffs(e) - 1;
-                e &= e - 1u;
-                const bool in = (C[t] >> o) & 1u;
-#pragma unroll
-                for (int w = 0; w < WRT; ++w) {
-                    const uint32_t r = __shfl_sync(FULL, rowc[t][w], o);
-                    if (in) D[w] &= r;
-                }
-            }
-        }
-        // canonical iff D adds no attribute below j = 32u + lane to B
-        bool ok = true;
-#pragma unroll
-        for (int w = 0; w < WRT; ++w) {
-            const uint32_t below = w < u ? FULL : (w == u ? (1u << lane) - 1u : 0u);
-            ok = ok && (D[w] & ~B[w] & below) == 0u;
-        }
-        cand[u] &= __ballot_sync(FULL, ok);
-        if (COUNT) S.ops += (unsigned long long)ne * 2 * WRT;
-    }
-}
-
-// Depth-first search of one subtree with the restricted columns in registers: lane l holds the
-// columns of compact attributes 32u + l, u < WRT (R <= 32 * WRT). Extent, intent and remaining
-// candidates of the current node are warp-uniform registers; the stack of ancestors is in shared
-// memory. A node's candidates are filtered once, when the node is entered, to the attributes
-// whose column meets its extent (the others give an empty extent, whose closure is the bottom
-// concept the host adds), so the loop only visits candidates with a non-empty C.
-template <int NW, int WRT, bool COUNT>
-__device__ void dfs_regs(SubtreeWarp &S, int R, int n, int jn, int slices, int slice)
-{
-    const unsigned lane = threadIdx.x & 31;
-    uint32_t col[WRT][NW];
-#pragma unroll
-    for (int u = 0; u < WRT; ++u) {
-        const int k = 32 * u + (int)lane;
-#pragma unroll
-        for (int t = 0; t < NW; ++t) col[u][t] = k < R ? S.cR[t * S.mp + k] : 0u;
-    }
-    // compact rows of the root's objects (lane l holds object 32t + l), for candidate screening:
-    // the transpose of the restricted columns, one 32 x 32 register transpose per word
-    constexpr bool SCREEN = WRT <= 4;
-    uint32_t rowc[NW][WRT];
-#pragma unroll
-    for (int t = 0; t < NW; ++t)
-#pragma unroll
-        for (int w = 0; w < WRT; ++w) rowc[t][w] = SCREEN ? warp_transpose32(col[w][t]) : 0u;
-    uint32_t B[WRT], cand[WRT];
-    uint32_t ext[NW];
-#pragma unroll
-    for (int t = 0; t < NW; ++t) {
-        const int k = n - 32 * t;
-        ext[t] = k >= 32 ? FULL : (k > 0 ? ((1u << k) - 1u) : 0u);
-    }
-    // the root: empty compact intent; candidates from jn on, in this slice, meeting the extent
-#pragma unroll
-    for (int u = 0; u < WRT; ++u) {
-        bool meets = false;
-#pragma unroll
-        for (int t = 0; t < NW; ++t) meets = meets || (ext[t] & col[u][t]) != 0u;
-        const int k = 32 * u + (int)lane;
-        const bool mine = slices <= 1 || k % slices == slice;
-        cand[u] = __ballot_sync(FULL, meets && mine) & ge_mask(u, jn);
-        B[u] = 0u;
-        if (COUNT) S.ops += 2ull * NW * (unsigned)max(0, min(32, R - 32 * u));
-    }
-    if (SCREEN) screen<NW, WRT, COUNT>(S, cand, ext, B, col, rowc);
-    int depth = 0;
-    for (;;) {
-        int j = -1;
-#pragma unroll
-        for (int u = 0; u < WRT; ++u)
-            if (j < 0 && cand[u]) j = 32 * u + __ffs(cand[u]) - 1;
-        if (j < 0) {
-            if (depth == 0) break;
-            --depth;
-            const uint32_t *f = S.stk + (size_t)depth * S.fs;
-#pragma unroll
-            for (int t = 0; t < NW; ++t) ext[t] = f[t];
-#pragma unroll
-            for (int u = 0; u < WRT; ++u) {
-                cand[u] = f[NW + u];
-                B[u] = f[NW + WRT + u];
-            }
-            __syncwarp();
-            continue;
-        }
-        const int ju = j >> 5;
-#pragma unroll
-        for (int u = 0; u < WRT; ++u)
-            if (u == ju) cand[u] &= cand[u] - 1u;     // j is the lowest remaining candidate
-        uint32_t C[NW];
-#pragma unroll
-        for (int t = 0; t < NW; ++t) C[t] = ext[t] & S.cR[t * S.mp + j];
-        if (COUNT) S.ops += NW;            // the extent intersection
-
-        // closure over the relevant attributes, canonical prefix first
-        const uint32_t jm = (1u << (j & 31)) - 1u;
-        uint32_t D[WRT];
-        bool canon = true;
-#pragma unroll
-        for (int u = 0; u < WRT; ++u) {
-            bool in = true;
-#pragma unroll
-            for (int t = 0; t < NW; ++t) in = in && ((C[t] & ~col[u][t]) == 0u);
-            D[u] = __ballot_sync(FULL, in);   // columns past R are 0, so those bits stay clear
-            if (COUNT) S.ops += 2ull * NW * (unsigned)max(0, min(32, R - 32 * u)) + (u <= ju ? 2 : 0);
-            if (u <= ju && (D[u] & ~B[u] & (u < ju ? FULL : jm))) { canon = false; break; }
-        }
-        if (!canon) continue;
-
-        // canonical child (C, D, j+1): write its intent, count its candidates, descend
-        S.emit_regs<WRT, COUNT>(D);
-        int above = 0;
-#pragma unroll
-        for (int u = 0; u < WRT; ++u) above += __popc(D[u] & ge_mask(u, j + 1));
-        S.count_child(j, above);
-        if (lane == 0) {
-            uint32_t *f = S.stk + (size_t)depth * S.fs;
-#pragma unroll
-            for (int t = 0; t < NW; ++t) f[t] = ext[t];
-#pragma unroll
-            for (int u = 0; u < WRT; ++u) {
-                f[NW + u] = cand[u];
-                f[NW + WRT + u] = B[u];
-            }
-        }
-        __syncwarp();
-        ++depth;
-#pragma unroll
-        for (int t = 0; t < NW; ++t) ext[t] = C[t];
-#pragma unroll
-        for (int u = 0; u < WRT; ++u) {
-            bool meets = false;
-#pragma unroll
-            for (int t = 0; t < NW; ++t) meets = meets || (C[t] & col[u][t]) != 0u;
-            B[u] = D[u];
-            cand[u] = __ballot_sync(FULL, meets) & ~D[u] & ge_mask(u, j + 1);
-            if (COUNT) S.ops += 2ull * NW * (unsigned)max(0, min(32, R - 32 * u));
-        }
-        if (SCREEN) screen<NW, WRT, COUNT>(S, cand, ext, B, col, rowc);
-    }
-}
-
-// Same search with the restricted columns read from shared memory, for any R <= M: lane u of the
-// warp holds word u of the current compact intent.
-template <int NW, bool COUNT>
-__device__ void dfs_smem(SubtreeWarp &S, int R, int n, int jn, int slices, int slice)
-{
-    const unsigned lane = threadIdx.x & 31;
-    const uint32_t validR = lt_mask((int)lane, R);
-    const int WR = (R + 31) >> 5;
-    uint32_t myB = 0;
-    uint32_t ext[NW];
-#pragma unroll
-    for (int t = 0; t < NW; ++t) {
-        const int k = n - 32 * t;
-        ext[t] = k >= 32 ? FULL : (k > 0 ? ((1u << k) - 1u) : 0u);
-    }
-    int depth = 0;
-    for (;;) {
-        const uint32_t cw = ~myB & validR & ge_mask((int)lane, jn);
-        const unsigned bal = __ballot_sync(FULL, cw != 0u);
-        if (bal == 0u) {
-            if (depth == 0) break;
-            --depth;
-            const uint32_t *f = S.stk + (size_t)depth * S.fs;
-#pragma unroll
-            for (int t = 0; t < NW; ++t) ext[t] = f[t];
-            jn = (int)f[NW];
-            myB = lane < (unsigned)S.wm ? f[NW + 1 + lane] : 0u;
-            __syncwarp();
-            continue;
-        }
-        const int u0 = __ffs(bal) - 1;
-        const uint32_t cwu = __shfl_sync(FULL, cw, u0);
-        const int j = u0 * 32 + __ffs(cwu) - 1;
-        jn = j + 1;
-        if (depth == 0 && slices > 1 && j % slices != slice) continue;   // another slice's child
-
-        uint32_t C[NW];
-        bool nonempty = false;
-#pragma unroll
-        for (int t = 0; t < NW; ++t) {
-            C[t] = ext[t] & S.cR[t * S.mp + j];
-            nonempty |= C[t] != 0u;
-        }
-        if (COUNT) S.ops += NW;
-        if (!nonempty) continue;
-
-        const int ju = j >> 5;
-        const uint32_t jm = (1u << (j & 31)) - 1u;
-        bool canon = true;
-        uint32_t myD = 0;
-        for (int u = 0; u < WR; ++u) {
-            const int k = u * 32 + (int)lane;
-            bool in = k < R;
-            if (in) {
-#pragma unroll
-                for (int t = 0; t < NW; ++t) in = in && ((C[t] & ~S.cR[t * S.mp + k]) == 0u);
-            }
-            const uint32_t Du = __ballot_sync(FULL, in);
-            if (COUNT) S.ops += 2ull * NW * (unsigned)min(32, R - 32 * u) + (u <= ju ? 2 : 0);
-            if (u <= ju) {
-                const uint32_t Bu = __shfl_sync(FULL, myB, u);
-                const uint32_t pm = u < ju ? FULL : jm;
-                if (Du & ~Bu & pm) { canon = false; break; }
-            }
-            if ((int)lane == u) myD = Du;
-        }
-        if (!canon) continue;
-
-        if (lane <= (unsigned)WR) S.dsc[lane] = lane < (unsigned)WR ? myD : 0u;
-        S.emit<COUNT>();
-        unsigned c = __popc(myD & ge_mask((int)lane, j + 1) & validR);
-        c = __reduce_add_sync(FULL, c);
-        S.count_child(j, (int)c);
-        {
-            uint32_t *f = S.stk + (size_t)depth * S.fs;
-#pragma unroll
-            for (int t = 0; t < NW; ++t)
-                if ((int)lane == t) f[t] = ext[t];
-            if (lane == 0) f[NW] = (uint32_t)jn;
-            if (lane < (unsigned)S.wm) f[NW + 1 + lane] = myB;
-            __syncwarp();
-            ++depth;
-#pragma unroll
-            for (int t = 0; t < NW; ++t) ext[t] = C[t];
-            myB = myD;
-        }
-    }
-}
-
-template <int NW, bool COUNT, int RW>
-__global__ void __launch_bounds__(256, RW > 4 ? 3 : 4) subtree_kernel(SubtreeArgs a)
-{
-    extern __shared__ uint32_t smw[];
-    const Dims d = a.d;
-    const SubtreeLayout L(d, NW);
-    const unsigned lane = threadIdx.x & 31;
-    const int wib = threadIdx.x >> 5;
-    uint32_t *base = smw + (size_t)wib * L.words;
-    SubtreeWarp S;
-    S.cR = base;
-    S.rmap = reinterpret_cast<uint16_t *>(base + L.o_rmap);
-    S.rootB = base + L.o_rootb;
-    S.Rm = base + L.o_rm;
-    S.rlo = base + L.o_rlo;
-    S.sufB = base + L.o_sufb;
-    S.dsc = base + L.o_dsc;
-    S.stk = base + L.o_stack;
-    S.ob = base + L.o_outbuf;
-    S.mp = L.mp;
-    S.wm = d.wm;
-    S.fs = L.fs;
-    S.m = d.m;
-    S.out = a.out;
-    S.capacity = a.capacity;
-    S.ctr = a.ctr;
-    S.nb = 0;
-    S.closures = 0;
-    S.ops = 0;
-    const int mp = L.mp, WM = d.wm, PER = 32 * NW;
-
-    const unsigned long long items = a.q_count * (unsigned long long)a.slices;
-    // Guided self-scheduling: a warp claims a run of consecutive items with one atomic, a quarter of
-    // its share of what was left at its last claim (so claims shrink to single items near the end),
-    // which keeps the launch-wide cursor from becoming a hot spot when items are short.
-    const unsigned long long nwarps = (unsigned long long)gridDim.x * (blockDim.x >> 5);
-    unsigned long long next = 0, end = 0, seen = 0;
-    for (;;) {
-        if (next >= end) {
-            unsigned long long base = 0;
-            const unsigned long long left = items > seen ? items - seen : 0;
-            const unsigned long long k = min(32ull, max(1ull, left / (4 * nwarps)));
-            if (lane == 0) base = atomicAdd(&a.ctr->q_head[a.q_index], k);
-            base = __shfl_sync(FULL, base, 0);
-            if (base >= items) break;
-            next = base;
-            end = min(items, base + k);
-            seen = base + k;
-        }
-        const unsigned long long item = next++;
-        // work item = (root, slice): the slice takes the root's children j with j % slices == slice
-        const unsigned long long r = item / (unsigned)a.slices;
-        const int slice = (int)(item % (unsigned)a.slices);
-
-        // ---- root: object ids, intent, cursor
-        const int n = a.q.n[r];
-        const int y0 = a.q.y[r];
-        uint32_t id[NW];
-#pragma unroll
-        for (int t = 0; t < NW; ++t) {
-            const int o = 32 * t + (int)lane;
-            id[t] = o < n ? a.q.ids[r * PER + o] : 0u;
-        }
-        const uint32_t myRootB = lane < (unsigned)WM ? a.q.itt[r * WM + lane] : 0u;
-        __syncwarp();
-        S.rootB[lane] = myRootB;
-
-        // ---- relevant attributes R (held by some but not all objects), compact index order =
-        //      attribute order, and the columns restricted to the subtree's objects. Lane l holds
-        //      the rows of objects 32t + l, loaded CH words at a time (independent loads); each
-        //      32 x 32 block of a word is transposed in registers, so lane b then holds the column of
-        //      attribute 32w + b, and the relevant lanes store theirs at their compact index.
-        constexpr int CH = RW < 8 ? RW : 8;
-        int R = 0;
-        for (int w0 = 0; w0 < WM; w0 += CH) {
-            uint32_t rw[NW][CH];
-#pragma unroll
-            for (int t = 0; t < NW; ++t)
-#pragma unroll
-                for (int i = 0; i < CH; ++i)
-                    rw[t][i] = (w0 + i < WM && 32 * t + (int)lane < n)
-                                   ? __ldg(a.rows + (size_t)id[t] * WM + w0 + i) : 0u;
-#pragma unroll
-            for (int i = 0; i < CH; ++i) {
-                const int w = w0 + i;
-                if (w >= WM) break;
-                uint32_t uni = 0;
-#pragma unroll
-                for (int t = 0; t < NW; ++t) uni |= rw[t][i];
-                uni = __reduce_or_sync(FULL, uni);
-                const uint32_t rm = uni & ~__shfl_sync(FULL, myRootB, w);
-                if (lane == 0) { S.Rm[w] = rm; S.rlo[w] = (uint32_t)R; }
-                if (rm == 0u) continue;
-                const bool mine = (rm >> lane) & 1u;
-                const int k = R + __popc(rm & ((1u << lane) - 1u));
-#pragma unroll
-                for (int t = 0; t < NW; ++t) {
-                    const uint32_t c = warp_transpose32(rw[t][i]);
-                    if (mine) S.cR[t * mp + k] = c;
-                }
-                if (mine) S.rmap[k] = (uint16_t)(32 * w + (int)lane);
-                R += __popc(rm);
-            }
-        }
-        if (lane == 0) S.rlo[WM] = (uint32_t)R;
-        {
-            // sufB[w] = number of root-intent attributes in words above w
-            const unsigned pc = lane < (unsigned)WM ? __popc(myRootB) : 0u;
-            unsigned incl = pc;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                const unsigned t = __shfl_up_sync(FULL, incl, off);
-                if (lane >= (unsigned)off) incl += t;
-            }
-            const unsigned tot = __shfl_sync(FULL, incl, 31);
-            S.sufB[lane] = tot - incl;
-        }
-        __syncwarp();
-
-        // ---- candidates of the root: attributes >= y0 outside its intent (counted by slice 0)
-        {
-            unsigned c = lane < (unsigned)WM ? __popc(myRootB & ge_mask((int)lane, y0)) : 0u;
-            c = __reduce_add_sync(FULL, c);
-            if (slice == 0) S.closures += (unsigned long long)(d.m - y0 - (int)c);
-        }
-        int jn;   // compact cursor: relevant attributes below y0 are not candidates
-        {
-            const unsigned c = lane < (unsigned)WM ? __popc(S.Rm[lane] & lt_mask((int)lane, y0)) : 0u;
-            jn = (int)__reduce_add_sync(FULL, c);
-        }
-
-        // ---- depth-first search of the subtree
-        const int sl = a.slices;
-        if (R <= 32) dfs_regs<NW, 1, COUNT>(S, R, n, jn, sl, slice);
-        else if (R <= 64) dfs_regs<NW, 2, COUNT>(S, R, n, jn, sl, slice);
-        else if (RW >= 4 && R <= 128) dfs_regs<NW, 4, COUNT>(S, R, n, jn, sl, slice);
-        else if (RW > 4 && R <= 32 * RW) dfs_regs<NW, RW, COUNT>(S, R, n, jn, sl, slice);
-        else dfs_smem<NW, COUNT>(S, R, n, jn, sl, slice);
-        __syncwarp();
-    }
-    if (S.nb) S.flush();
-    if (lane == 0 && S.closures) atomicAdd(&a.ctr->closures, S.closures);
-    if (COUNT && lane == 0 && S.ops) atomicAdd(&a.ctr->word_ops, S.ops);
-}
-
-}  // namespace
-
-static int warps_for(size_t per_warp)
-{
-    const size_t budget = 200 * 1024;
-    int w = WARPS_PER_BLOCK;
-    while (w > 1 && (size_t)w * per_warp > budget) --w;
-    return w;
-}
-
-// Block shape of the subtree kernel (persistent: at most one block per resident slot).
-template <int NW, bool COUNT, int RW>
-static int subtree_shape(const Dims &d, int *wpb_out, size_t *smem_out, int *per_sm_out)
-{
-    const size_t pw = SubtreeLayout(d, NW).words * 4;
-    const int wpb = warps_for(pw);
-    const size_t smem = pw * wpb;
-    static thread_local ShapeCache cache;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (cache.dev != dev || cache.smem != smem || cache.wpb != wpb) {
-        if (smem > 48 * 1024) {
-            cudaError_t e = cudaFuncSetAttribute(subtree_kernel<NW, COUNT, RW>,
-                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (e != cudaSuccess) return (int)e;
-        }
-        int ps = 0;
-        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ps, subtree_kernel<NW, COUNT, RW>, wpb * 32, smem);
-        if (e != cudaSuccess) return (int)e;
-        cache = ShapeCache{dev, smem, wpb, ps < 1 ? 1 : ps};
-    }
-    *wpb_out = wpb;
-    *smem_out = smem;
-    *per_sm_out = cache.per_sm;
-    return (int)cudaSuccess;
-}
 
 template <int NW, bool COUNT, int RW>
 static int launch_subtree_nw(const SubtreeArgs &a, int sm_count, void *stream)
 {
     int wpb = 0, per_sm = 0;
     size_t smem = 0;
-    int e = subtree_shape<NW, COUNT, RW>(a.d, &wpb, &smem, &per_sm);
+    int e = subtree_shape<NW, COUNT, RW, false>(a.d, &wpb, &smem, &per_sm);
     if (e != (int)cudaSuccess) return e;
     // split roots into slices when there are too few roots to keep every resident warp busy
     SubtreeArgs b = a;
@@ -594,12 +17,12 @@ static int launch_subtree_nw(const SubtreeArgs &a, int sm_count, void *stream)
     const unsigned long long want = 4 * resident;
     const unsigned long long qn = std::max<unsigned long long>(1, a.q_count);
     b.slices = (int)std::min<unsigned long long>(MAX_SLICES, std::max<unsigned long long>(1, (want + qn - 1) / qn));
-    unsigned long long blocks = (a.q_count * b.slices + wpb - 1) / wpb;
-    const unsigned long long cap = (unsigned long long)sm_count * per_sm;
-    if (blocks > cap) blocks = cap;
-    if (blocks < 1) blocks = 1;
-    subtree_kernel<NW, COUNT, RW><<<(unsigned)blocks, wpb * 32, smem, (cudaStream_t)stream>>>(b);
-    return (int)cudaGetLastError();
+    // work sharing pays when the launch has few items per warp (its tail is then a large part of
+    // it); with many short items the hand-overs cost more than they save. The counting pass runs
+    // without it.
+    b.share = !COUNT && a.share && a.q_count * (unsigned long long)b.slices <= 8 * resident ? 1 : 0;
+    if (b.share) return launch_subtree_shared(b, NW, RW, sm_count, stream);
+    return launch_subtree_kernel<NW, COUNT, RW, false>(b, sm_count, stream);
 }
 
 int launch_subtree(const SubtreeArgs &a, int nw, int sm_count, void *stream)
