@@ -277,12 +277,13 @@ __device__ void offer(SubtreeWarp &S, int R, int depth, const uint32_t (&ext)[NW
     __syncwarp();
 }
 
-// Candidate screening for dfs_regs (R <= 64): drops, from the remaining candidates of a node, those
+// Candidate screening for dfs_regs (R <= 128): drops, from the remaining candidates of a node, those
 // whose closure adds an attribute below j (not canonical), evaluating 32 candidates at once: lane l
 // takes candidate j = 32u + l, forms C = ext & c_j from its own column, and ANDs the compact rows of
-// the objects of C (broadcast by shuffles, one object of the extent at a time) into D. A word of
-// candidates is screened only when that costs fewer instructions than evaluating its candidates one
-// by one (about 2 WRT + 2 per object of the extent against about 40 per candidate).
+// the objects of C into words 0..u of D (broadcast by shuffles, one object at a time, over the
+// objects that lie in some live candidate's C). A word of candidates is screened only when that
+// costs fewer instructions than evaluating its candidates one by one (about 2u + 4 per object
+// against about 40 + 6(u + 1) per candidate).
 constexpr int SCREEN_PER_CAND = 40;
 
 template <int NW, int WRT, bool COUNT>
@@ -291,26 +292,33 @@ __device__ __forceinline__ void screen(SubtreeWarp &S, uint32_t (&cand)[WRT], co
                                        const uint32_t (&rowc)[NW][WRT])
 {
     const unsigned lane = threadIdx.x & 31;
-    int ne = 0;
-#pragma unroll
-    for (int t = 0; t < NW; ++t) ne += __popc(ext[t]);
 #pragma unroll
     for (int u = 0; u < WRT; ++u) {
-        if (ne * (2 * WRT + 2) >= (SCREEN_PER_CAND + 6 * WRT) * __popc(cand[u])) continue;   // uniform
-        uint32_t C[NW], D[WRT];
-#pragma unroll
-        for (int t = 0; t < NW; ++t) C[t] = ext[t] & col[u][t];
-#pragma unroll
-        for (int w = 0; w < WRT; ++w) D[w] = FULL;
+        if (cand[u] == 0u) continue;
+        // only objects in some candidate's C matter, and only the closure words up to u (the
+        // canonical test of j = 32u + lane looks at attributes below j)
+        const bool live = (cand[u] >> lane) & 1u;
+        uint32_t C[NW], E[NW];
+        int ne = 0;
 #pragma unroll
         for (int t = 0; t < NW; ++t) {
-            uint32_t e = ext[t];
+            C[t] = ext[t] & col[u][t];
+            E[t] = __reduce_or_sync(FULL, live ? C[t] : 0u);
+            ne += __popc(E[t]);
+        }
+        if (ne * (2 * u + 4) >= (SCREEN_PER_CAND + 6 * (u + 1)) * __popc(cand[u])) continue;   // uniform
+        uint32_t D[WRT];
+#pragma unroll
+        for (int w = 0; w <= u; ++w) D[w] = FULL;
+#pragma unroll
+        for (int t = 0; t < NW; ++t) {
+            uint32_t e = E[t];
             while (e) {
                 const int o = __ffs(e) - 1;
                 e &= e - 1u;
                 const bool in = (C[t] >> o) & 1u;
 #pragma unroll
-                for (int w = 0; w < WRT; ++w) {
+                for (int w = 0; w <= u; ++w) {
                     const uint32_t r = __shfl_sync(FULL, rowc[t][w], o);
                     if (in) D[w] &= r;
                 }
@@ -319,12 +327,12 @@ __device__ __forceinline__ void screen(SubtreeWarp &S, uint32_t (&cand)[WRT], co
         // canonical iff D adds no attribute below j = 32u + lane to B
         bool ok = true;
 #pragma unroll
-        for (int w = 0; w < WRT; ++w) {
-            const uint32_t below = w < u ? FULL : (w == u ? (1u << lane) - 1u : 0u);
+        for (int w = 0; w <= u; ++w) {
+            const uint32_t below = w < u ? FULL : (1u << lane) - 1u;
             ok = ok && (D[w] & ~B[w] & below) == 0u;
         }
         cand[u] &= __ballot_sync(FULL, ok);
-        if (COUNT) S.ops += (unsigned long long)ne * 2 * WRT;
+        if (COUNT) S.ops += (unsigned long long)ne * 2 * (u + 1);
     }
 }
 
