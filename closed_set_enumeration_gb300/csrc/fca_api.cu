@@ -45,7 +45,6 @@ struct fca_ctx {
     Counters *ctr = nullptr;        // device
     Counters *ctr_snap = nullptr;   // device copy taken before each bitmap-tier launch (rollback)
     Counters *ctr_host = nullptr;   // pinned host copy, read after each bitmap-tier launch
-    uint32_t *stage = nullptr;      // pinned host staging (root entry)
 
     uint32_t *host_out_dev = nullptr;   // device buffer behind fca_enumerate_host
     uint64_t host_out_rows = 0;
@@ -357,18 +356,10 @@ fca_status drain(Run &r, size_t lv)
         const uint64_t k = std::min(have, kmax);
         const uint64_t begin = have - k;
 
-        // the next level appends after its current fill; the counters as they are now are kept on
-        // the device, to be restored if the launch has to be rolled back
-        // (next_count and the launch's work cursor are adjacent: one copy sets both)
-        uint64_t *next_fill = reinterpret_cast<uint64_t *>(c->stage + 1000);
-        next_fill[0] = c->level_count[lv + 1];
-        next_fill[1] = 0;
-        static_assert(offsetof(Counters, work_head) == offsetof(Counters, next_count) + 8, "counter order");
-        CK(cudaMemcpyAsync(&c->ctr->next_count, next_fill, 2 * sizeof(uint64_t), cudaMemcpyHostToDevice, r.st),
-           "counter set");
-        CK(cudaMemsetAsync(&c->ctr->error, 0, sizeof(unsigned int), r.st), "counter set");
-        CK(cudaMemcpyAsync(c->ctr_snap, c->ctr, sizeof(Counters), cudaMemcpyDeviceToDevice, r.st),
-           "counter snapshot");
+        // the next level appends after its current fill; the counters as they are then are kept on
+        // the device, to be restored if the launch has to be rolled back (one small kernel)
+        CK((cudaError_t)launch_prepare_expand(c->ctr, c->ctr_snap, c->level_count[lv + 1], r.st),
+           "counter set-up kernel");
 
         ExpandArgs a{};
         a.d = c->d;
@@ -479,41 +470,14 @@ fca_status enumerate_impl(fca_ctx *c, uint32_t *out, uint64_t capacity, uint64_t
 
     Run r{c, out, capacity, st};
     const Dims &d = c->d;
-    // counters: the top intent already occupies output row 0
-    Counters init{};
-    init.out_count = 1;
-    if (capacity >= 1)
-        CK(cudaMemcpyAsync(out, c->top, d.wm * 4, cudaMemcpyDeviceToDevice, st), "top intent copy");
-
-    // the root node (G, G', 0)
-    if (d.n <= SMALL_MAX) {
-        const int qi = d.n <= 32 ? 0 : 1;
-        const int per = 32 << qi;
-        uint32_t *ids = c->stage;
-        for (int i = 0; i < per; ++i) ids[i] = i < d.n ? (uint32_t)i : 0u;
-        int32_t *meta = reinterpret_cast<int32_t *>(c->stage + per);
-        meta[0] = 0;
-        meta[1] = (int32_t)d.n;
-        Queue &Q = c->q[qi];
-        CK(cudaMemcpyAsync(Q.ids, ids, per * 4, cudaMemcpyHostToDevice, st), "root entry");
-        CK(cudaMemcpyAsync(Q.itt, c->top, d.wm * 4, cudaMemcpyDeviceToDevice, st), "root entry");
-        CK(cudaMemcpyAsync(Q.y, &meta[0], 4, cudaMemcpyHostToDevice, st), "root entry");
-        CK(cudaMemcpyAsync(Q.n, &meta[1], 4, cudaMemcpyHostToDevice, st), "root entry");
-        init.q_count[qi] = 1;
-        c->q_count[qi] = 1;
-    } else {
-        Level &L = c->levels[0];
-        int32_t *meta = reinterpret_cast<int32_t *>(c->stage);
-        meta[0] = 0;
-        meta[1] = (int32_t)d.n;
-        CK(cudaMemcpyAsync(L.ext, c->root_ext, d.wnp * 4, cudaMemcpyDeviceToDevice, st), "root entry");
-        CK(cudaMemcpyAsync(L.itt, c->top, d.wm * 4, cudaMemcpyDeviceToDevice, st), "root entry");
-        CK(cudaMemcpyAsync(L.y, &meta[0], 4, cudaMemcpyHostToDevice, st), "root entry");
-        CK(cudaMemcpyAsync(L.n, &meta[1], 4, cudaMemcpyHostToDevice, st), "root entry");
-        c->level_count[0] = 1;
-    }
-    *c->ctr_host = init;
-    CK(cudaMemcpyAsync(c->ctr, c->ctr_host, sizeof(Counters), cudaMemcpyHostToDevice, st), "counter write");
+    // counters (the top intent occupies output row 0) and the root node (G, G', 0): an object-list
+    // root when it has at most SMALL_MAX objects, else entry 0 of bitmap level 0 (one small kernel)
+    const int root_q = d.n <= SMALL_MAX ? (d.n <= 32 ? 0 : 1) : -1;
+    CK((cudaError_t)launch_start(c->ctr, c->top, c->root_ext, d, out, capacity, c->levels[0],
+                                 c->q[root_q < 0 ? 0 : root_q], root_q, st),
+       "start kernel");
+    if (root_q >= 0) c->q_count[root_q] = 1;
+    else c->level_count[0] = 1;
 
     if ((s = drain(r, 0)) != FCA_OK) return s;
     // The two queues are independent. The larger extents run first on the caller's stream; the
@@ -585,7 +549,6 @@ void fca_free(fca_ctx *ctx)
     cudaFree(ctx->ctr_snap);
     cudaFree(ctx->host_out_dev);
     cudaFreeHost(ctx->ctr_host);
-    cudaFreeHost(ctx->stage);
     cudaFree(ctx->flag_dev);
     delete ctx;
 }
@@ -626,8 +589,7 @@ fca_status fca_context_create(const uint32_t *rows, int64_t n_objects, int32_t n
         (s = alloc_raw(c, (void **)&c->ctr_snap, sizeof(Counters), "counter snapshot")) != FCA_OK)
         return fail(s);
     if ((s = alloc_raw(c, (void **)&c->flag_dev, sizeof(uint32_t), "flag")) != FCA_OK) return fail(s);
-    if (cudaMallocHost((void **)&c->ctr_host, sizeof(Counters)) != cudaSuccess ||
-        cudaMallocHost((void **)&c->stage, 4096) != cudaSuccess) {
+    if (cudaMallocHost((void **)&c->ctr_host, sizeof(Counters)) != cudaSuccess) {
         cudaGetLastError();
         c->err = "pinned host allocation failed";
         return fail(FCA_ERR_OOM);

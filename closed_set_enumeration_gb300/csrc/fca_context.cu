@@ -83,7 +83,70 @@ __global__ void append_bottom_kernel(const uint32_t *flag, const uint32_t *full_
         for (int w = (int)lane; w < wm; w += 32) out[slot * wm + w] = full_mask[w];
 }
 
+// Counter set-up before a bitmap-tier launch: the next level's current fill, a zero work cursor and
+// error word; then a copy of the counters, restored if the launch has to be rolled back.
+__global__ void prepare_expand_kernel(Counters *ctr, Counters *snap, unsigned long long next_fill)
+{
+    if (threadIdx.x == 0) {
+        ctr->next_count = next_fill;
+        ctr->work_head = 0ull;
+        ctr->error = 0u;
+    }
+    __syncthreads();
+    const uint32_t *src = reinterpret_cast<const uint32_t *>(ctr);
+    uint32_t *dst = reinterpret_cast<uint32_t *>(snap);
+    for (int i = (int)threadIdx.x; i < (int)(sizeof(Counters) / 4); i += (int)blockDim.x) dst[i] = src[i];
+}
+
+// Start of an enumeration: zero counters with the top intent in output row 0 (when capacity allows)
+// and the root node (G, G', 0), either as entry 0 of bitmap level 0 (qi < 0) or as the first root of
+// object-list queue qi.
+__global__ void start_kernel(Counters *ctr, const uint32_t *top, const uint32_t *root_ext, Dims d,
+                             uint32_t *out, unsigned long long capacity, Level L0, Queue Q, int qi)
+{
+    const int t = (int)threadIdx.x;
+    uint32_t *c = reinterpret_cast<uint32_t *>(ctr);
+    for (int i = t; i < (int)(sizeof(Counters) / 4); i += (int)blockDim.x) c[i] = 0u;
+    __syncthreads();
+    if (t == 0) {
+        ctr->out_count = 1ull;
+        if (qi >= 0) ctr->q_count[qi] = 1ull;
+    }
+    for (int w = t; w < d.wm; w += (int)blockDim.x) {
+        if (capacity >= 1ull) out[w] = top[w];
+        if (qi < 0) L0.itt[w] = top[w];
+        else Q.itt[w] = top[w];
+    }
+    if (qi < 0) {
+        for (long long q = t; q < d.wnp; q += blockDim.x) L0.ext[q] = root_ext[q];
+        if (t == 0) {
+            L0.y[0] = 0;
+            L0.n[0] = (int32_t)d.n;
+        }
+    } else {
+        const int per = 32 << qi;
+        for (int i = t; i < per; i += (int)blockDim.x) Q.ids[i] = i < d.n ? (uint32_t)i : 0u;
+        if (t == 0) {
+            Q.y[0] = 0;
+            Q.n[0] = (int32_t)d.n;
+        }
+    }
+}
+
 }  // namespace
+
+int launch_prepare_expand(Counters *ctr, Counters *snap, uint64_t next_fill, void *stream)
+{
+    prepare_expand_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(ctr, snap, next_fill);
+    return (int)cudaGetLastError();
+}
+
+int launch_start(Counters *ctr, const uint32_t *top, const uint32_t *root_ext, const Dims &d, uint32_t *out,
+                 uint64_t capacity, const Level &L0, const Queue &Q, int qi, void *stream)
+{
+    start_kernel<<<1, 256, 0, (cudaStream_t)stream>>>(ctr, top, root_ext, d, out, capacity, L0, Q, qi);
+    return (int)cudaGetLastError();
+}
 
 int launch_mask_rows(uint32_t *rows, const Dims &d, void *stream)
 {

@@ -216,7 +216,8 @@ __device__ __forceinline__ void finish_candidate(const ExpandArgs &a, const Dims
 // Bitmap tier. A work item is (parent, part of the attribute range). The block stages the parent's
 // non-zero extent chunks once. Extents of at most `a.restrict_max` objects are then turned into an
 // object list, and the rows of those objects are transposed into columns restricted to them (one
-// ballot per attribute and 32 objects); each candidate's C is read from those columns without any
+// 32 x 32 register transpose per row word and 32 objects); each candidate's C is read from those
+// columns without any
 // global column access. Larger extents keep the chunk list: each warp gathers column j on the
 // parent's non-zero chunks. Either way the warps of the block take the part's candidates j in turn.
 template <bool COUNT, int WARPS>
@@ -258,15 +259,16 @@ __global__ void __launch_bounds__(32 * WARPS, ExpandShape<WARPS>::blocks_per_sm)
         const unsigned long long p = a.p_begin + item / (unsigned)parts;
         const int part = (int)(item % (unsigned)parts);
         const int y = a.in.y[p];
-        // a parent small enough for restricted columns is expanded whole by its first part (the
-        // transposition is paid once), when its candidates make that cheaper than gathering
+        // this part's candidates; a parent small enough for restricted columns is expanded on them
+        // when its candidates in the part make that cheaper than gathering (the transposition is
+        // paid by every part: parts exist only when a level is too small to fill the GPU, where
+        // spreading a parent's candidates over blocks shortens the launch)
         const int np = a.in.n[p];
         const int gw = (np + 31) >> 5;
-        const bool restricted = np <= tr && (long long)(d.m - y) * min(wq, np) >= 4ll * gw * d.wm;
-        if (restricted && part > 0) continue;
-        const int j_lo = restricted ? y : max(y, part * span);
-        const int j_hi = restricted ? d.m : min(d.m, (part + 1) * span);
+        const int j_lo = max(y, part * span);
+        const int j_hi = min(d.m, (part + 1) * span);
         if (j_lo >= j_hi) continue;                       // uniform over the block
+        const bool restricted = np <= tr && (long long)(j_hi - j_lo) * min(wq, np) >= 4ll * gw * d.wm;
         // the parent intent, read by every candidate, in shared memory
         __shared__ uint32_t sB[MAX_ATTRS / 32];
         if ((int)threadIdx.x < d.wm) sB[threadIdx.x] = a.in.itt[p * d.wm + threadIdx.x];
@@ -322,12 +324,8 @@ __global__ void __launch_bounds__(32 * WARPS, ExpandShape<WARPS>::blocks_per_sm)
                 const int pidx = 32 * g + (int)lane;
                 const uint32_t v = pidx < na ? __ldg(a.rows + (size_t)oid[pidx] * d.wm + w) : 0u;
                 if (keep_rows && pidx < na) rowr[(size_t)pidx * d.wm + w] = v;
-                uint32_t mine = 0;
-#pragma unroll
-                for (int b = 0; b < 32; ++b) {
-                    const uint32_t bal = __ballot_sync(FULL, (v >> b) & 1u);
-                    if (lane == (unsigned)b) mine = bal;
-                }
+                // lane b receives the column of attribute 32w + b over these 32 objects
+                const uint32_t mine = warp_transpose32(v);
                 const int k = 32 * w + (int)lane;
                 if (k < d.m) colr[(size_t)k * G + g] = mine;
             }

@@ -114,6 +114,13 @@ int launch_top(const uint32_t *rows, uint32_t *top, uint32_t *flag_full_row, con
                void *stream);
 int launch_expand(const ExpandArgs &a, int sm_count, void *stream);
 // Append the all-attribute intent when *flag_full_row is 0 (one slot from Counters::out_count).
+// Before a bitmap-tier launch: Counters::next_count = next_fill, zero work cursor and error, then
+// the counters copied to *snap (for a rollback).
+int launch_prepare_expand(Counters *ctr, Counters *snap, uint64_t next_fill, void *stream);
+// Start of an enumeration: zero counters, the top intent in row 0, the root node as entry 0 of
+// level L0 (qi < 0) or as the first root of queue Q (queue index qi).
+int launch_start(Counters *ctr, const uint32_t *top, const uint32_t *root_ext, const Dims &d, uint32_t *out,
+                 uint64_t capacity, const Level &L0, const Queue &Q, int qi, void *stream);
 int launch_append_bottom(const uint32_t *flag_full_row, const uint32_t *full_mask, uint32_t *out,
                          uint64_t capacity, Counters *ctr, const Dims &d, void *stream);
 int launch_subtree(const SubtreeArgs &a, int nw, int sm_count, void *stream);
