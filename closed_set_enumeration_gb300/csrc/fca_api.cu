@@ -289,17 +289,20 @@ fca_status time_end(Run &r, size_t pair, cudaStream_t st)
     return FCA_OK;
 }
 
-// After the stream is idle: add the recorded launch times to the statistics.
-fca_status time_collect(fca_ctx *c)
+// The device times of the launches recorded by the last call (read when statistics are asked for,
+// so that a call does not wait on them): sums of expand and subtree launch durations in ms.
+void launch_times(const fca_ctx *c, double *expand_ms, double *subtree_ms)
 {
+    *expand_ms = *subtree_ms = 0.0;
     for (size_t i = 0; i < c->pairs_used; ++i) {
         float ms = 0.f;
-        CK(cudaEventElapsedTime(&ms, c->events[2 * i], c->events[2 * i + 1]), "cudaEventElapsedTime");
-        if (c->event_kind[i] == 0) c->stats.expand_ms += ms;
-        else c->stats.subtree_ms += ms;
+        if (cudaEventElapsedTime(&ms, c->events[2 * i], c->events[2 * i + 1]) != cudaSuccess) {
+            cudaGetLastError();
+            continue;
+        }
+        if (c->event_kind[i] == 0) *expand_ms += ms;
+        else *subtree_ms += ms;
     }
-    c->pairs_used = 0;
-    return FCA_OK;
 }
 
 fca_status read_counters(Run &r)
@@ -313,7 +316,7 @@ fca_status read_counters(Run &r)
 
 // Process every root waiting in object-list queue qi, then empty it; all on stream `st`. `share`
 // allows the launch to hand work between the warps of a block (see subtree_kernel).
-fca_status run_subtree(Run &r, int qi, cudaStream_t st, bool share = true)
+fca_status run_subtree(Run &r, int qi, cudaStream_t st, bool share = true, bool reset = true)
 {
     fca_ctx *c = r.c;
     if (c->q_count[qi] == 0) return FCA_OK;
@@ -337,9 +340,12 @@ fca_status run_subtree(Run &r, int qi, cudaStream_t st, bool share = true)
     c->stats.launches++;
     c->stats.subtree_launches++;
     c->stats.small_roots += c->q_count[qi];
-    // empty the queue: its append counter and its work cursor
-    CK(cudaMemsetAsync(&c->ctr->q_count[qi], 0, sizeof(unsigned long long), st), "queue reset");
-    CK(cudaMemsetAsync(&c->ctr->q_head[qi], 0, sizeof(unsigned long long), st), "queue reset");
+    // empty the queue: its append counter and its work cursor (not needed after the last launches
+    // of a call: the next call starts from zeroed counters)
+    if (reset) {
+        CK(cudaMemsetAsync(&c->ctr->q_count[qi], 0, sizeof(unsigned long long), st), "queue reset");
+        CK(cudaMemsetAsync(&c->ctr->q_head[qi], 0, sizeof(unsigned long long), st), "queue reset");
+    }
     c->q_count[qi] = 0;
     return FCA_OK;
 }
@@ -486,16 +492,16 @@ fca_status enumerate_impl(fca_ctx *c, uint32_t *out, uint64_t capacity, uint64_t
     // of the wider queue counted as four) may hand work between warps: helpers kept busy in the
     // lighter one would take issue slots from the heavier one, which ends the call.
     if (c->q_count[0] > 0 && c->q_count[1] > 0) {
-        CK(cudaEventRecord(c->fork, st), "cudaEventRecord");
-        CK(cudaStreamWaitEvent(c->side, c->fork, 0), "cudaStreamWaitEvent");
         const bool wide_heavier = 4 * c->q_count[1] >= c->q_count[0];
-        if ((s = run_subtree(r, 1, st, wide_heavier)) != FCA_OK) return s;
-        if ((s = run_subtree(r, 0, c->side, !wide_heavier)) != FCA_OK) return s;
+        CK(cudaEventRecord(c->fork, st), "cudaEventRecord");
+        if ((s = run_subtree(r, 1, st, wide_heavier, false)) != FCA_OK) return s;
+        CK(cudaStreamWaitEvent(c->side, c->fork, 0), "cudaStreamWaitEvent");
+        if ((s = run_subtree(r, 0, c->side, !wide_heavier, false)) != FCA_OK) return s;
         CK(cudaEventRecord(c->join, c->side), "cudaEventRecord");
         CK(cudaStreamWaitEvent(st, c->join, 0), "cudaStreamWaitEvent");
     } else {
         for (int qi = NQ - 1; qi >= 0; --qi)
-            if ((s = run_subtree(r, qi, st)) != FCA_OK) return s;
+            if ((s = run_subtree(r, qi, st, true, false)) != FCA_OK) return s;
     }
     // The bottom concept (M', M). When some object holds every attribute its extent is not empty and
     // the search reaches it. Otherwise only empty candidate extents close to it; the search skips
@@ -514,7 +520,6 @@ fca_status enumerate_impl(fca_ctx *c, uint32_t *out, uint64_t capacity, uint64_t
     c->stats.frontier_bytes = c->pool_bytes;
     c->stats.subtree_word_ops = c->ctr_host->word_ops;
     c->stats.expand_bytes = c->ctr_host->bytes;
-    if ((s = time_collect(c)) != FCA_OK) return s;
     *out_count = total;
     return total > capacity ? FCA_ERR_CAPACITY : FCA_OK;
 }
@@ -703,6 +708,8 @@ fca_status fca_get_stats(const fca_ctx *ctx, fca_stats *out)
 {
     if (!ctx || !out) return FCA_ERR_INVALID;
     *out = ctx->stats;
+    cudaSetDevice(ctx->device);
+    launch_times(ctx, &out->expand_ms, &out->subtree_ms);
     return FCA_OK;
 }
 
