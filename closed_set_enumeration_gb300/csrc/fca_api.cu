@@ -45,6 +45,12 @@ struct fca_ctx {
     Counters *ctr = nullptr;        // device
     Counters *ctr_snap = nullptr;   // device copy taken before each bitmap-tier launch (rollback)
     Counters *ctr_host = nullptr;   // pinned host copy, read after each bitmap-tier launch
+    ChainSlots *chain = nullptr;        // device records of a chain of bitmap-tier launches
+    ChainSlots *chain_host = nullptr;   // pinned host copy
+    // parents per bitmap level in the last call and its number of levels: they set how many levels
+    // are launched as one chain, and the launch shapes of the chained launches
+    std::vector<uint64_t> prev_counts, cur_counts;
+    uint64_t prev_levels = 0;
 
     uint32_t *host_out_dev = nullptr;   // device buffer behind fca_enumerate_host
     uint64_t host_out_rows = 0;
@@ -350,11 +356,100 @@ fca_status run_subtree(Run &r, int qi, cudaStream_t st, bool share = true, bool 
     return FCA_OK;
 }
 
-// Expand every entry of bitmap level `lv`, depth first.
-fca_status drain(Run &r, size_t lv)
+void count_level(fca_ctx *c, size_t lv, uint64_t k)
+{
+    if (c->cur_counts.size() <= lv) c->cur_counts.resize(lv + 1, 0);
+    c->cur_counts[lv] += k;
+    c->stats.large_parents += k;
+    c->stats.levels = std::max<uint64_t>(c->stats.levels, lv + 2);
+}
+
+// Launch levels lv .. lv+K-1 (level lv whole, the next level empty) back to back, each reading its
+// parent count on the device, and read the counters once at the end. Launches up to the first that
+// overflowed are committed; that one's counters as they were before it are restored and *failed
+// is set. *next_lv is the first level still holding parents.
+fca_status drain_chain(Run &r, size_t lv, int K, size_t *next_lv, bool *failed)
 {
     fca_ctx *c = r.c;
     fca_status s;
+    for (int i = 0; i < K; ++i)
+        if ((s = ensure_level(c, lv + i + 1)) != FCA_OK) return s;
+    const uint64_t n0 = c->level_count[lv];
+    for (int i = 0; i < K; ++i) {
+        const size_t L = lv + i;
+        CK((cudaError_t)launch_prepare_chain(c->ctr, c->chain, i, n0, r.st), "chain set-up kernel");
+        ExpandArgs a{};
+        a.d = c->d;
+        a.rows = c->rows;
+        a.cols = c->cols;
+        a.in = c->levels[L];
+        a.p_begin = 0;
+        a.p_count = i == 0 ? n0 : (L < c->prev_counts.size() ? std::max<uint64_t>(1, c->prev_counts[L]) : n0);
+        a.p_count_dev = i == 0 ? nullptr : &c->chain->pcount;
+        a.next = c->levels[L + 1];
+        for (int qi = 0; qi < NQ; ++qi) a.q[qi] = c->q[qi];
+        a.out = r.out;
+        a.capacity = r.capacity;
+        a.ctr = c->ctr;
+        a.count_work = c->count_work;
+        size_t pair = 0;
+        if ((s = time_begin(r, 0, &pair, r.st)) != FCA_OK) return s;
+        CK((cudaError_t)launch_expand(a, c->sm_count, r.st), "expand kernel launch");
+        if ((s = time_end(r, pair, r.st)) != FCA_OK) return s;
+        c->stats.launches += 2;
+        c->stats.expand_launches++;
+    }
+    CK(cudaMemcpyAsync(c->chain_host, c->chain, sizeof(ChainSlots), cudaMemcpyDeviceToHost, r.st), "chain read-back");
+    CK(cudaMemcpyAsync(c->ctr_host, c->ctr, sizeof(Counters), cudaMemcpyDeviceToHost, r.st), "counter readback");
+    CK(cudaStreamSynchronize(r.st), "stream synchronize");
+    const ChainSlots &cs = *c->chain_host;
+    const Counters &fin = *c->ctr_host;
+    int f = -1;   // the first launch after which the error word was set
+    for (int i = 0; i < K && f < 0; ++i)
+        if ((i + 1 < K ? cs.snaps[i + 1].error : fin.error) != 0u) f = i;
+    const int ok = f < 0 ? K : f;
+    for (int i = 0; i < ok; ++i) {
+        count_level(c, lv + i, cs.counts[i]);
+        const uint64_t produced = i + 1 < K ? cs.counts[i + 1] : fin.next_count;
+        c->stats.max_frontier = std::max<uint64_t>(c->stats.max_frontier, produced);
+        c->level_count[lv + i] = 0;
+    }
+    if (f < 0) {
+        c->level_count[lv + K] = fin.next_count;
+        for (int qi = 0; qi < NQ; ++qi) c->q_count[qi] = fin.q_count[qi];
+        *next_lv = lv + K;
+        *failed = false;
+        return FCA_OK;
+    }
+    // launch f overflowed a destination: the counters come back as they were before it, its parents
+    // wait again in level lv+f, and the caller continues there launch by launch
+    CK(cudaMemcpyAsync(c->ctr, &c->chain->snaps[f], sizeof(Counters), cudaMemcpyDeviceToDevice, r.st),
+       "counter restore");
+    c->level_count[lv + f] = cs.counts[f];
+    c->level_count[lv + f + 1] = 0;
+    for (int qi = 0; qi < NQ; ++qi) c->q_count[qi] = cs.snaps[f].q_count[qi];
+    c->stats.retries++;
+    *next_lv = lv + f;
+    *failed = true;
+    return FCA_OK;
+}
+
+// Expand every entry of bitmap level `lv`, depth first. With `chain`, a whole level whose next
+// level is empty starts a chain of launches as deep as the last call's search (drain_chain).
+fca_status drain(Run &r, size_t lv, bool chain = true)
+{
+    fca_ctx *c = r.c;
+    fca_status s;
+    if (chain && c->level_count[lv] > 0 && (lv + 1 >= c->levels.size() || c->level_count[lv + 1] == 0) &&
+        c->prev_levels > lv + 2) {
+        const int K = (int)std::min<uint64_t>(CHAIN_MAX, c->prev_levels - 1 - lv);
+        size_t next = lv;
+        bool failed = false;
+        if ((s = drain_chain(r, lv, K, &next, &failed)) != FCA_OK) return s;
+        if (failed) return drain(r, next, false);
+        if (next < c->levels.size() && c->level_count[next] > 0) return drain(r, next);
+        return FCA_OK;
+    }
     uint64_t kmax = ~(uint64_t)0;    // chunk limit, lowered only when the pools may not grow
     while (c->level_count[lv] > 0) {
         if ((s = ensure_level(c, lv + 1)) != FCA_OK) return s;
@@ -384,7 +479,7 @@ fca_status drain(Run &r, size_t lv)
         if ((s = time_begin(r, 0, &pair, r.st)) != FCA_OK) return s;
         CK((cudaError_t)launch_expand(a, c->sm_count, r.st), "expand kernel launch");
         if ((s = time_end(r, pair, r.st)) != FCA_OK) return s;
-        c->stats.launches++;
+        c->stats.launches += 2;   // counter set-up and expand
         c->stats.expand_launches++;
         if ((s = read_counters(r)) != FCA_OK) return s;
         const Counters after = *c->ctr_host;
@@ -437,8 +532,7 @@ fca_status drain(Run &r, size_t lv)
         c->level_count[lv] = begin;
         c->level_count[lv + 1] = after.next_count;
         for (int qi = 0; qi < NQ; ++qi) c->q_count[qi] = after.q_count[qi];
-        c->stats.large_parents += k;
-        c->stats.levels = std::max<uint64_t>(c->stats.levels, lv + 2);
+        count_level(c, lv, k);
         c->stats.max_frontier = std::max<uint64_t>(c->stats.max_frontier, c->level_count[lv + 1]);
     }
     if (lv + 1 < c->levels.size() && c->level_count[lv + 1] > 0) return drain(r, lv + 1);
@@ -468,6 +562,7 @@ fca_status enumerate_impl(fca_ctx *c, uint32_t *out, uint64_t capacity, uint64_t
     CK(cudaSetDevice(c->device), "cudaSetDevice");
     fca_status s;
     c->stats = fca_stats{};
+    std::fill(c->cur_counts.begin(), c->cur_counts.end(), 0);
     c->pairs_used = 0;
     if ((s = ensure_queues(c)) != FCA_OK) return s;
     if ((s = ensure_level(c, 0)) != FCA_OK) return s;
@@ -482,6 +577,7 @@ fca_status enumerate_impl(fca_ctx *c, uint32_t *out, uint64_t capacity, uint64_t
     CK((cudaError_t)launch_start(c->ctr, c->top, c->root_ext, d, out, capacity, c->levels[0],
                                  c->q[root_q < 0 ? 0 : root_q], root_q, st),
        "start kernel");
+    c->stats.launches++;
     if (root_q >= 0) c->q_count[root_q] = 1;
     else c->level_count[0] = 1;
 
@@ -521,6 +617,8 @@ fca_status enumerate_impl(fca_ctx *c, uint32_t *out, uint64_t capacity, uint64_t
     c->stats.subtree_word_ops = c->ctr_host->word_ops;
     c->stats.expand_bytes = c->ctr_host->bytes;
     *out_count = total;
+    c->prev_counts = c->cur_counts;
+    c->prev_levels = c->stats.levels;
     return total > capacity ? FCA_ERR_CAPACITY : FCA_OK;
 }
 
@@ -552,6 +650,8 @@ void fca_free(fca_ctx *ctx)
     if (ctx->side) cudaStreamDestroy(ctx->side);
     cudaFree(ctx->ctr);
     cudaFree(ctx->ctr_snap);
+    cudaFree(ctx->chain);
+    cudaFreeHost(ctx->chain_host);
     cudaFree(ctx->host_out_dev);
     cudaFreeHost(ctx->ctr_host);
     cudaFree(ctx->flag_dev);
@@ -591,10 +691,12 @@ fca_status fca_context_create(const uint32_t *rows, int64_t n_objects, int32_t n
         (s = alloc_raw(c, (void **)&c->full_mask, (size_t)d.wm * 4, "mask")) != FCA_OK ||
         (s = alloc_raw(c, (void **)&c->root_ext, (size_t)d.wnp * 4, "root extent")) != FCA_OK ||
         (s = alloc_raw(c, (void **)&c->ctr, sizeof(Counters), "counters")) != FCA_OK ||
-        (s = alloc_raw(c, (void **)&c->ctr_snap, sizeof(Counters), "counter snapshot")) != FCA_OK)
+        (s = alloc_raw(c, (void **)&c->ctr_snap, sizeof(Counters), "counter snapshot")) != FCA_OK ||
+        (s = alloc_raw(c, (void **)&c->chain, sizeof(ChainSlots), "chain records")) != FCA_OK)
         return fail(s);
     if ((s = alloc_raw(c, (void **)&c->flag_dev, sizeof(uint32_t), "flag")) != FCA_OK) return fail(s);
-    if (cudaMallocHost((void **)&c->ctr_host, sizeof(Counters)) != cudaSuccess) {
+    if (cudaMallocHost((void **)&c->ctr_host, sizeof(Counters)) != cudaSuccess ||
+        cudaMallocHost((void **)&c->chain_host, sizeof(ChainSlots)) != cudaSuccess) {
         cudaGetLastError();
         c->err = "pinned host allocation failed";
         return fail(FCA_ERR_OOM);

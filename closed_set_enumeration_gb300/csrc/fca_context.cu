@@ -98,6 +98,24 @@ __global__ void prepare_expand_kernel(Counters *ctr, Counters *snap, unsigned lo
     for (int i = (int)threadIdx.x; i < (int)(sizeof(Counters) / 4); i += (int)blockDim.x) dst[i] = src[i];
 }
 
+// Before launch i of a chain of bitmap-tier launches (see ChainSlots).
+__global__ void prepare_chain_kernel(Counters *ctr, ChainSlots *cs, int i, unsigned long long n0)
+{
+    if (threadIdx.x == 0) {
+        unsigned long long pc = i == 0 ? n0 : ctr->next_count;
+        if (i == 0) ctr->error = 0u;
+        else if (ctr->error) pc = 0ull;     // an earlier launch of the chain overflowed: no work
+        cs->counts[i] = pc;
+        cs->pcount = pc;
+        ctr->next_count = 0ull;
+        ctr->work_head = 0ull;
+    }
+    __syncthreads();
+    const uint32_t *src = reinterpret_cast<const uint32_t *>(ctr);
+    uint32_t *dst = reinterpret_cast<uint32_t *>(&cs->snaps[i]);
+    for (int w = (int)threadIdx.x; w < (int)(sizeof(Counters) / 4); w += (int)blockDim.x) dst[w] = src[w];
+}
+
 // Start of an enumeration: zero counters with the top intent in output row 0 (when capacity allows)
 // and the root node (G, G', 0), either as entry 0 of bitmap level 0 (qi < 0) or as the first root of
 // object-list queue qi.
@@ -138,6 +156,12 @@ __global__ void start_kernel(Counters *ctr, const uint32_t *top, const uint32_t 
 int launch_prepare_expand(Counters *ctr, Counters *snap, uint64_t next_fill, void *stream)
 {
     prepare_expand_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(ctr, snap, next_fill);
+    return (int)cudaGetLastError();
+}
+
+int launch_prepare_chain(Counters *ctr, ChainSlots *cs, int i, uint64_t n0, void *stream)
+{
+    prepare_chain_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(ctr, cs, i, n0);
     return (int)cudaGetLastError();
 }
 

@@ -213,6 +213,15 @@ __device__ __forceinline__ void finish_candidate(const ExpandArgs &a, const Dims
     }
 }
 
+// Parts per parent: each parent's attribute range is split when there are too few parents to fill
+// the GPU (two work items per resident block), with at least one candidate per warp in a part.
+__host__ __device__ inline int expand_parts(unsigned long long p_count, unsigned long long resident, int max_parts)
+{
+    const unsigned long long pc = p_count > 0 ? p_count : 1;
+    const unsigned long long want = (2 * resident + pc - 1) / pc;
+    return (int)(want < 1 ? 1 : (want > (unsigned long long)max_parts ? (unsigned long long)max_parts : want));
+}
+
 // Bitmap tier. A work item is (parent, part of the attribute range). The block stages the parent's
 // non-zero extent chunks once. Extents of at most `a.restrict_max` objects are then turned into an
 // object list, and the rows of those objects are transposed into columns restricted to them (one
@@ -244,9 +253,13 @@ __global__ void __launch_bounds__(32 * WARPS, ExpandShape<WARPS>::blocks_per_sm)
 
     unsigned long long my_closures = 0, my_bytes = 0;
     unsigned loads = 0;   // uint4 loads of columns by this lane (counting only)
-    const int parts = a.parts;
+    // the parent count: given, or (a launch queued behind the one producing this level) read from
+    // the device; then the parts per parent, as the launcher would choose them
+    const unsigned long long p_count = a.p_count_dev ? *a.p_count_dev : a.p_count;
+    const int parts = a.parts > 0 ? a.parts
+                                  : expand_parts(p_count, a.resident, max(1, d.m / wpb));
     const int span = (d.m + parts - 1) / parts;
-    const unsigned long long items = a.p_count * (unsigned long long)parts;
+    const unsigned long long items = p_count * (unsigned long long)parts;
     __shared__ unsigned long long next_item;
     for (;;) {
         // work items are dealt one at a time from a launch-wide cursor, so the blocks that draw
@@ -525,11 +538,15 @@ static int launch_expand_t(const ExpandArgs &a, int sm_count, void *stream)
     ExpandArgs b = a;
     b.restrict_max = tr;
     const unsigned long long resident = (unsigned long long)sm_count * per_sm;
-    const unsigned long long pc = std::max<unsigned long long>(1, a.p_count);
     const int max_parts = std::max(1, a.d.m / wpb);
-    b.parts = (int)std::min<unsigned long long>(max_parts, std::max<unsigned long long>(1, (2 * resident + pc - 1) / pc));
-    const unsigned long long items = a.p_count * (unsigned long long)b.parts;
-    unsigned long long blocks = std::min<unsigned long long>(items, resident);
+    b.resident = resident;
+    // with the count on the device the kernel chooses the parts; the grid is sized by the count
+    // the caller expects
+    b.parts = a.p_count_dev ? 0 : expand_parts(a.p_count, resident, max_parts);
+    const unsigned long long items = a.p_count * (unsigned long long)(b.parts > 0 ? b.parts : expand_parts(a.p_count, resident, max_parts));
+    // a launch that reads its count on the device gets the whole resident wave (blocks without work
+    // leave at once)
+    unsigned long long blocks = a.p_count_dev ? resident : std::min<unsigned long long>(items, resident);
     if (blocks < 1) blocks = 1;
     expand_bitmap_kernel<COUNT, WARPS><<<(unsigned)blocks, wpb * 32, smem, (cudaStream_t)stream>>>(b);
     return (int)cudaGetLastError();

@@ -49,6 +49,15 @@ struct Counters {
     unsigned int pad[2];
 };
 
+// Device records of a chain of bitmap-tier launches queued without host synchronisation between
+// them: the parent count of each launch and the counters as they were before it.
+constexpr int CHAIN_MAX = 32;
+struct ChainSlots {
+    unsigned long long pcount;               // parent count of the launch being run
+    unsigned long long counts[CHAIN_MAX];    // parent count of launch i (0 after a failed launch)
+    Counters snaps[CHAIN_MAX];               // counters before launch i
+};
+
 // A bitmap-tier frontier level (structure of arrays).
 struct Level {
     uint32_t *ext;   // cap x wnp words (bitmap extents, 16-byte aligned rows)
@@ -81,7 +90,12 @@ struct ExpandArgs {
     const uint32_t *cols;   // m x wnp
     Level in;               // parents
     uint64_t p_begin, p_count;
-    int parts;              // work items per parent: parts of the attribute range (set by the launcher)
+    // when not null, the parent count is read here on the device (a launch queued behind the one
+    // that produces its level); p_count is then only the launcher's estimate for the grid size
+    const unsigned long long *p_count_dev;
+    int parts;              // work items per parent: parts of the attribute range (set by the launcher;
+                            // 0: chosen by the kernel from the device count)
+    unsigned long long resident;   // resident blocks of the launch (set by the launcher)
     int restrict_max;       // largest extent rebuilt as restricted columns (set by the launcher)
     Level next;             // children with more than SMALL_MAX objects
     Queue q[NQ];            // children with <= 32 << q objects
@@ -121,6 +135,10 @@ int launch_prepare_expand(Counters *ctr, Counters *snap, uint64_t next_fill, voi
 // level L0 (qi < 0) or as the first root of queue Q (queue index qi).
 int launch_start(Counters *ctr, const uint32_t *top, const uint32_t *root_ext, const Dims &d, uint32_t *out,
                  uint64_t capacity, const Level &L0, const Queue &Q, int qi, void *stream);
+// Before launch i of a chain: its parent count (n0 for the first, else the previous launch's
+// next_count; 0 once a launch of the chain has overflowed), zero next level fill and cursor, and
+// the counters copied to cs->snaps[i].
+int launch_prepare_chain(Counters *ctr, ChainSlots *cs, int i, uint64_t n0, void *stream);
 int launch_append_bottom(const uint32_t *flag_full_row, const uint32_t *full_mask, uint32_t *out,
                          uint64_t capacity, Counters *ctr, const Dims &d, void *stream);
 int launch_subtree(const SubtreeArgs &a, int nw, int sm_count, void *stream);

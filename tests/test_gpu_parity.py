@@ -206,6 +206,40 @@ def test_small_pools_roll_back_and_chunk(monkeypatch, limit):
     assert st["retries"] > 0
 
 
+def test_chained_levels_roll_back(monkeypatch):
+    # After a first call, bitmap levels are launched as one chain as deep as that call's search.
+    # A second table of the same shape with a deeper, larger search overflows the (tiny) pools
+    # inside such a chain: the chain is committed up to the launch that overflowed, which is rolled
+    # back and retried launch by launch; a third call on the same table then chains without
+    # overflowing.
+    from closed_set_enumeration_gb300 import fca
+    n, m = 4000, 60
+    rows_a = cx.random_context(n, m, 0.10, 21)
+    rows_a[: n // 5, 0] |= np.uint32(0x000F000F)
+    rows_b = cx.random_context(n, m, 0.12, 22)
+    rows_b[: n // 3, 0] |= np.uint32(0x00FF00FF)
+    ref_a = oracle.cbo(rows_a, n, m, threads=8)
+    ref_b = oracle.cbo(rows_b, n, m, threads=8)
+    monkeypatch.setenv("FCA_LEVEL_BYTES", "1")
+    monkeypatch.setenv("FCA_QUEUE_ENTRIES", "1")
+    wm = (m + 31) // 32
+    with fca.Context(rows_a, n, m) as ctx:
+        got = ctx.enumerate(capacity=ref_a["intents"].shape[0] + 1).cpu().numpy().view(np.uint32).reshape(-1, wm)
+        assert same_set(got, ref_a["intents"])
+        assert ctx.stats()["levels"] >= 4
+        ctx.load(rows_b)
+        retries = []
+        for _ in range(2):
+            got = ctx.enumerate(capacity=ref_b["intents"].shape[0] + 1).cpu().numpy().view(np.uint32).reshape(-1, wm)
+            st = ctx.stats()
+            retries.append(st["retries"])
+            assert not has_duplicates(got)
+            assert same_set(got, ref_b["intents"])
+            assert st["closures"] == ref_b["closures"]
+        # the second table's first call overflowed, the last one reused the grown pools
+        assert retries[0] > 0 and retries[1] == 0
+
+
 @pytest.mark.parametrize("name", ["tiny", "sparse"])
 def test_workload_full_set(name):
     w = cx.WORKLOADS[name]
