@@ -51,6 +51,7 @@ struct fca_ctx {
     // are launched as one chain, and the launch shapes of the chained launches
     std::vector<uint64_t> prev_counts, cur_counts;
     uint64_t prev_levels = 0;
+    uint64_t prev_q[NQ]{}, last_q[NQ]{};   // roots of the last object-list launches (last call, this one)
 
     uint32_t *host_out_dev = nullptr;   // device buffer behind fca_enumerate_host
     uint64_t host_out_rows = 0;
@@ -322,17 +323,21 @@ fca_status read_counters(Run &r)
 
 // Process every root waiting in object-list queue qi, then empty it; all on stream `st`. `share`
 // allows the launch to hand work between the warps of a block (see subtree_kernel).
-fca_status run_subtree(Run &r, int qi, cudaStream_t st, bool share = true, bool reset = true)
+// With `guarded`, the root count is read on the device and the launch does nothing unless the
+// bitmap search ended cleanly (a launch queued before the host knew; see SubtreeArgs::guard).
+fca_status run_subtree(Run &r, int qi, cudaStream_t st, bool share = true, bool reset = true, bool guarded = false)
 {
     fca_ctx *c = r.c;
-    if (c->q_count[qi] == 0) return FCA_OK;
+    if (!guarded && c->q_count[qi] == 0) return FCA_OK;
     const int nw = 1 << qi;
     fca_status s;
     SubtreeArgs a{};
     a.d = c->d;
     a.rows = c->rows;
     a.q = c->q[qi];
-    a.q_count = c->q_count[qi];
+    a.q_count = guarded ? std::max<uint64_t>(1, c->prev_q[qi]) : c->q_count[qi];
+    a.q_count_dev = guarded ? &c->ctr->q_count[qi] : nullptr;
+    a.guard = guarded ? 1 : 0;
     a.q_index = qi;
     a.out = r.out;
     a.capacity = r.capacity;
@@ -345,7 +350,10 @@ fca_status run_subtree(Run &r, int qi, cudaStream_t st, bool share = true, bool 
     if ((s = time_end(r, pair, st)) != FCA_OK) return s;
     c->stats.launches++;
     c->stats.subtree_launches++;
-    c->stats.small_roots += c->q_count[qi];
+    if (!guarded) {
+        c->stats.small_roots += c->q_count[qi];
+        c->last_q[qi] = c->q_count[qi];
+    }
     // empty the queue: its append counter and its work cursor (not needed after the last launches
     // of a call: the next call starts from zeroed counters)
     if (reset) {
@@ -368,7 +376,7 @@ void count_level(fca_ctx *c, size_t lv, uint64_t k)
 // parent count on the device, and read the counters once at the end. Launches up to the first that
 // overflowed are committed; that one's counters as they were before it are restored and *failed
 // is set. *next_lv is the first level still holding parents.
-fca_status drain_chain(Run &r, size_t lv, int K, size_t *next_lv, bool *failed)
+fca_status enqueue_chain(Run &r, size_t lv, int K)
 {
     fca_ctx *c = r.c;
     fca_status s;
@@ -399,6 +407,14 @@ fca_status drain_chain(Run &r, size_t lv, int K, size_t *next_lv, bool *failed)
         c->stats.launches += 2;
         c->stats.expand_launches++;
     }
+    return FCA_OK;
+}
+
+// Read back the records of a chain queued by enqueue_chain (and the counters, after whatever was
+// queued behind it), commit it up to the first launch that overflowed, and restore that one.
+fca_status collect_chain(Run &r, size_t lv, int K, size_t *next_lv, bool *failed)
+{
+    fca_ctx *c = r.c;
     CK(cudaMemcpyAsync(c->chain_host, c->chain, sizeof(ChainSlots), cudaMemcpyDeviceToHost, r.st), "chain read-back");
     CK(cudaMemcpyAsync(c->ctr_host, c->ctr, sizeof(Counters), cudaMemcpyDeviceToHost, r.st), "counter readback");
     CK(cudaStreamSynchronize(r.st), "stream synchronize");
@@ -432,6 +448,13 @@ fca_status drain_chain(Run &r, size_t lv, int K, size_t *next_lv, bool *failed)
     *next_lv = lv + f;
     *failed = true;
     return FCA_OK;
+}
+
+fca_status drain_chain(Run &r, size_t lv, int K, size_t *next_lv, bool *failed)
+{
+    fca_status s = enqueue_chain(r, lv, K);
+    if (s != FCA_OK) return s;
+    return collect_chain(r, lv, K, next_lv, failed);
 }
 
 // Expand every entry of bitmap level `lv`, depth first. With `chain`, a whole level whose next
@@ -556,6 +579,33 @@ fca_status load_table(fca_ctx *c, const uint32_t *rows, cudaStream_t st)
     return FCA_OK;
 }
 
+// The roots left in the two queues: one launch each. The larger extents run first on the caller's
+// stream; the smaller ones on a side stream, so their blocks take the SMs that the last long
+// subtrees of the first launch leave idle. The caller's stream waits for both. Only the heavier
+// launch (a root of the wider queue counted as four) may hand work between warps: helpers kept busy
+// in the lighter one would take issue slots from the heavier one, which ends the call. `guarded`:
+// counts read on the device, estimates from the last call (see run_subtree).
+fca_status final_launches(Run &r, bool guarded)
+{
+    fca_ctx *c = r.c;
+    fca_status s;
+    const uint64_t q0 = guarded ? c->prev_q[0] : c->q_count[0];
+    const uint64_t q1 = guarded ? c->prev_q[1] : c->q_count[1];
+    if (guarded || (q0 > 0 && q1 > 0)) {
+        const bool wide_heavier = 4 * q1 >= q0;
+        CK(cudaEventRecord(c->fork, r.st), "cudaEventRecord");
+        if ((s = run_subtree(r, 1, r.st, wide_heavier, false, guarded)) != FCA_OK) return s;
+        CK(cudaStreamWaitEvent(c->side, c->fork, 0), "cudaStreamWaitEvent");
+        if ((s = run_subtree(r, 0, c->side, !wide_heavier, false, guarded)) != FCA_OK) return s;
+        CK(cudaEventRecord(c->join, c->side), "cudaEventRecord");
+        CK(cudaStreamWaitEvent(r.st, c->join, 0), "cudaStreamWaitEvent");
+        return FCA_OK;
+    }
+    for (int qi = NQ - 1; qi >= 0; --qi)
+        if ((s = run_subtree(r, qi, r.st, true, false)) != FCA_OK) return s;
+    return FCA_OK;
+}
+
 fca_status enumerate_impl(fca_ctx *c, uint32_t *out, uint64_t capacity, uint64_t *out_count,
                           cudaStream_t st)
 {
@@ -567,7 +617,7 @@ fca_status enumerate_impl(fca_ctx *c, uint32_t *out, uint64_t capacity, uint64_t
     if ((s = ensure_queues(c)) != FCA_OK) return s;
     if ((s = ensure_level(c, 0)) != FCA_OK) return s;
     for (size_t i = 0; i < c->levels.size(); ++i) c->level_count[i] = 0;
-    for (int qi = 0; qi < NQ; ++qi) c->q_count[qi] = 0;
+    for (int qi = 0; qi < NQ; ++qi) c->q_count[qi] = c->last_q[qi] = 0;
 
     Run r{c, out, capacity, st};
     const Dims &d = c->d;
@@ -581,31 +631,43 @@ fca_status enumerate_impl(fca_ctx *c, uint32_t *out, uint64_t capacity, uint64_t
     if (root_q >= 0) c->q_count[root_q] = 1;
     else c->level_count[0] = 1;
 
-    if ((s = drain(r, 0)) != FCA_OK) return s;
-    // The two queues are independent. The larger extents run first on the caller's stream; the
-    // smaller ones on a side stream, so their blocks take the SMs that the last long subtrees of the
-    // first launch leave idle. The caller's stream waits for both. Only the heavier launch (a root
-    // of the wider queue counted as four) may hand work between warps: helpers kept busy in the
-    // lighter one would take issue slots from the heavier one, which ends the call.
-    if (c->q_count[0] > 0 && c->q_count[1] > 0) {
-        const bool wide_heavier = 4 * c->q_count[1] >= c->q_count[0];
-        CK(cudaEventRecord(c->fork, st), "cudaEventRecord");
-        if ((s = run_subtree(r, 1, st, wide_heavier, false)) != FCA_OK) return s;
-        CK(cudaStreamWaitEvent(c->side, c->fork, 0), "cudaStreamWaitEvent");
-        if ((s = run_subtree(r, 0, c->side, !wide_heavier, false)) != FCA_OK) return s;
-        CK(cudaEventRecord(c->join, c->side), "cudaEventRecord");
-        CK(cudaStreamWaitEvent(st, c->join, 0), "cudaStreamWaitEvent");
-    } else {
-        for (int qi = NQ - 1; qi >= 0; --qi)
-            if ((s = run_subtree(r, qi, st, true, false)) != FCA_OK) return s;
+    // When the last call's bitmap search fit in one chain, queue it and, behind it, the last
+    // object-list launches and the bottom concept, guarded on the device: they run only if the
+    // chain ends the bitmap search cleanly (no overflow, no deeper level). One read-back then ends
+    // the call; otherwise they did nothing and the search goes on as below.
+    bool finished = false;
+    if (root_q < 0 && c->prev_levels > 2) {
+        const int K = (int)std::min<uint64_t>(CHAIN_MAX, c->prev_levels - 1);
+        size_t next = 0;
+        bool failed = false;
+        if ((s = enqueue_chain(r, 0, K)) != FCA_OK) return s;
+        if ((s = final_launches(r, true)) != FCA_OK) return s;
+        CK((cudaError_t)launch_append_bottom(c->flag_dev, c->full_mask, out, capacity, c->ctr, d, st, 1),
+           "bottom kernel");
+        c->stats.launches++;
+        if ((s = collect_chain(r, 0, K, &next, &failed)) != FCA_OK) return s;
+        if (!failed && (next >= c->levels.size() || c->level_count[next] == 0)) {
+            finished = true;
+            for (int qi = 0; qi < NQ; ++qi) {
+                c->stats.small_roots += c->ctr_host->q_count[qi];
+                c->last_q[qi] = c->ctr_host->q_count[qi];
+            }
+        } else if ((s = drain(r, next, !failed)) != FCA_OK) {
+            return s;
+        }
+    } else if ((s = drain(r, 0)) != FCA_OK) {
+        return s;
     }
-    // The bottom concept (M', M). When some object holds every attribute its extent is not empty and
-    // the search reaches it. Otherwise only empty candidate extents close to it; the search skips
-    // those, and it is appended here (a concept is output exactly once either way).
-    CK((cudaError_t)launch_append_bottom(c->flag_dev, c->full_mask, out, capacity, c->ctr, d, st),
-       "bottom kernel");
-    c->stats.launches++;
-    if ((s = read_counters(r)) != FCA_OK) return s;
+    if (!finished) {
+        if ((s = final_launches(r, false)) != FCA_OK) return s;
+        // The bottom concept (M', M). When some object holds every attribute its extent is not
+        // empty and the search reaches it. Otherwise only empty candidate extents close to it; the
+        // search skips those, and it is appended here (a concept is output exactly once either way).
+        CK((cudaError_t)launch_append_bottom(c->flag_dev, c->full_mask, out, capacity, c->ctr, d, st),
+           "bottom kernel");
+        c->stats.launches++;
+        if ((s = read_counters(r)) != FCA_OK) return s;
+    }
     if (c->ctr_host->fault & FAULT_WAIT) {
         c->err = "object-list kernel: a warp waited past its limit for work from its block";
         return FCA_ERR_CUDA;
@@ -619,6 +681,7 @@ fca_status enumerate_impl(fca_ctx *c, uint32_t *out, uint64_t capacity, uint64_t
     *out_count = total;
     c->prev_counts = c->cur_counts;
     c->prev_levels = c->stats.levels;
+    for (int qi = 0; qi < NQ; ++qi) c->prev_q[qi] = c->last_q[qi];
     return total > capacity ? FCA_ERR_CAPACITY : FCA_OK;
 }
 

@@ -72,8 +72,9 @@ __global__ void top_kernel(const uint32_t *__restrict__ rows, uint32_t *top, uin
 
 // The bottom concept when its extent is empty (no row holds every attribute): one more row.
 __global__ void append_bottom_kernel(const uint32_t *flag, const uint32_t *full_mask, uint32_t *out,
-                                     unsigned long long capacity, Counters *ctr, int wm)
+                                     unsigned long long capacity, Counters *ctr, int wm, int guard)
 {
+    if (guard && (ctr->error != 0u || ctr->next_count != 0ull)) return;   // the search did not end here
     if (*flag) return;   // some object holds every attribute: the search has output it
     const unsigned lane = threadIdx.x & 31;
     unsigned long long slot = 0;
@@ -190,9 +191,9 @@ int launch_transpose(const uint32_t *rows, uint32_t *cols, const Dims &d, void *
 }
 
 int launch_append_bottom(const uint32_t *flag, const uint32_t *full_mask, uint32_t *out, uint64_t capacity,
-                         Counters *ctr, const Dims &d, void *stream)
+                         Counters *ctr, const Dims &d, void *stream, int guard)
 {
-    append_bottom_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(flag, full_mask, out, capacity, ctr, d.wm);
+    append_bottom_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(flag, full_mask, out, capacity, ctr, d.wm, guard);
     return (int)cudaGetLastError();
 }
 

@@ -109,7 +109,10 @@ struct SubtreeArgs {
     Dims d;
     const uint32_t *rows;
     Queue q;
-    uint64_t q_count;
+    uint64_t q_count;       // roots (the launcher's estimate when q_count_dev is set)
+    const unsigned long long *q_count_dev;   // when not null, the root count is read here
+    int guard;              // 1: do nothing unless the bitmap search ended cleanly (Counters::error
+                            // and next_count both zero): a launch queued before the host knew
     int q_index;            // which q_head counter this queue uses
     int slices;             // work items per root (set by the launcher)
     int share;              // 1: warps may hand work to idle warps of their block (the launcher
@@ -139,8 +142,9 @@ int launch_start(Counters *ctr, const uint32_t *top, const uint32_t *root_ext, c
 // next_count; 0 once a launch of the chain has overflowed), zero next level fill and cursor, and
 // the counters copied to cs->snaps[i].
 int launch_prepare_chain(Counters *ctr, ChainSlots *cs, int i, uint64_t n0, void *stream);
+// With guard, only when Counters::error and next_count are both zero (see SubtreeArgs::guard).
 int launch_append_bottom(const uint32_t *flag_full_row, const uint32_t *full_mask, uint32_t *out,
-                         uint64_t capacity, Counters *ctr, const Dims &d, void *stream);
+                         uint64_t capacity, Counters *ctr, const Dims &d, void *stream, int guard = 0);
 int launch_subtree(const SubtreeArgs &a, int nw, int sm_count, void *stream);
 // The same with work sharing inside blocks, for a launch whose slices are already set in `b`
 // (called by launch_subtree; rw = register words of the search, 2, 4 or 8).

@@ -569,6 +569,8 @@ __device__ void dfs_smem(SubtreeWarp &S, int R, int n, int jn, int slices, int s
 template <int NW, bool COUNT, int RW, bool SHARE>
 __global__ void __launch_bounds__(256, RW > 4 ? 3 : 4) subtree_kernel(SubtreeArgs a)
 {
+    // a launch queued before the host knew whether the bitmap search had ended cleanly
+    if (a.guard && (a.ctr->error != 0u || a.ctr->next_count != 0ull)) return;
     uint32_t *const smw = subtree_smem + (SHARE ? HDR_WORDS : 0);
     const Dims d = a.d;
     const SubtreeLayout L(d, NW);
@@ -602,7 +604,8 @@ __global__ void __launch_bounds__(256, RW > 4 ? 3 : 4) subtree_kernel(SubtreeArg
     S.ops = 0;
     const int mp = L.mp, WM = d.wm, PER = 32 * NW;
 
-    const unsigned long long items = a.q_count * (unsigned long long)a.slices;
+    const unsigned long long q_count = a.q_count_dev ? *a.q_count_dev : a.q_count;
+    const unsigned long long items = q_count * (unsigned long long)a.slices;
     // Guided self-scheduling: a warp claims a run of consecutive items with one atomic, a quarter of
     // its share of what was left at its last claim (so claims shrink to single items near the end),
     // which keeps the launch-wide cursor from becoming a hot spot when items are short.
@@ -841,7 +844,8 @@ static int launch_subtree_kernel(const SubtreeArgs &b, int sm_count, void *strea
     size_t smem = 0;
     int e = subtree_shape<NW, COUNT, RW, SHARE>(b.d, &wpb, &smem, &per_sm);
     if (e != (int)cudaSuccess) return e;
-    unsigned long long blocks = (b.q_count * b.slices + wpb - 1) / wpb;
+    // a launch reading its root count on the device gets the whole resident wave
+    unsigned long long blocks = b.q_count_dev ? ~0ull : (b.q_count * b.slices + wpb - 1) / wpb;
     const unsigned long long cap = (unsigned long long)sm_count * per_sm;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
