@@ -35,7 +35,7 @@ struct fca_ctx {
     uint32_t *top = nullptr;       // wm
     uint32_t *full_mask = nullptr; // wm: every attribute (the bottom intent)
     uint32_t *root_ext = nullptr;  // wnp: every object
-    uint32_t *flag_dev = nullptr;  // device: some row holds every attribute
+    uint32_t *botext = nullptr;    // wn: objects holding every attribute (the bottom extent)
 
     // work pools, allocated on first use, grown on demand and kept for later calls
     std::vector<Level> levels;
@@ -568,14 +568,18 @@ fca_status load_table(fca_ctx *c, const uint32_t *rows, cudaStream_t st)
 {
     const Dims &d = c->d;
     CK(cudaSetDevice(c->device), "cudaSetDevice");
-    CK(cudaMemcpyAsync(c->rows, rows, (size_t)d.n * d.wm * 4, cudaMemcpyDefault, st), "row copy");
-    CK(cudaMemsetAsync(c->cols, 0, (size_t)d.m * d.wnp * 4, st), "column clear");
-    CK(cudaMemcpyAsync(c->top, c->full_mask, d.wm * 4, cudaMemcpyDeviceToDevice, st), "top reset");
-    CK(cudaMemsetAsync(c->flag_dev, 0, sizeof(uint32_t), st), "flag clear");
-    CK((cudaError_t)launch_mask_rows(c->rows, d, st), "padding mask kernel");
-    CK((cudaError_t)launch_transpose(c->rows, c->cols, d, st), "transpose kernel");
-    CK((cudaError_t)launch_top(c->rows, c->top, c->flag_dev, d, st), "top kernel");
-    c->table_launches = 2 + ((d.m & 31) ? 1 : 0);
+    // device rows are read in place by the table kernel; other memory is copied in first
+    cudaPointerAttributes pa{};
+    const bool on_device = cudaPointerGetAttributes(&pa, rows) == cudaSuccess && pa.type == cudaMemoryTypeDevice &&
+                           pa.device == c->device;
+    cudaGetLastError();
+    const uint32_t *src = rows;
+    if (!on_device) {
+        CK(cudaMemcpyAsync(c->rows, rows, (size_t)d.n * d.wm * 4, cudaMemcpyDefault, st), "row copy");
+        src = c->rows;
+    }
+    CK((cudaError_t)launch_table(src, c->rows, c->cols, c->top, c->full_mask, c->botext, d, st), "table kernels");
+    c->table_launches = 2;
     return FCA_OK;
 }
 
@@ -642,7 +646,7 @@ fca_status enumerate_impl(fca_ctx *c, uint32_t *out, uint64_t capacity, uint64_t
         bool failed = false;
         if ((s = enqueue_chain(r, 0, K)) != FCA_OK) return s;
         if ((s = final_launches(r, true)) != FCA_OK) return s;
-        CK((cudaError_t)launch_append_bottom(c->flag_dev, c->full_mask, out, capacity, c->ctr, d, st, 1),
+        CK((cudaError_t)launch_append_bottom(c->botext, c->full_mask, out, capacity, c->ctr, d, st, 1),
            "bottom kernel");
         c->stats.launches++;
         if ((s = collect_chain(r, 0, K, &next, &failed)) != FCA_OK) return s;
@@ -663,7 +667,7 @@ fca_status enumerate_impl(fca_ctx *c, uint32_t *out, uint64_t capacity, uint64_t
         // The bottom concept (M', M). When some object holds every attribute its extent is not
         // empty and the search reaches it. Otherwise only empty candidate extents close to it; the
         // search skips those, and it is appended here (a concept is output exactly once either way).
-        CK((cudaError_t)launch_append_bottom(c->flag_dev, c->full_mask, out, capacity, c->ctr, d, st),
+        CK((cudaError_t)launch_append_bottom(c->botext, c->full_mask, out, capacity, c->ctr, d, st),
            "bottom kernel");
         c->stats.launches++;
         if ((s = read_counters(r)) != FCA_OK) return s;
@@ -717,7 +721,7 @@ void fca_free(fca_ctx *ctx)
     cudaFreeHost(ctx->chain_host);
     cudaFree(ctx->host_out_dev);
     cudaFreeHost(ctx->ctr_host);
-    cudaFree(ctx->flag_dev);
+    cudaFree(ctx->botext);
     delete ctx;
 }
 
@@ -757,7 +761,12 @@ fca_status fca_context_create(const uint32_t *rows, int64_t n_objects, int32_t n
         (s = alloc_raw(c, (void **)&c->ctr_snap, sizeof(Counters), "counter snapshot")) != FCA_OK ||
         (s = alloc_raw(c, (void **)&c->chain, sizeof(ChainSlots), "chain records")) != FCA_OK)
         return fail(s);
-    if ((s = alloc_raw(c, (void **)&c->flag_dev, sizeof(uint32_t), "flag")) != FCA_OK) return fail(s);
+    if ((s = alloc_raw(c, (void **)&c->botext, (size_t)d.wn * 4, "bottom extent")) != FCA_OK) return fail(s);
+    // the padding words of the columns (past wn) stay zero; the table kernel writes only the others
+    if ((e = cudaMemset(c->cols, 0, (size_t)d.m * d.wnp * 4)) != cudaSuccess) {
+        cuda_fail(c, e, "column clear");
+        return fail(FCA_ERR_CUDA);
+    }
     if (cudaMallocHost((void **)&c->ctr_host, sizeof(Counters)) != cudaSuccess ||
         cudaMallocHost((void **)&c->chain_host, sizeof(ChainSlots)) != cudaSuccess) {
         cudaGetLastError();

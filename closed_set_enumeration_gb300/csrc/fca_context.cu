@@ -1,12 +1,12 @@
 // Context build kernels of libfca (sm_103a).
 //
-//  mask_rows_kernel      clears the padding bits past M of every row.
-//  transpose_kernel      ctxRows -> ctxCols, 32x32 bit tiles by warp ballots
-//                        (the Parallel FCBO article, section 3.1, builds the
-//                        same column bitmaps with one atomicOr per set bit).
-//  top_kernel            top intent G' = AND of all rows, and whether some
-//                        row holds every attribute (then the bottom concept
-//                        has a non-empty extent and the search reaches it).
+//  table_init_kernel     top intent and bottom extent set to every attribute / every object.
+//  table_kernel          ctxRows (padding bits cleared, copied from the caller's rows) -> ctxCols
+//                        by 32x32 register transposes of bit tiles (the Parallel FCBO article,
+//                        section 3.1, builds the same column bitmaps with one atomicOr per set bit),
+//                        and by AND-reductions the top intent G' (AND of all rows) and the bottom
+//                        extent M' (AND of all columns: the objects holding every attribute; when it
+//                        is not empty the search reaches the bottom concept).
 //  append_bottom_kernel  the bottom concept (intent M) when its extent is empty.
 #include <cuda_runtime.h>
 
@@ -16,15 +16,22 @@ namespace fca {
 namespace {
 
 
-// Clear the padding bits past M in the last word of every row (they are ignored on input).
-__global__ void mask_rows_kernel(uint32_t *rows, Dims d)
+// Start of a table build: the top intent (AND of all rows) starts as every attribute and the
+// bottom extent (objects holding every attribute) as every object; table_kernel narrows both.
+__global__ void table_init_kernel(uint32_t *top, const uint32_t *full_mask, uint32_t *botext, Dims d)
 {
-    const long long o = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (o < d.n) rows[o * d.wm + d.wm - 1] &= (1u << (d.m & 31)) - 1u;
+    const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (t < d.wm) top[t] = full_mask[t];
+    if (t < d.wn) botext[t] = FULL;
 }
 
-__global__ void transpose_kernel(const uint32_t *__restrict__ rows, uint32_t *__restrict__ cols,
-                                 Dims d)
+// The context's tables from the caller's rows, one warp per tile of 32 objects x 32 attributes:
+// padding bits past M cleared (they are ignored on input) in the context's row copy (which the
+// rows are copied into when `src` is another buffer), the columns as the tile's transpose (one
+// 32 x 32 register transpose), and the tile's share of the top intent and of the bottom extent by
+// AND-reductions and one atomicAnd each.
+__global__ void table_kernel(const uint32_t *__restrict__ src, uint32_t *rows, uint32_t *__restrict__ cols,
+                             uint32_t *top, uint32_t *botext, Dims d)
 {
     const int wpb = blockDim.x >> 5;
     const long long tile = (long long)blockIdx.x * wpb + (threadIdx.x >> 5);
@@ -33,50 +40,31 @@ __global__ void transpose_kernel(const uint32_t *__restrict__ rows, uint32_t *__
     const long long ot = tile / d.wm;             // 32 objects
     const int aw = (int)(tile % d.wm);            // 32 attributes
     const long long o = ot * 32 + lane;
-    uint32_t v = (o < d.n) ? rows[o * d.wm + aw] : 0u;
+    const bool obj = o < d.n;
+    uint32_t v = obj ? src[o * d.wm + aw] : 0u;
     const int valid = d.m - aw * 32;
     if (valid < 32) v &= (1u << valid) - 1u;      // ignore padding bits
-    uint32_t mine = 0;
-#pragma unroll
-    for (int b = 0; b < 32; ++b) {
-        const uint32_t bal = __ballot_sync(FULL, (v >> b) & 1u);
-        if (lane == (unsigned)b) mine = bal;
-    }
+    if (obj && (src != rows || valid < 32)) rows[o * d.wm + aw] = v;
+    const uint32_t col = warp_transpose32(v);     // lane b: attribute 32 aw + b over the tile's objects
     const int a = aw * 32 + (int)lane;
-    if (a < d.m) cols[(size_t)a * d.wnp + ot] = mine;
-}
-
-__global__ void top_kernel(const uint32_t *__restrict__ rows, uint32_t *top, uint32_t *flag, Dims d)
-{
-    __shared__ uint32_t red[32];
-    const long long o = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    const bool valid = o < d.n;
-    bool full_row = valid;
-    for (int w = 0; w < d.wm; ++w) {
-        const int vb = d.m - w * 32;
-        const uint32_t mask = vb >= 32 ? FULL : ((1u << vb) - 1u);
-        uint32_t v = valid ? (rows[o * d.wm + w] & mask) : FULL;
-        if (valid && v != mask) full_row = false;
-        v = __reduce_and_sync(FULL, v);
-        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-        __syncthreads();
-        if (threadIdx.x < 32) {
-            uint32_t x = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : FULL;
-            x = __reduce_and_sync(FULL, x);
-            if (threadIdx.x == 0) atomicAnd(&top[w], x);
-        }
-        __syncthreads();
+    if (a < d.m) cols[(size_t)a * d.wnp + ot] = col;
+    const uint32_t t_and = __reduce_and_sync(FULL, obj ? v : FULL);
+    const uint32_t b_and = __reduce_and_sync(FULL, a < d.m ? col : FULL);
+    if (lane == 0) {
+        atomicAnd(&top[aw], t_and);
+        atomicAnd(&botext[ot], b_and);
     }
-    if (full_row) atomicOr(flag, 1u);
 }
 
 // The bottom concept when its extent is empty (no row holds every attribute): one more row.
-__global__ void append_bottom_kernel(const uint32_t *flag, const uint32_t *full_mask, uint32_t *out,
+__global__ void append_bottom_kernel(const uint32_t *botext, long long wn, const uint32_t *full_mask, uint32_t *out,
                                      unsigned long long capacity, Counters *ctr, int wm, int guard)
 {
     if (guard && (ctr->error != 0u || ctr->next_count != 0ull)) return;   // the search did not end here
-    if (*flag) return;   // some object holds every attribute: the search has output it
     const unsigned lane = threadIdx.x & 31;
+    uint32_t any = 0;
+    for (long long q = lane; q < wn; q += 32) any |= botext[q];
+    if (__any_sync(FULL, any != 0u)) return;   // some object holds every attribute: the search output it
     unsigned long long slot = 0;
     if (lane == 0) slot = atomicAdd(&ctr->out_count, 1ull);
     slot = __shfl_sync(FULL, slot, 0);
@@ -173,35 +161,22 @@ int launch_start(Counters *ctr, const uint32_t *top, const uint32_t *root_ext, c
     return (int)cudaGetLastError();
 }
 
-int launch_mask_rows(uint32_t *rows, const Dims &d, void *stream)
+int launch_table(const uint32_t *src, uint32_t *rows, uint32_t *cols, uint32_t *top, const uint32_t *full_mask,
+                 uint32_t *botext, const Dims &d, void *stream)
 {
-    if ((d.m & 31) == 0) return (int)cudaSuccess;
-    const int tpb = 256;
-    mask_rows_kernel<<<(unsigned)((d.n + tpb - 1) / tpb), tpb, 0, (cudaStream_t)stream>>>(rows, d);
-    return (int)cudaGetLastError();
-}
-
-int launch_transpose(const uint32_t *rows, uint32_t *cols, const Dims &d, void *stream)
-{
+    const long long init = d.wn > d.wm ? d.wn : d.wm;
+    table_init_kernel<<<(unsigned)((init + 255) / 256), 256, 0, (cudaStream_t)stream>>>(top, full_mask, botext, d);
     const long long tiles = d.wn * (long long)d.wm;
     const int wpb = 8;
-    const long long blocks = (tiles + wpb - 1) / wpb;
-    transpose_kernel<<<(unsigned)blocks, wpb * 32, 0, (cudaStream_t)stream>>>(rows, cols, d);
+    table_kernel<<<(unsigned)((tiles + wpb - 1) / wpb), wpb * 32, 0, (cudaStream_t)stream>>>(src, rows, cols, top,
+                                                                                           botext, d);
     return (int)cudaGetLastError();
 }
 
-int launch_append_bottom(const uint32_t *flag, const uint32_t *full_mask, uint32_t *out, uint64_t capacity,
+int launch_append_bottom(const uint32_t *botext, const uint32_t *full_mask, uint32_t *out, uint64_t capacity,
                          Counters *ctr, const Dims &d, void *stream, int guard)
 {
-    append_bottom_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(flag, full_mask, out, capacity, ctr, d.wm, guard);
-    return (int)cudaGetLastError();
-}
-
-int launch_top(const uint32_t *rows, uint32_t *top, uint32_t *flag, const Dims &d, void *stream)
-{
-    const int tpb = 256;
-    const long long blocks = (d.n + tpb - 1) / tpb;
-    top_kernel<<<(unsigned)blocks, tpb, 0, (cudaStream_t)stream>>>(rows, top, flag, d);
+    append_bottom_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(botext, d.wn, full_mask, out, capacity, ctr, d.wm, guard);
     return (int)cudaGetLastError();
 }
 

@@ -125,12 +125,12 @@ struct SubtreeArgs {
 
 // Launch wrappers (defined in fca_context.cu, fca_expand.cu and fca_subtree.cu). Each returns a
 // cudaError_t value.
-int launch_mask_rows(uint32_t *rows, const Dims &d, void *stream);
-int launch_transpose(const uint32_t *rows, uint32_t *cols, const Dims &d, void *stream);
-int launch_top(const uint32_t *rows, uint32_t *top, uint32_t *flag_full_row, const Dims &d,
-               void *stream);
+// The context's tables from the rows at `src` (device memory; copied into `rows` when it is
+// another buffer): padding bits cleared, columns (m x wnp, padding words left as they are), the top
+// intent and the bottom extent botext (wn words). Two launches.
+int launch_table(const uint32_t *src, uint32_t *rows, uint32_t *cols, uint32_t *top, const uint32_t *full_mask,
+                 uint32_t *botext, const Dims &d, void *stream);
 int launch_expand(const ExpandArgs &a, int sm_count, void *stream);
-// Append the all-attribute intent when *flag_full_row is 0 (one slot from Counters::out_count).
 // Before a bitmap-tier launch: Counters::next_count = next_fill, zero work cursor and error, then
 // the counters copied to *snap (for a rollback).
 int launch_prepare_expand(Counters *ctr, Counters *snap, uint64_t next_fill, void *stream);
@@ -142,8 +142,10 @@ int launch_start(Counters *ctr, const uint32_t *top, const uint32_t *root_ext, c
 // next_count; 0 once a launch of the chain has overflowed), zero next level fill and cursor, and
 // the counters copied to cs->snaps[i].
 int launch_prepare_chain(Counters *ctr, ChainSlots *cs, int i, uint64_t n0, void *stream);
-// With guard, only when Counters::error and next_count are both zero (see SubtreeArgs::guard).
-int launch_append_bottom(const uint32_t *flag_full_row, const uint32_t *full_mask, uint32_t *out,
+// Append the all-attribute intent when the bottom extent botext (wn words) is empty (one slot from
+// Counters::out_count). With guard, only when Counters::error and next_count are both zero (see
+// SubtreeArgs::guard).
+int launch_append_bottom(const uint32_t *botext, const uint32_t *full_mask, uint32_t *out,
                          uint64_t capacity, Counters *ctr, const Dims &d, void *stream, int guard = 0);
 int launch_subtree(const SubtreeArgs &a, int nw, int sm_count, void *stream);
 // The same with work sharing inside blocks, for a launch whose slices are already set in `b`
