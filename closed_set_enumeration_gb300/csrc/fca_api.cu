@@ -14,6 +14,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstddef>
 #include <cstdio>
 #include <cstdlib>
@@ -31,8 +32,22 @@ struct fca_ctx {
     int sm_count = 0;
     Dims d{};
     uint32_t *rows = nullptr;      // n x wm
-    uint32_t *cols = nullptr;      // m x wnp
-    uint32_t *top = nullptr;       // wm
+    uint32_t *cols = nullptr;      // m x wnp, in processing order (one of cols_buf)
+    uint32_t *top = nullptr;       // wm, in processing order (one of top_buf)
+    // Processing order of the attributes (fca_set_option FCA_OPT_ATTR_ORDER: 0 attribute order, 1
+    // ascending support when the supports vary, 2 ascending support): the table kernels write
+    // cols_buf[0] and top_buf[0] in attribute order; in support order the permuted tables are
+    // cols_buf[1], top_buf[1] and the rows (overwritten), and every output intent is mapped back at
+    // the end of a call.
+    uint32_t *cols_buf[2]{};
+    uint32_t *top_buf[2]{};
+    uint32_t *sup = nullptr;        // m: attribute supports
+    int32_t *perm = nullptr;        // m: attribute -> position
+    int32_t *inv = nullptr;         // m: position -> attribute
+    int attr_order = 1;             // the option
+    bool decide = true;             // the next table load chooses the order (from its supports)
+    bool use_order = false;         // the choice: support order
+    bool ordered = false;           // the tables in use are in support order
     uint32_t *full_mask = nullptr; // wm: every attribute (the bottom intent)
     uint32_t *root_ext = nullptr;  // wnp: every object
     uint32_t *botext = nullptr;    // wn: objects holding every attribute (the bottom extent)
@@ -95,6 +110,10 @@ fca_status cuda_fail(fca_ctx *c, cudaError_t e, const char *what)
         cudaError_t e_ = (call);                              \
         if (e_ != cudaSuccess) return cuda_fail(c, e_, what); \
     } while (0)
+
+// Smallest coefficient of variation of the attribute supports for which option 1 of
+// FCA_OPT_ATTR_ORDER takes the support order.
+constexpr double ORDER_MIN_CV = 0.25;
 
 uint64_t env_u64(const char *name, uint64_t dflt)
 {
@@ -578,8 +597,40 @@ fca_status load_table(fca_ctx *c, const uint32_t *rows, cudaStream_t st)
         CK(cudaMemcpyAsync(c->rows, rows, (size_t)d.n * d.wm * 4, cudaMemcpyDefault, st), "row copy");
         src = c->rows;
     }
-    CK((cudaError_t)launch_table(src, c->rows, c->cols, c->top, c->full_mask, c->botext, d, st), "table kernels");
+    const bool need_sup = c->decide ? c->attr_order != 0 : c->use_order;
+    CK((cudaError_t)launch_table(src, c->rows, c->cols_buf[0], c->top_buf[0], c->full_mask, c->botext,
+                                 need_sup ? c->sup : nullptr, d, st),
+       "table kernels");
     c->table_launches = 2;
+    if (c->decide) {
+        // the order is chosen once (at creation, or after the option changed): with option 1 the
+        // support order is taken when the supports vary (coefficient of variation above 0.25):
+        // then rare attributes come first and far fewer candidates fail the canonical test,
+        // while on evenly dense tables a reordering saves little and its kernels cost more
+        c->use_order = c->attr_order == 2;
+        if (c->attr_order == 1) {
+            std::vector<uint32_t> h(d.m);
+            CK(cudaMemcpyAsync(h.data(), c->sup, (size_t)d.m * 4, cudaMemcpyDeviceToHost, st), "support read-back");
+            CK(cudaStreamSynchronize(st), "stream synchronize");
+            double sum = 0.0, sq = 0.0;
+            for (uint32_t v : h) {
+                sum += v;
+                sq += (double)v * v;
+            }
+            const double mean = sum / d.m, var = std::max(0.0, sq / d.m - mean * mean);
+            c->use_order = mean > 0.0 && std::sqrt(var) > ORDER_MIN_CV * mean;
+        }
+        c->decide = false;
+    }
+    c->ordered = c->use_order;
+    if (c->ordered) {
+        CK((cudaError_t)launch_order(c->sup, c->perm, c->inv, c->cols_buf[0], c->cols_buf[1], c->rows, c->top_buf[0],
+                                     c->top_buf[1], d, st),
+           "order kernels");
+        c->table_launches += 2;
+    }
+    c->cols = c->cols_buf[c->ordered ? 1 : 0];
+    c->top = c->top_buf[c->ordered ? 1 : 0];
     return FCA_OK;
 }
 
@@ -649,6 +700,11 @@ fca_status enumerate_impl(fca_ctx *c, uint32_t *out, uint64_t capacity, uint64_t
         CK((cudaError_t)launch_append_bottom(c->botext, c->full_mask, out, capacity, c->ctr, d, st, 1),
            "bottom kernel");
         c->stats.launches++;
+        if (c->ordered) {
+            CK((cudaError_t)launch_unpermute(out, capacity, c->ctr, c->perm, d, c->sm_count, st, 1),
+               "unpermute kernel");
+            c->stats.launches++;
+        }
         if ((s = collect_chain(r, 0, K, &next, &failed)) != FCA_OK) return s;
         if (!failed && (next >= c->levels.size() || c->level_count[next] == 0)) {
             finished = true;
@@ -670,6 +726,12 @@ fca_status enumerate_impl(fca_ctx *c, uint32_t *out, uint64_t capacity, uint64_t
         CK((cudaError_t)launch_append_bottom(c->botext, c->full_mask, out, capacity, c->ctr, d, st),
            "bottom kernel");
         c->stats.launches++;
+        // intents back from processing order to attribute order
+        if (c->ordered) {
+            CK((cudaError_t)launch_unpermute(out, capacity, c->ctr, c->perm, d, c->sm_count, st, 0),
+               "unpermute kernel");
+            c->stats.launches++;
+        }
         if ((s = read_counters(r)) != FCA_OK) return s;
     }
     if (c->ctr_host->fault & FAULT_WAIT) {
@@ -706,8 +768,13 @@ void fca_free(fca_ctx *ctx)
     if (!ctx) return;
     cudaSetDevice(ctx->device);
     cudaFree(ctx->rows);
-    cudaFree(ctx->cols);
-    cudaFree(ctx->top);
+    for (int i = 0; i < 2; ++i) {
+        cudaFree(ctx->cols_buf[i]);
+        cudaFree(ctx->top_buf[i]);
+    }
+    cudaFree(ctx->sup);
+    cudaFree(ctx->perm);
+    cudaFree(ctx->inv);
     cudaFree(ctx->full_mask);
     cudaFree(ctx->root_ext);
     free_pools(ctx);
@@ -753,8 +820,13 @@ fca_status fca_context_create(const uint32_t *rows, int64_t n_objects, int32_t n
 
     fca_status s;
     if ((s = alloc_raw(c, (void **)&c->rows, (size_t)d.n * d.wm * 4, "rows")) != FCA_OK ||
-        (s = alloc_raw(c, (void **)&c->cols, (size_t)d.m * d.wnp * 4, "columns")) != FCA_OK ||
-        (s = alloc_raw(c, (void **)&c->top, (size_t)d.wm * 4, "top")) != FCA_OK ||
+        (s = alloc_raw(c, (void **)&c->cols_buf[0], (size_t)d.m * d.wnp * 4, "columns")) != FCA_OK ||
+        (s = alloc_raw(c, (void **)&c->cols_buf[1], (size_t)d.m * d.wnp * 4, "columns")) != FCA_OK ||
+        (s = alloc_raw(c, (void **)&c->top_buf[0], (size_t)d.wm * 4, "top")) != FCA_OK ||
+        (s = alloc_raw(c, (void **)&c->top_buf[1], (size_t)d.wm * 4, "top")) != FCA_OK ||
+        (s = alloc_raw(c, (void **)&c->sup, (size_t)d.m * 4, "supports")) != FCA_OK ||
+        (s = alloc_raw(c, (void **)&c->perm, (size_t)d.m * 4, "order")) != FCA_OK ||
+        (s = alloc_raw(c, (void **)&c->inv, (size_t)d.m * 4, "order")) != FCA_OK ||
         (s = alloc_raw(c, (void **)&c->full_mask, (size_t)d.wm * 4, "mask")) != FCA_OK ||
         (s = alloc_raw(c, (void **)&c->root_ext, (size_t)d.wnp * 4, "root extent")) != FCA_OK ||
         (s = alloc_raw(c, (void **)&c->ctr, sizeof(Counters), "counters")) != FCA_OK ||
@@ -763,7 +835,8 @@ fca_status fca_context_create(const uint32_t *rows, int64_t n_objects, int32_t n
         return fail(s);
     if ((s = alloc_raw(c, (void **)&c->botext, (size_t)d.wn * 4, "bottom extent")) != FCA_OK) return fail(s);
     // the padding words of the columns (past wn) stay zero; the table kernel writes only the others
-    if ((e = cudaMemset(c->cols, 0, (size_t)d.m * d.wnp * 4)) != cudaSuccess) {
+    if ((e = cudaMemset(c->cols_buf[0], 0, (size_t)d.m * d.wnp * 4)) != cudaSuccess ||
+        (e = cudaMemset(c->cols_buf[1], 0, (size_t)d.m * d.wnp * 4)) != cudaSuccess) {
         cuda_fail(c, e, "column clear");
         return fail(FCA_ERR_CUDA);
     }
@@ -789,6 +862,11 @@ fca_status fca_context_create(const uint32_t *rows, int64_t n_objects, int32_t n
         (e = cudaMemcpy(c->root_ext, ext.data(), d.wnp * 4, cudaMemcpyHostToDevice)) != cudaSuccess) {
         cuda_fail(c, e, "context set-up");
         return fail(FCA_ERR_CUDA);
+    }
+    {
+        // processing order of the attributes (FCA_OPT_ATTR_ORDER), 1 unless FCA_ATTR_ORDER says 0 or 2
+        const char *v = getenv("FCA_ATTR_ORDER");
+        c->attr_order = (v && (v[0] == '0' || v[0] == '2') && v[1] == 0) ? v[0] - '0' : 1;
     }
     if ((s = load_table(c, rows, 0)) != FCA_OK) return fail(s);
     if ((e = cudaStreamSynchronize(0)) != cudaSuccess) {
@@ -865,6 +943,11 @@ fca_status fca_set_option(fca_ctx *ctx, int option, int64_t value)
         return FCA_OK;
     case FCA_OPT_LEVEL_BYTES:
     case FCA_OPT_QUEUE_ENTRIES:
+    case FCA_OPT_ATTR_ORDER:
+        if (value > 2) return FCA_ERR_INVALID;
+        c->attr_order = (int)value;
+        c->decide = true;
+        return FCA_OK;
     case FCA_OPT_POOL_LIMIT_BYTES:
         CK(cudaSetDevice(c->device), "cudaSetDevice");
         CK(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
@@ -904,6 +987,15 @@ fca_status fca_context_copy(const fca_ctx *ctx, int which, uint32_t *dst, uint64
     case 0: src = ctx->rows; words = (uint64_t)ctx->d.n * ctx->d.wm; break;
     case 1: src = ctx->cols; words = (uint64_t)ctx->d.m * ctx->d.wnp; break;
     case 2: src = ctx->top; words = (uint64_t)ctx->d.wm; break;
+    case 3:
+        if (!ctx->ordered) {   // attribute order: the identity
+            if (dst_words < (uint64_t)ctx->d.m) return FCA_ERR_INVALID;
+            for (int32_t a = 0; a < ctx->d.m; ++a) dst[a] = (uint32_t)a;
+            return FCA_OK;
+        }
+        src = reinterpret_cast<const uint32_t *>(ctx->perm);
+        words = (uint64_t)ctx->d.m;
+        break;
     default: return FCA_ERR_INVALID;
     }
     if (dst_words < words) return FCA_ERR_INVALID;

@@ -18,11 +18,12 @@ namespace {
 
 // Start of a table build: the top intent (AND of all rows) starts as every attribute and the
 // bottom extent (objects holding every attribute) as every object; table_kernel narrows both.
-__global__ void table_init_kernel(uint32_t *top, const uint32_t *full_mask, uint32_t *botext, Dims d)
+__global__ void table_init_kernel(uint32_t *top, const uint32_t *full_mask, uint32_t *botext, uint32_t *sup, Dims d)
 {
     const long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (t < d.wm) top[t] = full_mask[t];
     if (t < d.wn) botext[t] = FULL;
+    if (sup && t < d.m) sup[t] = 0u;
 }
 
 // The context's tables from the caller's rows, one warp per tile of 32 objects x 32 attributes:
@@ -31,7 +32,7 @@ __global__ void table_init_kernel(uint32_t *top, const uint32_t *full_mask, uint
 // 32 x 32 register transpose), and the tile's share of the top intent and of the bottom extent by
 // AND-reductions and one atomicAnd each.
 __global__ void table_kernel(const uint32_t *__restrict__ src, uint32_t *rows, uint32_t *__restrict__ cols,
-                             uint32_t *top, uint32_t *botext, Dims d)
+                             uint32_t *top, uint32_t *botext, uint32_t *sup, Dims d)
 {
     const int wpb = blockDim.x >> 5;
     const long long tile = (long long)blockIdx.x * wpb + (threadIdx.x >> 5);
@@ -47,12 +48,97 @@ __global__ void table_kernel(const uint32_t *__restrict__ src, uint32_t *rows, u
     if (obj && (src != rows || valid < 32)) rows[o * d.wm + aw] = v;
     const uint32_t col = warp_transpose32(v);     // lane b: attribute 32 aw + b over the tile's objects
     const int a = aw * 32 + (int)lane;
-    if (a < d.m) cols[(size_t)a * d.wnp + ot] = col;
+    if (a < d.m) {
+        cols[(size_t)a * d.wnp + ot] = col;
+        if (sup) atomicAdd(&sup[a], (uint32_t)__popc(col));   // the attribute's support
+    }
     const uint32_t t_and = __reduce_and_sync(FULL, obj ? v : FULL);
     const uint32_t b_and = __reduce_and_sync(FULL, a < d.m ? col : FULL);
     if (lane == 0) {
         atomicAnd(&top[aw], t_and);
         atomicAnd(&botext[ot], b_and);
+    }
+}
+
+// Processing order of the attributes: ascending support, ties by index (a stable sort). perm[a] is
+// the position of attribute a, inv[r] the attribute at position r. One block; the supports are
+// staged in shared memory and each thread ranks its attributes by counting (M <= 1024).
+__global__ void order_kernel(const uint32_t *sup, int32_t *perm, int32_t *inv, int m)
+{
+    __shared__ uint32_t s[MAX_ATTRS];
+    for (int a = (int)threadIdx.x; a < m; a += (int)blockDim.x) s[a] = sup[a];
+    __syncthreads();
+    for (int a = (int)threadIdx.x; a < m; a += (int)blockDim.x) {
+        const uint32_t v = s[a];
+        int r = 0;
+        for (int b = 0; b < m; ++b) r += (s[b] < v) || (s[b] == v && b < a);
+        perm[a] = r;
+        inv[r] = a;
+    }
+}
+
+// The tables in processing order, one warp per tile of 32 objects x 32 positions: lane b of tile
+// (ot, aw) gathers word ot of the column of attribute inv[32 aw + b] into position 32 aw + b of
+// cols2; one register transpose turns the tile into words aw of the rows of its 32 objects; the
+// tiles of object word 0 also write word aw of the permuted top intent.
+__global__ void permute_kernel(const uint32_t *__restrict__ cols, uint32_t *__restrict__ cols2, uint32_t *rows,
+                               const int32_t *inv, const uint32_t *top, uint32_t *top2, Dims d)
+{
+    const int wpb = blockDim.x >> 5;
+    const long long tile = (long long)blockIdx.x * wpb + (threadIdx.x >> 5);
+    if (tile >= d.wn * (long long)d.wm) return;  // uniform per warp
+    const unsigned lane = threadIdx.x & 31;
+    const long long ot = tile / d.wm;
+    const int aw = (int)(tile % d.wm);
+    const int r = aw * 32 + (int)lane;
+    const int a = r < d.m ? inv[r] : 0;
+    uint32_t col = 0u;
+    if (r < d.m) {
+        col = cols[(size_t)a * d.wnp + ot];
+        cols2[(size_t)r * d.wnp + ot] = col;
+    }
+    const uint32_t v = warp_transpose32(col);   // lane l: positions 32 aw .. of object 32 ot + l
+    const long long o = ot * 32 + lane;
+    if (o < d.n) rows[o * d.wm + aw] = v;
+    if (ot == 0) {
+        const bool bit = r < d.m && ((top[a >> 5] >> (a & 31)) & 1u);
+        const uint32_t w = __ballot_sync(FULL, bit);
+        if (lane == 0) top2[aw] = w;
+    }
+}
+
+// Output rows [0, min(out_count, capacity)) mapped back from processing order to attribute order:
+// bit a of a row becomes bit a of the result when it was at position perm[a]. One warp per row,
+// rows dealt grid-wide; `guard` as for the guarded launches (SubtreeArgs::guard).
+__global__ void unpermute_kernel(uint32_t *out, unsigned long long capacity, const Counters *ctr,
+                                 const int32_t *perm, int wm, int m, int guard)
+{
+    if (guard && (ctr->error != 0u || ctr->next_count != 0ull)) return;
+    __shared__ int32_t p[MAX_ATTRS];
+    __shared__ uint32_t stage[8][32];
+    for (int a = (int)threadIdx.x; a < m; a += (int)blockDim.x) p[a] = perm[a];
+    __syncthreads();
+    const unsigned lane = threadIdx.x & 31;
+    const int wib = (int)(threadIdx.x >> 5);
+    const unsigned long long total = ctr->out_count < capacity ? ctr->out_count : capacity;
+    const unsigned long long nw = (unsigned long long)gridDim.x * (blockDim.x >> 5);
+    for (unsigned long long row = (unsigned long long)blockIdx.x * (blockDim.x >> 5) + wib; row < total; row += nw) {
+        uint32_t *o = out + row * (unsigned long long)wm;
+        stage[wib][lane] = lane < (unsigned)wm ? o[lane] : 0u;
+        __syncwarp();
+        uint32_t res = 0u;
+        for (int w = 0; w < wm; ++w) {
+            const int a = 32 * w + (int)lane;
+            bool bit = false;
+            if (a < m) {
+                const int q = p[a];
+                bit = (stage[wib][q >> 5] >> (q & 31)) & 1u;
+            }
+            const uint32_t word = __ballot_sync(FULL, bit);
+            if (lane == (unsigned)w) res = word;
+        }
+        __syncwarp();
+        if (lane < (unsigned)wm) o[lane] = res;
     }
 }
 
@@ -162,14 +248,34 @@ int launch_start(Counters *ctr, const uint32_t *top, const uint32_t *root_ext, c
 }
 
 int launch_table(const uint32_t *src, uint32_t *rows, uint32_t *cols, uint32_t *top, const uint32_t *full_mask,
-                 uint32_t *botext, const Dims &d, void *stream)
+                 uint32_t *botext, uint32_t *sup, const Dims &d, void *stream)
 {
-    const long long init = d.wn > d.wm ? d.wn : d.wm;
-    table_init_kernel<<<(unsigned)((init + 255) / 256), 256, 0, (cudaStream_t)stream>>>(top, full_mask, botext, d);
+    long long init = d.wn > d.wm ? d.wn : d.wm;
+    if (init < d.m) init = d.m;
+    table_init_kernel<<<(unsigned)((init + 255) / 256), 256, 0, (cudaStream_t)stream>>>(top, full_mask, botext, sup, d);
     const long long tiles = d.wn * (long long)d.wm;
     const int wpb = 8;
     table_kernel<<<(unsigned)((tiles + wpb - 1) / wpb), wpb * 32, 0, (cudaStream_t)stream>>>(src, rows, cols, top,
-                                                                                           botext, d);
+                                                                                           botext, sup, d);
+    return (int)cudaGetLastError();
+}
+
+int launch_order(const uint32_t *sup, int32_t *perm, int32_t *inv, const uint32_t *cols, uint32_t *cols2,
+                 uint32_t *rows, const uint32_t *top, uint32_t *top2, const Dims &d, void *stream)
+{
+    order_kernel<<<1, 1024, 0, (cudaStream_t)stream>>>(sup, perm, inv, d.m);
+    const long long tiles = d.wn * (long long)d.wm;
+    const int wpb = 8;
+    permute_kernel<<<(unsigned)((tiles + wpb - 1) / wpb), wpb * 32, 0, (cudaStream_t)stream>>>(cols, cols2, rows, inv,
+                                                                                             top, top2, d);
+    return (int)cudaGetLastError();
+}
+
+int launch_unpermute(uint32_t *out, uint64_t capacity, const Counters *ctr, const int32_t *perm, const Dims &d,
+                     int sm_count, void *stream, int guard)
+{
+    unpermute_kernel<<<(unsigned)(4 * sm_count), 256, 0, (cudaStream_t)stream>>>(out, capacity, ctr, perm, d.wm, d.m,
+                                                                             guard);
     return (int)cudaGetLastError();
 }
 

@@ -127,9 +127,18 @@ struct SubtreeArgs {
 // cudaError_t value.
 // The context's tables from the rows at `src` (device memory; copied into `rows` when it is
 // another buffer): padding bits cleared, columns (m x wnp, padding words left as they are), the top
-// intent and the bottom extent botext (wn words). Two launches.
+// intent, the bottom extent botext (wn words) and, when sup is not null, the attribute supports
+// (m words). Two launches.
 int launch_table(const uint32_t *src, uint32_t *rows, uint32_t *cols, uint32_t *top, const uint32_t *full_mask,
-                 uint32_t *botext, const Dims &d, void *stream);
+                 uint32_t *botext, uint32_t *sup, const Dims &d, void *stream);
+// Processing order by ascending support (perm: attribute -> position, inv: position -> attribute),
+// then the tables in that order: cols2 from cols, rows (overwritten), top2 from top. Two launches.
+int launch_order(const uint32_t *sup, int32_t *perm, int32_t *inv, const uint32_t *cols, uint32_t *cols2,
+                 uint32_t *rows, const uint32_t *top, uint32_t *top2, const Dims &d, void *stream);
+// Output rows [0, min(out_count, capacity)) mapped back to attribute order (guard as for the
+// guarded launches).
+int launch_unpermute(uint32_t *out, uint64_t capacity, const Counters *ctr, const int32_t *perm, const Dims &d,
+                     int sm_count, void *stream, int guard);
 int launch_expand(const ExpandArgs &a, int sm_count, void *stream);
 // Before a bitmap-tier launch: Counters::next_count = next_fill, zero work cursor and error, then
 // the counters copied to *snap (for a rollback).

@@ -27,6 +27,7 @@ EXPORTS = (
 
 
 FCA_OPT_COUNT_WORK, FCA_OPT_LEVEL_BYTES, FCA_OPT_QUEUE_ENTRIES, FCA_OPT_POOL_LIMIT_BYTES = 1, 2, 3, 4
+FCA_OPT_ATTR_ORDER = 5
 
 
 class FcaStats(ctypes.Structure):
@@ -227,12 +228,14 @@ class Context:
         return int(n.value), int(m.value)
 
     def copy_layout(self, which: str) -> np.ndarray:
-        """Host copy of the device ``rows``, ``cols`` (padded to 4-word rows) or ``top``."""
+        """Host copy of the device ``rows``, ``cols`` (padded to 4-word rows) or ``top`` in processing
+        order, or the processing ``order`` (position of each attribute)."""
         wn = words(self.n_objects)
         wnp = (wn + 3) & ~3
-        shape = {"rows": (self.n_objects, self.wm), "cols": (self.n_attrs, wnp), "top": (self.wm,)}[which]
+        shape = {"rows": (self.n_objects, self.wm), "cols": (self.n_attrs, wnp), "top": (self.wm,),
+                 "order": (self.n_attrs,)}[which]
         dst = np.zeros(shape, dtype=np.uint32)
-        code = {"rows": 0, "cols": 1, "top": 2}[which]
+        code = {"rows": 0, "cols": 1, "top": 2, "order": 3}[which]
         self._check(self._lib.fca_context_copy(self._h, code, ctypes.c_void_p(dst.ctypes.data), dst.size),
                     "fca_context_copy")
         return dst

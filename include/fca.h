@@ -63,7 +63,10 @@ typedef enum {
     FCA_OPT_COUNT_WORK = 1,       /* 0/1: count the algorithmic work of each kernel (slower) */
     FCA_OPT_LEVEL_BYTES = 2,      /* initial bytes of one bitmap-frontier level (default 64 MiB) */
     FCA_OPT_QUEUE_ENTRIES = 3,    /* initial entries of each object-list queue (default 2^18) */
-    FCA_OPT_POOL_LIMIT_BYTES = 4  /* growth limit of all work pools (default: half the free memory) */
+    FCA_OPT_POOL_LIMIT_BYTES = 4, /* growth limit of all work pools (default: half the free memory) */
+    FCA_OPT_ATTR_ORDER = 5        /* processing order of the attributes: 0 attribute order,
+                                     1 (default) ascending support when the supports vary,
+                                     2 ascending support; chosen by the next table load */
 } fca_option;
 
 /*
@@ -126,7 +129,23 @@ fca_status fca_enumerate_host(fca_ctx *ctx, uint32_t *out_host, uint64_t capacit
                               uint64_t *out_count, void *stream);
 
 /*
- * Set an option of a context (fca_option). Pools start at the initial sizes
+ * Set an option of a context (fca_option).
+ *
+ * FCA_OPT_ATTR_ORDER: the search runs over the attributes in a processing
+ * order: attribute order (0), or ascending support (number of objects holding
+ * the attribute; ties by index), computed on the device (2). Every output
+ * intent is mapped back to attribute order, so the output set does not depend
+ * on the order, while the number of evaluated candidates (closures) does: a
+ * search that meets rare attributes first fails far fewer canonical tests
+ * (the usual ordering heuristic of Close-by-One implementations). With 1, the
+ * default, the support order is taken when the supports vary (coefficient of
+ * variation above 0.25); on evenly dense tables the reordering saves little
+ * and costs three kernels per call. The choice is made by the table load at
+ * creation, or by the next fca_context_load after the option is set (with 1
+ * it reads the supports back, one synchronisation), and kept for later loads.
+ * FCA_ATTR_ORDER=0, 1 or 2 in the environment sets the option before creation.
+ *
+ * Pools start at the initial sizes
  * (rounded up to at least 4*M entries) and grow on demand up to the limit;
  * past the limit a frontier level is expanded in smaller chunks. Changing a
  * pool option frees the pools, which are allocated again by the next
@@ -169,10 +188,12 @@ fca_status fca_get_stats(const fca_ctx *ctx, fca_stats *out);
 fca_status fca_context_dims(const fca_ctx *ctx, int64_t *n_objects, int32_t *n_attrs);
 
 /*
- * Copy the context's device row or column bitmap into `dst` (host or device
- * pointer): which = 0 -> rows (N x W_M words), 1 -> columns (M x W_Np words,
- * W_Np = W_N rounded up to a multiple of 4), 2 -> top intent (W_M words).
- * `dst_words` is the room in `dst`; FCA_ERR_INVALID if too small.
+ * Copy the context's device tables into `dst` (host or device pointer), in
+ * processing order (FCA_OPT_ATTR_ORDER): which = 0 -> rows (N x W_M words),
+ * 1 -> columns (M x W_Np words, W_Np = W_N rounded up to a multiple of 4),
+ * 2 -> top intent (W_M words), 3 -> the processing order (M words: the
+ * position of each attribute). `dst_words` is the room in `dst`;
+ * FCA_ERR_INVALID if too small.
  */
 fca_status fca_context_copy(const fca_ctx *ctx, int which, uint32_t *dst, uint64_t dst_words);
 

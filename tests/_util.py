@@ -27,6 +27,20 @@ def has_duplicates(rows: np.ndarray) -> bool:
     return np.unique(rows, axis=0).shape[0] != rows.shape[0]
 
 
+def support_order(rows: np.ndarray, n: int, m: int) -> Tuple[np.ndarray, np.ndarray]:
+    """The table with its attributes in ascending support order, ties by attribute index: the
+    library's default processing order. Returns (permuted packed rows, inv) where inv[r] is the
+    attribute at position r. The output set of an enumeration does not depend on the order; the
+    number of candidates it evaluates does."""
+    rows = np.ascontiguousarray(rows, dtype=np.uint32)
+    wm = (m + 31) // 32
+    bits = np.unpackbits(rows.view(np.uint8), bitorder="little").reshape(n, wm * 32)[:, :m]
+    inv = np.argsort(bits.sum(axis=0), kind="stable")
+    pad = np.zeros((n, wm * 32), dtype=np.uint8)
+    pad[:, :m] = bits[:, inv]
+    return np.packbits(pad, axis=1, bitorder="little").view(np.uint32).reshape(n, wm).copy(), inv
+
+
 def attrs_to_row(attrs, m: int) -> np.ndarray:
     row = np.zeros((m + 31) // 32, dtype=np.uint32)
     for a in attrs:

@@ -6,9 +6,13 @@ search depth, an order-independent digest of the intent set (sum and xor mod
 2^64 of one hash per intent, computed by the oracle's digest mode) and, when
 the intents fit in host memory, a SHA-256 digest of the intents sorted as big
 integers (last 32-bit word most significant), so that full-size GPU runs can
-be checked without re-running the oracle.
+be checked without re-running the oracle. It also records the closures of the
+same search over the table in ascending-support attribute order (the library's
+default processing order; the intent set is the same), with --order-closures
+alone without redoing the rest.
 
 usage: python tests/golden/make_workload_digests.py [workload ...] [--threads T] [--digest-only]
+                                                    [--order-closures]
 """
 import argparse
 import hashlib
@@ -25,6 +29,7 @@ sys.path.insert(0, ROOT)
 
 import oracle  # noqa: E402
 from closed_set_enumeration_gb300 import contexts as cx  # noqa: E402
+from tests._util import support_order  # noqa: E402
 
 OUT = os.path.join(HERE, "workload_digests.json")
 
@@ -40,11 +45,27 @@ def main():
     ap.add_argument("names", nargs="*", default=list(cx.WORKLOADS))
     ap.add_argument("--threads", type=int, default=os.cpu_count() or 1)
     ap.add_argument("--digest-only", action="store_true", help="skip the sorted SHA-256 (large sets)")
+    ap.add_argument("--order-closures", action="store_true",
+                    help="only (re)compute the closures in ascending-support order")
     args = ap.parse_args()
     data = json.load(open(OUT)) if os.path.exists(OUT) else {}
     for name in args.names:
         w = cx.WORKLOADS[name]
         rows = w.rows()
+        t0 = time.time()
+        go = oracle.cbo_digest(support_order(rows, w.n_objects, w.n_attrs)[0], w.n_objects, w.n_attrs,
+                               threads=args.threads)
+        if args.order_closures:
+            data = json.load(open(OUT)) if os.path.exists(OUT) else {}
+            entry = data.get(name, {})
+            if "concepts" in entry:
+                assert entry["concepts"] == go["count"]
+            entry["closures_support_order"] = go["closures"]
+            data[name] = entry
+            print(name, "support order", go["count"], go["closures"], f"{time.time() - t0:.1f}s", flush=True)
+            with open(OUT, "w") as f:
+                json.dump(data, f, indent=1, sort_keys=True)
+            continue
         t0 = time.time()
         g = oracle.cbo_digest(rows, w.n_objects, w.n_attrs, threads=args.threads)
         dt = time.time() - t0
@@ -57,6 +78,7 @@ def main():
             "concepts": g["count"], "closures": g["closures"], "depth_counts": depth,
             "multiset_hsum": f"{g['hsum']:016x}", "multiset_hxor": f"{g['hxor']:016x}",
             "oracle_seconds": round(dt, 1), "oracle_threads": args.threads,
+            "closures_support_order": go["closures"],
         })
         if not args.digest_only:
             r = oracle.cbo(rows, w.n_objects, w.n_attrs, threads=args.threads)

@@ -1,8 +1,9 @@
 """GPU parity: the CUDA library against the CPU oracle, through the C ABI.
 
 The intent set must be bit-exact (compared as a sorted set; output order is
-unspecified), the number of closures evaluated must equal the oracle's, and
-no intent may appear twice.
+unspecified), the number of closures evaluated must equal the oracle's over the
+table in the same processing order (ascending support by default), and no
+intent may appear twice.
 """
 import json
 import os
@@ -14,7 +15,7 @@ import oracle
 from closed_set_enumeration_gb300 import build as fbuild
 from closed_set_enumeration_gb300 import contexts as cx
 from tests._util import (GOLDEN, attrs_to_row, golden_names, has_duplicates, load_golden,
-                         same_set, sort_rows)
+                         same_set, sort_rows, support_order)
 
 pytestmark = pytest.mark.gpu
 
@@ -36,13 +37,18 @@ def gpu_run(rows, n, m, capacity=None):
         return got, ctx.stats()
 
 
+def ordered_closures(rows, n, m, threads=1):
+    """The oracle's closures over the table in the library's default processing order."""
+    return oracle.cbo(support_order(rows, n, m)[0], n, m, threads=threads)["closures"]
+
+
 def check_against_oracle(rows, n, m, threads=1):
     got, st = gpu_run(rows, n, m)
     ref = oracle.cbo(rows, n, m, threads=threads)
     assert not has_duplicates(got)
     assert same_set(got, ref["intents"])
     assert st["concepts"] == ref["intents"].shape[0]
-    assert st["closures"] == ref["closures"]
+    assert st["closures"] == ordered_closures(rows, n, m, threads)
     return got, st
 
 
@@ -131,23 +137,36 @@ def test_device_rows_input():
     dev = torch.from_numpy(rows.view(np.int32)).cuda()
     with fca.Context(dev, 500, 50) as ctx:
         got = ctx.enumerate().cpu().numpy().view(np.uint32)
-        assert np.array_equal(ctx.copy_layout("rows"), rows)
+        assert np.array_equal(ctx.copy_layout("rows"), support_order(rows, 500, 50)[0])
     assert same_set(got, oracle.cbo(rows, 500, 50)["intents"])
 
 
-def test_column_layout_is_transpose():
+@pytest.mark.parametrize("order", ["0", "1", "2"])
+def test_column_layout_is_transpose(monkeypatch, order):
+    # the device tables in processing order: attribute order (0), or ascending support (2, and 1
+    # for this table, whose supports vary)
     from closed_set_enumeration_gb300 import fca
+    monkeypatch.setenv("FCA_ATTR_ORDER", order)
     n, m = 1000, 70
     rows = cx.random_context(n, m, 0.3, 1)
+    rows[:, 0] |= np.uint32(0x0000F00F)    # uneven supports among the first attributes
+    prows, inv = support_order(rows, n, m) if order != "0" else (rows, np.arange(m))
     with fca.Context(rows, n, m) as ctx:
         cols = ctx.copy_layout("cols")
         top = ctx.copy_layout("top")
-    cells = cx.unpack_rows(rows, m)
+        pos = ctx.copy_layout("order")
+        got = ctx.enumerate().cpu().numpy().view(np.uint32).reshape(-1, (m + 31) // 32)
+        st = ctx.stats()
+    cells = cx.unpack_rows(prows, m)
     wn = (n + 31) // 32
     expect = cx.pack_rows(cells.T)
+    assert np.array_equal(pos[inv], np.arange(m))
     assert np.array_equal(cols[:, :wn], expect)
     assert not np.any(cols[:, wn:])
-    assert np.array_equal(top, oracle.derive_intent(rows, np.ones(n, bool), m))
+    assert np.array_equal(top, oracle.derive_intent(prows, np.ones(n, bool), m))
+    # the output is in attribute order either way; the closures follow the processing order
+    assert same_set(got, oracle.cbo(rows, n, m, threads=8)["intents"])
+    assert st["closures"] == oracle.cbo(prows, n, m, threads=8)["closures"]
 
 
 def test_capacity_contract():
@@ -185,6 +204,22 @@ def test_enumerate_host_and_reuse():
             assert same_set(got, ref)
 
 
+def test_default_order_keeps_attribute_order_on_even_supports(monkeypatch):
+    # option 1 (the default): on a table whose supports hardly vary the search keeps attribute
+    # order, and its closures are the oracle's in attribute order
+    from closed_set_enumeration_gb300 import fca
+    monkeypatch.setenv("FCA_ATTR_ORDER", "1")
+    n, m = 2000, 64
+    rows = cx.random_context(n, m, 0.15, 1)
+    ref = oracle.cbo(rows, n, m, threads=8)
+    with fca.Context(rows, n, m) as ctx:
+        assert np.array_equal(ctx.copy_layout("order"), np.arange(m))
+        got = ctx.enumerate(capacity=ref["intents"].shape[0] + 1).cpu().numpy().view(np.uint32).reshape(-1, 2)
+        st = ctx.stats()
+    assert same_set(got, ref["intents"])
+    assert st["closures"] == ref["closures"]
+
+
 @pytest.mark.parametrize("limit", [None, "1"])
 def test_small_pools_roll_back_and_chunk(monkeypatch, limit):
     # tiny initial pools: launches overflow, are rolled back and retried after the destinations are
@@ -202,7 +237,7 @@ def test_small_pools_roll_back_and_chunk(monkeypatch, limit):
     got, st = gpu_run(rows, n, m, capacity=ref["intents"].shape[0] + 1)
     assert not has_duplicates(got)
     assert same_set(got, ref["intents"])
-    assert st["closures"] == ref["closures"]
+    assert st["closures"] == ordered_closures(rows, n, m, threads=8)
     assert st["retries"] > 0
 
 
@@ -235,7 +270,7 @@ def test_chained_levels_roll_back(monkeypatch):
             retries.append(st["retries"])
             assert not has_duplicates(got)
             assert same_set(got, ref_b["intents"])
-            assert st["closures"] == ref_b["closures"]
+            assert st["closures"] == ordered_closures(rows_b, n, m, threads=8)
         # the second table's first call overflowed, the last one reused the grown pools
         assert retries[0] > 0 and retries[1] == 0
 
@@ -258,7 +293,7 @@ def _digest(intents):
 @pytest.mark.parametrize("name", ["sparse", "skewed", "zipf", "biclusters"])
 def test_workload_full_size_digest(name):
     """Full-size workloads against oracle digests written by tests/golden/make_workload_digests.py:
-    exact count and closures, the order-independent multiset digest of the intent set, the SHA-256
+    exact count and closures (in the default processing order), the order-independent multiset digest of the intent set, the SHA-256
     of the sorted set where recorded, and fixed points B'' = B of sampled intents computed one by
     one by the oracle's derivation operators."""
     from tests._util import multiset_digest
@@ -270,7 +305,7 @@ def test_workload_full_size_digest(name):
     rows = w.rows()
     got, st = gpu_run(rows, w.n_objects, w.n_attrs, capacity=ref["concepts"])
     assert got.shape[0] == ref["concepts"]
-    assert st["closures"] == ref["closures"]
+    assert st["closures"] == ref["closures_support_order"]   # the default processing order
     if "multiset_hsum" in ref:
         assert multiset_digest(got) == (int(ref["multiset_hsum"], 16), int(ref["multiset_hxor"], 16))
     if "sha256_sorted_intents" in ref:
