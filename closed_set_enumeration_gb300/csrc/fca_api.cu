@@ -56,6 +56,9 @@ struct fca_ctx {
     std::vector<Level> levels;
     std::vector<uint64_t> level_count;
     Queue q[NQ]{};
+    // roots spilled by object-list searches that ran past their time budget, per queue width; two
+    // sets, used in turn by the rounds that search them (spill_rounds)
+    Queue spq[2][NQ]{};
     uint64_t q_count[NQ]{};
     Counters *ctr = nullptr;        // device
     Counters *ctr_snap = nullptr;   // device copy taken before each bitmap-tier launch (rollback)
@@ -115,6 +118,12 @@ fca_status cuda_fail(fca_ctx *c, cudaError_t e, const char *what)
 // FCA_OPT_ATTR_ORDER takes the support order.
 constexpr double ORDER_MIN_CV = 0.25;
 
+// Time budget of one object-list search, in SM clock cycles (about 100 us): a search running
+// longer spills its unexplored nodes as new roots, searched in parallel by a following launch.
+constexpr long long SEARCH_BUDGET_CYCLES = 200000;
+// Roots each spill queue holds.
+constexpr uint64_t SPILL_CAP = 1ull << 16;
+
 uint64_t env_u64(const char *name, uint64_t dflt)
 {
     const char *v = getenv(name);
@@ -170,6 +179,8 @@ void free_pools(fca_ctx *c)
     c->levels.clear();
     c->level_count.clear();
     for (Queue &Q : c->q) free_queue(Q);
+    for (int k = 0; k < 2; ++k)
+        for (Queue &Q : c->spq[k]) free_queue(Q);
     c->pool_bytes = 0;
 }
 
@@ -223,6 +234,12 @@ fca_status ensure_level(fca_ctx *c, size_t idx)
 
 fca_status ensure_queues(fca_ctx *c)
 {
+    for (int k = 0; k < 2; ++k)
+        for (int qi = 0; qi < NQ; ++qi) {
+            if (c->spq[k][qi].ids) continue;
+            fca_status s = make_queue(c, &c->spq[k][qi], qi, SPILL_CAP);
+            if (s != FCA_OK) return s;
+        }
     for (int qi = 0; qi < NQ; ++qi) {
         if (c->q[qi].ids) continue;
         const uint64_t cap = initial_queue_cap(c);
@@ -363,6 +380,8 @@ fca_status run_subtree(Run &r, int qi, cudaStream_t st, bool share = true, bool 
     a.ctr = c->ctr;
     a.count_work = c->count_work;
     a.share = share ? 1 : 0;
+    a.budget = SEARCH_BUDGET_CYCLES;
+    a.spill = c->spq[0][qi];
     size_t pair = 0;
     if ((s = time_begin(r, 1, &pair, st)) != FCA_OK) return s;
     CK((cudaError_t)launch_subtree(a, nw, c->sm_count, st), "subtree kernel launch");
@@ -634,6 +653,58 @@ fca_status load_table(fca_ctx *c, const uint32_t *rows, cudaStream_t st)
     return FCA_OK;
 }
 
+// Search the roots that object-list searches spilled (the counters in ctr_host are current): one
+// launch per queue width and round, the next round taking what this one spilled, until none is
+// left; then the intents they output are mapped back to attribute order.
+fca_status spill_rounds(Run &r)
+{
+    fca_ctx *c = r.c;
+    fca_status s;
+    uint64_t cnt[NQ];
+    for (int qi = 0; qi < NQ; ++qi) cnt[qi] = std::min<uint64_t>(c->ctr_host->spill[qi], SPILL_CAP);
+    if (cnt[0] == 0 && cnt[1] == 0) return FCA_OK;
+    const uint64_t start = c->ctr_host->out_count;
+    int cur = 0;
+    while (cnt[0] || cnt[1]) {
+        c->stats.spill_rounds++;
+        CK(cudaMemsetAsync(c->ctr->spill, 0, sizeof(c->ctr->spill), r.st), "spill reset");
+        for (int qi = NQ - 1; qi >= 0; --qi) {
+            if (!cnt[qi]) continue;
+            SubtreeArgs a{};
+            a.d = c->d;
+            a.rows = c->rows;
+            a.q = c->spq[cur][qi];
+            a.q_count = cnt[qi];
+            a.q_index = qi;
+            a.out = r.out;
+            a.capacity = r.capacity;
+            a.ctr = c->ctr;
+            a.count_work = c->count_work;
+            a.share = 1;
+            a.budget = SEARCH_BUDGET_CYCLES;
+            a.spill = c->spq[1 - cur][qi];
+            CK(cudaMemsetAsync(&c->ctr->q_head[qi], 0, sizeof(unsigned long long), r.st), "cursor reset");
+            size_t pair = 0;
+            if ((s = time_begin(r, 1, &pair, r.st)) != FCA_OK) return s;
+            CK((cudaError_t)launch_subtree(a, 1 << qi, c->sm_count, r.st), "subtree kernel launch");
+            if ((s = time_end(r, pair, r.st)) != FCA_OK) return s;
+            c->stats.launches++;
+            c->stats.subtree_launches++;
+            c->stats.small_roots += cnt[qi];
+        }
+        if ((s = read_counters(r)) != FCA_OK) return s;
+        for (int qi = 0; qi < NQ; ++qi) cnt[qi] = std::min<uint64_t>(c->ctr_host->spill[qi], SPILL_CAP);
+        cur = 1 - cur;
+    }
+    if (c->ordered) {
+        CK((cudaError_t)launch_unpermute(r.out, r.capacity, c->ctr, c->perm, c->d, c->sm_count, r.st, 0, start),
+           "unpermute kernel");
+        c->stats.launches++;
+        if ((s = read_counters(r)) != FCA_OK) return s;
+    }
+    return FCA_OK;
+}
+
 // The roots left in the two queues: one launch each. The larger extents run first on the caller's
 // stream; the smaller ones on a side stream, so their blocks take the SMs that the last long
 // subtrees of the first launch leave idle. The caller's stream waits for both. Only the heavier
@@ -734,6 +805,7 @@ fca_status enumerate_impl(fca_ctx *c, uint32_t *out, uint64_t capacity, uint64_t
         }
         if ((s = read_counters(r)) != FCA_OK) return s;
     }
+    if ((s = spill_rounds(r)) != FCA_OK) return s;
     if (c->ctr_host->fault & FAULT_WAIT) {
         c->err = "object-list kernel: a warp waited past its limit for work from its block";
         return FCA_ERR_CUDA;

@@ -107,38 +107,48 @@ __global__ void permute_kernel(const uint32_t *__restrict__ cols, uint32_t *__re
     }
 }
 
-// Output rows [0, min(out_count, capacity)) mapped back from processing order to attribute order:
-// bit a of a row becomes bit a of the result when it was at position perm[a]. One warp per row,
-// rows dealt grid-wide; `guard` as for the guarded launches (SubtreeArgs::guard).
-__global__ void unpermute_kernel(uint32_t *out, unsigned long long capacity, const Counters *ctr,
-                                 const int32_t *perm, int wm, int m, int guard)
+// Output rows [start, min(out_count, capacity)) mapped back from processing order to attribute order:
+// bit a of a row becomes bit a of the result when it was at position perm[a]. Each warp takes runs
+// of UNPERM_ROWS consecutive rows (contiguous words, loaded and stored coalesced through shared
+// memory, so one memory latency serves the run) and forms each result word with one ballot;
+// `guard` as for the guarded launches (SubtreeArgs::guard).
+constexpr int UNPERM_ROWS = 8;
+__global__ void unpermute_kernel(uint32_t *out, unsigned long long start, unsigned long long capacity,
+                                 const Counters *ctr, const int32_t *perm, int wm, int m, int guard)
 {
     if (guard && (ctr->error != 0u || ctr->next_count != 0ull)) return;
     __shared__ int32_t p[MAX_ATTRS];
-    __shared__ uint32_t stage[8][32];
+    __shared__ uint32_t stage[8][UNPERM_ROWS * 32];
+    __shared__ uint32_t res[8][UNPERM_ROWS * 32];
     for (int a = (int)threadIdx.x; a < m; a += (int)blockDim.x) p[a] = perm[a];
     __syncthreads();
     const unsigned lane = threadIdx.x & 31;
     const int wib = (int)(threadIdx.x >> 5);
     const unsigned long long total = ctr->out_count < capacity ? ctr->out_count : capacity;
-    const unsigned long long nw = (unsigned long long)gridDim.x * (blockDim.x >> 5);
-    for (unsigned long long row = (unsigned long long)blockIdx.x * (blockDim.x >> 5) + wib; row < total; row += nw) {
-        uint32_t *o = out + row * (unsigned long long)wm;
-        stage[wib][lane] = lane < (unsigned)wm ? o[lane] : 0u;
+    const unsigned long long step = (unsigned long long)gridDim.x * (blockDim.x >> 5) * UNPERM_ROWS;
+    for (unsigned long long r0 = start + ((unsigned long long)blockIdx.x * (blockDim.x >> 5) + wib) * UNPERM_ROWS;
+         r0 < total; r0 += step) {
+        const int nr = (int)(total - r0 < (unsigned long long)UNPERM_ROWS ? total - r0 : UNPERM_ROWS);
+        const int words = nr * wm;
+        uint32_t *src = out + r0 * (unsigned long long)wm;
+        for (int i = (int)lane; i < words; i += 32) stage[wib][i] = src[i];
         __syncwarp();
-        uint32_t res = 0u;
-        for (int w = 0; w < wm; ++w) {
-            const int a = 32 * w + (int)lane;
-            bool bit = false;
-            if (a < m) {
-                const int q = p[a];
-                bit = (stage[wib][q >> 5] >> (q & 31)) & 1u;
+        for (int r = 0; r < nr; ++r) {
+            const uint32_t *row = stage[wib] + r * wm;
+            for (int w = 0; w < wm; ++w) {
+                const int a = 32 * w + (int)lane;
+                bool bit = false;
+                if (a < m) {
+                    const int q = p[a];
+                    bit = (row[q >> 5] >> (q & 31)) & 1u;
+                }
+                const uint32_t word = __ballot_sync(FULL, bit);
+                if (lane == 0) res[wib][r * wm + w] = word;
             }
-            const uint32_t word = __ballot_sync(FULL, bit);
-            if (lane == (unsigned)w) res = word;
         }
         __syncwarp();
-        if (lane < (unsigned)wm) o[lane] = res;
+        for (int i = (int)lane; i < words; i += 32) src[i] = res[wib][i];
+        __syncwarp();
     }
 }
 
@@ -272,10 +282,10 @@ int launch_order(const uint32_t *sup, int32_t *perm, int32_t *inv, const uint32_
 }
 
 int launch_unpermute(uint32_t *out, uint64_t capacity, const Counters *ctr, const int32_t *perm, const Dims &d,
-                     int sm_count, void *stream, int guard)
+                     int sm_count, void *stream, int guard, uint64_t start)
 {
-    unpermute_kernel<<<(unsigned)(4 * sm_count), 256, 0, (cudaStream_t)stream>>>(out, capacity, ctr, perm, d.wm, d.m,
-                                                                             guard);
+    unpermute_kernel<<<(unsigned)(4 * sm_count), 256, 0, (cudaStream_t)stream>>>(out, start, capacity, ctr, perm, d.wm,
+                                                                             d.m, guard);
     return (int)cudaGetLastError();
 }
 

@@ -47,6 +47,8 @@ struct Counters {
     unsigned int error;                // overflow bits (ERR_*)
     unsigned int fault;                // FAULT_* bits: a bounded wait inside a kernel ran out
     unsigned int pad[2];
+    unsigned long long spill[NQ];      // roots written to the spill queues (object-list searches
+                                       // that ran past their time budget)
 };
 
 // Device records of a chain of bitmap-tier launches queued without host synchronisation between
@@ -121,6 +123,11 @@ struct SubtreeArgs {
     uint64_t capacity;
     Counters *ctr;
     int count_work;         // 1: accumulate Counters::word_ops
+    // Time budget of one search (clock cycles; 0: none). A search still running past it writes what
+    // it has not explored to `spill` as new roots (Counters::spill[q_index] counts them; when the
+    // spill queue is full the search goes on instead).
+    long long budget;
+    Queue spill;
 };
 
 // Launch wrappers (defined in fca_context.cu, fca_expand.cu and fca_subtree.cu). Each returns a
@@ -135,10 +142,10 @@ int launch_table(const uint32_t *src, uint32_t *rows, uint32_t *cols, uint32_t *
 // then the tables in that order: cols2 from cols, rows (overwritten), top2 from top. Two launches.
 int launch_order(const uint32_t *sup, int32_t *perm, int32_t *inv, const uint32_t *cols, uint32_t *cols2,
                  uint32_t *rows, const uint32_t *top, uint32_t *top2, const Dims &d, void *stream);
-// Output rows [0, min(out_count, capacity)) mapped back to attribute order (guard as for the
+// Output rows [start, min(out_count, capacity)) mapped back to attribute order (guard as for the
 // guarded launches).
 int launch_unpermute(uint32_t *out, uint64_t capacity, const Counters *ctr, const int32_t *perm, const Dims &d,
-                     int sm_count, void *stream, int guard);
+                     int sm_count, void *stream, int guard, uint64_t start = 0);
 int launch_expand(const ExpandArgs &a, int sm_count, void *stream);
 // Before a bitmap-tier launch: Counters::next_count = next_fill, zero work cursor and error, then
 // the counters copied to *snap (for a rollback).

@@ -17,7 +17,7 @@ namespace {
 
 // Shared-memory layout of one warp of subtree_kernel<NW> (32-bit words).
 struct SubtreeLayout {
-    static constexpr int ROOTB_W = 32, RM_W = 32, RLO_W = 34, SUFB_W = 32, DSC_W = 34;
+    static constexpr int ROOTB_W = 32, RM_W = 32, RLO_W = 34, SUFB_W = 32, IDS_W = 64, DSC_W = 34;
     int mp, wm, fr, fs;
     size_t o_rmap, o_rootb, o_rm, o_rlo, o_sufb, o_dsc, o_stack, o_outbuf, words;
     __host__ __device__ SubtreeLayout(const Dims &d, int nw)
@@ -32,7 +32,7 @@ struct SubtreeLayout {
         o_rm = o_rootb + ROOTB_W;
         o_rlo = o_rm + RM_W;
         o_sufb = o_rlo + RLO_W;
-        o_dsc = o_sufb + SUFB_W;
+        o_dsc = o_sufb + SUFB_W + IDS_W;
         o_stack = o_dsc + DSC_W;
         o_outbuf = o_stack + (size_t)fr * fs;
         words = o_outbuf + (size_t)OUTBUF * wm;
@@ -63,12 +63,19 @@ struct SubtreeWarp {
     // root-intent attributes in the words above each word
     __device__ uint32_t *sufB() const { return rlo() + SL::RLO_W; }
     // compact intent of the child being written, or a handed-over node
-    __device__ uint32_t *dsc() const { return own + orm + mp / 2 + SL::ROOTB_W + SL::RM_W + SL::RLO_W + SL::SUFB_W; }
+    __device__ uint32_t *dsc() const
+    {
+        return own + orm + mp / 2 + SL::ROOTB_W + SL::RM_W + SL::RLO_W + SL::SUFB_W + SL::IDS_W;
+    }
+    // the root's object ids (32 * NW)
+    __device__ uint32_t *ids() const { return sufB() + SL::SUFB_W; }
     // search stack
     __device__ uint32_t *stk() const { return dsc() + SL::DSC_W; }
     // output buffer, OUTBUF x wm
     __device__ uint32_t *ob() const { return own + oob; }
     int mp, wm, fs, m;
+    const SubtreeArgs *args;   // the launch's arguments (spill queue, counters)
+    long long deadline;        // clock64() past which the current search spills (0: none)
     uint32_t *out;
     unsigned long long capacity;
     Counters *ctr;
@@ -125,8 +132,9 @@ struct SubtreeWarp {
     // Same for a compact intent held in warp-uniform registers (dfs_regs): lane l owns compact
     // attribute 32u + l of word u, and lane w collects full word w. Each full word that D touches
     // takes one OR-reduction of the bits of the lanes whose attribute lies in it.
-    template <int WRT, bool COUNT>
-    __device__ void emit_regs(const uint32_t (&D)[WRT])
+    // Word `lane` (lane < wm) of the full intent: root intent plus the compact bits of D mapped back.
+    template <int WRT>
+    __device__ uint32_t full_word(const uint32_t (&D)[WRT])
     {
         const unsigned lane = threadIdx.x & 31;
         uint32_t acc = lane < (unsigned)wm ? rootB()[lane] : 0u;
@@ -143,6 +151,14 @@ struct SubtreeWarp {
                 pend &= ~__ballot_sync(FULL, in);
             }
         }
+        return acc;
+    }
+
+    template <int WRT, bool COUNT>
+    __device__ void emit_regs(const uint32_t (&D)[WRT])
+    {
+        const unsigned lane = threadIdx.x & 31;
+        const uint32_t acc = full_word<WRT>(D);
         if (lane < (unsigned)wm) ob()[nb * wm + (int)lane] = acc;
         ++nb;
         if (COUNT) ops += (unsigned)wm;   // the intent words written
@@ -173,6 +189,7 @@ constexpr int H_R = 4;         // its relevant-attribute count
 constexpr int H_EXT = 5;       // extent (NW words)
 constexpr int H_B = 8;         // compact intent (WRT words)
 constexpr int H_CAND = 16;     // candidates to search (WRT words)
+constexpr int H_TAIL = 24;     // some warp of the block found no more work items (all kernels)
 constexpr int HDR_WORDS = 32;
 constexpr int MB_EMPTY = 0, MB_WRITING = 1, MB_FULL = 2, MB_TAKING = 3;
 // Nodes a search visits before it may hand work over: short searches finish sooner than a hand-over
@@ -336,6 +353,89 @@ __device__ __forceinline__ void screen(SubtreeWarp &S, uint32_t (&cand)[WRT], co
     }
 }
 
+// A search that ran past its time budget in the tail of its launch: the nodes it has not finished
+// (the current node and every ancestor on the stack from depth d_lo on with candidates left) are
+// written to the spill queue as roots of their own: the root's object ids selected by the node's extent, the full intent, and the cursor
+// at its first remaining candidate, stored as -(y + 1) because their candidates were counted when
+// the nodes were created. Candidates that screening had already dropped come back with the cursor
+// and fail again. Slots for all of them are taken with one atomicAdd; returns false (nothing
+// written) when the spill queue cannot hold them.
+template <int NW, int WRT>
+__device__ bool spill_rest(SubtreeWarp &S, int d_lo, int depth, const uint32_t (&ext)[NW], const uint32_t (&B)[WRT],
+                           const uint32_t (&cand)[WRT])
+{
+    const unsigned lane = threadIdx.x & 31;
+    const SubtreeArgs &a = *S.args;
+    int count = 0;
+    for (int d = d_lo; d <= depth; ++d) {
+        uint32_t any = 0;
+        if (d == depth) {
+#pragma unroll
+            for (int u = 0; u < WRT; ++u) any |= cand[u];
+        } else {
+            const uint32_t *f = S.stk() + (size_t)d * S.fs;
+#pragma unroll
+            for (int u = 0; u < WRT; ++u) any |= f[NW + u];
+        }
+        count += any != 0u;
+    }
+    if (count == 0) return true;
+    unsigned long long slot = 0;
+    if (lane == 0) slot = atomicAdd(&a.ctr->spill[a.q_index], (unsigned long long)count);
+    slot = __shfl_sync(FULL, slot, 0);
+    if (slot + count > a.spill.cap) {
+        // the queue is full: the reserved slots that exist become empty roots (no objects)
+        for (unsigned long long k = slot + lane; k < a.spill.cap && k < slot + count; k += 32) {
+            a.spill.n[k] = 0;
+            a.spill.y[k] = -1;
+        }
+        return false;
+    }
+    const int per = 32 * NW;
+    for (int d = d_lo; d <= depth; ++d) {
+        uint32_t e[NW], b[WRT], c[WRT];
+        if (d == depth) {
+#pragma unroll
+            for (int t = 0; t < NW; ++t) e[t] = ext[t];
+#pragma unroll
+            for (int u = 0; u < WRT; ++u) {
+                b[u] = B[u];
+                c[u] = cand[u];
+            }
+        } else {
+            const uint32_t *f = S.stk() + (size_t)d * S.fs;
+#pragma unroll
+            for (int t = 0; t < NW; ++t) e[t] = f[t];
+#pragma unroll
+            for (int u = 0; u < WRT; ++u) {
+                c[u] = f[NW + u];
+                b[u] = f[NW + WRT + u];
+            }
+        }
+        int first = -1;
+#pragma unroll
+        for (int u = 0; u < WRT; ++u)
+            if (first < 0 && c[u]) first = 32 * u + __ffs(c[u]) - 1;
+        if (first < 0) continue;
+        int pos = 0;
+#pragma unroll
+        for (int t = 0; t < NW; ++t) {
+            if ((e[t] >> lane) & 1u)
+                a.spill.ids[slot * per + pos + __popc(e[t] & ((1u << lane) - 1u))] = S.ids()[32 * t + (int)lane];
+            pos += __popc(e[t]);
+        }
+        const uint32_t w = S.full_word<WRT>(b);
+        if (lane < (unsigned)S.wm) a.spill.itt[slot * S.wm + lane] = w;
+        if (lane == 0) {
+            a.spill.n[slot] = pos;
+            a.spill.y[slot] = -((int)S.rmap()[first] + 1);
+        }
+        ++slot;
+    }
+    __syncwarp();
+    return true;
+}
+
 // Depth-first search of one subtree with the restricted columns in registers: lane l holds the
 // columns of compact attributes 32u + l, u < WRT (R <= 32 * WRT). Extent, intent and remaining
 // candidates of the current node are warp-uniform registers; the stack of ancestors is in shared
@@ -344,7 +444,7 @@ __device__ __forceinline__ void screen(SubtreeWarp &S, uint32_t (&cand)[WRT], co
 // concept the host adds), so the loop only visits candidates with a non-empty C. With `handed`,
 // the search starts instead from a node another warp handed over (extent, compact intent and the
 // candidates to search, already screened, in this warp's dsc[] area).
-template <int NW, int WRT, bool COUNT, bool SHARE>
+template <int NW, int WRT, bool COUNT, bool SHARE, bool SPILL>
 __device__ void dfs_regs(SubtreeWarp &S, int R, int n, int jn, int slices, int slice, bool handed)
 {
     const unsigned lane = threadIdx.x & 31;
@@ -396,8 +496,39 @@ __device__ void dfs_regs(SubtreeWarp &S, int R, int n, int jn, int slices, int s
     int depth = 0;
     int visits = 0;
     for (;;) {
+        // past the time budget: the rest of the search goes to the spill queue (when it fits)
+        // Past the time budget, once the block has run out of work items: the rest of the search
+        // goes to the spill queue (when it fits). A node whose candidates are a subset of its
+        // candidates from the cursor on (the root of a sliced item, a handed-over node, frames
+        // that handed candidates over) cannot be restarted from a cursor, so work-sharing searches
+        // never spill and a sliced or handed-over search keeps its depth-0 node and goes on there.
+        ++visits;
+        if (SPILL && !SHARE && S.deadline != 0 && (visits & 31) == 0 && clock64() > S.deadline &&
+            vload(&block_hdr()[H_TAIL]) != 0) {
+            const bool keep0 = handed || slices > 1;
+            if (!keep0) {
+                if (spill_rest<NW, WRT>(S, 0, depth, ext, B, cand)) return;
+                S.deadline = 0;
+            } else if (depth > 0) {
+                if (spill_rest<NW, WRT>(S, 1, depth, ext, B, cand)) {
+                    depth = 0;
+                    const uint32_t *f = S.stk();
+#pragma unroll
+                    for (int t = 0; t < NW; ++t) ext[t] = f[t];
+#pragma unroll
+                    for (int u = 0; u < WRT; ++u) {
+                        cand[u] = f[NW + u];
+                        B[u] = f[NW + WRT + u];
+                    }
+                    __syncwarp();
+                    S.deadline = clock64() + S.args->budget;
+                    continue;
+                }
+                S.deadline = 0;
+            }
+        }
         // an idle warp of the block is waiting and this search is long: hand it half of the rest
-        if (SHARE && ++visits > SHARE_AFTER &&
+        if (SHARE && visits > SHARE_AFTER &&
             __any_sync(FULL, vload(&block_hdr()[H_IDLE]) > 0 && vload(&block_hdr()[H_MB]) == MB_EMPTY))
             offer<NW, WRT>(S, R, depth, ext, B, cand);
         int j = -1;
@@ -567,11 +698,14 @@ __device__ void dfs_smem(SubtreeWarp &S, int R, int n, int jn, int slices, int s
 // SHARE: the block's warps hand parts of long searches to warps that have run out of work items
 // (the block-shared header comes first in shared memory); without it a warp ends when the items do.
 template <int NW, bool COUNT, int RW, bool SHARE>
-__global__ void __launch_bounds__(256, RW > 4 ? 3 : 4) subtree_kernel(SubtreeArgs a)
+__global__ void __launch_bounds__(256, RW > 4 ? 3 : 4) subtree_kernel(const __grid_constant__ SubtreeArgs a)
 {
     // a launch queued before the host knew whether the bitmap search had ended cleanly
     if (a.guard && (a.ctr->error != 0u || a.ctr->next_count != 0ull)) return;
-    uint32_t *const smw = subtree_smem + (SHARE ? HDR_WORDS : 0);
+    uint32_t *const smw = subtree_smem + HDR_WORDS;
+    // time-budgeted searches that spill in the tail: kernels of at most four register words (their
+    // extra code costs the wider ones more than it saves)
+    constexpr bool SPILLS = RW <= 4;
     const Dims d = a.d;
     const SubtreeLayout L(d, NW);
     const unsigned lane = threadIdx.x & 31;
@@ -579,14 +713,16 @@ __global__ void __launch_bounds__(256, RW > 4 ? 3 : 4) subtree_kernel(SubtreeArg
     const int nwb = (int)(blockDim.x >> 5);
     uint32_t *base = smw + (size_t)wib * L.words;
     int *const hdr = block_hdr();
-    if constexpr (SHARE) {
-        if (threadIdx.x == 0) {
+    if (threadIdx.x == 0) {
+        hdr[H_TAIL] = 0;
+        if (SHARE) {
             hdr[H_BUSY] = nwb;
             hdr[H_IDLE] = 0;
             hdr[H_MB] = MB_EMPTY;
         }
-        __syncthreads();
     }
+    __syncthreads();
+
     SubtreeWarp S;
     S.own = base;
     S.root = base;
@@ -596,6 +732,8 @@ __global__ void __launch_bounds__(256, RW > 4 ? 3 : 4) subtree_kernel(SubtreeArg
     S.wm = d.wm;
     S.fs = L.fs;
     S.m = d.m;
+    S.args = &a;
+    S.deadline = 0;
     S.out = a.out;
     S.capacity = a.capacity;
     S.ctr = a.ctr;
@@ -625,6 +763,7 @@ __global__ void __launch_bounds__(256, RW > 4 ? 3 : 4) subtree_kernel(SubtreeArg
                 base = __shfl_sync(FULL, base, 0);
                 if (base >= items) {
                     claiming = false;
+                    if (lane == 0) hdr[H_TAIL] = 1;   // the block's searches are now the tail
                     if (!SHARE) break;       // no work sharing in this launch: the warp is done
                     if (lane == 0) {
                         atomicSub(&hdr[H_BUSY], 1);
@@ -644,7 +783,10 @@ __global__ void __launch_bounds__(256, RW > 4 ? 3 : 4) subtree_kernel(SubtreeArg
 
             // ---- root: object ids, intent, cursor
             n = a.q.n[r];
-            const int y0 = a.q.y[r];
+            // a negative cursor -(y + 1) marks a root spilled by a search that ran out of time: its
+            // candidates were counted when it was created (cursor y)
+            const int yr = a.q.y[r];
+            const int y0 = yr < 0 ? -yr - 1 : yr;
             uint32_t id[NW];
 #pragma unroll
             for (int t = 0; t < NW; ++t) {
@@ -654,6 +796,8 @@ __global__ void __launch_bounds__(256, RW > 4 ? 3 : 4) subtree_kernel(SubtreeArg
             const uint32_t myRootB = lane < (unsigned)WM ? a.q.itt[r * WM + lane] : 0u;
             __syncwarp();
             S.rootB()[lane] = myRootB;
+#pragma unroll
+            for (int t = 0; t < NW; ++t) S.ids()[32 * t + (int)lane] = id[t];
 
             // ---- relevant attributes R (held by some but not all objects), compact index order =
             //      attribute order, and the columns restricted to the subtree's objects. Lane l holds
@@ -711,7 +855,7 @@ __global__ void __launch_bounds__(256, RW > 4 ? 3 : 4) subtree_kernel(SubtreeArg
             {
                 unsigned c = lane < (unsigned)WM ? __popc(myRootB & ge_mask((int)lane, y0)) : 0u;
                 c = __reduce_add_sync(FULL, c);
-                if (slice == 0) S.closures += (unsigned long long)(d.m - y0 - (int)c);
+                if (slice == 0 && yr >= 0) S.closures += (unsigned long long)(d.m - y0 - (int)c);
             }
             // compact cursor jn: relevant attributes below y0 are not candidates
             {
@@ -766,20 +910,21 @@ __global__ void __launch_bounds__(256, RW > 4 ? 3 : 4) subtree_kernel(SubtreeArg
             handed = true;
         }
 
-        // ---- depth-first search of the subtree (or of the handed-over node)
+        // ---- depth-first search of the subtree (or of the handed-over node), with its time budget
+        S.deadline = SPILLS && a.budget ? clock64() + a.budget : 0;
         const int sl = handed ? 1 : a.slices;
         const int wr = regs_width<RW>(R);
         if (SHARE && share) {
-            if (wr == 1) dfs_regs<NW, 1, COUNT, true>(S, R, n, jn, sl, slice, handed);
-            else if (wr == 2) dfs_regs<NW, 2, COUNT, true>(S, R, n, jn, sl, slice, handed);
-            else if (RW >= 4 && wr == 4) dfs_regs<NW, 4, COUNT, true>(S, R, n, jn, sl, slice, handed);
-            else if (RW > 4 && wr == RW) dfs_regs<NW, RW, COUNT, true>(S, R, n, jn, sl, slice, handed);
+            if (wr == 1) dfs_regs<NW, 1, COUNT, true, SPILLS>(S, R, n, jn, sl, slice, handed);
+            else if (wr == 2) dfs_regs<NW, 2, COUNT, true, SPILLS>(S, R, n, jn, sl, slice, handed);
+            else if (RW >= 4 && wr == 4) dfs_regs<NW, 4, COUNT, true, SPILLS>(S, R, n, jn, sl, slice, handed);
+            else if (RW > 4 && wr == RW) dfs_regs<NW, RW, COUNT, true, SPILLS>(S, R, n, jn, sl, slice, handed);
             else dfs_smem<NW, COUNT>(S, R, n, jn, sl, slice);
         } else {
-            if (wr == 1) dfs_regs<NW, 1, COUNT, false>(S, R, n, jn, sl, slice, false);
-            else if (wr == 2) dfs_regs<NW, 2, COUNT, false>(S, R, n, jn, sl, slice, false);
-            else if (RW >= 4 && wr == 4) dfs_regs<NW, 4, COUNT, false>(S, R, n, jn, sl, slice, false);
-            else if (RW > 4 && wr == RW) dfs_regs<NW, RW, COUNT, false>(S, R, n, jn, sl, slice, false);
+            if (wr == 1) dfs_regs<NW, 1, COUNT, false, SPILLS>(S, R, n, jn, sl, slice, false);
+            else if (wr == 2) dfs_regs<NW, 2, COUNT, false, SPILLS>(S, R, n, jn, sl, slice, false);
+            else if (RW >= 4 && wr == 4) dfs_regs<NW, 4, COUNT, false, SPILLS>(S, R, n, jn, sl, slice, false);
+            else if (RW > 4 && wr == RW) dfs_regs<NW, RW, COUNT, false, SPILLS>(S, R, n, jn, sl, slice, false);
             else dfs_smem<NW, COUNT>(S, R, n, jn, sl, slice);
         }
         __syncwarp();
@@ -811,7 +956,7 @@ template <int NW, bool COUNT, int RW, bool SHARE>
 static int subtree_shape(const Dims &d, int *wpb_out, size_t *smem_out, int *per_sm_out)
 {
     const size_t pw = SubtreeLayout(d, NW).words * 4;
-    const size_t header = SHARE ? HDR_WORDS * 4 : 0;
+    const size_t header = HDR_WORDS * 4;
     const int wpb = warps_for(pw, header);
     const size_t smem = pw * wpb + header;
     static thread_local ShapeCache cache;

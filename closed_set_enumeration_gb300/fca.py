@@ -34,7 +34,7 @@ class FcaStats(ctypes.Structure):
     _fields_ = [(name, ctypes.c_uint64) for name in (
         "concepts", "closures", "large_parents", "small_roots", "launches", "levels",
         "max_frontier", "frontier_bytes", "expand_launches", "subtree_launches",
-        "subtree_word_ops", "expand_bytes", "retries")] + [("expand_ms", ctypes.c_double),
+        "subtree_word_ops", "expand_bytes", "retries", "spill_rounds")] + [("expand_ms", ctypes.c_double),
                                                 ("subtree_ms", ctypes.c_double)]
 
     def as_dict(self) -> dict:

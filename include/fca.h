@@ -54,6 +54,8 @@ typedef struct {
     uint64_t subtree_word_ops; /* counted work of the object-list tier (FCA_OPT_COUNT_WORK) */
     uint64_t expand_bytes;     /* counted bytes moved by the bitmap tier (FCA_OPT_COUNT_WORK) */
     uint64_t retries;          /* bitmap-tier launches rolled back because a work pool was full */
+    uint64_t spill_rounds;     /* launch rounds over subtrees spilled by searches past their time
+                                  budget (their roots are counted in small_roots) */
     double expand_ms;          /* device time of the bitmap-extent kernel launches */
     double subtree_ms;         /* device time of the object-list kernel launches */
 } fca_stats;
