@@ -60,6 +60,10 @@ def main():
             entry = data.get(name, {})
             if "concepts" in entry:
                 assert entry["concepts"] == go["count"]
+            else:   # a workload whose search in attribute order is too long for the host
+                entry.update({"n_objects": w.n_objects, "n_attrs": w.n_attrs, "seed": w.seed,
+                              "concepts": go["count"], "oracle_order": "support",
+                              "oracle_seconds": round(time.time() - t0, 1), "oracle_threads": args.threads})
             entry["closures_support_order"] = go["closures"]
             data[name] = entry
             print(name, "support order", go["count"], go["closures"], f"{time.time() - t0:.1f}s", flush=True)

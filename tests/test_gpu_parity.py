@@ -293,9 +293,9 @@ def _digest(intents):
 @pytest.mark.parametrize("name", ["sparse", "skewed", "zipf", "biclusters"])
 def test_workload_full_size_digest(name):
     """Full-size workloads against oracle digests written by tests/golden/make_workload_digests.py:
-    exact count and closures (in the default processing order), the order-independent multiset digest of the intent set, the SHA-256
-    of the sorted set where recorded, and fixed points B'' = B of sampled intents computed one by
-    one by the oracle's derivation operators."""
+    exact count and closures (in the processing order of the tests), the order-independent
+    multiset digest of the intent set and the SHA-256 of the sorted set where recorded, and fixed
+    points B'' = B of sampled intents computed one by one by the oracle's derivation operators."""
     from tests._util import multiset_digest
     table = json.load(open(DIGESTS)) if os.path.exists(DIGESTS) else {}
     if name not in table:
