@@ -14,6 +14,8 @@ Contents:
   * :func:`derive_extent`,
     :func:`derive_intent`   the two derivation operators on packed bitmaps,
                             written with numpy for spot checks at any size;
+  * ``lattice``             extents of intents and the cover relation of the concept
+                            lattice (``cover_edges``, ``lower_covers_of``), with numpy;
   * ``workcount``           a separate counting pass (``workcount.c``) that counts
                             the algorithmic work of the enumeration in 32-bit
                             words, the numerator of the benchmark's roofline
@@ -23,3 +25,4 @@ Every pin that ties these to the pages' definitions lives in ``tests/``.
 """
 from .cbo_binding import build_oracle, cbo, cbo_digest, oracle_library_path  # noqa: F401
 from .brute import brute_force, brute_force_by_objects, derive_extent, derive_intent  # noqa: F401
+from . import lattice  # noqa: F401
