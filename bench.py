@@ -50,6 +50,9 @@ def parse_args():
                     help="budget of the CPU oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--stage", choices=["enumerate", "extents", "covers"], default="enumerate",
+                    help="enumerate: the intents (the default line); extents / covers: the lattice calls "
+                         "on the workload's intents, timed alone")
     return ap.parse_args()
 
 
@@ -473,6 +476,94 @@ def run_ours(args, world, rank, local):
     return result
 
 
+def run_lattice(args, world, rank, local):
+    """Time fca_extents or fca_cover_edges on the workload's complete intent set (enumerated once,
+    untimed), one call per step, with the L2 flushed between steps."""
+    import torch
+    from closed_set_enumeration_gb300 import build as fbuild
+    from closed_set_enumeration_gb300 import fca
+
+    fbuild.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = cx.WORKLOADS[args.workload]
+    rows = w.rows()
+    wm, wn = (w.n_attrs + 31) // 32, (w.n_objects + 31) // 32
+    stream = torch.cuda.current_stream(dev)
+    ctx = fca.Context(torch.from_numpy(rows.view(np.int32)).to(dev), w.n_objects, w.n_attrs)
+    intents = ctx.enumerate(stream=stream)
+    k = int(intents.shape[0])
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    if args.stage == "extents":
+        out = torch.empty((k, wn), dtype=torch.int32, device=dev)
+
+        def step():
+            ctx.extents_into(intents, out, stream=stream)
+        launches_per_step = 1
+    else:
+        edges = ctx.cover_edges(intents, stream=stream)
+        n_edges = int(edges.shape[0])
+        buf = torch.empty((n_edges, 2), dtype=torch.int32, device=dev)
+
+        def step():
+            st, cnt = ctx.cover_edges_into(intents, buf, n_edges, stream=stream)
+            if st != fca.FCA_OK or cnt != n_edges:
+                raise RuntimeError(f"fca_cover_edges returned {st}, {cnt} edges (expected {n_edges})")
+        launches_per_step = 2   # hash insert and covers (plus a memset)
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    barrier(world)
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    ms = []
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    for _ in range(args.steps):
+        flush.zero_()
+        ev0.record(stream)
+        step()
+        ev1.record(stream)
+        ev1.synchronize()
+        ms.append(ev0.elapsed_time(ev1))
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    total_s = max_over_ranks(sum(ms) / 1e3, world)
+    value = k * args.steps * world / total_s
+    peaks = load_peaks() or {}
+    result = {
+        "metric": f"{args.stage}_concepts_per_s", "value": value, "unit": "concepts/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total_s * 1e3 / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32", "data": "synthetic",
+        "config": {"workload": w.name, "n_objects": w.n_objects, "n_attrs": w.n_attrs, "seed": w.seed,
+                   "concepts": k, "stage": args.stage, "l2": "flushed between timed steps (512 MiB write)",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    mean_ms = statistics.mean(ms)
+    if args.stage == "extents":
+        # algorithmic bytes: intents read, extents written, the columns read once
+        alg = k * (wm + wn) * 4 + w.n_attrs * ((wn + 3) // 4 * 4) * 4
+        peak = peaks.get("hbm_gbs")
+        achieved = alg / (mean_ms * 1e-3) / 1e9
+        result["roofline"] = {"kernel": "extents_kernel", "bound": "hbm", "achieved": achieved,
+                              "peak": peak, "unit": "GB/s", "frac": achieved / peak if peak else None,
+                              "traffic": None, "algorithmic_bytes": alg,
+                              "basis": "event time of the one launch; peak: measured copy bandwidth"}
+    else:
+        result["edges"] = n_edges
+        result["edges_per_s"] = n_edges * args.steps * world / total_s
+        result["roofline"] = None
+        result["roofline_note"] = ("covers_kernel has no counted algorithmic work yet: its cost is "
+                                   "containment tests between attribute sets restricted to each extent")
+    ctx.close()
+    return result
+
+
 # ----------------------------------------------------------------------------- reference arm
 
 def run_reference(args):
@@ -511,6 +602,11 @@ def main():
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(run_reference(args)), flush=True)
+        return
+    if args.stage != "enumerate":
+        result = run_lattice(args, world, rank, local)
+        if rank == 0:
+            print(json.dumps(result), flush=True)
         return
     result = run_ours(args, world, rank, local)
     if rank == 0:

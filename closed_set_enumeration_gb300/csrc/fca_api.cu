@@ -1013,13 +1013,13 @@ fca_status fca_set_option(fca_ctx *ctx, int option, int64_t value)
     case FCA_OPT_COUNT_WORK:
         c->count_work = value != 0;
         return FCA_OK;
-    case FCA_OPT_LEVEL_BYTES:
-    case FCA_OPT_QUEUE_ENTRIES:
     case FCA_OPT_ATTR_ORDER:
         if (value > 2) return FCA_ERR_INVALID;
         c->attr_order = (int)value;
         c->decide = true;
         return FCA_OK;
+    case FCA_OPT_LEVEL_BYTES:
+    case FCA_OPT_QUEUE_ENTRIES:
     case FCA_OPT_POOL_LIMIT_BYTES:
         CK(cudaSetDevice(c->device), "cudaSetDevice");
         CK(cudaDeviceSynchronize(), "cudaDeviceSynchronize");
@@ -1075,6 +1075,67 @@ fca_status fca_context_copy(const fca_ctx *ctx, int which, uint32_t *dst, uint64
     CK(cudaSetDevice(c->device), "cudaSetDevice");
     CK(cudaMemcpy(dst, src, words * 4, cudaMemcpyDefault), "context copy");
     return FCA_OK;
+}
+
+fca_status fca_extents(fca_ctx *ctx, const uint32_t *intents, uint64_t count, uint32_t *extents, void *stream)
+{
+    if (!ctx || (count > 0 && (!intents || !extents))) return FCA_ERR_INVALID;
+    fca_ctx *c = ctx;
+    c->err.clear();
+    if (count > (uint64_t)INT64_MAX / (uint64_t)c->d.wn) {
+        c->err = "count x W_N words exceeds 64 bits";
+        return FCA_ERR_INVALID;
+    }
+    if (count == 0) return FCA_OK;
+    CK(cudaSetDevice(c->device), "cudaSetDevice");
+    CK((cudaError_t)launch_extents(intents, count, c->cols_buf[0], c->d, extents, c->sm_count, (cudaStream_t)stream),
+       "extents kernel");
+    return FCA_OK;
+}
+
+fca_status fca_cover_edges(fca_ctx *ctx, const uint32_t *intents, uint64_t count, uint32_t *edges,
+                           uint64_t capacity, uint64_t *out_edges, void *stream)
+{
+    if (!ctx || !out_edges || (count > 0 && !intents) || (capacity > 0 && !edges)) return FCA_ERR_INVALID;
+    fca_ctx *c = ctx;
+    c->err.clear();
+    *out_edges = 0;
+    if (count >= 0xffffffffull) {
+        c->err = "cover edges take fewer than 2^32 - 1 intents";
+        return FCA_ERR_INVALID;
+    }
+    if (covers_smem_per_warp(c->d) > 200 * 1024) {
+        c->err = "cover edges: N and M too large for one warp's shared memory";
+        return FCA_ERR_INVALID;
+    }
+    if (count == 0) return FCA_OK;
+    CK(cudaSetDevice(c->device), "cudaSetDevice");
+    cudaStream_t st = (cudaStream_t)stream;
+    uint64_t nslots = 64;
+    while (nslots < 2 * count) nslots <<= 1;
+    LatticeCounters *lc = nullptr;
+    uint32_t *slots = nullptr;
+    CK(cudaMallocAsync((void **)&lc, sizeof(LatticeCounters), st), "cudaMallocAsync");
+    cudaError_t e = cudaMallocAsync((void **)&slots, nslots * 4, st);
+    LatticeCounters h{};
+    if (e == cudaSuccess) e = cudaMemsetAsync(lc, 0, sizeof(LatticeCounters), st);
+    if (e == cudaSuccess)
+        e = (cudaError_t)launch_covers(intents, count, c->rows, c->ordered ? c->perm : nullptr, c->cols_buf[0], c->d,
+                                       slots, nslots, edges, capacity, lc, c->sm_count, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&h, lc, sizeof h, cudaMemcpyDeviceToHost, st);
+    if (slots) cudaFreeAsync(slots, st);
+    cudaFreeAsync(lc, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(c, e, "cover edges");
+    *out_edges = h.edges;
+    if (h.insert_failed || h.missing) {
+        char buf[160];
+        snprintf(buf, sizeof buf, "cover edges: %llu cover intents missing from the given set (%llu not stored)",
+                 (unsigned long long)h.missing, (unsigned long long)h.insert_failed);
+        c->err = buf;
+        return FCA_ERR_INVALID;
+    }
+    return h.edges > capacity ? FCA_ERR_CAPACITY : FCA_OK;
 }
 
 }  // extern "C"

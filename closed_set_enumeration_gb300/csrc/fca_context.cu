@@ -133,17 +133,40 @@ __global__ void unpermute_kernel(uint32_t *out, unsigned long long start, unsign
         uint32_t *src = out + r0 * (unsigned long long)wm;
         for (int i = (int)lane; i < words; i += 32) stage[wib][i] = src[i];
         __syncwarp();
-        for (int r = 0; r < nr; ++r) {
-            const uint32_t *row = stage[wib] + r * wm;
-            for (int w = 0; w < wm; ++w) {
+        if (wm <= 16) {
+            // each lane's source word and bit for the up to 16 result words, held in registers
+            int qw[16];
+            uint32_t qb[16];
+#pragma unroll
+            for (int w = 0; w < 16; ++w) {
                 const int a = 32 * w + (int)lane;
-                bool bit = false;
-                if (a < m) {
-                    const int q = p[a];
-                    bit = (row[q >> 5] >> (q & 31)) & 1u;
+                const int q = w < wm && a < m ? p[a] : -1;
+                qw[w] = q < 0 ? 0 : q >> 5;
+                qb[w] = q < 0 ? 32u : (uint32_t)(q & 31);
+            }
+            for (int r = 0; r < nr; ++r) {
+                const uint32_t *row = stage[wib] + r * wm;
+#pragma unroll
+                for (int w = 0; w < 16; ++w) {
+                    if (w >= wm) break;
+                    const bool bit = qb[w] < 32u && ((row[qw[w]] >> qb[w]) & 1u);
+                    const uint32_t word = __ballot_sync(FULL, bit);
+                    if (lane == 0) res[wib][r * wm + w] = word;
                 }
-                const uint32_t word = __ballot_sync(FULL, bit);
-                if (lane == 0) res[wib][r * wm + w] = word;
+            }
+        } else {
+            for (int r = 0; r < nr; ++r) {
+                const uint32_t *row = stage[wib] + r * wm;
+                for (int w = 0; w < wm; ++w) {
+                    const int a = 32 * w + (int)lane;
+                    bool bit = false;
+                    if (a < m) {
+                        const int q = p[a];
+                        bit = (row[q >> 5] >> (q & 31)) & 1u;
+                    }
+                    const uint32_t word = __ballot_sync(FULL, bit);
+                    if (lane == 0) res[wib][r * wm + w] = word;
+                }
             }
         }
         __syncwarp();

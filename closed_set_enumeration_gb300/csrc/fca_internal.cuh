@@ -60,6 +60,14 @@ struct ChainSlots {
     Counters snaps[CHAIN_MAX];               // counters before launch i
 };
 
+// Device counters of one cover-edge call (fca_cover_edges).
+struct LatticeCounters {
+    unsigned long long next;            // work cursor: next concept to take
+    unsigned long long edges;           // cover edges found (row index allocator)
+    unsigned long long missing;         // cover intents not found in the given set
+    unsigned long long insert_failed;   // intents the hash table had no room for
+};
+
 // A bitmap-tier frontier level (structure of arrays).
 struct Level {
     uint32_t *ext;   // cap x wnp words (bitmap extents, 16-byte aligned rows)
@@ -168,5 +176,18 @@ int launch_subtree(const SubtreeArgs &a, int nw, int sm_count, void *stream);
 // (called by launch_subtree; rw = register words of the search, 2, 4 or 8).
 int launch_subtree_shared(const SubtreeArgs &b, int nw, int rw, int sm_count, void *stream);
 size_t expand_smem_per_warp(const Dims &d);
+// Extent (wn words, padding bits zero) of each of `count` attribute sets (wm words each, attribute
+// order) from the columns in attribute order. One launch.
+int launch_extents(const uint32_t *intents, uint64_t count, const uint32_t *cols, const Dims &d, uint32_t *extents,
+                   int sm_count, void *stream);
+// Cover edges of a complete intent set: a hash table of the intents in `slots` (nslots, a power of two
+// of at least twice count), then the lower covers of every concept as (row, row of the cover) pairs.
+// rows are in processing order (perm: attribute -> position, null for the identity), cols in attribute
+// order; lc zeroed by the caller. A memset and two launches.
+int launch_covers(const uint32_t *intents, uint64_t count, const uint32_t *rows, const int32_t *perm,
+                  const uint32_t *cols, const Dims &d, uint32_t *slots, uint64_t nslots, uint32_t *edges,
+                  uint64_t capacity, LatticeCounters *lc, int sm_count, void *stream);
+// Shared memory of one covers_kernel warp (bytes).
+size_t covers_smem_per_warp(const Dims &d);
 
 }  // namespace fca

@@ -22,7 +22,7 @@ FCA_OK, FCA_ERR_INVALID, FCA_ERR_OOM, FCA_ERR_CAPACITY, FCA_ERR_CUDA = range(5)
 EXPORTS = (
     "fca_context_create", "fca_context_load", "fca_enumerate", "fca_enumerate_host", "fca_set_option",
     "fca_get_stats", "fca_context_dims", "fca_context_copy", "fca_last_error", "fca_free", "fca_status_string",
-    "fca_enumerate_small_noalloc",
+    "fca_enumerate_small_noalloc", "fca_extents", "fca_cover_edges",
 )
 
 
@@ -68,6 +68,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.fca_enumerate.argtypes = [vp, vp, u64, ctypes.POINTER(u64), vp]
         lib.fca_enumerate_host.argtypes = [vp, vp, u64, ctypes.POINTER(u64), vp]
         lib.fca_set_option.argtypes = [vp, ctypes.c_int, i64]
+        lib.fca_extents.argtypes = [vp, vp, u64, vp, vp]
+        lib.fca_cover_edges.argtypes = [vp, vp, u64, vp, u64, ctypes.POINTER(u64), vp]
         lib.fca_enumerate_small_noalloc.argtypes = [vp, i64, i32, vp, u64, ctypes.POINTER(u64), vp]
         lib.fca_enumerate_small_noalloc.restype = ctypes.c_int
         lib.fca_get_stats.argtypes = [vp, ctypes.POINTER(FcaStats)]
@@ -80,7 +82,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         lib.fca_status_string.argtypes = [ctypes.c_int]
         lib.fca_status_string.restype = ctypes.c_char_p
         for name in ("fca_context_create", "fca_context_load", "fca_enumerate", "fca_enumerate_host", "fca_set_option", "fca_get_stats",
-                     "fca_context_dims", "fca_context_copy"):
+                     "fca_context_dims", "fca_context_copy", "fca_extents", "fca_cover_edges"):
             getattr(lib, name).restype = ctypes.c_int
         _lib = lib
         return lib
@@ -211,6 +213,51 @@ class Context:
                                           ctypes.byref(count), ctypes.c_void_p(_stream_handle(stream)))
         self._check(st, "fca_enumerate_host", allow_capacity=True)
         return st, int(count.value)
+
+    def extents(self, intents, stream=None):
+        """Extent of each row of the device tensor ``intents`` (``K x W_M`` 32-bit words, attribute
+        order) as a device tensor ``(K, W_N)`` (int32 holding the uint32 words, objects LSB first)."""
+        import torch
+        out = torch.empty((int(intents.shape[0]), words(self.n_objects)), dtype=torch.int32, device=intents.device)
+        self.extents_into(intents, out, stream)
+        return out
+
+    def extents_into(self, intents, out, stream=None) -> None:
+        """Extents of the rows of ``intents`` into the caller's device buffer ``out`` (``K x W_N`` words);
+        enqueued on ``stream`` without waiting."""
+        k = int(intents.shape[0])
+        if k:
+            st = self._lib.fca_extents(self._h, ctypes.c_void_p(_ptr(intents)), k, ctypes.c_void_p(_ptr(out)),
+                                       ctypes.c_void_p(_stream_handle(stream)))
+            self._check(st, "fca_extents")
+
+    def enumerate_concepts(self, capacity: Optional[int] = None, stream=None):
+        """All concepts as two device tensors: intents ``(K, W_M)`` and their extents ``(K, W_N)``."""
+        intents = self.enumerate(capacity, stream)
+        return intents, self.extents(intents, stream)
+
+    def cover_edges_into(self, intents, edges, capacity: Optional[int] = None, stream=None) -> Tuple[int, int]:
+        """Cover edges of the complete intent set ``intents`` into the caller's device buffer ``edges``
+        (``capacity x 2`` 32-bit words). Returns ``(status, edge count)``."""
+        cap = int(edges.shape[0]) if capacity is None else int(capacity)
+        n = ctypes.c_uint64(0)
+        st = self._lib.fca_cover_edges(self._h, ctypes.c_void_p(_ptr(intents)), int(intents.shape[0]),
+                                       ctypes.c_void_p(_ptr(edges) if cap else 0), cap, ctypes.byref(n),
+                                       ctypes.c_void_p(_stream_handle(stream)))
+        self._check(st, "fca_cover_edges", allow_capacity=True)
+        return st, int(n.value)
+
+    def cover_edges(self, intents, capacity: Optional[int] = None, stream=None):
+        """Cover edges (upper row, lower row) of the complete intent set ``intents`` as a device tensor
+        ``(E, 2)`` (int32 holding row indices). Retries once with the exact size when needed."""
+        import torch
+        cap = int(capacity) if capacity is not None else max(64, 4 * int(intents.shape[0]))
+        while True:
+            out = torch.empty((max(cap, 1), 2), dtype=torch.int32, device=intents.device)
+            st, n = self.cover_edges_into(intents, out, cap, stream)
+            if st == FCA_OK:
+                return out[:n]
+            cap = n
 
     def set_option(self, option: int, value: int) -> None:
         self._check(self._lib.fca_set_option(self._h, int(option), int(value)), "fca_set_option")

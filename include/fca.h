@@ -131,6 +131,55 @@ fca_status fca_enumerate_host(fca_ctx *ctx, uint32_t *out_host, uint64_t capacit
                               uint64_t *out_count, void *stream);
 
 /*
+ * The extent of each given attribute set: Y' = the objects having every
+ * attribute of Y (FCbO-to-CUDA page, sections 1.1 and 4.4: the concept pool
+ * holds each concept's extent beside its intent; Parallel FCBO page,
+ * section 1.1). For the intents written by fca_enumerate this yields the
+ * concepts (B', B).
+ *
+ *   intents    device pointer, count x W_M words in attribute order (as
+ *              fca_enumerate writes them); padding bits past M are ignored.
+ *   count      rows of `intents` (0: nothing to do).
+ *   extents    device pointer, count x W_N words (W_N = ceil(N/32)),
+ *              caller-owned: row r receives the extent of row r, object o
+ *              being bit (o & 31) of word (o >> 5); padding bits are 0.
+ *   stream     cudaStream_t (NULL = legacy default stream).
+ * The work is enqueued on `stream` and the call returns without waiting;
+ * it reads the context's table, so it must be ordered after any
+ * fca_context_load that precedes it (the same stream does that).
+ * FCA_ERR_INVALID for NULL pointers with count > 0.
+ */
+fca_status fca_extents(fca_ctx *ctx, const uint32_t *intents, uint64_t count, uint32_t *extents, void *stream);
+
+/*
+ * The cover relation of the concept lattice (its Hasse diagram): the
+ * edges (i, j) such that concept j lies directly below concept i, i.e.
+ * intent i is a proper subset of intent j and no intent lies strictly
+ * between them (FCbO-to-CUDA page, section 4.4, and Parallel FCBO page,
+ * section 3.4: the lattice's edges are rebuilt from the concepts after the
+ * search, because the search tree's links are not them).
+ *
+ *   intents    device pointer, count x W_M words in attribute order: every
+ *              intent of the context, each once, in any order (the output
+ *              of fca_enumerate). 1 <= count < 2^32 - 1.
+ *   edges      device pointer, capacity x 2 uint32, caller-owned: edge e is
+ *              (edges[2e], edges[2e+1]) = (row of the upper concept, row of
+ *              the lower concept) in `intents`. Edge order is unspecified.
+ *   capacity   edges available (0 allowed: count only).
+ *   out_edges  host pointer; receives the number of edges, also when it
+ *              exceeds `capacity` (then FCA_ERR_CAPACITY, the first
+ *              `capacity` edges written).
+ *   stream     cudaStream_t (NULL = legacy default stream).
+ * Uses stream-ordered device scratch of about 8 bytes per intent and
+ * returns after the work on `stream` completes. FCA_ERR_INVALID when a
+ * cover's intent is not in the given set (the set was not complete), or
+ * when a warp's shared memory cannot hold three N-bit extents and 3M
+ * words (N up to about 500 000 objects at small M).
+ */
+fca_status fca_cover_edges(fca_ctx *ctx, const uint32_t *intents, uint64_t count, uint32_t *edges,
+                           uint64_t capacity, uint64_t *out_edges, void *stream);
+
+/*
  * Set an option of a context (fca_option).
  *
  * FCA_OPT_ATTR_ORDER: the search runs over the attributes in a processing

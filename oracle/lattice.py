@@ -53,20 +53,21 @@ def cover_edges(intents: np.ndarray, n_attrs: int) -> np.ndarray:
 def lower_covers_of(intents: np.ndarray, n_attrs: int, i: int) -> np.ndarray:
     """Row indices j (ascending) of the lower covers of concept i within the set ``intents``.
 
-    The proper supersets of intent_i are found by a scan of the whole set; among them the lower
-    covers are the minimal ones under inclusion (no other proper superset of intent_i inside them).
+    The proper supersets of intent_i are found by a scan of the whole set; the lower covers are the
+    minimal ones under inclusion. They are taken out in order of size: the smallest superset left is
+    minimal (a superset inside it would be smaller, and would either still be left or have gone with
+    a minimal one that is then inside it too), and every superset containing it is dropped with it.
     """
     x = np.ascontiguousarray(intents, dtype=np.uint32)
     b = x[i]
     sup = np.nonzero(np.all((x & b[None, :]) == b[None, :], axis=1))[0]
     sup = sup[sup != i]
-    if sup.size == 0:
-        return sup.astype(np.int64)
-    cand = x[sup]
-    cells = _bits(cand, n_attrs)
-    c = cells.astype(np.float32)
-    size = cells.sum(axis=1)
-    outside = size[:, None] - (c @ c.T)
-    below = (outside == 0) & (size[:, None] < size[None, :])   # below[a, b]: cand a inside cand b
-    minimal = ~below.any(axis=0)
-    return np.sort(sup[minimal]).astype(np.int64)
+    size = _bits(x[sup], n_attrs).sum(axis=1) if sup.size else np.zeros(0, dtype=np.int64)
+    left = sup[np.argsort(size, kind="stable")]
+    covers = []
+    while left.size:
+        c = left[0]
+        covers.append(c)
+        inside = np.all((x[left] & x[c][None, :]) == x[c][None, :], axis=1)
+        left = left[~inside]
+    return np.sort(np.asarray(covers, dtype=np.int64))

@@ -56,6 +56,8 @@ def test_null_context_calls(lib):
     cnt = ctypes.c_uint64(0)
     assert lib.fca_enumerate(None, None, 0, ctypes.byref(cnt), None) == fca.FCA_ERR_INVALID
     assert lib.fca_enumerate_host(None, None, 0, ctypes.byref(cnt), None) == fca.FCA_ERR_INVALID
+    assert lib.fca_extents(None, None, 0, None, None) == fca.FCA_ERR_INVALID
+    assert lib.fca_cover_edges(None, None, 0, None, 0, ctypes.byref(cnt), None) == fca.FCA_ERR_INVALID
     s = fca.FcaStats()
     assert lib.fca_get_stats(None, ctypes.byref(s)) == fca.FCA_ERR_INVALID
     assert lib.fca_last_error(None) == b""
