@@ -83,6 +83,8 @@ struct fca_ctx {
     // a second stream for the object-list launch that runs beside the other one
     cudaStream_t side = nullptr;
     cudaEvent_t fork = nullptr, join = nullptr;
+    cudaEvent_t lat_ev[2]{};        // around the kernels of the last lattice call
+    bool lat_timed = false;
 
     // device timing of kernel launches: event pairs recorded around each launch
     std::vector<cudaEvent_t> events;
@@ -852,6 +854,8 @@ void fca_free(fca_ctx *ctx)
     free_pools(ctx);
     for (cudaEvent_t e : ctx->events) cudaEventDestroy(e);
     if (ctx->fork) cudaEventDestroy(ctx->fork);
+    for (cudaEvent_t e : ctx->lat_ev)
+        if (e) cudaEventDestroy(e);
     if (ctx->join) cudaEventDestroy(ctx->join);
     if (ctx->side) cudaStreamDestroy(ctx->side);
     cudaFree(ctx->ctr);
@@ -1039,6 +1043,12 @@ fca_status fca_get_stats(const fca_ctx *ctx, fca_stats *out)
     *out = ctx->stats;
     cudaSetDevice(ctx->device);
     launch_times(ctx, &out->expand_ms, &out->subtree_ms);
+    out->lattice_ms = 0.0;
+    float ms = 0.f;
+    if (ctx->lat_timed) {
+        if (cudaEventElapsedTime(&ms, ctx->lat_ev[0], ctx->lat_ev[1]) == cudaSuccess) out->lattice_ms = ms;
+        else cudaGetLastError();
+    }
     return FCA_OK;
 }
 
@@ -1077,6 +1087,23 @@ fca_status fca_context_copy(const fca_ctx *ctx, int which, uint32_t *dst, uint64
     return FCA_OK;
 }
 
+// Create the lattice-call event pair on first use and record its start on `st`.
+static fca_status lattice_time_begin(fca_ctx *c, cudaStream_t st)
+{
+    for (cudaEvent_t &e : c->lat_ev)
+        if (!e) CK(cudaEventCreate(&e), "cudaEventCreate");
+    c->lat_timed = false;
+    CK(cudaEventRecord(c->lat_ev[0], st), "cudaEventRecord");
+    return FCA_OK;
+}
+
+static fca_status lattice_time_end(fca_ctx *c, cudaStream_t st)
+{
+    CK(cudaEventRecord(c->lat_ev[1], st), "cudaEventRecord");
+    c->lat_timed = true;
+    return FCA_OK;
+}
+
 fca_status fca_extents(fca_ctx *ctx, const uint32_t *intents, uint64_t count, uint32_t *extents, void *stream)
 {
     if (!ctx || (count > 0 && (!intents || !extents))) return FCA_ERR_INVALID;
@@ -1088,9 +1115,13 @@ fca_status fca_extents(fca_ctx *ctx, const uint32_t *intents, uint64_t count, ui
     }
     if (count == 0) return FCA_OK;
     CK(cudaSetDevice(c->device), "cudaSetDevice");
-    CK((cudaError_t)launch_extents(intents, count, c->cols_buf[0], c->d, extents, c->sm_count, (cudaStream_t)stream),
+    cudaStream_t st = (cudaStream_t)stream;
+    fca_status s = lattice_time_begin(c, st);
+    if (s != FCA_OK) return s;
+    CK((cudaError_t)launch_extents(intents, count, c->cols_buf[0], c->cols, c->ordered ? c->perm : nullptr, c->d,
+                                   extents, c->sm_count, st),
        "extents kernel");
-    return FCA_OK;
+    return lattice_time_end(c, st);
 }
 
 fca_status fca_cover_edges(fca_ctx *ctx, const uint32_t *intents, uint64_t count, uint32_t *edges,
@@ -1119,9 +1150,12 @@ fca_status fca_cover_edges(fca_ctx *ctx, const uint32_t *intents, uint64_t count
     cudaError_t e = cudaMallocAsync((void **)&slots, nslots * 4, st);
     LatticeCounters h{};
     if (e == cudaSuccess) e = cudaMemsetAsync(lc, 0, sizeof(LatticeCounters), st);
+    if (e == cudaSuccess && lattice_time_begin(c, st) != FCA_OK) e = cudaErrorUnknown;
     if (e == cudaSuccess)
-        e = (cudaError_t)launch_covers(intents, count, c->rows, c->ordered ? c->perm : nullptr, c->cols_buf[0], c->d,
-                                       slots, nslots, edges, capacity, lc, c->sm_count, st);
+        e = (cudaError_t)launch_covers(intents, count, c->rows, c->ordered ? c->inv : nullptr,
+                                       c->ordered ? c->perm : nullptr, c->cols_buf[0], c->cols, c->d, slots, nslots,
+                                       edges, capacity, lc, c->sm_count, st);
+    if (e == cudaSuccess && lattice_time_end(c, st) != FCA_OK) e = cudaErrorUnknown;
     if (e == cudaSuccess) e = cudaMemcpyAsync(&h, lc, sizeof h, cudaMemcpyDeviceToHost, st);
     if (slots) cudaFreeAsync(slots, st);
     cudaFreeAsync(lc, st);

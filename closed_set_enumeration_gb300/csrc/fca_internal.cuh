@@ -177,16 +177,19 @@ int launch_subtree(const SubtreeArgs &a, int nw, int sm_count, void *stream);
 int launch_subtree_shared(const SubtreeArgs &b, int nw, int rw, int sm_count, void *stream);
 size_t expand_smem_per_warp(const Dims &d);
 // Extent (wn words, padding bits zero) of each of `count` attribute sets (wm words each, attribute
-// order) from the columns in attribute order. One launch.
-int launch_extents(const uint32_t *intents, uint64_t count, const uint32_t *cols, const Dims &d, uint32_t *extents,
-                   int sm_count, void *stream);
+// order) from the columns in attribute order (cols) and in processing order (cols_p; perm: attribute
+// -> position, null when the two orders are the same). One launch.
+int launch_extents(const uint32_t *intents, uint64_t count, const uint32_t *cols, const uint32_t *cols_p,
+                   const int32_t *perm, const Dims &d, uint32_t *extents, int sm_count, void *stream);
 // Cover edges of a complete intent set: a hash table of the intents in `slots` (nslots, a power of two
 // of at least twice count), then the lower covers of every concept as (row, row of the cover) pairs.
-// rows are in processing order (perm: attribute -> position, null for the identity), cols in attribute
-// order; lc zeroed by the caller. A memset and two launches.
-int launch_covers(const uint32_t *intents, uint64_t count, const uint32_t *rows, const int32_t *perm,
-                  const uint32_t *cols, const Dims &d, uint32_t *slots, uint64_t nslots, uint32_t *edges,
-                  uint64_t capacity, LatticeCounters *lc, int sm_count, void *stream);
+// rows and cols_p are in processing order (inv: position -> attribute, perm: attribute -> position,
+// both null for the identity), cols in attribute order; lc zeroed by the caller. A memset and two
+// launches.
+int launch_covers(const uint32_t *intents, uint64_t count, const uint32_t *rows, const int32_t *inv,
+                  const int32_t *perm, const uint32_t *cols, const uint32_t *cols_p, const Dims &d, uint32_t *slots,
+                  uint64_t nslots, uint32_t *edges, uint64_t capacity, LatticeCounters *lc, int sm_count,
+                  void *stream);
 // Shared memory of one covers_kernel warp (bytes).
 size_t covers_smem_per_warp(const Dims &d);
 

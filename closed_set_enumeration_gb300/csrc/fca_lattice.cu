@@ -32,26 +32,128 @@ __device__ __forceinline__ uint32_t valid_bits(long long w, long long words, lon
     return (w == words - 1 && tail) ? ((1u << tail) - 1u) : FULL;
 }
 
+// The attributes of B in processing order, rarest first: lane w holds word w of B (attribute
+// order); the positions (perm maps an attribute to its position, null: the identity) are written in
+// ascending order to list[0..nb) and nb is returned to every lane. scratch holds W_M words.
+__device__ __forceinline__ int attr_list(uint32_t Bw, const int32_t *perm, uint16_t *list, uint32_t *scratch, int wm,
+                                         unsigned lane)
+{
+    if (perm) {
+        if ((int)lane < wm) scratch[lane] = 0u;
+        __syncwarp();
+        uint32_t bits = Bw;
+        while (bits) {
+            const int p = perm[32 * (int)lane + __ffs(bits) - 1];
+            bits &= bits - 1u;
+            atomicOr(scratch + (p >> 5), 1u << (p & 31));
+        }
+        __syncwarp();
+        Bw = (int)lane < wm ? scratch[lane] : 0u;
+    }
+    const unsigned c = __popc(Bw);
+    unsigned pre = c;   // inclusive prefix sum over the lanes
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned y = __shfl_up_sync(FULL, pre, o);
+        if ((int)lane >= o) pre += y;
+    }
+    unsigned q = pre - c;
+    while (Bw) {
+        list[q++] = (uint16_t)(32 * lane + __ffs(Bw) - 1);
+        Bw &= Bw - 1u;
+    }
+    __syncwarp();
+    return (int)__shfl_sync(FULL, pre, 31);
+}
+
+// Words w0 + 32u + lane (u < U) of the extent of an attribute list: the AND of column words, the
+// first (rarest) column alone, the rest four columns at a time (4U loads in flight per lane), until
+// every lane of the warp holds zero words (warp-wide).
+template <int U>
+__device__ __forceinline__ void extent_words(uint32_t (&acc)[U], const uint16_t *list, int nb, const uint32_t *cols,
+                                             long long wnp, long long w0, unsigned lane)
+{
+    if (nb > 0) {
+        const uint32_t *c0 = cols + (size_t)list[0] * wnp + w0 + lane;
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (acc[u]) acc[u] &= __ldg(c0 + 32 * u);
+    }
+    for (int q = 1; q < nb; q += 4) {
+        uint32_t any = 0;
+#pragma unroll
+        for (int u = 0; u < U; ++u) any |= acc[u];
+        if (!__any_sync(FULL, any != 0u)) break;
+        const int p0 = list[q];
+        const uint32_t *c0 = cols + (size_t)p0 * wnp + w0 + lane;
+        const uint32_t *c1 = cols + (size_t)(q + 1 < nb ? list[q + 1] : p0) * wnp + w0 + lane;
+        const uint32_t *c2 = cols + (size_t)(q + 2 < nb ? list[q + 2] : p0) * wnp + w0 + lane;
+        const uint32_t *c3 = cols + (size_t)(q + 3 < nb ? list[q + 3] : p0) * wnp + w0 + lane;
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (acc[u]) acc[u] &= __ldg(c0 + 32 * u) & __ldg(c1 + 32 * u) & __ldg(c2 + 32 * u) & __ldg(c3 + 32 * u);
+    }
+}
+
+constexpr int EXT_U = 4;   // extent words per lane and pass
+
+// G lanes per row (G a power of two, the smallest at least W_N, at most 32). With G = 32 a warp takes
+// one row, lists its attributes rarest first (columns in processing order) and walks the row 128
+// words at a time (four per lane), so its stores are consecutive words; with G < 32 (W_N <= 16) a warp takes 32 / G
+// rows and each lane ANDs the columns of its row's attributes in attribute order.
+template <int G>
 __global__ void __launch_bounds__(256) extents_kernel(const uint32_t *__restrict__ intents, unsigned long long count,
-                                                      const uint32_t *__restrict__ cols, Dims d,
+                                                      const uint32_t *__restrict__ cols,
+                                                      const uint32_t *__restrict__ cols_p,
+                                                      const int32_t *__restrict__ perm, Dims d,
                                                       uint32_t *__restrict__ extents)
 {
-    const unsigned long long total = count * (unsigned long long)d.wn;
-    const unsigned long long stride = (unsigned long long)gridDim.x * blockDim.x;
-    for (unsigned long long t = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; t < total; t += stride) {
-        const unsigned long long r = t / (unsigned long long)d.wn;
-        const long long w = (long long)(t - r * (unsigned long long)d.wn);
-        uint32_t acc = valid_bits(w, d.wn, d.n);
-        const uint32_t *b = intents + r * (unsigned long long)d.wm;
-        for (int iw = 0; iw < d.wm && acc; ++iw) {
-            uint32_t bits = __ldg(b + iw) & valid_bits(iw, d.wm, d.m);
-            while (bits && acc) {
-                const int a = 32 * iw + __ffs(bits) - 1;
-                bits &= bits - 1u;
-                acc &= __ldg(cols + (size_t)a * d.wnp + w);
+    constexpr int RPW = 32 / G;
+    const unsigned lane = threadIdx.x & 31;
+    const unsigned long long warp = ((unsigned long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const unsigned long long warps = ((unsigned long long)gridDim.x * blockDim.x) >> 5;
+    if constexpr (G == 32) {
+        __shared__ uint16_t lists[8][MAX_ATTRS];
+        __shared__ uint32_t scratch[8][32];
+        uint16_t *list = lists[threadIdx.x >> 5];
+        for (unsigned long long r = warp; r < count; r += warps) {
+            const uint32_t Bw = (int)lane < d.wm ? intents[r * d.wm + lane] & valid_bits(lane, d.wm, d.m) : 0u;
+            const int nb = attr_list(Bw, perm, list, scratch[threadIdx.x >> 5], d.wm, lane);
+            uint32_t *o = extents + r * (unsigned long long)d.wn;
+            for (long long w0 = 0; w0 < d.wn; w0 += 32 * EXT_U) {
+                uint32_t acc[EXT_U];
+#pragma unroll
+                for (int u = 0; u < EXT_U; ++u) {
+                    const long long w = w0 + 32 * u + lane;
+                    acc[u] = w < d.wn ? valid_bits(w, d.wn, d.n) : 0u;
+                }
+                extent_words<EXT_U>(acc, list, nb, cols_p, d.wnp, w0, lane);
+#pragma unroll
+                for (int u = 0; u < EXT_U; ++u) {
+                    const long long w = w0 + 32 * u + lane;
+                    if (w < d.wn) o[w] = acc[u];
+                }
             }
+            __syncwarp();
         }
-        extents[t] = acc;
+    } else {
+        const int gl = (int)(lane % G);
+        for (unsigned long long r0 = warp * RPW; r0 < count; r0 += warps * RPW) {
+            const unsigned long long r = r0 + lane / G;
+            const bool live = r < count && gl < d.wn;
+            if (!live) continue;
+            const uint32_t *b = intents + r * (unsigned long long)d.wm;
+            uint32_t acc = valid_bits(gl, d.wn, d.n);
+            for (int iw = 0; iw < d.wm && acc; ++iw) {
+                uint32_t bits = __ldg(b + iw) & valid_bits(iw, d.wm, d.m);
+                while (bits && acc) {
+                    const int a = 32 * iw + __ffs(bits) - 1;
+                    bits &= bits - 1u;
+                    acc &= __ldg(cols + (size_t)a * d.wnp + gl);
+                }
+            }
+            extents[r * (unsigned long long)d.wn + gl] = acc;
+        }
     }
 }
 
@@ -94,20 +196,26 @@ __global__ void __launch_bounds__(256) hash_insert_kernel(const uint32_t *__rest
     }
 }
 
-// Per-warp shared memory of covers_kernel, in 32-bit words: R (2M: 64-bit restricted columns by
-// processing position), s (M supports), Aw / Ai / Cw (wn each: A's non-zero words, their indices, C_k
-// on them), ids (64 object ids); rounded up to an even count.
+// Per-warp shared memory of covers_kernel, in 32-bit words: R (2M: 64-bit restricted sets by
+// attribute), s (M supports), eb (M: rows of the covers found for the current concept), Aw / Ai
+// (wn each: A's non-zero words and their indices), Cv / Ci (wn each: C_k's non-zero words and their
+// indices), ids (64 object ids), scratch (32), the attribute list of B (M 16-bit positions); rounded
+// up to an even count.
 __host__ __device__ inline long long covers_words_per_warp(const Dims &d)
 {
-    return (3ll * d.m + 3ll * d.wn + 64 + 1) & ~1ll;   // even: R stays 8-byte aligned
+    return (4ll * d.m + 4ll * d.wn + 64 + 32 + (d.m + 1) / 2 + 1) & ~1ll;   // even: R stays 8-byte aligned
 }
+
+constexpr int COVER_GRAB = 4;   // concepts a warp takes from the work cursor at a time
 
 struct CoversArgs {
     Dims d;
     const uint32_t *intents;   // count x wm, attribute order
     unsigned long long count;
     const uint32_t *rows;      // n x wm, processing order
+    const int32_t *inv;        // processing position -> attribute (null: the identity)
     const int32_t *perm;       // attribute -> processing position (null: the identity)
+    const uint32_t *cols_p;    // m x wnp, processing order
     const uint32_t *cols;      // m x wnp, attribute order
     const uint32_t *slots;     // hash table of intents
     unsigned long long mask;   // slots - 1
@@ -115,6 +223,26 @@ struct CoversArgs {
     unsigned long long capacity;
     LatticeCounters *lc;
 };
+
+// The row of intent D (lane w holds word w) in the intent set, through the hash table; -1 when it is
+// not there (warp-wide).
+__device__ __forceinline__ long long find_intent(const CoversArgs &a, uint32_t Dw, unsigned lane)
+{
+    const Dims &d = a.d;
+    unsigned long long h = (int)lane < d.wm ? word_hash((int)lane, Dw) : 0ull;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) h += __shfl_xor_sync(FULL, h, o);
+    unsigned long long slot = h & a.mask;
+    for (unsigned long long probe = 0; probe <= a.mask; ++probe) {
+        const uint32_t idx = a.slots[slot];
+        if (idx == EMPTY_SLOT) return -1;
+        const bool eq = (int)lane >= d.wm ||
+                        (a.intents[(size_t)idx * d.wm + lane] & valid_bits(lane, d.wm, d.m)) == Dw;
+        if (__all_sync(FULL, eq)) return idx;
+        slot = (slot + 1) & a.mask;
+    }
+    return -1;
+}
 
 __global__ void __launch_bounds__(256) covers_kernel(const __grid_constant__ CoversArgs a)
 {
@@ -125,201 +253,255 @@ __global__ void __launch_bounds__(256) covers_kernel(const __grid_constant__ Cov
     uint32_t *base = lat_smem + (size_t)warp * covers_words_per_warp(d);
     unsigned long long *R = reinterpret_cast<unsigned long long *>(base);
     int *s = reinterpret_cast<int *>(base + 2 * d.m);
-    uint32_t *Aw = base + 3 * d.m;
+    uint32_t *eb = base + 3 * d.m;
+    uint32_t *Aw = base + 4 * d.m;
     uint32_t *Ai = Aw + d.wn;
-    uint32_t *Cw = Ai + d.wn;
-    uint32_t *ids = Cw + d.wn;
+    uint32_t *Cv = Ai + d.wn;
+    uint32_t *Ci = Cv + d.wn;
+    uint32_t *ids = Ci + d.wn;
+    uint32_t *scratch = ids + 64;
+    uint16_t *list = reinterpret_cast<uint16_t *>(scratch + 32);
     const int chunks = (d.m + 31) >> 5;   // = wm
 
     for (;;) {
-        unsigned long long i = 0;
-        if (lane == 0) i = atomicAdd(&a.lc->next, 1ull);
-        i = __shfl_sync(FULL, i, 0);
-        if (i >= a.count) break;
+        unsigned long long i0 = 0;
+        if (lane == 0) i0 = atomicAdd(&a.lc->next, (unsigned long long)COVER_GRAB);
+        i0 = __shfl_sync(FULL, i0, 0);
+        if (i0 >= a.count) break;
+        const unsigned long long i1 = i0 + COVER_GRAB < a.count ? i0 + COVER_GRAB : a.count;
+        for (unsigned long long i = i0; i < i1; ++i) {
+            // B: lane w holds word w
+            const uint32_t Bw = (int)lane < d.wm ? a.intents[i * d.wm + lane] & valid_bits(lane, d.wm, d.m) : 0u;
 
-        // B: lane w holds word w
-        const uint32_t Bw = (int)lane < d.wm ? a.intents[i * d.wm + lane] & valid_bits(lane, d.wm, d.m) : 0u;
-
-        // A = B': AND of the columns of B's attributes, kept as its non-zero words
-        int nnz = 0, objs = 0;
-        for (long long w0 = 0; w0 < d.wn; w0 += 32) {
-            const long long w = w0 + lane;
-            uint32_t acc = w < d.wn ? valid_bits(w, d.wn, d.n) : 0u;
-            for (int t = 0; t < d.wm; ++t) {
-                uint32_t bits = __shfl_sync(FULL, Bw, t);
-                while (bits) {
-                    if (!__any_sync(FULL, acc != 0u)) break;
-                    const int at = 32 * t + __ffs(bits) - 1;
-                    bits &= bits - 1u;
-                    if (acc) acc &= __ldg(a.cols + (size_t)at * d.wnp + w);
-                }
-            }
-            const unsigned nzb = __ballot_sync(FULL, acc != 0u);
-            if (acc) {
-                const int p = nnz + __popc(nzb & ((1u << lane) - 1u));
-                Aw[p] = acc;
-                Ai[p] = (uint32_t)w;
-            }
-            nnz += __popc(nzb);
-            objs += __reduce_add_sync(FULL, (unsigned)__popc(acc));
-        }
-        __syncwarp();
-
-        const bool small = objs <= 64;
-        if (small) {
-            // object ids of A (at most 64; every non-zero word holds at least one object)
-            unsigned off = 0;
-            for (int j0 = 0; j0 < nnz; j0 += 32) {
-                const int j = j0 + (int)lane;
-                const uint32_t v = j < nnz ? Aw[j] : 0u;
-                const unsigned c = __popc(v);
-                unsigned pre = c;   // inclusive prefix sum of the popcounts
+            // A = B': AND of the columns of B's attributes (rarest first), kept as its non-zero words
+            const int nb = attr_list(Bw, a.perm, list, scratch, d.wm, lane);
+            int nnz = 0, objs = 0;
+            for (long long w0 = 0; w0 < d.wn; w0 += 32 * EXT_U) {
+                uint32_t acc[EXT_U];
 #pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const unsigned y = __shfl_up_sync(FULL, pre, o);
-                    if ((int)lane >= o) pre += y;
+                for (int u = 0; u < EXT_U; ++u) {
+                    const long long w = w0 + 32 * u + lane;
+                    acc[u] = w < d.wn ? valid_bits(w, d.wn, d.n) : 0u;
                 }
-                unsigned p = off + pre - c;
-                uint32_t x = v;
-                while (x) {
-                    const int b = __ffs(x) - 1;
-                    x &= x - 1u;
-                    ids[p++] = (uint32_t)(32 * Ai[j] + b);
+                extent_words<EXT_U>(acc, list, nb, a.cols_p, d.wnp, w0, lane);
+#pragma unroll
+                for (int u = 0; u < EXT_U; ++u) {
+                    const unsigned nzb = __ballot_sync(FULL, acc[u] != 0u);
+                    if (acc[u]) {
+                        const int p = nnz + __popc(nzb & ((1u << lane) - 1u));
+                        Aw[p] = acc[u];
+                        Ai[p] = (uint32_t)(w0 + 32 * u + lane);
+                    }
+                    nnz += __popc(nzb);
+                    objs += __reduce_add_sync(FULL, (unsigned)__popc(acc[u]));
                 }
-                off += __shfl_sync(FULL, pre, 31);
             }
             __syncwarp();
-            // restricted columns by processing position: R[p] bit o = object ids[o] has the
-            // attribute at position p (rows are in processing order)
-            const uint32_t *r0 = (int)lane < objs ? a.rows + (size_t)ids[lane] * d.wm : nullptr;
-            const uint32_t *r1 = (int)lane + 32 < objs ? a.rows + (size_t)ids[lane + 32] * d.wm : nullptr;
-            for (int t = 0; t < d.wm; ++t) {
-                const uint32_t lo = warp_transpose32(r0 ? __ldg(r0 + t) : 0u);
-                const uint32_t hi = objs > 32 ? warp_transpose32(r1 ? __ldg(r1 + t) : 0u) : 0u;
-                const int p = 32 * t + (int)lane;
-                if (p < d.m) R[p] = ((unsigned long long)hi << 32) | lo;
-            }
-            __syncwarp();
-        }
 
-        // supports s_k = |C_k| for k not in B (-1 for k in B)
-        for (int c = 0; c < chunks; ++c) {
-            const int k = 32 * c + (int)lane;
-            const uint32_t bword = __shfl_sync(FULL, Bw, c);
-            const bool inB = (bword >> lane) & 1u;
-            int sk = -1;
-            if (k < d.m && !inB) {
-                if (small) {
-                    const int p = a.perm ? a.perm[k] : k;
-                    sk = __popcll(R[p]);
-                } else {
-                    sk = 0;
-                    const uint32_t *col = a.cols + (size_t)k * d.wnp;
-                    for (int j = 0; j < nnz; ++j) sk += __popc(Aw[j] & __ldg(col + Ai[j]));
+            int ne = 0;   // covers found for concept i (rows in eb)
+            const bool small = objs <= 64;
+            if (small) {
+                // object ids of A (at most 64; every non-zero word holds at least one object)
+                unsigned off = 0;
+                for (int j0 = 0; j0 < nnz; j0 += 32) {
+                    const int j = j0 + (int)lane;
+                    const uint32_t v = j < nnz ? Aw[j] : 0u;
+                    const unsigned c = __popc(v);
+                    unsigned pre = c;   // inclusive prefix sum of the popcounts
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const unsigned y = __shfl_up_sync(FULL, pre, o);
+                        if ((int)lane >= o) pre += y;
+                    }
+                    unsigned p = off + pre - c;
+                    uint32_t x = v;
+                    while (x) {
+                        const int b = __ffs(x) - 1;
+                        x &= x - 1u;
+                        ids[p++] = (uint32_t)(32 * Ai[j] + b);
+                    }
+                    off += __shfl_sync(FULL, pre, 31);
                 }
-            }
-            if (k < d.m) s[k] = sk;
-        }
-        __syncwarp();
-
-        // each candidate k: maximal among the C_k and the smallest attribute of its class
-        for (int c = 0; c < chunks; ++c) {
-            uint32_t cand = ~__shfl_sync(FULL, Bw, c) & valid_bits(c, d.wm, d.m);
-            while (cand) {
-                const int k = 32 * c + __ffs(cand) - 1;
-                cand &= cand - 1u;
-                const int sk = s[k];
-                unsigned long long Rk = 0;
-                if (small) {
-                    Rk = R[a.perm ? a.perm[k] : k];
-                } else {
-                    const uint32_t *col = a.cols + (size_t)k * d.wnp;
-                    for (int j = (int)lane; j < nnz; j += 32) Cw[j] = Aw[j] & __ldg(col + Ai[j]);
-                    __syncwarp();
+                __syncwarp();
+                // restricted sets by attribute: R[k] bit o = object ids[o] has attribute k (the rows are
+                // in processing order; inv maps a position back to its attribute)
+                const uint32_t *r0 = (int)lane < objs ? a.rows + (size_t)ids[lane] * d.wm : nullptr;
+                const uint32_t *r1 = (int)lane + 32 < objs ? a.rows + (size_t)ids[lane + 32] * d.wm : nullptr;
+                for (int t = 0; t < d.wm; ++t) {
+                    const uint32_t lo = warp_transpose32(r0 ? __ldg(r0 + t) : 0u);
+                    const uint32_t hi = objs > 32 ? warp_transpose32(r1 ? __ldg(r1 + t) : 0u) : 0u;
+                    const int p = 32 * t + (int)lane;
+                    if (p < d.m) R[a.inv ? a.inv[p] : p] = ((unsigned long long)hi << 32) | lo;
                 }
-                bool bad = false;
-                uint32_t Dw = Bw;
-                for (int c2 = 0; c2 < chunks && !bad; ++c2) {
-                    const int k2 = 32 * c2 + (int)lane;
-                    bool in = false;
-                    if (k2 < d.m && k2 != k) {
+                __syncwarp();
+                // supports s_k = |C_k| for k not in B (-1 for k in B)
+                for (int c = 0; c < chunks; ++c) {
+                    const int k = 32 * c + (int)lane;
+                    const bool inB = (__shfl_sync(FULL, Bw, c) >> lane) & 1u;
+                    if (k < d.m) s[k] = inB ? -1 : __popcll(R[k]);
+                }
+                __syncwarp();
+                // the covers: candidates k whose C_k is maximal among the C_k and that are the smallest
+                // attribute of their class (no other k2 has C_k inside C_k2 with more objects, or the
+                // same set and a smaller index). Each lane tests its own candidates against every
+                // attribute; the loop over k2 is the same in every lane, so its shared-memory reads are
+                // broadcasts.
+                for (int c = 0; c < chunks; ++c) {
+                    const int k = 32 * c + (int)lane;
+                    const int sk = k < d.m ? s[k] : -1;
+                    const unsigned long long Rk = sk >= 0 ? R[k] : 0ull;
+                    bool bad = sk < 0;
+                    for (int k2 = 0; k2 < d.m; ++k2) {
+                        if ((k2 & 15) == 0 && __all_sync(FULL, bad)) break;
                         const int s2 = s[k2];
-                        if (s2 >= sk) {   // s2 < 0 for attributes of B
-                            if (small) {
-                                in = (Rk & ~R[a.perm ? a.perm[k2] : k2]) == 0ull;
-                            } else {
+                        if (!bad && k2 != k && s2 >= sk && (Rk & ~R[k2]) == 0ull && (s2 > sk || k2 < k)) bad = true;
+                    }
+                    unsigned emit = __ballot_sync(FULL, !bad);
+                    while (emit) {
+                        const int kk = 32 * c + __ffs(emit) - 1;
+                        emit &= emit - 1u;
+                        const int skk = s[kk];
+                        const unsigned long long Rkk = R[kk];
+                        // D = B + {k2 : C_k2 = C_kk}
+                        uint32_t Dw = Bw;
+                        for (int c2 = 0; c2 < chunks; ++c2) {
+                            const int k2 = 32 * c2 + (int)lane;
+                            const bool in = k2 < d.m && s[k2] == skk && (Rkk & ~R[k2]) == 0ull;
+                            const uint32_t word = __ballot_sync(FULL, in);
+                            if ((int)lane == c2) Dw |= word;
+                        }
+                        const long long row = find_intent(a, Dw, lane);
+                        if (row < 0) {
+                            if (lane == 0) atomicAdd(&a.lc->missing, 1ull);
+                        } else {
+                            if (lane == 0) eb[ne] = (uint32_t)row;
+                            ++ne;
+                        }
+                    }
+                }
+            } else {
+                // supports, one attribute at a time, lanes over A's non-zero words
+                for (int c = 0; c < chunks; ++c) {
+                    const int k = 32 * c + (int)lane;
+                    if (k < d.m) s[k] = -1;
+                }
+                __syncwarp();
+                for (int c = 0; c < chunks; ++c) {
+                    uint32_t cand = ~__shfl_sync(FULL, Bw, c) & valid_bits(c, d.wm, d.m);
+                    while (cand) {
+                        const int k = 32 * c + __ffs(cand) - 1;
+                        cand &= cand - 1u;
+                        const uint32_t *col = a.cols + (size_t)k * d.wnp;
+                        unsigned cnt = 0;
+                        for (int j = (int)lane; j < nnz; j += 32) cnt += __popc(Aw[j] & __ldg(col + Ai[j]));
+                        cnt = __reduce_add_sync(FULL, cnt);
+                        if (lane == 0) s[k] = (int)cnt;
+                    }
+                }
+                __syncwarp();
+                // each candidate in turn: C_k's non-zero words compacted, then lanes take the k2 and
+                // test C_k inside column k2 on those words only
+                for (int c = 0; c < chunks; ++c) {
+                    uint32_t cand = ~__shfl_sync(FULL, Bw, c) & valid_bits(c, d.wm, d.m);
+                    while (cand) {
+                        const int k = 32 * c + __ffs(cand) - 1;
+                        cand &= cand - 1u;
+                        const int sk = s[k];
+                        const uint32_t *col = a.cols + (size_t)k * d.wnp;
+                        int cnz = 0;
+                        for (int j0 = 0; j0 < nnz; j0 += 32) {
+                            const int j = j0 + (int)lane;
+                            const uint32_t v = j < nnz ? Aw[j] & __ldg(col + Ai[j]) : 0u;
+                            const unsigned nzb = __ballot_sync(FULL, v != 0u);
+                            if (v) {
+                                const int p = cnz + __popc(nzb & ((1u << lane) - 1u));
+                                Cv[p] = v;
+                                Ci[p] = Ai[j];
+                            }
+                            cnz += __popc(nzb);
+                        }
+                        __syncwarp();
+                        bool bad = false;
+                        uint32_t Dw = Bw;
+                        for (int c2 = 0; c2 < chunks && !bad; ++c2) {
+                            const int k2 = 32 * c2 + (int)lane;
+                            bool in = false;
+                            if (k2 < d.m && k2 != k && s[k2] >= sk) {   // s < 0 for attributes of B
                                 const uint32_t *col2 = a.cols + (size_t)k2 * d.wnp;
                                 in = true;
-                                for (int j = 0; j < nnz; ++j) {
-                                    if (Cw[j] & ~__ldg(col2 + Ai[j])) {
+                                for (int j = 0; j < cnz; ++j) {
+                                    if (Cv[j] & ~__ldg(col2 + Ci[j])) {
                                         in = false;
                                         break;
                                     }
                                 }
+                                if (in && (s[k2] > sk || k2 < k)) bad = true;
                             }
-                            if (in && (s2 > sk || k2 < k)) bad = true;
+                            bad = __any_sync(FULL, bad);
+                            const uint32_t word = __ballot_sync(FULL, in);
+                            if ((int)lane == c2) Dw |= word;
                         }
-                    }
-                    bad = __any_sync(FULL, bad);
-                    const uint32_t word = __ballot_sync(FULL, in);
-                    if ((int)lane == c2) Dw |= word;
-                }
-                if (!small) __syncwarp();
-                if (bad) continue;
-                if ((int)lane == (k >> 5)) Dw |= 1u << (k & 31);
-
-                // row index of D
-                unsigned long long h = (int)lane < d.wm ? word_hash(lane, Dw) : 0ull;
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) h += __shfl_xor_sync(FULL, h, o);
-                unsigned long long slot = h & a.mask;
-                long long found = -1;
-                for (unsigned long long probe = 0; probe <= a.mask; ++probe) {
-                    const uint32_t idx = a.slots[slot];
-                    if (idx == EMPTY_SLOT) break;
-                    const bool eq = (int)lane >= d.wm ||
-                                    (a.intents[(size_t)idx * d.wm + lane] & valid_bits(lane, d.wm, d.m)) == Dw;
-                    if (__all_sync(FULL, eq)) {
-                        found = idx;
-                        break;
-                    }
-                    slot = (slot + 1) & a.mask;
-                }
-                if (lane == 0) {
-                    if (found < 0) {
-                        atomicAdd(&a.lc->missing, 1ull);
-                    } else {
-                        const unsigned long long e = atomicAdd(&a.lc->edges, 1ull);
-                        if (e < a.capacity) {
-                            a.edges[2 * e] = (uint32_t)i;
-                            a.edges[2 * e + 1] = (uint32_t)found;
+                        __syncwarp();
+                        if (bad) continue;
+                        if ((int)lane == (k >> 5)) Dw |= 1u << (k & 31);
+                        const long long row = find_intent(a, Dw, lane);
+                        if (row < 0) {
+                            if (lane == 0) atomicAdd(&a.lc->missing, 1ull);
+                        } else {
+                            if (lane == 0) eb[ne] = (uint32_t)row;
+                            ++ne;
                         }
                     }
                 }
             }
+            // the concept's edges: one slot allocation, then the rows
+            __syncwarp();
+            if (ne) {
+                unsigned long long e0 = 0;
+                if (lane == 0) e0 = atomicAdd(&a.lc->edges, (unsigned long long)ne);
+                e0 = __shfl_sync(FULL, e0, 0);
+                for (int j = (int)lane; j < ne; j += 32) {
+                    const unsigned long long e = e0 + j;
+                    if (e < a.capacity) {
+                        a.edges[2 * e] = (uint32_t)i;
+                        a.edges[2 * e + 1] = eb[j];
+                    }
+                }
+            }
+            __syncwarp();
         }
-        __syncwarp();
     }
 }
 
 }  // namespace
 
-int launch_extents(const uint32_t *intents, uint64_t count, const uint32_t *cols, const Dims &d, uint32_t *extents,
-                   int sm_count, void *stream)
+int launch_extents(const uint32_t *intents, uint64_t count, const uint32_t *cols, const uint32_t *cols_p,
+                   const int32_t *perm, const Dims &d, uint32_t *extents, int sm_count, void *stream)
 {
     if (count == 0) return (int)cudaSuccess;
-    const unsigned long long total = count * (unsigned long long)d.wn;
-    const unsigned long long want = (total + 255) / 256;
-    const unsigned blocks = (unsigned)std::min<unsigned long long>(want, 16ull * sm_count);
-    extents_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>(intents, count, cols, d, extents);
+    int g = 1;
+    while (g < 32 && g < d.wn) g <<= 1;
+    const unsigned long long rows_per_block = 8ull * (32 / g);
+    const unsigned blocks = (unsigned)std::min<unsigned long long>((count + rows_per_block - 1) / rows_per_block,
+                                                                   8ull * sm_count);
+    cudaStream_t st = (cudaStream_t)stream;
+    switch (g) {
+    case 1: extents_kernel<1><<<blocks, 256, 0, st>>>(intents, count, cols, cols_p, perm, d, extents); break;
+    case 2: extents_kernel<2><<<blocks, 256, 0, st>>>(intents, count, cols, cols_p, perm, d, extents); break;
+    case 4: extents_kernel<4><<<blocks, 256, 0, st>>>(intents, count, cols, cols_p, perm, d, extents); break;
+    case 8: extents_kernel<8><<<blocks, 256, 0, st>>>(intents, count, cols, cols_p, perm, d, extents); break;
+    case 16: extents_kernel<16><<<blocks, 256, 0, st>>>(intents, count, cols, cols_p, perm, d, extents); break;
+    default: extents_kernel<32><<<blocks, 256, 0, st>>>(intents, count, cols, cols_p, perm, d, extents); break;
+    }
     return (int)cudaGetLastError();
 }
 
 size_t covers_smem_per_warp(const Dims &d) { return (size_t)covers_words_per_warp(d) * 4; }
 
-int launch_covers(const uint32_t *intents, uint64_t count, const uint32_t *rows, const int32_t *perm,
-                  const uint32_t *cols, const Dims &d, uint32_t *slots, uint64_t nslots, uint32_t *edges,
-                  uint64_t capacity, LatticeCounters *lc, int sm_count, void *stream)
+int launch_covers(const uint32_t *intents, uint64_t count, const uint32_t *rows, const int32_t *inv,
+                  const int32_t *perm, const uint32_t *cols, const uint32_t *cols_p, const Dims &d, uint32_t *slots,
+                  uint64_t nslots, uint32_t *edges, uint64_t capacity, LatticeCounters *lc, int sm_count,
+                  void *stream)
 {
     cudaStream_t st = (cudaStream_t)stream;
     cudaError_t e = cudaMemsetAsync(slots, 0xff, (size_t)nslots * 4, st);
@@ -349,7 +531,9 @@ int launch_covers(const uint32_t *intents, uint64_t count, const uint32_t *rows,
     a.intents = intents;
     a.count = count;
     a.rows = rows;
+    a.inv = inv;
     a.perm = perm;
+    a.cols_p = cols_p;
     a.cols = cols;
     a.slots = slots;
     a.mask = nslots - 1;

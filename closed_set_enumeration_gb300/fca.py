@@ -35,7 +35,8 @@ class FcaStats(ctypes.Structure):
         "concepts", "closures", "large_parents", "small_roots", "launches", "levels",
         "max_frontier", "frontier_bytes", "expand_launches", "subtree_launches",
         "subtree_word_ops", "expand_bytes", "retries", "spill_rounds")] + [("expand_ms", ctypes.c_double),
-                                                ("subtree_ms", ctypes.c_double)]
+                                                ("subtree_ms", ctypes.c_double),
+                                                ("lattice_ms", ctypes.c_double)]
 
     def as_dict(self) -> dict:
         return {name: (float(getattr(self, name)) if ty is ctypes.c_double else int(getattr(self, name)))

@@ -58,6 +58,8 @@ typedef struct {
                                   budget (their roots are counted in small_roots) */
     double expand_ms;          /* device time of the bitmap-extent kernel launches */
     double subtree_ms;         /* device time of the object-list kernel launches */
+    double lattice_ms;         /* device time of the kernels of the last fca_extents or
+                                  fca_cover_edges call on the context (0 before the first) */
 } fca_stats;
 
 /* Options for fca_set_option. */
@@ -173,8 +175,8 @@ fca_status fca_extents(fca_ctx *ctx, const uint32_t *intents, uint64_t count, ui
  * Uses stream-ordered device scratch of about 8 bytes per intent and
  * returns after the work on `stream` completes. FCA_ERR_INVALID when a
  * cover's intent is not in the given set (the set was not complete), or
- * when a warp's shared memory cannot hold three N-bit extents and 3M
- * words (N up to about 500 000 objects at small M).
+ * when a warp's shared memory cannot hold four N-bit sets and 4.5 M
+ * words (N up to about 400 000 objects at small M).
  */
 fca_status fca_cover_edges(fca_ctx *ctx, const uint32_t *intents, uint64_t count, uint32_t *edges,
                            uint64_t capacity, uint64_t *out_edges, void *stream);
