@@ -1135,28 +1135,31 @@ fca_status fca_cover_edges(fca_ctx *ctx, const uint32_t *intents, uint64_t count
         c->err = "cover edges take fewer than 2^32 - 1 intents";
         return FCA_ERR_INVALID;
     }
-    if (covers_smem_per_warp(c->d) > 200 * 1024) {
-        c->err = "cover edges: N and M too large for one warp's shared memory";
-        return FCA_ERR_INVALID;
-    }
     if (count == 0) return FCA_OK;
     CK(cudaSetDevice(c->device), "cudaSetDevice");
     cudaStream_t st = (cudaStream_t)stream;
     uint64_t nslots = 64;
     while (nslots < 2 * count) nslots <<= 1;
+    int wpb = 0;
+    unsigned blocks = 0;
+    size_t smem = 0;
+    CK((cudaError_t)covers_shape(c->d, count, c->sm_count, &wpb, &blocks, &smem), "cover kernel shape");
+    const size_t ws_bytes = (size_t)blocks * wpb * 4 * (size_t)c->d.wn * 4;
     LatticeCounters *lc = nullptr;
-    uint32_t *slots = nullptr;
+    uint32_t *slots = nullptr, *ws = nullptr;
     CK(cudaMallocAsync((void **)&lc, sizeof(LatticeCounters), st), "cudaMallocAsync");
     cudaError_t e = cudaMallocAsync((void **)&slots, nslots * 4, st);
+    if (e == cudaSuccess) e = cudaMallocAsync((void **)&ws, ws_bytes, st);
     LatticeCounters h{};
     if (e == cudaSuccess) e = cudaMemsetAsync(lc, 0, sizeof(LatticeCounters), st);
     if (e == cudaSuccess && lattice_time_begin(c, st) != FCA_OK) e = cudaErrorUnknown;
     if (e == cudaSuccess)
         e = (cudaError_t)launch_covers(intents, count, c->rows, c->ordered ? c->inv : nullptr,
                                        c->ordered ? c->perm : nullptr, c->cols_buf[0], c->cols, c->d, slots, nslots,
-                                       edges, capacity, lc, c->sm_count, st);
+                                       edges, capacity, lc, ws, wpb, blocks, smem, c->sm_count, st);
     if (e == cudaSuccess && lattice_time_end(c, st) != FCA_OK) e = cudaErrorUnknown;
     if (e == cudaSuccess) e = cudaMemcpyAsync(&h, lc, sizeof h, cudaMemcpyDeviceToHost, st);
+    if (ws) cudaFreeAsync(ws, st);
     if (slots) cudaFreeAsync(slots, st);
     cudaFreeAsync(lc, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);

@@ -181,15 +181,19 @@ size_t expand_smem_per_warp(const Dims &d);
 // -> position, null when the two orders are the same). One launch.
 int launch_extents(const uint32_t *intents, uint64_t count, const uint32_t *cols, const uint32_t *cols_p,
                    const int32_t *perm, const Dims &d, uint32_t *extents, int sm_count, void *stream);
+// Launch shape of the cover kernel for `count` intents: warps per block, blocks (a persistent grid of
+// at most the resident blocks) and dynamic shared memory; the caller allocates 4 x wn words of
+// workspace per warp of that grid.
+int covers_shape(const Dims &d, uint64_t count, int sm_count, int *wpb, unsigned *blocks, size_t *smem);
 // Cover edges of a complete intent set: a hash table of the intents in `slots` (nslots, a power of two
 // of at least twice count), then the lower covers of every concept as (row, row of the cover) pairs.
 // rows and cols_p are in processing order (inv: position -> attribute, perm: attribute -> position,
-// both null for the identity), cols in attribute order; lc zeroed by the caller. A memset and two
-// launches.
+// both null for the identity), cols in attribute order; lc zeroed by the caller; ws, wpb, blocks and
+// smem from covers_shape. A memset and two launches.
 int launch_covers(const uint32_t *intents, uint64_t count, const uint32_t *rows, const int32_t *inv,
                   const int32_t *perm, const uint32_t *cols, const uint32_t *cols_p, const Dims &d, uint32_t *slots,
-                  uint64_t nslots, uint32_t *edges, uint64_t capacity, LatticeCounters *lc, int sm_count,
-                  void *stream);
+                  uint64_t nslots, uint32_t *edges, uint64_t capacity, LatticeCounters *lc, uint32_t *ws, int wpb,
+                  unsigned blocks, size_t smem, int sm_count, void *stream);
 // Shared memory of one covers_kernel warp (bytes).
 size_t covers_smem_per_warp(const Dims &d);
 

@@ -34,7 +34,8 @@ __device__ __forceinline__ uint32_t valid_bits(long long w, long long words, lon
 
 // The attributes of B in processing order, rarest first: lane w holds word w of B (attribute
 // order); the positions (perm maps an attribute to its position, null: the identity) are written in
-// ascending order to list[0..nb) and nb is returned to every lane. scratch holds W_M words.
+// ascending order to list[0..nb) and nb is returned to every lane. scratch (W_M words) receives B by
+// position.
 __device__ __forceinline__ int attr_list(uint32_t Bw, const int32_t *perm, uint16_t *list, uint32_t *scratch, int wm,
                                          unsigned lane)
 {
@@ -49,6 +50,9 @@ __device__ __forceinline__ int attr_list(uint32_t Bw, const int32_t *perm, uint1
         }
         __syncwarp();
         Bw = (int)lane < wm ? scratch[lane] : 0u;
+    } else {
+        if ((int)lane < wm) scratch[lane] = Bw;
+        __syncwarp();
     }
     const unsigned c = __popc(Bw);
     unsigned pre = c;   // inclusive prefix sum over the lanes
@@ -197,13 +201,13 @@ __global__ void __launch_bounds__(256) hash_insert_kernel(const uint32_t *__rest
 }
 
 // Per-warp shared memory of covers_kernel, in 32-bit words: R (2M: 64-bit restricted sets by
-// attribute), s (M supports), eb (M: rows of the covers found for the current concept), Aw / Ai
-// (wn each: A's non-zero words and their indices), Cv / Ci (wn each: C_k's non-zero words and their
-// indices), ids (64 object ids), scratch (32), the attribute list of B (M 16-bit positions); rounded
-// up to an even count.
+// attribute), s (M supports), eb (M: rows of the covers found for the current concept), ids (64 object
+// ids), scratch (32: B by position), rows of A's objects (64 x W_M, when A has at most 64), the
+// attribute list of B (M 16-bit positions); rounded up to an even count. Each warp also has 4 W_N words
+// of global workspace: A's non-zero words and their indices, C_k's non-zero words and their indices.
 __host__ __device__ inline long long covers_words_per_warp(const Dims &d)
 {
-    return (4ll * d.m + 4ll * d.wn + 64 + 32 + (d.m + 1) / 2 + 1) & ~1ll;   // even: R stays 8-byte aligned
+    return (4ll * d.m + 64 + 32 + 64ll * d.wm + (d.m + 1) / 2 + 1) & ~1ll;   // even: R 8-byte aligned
 }
 
 constexpr int COVER_GRAB = 4;   // concepts a warp takes from the work cursor at a time
@@ -222,6 +226,7 @@ struct CoversArgs {
     uint32_t *edges;           // capacity x 2
     unsigned long long capacity;
     LatticeCounters *lc;
+    uint32_t *ws;              // 4 x wn words per warp of the grid
 };
 
 // The row of intent D (lane w holds word w) in the intent set, through the hash table; -1 when it is
@@ -254,13 +259,14 @@ __global__ void __launch_bounds__(256) covers_kernel(const __grid_constant__ Cov
     unsigned long long *R = reinterpret_cast<unsigned long long *>(base);
     int *s = reinterpret_cast<int *>(base + 2 * d.m);
     uint32_t *eb = base + 3 * d.m;
-    uint32_t *Aw = base + 4 * d.m;
+    uint32_t *ids = base + 4 * d.m;
+    uint32_t *Aw = a.ws + ((size_t)blockIdx.x * (blockDim.x >> 5) + warp) * 4 * (size_t)d.wn;
     uint32_t *Ai = Aw + d.wn;
     uint32_t *Cv = Ai + d.wn;
     uint32_t *Ci = Cv + d.wn;
-    uint32_t *ids = Ci + d.wn;
     uint32_t *scratch = ids + 64;
-    uint16_t *list = reinterpret_cast<uint16_t *>(scratch + 32);
+    uint32_t *rowsm = scratch + 32;
+    uint16_t *list = reinterpret_cast<uint16_t *>(rowsm + 64 * d.wm);
     const int chunks = (d.m + 31) >> 5;   // = wm
 
     for (;;) {
@@ -323,13 +329,17 @@ __global__ void __launch_bounds__(256) covers_kernel(const __grid_constant__ Cov
                     off += __shfl_sync(FULL, pre, 31);
                 }
                 __syncwarp();
-                // restricted sets by attribute: R[k] bit o = object ids[o] has attribute k (the rows are
-                // in processing order; inv maps a position back to its attribute)
-                const uint32_t *r0 = (int)lane < objs ? a.rows + (size_t)ids[lane] * d.wm : nullptr;
-                const uint32_t *r1 = (int)lane + 32 < objs ? a.rows + (size_t)ids[lane + 32] * d.wm : nullptr;
+                // the rows of A's objects (processing order), then the restricted sets by attribute:
+                // R[k] bit o = object ids[o] has attribute k (inv maps a position back to its attribute)
+                for (int x = (int)lane; x < objs * d.wm; x += 32) {
+                    const int o = x / d.wm;
+                    rowsm[x] = __ldg(a.rows + (size_t)ids[o] * d.wm + (x - o * d.wm));
+                }
+                __syncwarp();
                 for (int t = 0; t < d.wm; ++t) {
-                    const uint32_t lo = warp_transpose32(r0 ? __ldg(r0 + t) : 0u);
-                    const uint32_t hi = objs > 32 ? warp_transpose32(r1 ? __ldg(r1 + t) : 0u) : 0u;
+                    const uint32_t lo = warp_transpose32((int)lane < objs ? rowsm[lane * d.wm + t] : 0u);
+                    const uint32_t hi =
+                        objs > 32 ? warp_transpose32((int)lane + 32 < objs ? rowsm[(lane + 32) * d.wm + t] : 0u) : 0u;
                     const int p = 32 * t + (int)lane;
                     if (p < d.m) R[a.inv ? a.inv[p] : p] = ((unsigned long long)hi << 32) | lo;
                 }
@@ -343,18 +353,36 @@ __global__ void __launch_bounds__(256) covers_kernel(const __grid_constant__ Cov
                 __syncwarp();
                 // the covers: candidates k whose C_k is maximal among the C_k and that are the smallest
                 // attribute of their class (no other k2 has C_k inside C_k2 with more objects, or the
-                // same set and a smaller index). Each lane tests its own candidates against every
-                // attribute; the loop over k2 is the same in every lane, so its shared-memory reads are
-                // broadcasts.
+                // same set and a smaller index). The k2 with C_k inside C_k2 are the attributes of
+                // D_k = C_k', the AND of the rows of C_k's objects (every attribute when C_k is empty),
+                // so each lane closes its own candidate and checks the supports of D_k outside B.
                 for (int c = 0; c < chunks; ++c) {
                     const int k = 32 * c + (int)lane;
                     const int sk = k < d.m ? s[k] : -1;
-                    const unsigned long long Rk = sk >= 0 ? R[k] : 0ull;
                     bool bad = sk < 0;
-                    for (int k2 = 0; k2 < d.m; ++k2) {
-                        if ((k2 & 15) == 0 && __all_sync(FULL, bad)) break;
-                        const int s2 = s[k2];
-                        if (!bad && k2 != k && s2 >= sk && (Rk & ~R[k2]) == 0ull && (s2 > sk || k2 < k)) bad = true;
+                    if (!bad) {
+                        const unsigned long long Rk = R[k];
+                        for (int t = 0; t < d.wm && !bad; ++t) {
+                            uint32_t dk = valid_bits(t, d.wm, d.m);
+                            unsigned long long x = Rk;
+                            while (x && dk) {
+                                const int o = __ffsll(x) - 1;
+                                x &= x - 1ull;
+                                dk &= rowsm[o * d.wm + t];
+                            }
+                            dk &= ~scratch[t];   // D_k outside B, by processing position
+                            while (dk) {
+                                const int p = 32 * t + __ffs(dk) - 1;
+                                dk &= dk - 1u;
+                                const int k2 = a.inv ? a.inv[p] : p;
+                                if (k2 == k) continue;
+                                const int s2 = s[k2];
+                                if (s2 > sk || (s2 == sk && k2 < k)) {
+                                    bad = true;
+                                    break;
+                                }
+                            }
+                        }
                     }
                     unsigned emit = __ballot_sync(FULL, !bad);
                     while (emit) {
@@ -498,10 +526,28 @@ int launch_extents(const uint32_t *intents, uint64_t count, const uint32_t *cols
 
 size_t covers_smem_per_warp(const Dims &d) { return (size_t)covers_words_per_warp(d) * 4; }
 
+int covers_shape(const Dims &d, uint64_t count, int sm_count, int *wpb, unsigned *blocks, size_t *smem)
+{
+    const size_t per_warp = covers_smem_per_warp(d);
+    *wpb = (int)std::max<size_t>(1, std::min<size_t>(8, (200 * 1024) / per_warp));
+    *smem = per_warp * *wpb;
+    if (*smem > 227 * 1024) return (int)cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(covers_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)*smem);
+    if (e != cudaSuccess) return (int)e;
+    int per_sm = 1;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, covers_kernel, *wpb * 32, *smem)) != cudaSuccess)
+        return (int)e;
+    per_sm = std::max(1, per_sm);
+    *blocks = (unsigned)std::max<unsigned long long>(
+        1, std::min<unsigned long long>((std::max<uint64_t>(count, 1) + *wpb - 1) / *wpb,
+                                        (unsigned long long)per_sm * sm_count));
+    return (int)cudaSuccess;
+}
+
 int launch_covers(const uint32_t *intents, uint64_t count, const uint32_t *rows, const int32_t *inv,
                   const int32_t *perm, const uint32_t *cols, const uint32_t *cols_p, const Dims &d, uint32_t *slots,
-                  uint64_t nslots, uint32_t *edges, uint64_t capacity, LatticeCounters *lc, int sm_count,
-                  void *stream)
+                  uint64_t nslots, uint32_t *edges, uint64_t capacity, LatticeCounters *lc, uint32_t *ws, int wpb,
+                  unsigned blocks, size_t smem, int sm_count, void *stream)
 {
     cudaStream_t st = (cudaStream_t)stream;
     cudaError_t e = cudaMemsetAsync(slots, 0xff, (size_t)nslots * 4, st);
@@ -510,22 +556,6 @@ int launch_covers(const uint32_t *intents, uint64_t count, const uint32_t *rows,
     const unsigned ib = (unsigned)std::min<unsigned long long>((count + 255) / 256, 16ull * sm_count);
     hash_insert_kernel<<<ib, 256, 0, st>>>(intents, count, d.wm, d.m, slots, nslots - 1, lc);
     if ((e = cudaGetLastError()) != cudaSuccess) return (int)e;
-
-    const size_t per_warp = covers_smem_per_warp(d);
-    const size_t limit = 200 * 1024;
-    const int wpb = (int)std::max<size_t>(1, std::min<size_t>(8, limit / per_warp));
-    const size_t smem = per_warp * wpb;
-    if (smem > 227 * 1024) return (int)cudaErrorInvalidValue;
-    if ((e = cudaFuncSetAttribute(covers_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
-        cudaSuccess)
-        return (int)e;
-    int per_sm = 1;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, covers_kernel, wpb * 32, smem)) != cudaSuccess)
-        return (int)e;
-    per_sm = std::max(1, per_sm);
-    const unsigned long long warps_needed = count;
-    const unsigned blocks = (unsigned)std::max<unsigned long long>(
-        1, std::min<unsigned long long>((warps_needed + wpb - 1) / wpb, (unsigned long long)per_sm * sm_count));
     CoversArgs a;
     a.d = d;
     a.intents = intents;
@@ -540,6 +570,7 @@ int launch_covers(const uint32_t *intents, uint64_t count, const uint32_t *rows,
     a.edges = edges;
     a.capacity = capacity;
     a.lc = lc;
+    a.ws = ws;
     covers_kernel<<<blocks, wpb * 32, smem, st>>>(a);
     return (int)cudaGetLastError();
 }

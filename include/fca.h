@@ -172,11 +172,11 @@ fca_status fca_extents(fca_ctx *ctx, const uint32_t *intents, uint64_t count, ui
  *              exceeds `capacity` (then FCA_ERR_CAPACITY, the first
  *              `capacity` edges written).
  *   stream     cudaStream_t (NULL = legacy default stream).
- * Uses stream-ordered device scratch of about 8 bytes per intent and
- * returns after the work on `stream` completes. FCA_ERR_INVALID when a
- * cover's intent is not in the given set (the set was not complete), or
- * when a warp's shared memory cannot hold four N-bit sets and 4.5 M
- * words (N up to about 400 000 objects at small M).
+ * Uses stream-ordered device scratch (about 8 bytes per intent, plus
+ * 16 W_N bytes for each warp of the kernel's grid, which is sized to the
+ * warps resident on the GPU) and returns after the work on `stream`
+ * completes. FCA_ERR_INVALID when a cover's intent is not in the given
+ * set (the set was not complete).
  */
 fca_status fca_cover_edges(fca_ctx *ctx, const uint32_t *intents, uint64_t count, uint32_t *edges,
                            uint64_t capacity, uint64_t *out_edges, void *stream);
