@@ -50,6 +50,8 @@ def parse_args():
                     help="budget of the CPU oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--lattice-rows", type=int, default=0,
+                    help="extents / covers stages: only the first R intents (0: all; covers needs all)")
     ap.add_argument("--stage", choices=["enumerate", "extents", "covers"], default="enumerate",
                     help="enumerate: the intents (the default line); extents / covers: the lattice calls "
                          "on the workload's intents, timed alone")
@@ -217,7 +219,8 @@ def cpu_baseline(rows, w, budget_s: float):
 # ----------------------------------------------------------------------------- roofline helpers
 
 # The source file of each kernel a roofline is reported for.
-KERNEL_SOURCES = {"subtree_kernel": "fca_subtree.cuh", "expand_bitmap_kernel": "fca_expand.cu"}
+KERNEL_SOURCES = {"subtree_kernel": "fca_subtree.cuh", "expand_bitmap_kernel": "fca_expand.cu",
+                  "extents_kernel": "fca_lattice.cu", "covers_kernel": "fca_lattice.cu"}
 
 
 def profile_traffic(kernel: str, workload: str):
@@ -245,6 +248,20 @@ def profile_traffic(kernel: str, workload: str):
     try:
         return float(fields["traffic_bytes_per_launch"])
     except (KeyError, ValueError):
+        return None
+
+
+def profile_traffic_per_row(kernel: str, workload: str):
+    """DRAM bytes per processed row of `kernel` on `workload` from its committed ncu summary (the
+    capture's traffic over its rows), or None once the kernel source has changed."""
+    t = profile_traffic(kernel, workload)
+    if t is None:
+        return None
+    try:
+        text = open(os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")).read()
+        rows = [ln.split(":", 1)[1] for ln in text.splitlines() if ln.strip().lstrip("-* ").startswith("rows_per_launch:")]
+        return t / float(rows[0].strip().replace(",", ""))
+    except (OSError, IndexError, ValueError):
         return None
 
 
@@ -492,6 +509,8 @@ def run_lattice(args, world, rank, local):
     stream = torch.cuda.current_stream(dev)
     ctx = fca.Context(torch.from_numpy(rows.view(np.int32)).to(dev), w.n_objects, w.n_attrs)
     intents = ctx.enumerate(stream=stream)
+    if args.lattice_rows > 0 and args.stage == "extents":
+        intents = intents[: args.lattice_rows]
     k = int(intents.shape[0])
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
     if args.stage == "extents":
@@ -552,9 +571,12 @@ def run_lattice(args, world, rank, local):
         alg = k * (wm + wn) * 4 + w.n_attrs * ((wn + 3) // 4 * 4) * 4
         peak = peaks.get("hbm_gbs")
         achieved = alg / (mean_ms * 1e-3) / 1e9
+        # DRAM bytes per launch from the committed ncu summary (captured on the workload's first rows;
+        # the traffic grows with the rows, so it is scaled to this launch's rows)
+        per_row = profile_traffic_per_row("extents_kernel", w.name)
         result["roofline"] = {"kernel": "extents_kernel", "bound": "hbm", "achieved": achieved,
                               "peak": peak, "unit": "GB/s", "frac": achieved / peak if peak else None,
-                              "traffic": None, "algorithmic_bytes": alg,
+                              "traffic": per_row * k if per_row is not None else None, "algorithmic_bytes": alg,
                               "basis": "library events around the one launch; peak: measured copy bandwidth"}
     else:
         result["edges"] = n_edges
