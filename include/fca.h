@@ -175,8 +175,10 @@ fca_status fca_extents(fca_ctx *ctx, const uint32_t *intents, uint64_t count, ui
  * Uses stream-ordered device scratch (about 8 bytes per intent, plus
  * 16 W_N bytes for each warp of the kernel's grid, which is sized to the
  * warps resident on the GPU) and returns after the work on `stream`
- * completes. FCA_ERR_INVALID when a cover's intent is not in the given
- * set (the set was not complete).
+ * completes. It reads the context's table, so it must be ordered after
+ * any fca_context_load that precedes it (the same stream does that).
+ * FCA_ERR_INVALID when a cover's intent is not in the given set (the set
+ * was not complete).
  */
 fca_status fca_cover_edges(fca_ctx *ctx, const uint32_t *intents, uint64_t count, uint32_t *edges,
                            uint64_t capacity, uint64_t *out_edges, void *stream);
