@@ -11,7 +11,11 @@ textbook contexts and against a pure-Python set enumeration on tiny contexts, ne
   every edge goes from an intent to a proper superset;
 - pure-Python brute force on tiny random contexts (intents as frozensets, the cover relation by
   three nested loops);
-- planted mistakes in a copy of the cover oracle each fail one of the above.
+- planted mistakes in a copy of the cover oracle each fail one of the above;
+- the rule the cover kernel computes (lower covers = the maximal distinct restrictions A & {k}',
+  each with intent B plus the attributes giving the same set), restated with Python sets, equals
+  the oracle's cover relation; and the oracle's two formulations (whole relation, one concept's
+  lower covers) agree on a thousand-concept lattice.
 """
 import itertools
 
@@ -197,3 +201,45 @@ def test_planted_cover_mistakes_are_caught(mutant):
             sets[i] < sets[j] and len(sets[j]) == len(sets[i]) + 1 for i, j in e)
         caught |= not ok
     assert caught
+
+
+# ---------------------------------------------------------------- the rule the cover kernel uses
+
+def covers_by_maximal_restrictions(rows, n, m, intents):
+    """Lower covers of each concept (A, B) as the maximal distinct sets C_k = A & {k}' over k not in
+    B, each with intent B + {k2 : C_k2 = C_k}, emitted once from its smallest k (plain Python sets)."""
+    cells = cx.unpack_rows(rows, m)
+    sets = intent_sets(intents, m)
+    row_of = {s: i for i, s in enumerate(sets)}
+    out = []
+    for i, b in enumerate(sets):
+        a = frozenset(o for o in range(n) if all(cells[o][x] for x in b))
+        c = {k: frozenset(o for o in a if cells[o][k]) for k in range(m) if k not in b}
+        for k, ck in c.items():
+            dominated = any(ck < c2 for c2 in c.values())
+            first = min(k2 for k2, c2 in c.items() if c2 == ck) == k
+            if dominated or not first:
+                continue
+            d = b | {k2 for k2, c2 in c.items() if c2 == ck}
+            out.append((i, row_of[frozenset(d)]))
+    return sorted(out)
+
+
+@pytest.mark.parametrize("n,m,p,seed", [(20, 8, 0.4, 1), (40, 12, 0.3, 2), (70, 40, 0.2, 3), (15, 6, 0.6, 4)])
+def test_maximal_restrictions_give_the_covers(n, m, p, seed):
+    rows = cx.random_context(n, m, p, seed)
+    intents = oracle.cbo(rows, n, m)["intents"]
+    assert covers_by_maximal_restrictions(rows, n, m, intents) == \
+        sorted(map(tuple, lattice.cover_edges(intents, m).tolist()))
+
+
+def test_two_cover_formulations_agree_at_a_thousand_concepts():
+    rows = cx.random_context(1000, 30, 0.1, 11)
+    intents = oracle.cbo(rows, 1000, 30)["intents"]
+    e = lattice.cover_edges(intents, 30)
+    by_row = {}
+    for i, j in e.tolist():
+        by_row.setdefault(i, []).append(j)
+    rng = np.random.default_rng(2)
+    for i in rng.choice(intents.shape[0], 120, replace=False):
+        assert lattice.lower_covers_of(intents, 30, int(i)).tolist() == sorted(by_row.get(int(i), []))
