@@ -68,6 +68,8 @@ typedef struct {
     int digest_only;     /* keep no intents; accumulate an order-independent digest instead */
     int32_t words32;     /* 32-bit words of an intent (for the digest) */
     uint64_t hsum, hxor; /* sum and xor of the per-intent hashes */
+    const int32_t *label; /* digest only, optional: attribute at position r is label[r] */
+    uint64_t *relabeled; /* scratch for the renumbered intent (wm words) */
 } osink;
 
 /* splitmix64 finaliser (Steele, Lea and Flood, "Fast splittable pseudorandom number generators"). */
@@ -125,6 +127,15 @@ static void sink_emit(const octx *c, osink *s, const uint64_t *extent, const uin
 {
     if (s->oom) return;
     if (s->digest_only) {
+        if (s->label) {   /* hash the intent with its attributes renumbered */
+            memset(s->relabeled, 0, (size_t)c->wm * sizeof(uint64_t));
+            for (int32_t r = 0; r < c->m; ++r)
+                if (bit_of(intent, r)) {
+                    int32_t a = s->label[r];
+                    s->relabeled[a >> 6] |= ((uint64_t)1) << (a & 63);
+                }
+            intent = s->relabeled;
+        }
         uint64_t h = intent_hash(intent, s->words32);
         s->hsum += h;
         s->hxor ^= h;
@@ -276,9 +287,9 @@ int oracle_cbo_limited(const uint32_t *rows32, int64_t n, int32_t m, int threads
                        uint64_t *out_count, uint64_t *out_closures, uint64_t *depth_counts);
 
 static int run_cbo(const uint32_t *rows32, int64_t n, int32_t m, int threads, int want_extents,
-                   uint64_t limit, int digest_only, uint32_t **out_intents, uint32_t **out_extents,
-                   uint64_t *out_count, uint64_t *out_closures, uint64_t *depth_counts,
-                   uint64_t *hsum, uint64_t *hxor);
+                   uint64_t limit, int digest_only, const int32_t *label, uint32_t **out_intents,
+                   uint32_t **out_extents, uint64_t *out_count, uint64_t *out_closures,
+                   uint64_t *depth_counts, uint64_t *hsum, uint64_t *hxor);
 
 int oracle_cbo(const uint32_t *rows32, int64_t n, int32_t m, int threads, int want_extents,
                uint32_t **out_intents, uint32_t **out_extents, uint64_t *out_count,
@@ -292,8 +303,8 @@ int oracle_cbo_limited(const uint32_t *rows32, int64_t n, int32_t m, int threads
                        uint64_t limit, uint32_t **out_intents, uint32_t **out_extents,
                        uint64_t *out_count, uint64_t *out_closures, uint64_t *depth_counts)
 {
-    return run_cbo(rows32, n, m, threads, want_extents, limit, 0, out_intents, out_extents, out_count,
-                   out_closures, depth_counts, NULL, NULL);
+    return run_cbo(rows32, n, m, threads, want_extents, limit, 0, NULL, out_intents, out_extents,
+                   out_count, out_closures, depth_counts, NULL, NULL);
 }
 
 /*
@@ -306,14 +317,39 @@ int oracle_cbo_digest(const uint32_t *rows32, int64_t n, int32_t m, int threads,
                       uint64_t *out_closures, uint64_t *depth_counts, uint64_t *hsum, uint64_t *hxor)
 {
     if (!hsum || !hxor) return -1;
-    return run_cbo(rows32, n, m, threads, 0, 0, 1, NULL, NULL, out_count, out_closures, depth_counts,
-                   hsum, hxor);
+    return run_cbo(rows32, n, m, threads, 0, 0, 1, NULL, NULL, NULL, out_count, out_closures,
+                   depth_counts, hsum, hxor);
+}
+
+/*
+ * The digest of a table whose attributes were renumbered (columns listed in another order), taken
+ * over the intents in the original numbering: label[r] is the original number of the attribute at
+ * position r (a permutation of 0 .. m-1). The set of intents does not depend on the order in which
+ * the search takes the attributes, so the digest equals that of the original table, while the
+ * closures counted are those of the search in the given order.
+ */
+int oracle_cbo_digest_relabel(const uint32_t *rows32, int64_t n, int32_t m, int threads,
+                              const int32_t *label, uint64_t *out_count, uint64_t *out_closures,
+                              uint64_t *depth_counts, uint64_t *hsum, uint64_t *hxor)
+{
+    if (!hsum || !hxor || !label || m < 1) return -1;
+    char *seen = (char *)calloc((size_t)m, 1);
+    if (!seen) return -1;
+    int ok = 1;
+    for (int32_t r = 0; r < m; ++r) {
+        if (label[r] < 0 || label[r] >= m || seen[label[r]]) ok = 0;
+        else seen[label[r]] = 1;
+    }
+    free(seen);
+    if (!ok) return -1;
+    return run_cbo(rows32, n, m, threads, 0, 0, 1, label, NULL, NULL, out_count, out_closures,
+                   depth_counts, hsum, hxor);
 }
 
 static int run_cbo(const uint32_t *rows32, int64_t n, int32_t m, int threads, int want_extents,
-                   uint64_t limit, int digest_only, uint32_t **out_intents, uint32_t **out_extents,
-                   uint64_t *out_count, uint64_t *out_closures, uint64_t *depth_counts,
-                   uint64_t *hsum, uint64_t *hxor)
+                   uint64_t limit, int digest_only, const int32_t *label, uint32_t **out_intents,
+                   uint32_t **out_extents, uint64_t *out_count, uint64_t *out_closures,
+                   uint64_t *depth_counts, uint64_t *hsum, uint64_t *hxor)
 {
     if (!rows32 || n < 1 || m < 1 || (!digest_only && !out_intents) || !out_count || !out_closures ||
         !depth_counts)
@@ -337,6 +373,9 @@ static int run_cbo(const uint32_t *rows32, int64_t n, int32_t m, int threads, in
         wks[t].sink.digest_only = digest_only;
         wks[t].sink.words32 = (m + 31) / 32;
         wks[t].sink.depth_counts = (uint64_t *)calloc((size_t)(m + 2), sizeof(uint64_t));
+        wks[t].sink.label = label;
+        wks[t].sink.relabeled = (uint64_t *)calloc((size_t)c.wm, sizeof(uint64_t));
+        if (!wks[t].sink.depth_counts || !wks[t].sink.relabeled) wks[t].sink.oom = 1;
     }
     int rc = 0;
     if (nthr == 1) {
@@ -373,6 +412,7 @@ static int run_cbo(const uint32_t *rows32, int64_t n, int32_t m, int threads, in
     }
     int64_t w32m = (m + 31) / 32, w32n = (n + 31) / 32;
     uint32_t *oi = NULL, *oe = NULL;
+    for (int t = 0; t < nthr; ++t) free(wks[t].sink.relabeled);
     if (digest_only) {
         for (int t = 0; t < nthr; ++t) free(wks[t].sink.depth_counts);
         free(wks);

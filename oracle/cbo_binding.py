@@ -61,6 +61,9 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_cbo_digest.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int,
                                       u64p, u64p, ctypes.c_void_p, u64p, u64p]
     lib.oracle_cbo_digest.restype = ctypes.c_int
+    lib.oracle_cbo_digest_relabel.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int,
+                                              ctypes.c_void_p, u64p, u64p, ctypes.c_void_p, u64p, u64p]
+    lib.oracle_cbo_digest_relabel.restype = ctypes.c_int
     lib.oracle_free.argtypes = [ctypes.c_void_p]
     lib.oracle_free.restype = None
     return lib
@@ -112,9 +115,13 @@ def cbo(rows: np.ndarray, n_objects: int, n_attrs: int, threads: int = 1,
 
 
 def cbo_digest(rows: np.ndarray, n_objects: int, n_attrs: int, threads: int = 1,
-               lib: Optional[ctypes.CDLL] = None) -> dict:
+               lib: Optional[ctypes.CDLL] = None, label: Optional[np.ndarray] = None) -> dict:
     """The same search keeping no intents: their number, the closures, the depth counts and an
-    order-independent digest of the intent set (sum and xor mod 2^64 of one hash per intent)."""
+    order-independent digest of the intent set (sum and xor mod 2^64 of one hash per intent).
+
+    ``label`` (optional, a permutation of 0..M-1): the table's attribute at position r is attribute
+    ``label[r]`` of the original table; the digest is then taken over the intents renumbered back to
+    the original attributes (the closures stay those of the search in the given order)."""
     lib = lib or load()
     rows = np.ascontiguousarray(rows, dtype=np.uint32)
     if rows.shape != (n_objects, (n_attrs + 31) // 32):
@@ -122,9 +129,17 @@ def cbo_digest(rows: np.ndarray, n_objects: int, n_attrs: int, threads: int = 1,
     count, closures = ctypes.c_uint64(0), ctypes.c_uint64(0)
     hsum, hxor = ctypes.c_uint64(0), ctypes.c_uint64(0)
     depth = np.zeros(n_attrs + 2, dtype=np.uint64)
-    rc = lib.oracle_cbo_digest(rows.ctypes.data, n_objects, n_attrs, int(threads), ctypes.byref(count),
-                               ctypes.byref(closures), depth.ctypes.data, ctypes.byref(hsum),
-                               ctypes.byref(hxor))
+    if label is not None:
+        lab = np.ascontiguousarray(label, dtype=np.int32)
+        if lab.shape != (n_attrs,):
+            raise ValueError("label must hold one attribute number per column")
+        rc = lib.oracle_cbo_digest_relabel(rows.ctypes.data, n_objects, n_attrs, int(threads), lab.ctypes.data,
+                                           ctypes.byref(count), ctypes.byref(closures), depth.ctypes.data,
+                                           ctypes.byref(hsum), ctypes.byref(hxor))
+    else:
+        rc = lib.oracle_cbo_digest(rows.ctypes.data, n_objects, n_attrs, int(threads), ctypes.byref(count),
+                                   ctypes.byref(closures), depth.ctypes.data, ctypes.byref(hsum),
+                                   ctypes.byref(hxor))
     if rc != 0:
         raise RuntimeError("oracle_cbo_digest failed")
     return {"count": int(count.value), "closures": int(closures.value), "depth_counts": depth,

@@ -9,7 +9,9 @@ integers (last 32-bit word most significant), so that full-size GPU runs can
 be checked without re-running the oracle. It also records the closures of the
 same search over the table in ascending-support attribute order (the library's
 default processing order; the intent set is the same), with --order-closures
-alone without redoing the rest.
+alone without redoing the rest. That search also digests its intents renumbered
+back to the original attributes, which gives the multiset digest of a workload
+whose search in attribute order is too long for the host.
 
 usage: python tests/golden/make_workload_digests.py [workload ...] [--threads T] [--digest-only]
                                                     [--order-closures]
@@ -53,8 +55,8 @@ def main():
         w = cx.WORKLOADS[name]
         rows = w.rows()
         t0 = time.time()
-        go = oracle.cbo_digest(support_order(rows, w.n_objects, w.n_attrs)[0], w.n_objects, w.n_attrs,
-                               threads=args.threads)
+        prows, inv = support_order(rows, w.n_objects, w.n_attrs)
+        go = oracle.cbo_digest(prows, w.n_objects, w.n_attrs, threads=args.threads, label=inv)
         if args.order_closures:
             data = json.load(open(OUT)) if os.path.exists(OUT) else {}
             entry = data.get(name, {})
@@ -65,6 +67,11 @@ def main():
                               "concepts": go["count"], "oracle_order": "support",
                               "oracle_seconds": round(time.time() - t0, 1), "oracle_threads": args.threads})
             entry["closures_support_order"] = go["closures"]
+            hs, hx = f"{go['hsum']:016x}", f"{go['hxor']:016x}"
+            if "multiset_hsum" in entry:
+                assert (entry["multiset_hsum"], entry["multiset_hxor"]) == (hs, hx)
+            else:
+                entry.update({"multiset_hsum": hs, "multiset_hxor": hx, "digest_search_order": "support"})
             data[name] = entry
             print(name, "support order", go["count"], go["closures"], f"{time.time() - t0:.1f}s", flush=True)
             with open(OUT, "w") as f:
@@ -84,6 +91,8 @@ def main():
             "oracle_seconds": round(dt, 1), "oracle_threads": args.threads,
             "closures_support_order": go["closures"],
         })
+        # the intent set does not depend on the order of the search
+        assert (g["hsum"], g["hxor"]) == (go["hsum"], go["hxor"])
         if not args.digest_only:
             r = oracle.cbo(rows, w.n_objects, w.n_attrs, threads=args.threads)
             assert r["intents"].shape[0] == g["count"] and r["closures"] == g["closures"]

@@ -247,6 +247,33 @@ def test_digest_mode_matches_full_output(n, m, density, seed, threads):
     assert multiset_digest(changed) != (dig["hsum"], dig["hxor"])
 
 
+@pytest.mark.parametrize("n,m,density,seed,threads", [(300, 33, 0.2, 4, 2), (400, 70, 0.12, 5, 4),
+                                                      (120, 16, 0.35, 6, 1)])
+def test_relabeled_digest_is_the_original_tables_digest(n, m, density, seed, threads):
+    """The intent set does not depend on how the attributes are numbered: searching the table with
+    its columns in another order and renumbering each intent back must digest to the original
+    table's full output. The permuted search evaluates other candidates (its closures differ from
+    the original search's on these tables), so equal digests are not an artefact of equal work."""
+    from tests._util import multiset_digest
+    rows = cx.random_context(n, m, density, seed)
+    full = oracle.cbo(rows, n, m, threads=threads)
+    want = multiset_digest(full["intents"])
+    perm = np.random.default_rng(seed).permutation(m)        # position r holds attribute perm[r]
+    cells = cx.unpack_rows(rows, m)[:, perm]
+    prows = cx.pack_rows(cells)
+    got = oracle.cbo_digest(prows, n, m, threads=threads, label=perm)
+    assert got["count"] == full["intents"].shape[0]
+    assert (got["hsum"], got["hxor"]) == want
+    assert got["closures"] == oracle.cbo(prows, n, m)["closures"]
+    assert got["closures"] != full["closures"]
+    # without the renumbering, or with the inverse permutation, the digest is another set's
+    assert (oracle.cbo_digest(prows, n, m, threads=threads)["hsum"]) != want[0]
+    inverse = np.argsort(perm)
+    assert (oracle.cbo_digest(prows, n, m, threads=threads, label=inverse)["hsum"]) != want[0]
+    with pytest.raises(RuntimeError):   # a label that is not a permutation is refused
+        oracle.cbo_digest(prows, n, m, label=np.zeros(m, dtype=np.int32))
+
+
 def test_extents_are_derivations():
     rows = cx.random_context(70, 40, 0.3, 9)
     r = oracle.cbo(rows, 70, 40, want_extents=True)
