@@ -1,9 +1,9 @@
 """ctypes binding of the work-counting pass in ``workcount.c`` (test and measurement infrastructure).
 
-``workcount(rows, n, m)`` returns, per tier, the algorithmic work of enumerating the context in
-32-bit words: the units and the per-unit counts that the roofline uses (see the header of
-``workcount.c``). Tier ``"list"`` holds the parents with at most 64 objects, tier ``"bitmap"`` the
-larger ones.
+``workcount(rows, n, m, mid_max=T)`` returns, per tier, the algorithmic work of enumerating the
+context in 32-bit words: the units and the per-unit counts that the roofline uses (see the header
+of ``workcount.c``). Tier ``"list"`` holds the parents with at most 64 objects, tier ``"mid"`` those
+with at most T objects (none when T <= 64), tier ``"bitmap"`` the larger ones.
 """
 from __future__ import annotations
 
@@ -21,8 +21,9 @@ _LIB_PATH = os.path.join(_HERE, "libworkcount.so")
 _lock = threading.Lock()
 _lib: Optional[ctypes.CDLL] = None
 
-FIELDS = ("parents", "closures", "children", "isect_words", "closure_words", "canon_words", "hbm_words")
-TIERS = ("list", "bitmap")
+FIELDS = ("parents", "closures", "children", "isect_words", "closure_words", "canon_words", "hbm_words",
+          "hbm_lean_words", "l2_lean_words")
+TIERS = ("list", "mid", "bitmap")
 
 
 def build(force: bool = False) -> str:
@@ -42,20 +43,23 @@ def _load() -> ctypes.CDLL:
             build()
             lib = ctypes.CDLL(_LIB_PATH)
             lib.workcount.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int,
-                                      ctypes.POINTER(ctypes.c_uint64)]
+                                      ctypes.c_int64, ctypes.c_int64, ctypes.POINTER(ctypes.c_uint64)]
             lib.workcount.restype = ctypes.c_int
             _lib = lib
     return _lib
 
 
-def workcount(rows: np.ndarray, n_objects: int, n_attrs: int, threads: int = 1) -> Dict[str, Dict[str, int]]:
-    """Per-tier work counts of enumerating ``rows`` (``N x ceil(M/32)`` uint32, LSB-first)."""
+def workcount(rows: np.ndarray, n_objects: int, n_attrs: int, threads: int = 1,
+              mid_max: int = 0, list_max: int = 0) -> Dict[str, Dict[str, int]]:
+    """Per-tier work counts of enumerating ``rows`` (``N x ceil(M/32)`` uint32, LSB-first). The lean
+    model's fields depend on ``list_max`` (largest extent kept as an id list; 0: none)."""
     rows = np.ascontiguousarray(rows, dtype=np.uint32)
-    out = (ctypes.c_uint64 * 14)()
-    st = _load().workcount(rows.ctypes.data, int(n_objects), int(n_attrs), int(threads), out)
+    out = (ctypes.c_uint64 * 27)()
+    st = _load().workcount(rows.ctypes.data, int(n_objects), int(n_attrs), int(threads), int(mid_max),
+                           int(list_max), out)
     if st != 0:
         raise RuntimeError("workcount failed")
-    return {t: {f: int(out[7 * i + k]) for k, f in enumerate(FIELDS)} for i, t in enumerate(TIERS)}
+    return {t: {f: int(out[9 * i + k]) for k, f in enumerate(FIELDS)} for i, t in enumerate(TIERS)}
 
 
 def derived(counts: Dict[str, int]) -> Dict[str, int]:

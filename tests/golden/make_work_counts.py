@@ -1,14 +1,21 @@
 """Write tests/golden/work_counts.json from the work-counting pass in oracle/ (and nothing else).
 
 For each named synthetic workload it records, per tier of parent extent (at most 64 objects:
-"list"; more: "bitmap"), the algorithmic work of the whole enumeration in 32-bit words: parents,
+"list"; at most --mid-max objects: "mid"; more: "bitmap"), the algorithmic work of the whole enumeration in 32-bit words: parents,
 closures, canonical children, extent-intersection words, closure words (the cheaper of the row and
 column routes), canonical-test words and HBM words (extent reads, frontier and output writes).
 The benchmark divides these by measured kernel time for its roofline figures. The search runs over
 the table in the library's default processing order (ascending attribute support), the order in
 which the kernels do their work; --order natural counts the attribute order instead.
 
+The mid-tier bound is the largest extent the library expands one search node per warp, and the
+list bound the largest extent it keeps as an object-id list (its statistics report them as mid_max
+and list_max: 256, and 315 / 928 / 1312 objects for the skewed / zipf / planted-bicluster tables;
+none for the two smaller ones); they are given on the command line, so that this script calls only
+oracle/. The list bound enters only the lean model's fields (hbm_lean_words, l2_lean_words).
+
 usage: python tests/golden/make_work_counts.py [workload ...] [--threads T] [--order support|natural]
+                                               [--mid-max T] [--list-max L]
 """
 import argparse
 import json
@@ -32,6 +39,8 @@ def main():
     ap.add_argument("names", nargs="*", default=["tiny", "sparse", "zipf", "skewed"])
     ap.add_argument("--threads", type=int, default=os.cpu_count() or 1)
     ap.add_argument("--order", choices=["support", "natural"], default="support")
+    ap.add_argument("--mid-max", type=int, default=0, help="largest extent of the mid tier (0: none)")
+    ap.add_argument("--list-max", type=int, default=0, help="largest extent kept as an id list (0: none)")
     args = ap.parse_args()
     for name in args.names:
         w = cx.WORKLOADS[name]
@@ -39,12 +48,15 @@ def main():
         if args.order == "support":
             rows = support_order(rows, w.n_objects, w.n_attrs)[0]
         t0 = time.time()
-        counts = workcount(rows, w.n_objects, w.n_attrs, threads=args.threads)
+        counts = workcount(rows, w.n_objects, w.n_attrs, threads=args.threads, mid_max=args.mid_max,
+                           list_max=args.list_max)
         dt = time.time() - t0
         # re-read before writing: several runs may fill in different workloads
         data = json.load(open(OUT)) if os.path.exists(OUT) else {}
         data[name] = {"n_objects": w.n_objects, "n_attrs": w.n_attrs, "seed": w.seed, "tiers": counts,
-                      "order": args.order, "seconds": round(dt, 1), "threads": args.threads}
+                      "order": args.order, "mid_max": args.mid_max, "list_max": args.list_max,
+                      "seconds": round(dt, 1),
+                      "threads": args.threads}
         with open(OUT + ".tmp", "w") as f:
             json.dump(data, f, indent=1, sort_keys=True)
             f.write("\n")
