@@ -3,9 +3,11 @@
 
 One step = one pass of the whole hot path over one synthetic context: load the
 rows into the context (row copy, padding mask, transpose to columns, top
-intent) and enumerate every intent (bitmap-tier expansion, object-list
+intent) and enumerate every intent (bitmap- and mid-tier expansion, object-list
 subtrees, compaction into the output buffer). Inputs are resident in device
-memory when the timed region starts; L2 is flushed between timed steps.
+memory when the timed region starts; L2 is flushed between timed steps. The
+default workload is the largest one that fits one GPU, the planted-bicluster
+table (100 000 x 256, 519 340 217 concepts).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -33,7 +35,7 @@ from closed_set_enumeration_gb300 import contexts as cx  # noqa: E402
 
 METRIC = "concepts/sec (closures/sec) per GB300; fraction of bitwise INT/L2 roofline"
 UNIT = "concepts/s"
-DEFAULT_WORKLOAD = "sparse"
+DEFAULT_WORKLOAD = "biclusters"
 L2_FLUSH_BYTES = 512 << 20
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 INT_LANES_PER_SM = 64        # 32-bit logical-op results per SM per clock (checked by the LOP3 probe)
@@ -42,14 +44,14 @@ INT_LANES_PER_SM = 64        # 32-bit logical-op results per SM per clock (check
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(cx.WORKLOADS))
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="budget of the CPU oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--lattice-rows", type=int, default=0,
                     help="extents / covers stages: only the first R intents (0: all; covers needs all)")
     ap.add_argument("--stage", choices=["enumerate", "extents", "covers"], default="enumerate",
@@ -210,17 +212,24 @@ class OracleSampler:
 
 
 def cpu_baseline(rows, w, budget_s: float):
+    """The oracle on all host cores (the top-level attributes split between threads) and, beside
+    it, on one thread (the single-thread form of the pages' CPU baseline), each on a bounded
+    sample of the workload."""
     threads = os.cpu_count() or 1
     rate, sample, dt = OracleSampler(rows, w, threads).sample(budget_s)
+    rate1, sample1, dt1 = OracleSampler(rows, w, 1).sample(max(1.0, budget_s / 2))
     return {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": sample,
-            "seconds": round(dt, 2)}
+            "seconds": round(dt, 2),
+            "single_thread": {"value": rate1, "unit": UNIT, "cores": 1, "sample": sample1,
+                              "seconds": round(dt1, 2)}}
 
 
 # ----------------------------------------------------------------------------- roofline helpers
 
 # The source file of each kernel a roofline is reported for.
 KERNEL_SOURCES = {"subtree_kernel": "fca_subtree.cuh", "expand_bitmap_kernel": "fca_expand.cu",
-                  "extents_kernel": "fca_lattice.cu", "covers_kernel": "fca_lattice.cu"}
+                  "expand_mid_kernel": "fca_mid.cu", "extents_kernel": "fca_lattice.cu",
+                  "covers_kernel": "fca_lattice.cu"}
 
 
 def profile_traffic(kernel: str, workload: str):
@@ -291,36 +300,65 @@ def probe_peaks():
 WORK_FILE = os.path.join(ROOT, "tests", "golden", "work_counts.json")
 
 
-def load_work_counts(workload: str, order: str):
+def load_work_counts(workload: str, order: str, mid_max: int, list_max: int):
     """Per-tier algorithmic work of a workload, written by tests/golden/make_work_counts.py, when it
-    was counted over the attribute order the library processes ("natural" or "support")."""
+    was counted over the attribute order the library processes ("natural" or "support") and with
+    the library's tier split and id-list bound."""
     try:
         entry = json.load(open(WORK_FILE))[workload]
     except (OSError, ValueError, KeyError):
         return None
-    if entry.get("order", "natural") != order:
+    if (entry.get("order", "natural") != order or int(entry.get("mid_max", 0)) != int(mid_max)
+            or int(entry.get("list_max", 0)) != int(list_max)):
         return None
     return entry.get("tiers")
 
 
-def roofline_of(workload, order, sub_ms, exp_ms, last, counted, probes, peaks, sm_count, sm_max):
-    """Roofline of the kernel with the larger device time per step.
+# the kernel of each tier: parents of at most 64 objects, of at most mid_max, and larger
+TIER_KERNELS = (("list", "subtree_kernel", "subtree_ms", "subtree_launches"),
+                ("mid", "expand_mid_kernel", "mid_ms", "mid_launches"),
+                ("bitmap", "expand_bitmap_kernel", "expand_ms", "expand_launches"))
+
+
+def bound_of(hbm_b, l2_b, ops, nl, avg_ms, hbm_peak, hbm_basis, l2_peak, int_peak, sm_count, sm_max):
+    """The slowest of HBM bytes at the measured copy bandwidth, HBM + L2 bytes at the probed L2 read
+    bandwidth and word operations at the int32 issue rate; achieved = the bound's quantity per
+    launch over the average launch time."""
+    times = {"hbm": hbm_b / (hbm_peak * 1e9), "l2": (hbm_b + l2_b) / (l2_peak * 1e9), "alu": ops / (int_peak * 1e9)}
+    bound = max(times, key=times.get)
+    if bound == "alu":
+        per_launch, unit, peak, basis = ops / nl, "Gop/s", int_peak, \
+            f"{sm_count} SMs x {INT_LANES_PER_SM} int32 lanes x {sm_max:.0f} MHz"
+    elif bound == "hbm":
+        per_launch, unit, peak, basis = hbm_b / nl, "GB/s", hbm_peak, hbm_basis
+    else:
+        per_launch, unit, peak, basis = (hbm_b + l2_b) / nl, "GB/s", l2_peak, \
+            "L2 read probe in this run (16 MiB buffer re-read)"
+    achieved = per_launch / (avg_ms * 1e-3) / 1e9
+    return {"bound": bound, "achieved": achieved, "peak": peak, "unit": unit, "frac": achieved / peak,
+            "peak_basis": basis, "per_launch": per_launch, "bound_ms": {k: v * 1e3 for k, v in times.items()}}
+
+
+def roofline_of(workload, order, kernel_ms, last, counted, probes, peaks, sm_count, sm_max):
+    """Roofline of the kernel with the largest device time per step.
 
     The numerator is the algorithmic work of that kernel's tier (parents of at most 64 objects run
-    in subtree_kernel, larger ones in expand_bitmap_kernel), counted exactly by the CPU counting
-    pass: HBM words (extent reads, frontier and output writes), L2 words (extent intersections and
-    the cheaper closure route) and word operations. The bound is the slowest of HBM bytes at the
-    measured copy bandwidth, HBM + L2 bytes at the L2 read bandwidth probed in this run, and word
-    operations at the int32 issue rate (SMs x 64 lanes x maximum SM clock). achieved / peak is the
-    bound's time over the measured kernel time. Without stored counts for the workload in the
-    library's processing order of the attributes, the kernel's own counted work (the counting
-    launch) stands in, and `basis` says so.
+    in subtree_kernel, those of at most mid_max objects in expand_mid_kernel, larger ones in
+    expand_bitmap_kernel), counted exactly by the CPU counting pass. Two models of the words moved:
+    the method's (every search node's extent an N-bit bitmap read once, every child's written) and
+    the lean one of this library's representation (extents of at most list_max objects as id lists,
+    object-list subtrees searched in place, rows gathered once per parent kept as a list). The
+    roofline reported is the lean model's, the tighter bound for these kernels; the bitmap model's
+    figures come beside it. Either bound is the slowest of HBM bytes at the measured copy bandwidth,
+    HBM + L2 bytes at the L2 read bandwidth probed in this run, and word operations at the int32
+    issue rate (SMs x 64 lanes x maximum SM clock); achieved / peak is the bound's time over the
+    measured kernel time (the union of the launches' intervals, per step). Without stored counts
+    for the workload in the library's processing order and tier split, the kernel's own counted
+    work (the counting launch) stands in for the object-list tier, and `basis` says so.
     """
-    sub = sub_ms >= exp_ms
-    kernel = "subtree_kernel" if sub else "expand_bitmap_kernel"
-    tier = "list" if sub else "bitmap"
-    kms = sub_ms if sub else exp_ms
-    nl = max(1, last["subtree_launches"] if sub else last["expand_launches"])
+    tier, kernel, _, launches_key = max(TIER_KERNELS, key=lambda t: kernel_ms[t[1]])
+    kms = kernel_ms[kernel]
+    nl = max(1, last[launches_key])
     avg_ms = kms / nl
     hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
     hbm_basis = "MEASURED_PEAKS.json hbm_gbs" if "hbm_gbs" in peaks else "fallback 6.8 TB/s"
@@ -328,31 +366,16 @@ def roofline_of(workload, order, sub_ms, exp_ms, last, counted, probes, peaks, s
     int_peak = sm_count * INT_LANES_PER_SM * sm_max * 1e6 / 1e9   # Gop/s
     out = {"kernel": kernel, "avg_launch_ms": avg_ms, "launches_per_step": nl,
            "traffic": profile_traffic(kernel, workload)}
-    work = load_work_counts(workload, order)
-    if work is not None:
+    work = load_work_counts(workload, order, last.get("mid_max", 0), last.get("list_max", 0))
+    args = (nl, avg_ms, hbm_peak, hbm_basis, l2_peak, int_peak, sm_count, sm_max)
+    if work is not None and tier in work and "hbm_lean_words" in work[tier]:
         t = work[tier]
-        hbm_b = 4.0 * t["hbm_words"]
-        l2_b = 4.0 * (t["isect_words"] + t["closure_words"])
         ops = t["isect_words"] + t["closure_words"] + t["canon_words"]
-        times = {"hbm": hbm_b / (hbm_peak * 1e9), "l2": (hbm_b + l2_b) / (l2_peak * 1e9),
-                 "alu": ops / (int_peak * 1e9)}
-        bound = max(times, key=times.get)
-        if bound == "alu":
-            per_launch, unit, peak, basis = ops / nl, "Gop/s", int_peak, \
-                f"{sm_count} SMs x {INT_LANES_PER_SM} int32 lanes x {sm_max:.0f} MHz"
-        elif bound == "hbm":
-            per_launch, unit, peak, basis = hbm_b / nl, "GB/s", hbm_peak, hbm_basis
-        else:
-            per_launch, unit, peak, basis = (hbm_b + l2_b) / nl, "GB/s", l2_peak, \
-                "L2 read probe in this run (16 MiB buffer re-read)"
-        achieved = per_launch / (avg_ms * 1e-3) / 1e9
-        out.update({"bound": bound, "achieved": achieved, "peak": peak, "unit": unit,
-                    "frac": achieved / peak, "peak_basis": basis,
-                    "per_launch": per_launch, "basis": "algorithmic work of the tier (oracle/workcount.c)",
-                    "units_per_step": {"parents": t["parents"], "closures": t["closures"],
-                                       "children": t["children"]},
-                    "bound_ms": {k: v * 1e3 for k, v in times.items()}})
-    elif sub:
+        out.update(bound_of(4.0 * t["hbm_lean_words"], 4.0 * t["l2_lean_words"], ops, *args))
+        out["basis"] = "algorithmic work of the tier, lean model (oracle/workcount.c)"
+        out["bitmap_model"] = bound_of(4.0 * t["hbm_words"], 4.0 * (t["isect_words"] + t["closure_words"]), ops, *args)
+        out["units_per_step"] = {"parents": t["parents"], "closures": t["closures"], "children": t["children"]}
+    elif tier == "list":
         per_launch = counted["subtree_word_ops"] / max(1, counted["subtree_launches"])
         achieved = per_launch / (avg_ms * 1e-3) / 1e9
         out.update({"bound": "alu", "achieved": achieved, "peak": int_peak, "unit": "Gop/s",
@@ -360,12 +383,8 @@ def roofline_of(workload, order, sub_ms, exp_ms, last, counted, probes, peaks, s
                     "peak_basis": f"{sm_count} SMs x {INT_LANES_PER_SM} int32 lanes x {sm_max:.0f} MHz",
                     "basis": "word operations counted by the kernel (counting launch)"})
     else:
-        per_launch = counted["expand_bytes"] / max(1, counted["expand_launches"])
-        achieved = per_launch / (avg_ms * 1e-3) / 1e9
-        out.update({"bound": "l2", "achieved": achieved, "peak": l2_peak, "unit": "GB/s",
-                    "frac": achieved / l2_peak, "per_launch": per_launch,
-                    "peak_basis": "L2 read probe in this run (16 MiB buffer re-read)",
-                    "basis": "bytes counted by the kernel (counting launch)"})
+        out.update({"bound": None, "achieved": None, "peak": None, "frac": None,
+                    "basis": "no stored work counts for this workload, order and tier split"})
     # the kernel's own counted work, for reference
     out["kernel_counted"] = {"subtree_word_ops": counted["subtree_word_ops"],
                              "expand_bytes": counted["expand_bytes"]}
@@ -419,7 +438,8 @@ def run_ours(args, world, rank, local):
     if sampler:
         sampler.start()
         time.sleep(0.3)
-    step_ms, sub_ms, exp_ms, launches = [], 0.0, 0.0, 0
+    step_ms, launches = [], 0
+    kernel_ms = {k: 0.0 for _, k, _, _ in TIER_KERNELS}
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     for _ in range(args.steps):
@@ -430,8 +450,8 @@ def run_ours(args, world, rank, local):
         ev1.synchronize()
         step_ms.append(ev0.elapsed_time(ev1))
         s = ctx.stats()
-        sub_ms += s["subtree_ms"]
-        exp_ms += s["expand_ms"]
+        for _, k, ms_key, _ in TIER_KERNELS:
+            kernel_ms[k] += s[ms_key]
         launches += s["launches"] + table_kernels
     torch.cuda.synchronize(dev)
     barrier(world)
@@ -468,8 +488,8 @@ def run_ours(args, world, rank, local):
     sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
     sm_max = float(peaks.get("sm_max_mhz", 2070.0))
     steps = args.steps
-    roofline = roofline_of(w.name, attr_order, sub_ms / steps, exp_ms / steps, last, counted, probes, peaks,
-                           sm_count, sm_max)
+    per_step = {k: v / steps for k, v in kernel_ms.items()}
+    roofline = roofline_of(w.name, attr_order, per_step, last, counted, probes, peaks, sm_count, sm_max)
 
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": steps,
@@ -484,7 +504,9 @@ def run_ours(args, world, rank, local):
         "e2e": {"value": concepts * e2e_steps * world / e2e_s, "unit": UNIT,
                 "h2d_bytes_per_step": int(rows.nbytes), "d2h_bytes_per_step": int(concepts * wm * 4)},
         "gpu_launches": launches,
-        "kernel_ms_per_step": {"subtree_kernel": sub_ms / steps, "expand_bitmap_kernel": exp_ms / steps},
+        "kernel_ms_per_step": per_step,
+        "tiers": {"list_max": last["list_max"], "mid_max": last["mid_max"],
+                  "large_parents": last["large_parents"], "small_roots": last["small_roots"]},
         "roofline": roofline,
         "clocks": clocks,
         "probes": probes,

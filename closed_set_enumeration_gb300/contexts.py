@@ -17,7 +17,7 @@ software-configuration context of 1,920 x 96), which are not available.
 from __future__ import annotations
 
 from dataclasses import dataclass
-from typing import Callable, Dict
+from typing import Callable, Dict, Tuple
 
 import numpy as np
 
@@ -106,17 +106,23 @@ def _zipf() -> np.ndarray:
     return bernoulli_cells(50000, 400, zipf_profile(400, 1.1, 0.02), rng)
 
 
-def _biclusters() -> np.ndarray:
-    rng = np.random.default_rng(4)
-    n, m = 100000, 256
-    cells = bernoulli_cells(n, m, np.full(m, 0.01), rng)
-    for _ in range(40):
-        no = int(rng.integers(500, 5001))
-        na = int(rng.integers(6, 21))
+def planted_cells(n: int, m: int, p: float, blocks: int, objects: Tuple[int, int], attrs: Tuple[int, int],
+                  rng: np.random.Generator) -> np.ndarray:
+    """Bernoulli(p) background, then `blocks` all-ones blocks set in order: for each, a number of
+    objects drawn from [objects[0], objects[1]] and of attributes from [attrs[0], attrs[1]], then
+    that many distinct objects and attributes (blocks may overlap)."""
+    cells = bernoulli_cells(n, m, np.full(m, p), rng)
+    for _ in range(blocks):
+        no = int(rng.integers(objects[0], objects[1] + 1))
+        na = int(rng.integers(attrs[0], attrs[1] + 1))
         objs = rng.choice(n, no, replace=False)
-        attrs = rng.choice(m, na, replace=False)
-        cells[np.ix_(objs, attrs)] = True
+        cols = rng.choice(m, na, replace=False)
+        cells[np.ix_(objs, cols)] = True
     return cells
+
+
+def _biclusters() -> np.ndarray:
+    return planted_cells(100000, 256, 0.01, 40, (500, 5000), (6, 20), np.random.default_rng(4))
 
 
 WORKLOADS: Dict[str, Workload] = {
@@ -138,6 +144,13 @@ def random_context(n: int, m: int, density: float, seed: int) -> np.ndarray:
     """Packed rows of an i.i.d. Bernoulli(density) context (test helper)."""
     rng = np.random.default_rng(seed)
     return pack_rows(bernoulli_cells(n, m, np.full(m, density), rng))
+
+
+def planted_context(n: int, m: int, p: float, blocks: int, objects: Tuple[int, int], attrs: Tuple[int, int],
+                    seed: int) -> np.ndarray:
+    """Packed rows of a small planted-block context (test helper; the recipe of the planted-bicluster
+    workload at other sizes)."""
+    return pack_rows(planted_cells(n, m, p, blocks, objects, attrs, np.random.default_rng(seed)))
 
 
 def contranominal(n: int) -> np.ndarray:

@@ -20,6 +20,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <string>
+#include <utility>
 #include <vector>
 
 #include "fca.h"
@@ -53,8 +54,10 @@ struct fca_ctx {
     uint32_t *botext = nullptr;    // wn: objects holding every attribute (the bottom extent)
 
     // work pools, allocated on first use, grown on demand and kept for later calls
-    std::vector<Level> levels;
-    std::vector<uint64_t> level_count;
+    std::vector<Level> levels;        // per level: the big pool (slots of W_Np words)
+    std::vector<Level> mids;          // per level: the mid pool (slots of mid_stride words; cap 0 when
+                                      // there is no mid tier)
+    std::vector<uint64_t> level_count, mid_count;   // entries waiting in each pool
     Queue q[NQ]{};
     // roots spilled by object-list searches that ran past their time budget, per queue width; two
     // sets, used in turn by the rounds that search them (spill_rounds)
@@ -67,7 +70,8 @@ struct fca_ctx {
     ChainSlots *chain_host = nullptr;   // pinned host copy
     // parents per bitmap level in the last call and its number of levels: they set how many levels
     // are launched as one chain, and the launch shapes of the chained launches
-    std::vector<uint64_t> prev_counts, cur_counts;
+    std::vector<uint64_t> prev_counts, cur_counts;   // big-pool parents per level
+    std::vector<uint64_t> prev_mids, cur_mids;       // mid-pool parents per level
     uint64_t prev_levels = 0;
     uint64_t prev_q[NQ]{}, last_q[NQ]{};   // roots of the last object-list launches (last call, this one)
 
@@ -78,6 +82,13 @@ struct fca_ctx {
     size_t pool_limit = 0;          // growth stops here; levels are then split into chunks
     uint64_t level_bytes = 0, queue_entries = 0;   // initial pool sizes
     int count_work = 0;
+    // extents of SMALL_MAX < n <= list_max objects are stored as object-id lists; those of at most
+    // mid_max objects are kept in the mid pools (slots of mid_stride words) and expanded one per warp
+    // by the mid-tier kernel (0: off)
+    int list_max = 0, mid_max = 0;
+    int64_t mid_stride = 0;
+    uint64_t mid_min = 0;           // smallest mid-pool launch given to the mid-tier kernel
+    uint64_t wait_ns = 0;           // bound of a work-sharing wait (0: the kernels' default)
     uint64_t table_launches = 0;    // kernels launched by the last table load
 
     // a second stream for the object-list launch that runs beside the other one
@@ -88,7 +99,7 @@ struct fca_ctx {
 
     // device timing of kernel launches: event pairs recorded around each launch
     std::vector<cudaEvent_t> events;
-    std::vector<int> event_kind;    // per pair: 0 = expand, 1 = subtree
+    std::vector<int> event_kind;    // per pair: 0 = bitmap-tier expand, 1 = subtree, 2 = mid-tier expand
     size_t pairs_used = 0;
 
     fca_stats stats{};
@@ -148,11 +159,17 @@ fca_status alloc_raw(fca_ctx *c, void **p, size_t bytes, const char *what)
 }
 
 uint64_t level_entry_bytes(const Dims &d) { return ((uint64_t)d.wnp + d.wm + 2) * 4; }
+uint64_t mid_entry_bytes(const fca_ctx *c) { return ((uint64_t)c->mid_stride + c->d.wm + 2) * 4; }
 uint64_t queue_entry_bytes(const Dims &d, int qi) { return ((uint64_t)(32 << qi) + d.wm + 2) * 4; }
 
 uint64_t initial_level_cap(const fca_ctx *c)
 {
     return std::max<uint64_t>(4 * (uint64_t)c->d.m, c->level_bytes / level_entry_bytes(c->d));
+}
+
+uint64_t initial_mid_cap(const fca_ctx *c)
+{
+    return std::max<uint64_t>(4 * (uint64_t)c->d.m, c->level_bytes / mid_entry_bytes(c));
 }
 
 uint64_t initial_queue_cap(const fca_ctx *c) { return std::max<uint64_t>(4 * (uint64_t)c->d.m, c->queue_entries); }
@@ -178,21 +195,25 @@ void free_queue(Queue &Q)
 void free_pools(fca_ctx *c)
 {
     for (Level &L : c->levels) free_level(L);
+    for (Level &L : c->mids) free_level(L);
     c->levels.clear();
+    c->mids.clear();
     c->level_count.clear();
+    c->mid_count.clear();
     for (Queue &Q : c->q) free_queue(Q);
     for (int k = 0; k < 2; ++k)
         for (Queue &Q : c->spq[k]) free_queue(Q);
     c->pool_bytes = 0;
 }
 
-fca_status make_level(fca_ctx *c, Level *L, uint64_t cap)
+fca_status make_level(fca_ctx *c, Level *L, uint64_t cap, int64_t stride)
 {
     const Dims &d = c->d;
     Level n{};
     n.cap = cap;
+    n.stride = stride;
     fca_status s;
-    if ((s = alloc_raw(c, (void **)&n.ext, cap * d.wnp * 4, "frontier extents")) != FCA_OK ||
+    if ((s = alloc_raw(c, (void **)&n.ext, cap * stride * 4, "frontier extents")) != FCA_OK ||
         (s = alloc_raw(c, (void **)&n.itt, cap * d.wm * 4, "frontier intents")) != FCA_OK ||
         (s = alloc_raw(c, (void **)&n.y, cap * 4, "frontier cursors")) != FCA_OK ||
         (s = alloc_raw(c, (void **)&n.n, cap * 4, "frontier sizes")) != FCA_OK) {
@@ -224,12 +245,22 @@ fca_status ensure_level(fca_ctx *c, size_t idx)
 {
     while (c->levels.size() <= idx) {
         const uint64_t cap = initial_level_cap(c);
-        Level L{};
-        fca_status s = make_level(c, &L, cap);
+        Level L{}, M{};
+        fca_status s = make_level(c, &L, cap, c->d.wnp);
         if (s != FCA_OK) return s;
         c->pool_bytes += cap * level_entry_bytes(c->d);
+        if (c->mid_max > SMALL_MAX) {
+            const uint64_t mcap = initial_mid_cap(c);
+            if ((s = make_level(c, &M, mcap, c->mid_stride)) != FCA_OK) {
+                free_level(L);
+                return s;
+            }
+            c->pool_bytes += mcap * mid_entry_bytes(c);
+        }
         c->levels.push_back(L);
+        c->mids.push_back(M);
         c->level_count.push_back(0);
+        c->mid_count.push_back(0);
     }
     return FCA_OK;
 }
@@ -252,20 +283,20 @@ fca_status ensure_queues(fca_ctx *c)
     return FCA_OK;
 }
 
-// Grow level `idx` to hold at least `need` entries, keeping its current entries. Returns
-// FCA_ERR_CAPACITY (nothing changed) when that would pass the pool limit.
-fca_status grow_level(fca_ctx *c, size_t idx, uint64_t need, cudaStream_t st)
+// Grow a pool of level `idx` (the mid pool when `mid`) to hold at least `need` entries, keeping its
+// current entries. Returns FCA_ERR_CAPACITY (nothing changed) when that would pass the pool limit.
+fca_status grow_level(fca_ctx *c, size_t idx, bool mid, uint64_t need, cudaStream_t st)
 {
-    Level &L = c->levels[idx];
+    Level &L = mid ? c->mids[idx] : c->levels[idx];
     const uint64_t cap = std::max<uint64_t>(2 * L.cap, need + need / 4);
-    const uint64_t eb = level_entry_bytes(c->d);
+    const uint64_t eb = mid ? mid_entry_bytes(c) : level_entry_bytes(c->d);
     if (c->pool_bytes + (cap - L.cap) * eb > c->pool_limit) return FCA_ERR_CAPACITY;
     Level n{};
-    fca_status s = make_level(c, &n, cap);
+    fca_status s = make_level(c, &n, cap, L.stride);
     if (s != FCA_OK) return s;
-    const uint64_t cnt = c->level_count[idx];
+    const uint64_t cnt = mid ? c->mid_count[idx] : c->level_count[idx];
     const Dims &d = c->d;
-    CK(cudaMemcpyAsync(n.ext, L.ext, cnt * d.wnp * 4, cudaMemcpyDeviceToDevice, st), "level grow");
+    CK(cudaMemcpyAsync(n.ext, L.ext, cnt * L.stride * 4, cudaMemcpyDeviceToDevice, st), "level grow");
     CK(cudaMemcpyAsync(n.itt, L.itt, cnt * d.wm * 4, cudaMemcpyDeviceToDevice, st), "level grow");
     CK(cudaMemcpyAsync(n.y, L.y, cnt * 4, cudaMemcpyDeviceToDevice, st), "level grow");
     CK(cudaMemcpyAsync(n.n, L.n, cnt * 4, cudaMemcpyDeviceToDevice, st), "level grow");
@@ -335,18 +366,41 @@ fca_status time_end(Run &r, size_t pair, cudaStream_t st)
 }
 
 // The device times of the launches recorded by the last call (read when statistics are asked for,
-// so that a call does not wait on them): sums of expand and subtree launch durations in ms.
-void launch_times(const fca_ctx *c, double *expand_ms, double *subtree_ms)
+// so that a call does not wait on them), per kind of kernel in ms: the length of the union of the
+// launches' intervals, so that launches that run side by side on two streams count once.
+void launch_times(const fca_ctx *c, double *expand_ms, double *subtree_ms, double *mid_ms)
 {
-    *expand_ms = *subtree_ms = 0.0;
+    *expand_ms = *subtree_ms = *mid_ms = 0.0;
+    if (c->pairs_used == 0) return;
+    std::vector<std::pair<float, float>> iv[3];
     for (size_t i = 0; i < c->pairs_used; ++i) {
-        float ms = 0.f;
-        if (cudaEventElapsedTime(&ms, c->events[2 * i], c->events[2 * i + 1]) != cudaSuccess) {
+        float t0 = 0.f, t1 = 0.f;
+        if (cudaEventElapsedTime(&t0, c->events[0], c->events[2 * i]) != cudaSuccess ||
+            cudaEventElapsedTime(&t1, c->events[0], c->events[2 * i + 1]) != cudaSuccess) {
             cudaGetLastError();
             continue;
         }
-        if (c->event_kind[i] == 0) *expand_ms += ms;
-        else *subtree_ms += ms;
+        const int k = c->event_kind[i];
+        if (k >= 0 && k < 3) iv[k].emplace_back(t0, t1);
+    }
+    double *dst[3] = {expand_ms, subtree_ms, mid_ms};
+    for (int k = 0; k < 3; ++k) {
+        std::sort(iv[k].begin(), iv[k].end());
+        double total = 0.0;
+        float lo = 0.f, hi = 0.f;
+        bool open = false;
+        for (const auto &v : iv[k]) {
+            if (open && v.first <= hi) {
+                hi = std::max(hi, v.second);
+                continue;
+            }
+            if (open) total += hi - lo;
+            lo = v.first;
+            hi = v.second;
+            open = true;
+        }
+        if (open) total += hi - lo;
+        *dst[k] = total;
     }
 }
 
@@ -383,6 +437,7 @@ fca_status run_subtree(Run &r, int qi, cudaStream_t st, bool share = true, bool 
     a.count_work = c->count_work;
     a.share = share ? 1 : 0;
     a.budget = SEARCH_BUDGET_CYCLES;
+    a.wait_ns = c->wait_ns;
     a.spill = c->spq[0][qi];
     size_t pair = 0;
     if ((s = time_begin(r, 1, &pair, st)) != FCA_OK) return s;
@@ -404,16 +459,93 @@ fca_status run_subtree(Run &r, int qi, cudaStream_t st, bool share = true, bool 
     return FCA_OK;
 }
 
-void count_level(fca_ctx *c, size_t lv, uint64_t k)
+void count_level(fca_ctx *c, size_t lv, uint64_t kb, uint64_t km)
 {
     if (c->cur_counts.size() <= lv) c->cur_counts.resize(lv + 1, 0);
-    c->cur_counts[lv] += k;
-    c->stats.large_parents += k;
+    if (c->cur_mids.size() <= lv) c->cur_mids.resize(lv + 1, 0);
+    c->cur_counts[lv] += kb;
+    c->cur_mids[lv] += km;
+    c->stats.large_parents += kb + km;
     c->stats.levels = std::max<uint64_t>(c->stats.levels, lv + 2);
 }
 
+fca_status drain(Run &r, size_t lv, bool chain = true);
+
+// Mid-pool parents per SM below which a level's mid pool is expanded by the block-wide kernel
+// instead (it reads id lists as well): with fewer parents than about twice the warps the mid-tier
+// kernel keeps resident, a launch lasts as long as its slowest parent searched by a single warp,
+// while a block of 8 to 16 warps takes one parent's candidates together. Measured on zipf, whose mid
+// levels hold at most 3 769 parents: 0.90 ms of mid-tier launches per enumeration against ... with
+// blocks. FCA_MID_MIN (parents) in the environment replaces the bound (1: every mid level).
+constexpr uint64_t MID_MIN_PARENTS_PER_SM = 32;
+
+// Launch one level (or a chunk of it): mid-pool parents [bm, bm + km) and big-pool parents
+// [bb, bb + kb), both writing into level lv + 1 and the object-list queues. The mid pool goes to the
+// mid-tier kernel (one parent per warp) when it holds enough parents to fill the GPU, else to the
+// block-wide kernel like the big pool. With `chain_i` >= 1 the parent counts are read on the device
+// (the launch is queued behind the one that produces its level: km and kb are then the last call's
+// counts, used for the launch shapes; a kernel without parents returns at once). Each kernel is
+// timed by its own pair of events.
+fca_status launch_level(Run &r, size_t lv, uint64_t bb, uint64_t kb, uint64_t bm, uint64_t km, int chain_i)
+{
+    fca_ctx *c = r.c;
+    fca_status s;
+    size_t pair = 0;
+    ExpandArgs a{};
+    a.d = c->d;
+    a.rows = c->rows;
+    a.cols = c->cols;
+    a.next = c->levels[lv + 1];
+    a.next_mid = c->mids[lv + 1];
+    for (int qi = 0; qi < NQ; ++qi) a.q[qi] = c->q[qi];
+    a.out = r.out;
+    a.capacity = r.capacity;
+    a.ctr = c->ctr;
+    a.count_work = c->count_work;
+    a.list_max = c->list_max;
+    a.mid_max = c->mid_max;
+    const bool on_device = chain_i >= 1;
+    const bool has_mid = c->mid_max > SMALL_MAX && (km > 0 || on_device);
+    const bool warps = has_mid && km >= c->mid_min;
+    if (warps) {
+        ExpandArgs m = a;
+        m.in = c->mids[lv];
+        m.p_begin = bm;
+        m.p_count = std::max<uint64_t>(1, km);
+        m.p_count_dev = on_device ? &c->chain->pcount_mid : nullptr;
+        if ((s = time_begin(r, 2, &pair, r.st)) != FCA_OK) return s;
+        CK((cudaError_t)launch_expand_mid(m, c->sm_count, r.st), "mid kernel launch");
+        if ((s = time_end(r, pair, r.st)) != FCA_OK) return s;
+        c->stats.launches++;
+        c->stats.mid_launches++;
+    } else if (has_mid) {
+        // a small mid pool goes to the block-wide kernel, in the big pool's launch
+        a.in2 = c->mids[lv];
+        a.p_begin2 = bm;
+        a.p_count2 = km;
+        a.p_count2_dev = on_device ? &c->chain->pcount_mid : nullptr;
+    }
+    if (kb > 0 || on_device || (has_mid && !warps)) {
+        a.in = c->levels[lv];
+        a.p_begin = bb;
+        a.p_count = kb;
+        a.p_count_dev = on_device ? &c->chain->pcount : nullptr;
+        if ((s = time_begin(r, 0, &pair, r.st)) != FCA_OK) return s;
+        CK((cudaError_t)launch_expand(a, c->sm_count, r.st), "expand kernel launch");
+        if ((s = time_end(r, pair, r.st)) != FCA_OK) return s;
+        c->stats.launches++;
+        c->stats.expand_launches++;
+    }
+    return FCA_OK;
+}
+
+bool level_empty(const fca_ctx *c, size_t lv)
+{
+    return lv >= c->levels.size() || (c->level_count[lv] == 0 && c->mid_count[lv] == 0);
+}
+
 // Launch levels lv .. lv+K-1 (level lv whole, the next level empty) back to back, each reading its
-// parent count on the device, and read the counters once at the end. Launches up to the first that
+// parent counts on the device, and read the counters once at the end. Launches up to the first that
 // overflowed are committed; that one's counters as they were before it are restored and *failed
 // is set. *next_lv is the first level still holding parents.
 fca_status enqueue_chain(Run &r, size_t lv, int K)
@@ -422,30 +554,15 @@ fca_status enqueue_chain(Run &r, size_t lv, int K)
     fca_status s;
     for (int i = 0; i < K; ++i)
         if ((s = ensure_level(c, lv + i + 1)) != FCA_OK) return s;
-    const uint64_t n0 = c->level_count[lv];
+    const uint64_t n0 = c->level_count[lv], m0 = c->mid_count[lv];
     for (int i = 0; i < K; ++i) {
         const size_t L = lv + i;
-        CK((cudaError_t)launch_prepare_chain(c->ctr, c->chain, i, n0, r.st), "chain set-up kernel");
-        ExpandArgs a{};
-        a.d = c->d;
-        a.rows = c->rows;
-        a.cols = c->cols;
-        a.in = c->levels[L];
-        a.p_begin = 0;
-        a.p_count = i == 0 ? n0 : (L < c->prev_counts.size() ? std::max<uint64_t>(1, c->prev_counts[L]) : n0);
-        a.p_count_dev = i == 0 ? nullptr : &c->chain->pcount;
-        a.next = c->levels[L + 1];
-        for (int qi = 0; qi < NQ; ++qi) a.q[qi] = c->q[qi];
-        a.out = r.out;
-        a.capacity = r.capacity;
-        a.ctr = c->ctr;
-        a.count_work = c->count_work;
-        size_t pair = 0;
-        if ((s = time_begin(r, 0, &pair, r.st)) != FCA_OK) return s;
-        CK((cudaError_t)launch_expand(a, c->sm_count, r.st), "expand kernel launch");
-        if ((s = time_end(r, pair, r.st)) != FCA_OK) return s;
-        c->stats.launches += 2;
-        c->stats.expand_launches++;
+        CK((cudaError_t)launch_prepare_chain(c->ctr, c->chain, i, n0, m0, r.st), "chain set-up kernel");
+        c->stats.launches++;
+        // launch shapes of the device-counted launches: the last call's counts of the level
+        const uint64_t eb = i == 0 ? n0 : (L < c->prev_counts.size() ? c->prev_counts[L] : n0);
+        const uint64_t em = i == 0 ? m0 : (L < c->prev_mids.size() ? c->prev_mids[L] : m0);
+        if ((s = launch_level(r, L, 0, eb, 0, em, i)) != FCA_OK) return s;
     }
     return FCA_OK;
 }
@@ -465,13 +582,15 @@ fca_status collect_chain(Run &r, size_t lv, int K, size_t *next_lv, bool *failed
         if ((i + 1 < K ? cs.snaps[i + 1].error : fin.error) != 0u) f = i;
     const int ok = f < 0 ? K : f;
     for (int i = 0; i < ok; ++i) {
-        count_level(c, lv + i, cs.counts[i]);
-        const uint64_t produced = i + 1 < K ? cs.counts[i + 1] : fin.next_count;
+        count_level(c, lv + i, cs.counts[i], cs.mcounts[i]);
+        const uint64_t produced = i + 1 < K ? cs.counts[i + 1] + cs.mcounts[i + 1] : fin.next_count + fin.next_mid;
         c->stats.max_frontier = std::max<uint64_t>(c->stats.max_frontier, produced);
         c->level_count[lv + i] = 0;
+        c->mid_count[lv + i] = 0;
     }
     if (f < 0) {
         c->level_count[lv + K] = fin.next_count;
+        c->mid_count[lv + K] = fin.next_mid;
         for (int qi = 0; qi < NQ; ++qi) c->q_count[qi] = fin.q_count[qi];
         *next_lv = lv + K;
         *failed = false;
@@ -482,7 +601,9 @@ fca_status collect_chain(Run &r, size_t lv, int K, size_t *next_lv, bool *failed
     CK(cudaMemcpyAsync(c->ctr, &c->chain->snaps[f], sizeof(Counters), cudaMemcpyDeviceToDevice, r.st),
        "counter restore");
     c->level_count[lv + f] = cs.counts[f];
+    c->mid_count[lv + f] = cs.mcounts[f];
     c->level_count[lv + f + 1] = 0;
+    c->mid_count[lv + f + 1] = 0;
     for (int qi = 0; qi < NQ; ++qi) c->q_count[qi] = cs.snaps[f].q_count[qi];
     c->stats.retries++;
     *next_lv = lv + f;
@@ -497,53 +618,56 @@ fca_status drain_chain(Run &r, size_t lv, int K, size_t *next_lv, bool *failed)
     return collect_chain(r, lv, K, next_lv, failed);
 }
 
-// Expand every entry of bitmap level `lv`, depth first. With `chain`, a whole level whose next
+// Make room in pool `mid` of level lv + 1 for what a rolled-back launch wanted to append (`after`
+// its counters): grow it, or past the pool limit empty the level (drain it depth first) and grow it
+// only if the launch alone needs more. Sets *limited when even that is not possible (the caller
+// then expands smaller chunks).
+fca_status make_room(Run &r, size_t lv, bool mid, const Counters &after, bool *limited)
+{
+    fca_ctx *c = r.c;
+    const uint64_t wanted = mid ? after.next_mid : after.next_count;
+    const uint64_t need = wanted - (mid ? c->mid_count[lv + 1] : c->level_count[lv + 1]);
+    fca_status s = grow_level(c, lv + 1, mid, wanted, r.st);
+    if (s == FCA_OK) return FCA_OK;
+    if (s != FCA_ERR_CAPACITY) return s;
+    if ((s = drain(r, lv + 1)) != FCA_OK) return s;
+    if (need > (mid ? c->mids[lv + 1].cap : c->levels[lv + 1].cap)) {
+        s = grow_level(c, lv + 1, mid, need, r.st);
+        if (s == FCA_ERR_CAPACITY) *limited = true;
+        else if (s != FCA_OK) return s;
+    }
+    return FCA_OK;
+}
+
+// Expand every entry of level `lv` (both pools), depth first. With `chain`, a whole level whose next
 // level is empty starts a chain of launches as deep as the last call's search (drain_chain).
-fca_status drain(Run &r, size_t lv, bool chain = true)
+fca_status drain(Run &r, size_t lv, bool chain)
 {
     fca_ctx *c = r.c;
     fca_status s;
-    if (chain && c->level_count[lv] > 0 && (lv + 1 >= c->levels.size() || c->level_count[lv + 1] == 0) &&
-        c->prev_levels > lv + 2) {
+    if (chain && !level_empty(c, lv) && level_empty(c, lv + 1) && c->prev_levels > lv + 2) {
         const int K = (int)std::min<uint64_t>(CHAIN_MAX, c->prev_levels - 1 - lv);
         size_t next = lv;
         bool failed = false;
         if ((s = drain_chain(r, lv, K, &next, &failed)) != FCA_OK) return s;
         if (failed) return drain(r, next, false);
-        if (next < c->levels.size() && c->level_count[next] > 0) return drain(r, next);
+        if (!level_empty(c, next)) return drain(r, next, true);
         return FCA_OK;
     }
-    uint64_t kmax = ~(uint64_t)0;    // chunk limit, lowered only when the pools may not grow
-    while (c->level_count[lv] > 0) {
+    uint64_t kmax = ~(uint64_t)0;    // chunk limit per pool, lowered only when the pools may not grow
+    while (!level_empty(c, lv)) {
         if ((s = ensure_level(c, lv + 1)) != FCA_OK) return s;
-        const uint64_t have = c->level_count[lv];
-        const uint64_t k = std::min(have, kmax);
-        const uint64_t begin = have - k;
+        const uint64_t hb = c->level_count[lv], hm = c->mid_count[lv];
+        const uint64_t kb = std::min(hb, kmax), km = std::min(hm, kmax);
+        const uint64_t bb = hb - kb, bm = hm - km;
 
-        // the next level appends after its current fill; the counters as they are then are kept on
+        // the next level appends after its current fills; the counters as they are then are kept on
         // the device, to be restored if the launch has to be rolled back (one small kernel)
-        CK((cudaError_t)launch_prepare_expand(c->ctr, c->ctr_snap, c->level_count[lv + 1], r.st),
+        CK((cudaError_t)launch_prepare_expand(c->ctr, c->ctr_snap, c->level_count[lv + 1], c->mid_count[lv + 1],
+                                              r.st),
            "counter set-up kernel");
-
-        ExpandArgs a{};
-        a.d = c->d;
-        a.rows = c->rows;
-        a.cols = c->cols;
-        a.in = c->levels[lv];
-        a.p_begin = begin;
-        a.p_count = k;
-        a.next = c->levels[lv + 1];
-        for (int qi = 0; qi < NQ; ++qi) a.q[qi] = c->q[qi];
-        a.out = r.out;
-        a.capacity = r.capacity;
-        a.ctr = c->ctr;
-        a.count_work = c->count_work;
-        size_t pair = 0;
-        if ((s = time_begin(r, 0, &pair, r.st)) != FCA_OK) return s;
-        CK((cudaError_t)launch_expand(a, c->sm_count, r.st), "expand kernel launch");
-        if ((s = time_end(r, pair, r.st)) != FCA_OK) return s;
-        c->stats.launches += 2;   // counter set-up and expand
-        c->stats.expand_launches++;
+        c->stats.launches++;
+        if ((s = launch_level(r, lv, bb, kb, bm, km, 0)) != FCA_OK) return s;
         if ((s = read_counters(r)) != FCA_OK) return s;
         const Counters after = *c->ctr_host;
 
@@ -570,35 +694,26 @@ fca_status drain(Run &r, size_t lv, bool chain = true)
                     else if (s != FCA_OK) return s;
                 }
             }
-            if (after.error & ERR_NEXT) {
-                const uint64_t need = after.next_count - c->level_count[lv + 1];
-                s = grow_level(c, lv + 1, after.next_count, r.st);
-                if (s != FCA_OK && s != FCA_ERR_CAPACITY) return s;
-                if (s == FCA_ERR_CAPACITY) {
-                    if ((s = drain(r, lv + 1)) != FCA_OK) return s;
-                    if (need > c->levels[lv + 1].cap) {
-                        s = grow_level(c, lv + 1, need, r.st);
-                        if (s == FCA_ERR_CAPACITY) limited = true;
-                        else if (s != FCA_OK) return s;
-                    }
-                }
-            }
+            if ((after.error & ERR_NEXT) && (s = make_room(r, lv, false, after, &limited)) != FCA_OK) return s;
+            if ((after.error & ERR_NEXT_MID) && (s = make_room(r, lv, true, after, &limited)) != FCA_OK) return s;
             if (limited) {
-                if (k == 1) {
+                if (kb + km <= 1) {
                     c->err = "work pools too small for one search node (raise FCA_POOL_LIMIT_BYTES)";
                     return FCA_ERR_OOM;
                 }
-                kmax = std::max<uint64_t>(1, k / 2);
+                kmax = std::max<uint64_t>(1, std::max(kb, km) / 2);
             }
             continue;
         }
-        c->level_count[lv] = begin;
+        c->level_count[lv] = bb;
+        c->mid_count[lv] = bm;
         c->level_count[lv + 1] = after.next_count;
+        c->mid_count[lv + 1] = after.next_mid;
         for (int qi = 0; qi < NQ; ++qi) c->q_count[qi] = after.q_count[qi];
-        count_level(c, lv, k);
-        c->stats.max_frontier = std::max<uint64_t>(c->stats.max_frontier, c->level_count[lv + 1]);
+        count_level(c, lv, kb, km);
+        c->stats.max_frontier = std::max<uint64_t>(c->stats.max_frontier, after.next_count + after.next_mid);
     }
-    if (lv + 1 < c->levels.size() && c->level_count[lv + 1] > 0) return drain(r, lv + 1);
+    if (!level_empty(c, lv + 1)) return drain(r, lv + 1, true);
     return FCA_OK;
 }
 
@@ -684,6 +799,7 @@ fca_status spill_rounds(Run &r)
             a.count_work = c->count_work;
             a.share = 1;
             a.budget = SEARCH_BUDGET_CYCLES;
+            a.wait_ns = c->wait_ns;
             a.spill = c->spq[1 - cur][qi];
             CK(cudaMemsetAsync(&c->ctr->q_head[qi], 0, sizeof(unsigned long long), r.st), "cursor reset");
             size_t pair = 0;
@@ -741,10 +857,11 @@ fca_status enumerate_impl(fca_ctx *c, uint32_t *out, uint64_t capacity, uint64_t
     fca_status s;
     c->stats = fca_stats{};
     std::fill(c->cur_counts.begin(), c->cur_counts.end(), 0);
+    std::fill(c->cur_mids.begin(), c->cur_mids.end(), 0);
     c->pairs_used = 0;
     if ((s = ensure_queues(c)) != FCA_OK) return s;
     if ((s = ensure_level(c, 0)) != FCA_OK) return s;
-    for (size_t i = 0; i < c->levels.size(); ++i) c->level_count[i] = 0;
+    for (size_t i = 0; i < c->levels.size(); ++i) c->level_count[i] = c->mid_count[i] = 0;
     for (int qi = 0; qi < NQ; ++qi) c->q_count[qi] = c->last_q[qi] = 0;
 
     Run r{c, out, capacity, st};
@@ -779,7 +896,7 @@ fca_status enumerate_impl(fca_ctx *c, uint32_t *out, uint64_t capacity, uint64_t
             c->stats.launches++;
         }
         if ((s = collect_chain(r, 0, K, &next, &failed)) != FCA_OK) return s;
-        if (!failed && (next >= c->levels.size() || c->level_count[next] == 0)) {
+        if (!failed && level_empty(c, next)) {
             finished = true;
             for (int qi = 0; qi < NQ; ++qi) {
                 c->stats.small_roots += c->ctr_host->q_count[qi];
@@ -820,6 +937,7 @@ fca_status enumerate_impl(fca_ctx *c, uint32_t *out, uint64_t capacity, uint64_t
     c->stats.expand_bytes = c->ctr_host->bytes;
     *out_count = total;
     c->prev_counts = c->cur_counts;
+    c->prev_mids = c->cur_mids;
     c->prev_levels = c->stats.levels;
     for (int qi = 0; qi < NQ; ++qi) c->prev_q[qi] = c->last_q[qi];
     return total > capacity ? FCA_ERR_CAPACITY : FCA_OK;
@@ -959,6 +1077,19 @@ fca_status fca_context_create(const uint32_t *rows, int64_t n_objects, int32_t n
     c->level_bytes = env_u64("FCA_LEVEL_BYTES", 64ull << 20);
     c->queue_entries = env_u64("FCA_QUEUE_ENTRIES", 1ull << 18);
     c->pool_limit = (size_t)env_u64("FCA_POOL_LIMIT_BYTES", free_b / 2);
+    c->wait_ns = env_u64("FCA_WAIT_LIMIT_NS", 0);
+    // id lists and the mid tier (FCA_LIST_MAX=0 stores every level entry as a bitmap; FCA_MID_MAX=0
+    // leaves the id-list entries to the bitmap-tier kernel)
+    c->list_max = list_max_for(c->d);
+    c->mid_max = mid_max_for(c->d);
+    {
+        const char *v = getenv("FCA_LIST_MAX");
+        if (v && v[0] == '0' && v[1] == 0) c->list_max = c->mid_max = 0;
+        v = getenv("FCA_MID_MAX");
+        if (v && v[0] == '0' && v[1] == 0) c->mid_max = 0;
+    }
+    c->mid_stride = c->mid_max > SMALL_MAX ? ((int64_t)c->mid_max + 3) & ~(int64_t)3 : 0;
+    c->mid_min = env_u64("FCA_MID_MIN", MID_MIN_PARENTS_PER_SM * (uint64_t)c->sm_count);
     *out_ctx = c;
     return FCA_OK;
 }
@@ -1017,6 +1148,9 @@ fca_status fca_set_option(fca_ctx *ctx, int option, int64_t value)
     case FCA_OPT_COUNT_WORK:
         c->count_work = value != 0;
         return FCA_OK;
+    case FCA_OPT_WAIT_LIMIT_NS:
+        c->wait_ns = (uint64_t)value;
+        return FCA_OK;
     case FCA_OPT_ATTR_ORDER:
         if (value > 2) return FCA_ERR_INVALID;
         c->attr_order = (int)value;
@@ -1042,7 +1176,9 @@ fca_status fca_get_stats(const fca_ctx *ctx, fca_stats *out)
     if (!ctx || !out) return FCA_ERR_INVALID;
     *out = ctx->stats;
     cudaSetDevice(ctx->device);
-    launch_times(ctx, &out->expand_ms, &out->subtree_ms);
+    launch_times(ctx, &out->expand_ms, &out->subtree_ms, &out->mid_ms);
+    out->list_max = ctx->list_max > SMALL_MAX ? (uint64_t)ctx->list_max : 0;
+    out->mid_max = ctx->mid_max > SMALL_MAX ? (uint64_t)ctx->mid_max : 0;
     out->lattice_ms = 0.0;
     float ms = 0.f;
     if (ctx->lat_timed) {
@@ -1165,6 +1301,13 @@ fca_status fca_cover_edges(fca_ctx *ctx, const uint32_t *intents, uint64_t count
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return cuda_fail(c, e, "cover edges");
     *out_edges = h.edges;
+    if (h.duplicates) {
+        char buf[120];
+        snprintf(buf, sizeof buf, "cover edges: %llu given intents repeat an earlier one (each must be given once)",
+                 (unsigned long long)h.duplicates);
+        c->err = buf;
+        return FCA_ERR_INVALID;
+    }
     if (h.insert_failed || h.missing) {
         char buf[160];
         snprintf(buf, sizeof buf, "cover edges: %llu cover intents missing from the given set (%llu not stored)",

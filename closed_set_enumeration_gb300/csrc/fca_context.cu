@@ -191,13 +191,16 @@ __global__ void append_bottom_kernel(const uint32_t *botext, long long wn, const
         for (int w = (int)lane; w < wm; w += 32) out[slot * wm + w] = full_mask[w];
 }
 
-// Counter set-up before a bitmap-tier launch: the next level's current fill, a zero work cursor and
+// Counter set-up before a level launch: the next level's current fills, zero work cursors and
 // error word; then a copy of the counters, restored if the launch has to be rolled back.
-__global__ void prepare_expand_kernel(Counters *ctr, Counters *snap, unsigned long long next_fill)
+__global__ void prepare_expand_kernel(Counters *ctr, Counters *snap, unsigned long long next_fill,
+                                      unsigned long long next_mid_fill)
 {
     if (threadIdx.x == 0) {
         ctr->next_count = next_fill;
+        ctr->next_mid = next_mid_fill;
         ctr->work_head = 0ull;
+        ctr->mid_head = 0ull;
         ctr->error = 0u;
     }
     __syncthreads();
@@ -206,17 +209,23 @@ __global__ void prepare_expand_kernel(Counters *ctr, Counters *snap, unsigned lo
     for (int i = (int)threadIdx.x; i < (int)(sizeof(Counters) / 4); i += (int)blockDim.x) dst[i] = src[i];
 }
 
-// Before launch i of a chain of bitmap-tier launches (see ChainSlots).
-__global__ void prepare_chain_kernel(Counters *ctr, ChainSlots *cs, int i, unsigned long long n0)
+// Before launch i of a chain of level launches (see ChainSlots).
+__global__ void prepare_chain_kernel(Counters *ctr, ChainSlots *cs, int i, unsigned long long n0,
+                                     unsigned long long n0_mid)
 {
     if (threadIdx.x == 0) {
         unsigned long long pc = i == 0 ? n0 : ctr->next_count;
+        unsigned long long pm = i == 0 ? n0_mid : ctr->next_mid;
         if (i == 0) ctr->error = 0u;
-        else if (ctr->error) pc = 0ull;     // an earlier launch of the chain overflowed: no work
+        else if (ctr->error) pc = pm = 0ull;   // an earlier launch of the chain overflowed: no work
         cs->counts[i] = pc;
+        cs->mcounts[i] = pm;
         cs->pcount = pc;
+        cs->pcount_mid = pm;
         ctr->next_count = 0ull;
+        ctr->next_mid = 0ull;
         ctr->work_head = 0ull;
+        ctr->mid_head = 0ull;
     }
     __syncthreads();
     const uint32_t *src = reinterpret_cast<const uint32_t *>(ctr);
@@ -261,15 +270,15 @@ __global__ void start_kernel(Counters *ctr, const uint32_t *top, const uint32_t 
 
 }  // namespace
 
-int launch_prepare_expand(Counters *ctr, Counters *snap, uint64_t next_fill, void *stream)
+int launch_prepare_expand(Counters *ctr, Counters *snap, uint64_t next_fill, uint64_t next_mid_fill, void *stream)
 {
-    prepare_expand_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(ctr, snap, next_fill);
+    prepare_expand_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(ctr, snap, next_fill, next_mid_fill);
     return (int)cudaGetLastError();
 }
 
-int launch_prepare_chain(Counters *ctr, ChainSlots *cs, int i, uint64_t n0, void *stream)
+int launch_prepare_chain(Counters *ctr, ChainSlots *cs, int i, uint64_t n0, uint64_t n0_mid, void *stream)
 {
-    prepare_chain_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(ctr, cs, i, n0);
+    prepare_chain_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(ctr, cs, i, n0, n0_mid);
     return (int)cudaGetLastError();
 }
 

@@ -122,12 +122,13 @@ __device__ __forceinline__ int block_exclusive_sum(int v, int *scratch, int *tot
 // decided by `subset(k)` in ascending order, so a violation below j ends the candidate early),
 // the canonical test, the intent and the child. `row_word(i, w)` is word w of the row of the i-th
 // object of C and `obj_id(i)` its object id; `write_ext(dst)` writes C as a dense bitmap for a
-// child of the next level; `all_ids()` completes the list of a small child (need < |C|).
-template <bool COUNT, class RowWord, class ObjId, class Subset, class WriteExt, class AllIds>
+// child of the next level, `write_list(dst)` as its ascending object ids (a child of at most
+// list_max objects); `all_ids()` completes the list of a small child (need < |C|).
+template <bool COUNT, class RowWord, class ObjId, class Subset, class WriteExt, class WriteList, class AllIds>
 __device__ __forceinline__ void finish_candidate(const ExpandArgs &a, const Dims &d, const uint32_t *B, int j,
                                                  unsigned cnt, unsigned need, RowWord &&row_word, ObjId &&obj_id,
-                                                 Subset &&subset, WriteExt &&write_ext, AllIds &&all_ids,
-                                                 unsigned long long &my_bytes)
+                                                 Subset &&subset, WriteExt &&write_ext, WriteList &&write_list,
+                                                 AllIds &&all_ids, unsigned long long &my_bytes)
 {
     const unsigned lane = threadIdx.x & 31;
     // AND of the rows: lanes take (object, word) pairs with the words padded to a power of two W2
@@ -173,7 +174,8 @@ __device__ __forceinline__ void finish_candidate(const ExpandArgs &a, const Dims
     if (COUNT && lane == 0) {   // the intent row and the child entry written
         my_bytes += (unsigned long long)d.wm * 4;
         my_bytes += cnt <= (unsigned)SMALL_MAX ? 4ull * queue_entry_words(cnt, d.wm)
-                                               : (unsigned long long)(4 * d.wnp + 4 * d.wm + 4);
+                    : (int)cnt <= a.list_max ? 4ull * (cnt + d.wm + 2)
+                                             : (unsigned long long)(4 * d.wnp + 4 * d.wm + 4);
     }
     // emit the intent
     unsigned long long slot = 0;
@@ -200,16 +202,21 @@ __device__ __forceinline__ void finish_candidate(const ExpandArgs &a, const Dims
         if (lane < (unsigned)d.wm) Q.itt[s * d.wm + lane] = Dw;
         if (lane == 0) { Q.y[s] = j + 1; Q.n[s] = (int)cnt; }
     } else {
+        // the next level: its mid pool (an id list of at most mid_max objects) or its big pool (an
+        // id list up to list_max objects, a bitmap above)
+        const bool mid = (int)cnt <= a.mid_max;
+        const Level &X = mid ? a.next_mid : a.next;
         unsigned long long s = 0;
-        if (lane == 0) s = atomicAdd(&a.ctr->next_count, 1ull);
+        if (lane == 0) s = atomicAdd(mid ? &a.ctr->next_mid : &a.ctr->next_count, 1ull);
         s = __shfl_sync(FULL, s, 0);
-        if (s >= a.next.cap) {
-            if (lane == 0) atomicOr(&a.ctr->error, ERR_NEXT);
+        if (s >= X.cap) {
+            if (lane == 0) atomicOr(&a.ctr->error, mid ? ERR_NEXT_MID : ERR_NEXT);
             return;
         }
-        write_ext(a.next.ext + s * (size_t)d.wnp);
-        if (lane < (unsigned)d.wm) a.next.itt[s * d.wm + lane] = Dw;
-        if (lane == 0) { a.next.y[s] = j + 1; a.next.n[s] = (int)cnt; }
+        if ((int)cnt <= a.list_max) write_list(X.ext + s * (size_t)X.stride);
+        else write_ext(X.ext + s * (size_t)X.stride);
+        if (lane < (unsigned)d.wm) X.itt[s * d.wm + lane] = Dw;
+        if (lane == 0) { X.y[s] = j + 1; X.n[s] = (int)cnt; }
     }
 }
 
@@ -223,12 +230,12 @@ __host__ __device__ inline int expand_parts(unsigned long long p_count, unsigned
 }
 
 // Bitmap tier. A work item is (parent, part of the attribute range). The block stages the parent's
-// non-zero extent chunks once. Extents of at most `a.restrict_max` objects are then turned into an
-// object list, and the rows of those objects are transposed into columns restricted to them (one
-// 32 x 32 register transpose per row word and 32 objects); each candidate's C is read from those
-// columns without any
-// global column access. Larger extents keep the chunk list: each warp gathers column j on the
-// parent's non-zero chunks. Either way the warps of the block take the part's candidates j in turn.
+// non-zero extent chunks once (an entry stored as an object-id list is read as such). Extents of at
+// most `a.restrict_max` objects are then turned into an object list, and the rows of those objects
+// are transposed into columns restricted to them (one 32 x 32 register transpose per row word and 32
+// objects); each candidate's C is read from those columns without any global column access. Larger
+// extents keep the chunk list: each warp gathers column j on the parent's non-zero chunks. Either
+// way the warps of the block take the part's candidates j in turn.
 template <bool COUNT, int WARPS>
 __global__ void __launch_bounds__(32 * WARPS, ExpandShape<WARPS>::blocks_per_sm) expand_bitmap_kernel(ExpandArgs a)
 {
@@ -249,13 +256,13 @@ __global__ void __launch_bounds__(32 * WARPS, ExpandShape<WARPS>::blocks_per_sm)
     uint32_t *rids = reinterpret_cast<uint32_t *>(smem + L.o_rids) + (size_t)wib * SMALL_MAX;
     int *blk = reinterpret_cast<int *>(smem + L.o_blk);   // [0..31] scan scratch
     const uint4 *cols4 = reinterpret_cast<const uint4 *>(a.cols);
-    const uint4 *ext4 = reinterpret_cast<const uint4 *>(a.in.ext);
 
     unsigned long long my_closures = 0, my_bytes = 0;
     unsigned loads = 0;   // uint4 loads of columns by this lane (counting only)
     // the parent count: given, or (a launch queued behind the one producing this level) read from
     // the device; then the parts per parent, as the launcher would choose them
-    const unsigned long long p_count = a.p_count_dev ? *a.p_count_dev : a.p_count;
+    const unsigned long long p_count1 = a.p_count_dev ? *a.p_count_dev : a.p_count;
+    const unsigned long long p_count = p_count1 + (a.p_count2_dev ? *a.p_count2_dev : a.p_count2);
     const int parts = a.parts > 0 ? a.parts
                                   : expand_parts(p_count, a.resident, max(1, d.m / wpb));
     const int span = (d.m + parts - 1) / parts;
@@ -269,29 +276,33 @@ __global__ void __launch_bounds__(32 * WARPS, ExpandShape<WARPS>::blocks_per_sm)
         __syncthreads();
         const unsigned long long item = next_item;
         if (item >= items) break;
-        const unsigned long long p = a.p_begin + item / (unsigned)parts;
+        const unsigned long long idx = item / (unsigned)parts;
+        const bool second = idx >= p_count1;             // a parent of the second pool
+        const Level &P = second ? a.in2 : a.in;
+        const unsigned long long p = second ? a.p_begin2 + (idx - p_count1) : a.p_begin + idx;
         const int part = (int)(item % (unsigned)parts);
-        const int y = a.in.y[p];
+        const int y = P.y[p];
         // this part's candidates; a parent small enough for restricted columns is expanded on them
         // when its candidates in the part make that cheaper than gathering (the transposition is
         // paid by every part: parts exist only when a level is too small to fill the GPU, where
         // spreading a parent's candidates over blocks shortens the launch)
-        const int np = a.in.n[p];
+        const int np = P.n[p];
         const int gw = (np + 31) >> 5;
         const int j_lo = max(y, part * span);
         const int j_hi = min(d.m, (part + 1) * span);
         if (j_lo >= j_hi) continue;                       // uniform over the block
-        const bool restricted = np <= tr && (long long)(j_hi - j_lo) * min(wq, np) >= 4ll * gw * d.wm;
+        const bool is_list = np <= a.list_max;             // the entry holds its object ids
+        const bool restricted = is_list || (np <= tr && (long long)(j_hi - j_lo) * min(wq, np) >= 4ll * gw * d.wm);
         // the parent intent, read by every candidate, in shared memory
         __shared__ uint32_t sB[MAX_ATTRS / 32];
-        if ((int)threadIdx.x < d.wm) sB[threadIdx.x] = a.in.itt[p * d.wm + threadIdx.x];
+        if ((int)threadIdx.x < d.wm) sB[threadIdx.x] = P.itt[p * d.wm + threadIdx.x];
         const uint32_t *B = sB;
 
         // ---- stage the non-zero chunks of A in order (block-wide compaction), and |A|
-        const uint4 *A4 = ext4 + p * wq;
+        const uint4 *A4 = reinterpret_cast<const uint4 *>(P.ext) + p * wq;   // a bitmap entry: big pool
         __syncthreads();
         int nnz = 0, na = 0;
-        for (int base = 0; base < wq; base += blockDim.x) {
+        for (int base = 0; base < (is_list ? 0 : wq); base += blockDim.x) {
             const int q = base + (int)threadIdx.x;
             uint4 x = make_uint4(0u, 0u, 0u, 0u);
             if (q < wq) x = A4[q];
@@ -304,10 +315,15 @@ __global__ void __launch_bounds__(32 * WARPS, ExpandShape<WARPS>::blocks_per_sm)
             na += round_na;
         }
         __syncthreads();
-        if (COUNT && threadIdx.x == 0) my_bytes += (unsigned long long)d.wnp * 4;   // the parent extent
+        if (COUNT && threadIdx.x == 0) my_bytes += is_list ? 4ull * np : (unsigned long long)d.wnp * 4;   // the parent extent
 
         if (restricted) {
             // ---- restricted path: object list, then the columns restricted to these objects
+            if (is_list) {
+                const uint32_t *src = P.ext + p * (size_t)P.stride;
+                for (int i = (int)threadIdx.x; i < np; i += blockDim.x) oid[i] = src[i];
+                na = np;
+            }
             int base_id = 0;
             for (int base = 0; base < nnz; base += blockDim.x) {
                 const int i = base + (int)threadIdx.x;
@@ -418,6 +434,29 @@ __global__ void __launch_bounds__(32 * WARPS, ExpandShape<WARPS>::blocks_per_sm)
                             }
                         }
                     },
+                    [&](uint32_t *dst) {
+                        // positions 32 g + b of C in ascending order map to ascending object ids
+                        unsigned got = 0;
+#pragma unroll
+                        for (int r = 0; r < RPL; ++r) {
+                            const unsigned pc = __popc(c[r]);
+                            unsigned incl = pc;
+#pragma unroll
+                            for (int off = 1; off < 32; off <<= 1) {
+                                const unsigned t = __shfl_up_sync(FULL, incl, off);
+                                if (lane >= (unsigned)off) incl += t;
+                            }
+                            unsigned pos = got + incl - pc;
+                            uint32_t bits = c[r];
+                            const int g = 32 * r + (int)lane;
+                            while (bits) {
+                                const int b = __ffs(bits) - 1;
+                                bits &= bits - 1u;
+                                dst[pos++] = oid[32 * g + b];
+                            }
+                            got += __shfl_sync(FULL, incl, 31);
+                        }
+                    },
                     [&]() { collect(cnt); },
                     my_bytes);
                 __syncwarp();
@@ -491,6 +530,40 @@ __global__ void __launch_bounds__(32 * WARPS, ExpandShape<WARPS>::blocks_per_sm)
                         if (x.x | x.y | x.z | x.w) dst4[aidx[i]] = x;
                     }
                 },
+                [&](uint32_t *dst) {
+                    // the ids of C in ascending order, chunk by chunk
+                    unsigned got = 0;
+                    for (int base = 0; base < nnz; base += 32) {
+                        const int i = base + (int)lane;
+                        uint4 x = make_uint4(0u, 0u, 0u, 0u);
+                        uint32_t q = 0u;
+                        if (i < nnz) {
+                            const uint4 av = aval[i];
+                            q = aidx[i];
+                            const uint4 cc = __ldg(J4 + q);
+                            x = make_uint4(av.x & cc.x, av.y & cc.y, av.z & cc.z, av.w & cc.w);
+                        }
+                        const unsigned pc = popc4(x);
+                        unsigned incl = pc;
+#pragma unroll
+                        for (int off = 1; off < 32; off <<= 1) {
+                            const unsigned t = __shfl_up_sync(FULL, incl, off);
+                            if (lane >= (unsigned)off) incl += t;
+                        }
+                        unsigned pos = got + incl - pc;
+                        const uint32_t w4[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            uint32_t bits = w4[t];
+                            while (bits) {
+                                const int b = __ffs(bits) - 1;
+                                bits &= bits - 1u;
+                                dst[pos++] = (uint32_t)((4 * q + t) * 32 + b);
+                            }
+                        }
+                        got += __shfl_sync(FULL, incl, 31);
+                    }
+                },
                 [&]() {},
                 my_bytes);
             __syncwarp();
@@ -507,6 +580,27 @@ __global__ void __launch_bounds__(32 * WARPS, ExpandShape<WARPS>::blocks_per_sm)
 
 size_t expand_smem_per_warp(const Dims &d) { return ExpandLayout(d, 1, 0).bytes; }
 
+// Largest extent whose columns a block of the WARPS shape rebuilds restricted to its objects (the
+// launcher's choice below).
+template <int WARPS>
+static int restrict_max_of(const Dims &d)
+{
+    int wpb = WARPS;
+    while (wpb > 1 && ExpandLayout(d, wpb, 0).bytes > 200 * 1024) --wpb;
+    const size_t budget = std::max<size_t>(ExpandLayout(d, wpb, 0).bytes, ExpandShape<WARPS>::smem_budget);
+    int tr = RESTRICT_CAP;
+    while (tr > 0 && ExpandLayout(d, wpb, tr).bytes > budget) tr -= 32;
+    return tr;
+}
+
+int list_max_for(const Dims &d)
+{
+    // a list is stored only where it is shorter than the bitmap (n < W_Np words) and where either
+    // block shape can take it on its restricted path
+    const long long lim = std::min<long long>(std::min(restrict_max_of<8>(d), restrict_max_of<16>(d)), d.wnp - 1);
+    return lim > SMALL_MAX ? (int)lim : 0;
+}
+
 template <bool COUNT, int WARPS>
 static int launch_expand_t(const ExpandArgs &a, int sm_count, void *stream)
 {
@@ -514,9 +608,7 @@ static int launch_expand_t(const ExpandArgs &a, int sm_count, void *stream)
     while (wpb > 1 && ExpandLayout(a.d, wpb, 0).bytes > 200 * 1024) --wpb;
     // the largest restricted extent whose columns fit in the shared memory of the shape's blocks per
     // SM (or next to the gather path's own, when that is larger)
-    const size_t budget = std::max<size_t>(ExpandLayout(a.d, wpb, 0).bytes, ExpandShape<WARPS>::smem_budget);
-    int tr = RESTRICT_CAP;
-    while (tr > 0 && ExpandLayout(a.d, wpb, tr).bytes > budget) tr -= 32;
+    const int tr = restrict_max_of<WARPS>(a.d);
     const size_t smem = ExpandLayout(a.d, wpb, tr).bytes;
     // the shared-memory attribute and the occupancy query, once per device and size (per thread)
     static thread_local ShapeCache cache;
@@ -542,11 +634,13 @@ static int launch_expand_t(const ExpandArgs &a, int sm_count, void *stream)
     b.resident = resident;
     // with the count on the device the kernel chooses the parts; the grid is sized by the count
     // the caller expects
-    b.parts = a.p_count_dev ? 0 : expand_parts(a.p_count, resident, max_parts);
-    const unsigned long long items = a.p_count * (unsigned long long)(b.parts > 0 ? b.parts : expand_parts(a.p_count, resident, max_parts));
+    const bool on_device = a.p_count_dev || a.p_count2_dev;
+    const unsigned long long pc = a.p_count + a.p_count2;   // both pools (the second one may be empty)
+    b.parts = on_device ? 0 : expand_parts(pc, resident, max_parts);
+    const unsigned long long items = pc * (unsigned long long)(b.parts > 0 ? b.parts : expand_parts(pc, resident, max_parts));
     // a launch that reads its count on the device gets the whole resident wave (blocks without work
     // leave at once)
-    unsigned long long blocks = a.p_count_dev ? resident : std::min<unsigned long long>(items, resident);
+    unsigned long long blocks = on_device ? resident : std::min<unsigned long long>(items, resident);
     if (blocks < 1) blocks = 1;
     expand_bitmap_kernel<COUNT, WARPS><<<(unsigned)blocks, wpb * 32, smem, (cudaStream_t)stream>>>(b);
     return (int)cudaGetLastError();
@@ -555,7 +649,7 @@ static int launch_expand_t(const ExpandArgs &a, int sm_count, void *stream)
 int launch_expand(const ExpandArgs &a, int sm_count, void *stream)
 {
     // wide blocks for many attributes, or for levels too small to fill the GPU with narrow blocks
-    if (a.d.m >= WIDE_EXPAND_MIN_ATTRS || a.p_count < 2ull * 3 * (unsigned long long)sm_count)
+    if (a.d.m >= WIDE_EXPAND_MIN_ATTRS || a.p_count + a.p_count2 < 2ull * 3 * (unsigned long long)sm_count)
         return a.count_work ? launch_expand_t<true, 16>(a, sm_count, stream) : launch_expand_t<false, 16>(a, sm_count, stream);
     return a.count_work ? launch_expand_t<true, 8>(a, sm_count, stream) : launch_expand_t<false, 8>(a, sm_count, stream);
 }

@@ -190,7 +190,20 @@ __global__ void __launch_bounds__(256) hash_insert_kernel(const uint32_t *__rest
         unsigned long long s = h & mask;
         bool done = false;
         for (unsigned long long probe = 0; probe <= mask; ++probe) {
-            if (atomicCAS(slots + s, EMPTY_SLOT, (uint32_t)r) == EMPTY_SLOT) {
+            const uint32_t held = atomicCAS(slots + s, EMPTY_SLOT, (uint32_t)r);
+            if (held == EMPTY_SLOT) {
+                done = true;
+                break;
+            }
+            // an occupant with the same intent: the set holds a duplicate (each intent must be given
+            // once, or a cover would resolve to either copy)
+            bool same = true;
+            for (int w = 0; w < wm && same; ++w) {
+                const uint32_t vm = valid_bits(w, wm, m);
+                same = (__ldg(intents + r * wm + w) & vm) == (__ldg(intents + (unsigned long long)held * wm + w) & vm);
+            }
+            if (same) {
+                atomicAdd(&lc->duplicates, 1ull);
                 done = true;
                 break;
             }

@@ -13,6 +13,9 @@
 // Every GPU that loads the library holds this array (STATIC_SCRATCH_WORDS words, under 10 KB)
 // until the process exits. All calls on a device share it and each call starts by rewriting it,
 // so calls whose GPU work overlaps in time (on different streams or host threads) race on it.
+// The array's device address is looked up once per device and kept: a cudaDeviceReset unloads the
+// module that holds it (and frees every context of the library on that device), so the library is
+// not to be used on a device after a reset.
 #include <cuda_runtime.h>
 
 #include <cstring>
@@ -30,9 +33,9 @@ constexpr int STATIC_MAX_WORDS = MAX_ATTRS / 32;       // intent words
 constexpr int MAX_DEVICES = 64;
 
 // Word offsets inside the scratch array.
-constexpr int OFF_CTR = 0;                                             // Counters (120 bytes)
-constexpr int OFF_FLAG = 30;                                           // some row holds every attribute
-constexpr int OFF_ROWS = 32;                                           // rows, padding cleared
+constexpr int OFF_CTR = 0;                                             // Counters (128 bytes)
+constexpr int OFF_FLAG = 32;                                           // some row holds every attribute
+constexpr int OFF_ROWS = 64;                                           // rows, padding cleared
 constexpr int OFF_IDS = OFF_ROWS + STATIC_MAX_OBJECTS * STATIC_MAX_WORDS;
 constexpr int OFF_ITT = OFF_IDS + STATIC_MAX_OBJECTS;                  // root intent = top intent
 constexpr int OFF_Y = OFF_ITT + STATIC_MAX_WORDS;                      // root cursor

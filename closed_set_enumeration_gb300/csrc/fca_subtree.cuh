@@ -195,9 +195,6 @@ constexpr int MB_EMPTY = 0, MB_WRITING = 1, MB_FULL = 2, MB_TAKING = 3;
 // Nodes a search visits before it may hand work over: short searches finish sooner than a hand-over
 // would pay for itself.
 constexpr int SHARE_AFTER = 24;
-// Longest a warp waits for a hand-over or for the block's last busy warp; past it the kernel
-// records FAULT_WAIT and the warp stops waiting.
-constexpr unsigned long long WAIT_LIMIT_NS = 30ull * 1000000000ull;
 
 __device__ __forceinline__ unsigned long long global_ns()
 {
@@ -751,6 +748,7 @@ __global__ void __launch_bounds__(256, RW > 4 ? 3 : 4) subtree_kernel(const __gr
     unsigned long long next = 0, end = 0, seen = 0;
     bool claiming = true;            // work items may be left
     unsigned long long t0 = 0;       // start of the current wait for a hand-over
+    const unsigned long long wait_ns = a.wait_ns ? a.wait_ns : DEFAULT_WAIT_NS;
     for (;;) {
         bool handed = false, share = false;
         int R = 0, n = 0, jn = 0, slice = 0;
@@ -868,14 +866,14 @@ __global__ void __launch_bounds__(256, RW > 4 ? 3 : 4) subtree_kernel(const __gr
             share = SHARE && next >= end;
         } else if constexpr (SHARE) {
             // ---- no work items left: search what busy warps of the block hand over, until none
-            //      is busy. Each wait is bounded (WAIT_LIMIT_NS); past it FAULT_WAIT is recorded
-            //      and the warp stops.
+            //      is busy. Each wait is bounded (SubtreeArgs::wait_ns); past it FAULT_WAIT is
+            //      recorded and the warp stops.
             int st = 0;   // 0: wait, 1: took a hand-over, 2: block done, 3: waited too long
             if (lane == 0) {
                 const int mb = vload(&hdr[H_MB]);
                 if (mb == MB_FULL && atomicCAS(&hdr[H_MB], MB_FULL, MB_TAKING) == MB_FULL) st = 1;
                 else if (mb == MB_EMPTY && vload(&hdr[H_BUSY]) == 0) st = 2;
-                else if (global_ns() - t0 > WAIT_LIMIT_NS) st = 3;
+                else if (global_ns() - t0 > wait_ns) st = 3;
             }
             st = __shfl_sync(FULL, st, 0);
             if (st == 2) break;

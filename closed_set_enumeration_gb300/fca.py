@@ -28,6 +28,7 @@ EXPORTS = (
 
 FCA_OPT_COUNT_WORK, FCA_OPT_LEVEL_BYTES, FCA_OPT_QUEUE_ENTRIES, FCA_OPT_POOL_LIMIT_BYTES = 1, 2, 3, 4
 FCA_OPT_ATTR_ORDER = 5
+FCA_OPT_WAIT_LIMIT_NS = 6
 
 
 class FcaStats(ctypes.Structure):
@@ -36,7 +37,11 @@ class FcaStats(ctypes.Structure):
         "max_frontier", "frontier_bytes", "expand_launches", "subtree_launches",
         "subtree_word_ops", "expand_bytes", "retries", "spill_rounds")] + [("expand_ms", ctypes.c_double),
                                                 ("subtree_ms", ctypes.c_double),
-                                                ("lattice_ms", ctypes.c_double)]
+                                                ("lattice_ms", ctypes.c_double),
+                                                ("mid_launches", ctypes.c_uint64),
+                                                ("mid_ms", ctypes.c_double),
+                                                ("list_max", ctypes.c_uint64),
+                                                ("mid_max", ctypes.c_uint64)]
 
     def as_dict(self) -> dict:
         return {name: (float(getattr(self, name)) if ty is ctypes.c_double else int(getattr(self, name)))

@@ -39,27 +39,36 @@ typedef enum {
     FCA_ERR_CUDA = 4      /* a CUDA runtime call or kernel failed; see fca_last_error */
 } fca_status;
 
-/* Statistics of the last fca_enumerate call on a context. */
+/* Statistics of the last fca_enumerate call on a context. Device times are
+ * the union of the launches' intervals per kind of kernel (launches that run
+ * side by side count once). */
 typedef struct {
     uint64_t concepts;         /* intents found (= *out_count) */
     uint64_t closures;         /* candidates (A, B, j) evaluated: j >= cursor, j not in B */
-    uint64_t large_parents;    /* search nodes expanded by the bitmap-extent kernel */
+    uint64_t large_parents;    /* search nodes of more than 64 objects (list- and bitmap-tier kernels) */
     uint64_t small_roots;      /* subtrees handed to the object-list kernels (extent <= 64) */
     uint64_t launches;         /* kernels launched by the call */
     uint64_t levels;           /* deepest bitmap-frontier level used, plus one */
     uint64_t max_frontier;     /* largest number of bitmap entries held by one level */
     uint64_t frontier_bytes;   /* device bytes held by frontier and queue buffers */
-    uint64_t expand_launches;  /* launches of the bitmap-extent kernel */
+    uint64_t expand_launches;  /* launches of the bitmap-tier kernel */
     uint64_t subtree_launches; /* launches of the object-list kernels */
     uint64_t subtree_word_ops; /* counted work of the object-list tier (FCA_OPT_COUNT_WORK) */
-    uint64_t expand_bytes;     /* counted bytes moved by the bitmap tier (FCA_OPT_COUNT_WORK) */
+    uint64_t expand_bytes;     /* counted bytes moved by the list and bitmap tiers (FCA_OPT_COUNT_WORK) */
     uint64_t retries;          /* bitmap-tier launches rolled back because a work pool was full */
     uint64_t spill_rounds;     /* launch rounds over subtrees spilled by searches past their time
                                   budget (their roots are counted in small_roots) */
-    double expand_ms;          /* device time of the bitmap-extent kernel launches */
+    double expand_ms;          /* device time of the bitmap-tier kernel launches */
     double subtree_ms;         /* device time of the object-list kernel launches */
     double lattice_ms;         /* device time of the kernels of the last fca_extents or
                                   fca_cover_edges call on the context (0 before the first) */
+    uint64_t mid_launches;     /* launches of the mid-tier kernel (search nodes of 65 to a few
+                                  hundred objects, held as object-id lists, one per warp) */
+    double mid_ms;             /* device time of the mid-tier kernel launches */
+    uint64_t list_max;         /* largest search-node extent kept as an object-id list (0: none;
+                                  fixed by N and M, or FCA_LIST_MAX=0 in the environment) */
+    uint64_t mid_max;          /* largest search-node extent expanded by the mid-tier kernel (0:
+                                  no mid tier; FCA_MID_MAX=0 turns it off) */
 } fca_stats;
 
 /* Options for fca_set_option. */
@@ -68,9 +77,11 @@ typedef enum {
     FCA_OPT_LEVEL_BYTES = 2,      /* initial bytes of one bitmap-frontier level (default 64 MiB) */
     FCA_OPT_QUEUE_ENTRIES = 3,    /* initial entries of each object-list queue (default 2^18) */
     FCA_OPT_POOL_LIMIT_BYTES = 4, /* growth limit of all work pools (default: half the free memory) */
-    FCA_OPT_ATTR_ORDER = 5        /* processing order of the attributes: 0 attribute order,
+    FCA_OPT_ATTR_ORDER = 5,       /* processing order of the attributes: 0 attribute order,
                                      1 (default) ascending support when the supports vary,
                                      2 ascending support; chosen by the next table load */
+    FCA_OPT_WAIT_LIMIT_NS = 6     /* bound, in ns, of a device-side wait of the object-list
+                                     kernel (0: the default, 1 s); see fca_set_option */
 } fca_option;
 
 /*
@@ -178,13 +189,23 @@ fca_status fca_extents(fca_ctx *ctx, const uint32_t *intents, uint64_t count, ui
  * completes. It reads the context's table, so it must be ordered after
  * any fca_context_load that precedes it (the same stream does that).
  * FCA_ERR_INVALID when a cover's intent is not in the given set (the set
- * was not complete).
+ * was not complete) or when an intent is given more than once (the edges
+ * are then not computed; *out_edges is not meaningful).
  */
 fca_status fca_cover_edges(fca_ctx *ctx, const uint32_t *intents, uint64_t count, uint32_t *edges,
                            uint64_t capacity, uint64_t *out_edges, void *stream);
 
 /*
  * Set an option of a context (fca_option).
+ *
+ * FCA_OPT_WAIT_LIMIT_NS: in launches that hand work between the warps of a
+ * thread block, a warp with nothing left to do waits for a hand-over or for
+ * the block's busy warps to finish. The wait is bounded: past the limit the
+ * warp stops waiting and the call returns FCA_ERR_CUDA with a message in
+ * fca_last_error (the kernel records the fault instead of hanging; the
+ * context stays usable). The default, 1 s, is far above the time of any one
+ * subtree search; the environment variable FCA_WAIT_LIMIT_NS sets it before
+ * creation.
  *
  * FCA_OPT_ATTR_ORDER: the search runs over the attributes in a processing
  * order: attribute order (0), or ascending support (number of objects holding
@@ -228,9 +249,12 @@ fca_status fca_set_option(fca_ctx *ctx, int option, int64_t value);
  * Larger sizes return FCA_ERR_INVALID. Its scratch (under 10 KB) is one
  * file-scope device array, held by every GPU that loads the library until the
  * process exits; the first call on a device looks up that array's device
- * address, so make that first call before any stream capture. All calls on a
- * device share the array and rewrite it: calls whose GPU work overlaps in time
- * race. The call returns after the work on `stream` completes.
+ * address, so make that first call before any stream capture. The address is
+ * kept for the life of the process: after a cudaDeviceReset (which also ends
+ * every context of this library on that device) do not call the library on
+ * that device again. All calls on a device share the array and rewrite it:
+ * calls whose GPU work overlaps in time race. The call returns after the work
+ * on `stream` completes.
  */
 fca_status fca_enumerate_small_noalloc(const uint32_t *rows, int64_t n_objects, int32_t n_attrs,
                                        uint32_t *out, uint64_t capacity, uint64_t *out_count,

@@ -62,3 +62,12 @@ def test_null_context_calls(lib):
     assert lib.fca_get_stats(None, ctypes.byref(s)) == fca.FCA_ERR_INVALID
     assert lib.fca_last_error(None) == b""
     lib.fca_free(None)   # NULL is ignored
+
+
+def test_binding_constants_match_the_header():
+    """The binding's status and option numbers are the header's enum values."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    values = {k: int(v) for k, v in re.findall(r"\b(FCA_[A-Z_0-9]+)\s*=\s*(\d+)", text)}
+    assert values["FCA_OPT_WAIT_LIMIT_NS"] == 6
+    for name, v in values.items():
+        assert getattr(fca, name) == v, name

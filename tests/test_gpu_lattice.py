@@ -159,6 +159,26 @@ def test_cover_edges_capacity_and_incomplete_set():
         assert err.value.status == fca.FCA_ERR_INVALID
 
 
+@pytest.mark.parametrize("dup_row,padding", [(0, False), (17, False), (17, True)])
+def test_cover_edges_reject_a_repeated_intent(dup_row, padding):
+    """An intent given twice (also when the copy differs only in padding bits past M, which are
+    ignored) is refused with FCA_ERR_INVALID instead of edges that resolve to either copy; the same
+    set without the copy is accepted."""
+    from closed_set_enumeration_gb300 import fca
+    rows, n, m = cx.random_context(90, 37, 0.2, 3), 90, 37
+    intents = oracle.cbo(rows, n, m)["intents"]
+    copy = intents[dup_row].copy()
+    if padding:
+        copy[-1] |= np.uint32(1 << 31)   # bit 63: past M = 37
+    with fca.Context(rows, n, m) as ctx:
+        with pytest.raises(fca.FcaError) as err:
+            ctx.cover_edges(dev(np.vstack([intents, copy[None, :]])))
+        assert err.value.status == fca.FCA_ERR_INVALID
+        assert "repeat" in str(err.value)
+        e = host(ctx.cover_edges(dev(intents))).astype(np.int64).reshape(-1, 2)
+        assert edge_set(e) == edge_set(lattice.cover_edges(intents, m))
+
+
 @pytest.mark.parametrize("order", ["0", "2"])
 def test_cover_edges_full_size_sparse(order, monkeypatch):
     """The sparse workload (2 000 x 64, 149 629 concepts): Hasse-diagram properties on every edge,

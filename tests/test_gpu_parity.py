@@ -314,3 +314,59 @@ def test_workload_full_size_digest(name):
     for i in rng.choice(got.shape[0], 200, replace=False):
         ext = oracle.derive_extent(rows, got[i])
         assert np.array_equal(oracle.derive_intent(rows, ext, w.n_attrs), got[i])
+
+
+def test_bounded_wait_reports_instead_of_hanging():
+    """The object-list kernel's work-sharing wait is bounded (FCA_OPT_WAIT_LIMIT_NS). A single
+    object-list root (contranominal scale of 20 objects: one subtree of 2^20 concepts) is split
+    into slices, and the warps whose slices are empty wait for hand-overs from the busy ones. With
+    the limit at 1 ns their waits run out: the call must return FCA_ERR_CUDA with the wait message
+    (no hang, no device fault), and the same context must then enumerate correctly with the
+    default limit."""
+    from closed_set_enumeration_gb300 import fca
+    n = 20
+    rows = cx.contranominal(n)
+    want = oracle.cbo(rows, n, n)["intents"]
+    with fca.Context(rows, n, n) as ctx:
+        ctx.set_option(fca.FCA_OPT_WAIT_LIMIT_NS, 1)
+        with pytest.raises(fca.FcaError) as err:
+            ctx.enumerate(capacity=want.shape[0])
+        assert err.value.status == fca.FCA_ERR_CUDA
+        assert "waited past its limit" in str(err.value)
+        ctx.set_option(fca.FCA_OPT_WAIT_LIMIT_NS, 0)
+        got = ctx.enumerate(capacity=want.shape[0]).cpu().numpy().view(np.uint32)
+        assert same_set(got, want)
+
+
+# Small planted-block tables (the planted-bicluster recipe at other sizes): many extents of 65 to a
+# few hundred objects, which are stored as object-id lists and expanded one per warp by the mid-tier
+# kernel, beside larger ones for the bitmap-tier kernel.
+LIST_TIER_CASES = [(4000, 48, 0.03, 6, (80, 400), (4, 10), 1), (5000, 64, 0.05, 10, (100, 600), (4, 12), 3),
+                   (8000, 100, 0.03, 14, (150, 900), (5, 12), 6), (40000, 33, 0.02, 8, (100, 3000), (3, 8), 5)]
+
+
+@pytest.mark.parametrize("mode", ["mid_kernel", "default", "mid_off", "lists_off"])
+@pytest.mark.parametrize("case", LIST_TIER_CASES)
+def test_list_tier_modes(case, mode, monkeypatch):
+    """The same intents and closures whichever kernel takes the extents of 65 to a few hundred
+    objects: the mid-tier kernel on every mid level (FCA_MID_MIN=1), the default choice (these
+    levels are small, so the block-wide kernel takes the mid pools), the bitmap-tier kernel reading
+    id lists from the big pools (FCA_MID_MAX=0), or the bitmap-tier kernel on N-bit bitmaps only
+    (FCA_LIST_MAX=0)."""
+    n, m, p, blocks, objects, attrs, seed = case
+    if mode == "mid_kernel":
+        monkeypatch.setenv("FCA_MID_MIN", "1")
+    elif mode == "mid_off":
+        monkeypatch.setenv("FCA_MID_MAX", "0")
+    elif mode == "lists_off":
+        monkeypatch.setenv("FCA_LIST_MAX", "0")
+    rows = cx.planted_context(n, m, p, blocks, objects, attrs, seed)
+    _, st = check_against_oracle(rows, n, m, threads=8)
+    if mode == "mid_kernel":
+        assert st["mid_launches"] > 0
+    elif mode != "default":
+        assert st["mid_launches"] == 0
+    if mode in ("mid_kernel", "default", "mid_off"):
+        assert st["list_max"] > 64
+    if mode in ("mid_kernel", "default"):
+        assert st["mid_max"] == min(256, st["list_max"])
