@@ -175,6 +175,65 @@ __global__ void unpermute_kernel(uint32_t *out, unsigned long long start, unsign
     }
 }
 
+// The same map for rows of at most WMAX words (M <= 32 WMAX), a tile of 32 rows per warp: lane l
+// loads row l of the tile (all its words in flight), and each 32 x 32 bit block (32 rows x one word)
+// is transposed in registers, so that lane b holds position 32q + b of every row of the tile as one
+// word. Permuting the attributes is then a gather of those columns (lane l of result word w takes
+// column perm[32w + l], by one shuffle per source word), and transposing back gives each lane its
+// row in attribute order. About 15 instructions per row against some 64 for a ballot per result word.
+template <int WMAX>
+__global__ void __launch_bounds__(256) unpermute_tiles_kernel(uint32_t *out, unsigned long long start,
+                                                              unsigned long long capacity, const Counters *ctr,
+                                                              const int32_t *perm, int wm, int m, int guard)
+{
+    if (guard && (ctr->error != 0u || ctr->next_count != 0ull)) return;
+    const unsigned lane = threadIdx.x & 31;
+    // this lane's source word and bit for each result word (bit 32: past M, left clear)
+    int pq[WMAX];
+    uint32_t pb[WMAX];
+#pragma unroll
+    for (int w = 0; w < WMAX; ++w) {
+        const int a = 32 * w + (int)lane;
+        const int q = w < wm && a < m ? perm[a] : -1;
+        pq[w] = q < 0 ? -1 : q >> 5;
+        pb[w] = q < 0 ? 0u : (uint32_t)(q & 31);
+    }
+    const unsigned long long total = ctr->out_count < capacity ? ctr->out_count : capacity;
+    const unsigned long long nwarps = (unsigned long long)gridDim.x * (blockDim.x >> 5);
+    for (unsigned long long r0 = start + 32ull * ((unsigned long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5));
+         r0 < total; r0 += 32ull * nwarps) {
+        const unsigned long long r = r0 + lane;
+        const bool mine = r < total;
+        uint32_t *row = out + r * (unsigned long long)wm;
+        uint32_t t[WMAX];
+#pragma unroll
+        for (int q = 0; q < WMAX; ++q) t[q] = (mine && q < wm) ? row[q] : 0u;
+#pragma unroll
+        for (int q = 0; q < WMAX; ++q)
+            if (q < wm) t[q] = warp_transpose32(t[q]);
+        uint32_t o[WMAX];
+#pragma unroll
+        for (int w = 0; w < WMAX; ++w) {
+            uint32_t v = 0u;
+            if (w < wm) {
+#pragma unroll
+                for (int q = 0; q < WMAX; ++q) {
+                    if (q >= wm) break;
+                    const uint32_t x = __shfl_sync(FULL, t[q], pb[w]);
+                    if (q == pq[w]) v = x;
+                }
+            }
+            o[w] = v;
+        }
+#pragma unroll
+        for (int w = 0; w < WMAX; ++w)
+            if (w < wm) {
+                const uint32_t x = warp_transpose32(o[w]);
+                if (mine) row[w] = x;
+            }
+    }
+}
+
 // The bottom concept when its extent is empty (no row holds every attribute): one more row.
 __global__ void append_bottom_kernel(const uint32_t *botext, long long wn, const uint32_t *full_mask, uint32_t *out,
                                      unsigned long long capacity, Counters *ctr, int wm, int guard)
@@ -316,8 +375,13 @@ int launch_order(const uint32_t *sup, int32_t *perm, int32_t *inv, const uint32_
 int launch_unpermute(uint32_t *out, uint64_t capacity, const Counters *ctr, const int32_t *perm, const Dims &d,
                      int sm_count, void *stream, int guard, uint64_t start)
 {
-    unpermute_kernel<<<(unsigned)(4 * sm_count), 256, 0, (cudaStream_t)stream>>>(out, start, capacity, ctr, perm, d.wm,
-                                                                             d.m, guard);
+    cudaStream_t st = (cudaStream_t)stream;
+    if (d.wm <= 8)
+        unpermute_tiles_kernel<8><<<(unsigned)(8 * sm_count), 256, 0, st>>>(out, start, capacity, ctr, perm, d.wm, d.m, guard);
+    else if (d.wm <= 16)
+        unpermute_tiles_kernel<16><<<(unsigned)(8 * sm_count), 256, 0, st>>>(out, start, capacity, ctr, perm, d.wm, d.m, guard);
+    else
+        unpermute_kernel<<<(unsigned)(4 * sm_count), 256, 0, st>>>(out, start, capacity, ctr, perm, d.wm, d.m, guard);
     return (int)cudaGetLastError();
 }
 
