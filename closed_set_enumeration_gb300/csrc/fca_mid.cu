@@ -97,23 +97,40 @@ __global__ void __launch_bounds__(256) expand_mid_kernel(const __grid_constant__
         __syncwarp();
 
         // ---- restricted columns: per group g of 32 objects and row word w, one register transpose
-        //      gives lane b the bits of attribute 32 w + b over the group
+        //      gives lane b the bits of attribute 32 w + b over the group. The rows of the next group
+        //      (8 words at a time) are loaded while the current one is transposed.
         uint32_t held = 0;   // bit w: attribute 32 w + lane is held by some object of A
-        for (int g = 0; g < G; ++g) {
+        const int chunks = (wm + 7) >> 3;
+        const int steps = G * chunks;
+        auto load8 = [&](int step, uint32_t (&v)[8]) {
+            const int g = step / chunks, w0 = (step - g * chunks) * 8;
             const int i = 32 * g + (int)lane;
-            const uint32_t *row = a.rows + (size_t)(i < n ? ids[i] : 0u) * wm;
-            for (int w0 = 0; w0 < wm; w0 += 8) {
-                uint32_t v[8];
+            const uint32_t *row = a.rows + (size_t)(i < n ? ids[i] : 0u) * wm + w0;
+            if (wm == 8 && i < n) {   // one 32-byte row: two 16-byte loads
+                const uint4 x = __ldg(reinterpret_cast<const uint4 *>(row));
+                const uint4 y = __ldg(reinterpret_cast<const uint4 *>(row) + 1);
+                v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+                v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
+            } else {
 #pragma unroll
-                for (int t = 0; t < 8; ++t) v[t] = (i < n && w0 + t < wm) ? __ldg(row + w0 + t) : 0u;
+                for (int t = 0; t < 8; ++t) v[t] = (i < n && w0 + t < wm) ? __ldg(row + t) : 0u;
+            }
+        };
+        uint32_t nxt[8];
+        load8(0, nxt);
+        for (int step = 0; step < steps; ++step) {
+            uint32_t v[8];
 #pragma unroll
-                for (int t = 0; t < 8; ++t) {
-                    if (w0 + t < wm) {
-                        const uint32_t col = warp_transpose32(v[t]);
-                        const int k = 32 * (w0 + t) + (int)lane;
-                        if (k < d.m) R[(size_t)k * gs + g] = col;
-                        held |= (col != 0u ? 1u : 0u) << (w0 + t);
-                    }
+            for (int t = 0; t < 8; ++t) v[t] = nxt[t];
+            if (step + 1 < steps) load8(step + 1, nxt);
+            const int g = step / chunks, w0 = (step - g * chunks) * 8;
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                if (w0 + t < wm) {
+                    const uint32_t col = warp_transpose32(v[t]);
+                    const int k = 32 * (w0 + t) + (int)lane;
+                    if (k < d.m) R[(size_t)k * gs + g] = col;
+                    held |= (col != 0u ? 1u : 0u) << (w0 + t);
                 }
             }
         }
@@ -156,16 +173,13 @@ __global__ void __launch_bounds__(256) expand_mid_kernel(const __grid_constant__
                 bool in = false;
                 const int k = 32 * t + (int)lane;
                 if (((rel >> t) & 1u) && k != j) {
+                    // every word at once (independent loads): C inside R[k]
                     const uint32_t *Rk = R + (size_t)k * gs;
-                    in = true;
+                    uint32_t bad = 0u;
 #pragma unroll
-                    for (int g = 0; g < GMAX; ++g) {
-                        if (g >= G) break;
-                        if (c[g] & ~Rk[g]) {
-                            in = false;
-                            break;
-                        }
-                    }
+                    for (int g = 0; g < GMAX; ++g)
+                        if (g < G) bad |= c[g] & ~Rk[g];
+                    in = bad == 0u;
                 }
                 const uint32_t dt = __ballot_sync(FULL, in);
                 if (t <= u && (dt & lt_mask(t, j))) {
