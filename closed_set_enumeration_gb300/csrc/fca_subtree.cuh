@@ -210,11 +210,16 @@ __device__ __forceinline__ int vload(const int *p) { return *reinterpret_cast<co
 extern __shared__ uint32_t subtree_smem[];
 __device__ __forceinline__ int *block_hdr() { return reinterpret_cast<int *>(subtree_smem); }
 
-// Register width used for R relevant attributes (must match the dispatch in subtree_kernel).
+// Register width used for R relevant attributes (must match the dispatch in subtree_kernel): kernels
+// with RW <= 4 take the narrowest of 1, 2 and 4 words; the wider kernels search every subtree of up
+// to 32·RW relevant attributes at RW words, so that they hold one register search variant instead
+// of four (their code then fits the instruction caches better, which measured faster than the
+// narrower registers).
 template <int RW>
 __device__ __forceinline__ int regs_width(int R)
 {
-    return R <= 32 ? 1 : (R <= 64 ? 2 : (RW >= 4 && R <= 128 ? 4 : (RW > 4 && R <= 32 * RW ? RW : 0)));
+    if (RW > 4) return R <= 32 * RW ? RW : 0;
+    return R <= 32 ? 1 : (R <= 64 ? 2 : (RW >= 4 && R <= 128 ? 4 : 0));
 }
 
 // Offer half of this warp's remaining search to an idle warp of the block: the remaining
@@ -490,6 +495,32 @@ __device__ void dfs_regs(SubtreeWarp &S, int R, int n, int jn, int slices, int s
         }
         if (SCREEN) screen<NW, WRT, COUNT>(S, cand, ext, B, col, rowc);
     }
+    // Candidate cursor: cu is the lowest word of cand[] with candidates left and cw its remaining
+    // bits (cand[cu] itself is stale, words below cu are spent), so taking the next candidate costs
+    // a few instructions whatever WRT is; cand[] is brought up to date only when a frame is pushed
+    // or the candidates leave the search (spill, hand-over).
+    int cu;
+    uint32_t cw;
+    auto cursor_from_cand = [&]() {
+        cu = WRT;
+        cw = 0u;
+#pragma unroll
+        for (int u = WRT - 1; u >= 0; --u)
+            if (cand[u]) {
+                cu = u;
+                cw = cand[u];
+            }
+    };
+    auto cand_from_cursor = [&]() {
+#pragma unroll
+        for (int u = 0; u < WRT; ++u) cand[u] = u < cu ? 0u : (u == cu ? cw : cand[u]);
+    };
+    cursor_from_cand();
+    // Column prefetch (R <= 128, where the registers allow it; with 256 relevant attributes the two
+    // extra registers per extent word cost more than the load latency they hide)
+    constexpr bool PREFETCH = WRT <= 4;
+    int pj = -1;        // compact index whose column pc[] holds
+    uint32_t pc[NW];
     int depth = 0;
     int visits = 0;
     for (;;) {
@@ -503,6 +534,7 @@ __device__ void dfs_regs(SubtreeWarp &S, int R, int n, int jn, int slices, int s
         if (SPILL && !SHARE && S.deadline != 0 && (visits & 31) == 0 && clock64() > S.deadline &&
             vload(&block_hdr()[H_TAIL]) != 0) {
             const bool keep0 = handed || slices > 1;
+            cand_from_cursor();
             if (!keep0) {
                 if (spill_rest<NW, WRT>(S, 0, depth, ext, B, cand)) return;
                 S.deadline = 0;
@@ -519,6 +551,7 @@ __device__ void dfs_regs(SubtreeWarp &S, int R, int n, int jn, int slices, int s
                     }
                     __syncwarp();
                     S.deadline = clock64() + S.args->budget;
+                    cursor_from_cand();
                     continue;
                 }
                 S.deadline = 0;
@@ -526,13 +559,25 @@ __device__ void dfs_regs(SubtreeWarp &S, int R, int n, int jn, int slices, int s
         }
         // an idle warp of the block is waiting and this search is long: hand it half of the rest
         if (SHARE && visits > SHARE_AFTER &&
-            __any_sync(FULL, vload(&block_hdr()[H_IDLE]) > 0 && vload(&block_hdr()[H_MB]) == MB_EMPTY))
+            __any_sync(FULL, vload(&block_hdr()[H_IDLE]) > 0 && vload(&block_hdr()[H_MB]) == MB_EMPTY)) {
+            cand_from_cursor();
             offer<NW, WRT>(S, R, depth, ext, B, cand);
-        int j = -1;
+            cursor_from_cand();
+        }
+        if (cw == 0u) {
+            // the next word with candidates, or back up to the parent
+            int nu = WRT;
+            uint32_t nw = 0u;
 #pragma unroll
-        for (int u = 0; u < WRT; ++u)
-            if (j < 0 && cand[u]) j = 32 * u + __ffs(cand[u]) - 1;
-        if (j < 0) {
+            for (int u = WRT - 1; u >= 0; --u)
+                if (u > cu && cand[u]) {
+                    nu = u;
+                    nw = cand[u];
+                }
+            cu = nu;
+            cw = nw;
+        }
+        if (cw == 0u) {
             if (depth == 0) break;
             --depth;
             const uint32_t *f = S.stk() + (size_t)depth * S.fs;
@@ -544,15 +589,28 @@ __device__ void dfs_regs(SubtreeWarp &S, int R, int n, int jn, int slices, int s
                 B[u] = f[NW + WRT + u];
             }
             __syncwarp();
+            cursor_from_cand();
             continue;
         }
-        const int ju = j >> 5;
-#pragma unroll
-        for (int u = 0; u < WRT; ++u)
-            if (u == ju) cand[u] &= cand[u] - 1u;     // j is the lowest remaining candidate
+        const int ju = cu;
+        const int j = 32 * cu + __ffs(cw) - 1;   // the lowest remaining candidate
+        cw &= cw - 1u;
         uint32_t C[NW];
+        if (PREFETCH && j == pj) {
 #pragma unroll
-        for (int t = 0; t < NW; ++t) C[t] = ext[t] & S.cR()[t * S.mp + j];
+            for (int t = 0; t < NW; ++t) C[t] = ext[t] & pc[t];
+        } else {
+#pragma unroll
+            for (int t = 0; t < NW; ++t) C[t] = ext[t] & S.cR()[t * S.mp + j];
+        }
+        if (PREFETCH) {
+            // the column of the next candidate of this word, loaded while this one is evaluated
+            pj = cw ? 32 * cu + __ffs(cw) - 1 : -1;
+            if (pj >= 0) {
+#pragma unroll
+                for (int t = 0; t < NW; ++t) pc[t] = S.cR()[t * S.mp + pj];
+            }
+        }
         if (COUNT) S.ops += NW;            // the extent intersection
 
         // closure over the relevant attributes, canonical prefix first
@@ -582,7 +640,7 @@ __device__ void dfs_regs(SubtreeWarp &S, int R, int n, int jn, int slices, int s
             for (int t = 0; t < NW; ++t) f[t] = ext[t];
 #pragma unroll
             for (int u = 0; u < WRT; ++u) {
-                f[NW + u] = cand[u];
+                f[NW + u] = u < cu ? 0u : (u == cu ? cw : cand[u]);
                 f[NW + WRT + u] = B[u];
             }
         }
@@ -600,6 +658,7 @@ __device__ void dfs_regs(SubtreeWarp &S, int R, int n, int jn, int slices, int s
             if (COUNT) S.ops += 2ull * NW * (unsigned)max(0, min(32, R - 32 * u));
         }
         if (SCREEN) screen<NW, WRT, COUNT>(S, cand, ext, B, col, rowc);
+        cursor_from_cand();
     }
 }
 
@@ -913,15 +972,15 @@ __global__ void __launch_bounds__(256, RW > 4 ? 3 : 4) subtree_kernel(const __gr
         const int sl = handed ? 1 : a.slices;
         const int wr = regs_width<RW>(R);
         if (SHARE && share) {
-            if (wr == 1) dfs_regs<NW, 1, COUNT, true, SPILLS>(S, R, n, jn, sl, slice, handed);
-            else if (wr == 2) dfs_regs<NW, 2, COUNT, true, SPILLS>(S, R, n, jn, sl, slice, handed);
-            else if (RW >= 4 && wr == 4) dfs_regs<NW, 4, COUNT, true, SPILLS>(S, R, n, jn, sl, slice, handed);
+            if (RW <= 4 && wr == 1) dfs_regs<NW, 1, COUNT, true, SPILLS>(S, R, n, jn, sl, slice, handed);
+            else if (RW <= 4 && wr == 2) dfs_regs<NW, 2, COUNT, true, SPILLS>(S, R, n, jn, sl, slice, handed);
+            else if (RW == 4 && wr == 4) dfs_regs<NW, 4, COUNT, true, SPILLS>(S, R, n, jn, sl, slice, handed);
             else if (RW > 4 && wr == RW) dfs_regs<NW, RW, COUNT, true, SPILLS>(S, R, n, jn, sl, slice, handed);
             else dfs_smem<NW, COUNT>(S, R, n, jn, sl, slice);
         } else {
-            if (wr == 1) dfs_regs<NW, 1, COUNT, false, SPILLS>(S, R, n, jn, sl, slice, false);
-            else if (wr == 2) dfs_regs<NW, 2, COUNT, false, SPILLS>(S, R, n, jn, sl, slice, false);
-            else if (RW >= 4 && wr == 4) dfs_regs<NW, 4, COUNT, false, SPILLS>(S, R, n, jn, sl, slice, false);
+            if (RW <= 4 && wr == 1) dfs_regs<NW, 1, COUNT, false, SPILLS>(S, R, n, jn, sl, slice, false);
+            else if (RW <= 4 && wr == 2) dfs_regs<NW, 2, COUNT, false, SPILLS>(S, R, n, jn, sl, slice, false);
+            else if (RW == 4 && wr == 4) dfs_regs<NW, 4, COUNT, false, SPILLS>(S, R, n, jn, sl, slice, false);
             else if (RW > 4 && wr == RW) dfs_regs<NW, RW, COUNT, false, SPILLS>(S, R, n, jn, sl, slice, false);
             else dfs_smem<NW, COUNT>(S, R, n, jn, sl, slice);
         }
