@@ -125,6 +125,11 @@ def _biclusters() -> np.ndarray:
     return planted_cells(100000, 256, 0.01, 40, (500, 5000), (6, 20), np.random.default_rng(4))
 
 
+def _biclusters_50k() -> np.ndarray:
+    # the same recipe at half the objects and blocks: a case small enough for multi-pass profiling
+    return planted_cells(50000, 256, 0.01, 20, (500, 5000), (6, 20), np.random.default_rng(5))
+
+
 WORKLOADS: Dict[str, Workload] = {
     w.name: w
     for w in [
@@ -136,6 +141,8 @@ WORKLOADS: Dict[str, Workload] = {
                  "50,000x400; per-attribute Zipf(s=1.1) densities, mean 0.02", _zipf),
         Workload("biclusters", 100000, 256, 4,
                  "100,000x256; Bernoulli(0.01) background + 40 planted blocks", _biclusters),
+        Workload("biclusters_50k", 50000, 256, 5,
+                 "50,000x256; Bernoulli(0.01) background + 20 planted blocks", _biclusters_50k),
     ]
 }
 
