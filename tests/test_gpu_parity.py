@@ -290,7 +290,7 @@ def _digest(intents):
     return hashlib.sha256(np.ascontiguousarray(rows).tobytes()).hexdigest()
 
 
-@pytest.mark.parametrize("name", ["sparse", "skewed", "zipf", "biclusters"])
+@pytest.mark.parametrize("name", ["sparse", "skewed", "zipf", "biclusters_50k", "biclusters"])
 def test_workload_full_size_digest(name):
     """Full-size workloads against oracle digests written by tests/golden/make_workload_digests.py:
     exact count and closures (in the processing order of the tests), the order-independent
