@@ -181,8 +181,16 @@ __global__ void __launch_bounds__(256) expand_mid_kernel(const __grid_constant__
                         if (g < G) bad |= c[g] & ~Rk[g];
                     in = bad == 0u;
                 }
+                if (t < u) {
+                    // a word below j's: any attribute of it in the closure (none is in B) ends j
+                    if (__any_sync(FULL, in)) {
+                        canonical = false;
+                        break;
+                    }
+                    continue;
+                }
                 const uint32_t dt = __ballot_sync(FULL, in);
-                if (t <= u && (dt & lt_mask(t, j))) {
+                if (t == u && (dt & lt_mask(t, j))) {
                     canonical = false;
                     break;
                 }
