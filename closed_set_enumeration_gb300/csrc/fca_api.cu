@@ -87,6 +87,8 @@ struct fca_ctx {
     // by the mid-tier kernel (0: off)
     int list_max = 0, mid_max = 0;
     int64_t mid_stride = 0;
+    // inherited failures kept in mid-pool slots (M <= 256: one byte per attribute) after the ids
+    int wit_off = 0, wit_words = 0;
     uint64_t mid_min = 0;           // smallest mid-pool launch given to the mid-tier kernel
     uint64_t wait_ns = 0;           // bound of a work-sharing wait (0: the kernels' default)
     uint64_t table_launches = 0;    // kernels launched by the last table load
@@ -504,6 +506,8 @@ fca_status launch_level(Run &r, size_t lv, uint64_t bb, uint64_t kb, uint64_t bm
     a.count_work = c->count_work;
     a.list_max = c->list_max;
     a.mid_max = c->mid_max;
+    a.wit_off = c->wit_off;
+    a.wit_words = c->wit_words;
     const bool on_device = chain_i >= 1;
     const bool has_mid = c->mid_max > SMALL_MAX && (km > 0 || on_device);
     const bool warps = has_mid && km >= c->mid_min;
@@ -1089,6 +1093,11 @@ fca_status fca_context_create(const uint32_t *rows, int64_t n_objects, int32_t n
         if (v && v[0] == '0' && v[1] == 0) c->mid_max = 0;
     }
     c->mid_stride = c->mid_max > SMALL_MAX ? ((int64_t)c->mid_max + 3) & ~(int64_t)3 : 0;
+    if (c->mid_stride > 0 && c->d.m <= 256 && !(getenv("FCA_NO_INHERIT") && getenv("FCA_NO_INHERIT")[0] == '1')) {
+        c->wit_off = (int)c->mid_stride;
+        c->wit_words = ((c->d.m + 3) / 4 + 3) & ~3;
+        c->mid_stride += c->wit_words;
+    }
     c->mid_min = env_u64("FCA_MID_MIN", MID_MIN_PARENTS_PER_SM * (uint64_t)c->sm_count);
     *out_ctx = c;
     return FCA_OK;

@@ -215,6 +215,9 @@ __device__ __forceinline__ void finish_candidate(const ExpandArgs &a, const Dims
         }
         if ((int)cnt <= a.list_max) write_list(X.ext + s * (size_t)X.stride);
         else write_ext(X.ext + s * (size_t)X.stride);
+        // a mid-pool child inherits no failures from this tier
+        if (mid)
+            for (int i = (int)lane; i < a.wit_words; i += 32) X.ext[s * (size_t)X.stride + a.wit_off + i] = FULL;
         if (lane < (unsigned)d.wm) X.itt[s * d.wm + lane] = Dw;
         if (lane == 0) { X.y[s] = j + 1; X.n[s] = (int)cnt; }
     }

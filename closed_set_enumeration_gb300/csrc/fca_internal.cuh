@@ -131,6 +131,10 @@ struct ExpandArgs {
                             // level (mid_max <= SMALL_MAX: no mid tier)
     Level next;             // children with more than max(SMALL_MAX, mid_max) objects (big pool)
     Level next_mid;         // children with SMALL_MAX < n <= mid_max objects (mid pool)
+    int wit_off;            // mid-pool entries: word offset, inside the entry's slot, of its inherited
+                            // failures (one byte per attribute: the witness of a candidate that failed
+                            // at an ancestor, 0xff for none); 0 when they are not kept
+    int wit_words;          // words of those bytes
     Queue q[NQ];            // children with <= 32 << q objects
     uint32_t *out;          // capacity x wm
     uint64_t capacity;

@@ -23,13 +23,20 @@
 namespace fca {
 namespace {
 
+// Mid-pool children of one entry whose inherited failures are written when the entry is done.
+constexpr int WIT_SLOTS = 32;
+
 // Per-warp shared memory in 32-bit words: R (M attributes, stride G | 1, at most GMAX + 1: an odd
 // stride keeps the per-attribute reads of one word by 32 lanes and the lane-wise stores of the
-// transposes free of bank conflicts), then the object ids (32 GMAX).
+// transposes free of bank conflicts), then the object ids (32 GMAX), then the entry's failure
+// witnesses (ww words, one byte per attribute) and the slots of its mid-pool children.
 template <int GMAX>
 struct MidLayout {
     static constexpr int GS = GMAX + 1;
-    __host__ __device__ static size_t words(int m) { return (size_t)m * GS + 32u * GMAX; }
+    __host__ __device__ static size_t words(int m, int ww)
+    {
+        return (size_t)m * GS + 32u * GMAX + (ww > 0 ? (size_t)ww + WIT_SLOTS : 0u);
+    }
 };
 
 // The ids of the objects of C (bits of word `cw` of lane g < G: object 32 g + b of the list `ids`)
@@ -53,7 +60,7 @@ __device__ __forceinline__ void write_ids(uint32_t cw, const uint32_t *ids, uint
     for (int i = (int)cnt + (int)lane; i < fill; i += 32) dst[i] = 0u;
 }
 
-template <bool COUNT, int GMAX>
+template <bool COUNT, int GMAX, bool INHERIT>
 __global__ void __launch_bounds__(256) expand_mid_kernel(const __grid_constant__ ExpandArgs a)
 {
     extern __shared__ __align__(16) uint32_t mid_smem[];
@@ -61,8 +68,13 @@ __global__ void __launch_bounds__(256) expand_mid_kernel(const __grid_constant__
     const int wm = d.wm;
     const unsigned lane = threadIdx.x & 31;
     const int wib = threadIdx.x >> 5;
-    uint32_t *R = mid_smem + (size_t)wib * MidLayout<GMAX>::words(d.m);
+    uint32_t *R = mid_smem + (size_t)wib * MidLayout<GMAX>::words(d.m, a.wit_words);
     uint32_t *ids = R + (size_t)d.m * MidLayout<GMAX>::GS;
+    // inherited failures (the Fast Close-by-One rule): witness byte per attribute, 0xff for none
+    constexpr bool inherit = INHERIT;
+    uint32_t *witw = ids + 32 * GMAX;
+    uint8_t *wit = reinterpret_cast<uint8_t *>(witw);
+    uint32_t *slots = witw + a.wit_words;
     const uint32_t valid_last = (d.m & 31) ? ((1u << (d.m & 31)) - 1u) : FULL;
     const unsigned long long p_count = a.p_count_dev ? *a.p_count_dev : a.p_count;
     const unsigned long long nwarps = (unsigned long long)gridDim.x * (blockDim.x >> 5);
@@ -93,7 +105,10 @@ __global__ void __launch_bounds__(256) expand_mid_kernel(const __grid_constant__
         const int gs = G | 1;
         const uint32_t *src = a.in.ext + p * (size_t)a.in.stride;
         for (int i = (int)lane; i < n; i += 32) ids[i] = src[i];
+        if (inherit)
+            for (int i = (int)lane; i < a.wit_words; i += 32) witw[i] = src[a.wit_off + i];
         const uint32_t Bw = (int)lane < wm ? a.in.itt[p * wm + lane] : 0u;
+        int nslots = 0;   // mid-pool children recorded in slots[]
         __syncwarp();
 
         // ---- restricted columns: per group g of 32 objects and row word w, one register transpose
@@ -157,6 +172,12 @@ __global__ void __launch_bounds__(256) expand_mid_kernel(const __grid_constant__
             ++my_closures;
             // no object of A holds j: C is empty (its closure is the bottom, added by the host)
             if (!((__shfl_sync(FULL, held, jb) >> u) & 1u)) continue;
+            // j failed at an ancestor whose extent holds A, its closure there containing the witness
+            // k < j: while k stays outside B, j's closure here contains k too and j fails again
+            if (inherit) {
+                const unsigned w = wit[j];
+                if (w != 0xffu && !((__shfl_sync(FULL, Bw, (int)(w >> 5)) >> (w & 31)) & 1u)) continue;
+            }
 
             uint32_t c[GMAX];
             unsigned cnt = 0;
@@ -181,6 +202,18 @@ __global__ void __launch_bounds__(256) expand_mid_kernel(const __grid_constant__
                         if (g < G) bad |= c[g] & ~Rk[g];
                     in = bad == 0u;
                 }
+                if (inherit) {
+                    // the lowest attribute below j in the closure is the failure's witness
+                    const uint32_t dt = __ballot_sync(FULL, in);
+                    const uint32_t viol = t < u ? dt : (t == u ? dt & lt_mask(t, j) : 0u);
+                    if (viol) {
+                        if (lane == 0) wit[j] = (uint8_t)(32 * t + __ffs(viol) - 1);
+                        canonical = false;
+                        break;
+                    }
+                    if ((int)lane == t) Dw |= dt;
+                    continue;
+                }
                 if (t < u) {
                     // a word below j's: any attribute of it in the closure (none is in B) ends j
                     if (__any_sync(FULL, in)) {
@@ -197,6 +230,7 @@ __global__ void __launch_bounds__(256) expand_mid_kernel(const __grid_constant__
                 if ((int)lane == t) Dw |= dt;
             }
             if (!canonical) continue;
+            if (inherit && lane == 0) wit[j] = 0xffu;
 
             // ---- emit the intent
             unsigned long long slot = 0;
@@ -243,9 +277,26 @@ __global__ void __launch_bounds__(256) expand_mid_kernel(const __grid_constant__
                     X.y[s] = j + 1;
                     X.n[s] = (int)cnt;
                 }
+                // its inherited failures are written once every candidate of this entry is done
+                // (past WIT_SLOTS children: none)
+                if (inherit) {
+                    if (nslots < WIT_SLOTS) {
+                        if (lane == 0) slots[nslots] = (uint32_t)s;
+                        ++nslots;
+                    } else {
+                        for (int i = (int)lane; i < a.wit_words; i += 32)
+                            X.ext[s * (size_t)X.stride + a.wit_off + i] = FULL;
+                    }
+                }
             }
         }
-        __syncwarp();   // ids and R are rewritten by the next entry
+        __syncwarp();
+        if (inherit)
+            for (int ci = 0; ci < nslots; ++ci) {
+                uint32_t *dst = a.next_mid.ext + (size_t)slots[ci] * a.next_mid.stride + a.wit_off;
+                for (int i = (int)lane; i < a.wit_words; i += 32) dst[i] = witw[i];
+            }
+        __syncwarp();   // ids, R and the witnesses are rewritten by the next entry
     }
     if (lane == 0) {
         if (my_closures) atomicAdd(&a.ctr->closures, my_closures);
@@ -257,10 +308,10 @@ __global__ void __launch_bounds__(256) expand_mid_kernel(const __grid_constant__
 // M x (GMAX + 1) words plus the object ids).
 int mid_gmax(int m) { return m <= 512 ? 8 : 4; }
 
-template <bool COUNT, int GMAX>
+template <bool COUNT, int GMAX, bool INHERIT>
 int launch_mid_t(const ExpandArgs &a, int sm_count, void *stream)
 {
-    const size_t per_warp = MidLayout<GMAX>::words(a.d.m) * 4;
+    const size_t per_warp = MidLayout<GMAX>::words(a.d.m, a.wit_words) * 4;
     // warps per block: the shape with the most resident warps per SM (ties: the larger block)
     static thread_local ShapeCache cache;
     int dev = 0;
@@ -270,11 +321,11 @@ int launch_mid_t(const ExpandArgs &a, int sm_count, void *stream)
         for (int wpb = 8; wpb >= 1; wpb >>= 1) {
             const size_t smem = per_warp * wpb;
             if (smem > 200 * 1024) continue;
-            cudaError_t e = cudaFuncSetAttribute(expand_mid_kernel<COUNT, GMAX>,
+            cudaError_t e = cudaFuncSetAttribute(expand_mid_kernel<COUNT, GMAX, INHERIT>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) return (int)e;
             int ps = 0;
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ps, expand_mid_kernel<COUNT, GMAX>, wpb * 32, smem);
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ps, expand_mid_kernel<COUNT, GMAX, INHERIT>, wpb * 32, smem);
             if (ps * wpb > best_w) {
                 best_w = ps * wpb;
                 best_wpb = wpb;
@@ -282,7 +333,7 @@ int launch_mid_t(const ExpandArgs &a, int sm_count, void *stream)
             }
         }
         if (best_w == 0) return (int)cudaErrorInvalidConfiguration;
-        cudaError_t e = cudaFuncSetAttribute(expand_mid_kernel<COUNT, GMAX>,
+        cudaError_t e = cudaFuncSetAttribute(expand_mid_kernel<COUNT, GMAX, INHERIT>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(per_warp * best_wpb));
         if (e != cudaSuccess) return (int)e;
         cache = ShapeCache{dev, per_warp, best_wpb, best_ps};
@@ -292,7 +343,7 @@ int launch_mid_t(const ExpandArgs &a, int sm_count, void *stream)
     unsigned long long blocks = a.p_count_dev ? resident
                                               : std::min<unsigned long long>(resident, (a.p_count + wpb - 1) / wpb);
     if (blocks < 1) blocks = 1;
-    expand_mid_kernel<COUNT, GMAX><<<(unsigned)blocks, wpb * 32, per_warp * wpb, (cudaStream_t)stream>>>(a);
+    expand_mid_kernel<COUNT, GMAX, INHERIT><<<(unsigned)blocks, wpb * 32, per_warp * wpb, (cudaStream_t)stream>>>(a);
     return (int)cudaGetLastError();
 }
 
@@ -307,9 +358,16 @@ int mid_max_for(const Dims &d)
 
 int launch_expand_mid(const ExpandArgs &a, int sm_count, void *stream)
 {
-    if (mid_gmax(a.d.m) == 8)
-        return a.count_work ? launch_mid_t<true, 8>(a, sm_count, stream) : launch_mid_t<false, 8>(a, sm_count, stream);
-    return a.count_work ? launch_mid_t<true, 4>(a, sm_count, stream) : launch_mid_t<false, 4>(a, sm_count, stream);
+    // inherited failures are kept only for M <= 256 (one byte per attribute), where GMAX is 8
+    if (mid_gmax(a.d.m) == 8) {
+        if (a.wit_words > 0)
+            return a.count_work ? launch_mid_t<true, 8, true>(a, sm_count, stream)
+                                : launch_mid_t<false, 8, true>(a, sm_count, stream);
+        return a.count_work ? launch_mid_t<true, 8, false>(a, sm_count, stream)
+                            : launch_mid_t<false, 8, false>(a, sm_count, stream);
+    }
+    return a.count_work ? launch_mid_t<true, 4, false>(a, sm_count, stream)
+                        : launch_mid_t<false, 4, false>(a, sm_count, stream);
 }
 
 }  // namespace fca

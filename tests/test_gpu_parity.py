@@ -345,28 +345,32 @@ LIST_TIER_CASES = [(4000, 48, 0.03, 6, (80, 400), (4, 10), 1), (5000, 64, 0.05, 
                    (8000, 100, 0.03, 14, (150, 900), (5, 12), 6), (40000, 33, 0.02, 8, (100, 3000), (3, 8), 5)]
 
 
-@pytest.mark.parametrize("mode", ["mid_kernel", "default", "mid_off", "lists_off"])
+@pytest.mark.parametrize("mode", ["mid_kernel", "mid_kernel_no_inherit", "default", "mid_off", "lists_off"])
 @pytest.mark.parametrize("case", LIST_TIER_CASES)
 def test_list_tier_modes(case, mode, monkeypatch):
     """The same intents and closures whichever kernel takes the extents of 65 to a few hundred
-    objects: the mid-tier kernel on every mid level (FCA_MID_MIN=1), the default choice (these
-    levels are small, so the block-wide kernel takes the mid pools), the bitmap-tier kernel reading
-    id lists from the big pools (FCA_MID_MAX=0), or the bitmap-tier kernel on N-bit bitmaps only
-    (FCA_LIST_MAX=0)."""
+    objects: the mid-tier kernel on every mid level (FCA_MID_MIN=1), with and without the failures
+    its entries inherit from their mid-tier ancestors (FCA_NO_INHERIT=1: every candidate's closure
+    is computed), the default choice (these levels are small, so the block-wide kernel takes the mid
+    pools), the bitmap-tier kernel reading id lists from the big pools (FCA_MID_MAX=0), or the
+    bitmap-tier kernel on N-bit bitmaps only (FCA_LIST_MAX=0). The closure count includes the
+    candidates skipped by inheritance, so it matches the oracle's in every mode."""
     n, m, p, blocks, objects, attrs, seed = case
-    if mode == "mid_kernel":
+    if mode.startswith("mid_kernel"):
         monkeypatch.setenv("FCA_MID_MIN", "1")
+    if mode == "mid_kernel_no_inherit":
+        monkeypatch.setenv("FCA_NO_INHERIT", "1")
     elif mode == "mid_off":
         monkeypatch.setenv("FCA_MID_MAX", "0")
     elif mode == "lists_off":
         monkeypatch.setenv("FCA_LIST_MAX", "0")
     rows = cx.planted_context(n, m, p, blocks, objects, attrs, seed)
     _, st = check_against_oracle(rows, n, m, threads=8)
-    if mode == "mid_kernel":
+    if mode.startswith("mid_kernel"):
         assert st["mid_launches"] > 0
     elif mode != "default":
         assert st["mid_launches"] == 0
-    if mode in ("mid_kernel", "default", "mid_off"):
+    if mode in ("mid_kernel", "mid_kernel_no_inherit", "default", "mid_off"):
         assert st["list_max"] > 64
-    if mode in ("mid_kernel", "default"):
+    if mode in ("mid_kernel", "mid_kernel_no_inherit", "default"):
         assert st["mid_max"] == min(256, st["list_max"])
