@@ -87,8 +87,10 @@ struct fca_ctx {
     // by the mid-tier kernel (0: off)
     int list_max = 0, mid_max = 0;
     int64_t mid_stride = 0;
-    // inherited failures kept in mid-pool slots (M <= 256: one byte per attribute) after the ids
+    // inherited failures (M <= 256: one byte per attribute) kept in every level entry after its
+    // extent: at word wit_off of a mid-pool slot, at word wnp of a big-pool slot (big_stride words)
     int wit_off = 0, wit_words = 0;
+    int64_t big_stride = 0;
     uint64_t mid_min = 0;           // smallest mid-pool launch given to the mid-tier kernel
     uint64_t wait_ns = 0;           // bound of a work-sharing wait (0: the kernels' default)
     uint64_t table_launches = 0;    // kernels launched by the last table load
@@ -160,13 +162,13 @@ fca_status alloc_raw(fca_ctx *c, void **p, size_t bytes, const char *what)
     return FCA_OK;
 }
 
-uint64_t level_entry_bytes(const Dims &d) { return ((uint64_t)d.wnp + d.wm + 2) * 4; }
+uint64_t level_entry_bytes(const fca_ctx *c) { return ((uint64_t)c->big_stride + c->d.wm + 2) * 4; }
 uint64_t mid_entry_bytes(const fca_ctx *c) { return ((uint64_t)c->mid_stride + c->d.wm + 2) * 4; }
 uint64_t queue_entry_bytes(const Dims &d, int qi) { return ((uint64_t)(32 << qi) + d.wm + 2) * 4; }
 
 uint64_t initial_level_cap(const fca_ctx *c)
 {
-    return std::max<uint64_t>(4 * (uint64_t)c->d.m, c->level_bytes / level_entry_bytes(c->d));
+    return std::max<uint64_t>(4 * (uint64_t)c->d.m, c->level_bytes / level_entry_bytes(c));
 }
 
 uint64_t initial_mid_cap(const fca_ctx *c)
@@ -248,9 +250,9 @@ fca_status ensure_level(fca_ctx *c, size_t idx)
     while (c->levels.size() <= idx) {
         const uint64_t cap = initial_level_cap(c);
         Level L{}, M{};
-        fca_status s = make_level(c, &L, cap, c->d.wnp);
+        fca_status s = make_level(c, &L, cap, c->big_stride);
         if (s != FCA_OK) return s;
-        c->pool_bytes += cap * level_entry_bytes(c->d);
+        c->pool_bytes += cap * level_entry_bytes(c);
         if (c->mid_max > SMALL_MAX) {
             const uint64_t mcap = initial_mid_cap(c);
             if ((s = make_level(c, &M, mcap, c->mid_stride)) != FCA_OK) {
@@ -291,7 +293,7 @@ fca_status grow_level(fca_ctx *c, size_t idx, bool mid, uint64_t need, cudaStrea
 {
     Level &L = mid ? c->mids[idx] : c->levels[idx];
     const uint64_t cap = std::max<uint64_t>(2 * L.cap, need + need / 4);
-    const uint64_t eb = mid ? mid_entry_bytes(c) : level_entry_bytes(c->d);
+    const uint64_t eb = mid ? mid_entry_bytes(c) : level_entry_bytes(c);
     if (c->pool_bytes + (cap - L.cap) * eb > c->pool_limit) return FCA_ERR_CAPACITY;
     Level n{};
     fca_status s = make_level(c, &n, cap, L.stride);
@@ -508,6 +510,7 @@ fca_status launch_level(Run &r, size_t lv, uint64_t bb, uint64_t kb, uint64_t bm
     a.mid_max = c->mid_max;
     a.wit_off = c->wit_off;
     a.wit_words = c->wit_words;
+    a.wit_off_big = (int)c->d.wnp;
     const bool on_device = chain_i >= 1;
     const bool has_mid = c->mid_max > SMALL_MAX && (km > 0 || on_device);
     const bool warps = has_mid && km >= c->mid_min;
@@ -1093,10 +1096,14 @@ fca_status fca_context_create(const uint32_t *rows, int64_t n_objects, int32_t n
         if (v && v[0] == '0' && v[1] == 0) c->mid_max = 0;
     }
     c->mid_stride = c->mid_max > SMALL_MAX ? ((int64_t)c->mid_max + 3) & ~(int64_t)3 : 0;
-    if (c->mid_stride > 0 && c->d.m <= 256 && !(getenv("FCA_NO_INHERIT") && getenv("FCA_NO_INHERIT")[0] == '1')) {
-        c->wit_off = (int)c->mid_stride;
+    c->big_stride = c->d.wnp;
+    if (c->d.m <= 256 && !(getenv("FCA_NO_INHERIT") && getenv("FCA_NO_INHERIT")[0] == '1')) {
         c->wit_words = ((c->d.m + 3) / 4 + 3) & ~3;
-        c->mid_stride += c->wit_words;
+        c->big_stride += c->wit_words;
+        if (c->mid_stride > 0) {
+            c->wit_off = (int)c->mid_stride;
+            c->mid_stride += c->wit_words;
+        }
     }
     c->mid_min = env_u64("FCA_MID_MIN", MID_MIN_PARENTS_PER_SM * (uint64_t)c->sm_count);
     *out_ctx = c;

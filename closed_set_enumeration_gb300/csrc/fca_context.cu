@@ -313,6 +313,8 @@ __global__ void start_kernel(Counters *ctr, const uint32_t *top, const uint32_t 
     }
     if (qi < 0) {
         for (long long q = t; q < d.wnp; q += blockDim.x) L0.ext[q] = root_ext[q];
+        // the root inherits no failures (the entry's words past its extent, when kept)
+        for (long long q = d.wnp + t; q < L0.stride; q += blockDim.x) L0.ext[q] = 0xffffffffu;
         if (t == 0) {
             L0.y[0] = 0;
             L0.n[0] = (int32_t)d.n;

@@ -63,6 +63,8 @@ template <> struct ExpandShape<16> {
     static constexpr size_t smem_budget = 108 * 1024;
 };
 constexpr int ROWS_KEPT = 256;             // restricted extents up to this size keep their rows in shared memory
+constexpr int CHILD_SLOTS = 64;            // level children of one work item that inherit its failures
+constexpr int WIT_WORDS_MAX = 64;          // failure witnesses of one parent (M <= 256: a byte each)
 
 // Shared memory of expand_bitmap_kernel. Both paths first stage the parent's non-zero extent
 // chunks (uint4 index and value). The gather path then keeps, per warp, up to SMALL_MAX object
@@ -124,11 +126,13 @@ __device__ __forceinline__ int block_exclusive_sum(int v, int *scratch, int *tot
 // object of C and `obj_id(i)` its object id; `write_ext(dst)` writes C as a dense bitmap for a
 // child of the next level, `write_list(dst)` as its ascending object ids (a child of at most
 // list_max objects); `all_ids()` completes the list of a small child (need < |C|).
-template <bool COUNT, class RowWord, class ObjId, class Subset, class WriteExt, class WriteList, class AllIds>
-__device__ __forceinline__ void finish_candidate(const ExpandArgs &a, const Dims &d, const uint32_t *B, int j,
-                                                 unsigned cnt, unsigned need, RowWord &&row_word, ObjId &&obj_id,
-                                                 Subset &&subset, WriteExt &&write_ext, WriteList &&write_list,
-                                                 AllIds &&all_ids, unsigned long long &my_bytes)
+template <bool COUNT, bool INHERIT, class RowWord, class ObjId, class Subset, class WriteExt, class WriteList,
+          class AllIds>
+__device__ __forceinline__ int finish_candidate(const ExpandArgs &a, const Dims &d, const uint32_t *B, int j,
+                                                unsigned cnt, unsigned need, RowWord &&row_word, ObjId &&obj_id,
+                                                Subset &&subset, WriteExt &&write_ext, WriteList &&write_list,
+                                                AllIds &&all_ids, unsigned long long &my_bytes, uint32_t *cslots,
+                                                int *ccount)
 {
     const unsigned lane = threadIdx.x & 31;
     // AND of the rows: lanes take (object, word) pairs with the words padded to a power of two W2
@@ -150,7 +154,13 @@ __device__ __forceinline__ void finish_candidate(const ExpandArgs &a, const Dims
     uint32_t Dw;
     if (need == cnt) {
         Dw = U;
-        if (__any_sync(FULL, (U & ~Bw & pm) != 0u)) return;
+        // not canonical: the lowest attribute below j in the closure is the failure's witness
+        const uint32_t viol = U & ~Bw & pm;
+        const unsigned vb = __ballot_sync(FULL, viol != 0u);
+        if (vb) {
+            const int vw = __ffs(vb) - 1;
+            return 32 * vw + __ffs(__shfl_sync(FULL, viol, vw)) - 1;
+        }
     } else {
         // attributes that may still join: in U, not in B, not j; tested in ascending order
         uint32_t X = U & ~Bw;
@@ -165,7 +175,7 @@ __device__ __forceinline__ void finish_candidate(const ExpandArgs &a, const Dims
             const int k = u * 32 + b;
             if ((int)lane == u) X &= ~(1u << b);
             if (subset(k)) {
-                if (k < j) return;                      // not canonical
+                if (k < j) return k;                    // not canonical, k its witness
                 if ((int)lane == u) Dw |= 1u << b;
             }
         }
@@ -194,7 +204,7 @@ __device__ __forceinline__ void finish_candidate(const ExpandArgs &a, const Dims
         s = __shfl_sync(FULL, s, 0);
         if (s >= Q.cap) {
             if (lane == 0) atomicOr(&a.ctr->error, ERR_QUEUE0 << qi);
-            return;
+            return -1;
         }
         if (need < cnt) all_ids();
         __syncwarp();
@@ -211,16 +221,27 @@ __device__ __forceinline__ void finish_candidate(const ExpandArgs &a, const Dims
         s = __shfl_sync(FULL, s, 0);
         if (s >= X.cap) {
             if (lane == 0) atomicOr(&a.ctr->error, mid ? ERR_NEXT_MID : ERR_NEXT);
-            return;
+            return -1;
         }
         if ((int)cnt <= a.list_max) write_list(X.ext + s * (size_t)X.stride);
         else write_ext(X.ext + s * (size_t)X.stride);
-        // a mid-pool child inherits no failures from this tier
-        if (mid)
-            for (int i = (int)lane; i < a.wit_words; i += 32) X.ext[s * (size_t)X.stride + a.wit_off + i] = FULL;
         if (lane < (unsigned)d.wm) X.itt[s * d.wm + lane] = Dw;
         if (lane == 0) { X.y[s] = j + 1; X.n[s] = (int)cnt; }
+        if (INHERIT) {
+            // the child's inherited failures are written when the work item is done (past
+            // CHILD_SLOTS children of one item: none)
+            int ci = 0;
+            if (lane == 0) ci = atomicAdd(ccount, 1);
+            ci = __shfl_sync(FULL, ci, 0);
+            if (ci < CHILD_SLOTS) {
+                if (lane == 0) cslots[ci] = (uint32_t)s | (mid ? 0x80000000u : 0u);
+            } else {
+                uint32_t *w = X.ext + s * (size_t)X.stride + (mid ? a.wit_off : a.wit_off_big);
+                for (int i = (int)lane; i < a.wit_words; i += 32) w[i] = FULL;
+            }
+        }
     }
+    return -1;
 }
 
 // Parts per parent: each parent's attribute range is split when there are too few parents to fill
@@ -239,7 +260,7 @@ __host__ __device__ inline int expand_parts(unsigned long long p_count, unsigned
 // objects); each candidate's C is read from those columns without any global column access. Larger
 // extents keep the chunk list: each warp gathers column j on the parent's non-zero chunks. Either
 // way the warps of the block take the part's candidates j in turn.
-template <bool COUNT, int WARPS>
+template <bool COUNT, int WARPS, bool INHERIT>
 __global__ void __launch_bounds__(32 * WARPS, ExpandShape<WARPS>::blocks_per_sm) expand_bitmap_kernel(ExpandArgs a)
 {
     extern __shared__ __align__(16) unsigned char smem[];
@@ -271,10 +292,30 @@ __global__ void __launch_bounds__(32 * WARPS, ExpandShape<WARPS>::blocks_per_sm)
     const int span = (d.m + parts - 1) / parts;
     const unsigned long long items = p_count * (unsigned long long)parts;
     __shared__ unsigned long long next_item;
+    // inherited failures (the Fast Close-by-One rule): the parent's witness byte per attribute
+    // (0xff: none), updated by the item's own failures, and the level children that receive it
+    __shared__ uint32_t bwit[INHERIT ? WIT_WORDS_MAX : 1];
+    __shared__ uint32_t cslots[INHERIT ? CHILD_SLOTS : 1];
+    __shared__ int ccount;
+    const uint8_t *bwitb = reinterpret_cast<const uint8_t *>(bwit);
+    if (INHERIT && threadIdx.x == 0) ccount = 0;
     for (;;) {
         // work items are dealt one at a time from a launch-wide cursor, so the blocks that draw
         // large parents do not hold back the rest
         __syncthreads();
+        if (INHERIT) {
+            // the previous item's level children get its failures, now that all its candidates are done
+            const int nc = min(ccount, CHILD_SLOTS);
+            for (int e = (int)threadIdx.x; e < nc * a.wit_words; e += (int)blockDim.x) {
+                const int ci = e / a.wit_words, wi = e - ci * a.wit_words;
+                const uint32_t v = cslots[ci];
+                const bool to_mid = (v >> 31) != 0u;
+                const Level &X = to_mid ? a.next_mid : a.next;
+                X.ext[(size_t)(v & 0x7fffffffu) * X.stride + (to_mid ? a.wit_off : a.wit_off_big) + wi] = bwit[wi];
+            }
+            __syncthreads();
+            if (threadIdx.x == 0) ccount = 0;
+        }
         if (threadIdx.x == 0) next_item = atomicAdd(&a.ctr->work_head, 1ull);
         __syncthreads();
         const unsigned long long item = next_item;
@@ -300,9 +341,13 @@ __global__ void __launch_bounds__(32 * WARPS, ExpandShape<WARPS>::blocks_per_sm)
         __shared__ uint32_t sB[MAX_ATTRS / 32];
         if ((int)threadIdx.x < d.wm) sB[threadIdx.x] = P.itt[p * d.wm + threadIdx.x];
         const uint32_t *B = sB;
+        if (INHERIT) {
+            const uint32_t *ws = P.ext + p * (size_t)P.stride + (second ? a.wit_off : a.wit_off_big);
+            for (int i = (int)threadIdx.x; i < a.wit_words; i += (int)blockDim.x) bwit[i] = ws[i];
+        }
 
         // ---- stage the non-zero chunks of A in order (block-wide compaction), and |A|
-        const uint4 *A4 = reinterpret_cast<const uint4 *>(P.ext) + p * wq;   // a bitmap entry: big pool
+        const uint4 *A4 = reinterpret_cast<const uint4 *>(P.ext + p * (size_t)P.stride);   // a bitmap entry: big pool
         __syncthreads();
         int nnz = 0, na = 0;
         for (int base = 0; base < (is_list ? 0 : wq); base += blockDim.x) {
@@ -367,6 +412,12 @@ __global__ void __launch_bounds__(32 * WARPS, ExpandShape<WARPS>::blocks_per_sm)
             for (int j = j_lo + wib; j < j_hi; j += wpb) {
                 if ((B[j >> 5] >> (j & 31)) & 1u) continue;   // saturation: A inside column j
                 ++my_closures;
+                if (INHERIT) {
+                    // j failed at an ancestor with a witness k < j in its closure: while k stays
+                    // outside B, the closure here (of a subset of that extent) holds k again
+                    const unsigned w = bwitb[j];
+                    if (w != 0xffu && !((B[w >> 5] >> (w & 31)) & 1u)) continue;
+                }
                 uint32_t c[RPL];
                 unsigned cnt = 0;
 #pragma unroll
@@ -406,7 +457,7 @@ __global__ void __launch_bounds__(32 * WARPS, ExpandShape<WARPS>::blocks_per_sm)
                 const unsigned need = cnt < (unsigned)ROW_BOUND ? cnt : (unsigned)ROW_BOUND;
                 collect(need);
                 __syncwarp();
-                finish_candidate<COUNT>(
+                const int wk = finish_candidate<COUNT, INHERIT>(
                     a, d, B, j, cnt, need,
                     [&](unsigned i, int w) {
                         const uint32_t p = rids[i];
@@ -461,7 +512,8 @@ __global__ void __launch_bounds__(32 * WARPS, ExpandShape<WARPS>::blocks_per_sm)
                         }
                     },
                     [&]() { collect(cnt); },
-                    my_bytes);
+                    my_bytes, cslots, &ccount);
+                if (INHERIT && lane == 0) reinterpret_cast<uint8_t *>(bwit)[j] = wk >= 0 ? (uint8_t)wk : 0xffu;
                 __syncwarp();
             }
             continue;
@@ -471,6 +523,10 @@ __global__ void __launch_bounds__(32 * WARPS, ExpandShape<WARPS>::blocks_per_sm)
         for (int j = j_lo + wib; j < j_hi; j += wpb) {
             if ((B[j >> 5] >> (j & 31)) & 1u) continue;   // saturation: A inside column j
             ++my_closures;
+            if (INHERIT) {
+                const unsigned w = bwitb[j];
+                if (w != 0xffu && !((B[w >> 5] >> (w & 31)) & 1u)) continue;
+            }
 
             // |C| for C = A & column j on the chunks of A (C itself is recomputed when needed)
             const uint4 *J4 = cols4 + (size_t)j * wq;
@@ -518,7 +574,7 @@ __global__ void __launch_bounds__(32 * WARPS, ExpandShape<WARPS>::blocks_per_sm)
                 got += __shfl_sync(FULL, incl, 31);
             }
             __syncwarp();
-            finish_candidate<COUNT>(
+            const int wk = finish_candidate<COUNT, INHERIT>(
                 a, d, B, j, cnt, need,
                 [&](unsigned i, int w) { return __ldg(a.rows + (size_t)gids[i] * d.wm + w); },
                 [&](unsigned i) { return gids[i]; },
@@ -568,7 +624,8 @@ __global__ void __launch_bounds__(32 * WARPS, ExpandShape<WARPS>::blocks_per_sm)
                     }
                 },
                 [&]() {},
-                my_bytes);
+                my_bytes, cslots, &ccount);
+            if (INHERIT && lane == 0) reinterpret_cast<uint8_t *>(bwit)[j] = wk >= 0 ? (uint8_t)wk : 0xffu;
             __syncwarp();
         }
     }
@@ -604,7 +661,7 @@ int list_max_for(const Dims &d)
     return lim > SMALL_MAX ? (int)lim : 0;
 }
 
-template <bool COUNT, int WARPS>
+template <bool COUNT, int WARPS, bool INHERIT>
 static int launch_expand_t(const ExpandArgs &a, int sm_count, void *stream)
 {
     int wpb = WARPS;
@@ -619,12 +676,12 @@ static int launch_expand_t(const ExpandArgs &a, int sm_count, void *stream)
     cudaGetDevice(&dev);
     if (cache.dev != dev || cache.smem != smem || cache.wpb != wpb) {
         if (smem > 48 * 1024) {
-            cudaError_t e = cudaFuncSetAttribute(expand_bitmap_kernel<COUNT, WARPS>,
+            cudaError_t e = cudaFuncSetAttribute(expand_bitmap_kernel<COUNT, WARPS, INHERIT>,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) return (int)e;
         }
         int ps = 0;
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ps, expand_bitmap_kernel<COUNT, WARPS>, wpb * 32, smem);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&ps, expand_bitmap_kernel<COUNT, WARPS, INHERIT>, wpb * 32, smem);
         cache = ShapeCache{dev, smem, wpb, ps < 1 ? 1 : ps};
     }
     const int per_sm = cache.per_sm;
@@ -645,16 +702,22 @@ static int launch_expand_t(const ExpandArgs &a, int sm_count, void *stream)
     // leave at once)
     unsigned long long blocks = on_device ? resident : std::min<unsigned long long>(items, resident);
     if (blocks < 1) blocks = 1;
-    expand_bitmap_kernel<COUNT, WARPS><<<(unsigned)blocks, wpb * 32, smem, (cudaStream_t)stream>>>(b);
+    expand_bitmap_kernel<COUNT, WARPS, INHERIT><<<(unsigned)blocks, wpb * 32, smem, (cudaStream_t)stream>>>(b);
     return (int)cudaGetLastError();
 }
 
 int launch_expand(const ExpandArgs &a, int sm_count, void *stream)
 {
     // wide blocks for many attributes, or for levels too small to fill the GPU with narrow blocks
+#define FCA_EXPAND(W)                                                                               \
+    (a.wit_words > 0 ? (a.count_work ? launch_expand_t<true, W, true>(a, sm_count, stream)              \
+                                     : launch_expand_t<false, W, true>(a, sm_count, stream))            \
+                     : (a.count_work ? launch_expand_t<true, W, false>(a, sm_count, stream)             \
+                                     : launch_expand_t<false, W, false>(a, sm_count, stream)))
     if (a.d.m >= WIDE_EXPAND_MIN_ATTRS || a.p_count + a.p_count2 < 2ull * 3 * (unsigned long long)sm_count)
-        return a.count_work ? launch_expand_t<true, 16>(a, sm_count, stream) : launch_expand_t<false, 16>(a, sm_count, stream);
-    return a.count_work ? launch_expand_t<true, 8>(a, sm_count, stream) : launch_expand_t<false, 8>(a, sm_count, stream);
+        return FCA_EXPAND(16);
+    return FCA_EXPAND(8);
+#undef FCA_EXPAND
 }
 
 }  // namespace fca

@@ -134,7 +134,8 @@ struct ExpandArgs {
     int wit_off;            // mid-pool entries: word offset, inside the entry's slot, of its inherited
                             // failures (one byte per attribute: the witness of a candidate that failed
                             // at an ancestor, 0xff for none); 0 when they are not kept
-    int wit_words;          // words of those bytes
+    int wit_words;          // words of those bytes (0: failures are not inherited)
+    int wit_off_big;        // the same offset in a big-pool entry (after its W_Np extent words)
     Queue q[NQ];            // children with <= 32 << q objects
     uint32_t *out;          // capacity x wm
     uint64_t capacity;

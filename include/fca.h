@@ -44,7 +44,11 @@ typedef enum {
  * side by side count once). */
 typedef struct {
     uint64_t concepts;         /* intents found (= *out_count) */
-    uint64_t closures;         /* candidates (A, B, j) evaluated: j >= cursor, j not in B */
+    uint64_t closures;         /* candidates (A, B, j) considered: j >= cursor, j not in B (with
+                                  M <= 256 the bitmap and mid tiers skip the closure of a candidate
+                                  whose failure a search-tree ancestor recorded with a witness still
+                                  outside B, the Fast Close-by-One rule; such candidates are counted
+                                  here too; FCA_NO_INHERIT=1 in the environment turns the rule off) */
     uint64_t large_parents;    /* search nodes of more than 64 objects (list- and bitmap-tier kernels) */
     uint64_t small_roots;      /* subtrees handed to the object-list kernels (extent <= 64) */
     uint64_t launches;         /* kernels launched by the call */
