@@ -300,6 +300,15 @@ def probe_peaks():
 WORK_FILE = os.path.join(ROOT, "tests", "golden", "work_counts.json")
 
 
+def load_cover_counts(workload: str):
+    """Work of the lower-cover search over a workload's intent set, written by
+    tests/golden/make_work_counts.py --covers, or None."""
+    try:
+        return json.load(open(WORK_FILE))[workload].get("covers")
+    except (OSError, ValueError, KeyError):
+        return None
+
+
 def load_work_counts(workload: str, order: str, mid_max: int, list_max: int):
     """Per-tier algorithmic work of a workload, written by tests/golden/make_work_counts.py, when it
     was counted over the attribute order the library processes ("natural" or "support") and with
@@ -603,9 +612,29 @@ def run_lattice(args, world, rank, local):
     else:
         result["edges"] = n_edges
         result["edges_per_s"] = n_edges * args.steps * world / total_s
-        result["roofline"] = None
-        result["roofline_note"] = ("covers_kernel has no counted algorithmic work yet: its cost is "
-                                   "containment tests between attribute sets restricted to each extent")
+        # algorithmic work of the lower-cover search over the whole intent set (oracle/coverwork.c,
+        # stored by tests/golden/make_work_counts.py --covers): per concept its extent, the
+        # intersections A & column k for k outside B, the closure of each non-empty one by rows
+        cw = load_cover_counts(w.name)
+        if cw is not None and cw.get("concepts") == k:
+            sm_count = torch.cuda.get_device_properties(dev).multi_processor_count
+            sm_max = float(peaks.get("sm_max_mhz", 2070.0))
+            probes = probe_peaks() if rank == 0 else {}
+            hbm_peak = float(peaks.get("hbm_gbs", 6800.0))
+            hbm_basis = "MEASURED_PEAKS.json hbm_gbs" if "hbm_gbs" in peaks else "fallback 6.8 TB/s"
+            l2_peak = probes.get("l2_read_gbs") or hbm_peak
+            int_peak = sm_count * INT_LANES_PER_SM * sm_max * 1e6 / 1e9
+            ops = cw["extent_words"] + cw["isect_words"] + cw["closure_words"]
+            hbm_b = 4.0 * k * wm + 8.0 * n_edges                 # intents read, edges written
+            l2_b = 4.0 * (cw["isect_words"] + cw["closure_words"])   # column and row words
+            r = bound_of(hbm_b, l2_b, ops, 1, mean_ms, hbm_peak, hbm_basis, l2_peak, int_peak, sm_count, sm_max)
+            result["roofline"] = {"kernel": "covers_kernel", **r,
+                                  "traffic": profile_traffic("covers_kernel", w.name),
+                                  "basis": "algorithmic work of the lower-cover search (oracle/coverwork.c); "
+                                           "time: library events around the hash-insert and covers launches"}
+        else:
+            result["roofline"] = None
+            result["roofline_note"] = "no stored cover-search work counts for this workload"
     ctx.close()
     return result
 

@@ -225,3 +225,56 @@ def test_lean_model(list_max):
         assert big["l2_lean_words"] == big["isect_words"] + big["closure_words"]
     assert got["list"]["hbm_lean_words"] < got["list"]["hbm_words"]
     assert got["list"]["hbm_lean_words"] >= got["list"]["children"] * ((m + 31) // 32)
+
+
+# ---- lower-cover search (oracle/coverwork.c)
+
+def python_coverwork(rows: np.ndarray, n: int, m: int, intents: np.ndarray):
+    """The cover-search counts restated from their definitions, with plain Python integers as
+    bitsets: per concept (A, B), W_N extent words, (M - |B|) * nnzw(A) intersection words, and
+    |C_k| * W_M closure words for every k outside B with C_k = A & column k non-empty."""
+    wn, wm = (n + 31) // 32, (m + 31) // 32
+    row_bits = []
+    for o in range(n):
+        v = 0
+        for w in range(wm):
+            v |= int(rows[o, w]) << (32 * w)
+        row_bits.append(v & ((1 << m) - 1))
+    out = {"concepts": 0, "extent_words": 0, "isect_words": 0, "closure_words": 0}
+    for r in range(intents.shape[0]):
+        b = 0
+        for w in range(wm):
+            b |= int(intents[r, w]) << (32 * w)
+        ext = [o for o in range(n) if row_bits[o] & b == b]
+        nnzw = len({o // 32 for o in ext})
+        out["concepts"] += 1
+        out["extent_words"] += wn
+        out["isect_words"] += (m - bin(b).count("1")) * nnzw
+        for k in range(m):
+            if (b >> k) & 1:
+                continue
+            ck = sum(1 for o in ext if (row_bits[o] >> k) & 1)
+            out["closure_words"] += ck * wm
+    return out
+
+
+def test_coverwork_hand_worked():
+    """Two objects with one attribute each: concepts {} (both objects), {a0}, {a1}, {a0, a1} (no
+    object). Intersections: 2 + 1 + 1 + 0 words; closures: the two singletons under {} only."""
+    from oracle.workcount import coverwork
+    rows = np.array([[0b01], [0b10]], dtype=np.uint32)
+    intents = np.array([[0b00], [0b01], [0b10], [0b11]], dtype=np.uint32)
+    assert coverwork(rows, 2, 2, intents) == {"concepts": 4, "extent_words": 4, "isect_words": 4,
+                                               "closure_words": 2}
+
+
+@pytest.mark.parametrize("n,m,p,seed", [(40, 12, 0.3, 1), (70, 33, 0.2, 2), (100, 40, 0.15, 3)])
+def test_coverwork_matches_python_restatement(n, m, p, seed):
+    """The C count against the Python restatement on the oracle's full intent set, across word
+    boundaries of N and M, and independent of the thread split and of the order of the intents."""
+    from oracle.workcount import coverwork
+    rows = cx.random_context(n, m, p, seed)
+    intents = oracle.cbo(rows, n, m)["intents"]
+    want = python_coverwork(rows, n, m, intents)
+    assert coverwork(rows, n, m, intents, threads=1) == want
+    assert coverwork(rows, n, m, intents[::-1].copy(), threads=3) == want
