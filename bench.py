@@ -13,7 +13,10 @@ table (100 000 x 256, 519 340 217 concepts).
 
 Prints one JSON line (rank 0). With N > 1 (torchrun), every rank enumerates its
 own copy of the workload (independent replicas, no collective on the data
-path); value = concepts of all ranks / slowest rank's time.
+path); value = concepts of all ranks / slowest rank's time. The timed steps
+reuse the context's work pools; `first_call_ms` is the first enumeration on a
+fresh context (pools allocated and levels planned inside the call), reported
+beside them.
 """
 from __future__ import annotations
 
@@ -520,7 +523,18 @@ def run_ours(args, world, rank, local):
         "clocks": clocks,
         "probes": probes,
     }
+    # the first call on a fresh context (the work pools allocated and the levels planned inside the
+    # call), which a caller with a new table pays once; the timed steps reuse the context's pools
     ctx.close()
+    del pin_out, pin_out_np
+    torch.cuda.synchronize(dev)
+    fresh = fca.Context(rows_dev, w.n_objects, w.n_attrs)
+    torch.cuda.synchronize(dev)
+    t_first = time.perf_counter()
+    fresh.enumerate_into(out, concepts, stream=stream)
+    torch.cuda.synchronize(dev)
+    result["first_call_ms"] = (time.perf_counter() - t_first) * 1e3
+    fresh.close()
     return result
 
 
