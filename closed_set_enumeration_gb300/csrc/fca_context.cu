@@ -200,14 +200,26 @@ __global__ void __launch_bounds__(256) unpermute_tiles_kernel(uint32_t *out, uns
     }
     const unsigned long long total = ctr->out_count < capacity ? ctr->out_count : capacity;
     const unsigned long long nwarps = (unsigned long long)gridDim.x * (blockDim.x >> 5);
+    // rows of a multiple of 4 words in a 16-byte aligned buffer move as uint4
+    const bool vec = (wm & 3) == 0 && (reinterpret_cast<uintptr_t>(out) & 15) == 0;
     for (unsigned long long r0 = start + 32ull * ((unsigned long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5));
          r0 < total; r0 += 32ull * nwarps) {
         const unsigned long long r = r0 + lane;
         const bool mine = r < total;
         uint32_t *row = out + r * (unsigned long long)wm;
         uint32_t t[WMAX];
+        if (vec) {
+            // whole rows of 4-word groups, 16-byte aligned: one vector load per group
 #pragma unroll
-        for (int q = 0; q < WMAX; ++q) t[q] = (mine && q < wm) ? row[q] : 0u;
+            for (int q = 0; q < WMAX; q += 4) {
+                uint4 x = make_uint4(0u, 0u, 0u, 0u);
+                if (mine && q < wm) x = *reinterpret_cast<const uint4 *>(row + q);
+                t[q] = x.x; t[q + 1] = x.y; t[q + 2] = x.z; t[q + 3] = x.w;
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < WMAX; ++q) t[q] = (mine && q < wm) ? row[q] : 0u;
+        }
 #pragma unroll
         for (int q = 0; q < WMAX; ++q)
             if (q < wm) t[q] = warp_transpose32(t[q]);
@@ -227,10 +239,16 @@ __global__ void __launch_bounds__(256) unpermute_tiles_kernel(uint32_t *out, uns
         }
 #pragma unroll
         for (int w = 0; w < WMAX; ++w)
-            if (w < wm) {
-                const uint32_t x = warp_transpose32(o[w]);
-                if (mine) row[w] = x;
-            }
+            if (w < wm) o[w] = warp_transpose32(o[w]);
+        if (vec) {
+#pragma unroll
+            for (int w = 0; w < WMAX; w += 4)
+                if (mine && w < wm) *reinterpret_cast<uint4 *>(row + w) = make_uint4(o[w], o[w + 1], o[w + 2], o[w + 3]);
+        } else {
+#pragma unroll
+            for (int w = 0; w < WMAX; ++w)
+                if (mine && w < wm) row[w] = o[w];
+        }
     }
 }
 

@@ -374,3 +374,30 @@ def test_list_tier_modes(case, mode, monkeypatch):
         assert st["list_max"] > 64
     if mode in ("mid_kernel", "mid_kernel_no_inherit", "default"):
         assert st["mid_max"] == min(256, st["list_max"])
+
+
+@pytest.mark.parametrize("m", [128, 256, 96])
+def test_output_buffer_alignment(m):
+    """The output rows are mapped back to attribute order in place, with 16-byte vector accesses when
+    the rows are a multiple of four words and the caller's buffer is 16-byte aligned, word by word
+    otherwise: a buffer that starts 4 bytes past an aligned address must give the same rows, and
+    the word before it must stay untouched."""
+    import torch
+    from closed_set_enumeration_gb300 import fca
+    n = 3000
+    rows = cx.random_context(n, m, 0.04, 7)
+    ref = oracle.cbo(rows, n, m, threads=8)["intents"]
+    wm = (m + 31) // 32
+    k = ref.shape[0]
+    for offset in (0, 1):
+        buf = torch.full((k * wm + offset + 1,), -7, dtype=torch.int32, device="cuda")
+        out = buf[offset:offset + k * wm].view(k, wm)
+        with fca.Context(rows, n, m) as ctx:
+            st, cnt = ctx.enumerate_into(out, k)
+        assert st == fca.FCA_OK and cnt == k
+        got = out.cpu().numpy().view(np.uint32)
+        assert same_set(got, ref)
+        host = buf.cpu().numpy()
+        if offset:
+            assert host[0] == -7
+        assert host[-1] == -7
