@@ -213,6 +213,11 @@ void free_pools(fca_ctx *c)
 fca_status make_level(fca_ctx *c, Level *L, uint64_t cap, int64_t stride)
 {
     const Dims &d = c->d;
+    // the level kernels record child slots in 31 bits (the inherited-failure patch lists)
+    if (cap >= (1ull << 31)) {
+        c->err = "level pool capacity past 2^31 entries";
+        return FCA_ERR_OOM;
+    }
     Level n{};
     n.cap = cap;
     n.stride = stride;
