@@ -297,7 +297,9 @@ fca_status ensure_queues(fca_ctx *c)
 fca_status grow_level(fca_ctx *c, size_t idx, bool mid, uint64_t need, cudaStream_t st)
 {
     Level &L = mid ? c->mids[idx] : c->levels[idx];
-    const uint64_t cap = std::max<uint64_t>(2 * L.cap, need + need / 4);
+    constexpr uint64_t CAP_MAX = (1ull << 31) - 1;   // see make_level
+    if (need > CAP_MAX) return FCA_ERR_CAPACITY;
+    const uint64_t cap = std::min<uint64_t>(CAP_MAX, std::max<uint64_t>(2 * L.cap, need + need / 4));
     const uint64_t eb = mid ? mid_entry_bytes(c) : level_entry_bytes(c);
     if (c->pool_bytes + (cap - L.cap) * eb > c->pool_limit) return FCA_ERR_CAPACITY;
     Level n{};
