@@ -753,8 +753,11 @@ __device__ void dfs_smem(SubtreeWarp &S, int R, int n, int jn, int slices, int s
 
 // SHARE: the block's warps hand parts of long searches to warps that have run out of work items
 // (the block-shared header comes first in shared memory); without it a warp ends when the items do.
+// Four blocks per SM (64 registers) except for the 33-64-object kernel with eight register words,
+// which needs about 80 and whose shared memory allows three blocks anyway; the 1-32-object one fits
+// four in shared memory and runs faster there in spite of a few spilled registers.
 template <int NW, bool COUNT, int RW, bool SHARE>
-__global__ void __launch_bounds__(256, RW > 4 ? 3 : 4) subtree_kernel(const __grid_constant__ SubtreeArgs a)
+__global__ void __launch_bounds__(256, (RW > 4 && NW > 1) ? 3 : 4) subtree_kernel(const __grid_constant__ SubtreeArgs a)
 {
     // a launch queued before the host knew whether the bitmap search had ended cleanly
     if (a.guard && (a.ctr->error != 0u || a.ctr->next_count != 0ull)) return;
