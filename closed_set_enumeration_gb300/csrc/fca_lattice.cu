@@ -3,7 +3,10 @@
 // the lattice's edges are rebuilt afterwards by extent inclusion; Parallel FCBO article, section 3.4).
 //
 //  extents_kernel      A = B' for each given attribute set B: the AND of the columns of B's
-//                      attributes (every object for the empty set). One thread per output word.
+//                      attributes (every object for the empty set). Short extents (W_N <= 16):
+//                      a group of lanes per intent, one output word per lane; longer ones: a warp
+//                      per intent, the rarest column first, then four columns per step over 128
+//                      words at a time, until every lane holds zero words.
 //  hash_insert_kernel  an open-addressing table from intent to row index (linear probing).
 //  covers_kernel       the lower covers of each concept (A, B), one warp per concept. For k not in
 //                      B let C_k = A & column k. The extents of the lower covers are exactly the
