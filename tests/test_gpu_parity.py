@@ -401,3 +401,27 @@ def test_output_buffer_alignment(m):
         if offset:
             assert host[0] == -7
         assert host[-1] == -7
+
+
+@pytest.mark.parametrize("mid_min", [None, "1"])
+def test_inherited_failures_past_the_child_lists(mid_min, monkeypatch):
+    """A mid-tier node with more level children than a node records for its inherited failures
+    (32 per mid node, 64 per bitmap-tier work item): the 200 objects holding attribute 0 form a node
+    of the mid tier (9 000 objects, so id lists reach 256) whose 36 candidates are held by 80 of them
+    each, so most of its children are mid-tier nodes again. Those past the recorded ones inherit no
+    failures; the intents and the closure count must still be the oracle's, with the mid kernel on
+    every mid level (FCA_MID_MIN=1) and with the default choice."""
+    if mid_min:
+        monkeypatch.setenv("FCA_MID_MIN", mid_min)
+    rng = np.random.default_rng(11)
+    n, m = 9000, 64
+    cells = np.zeros((n, m), dtype=bool)
+    cells[:200, 0] = True
+    for a in range(1, 37):
+        cells[rng.choice(200, 80, replace=False), a] = True
+    cells[200:, 50:] = rng.random((n - 200, 14)) < 0.1
+    rows = cx.pack_rows(cells)
+    _, st = check_against_oracle(rows, n, m, threads=8)
+    assert st["mid_max"] == 256
+    if mid_min:
+        assert st["mid_launches"] > 0
