@@ -82,6 +82,12 @@ struct fca_ctx {
     size_t pool_limit = 0;          // growth stops here; levels are then split into chunks
     uint64_t level_bytes = 0, queue_entries = 0;   // initial pool sizes
     int count_work = 0;
+    // growth ahead of a level launch (unchained levels): the destinations are grown to what the
+    // previous launch's children per parent predict for this one, so that a first call on a table
+    // does not overflow and re-run most of its levels (FCA_PREGROW=0 turns it off)
+    int pregrow = 1;
+    bool ratio_known = false;
+    double ratio_big = 0, ratio_mid = 0, ratio_q[NQ]{};
     // extents of SMALL_MAX < n <= list_max objects are stored as object-id lists; those of at most
     // mid_max objects are kept in the mid pools (slots of mid_stride words) and expanded one per warp
     // by the mid-tier kernel (0: off)
@@ -294,14 +300,15 @@ fca_status ensure_queues(fca_ctx *c)
 
 // Grow a pool of level `idx` (the mid pool when `mid`) to hold at least `need` entries, keeping its
 // current entries. Returns FCA_ERR_CAPACITY (nothing changed) when that would pass the pool limit.
-fca_status grow_level(fca_ctx *c, size_t idx, bool mid, uint64_t need, cudaStream_t st)
+fca_status grow_level(fca_ctx *c, size_t idx, bool mid, uint64_t need, cudaStream_t st, size_t limit = 0)
 {
     Level &L = mid ? c->mids[idx] : c->levels[idx];
     constexpr uint64_t CAP_MAX = (1ull << 31) - 1;   // see make_level
     if (need > CAP_MAX) return FCA_ERR_CAPACITY;
-    const uint64_t cap = std::min<uint64_t>(CAP_MAX, std::max<uint64_t>(2 * L.cap, need + need / 4));
+    // an overflow grows with headroom; a growth ahead of a launch (limit given) to the prediction
+    const uint64_t cap = limit ? need : std::min<uint64_t>(CAP_MAX, std::max<uint64_t>(2 * L.cap, need + need / 4));
     const uint64_t eb = mid ? mid_entry_bytes(c) : level_entry_bytes(c);
-    if (c->pool_bytes + (cap - L.cap) * eb > c->pool_limit) return FCA_ERR_CAPACITY;
+    if (c->pool_bytes + (cap - L.cap) * eb > (limit ? limit : c->pool_limit)) return FCA_ERR_CAPACITY;
     Level n{};
     fca_status s = make_level(c, &n, cap, L.stride);
     if (s != FCA_OK) return s;
@@ -319,12 +326,12 @@ fca_status grow_level(fca_ctx *c, size_t idx, bool mid, uint64_t need, cudaStrea
 }
 
 // Grow (empty) queue qi to hold at least `need` entries.
-fca_status grow_queue(fca_ctx *c, int qi, uint64_t need, cudaStream_t st)
+fca_status grow_queue(fca_ctx *c, int qi, uint64_t need, cudaStream_t st, size_t limit = 0)
 {
     Queue &Q = c->q[qi];
-    const uint64_t cap = std::max<uint64_t>(2 * Q.cap, need + need / 4);
+    const uint64_t cap = limit ? need : std::max<uint64_t>(2 * Q.cap, need + need / 4);
     const uint64_t eb = queue_entry_bytes(c->d, qi);
-    if (c->pool_bytes + (cap - Q.cap) * eb > c->pool_limit) return FCA_ERR_CAPACITY;
+    if (c->pool_bytes + (cap - Q.cap) * eb > (limit ? limit : c->pool_limit)) return FCA_ERR_CAPACITY;
     Queue n{};
     fca_status s = make_queue(c, &n, qi, cap);
     if (s != FCA_OK) return s;
@@ -674,6 +681,30 @@ fca_status drain(Run &r, size_t lv, bool chain)
         const uint64_t hb = c->level_count[lv], hm = c->mid_count[lv];
         const uint64_t kb = std::min(hb, kmax), km = std::min(hm, kmax);
         const uint64_t bb = hb - kb, bm = hm - km;
+        if (c->pregrow && c->ratio_known) {
+            // what the previous launch's children per parent predict for this one, with a margin,
+            // allocated exactly and only while all pools stay within half the pool limit (a wrong
+            // prediction must not take the memory that the overflow path below may need)
+            const double parents = (double)(kb + km);
+            const size_t lim = c->pool_limit / 2;
+            auto want = [&](uint64_t have, double ratio) { return have + (uint64_t)(1.25 * ratio * parents) + 16; };
+            uint64_t need = want(c->level_count[lv + 1], c->ratio_big);
+            if (need > c->levels[lv + 1].cap && (s = grow_level(c, lv + 1, false, need, r.st, lim)) != FCA_OK &&
+                s != FCA_ERR_CAPACITY)
+                return s;
+            if (c->mid_max > SMALL_MAX) {
+                need = want(c->mid_count[lv + 1], c->ratio_mid);
+                if (need > c->mids[lv + 1].cap && (s = grow_level(c, lv + 1, true, need, r.st, lim)) != FCA_OK &&
+                    s != FCA_ERR_CAPACITY)
+                    return s;
+            }
+            for (int qi = 0; qi < NQ; ++qi) {
+                need = want(c->q_count[qi], c->ratio_q[qi]);
+                if (need > c->q[qi].cap && (s = grow_queue(c, qi, need, r.st, lim)) != FCA_OK &&
+                    s != FCA_ERR_CAPACITY)
+                    return s;
+            }
+        }
 
         // the next level appends after its current fills; the counters as they are then are kept on
         // the device, to be restored if the launch has to be rolled back (one small kernel)
@@ -718,6 +749,13 @@ fca_status drain(Run &r, size_t lv, bool chain)
                 kmax = std::max<uint64_t>(1, std::max(kb, km) / 2);
             }
             continue;
+        }
+        if (kb + km > 0) {
+            const double parents = (double)(kb + km);
+            c->ratio_big = (double)(after.next_count - c->level_count[lv + 1]) / parents;
+            c->ratio_mid = (double)(after.next_mid - c->mid_count[lv + 1]) / parents;
+            for (int qi = 0; qi < NQ; ++qi) c->ratio_q[qi] = (double)(after.q_count[qi] - c->q_count[qi]) / parents;
+            c->ratio_known = true;
         }
         c->level_count[lv] = bb;
         c->mid_count[lv] = bm;
@@ -877,6 +915,7 @@ fca_status enumerate_impl(fca_ctx *c, uint32_t *out, uint64_t capacity, uint64_t
     if ((s = ensure_level(c, 0)) != FCA_OK) return s;
     for (size_t i = 0; i < c->levels.size(); ++i) c->level_count[i] = c->mid_count[i] = 0;
     for (int qi = 0; qi < NQ; ++qi) c->q_count[qi] = c->last_q[qi] = 0;
+    c->ratio_known = false;
 
     Run r{c, out, capacity, st};
     const Dims &d = c->d;
@@ -1089,6 +1128,10 @@ fca_status fca_context_create(const uint32_t *rows, int64_t n_objects, int32_t n
         free_b = (size_t)8 << 30;
     }
     c->level_bytes = env_u64("FCA_LEVEL_BYTES", 64ull << 20);
+    {
+        const char *v = getenv("FCA_PREGROW");
+        c->pregrow = !(v && v[0] == '0' && v[1] == 0);
+    }
     c->queue_entries = env_u64("FCA_QUEUE_ENTRIES", 1ull << 18);
     c->pool_limit = (size_t)env_u64("FCA_POOL_LIMIT_BYTES", free_b / 2);
     c->wait_ns = env_u64("FCA_WAIT_LIMIT_NS", 0);

@@ -230,6 +230,7 @@ def test_small_pools_roll_back_and_chunk(monkeypatch, limit):
     ref = oracle.cbo(rows, n, m, threads=8)
     monkeypatch.setenv("FCA_LEVEL_BYTES", "1")       # floor: 4*M entries per level
     monkeypatch.setenv("FCA_QUEUE_ENTRIES", "1")     # floor: 4*M entries per queue
+    monkeypatch.setenv("FCA_PREGROW", "0")           # no growth ahead of the launches
     if limit:
         monkeypatch.setenv("FCA_POOL_LIMIT_BYTES", limit)
     # output sized up front: a capacity miss would re-run the enumeration on the pools the first
@@ -257,6 +258,7 @@ def test_chained_levels_roll_back(monkeypatch):
     ref_b = oracle.cbo(rows_b, n, m, threads=8)
     monkeypatch.setenv("FCA_LEVEL_BYTES", "1")
     monkeypatch.setenv("FCA_QUEUE_ENTRIES", "1")
+    monkeypatch.setenv("FCA_PREGROW", "0")
     wm = (m + 31) // 32
     with fca.Context(rows_a, n, m) as ctx:
         got = ctx.enumerate(capacity=ref_a["intents"].shape[0] + 1).cpu().numpy().view(np.uint32).reshape(-1, wm)
@@ -425,3 +427,28 @@ def test_inherited_failures_past_the_child_lists(mid_min, monkeypatch):
     assert st["mid_max"] == 256
     if mid_min:
         assert st["mid_launches"] > 0
+
+
+def test_growth_ahead_of_launches():
+    """With tiny initial pools, the first call grows each level's destinations ahead of its launch
+    from the previous launch's children per parent: fewer launches are rolled back than without it
+    (FCA_PREGROW=0), and the intents and closures are the oracle's either way."""
+    n, m = 4000, 60
+    rows = cx.random_context(n, m, 0.12, 12)
+    rows[: n // 4, 0] |= np.uint32(0x00FF00FF)
+    ref = oracle.cbo(rows, n, m, threads=8)
+    retries = {}
+    for mode in ("1", "0"):
+        mp = pytest.MonkeyPatch()
+        mp.setenv("FCA_LEVEL_BYTES", "1")
+        mp.setenv("FCA_QUEUE_ENTRIES", "1")
+        mp.setenv("FCA_PREGROW", mode)
+        try:
+            got, st = gpu_run(rows, n, m, capacity=ref["intents"].shape[0] + 1)
+        finally:
+            mp.undo()
+        assert not has_duplicates(got)
+        assert same_set(got, ref["intents"])
+        assert st["closures"] == ordered_closures(rows, n, m, threads=8)
+        retries[mode] = st["retries"]
+    assert retries["1"] < retries["0"]
