@@ -87,6 +87,7 @@ struct fca_ctx {
     // does not overflow and re-run most of its levels (FCA_PREGROW=0 turns it off)
     int pregrow = 1;
     bool ratio_known = false;
+    size_t ratio_lv = 0;            // level whose launch gave the ratios
     double ratio_big = 0, ratio_mid = 0, ratio_q[NQ]{};
     // extents of SMALL_MAX < n <= list_max objects are stored as object-id lists; those of at most
     // mid_max objects are kept in the mid pools (slots of mid_stride words) and expanded one per warp
@@ -146,6 +147,9 @@ constexpr double ORDER_MIN_CV = 0.25;
 constexpr long long SEARCH_BUDGET_CYCLES = 200000;
 // Roots each spill queue holds.
 constexpr uint64_t SPILL_CAP = 1ull << 16;
+// Levels of at least this many parents are first launched on an eighth of them when their children
+// per parent are not known yet (the first call on a table)
+constexpr uint64_t PROBE_MIN_PARENTS = 1ull << 16;
 
 uint64_t env_u64(const char *name, uint64_t dflt)
 {
@@ -679,32 +683,49 @@ fca_status drain(Run &r, size_t lv, bool chain)
     while (!level_empty(c, lv)) {
         if ((s = ensure_level(c, lv + 1)) != FCA_OK) return s;
         const uint64_t hb = c->level_count[lv], hm = c->mid_count[lv];
-        const uint64_t kb = std::min(hb, kmax), km = std::min(hm, kmax);
-        const uint64_t bb = hb - kb, bm = hm - km;
-        if (c->pregrow && c->ratio_known) {
-            // what the previous launch's children per parent predict for this one, with a margin,
-            // allocated exactly and only while all pools stay within half the pool limit (a wrong
-            // prediction must not take the memory that the overflow path below may need)
-            const double parents = (double)(kb + km);
-            const size_t lim = c->pool_limit / 2;
-            auto want = [&](uint64_t have, double ratio) { return have + (uint64_t)(1.25 * ratio * parents) + 16; };
+        uint64_t kb = std::min(hb, kmax), km = std::min(hm, kmax);
+        const bool same_level = c->ratio_known && c->ratio_lv == lv;
+        // Growth ahead of the launch: what the last launch's children per parent predict for `par`
+        // parents, with a margin, allocated exactly. A prediction from an earlier part of the same
+        // level may use the whole pool limit; one from the previous level only half of it (a wrong
+        // prediction must not take the memory that the overflow path below may need). Returns
+        // whether some destination could not be grown that far.
+        auto grow_ahead = [&](double par, bool same, bool *refused) -> fca_status {
+            const size_t lim = same ? c->pool_limit : c->pool_limit / 2;
+            const double margin = same ? 1.5 : 1.25;
+            auto want = [&](uint64_t have, double ratio) { return have + (uint64_t)(margin * ratio * par) + 16; };
+            auto note = [&](fca_status g) {
+                if (g == FCA_ERR_CAPACITY) *refused = true;
+                return g == FCA_ERR_CAPACITY ? FCA_OK : g;
+            };
+            fca_status g;
             uint64_t need = want(c->level_count[lv + 1], c->ratio_big);
-            if (need > c->levels[lv + 1].cap && (s = grow_level(c, lv + 1, false, need, r.st, lim)) != FCA_OK &&
-                s != FCA_ERR_CAPACITY)
-                return s;
+            if (need > c->levels[lv + 1].cap && (g = note(grow_level(c, lv + 1, false, need, r.st, lim))) != FCA_OK)
+                return g;
             if (c->mid_max > SMALL_MAX) {
                 need = want(c->mid_count[lv + 1], c->ratio_mid);
-                if (need > c->mids[lv + 1].cap && (s = grow_level(c, lv + 1, true, need, r.st, lim)) != FCA_OK &&
-                    s != FCA_ERR_CAPACITY)
-                    return s;
+                if (need > c->mids[lv + 1].cap && (g = note(grow_level(c, lv + 1, true, need, r.st, lim))) != FCA_OK)
+                    return g;
             }
             for (int qi = 0; qi < NQ; ++qi) {
                 need = want(c->q_count[qi], c->ratio_q[qi]);
-                if (need > c->q[qi].cap && (s = grow_queue(c, qi, need, r.st, lim)) != FCA_OK &&
-                    s != FCA_ERR_CAPACITY)
-                    return s;
+                if (need > c->q[qi].cap && (g = note(grow_queue(c, qi, need, r.st, lim))) != FCA_OK) return g;
             }
+            return FCA_OK;
+        };
+        bool refused = false;
+        if (c->pregrow && c->ratio_known && (s = grow_ahead((double)(kb + km), same_level, &refused)) != FCA_OK)
+            return s;
+        // a large level whose growth could not be predicted (the first level of a call, or a
+        // prediction past the bound) is first launched on an eighth of its parents, which measures
+        // its children per parent for the rest
+        if (c->pregrow && !same_level && (refused || !c->ratio_known) && hb + hm >= PROBE_MIN_PARENTS) {
+            kb = std::min(kb, std::max<uint64_t>(1, hb / 8));
+            km = std::min(km, std::max<uint64_t>(1, hm / 8));
+            bool r2 = false;
+            if (c->ratio_known && (s = grow_ahead((double)(kb + km), false, &r2)) != FCA_OK) return s;
         }
+        const uint64_t bb = hb - kb, bm = hm - km;
 
         // the next level appends after its current fills; the counters as they are then are kept on
         // the device, to be restored if the launch has to be rolled back (one small kernel)
@@ -756,6 +777,7 @@ fca_status drain(Run &r, size_t lv, bool chain)
             c->ratio_mid = (double)(after.next_mid - c->mid_count[lv + 1]) / parents;
             for (int qi = 0; qi < NQ; ++qi) c->ratio_q[qi] = (double)(after.q_count[qi] - c->q_count[qi]) / parents;
             c->ratio_known = true;
+            c->ratio_lv = lv;
         }
         c->level_count[lv] = bb;
         c->mid_count[lv] = bm;
