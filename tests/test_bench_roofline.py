@@ -47,3 +47,21 @@ def test_roofline_uses_the_dominant_tier_and_both_models(bench, monkeypatch):
     # bitmap model: HBM 4000 B, L2 600 B
     assert r["bitmap_model"]["per_launch"] == pytest.approx(4600.0 / 4)
     assert r["units_per_step"] == {"parents": 1, "closures": 2, "children": 3}
+
+
+def test_cover_counts_are_stored_and_consistent(bench):
+    """The cover-search work counts that the covers stage divides by its time are stored for the
+    workloads it is run on, with one concept per intent of the stored digests and the intersection
+    words at most (M - 0) x W_N per concept (every attribute outside B over at most every word)."""
+    import json
+    digests = json.load(open(os.path.join(ROOT, "tests", "golden", "workload_digests.json")))
+    for name in ("sparse", "zipf", "skewed"):
+        cw = bench.load_cover_counts(name)
+        assert cw is not None, name
+        d = digests[name]
+        assert cw["concepts"] == d["concepts"]
+        wn = (d["n_objects"] + 31) // 32
+        assert cw["extent_words"] == cw["concepts"] * wn
+        assert 0 < cw["isect_words"] <= cw["concepts"] * d["n_attrs"] * wn
+        assert cw["closure_words"] > 0
+    assert bench.load_cover_counts("no such workload") is None
