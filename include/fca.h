@@ -59,7 +59,9 @@ typedef struct {
     uint64_t subtree_launches; /* launches of the object-list kernels */
     uint64_t subtree_word_ops; /* counted work of the object-list tier (FCA_OPT_COUNT_WORK) */
     uint64_t expand_bytes;     /* counted bytes moved by the list and bitmap tiers (FCA_OPT_COUNT_WORK) */
-    uint64_t retries;          /* bitmap-tier launches rolled back because a work pool was full */
+    uint64_t retries;          /* level launches rolled back because a work pool was full (before
+                                  each unchained level launch the pools are grown to what the last
+                                  launch predicts; FCA_PREGROW=0 in the environment turns that off) */
     uint64_t spill_rounds;     /* launch rounds over subtrees spilled by searches past their time
                                   budget (their roots are counted in small_roots) */
     double expand_ms;          /* device time of the bitmap-tier kernel launches */
