@@ -690,9 +690,7 @@ fca_status drain(Run &r, size_t lv, bool chain)
         // level may use the whole pool limit; one from the previous level only half of it (a wrong
         // prediction must not take the memory that the overflow path below may need). Returns
         // whether some destination could not be grown that far.
-        auto grow_ahead = [&](double par, bool same, bool *refused) -> fca_status {
-            const size_t lim = same ? c->pool_limit : c->pool_limit / 2;
-            const double margin = same ? 1.5 : 1.25;
+        auto grow_ahead = [&](double par, size_t lim, double margin, bool *refused) -> fca_status {
             auto want = [&](uint64_t have, double ratio) { return have + (uint64_t)(margin * ratio * par) + 16; };
             auto note = [&](fca_status g) {
                 if (g == FCA_ERR_CAPACITY) *refused = true;
@@ -714,7 +712,9 @@ fca_status drain(Run &r, size_t lv, bool chain)
             return FCA_OK;
         };
         bool refused = false;
-        if (c->pregrow && c->ratio_known && (s = grow_ahead((double)(kb + km), same_level, &refused)) != FCA_OK)
+        if (c->pregrow && c->ratio_known &&
+            (s = grow_ahead((double)(kb + km), same_level ? c->pool_limit : c->pool_limit / 2,
+                            same_level ? 1.5 : 1.25, &refused)) != FCA_OK)
             return s;
         // a large level whose growth could not be predicted (the first level of a call, or a
         // prediction past the bound) is first launched on an eighth of its parents, which measures
@@ -722,8 +722,10 @@ fca_status drain(Run &r, size_t lv, bool chain)
         if (c->pregrow && !same_level && (refused || !c->ratio_known) && hb + hm >= PROBE_MIN_PARENTS) {
             kb = std::min(kb, std::max<uint64_t>(1, hb / 8));
             km = std::min(km, std::max<uint64_t>(1, hm / 8));
+            // the eighth itself: the previous level's prediction, within the whole limit (an eighth
+            // of a wrong prediction costs little)
             bool r2 = false;
-            if (c->ratio_known && (s = grow_ahead((double)(kb + km), false, &r2)) != FCA_OK) return s;
+            if (c->ratio_known && (s = grow_ahead((double)(kb + km), c->pool_limit, 1.25, &r2)) != FCA_OK) return s;
         }
         const uint64_t bb = hb - kb, bm = hm - km;
 
