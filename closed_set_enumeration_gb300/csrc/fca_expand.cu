@@ -292,6 +292,9 @@ __global__ void __launch_bounds__(32 * WARPS, ExpandShape<WARPS>::blocks_per_sm)
     const int span = (d.m + parts - 1) / parts;
     const unsigned long long items = p_count * (unsigned long long)parts;
     __shared__ unsigned long long next_item;
+    // the item's candidates are dealt to its warps one at a time (a fixed stride over the warps left
+    // the block waiting at the next item for the warps that drew the expensive candidates)
+    __shared__ int jclaim;
     // inherited failures (the Fast Close-by-One rule): the parent's witness byte per attribute
     // (0xff: none), updated by the item's own failures, and the level children that receive it
     __shared__ uint32_t bwit[INHERIT ? WIT_WORDS_MAX : 1];
@@ -316,7 +319,10 @@ __global__ void __launch_bounds__(32 * WARPS, ExpandShape<WARPS>::blocks_per_sm)
             __syncthreads();
             if (threadIdx.x == 0) ccount = 0;
         }
-        if (threadIdx.x == 0) next_item = atomicAdd(&a.ctr->work_head, 1ull);
+        if (threadIdx.x == 0) {
+            next_item = atomicAdd(&a.ctr->work_head, 1ull);
+            jclaim = 0;
+        }
         __syncthreads();
         const unsigned long long item = next_item;
         if (item >= items) break;
@@ -409,7 +415,11 @@ __global__ void __launch_bounds__(32 * WARPS, ExpandShape<WARPS>::blocks_per_sm)
             __syncthreads();
             if (COUNT && threadIdx.x == 0) my_bytes += (unsigned long long)na * d.wm * 4;   // rows of A
 
-            for (int j = j_lo + wib; j < j_hi; j += wpb) {
+            for (;;) {
+                int j = 0;
+                if (lane == 0) j = j_lo + atomicAdd(&jclaim, 1);
+                j = __shfl_sync(FULL, j, 0);
+                if (j >= j_hi) break;
                 if ((B[j >> 5] >> (j & 31)) & 1u) continue;   // saturation: A inside column j
                 ++my_closures;
                 if (INHERIT) {
@@ -520,7 +530,11 @@ __global__ void __launch_bounds__(32 * WARPS, ExpandShape<WARPS>::blocks_per_sm)
         }
 
         // ---- gather path: candidates j of this part, warps in turn
-        for (int j = j_lo + wib; j < j_hi; j += wpb) {
+        for (;;) {
+                int j = 0;
+                if (lane == 0) j = j_lo + atomicAdd(&jclaim, 1);
+                j = __shfl_sync(FULL, j, 0);
+                if (j >= j_hi) break;
             if ((B[j >> 5] >> (j & 31)) & 1u) continue;   // saturation: A inside column j
             ++my_closures;
             if (INHERIT) {
