@@ -16,7 +16,12 @@
 //                      emitted once, by the smallest k with C_k = C, and its row index is looked up.
 //                      With at most 64 objects in A, the sets C_k are 64-bit masks over A's objects
 //                      (built from the rows by 32 x 32 bit transposes); above that they are words of
-//                      the object bitmap, restricted to the words where A is not zero.
+//                      the object bitmap, restricted to the words where A is not zero; there the
+//                      supports are counted a few attributes per pass, and the containment tests read
+//                      C_k's compacted words warp-wide and gather several column words at a time, so
+//                      that the loads of one lane are not a chain of dependent round trips. In both
+//                      forms the candidates with an empty C_k (most of them, on sparse tables) are
+//                      settled by one vote: such a C_k is a cover's extent only when all are empty.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -226,7 +231,12 @@ __host__ __device__ inline long long covers_words_per_warp(const Dims &d)
     return (4ll * d.m + 64 + 32 + 64ll * d.wm + (d.m + 1) / 2 + 1) & ~1ll;   // even: R 8-byte aligned
 }
 
-constexpr int COVER_GRAB = 4;   // concepts a warp takes from the work cursor at a time
+// Extents of more than 64 objects: attributes whose supports one pass counts, words of A whose
+// restriction to a column one compaction step forms (per lane), compacted words of a C_k of more
+// than 64 objects one containment step tests (per lane).
+constexpr int SUP_BATCH = 4;
+constexpr int COMPACT_U = 4;
+constexpr int SCAN_BATCH = 8;
 
 struct CoversArgs {
     Dims d;
@@ -265,7 +275,51 @@ __device__ __forceinline__ long long find_intent(const CoversArgs &a, uint32_t D
     return -1;
 }
 
-__global__ void __launch_bounds__(256) covers_kernel(const __grid_constant__ CoversArgs a)
+// The objects of a set kept as its non-zero words (value v[j] of word index wi[j], j < nw) into
+// ids[], ascending; the caller knows there are at most as many as ids[] holds.
+__device__ __forceinline__ void list_objects(const uint32_t *v, const uint32_t *wi, int nw, uint32_t *ids,
+                                             unsigned lane)
+{
+    unsigned off = 0;
+    for (int j0 = 0; j0 < nw; j0 += 32) {
+        const int j = j0 + (int)lane;
+        const uint32_t x0 = j < nw ? v[j] : 0u;
+        const unsigned c = __popc(x0);
+        unsigned pre = c;   // inclusive prefix sum of the popcounts
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned y = __shfl_up_sync(FULL, pre, o);
+            if ((int)lane >= o) pre += y;
+        }
+        unsigned p = off + pre - c;
+        uint32_t x = x0;
+        while (x) {
+            const int b = __ffs(x) - 1;
+            x &= x - 1u;
+            ids[p++] = (uint32_t)(32 * wi[j] + b);
+        }
+        off += __shfl_sync(FULL, pre, 31);
+    }
+    __syncwarp();
+}
+
+// Candidates with an empty C_k: such a C_k is maximal only when every C_k outside B is empty, and the
+// cover is then the bottom concept (extent empty, intent M), emitted by the smallest such k. One vote
+// over the supports (s_k, -1 for k in B) gives both facts to every lane.
+__device__ __forceinline__ void empty_vote(const int *s, int m, unsigned lane, bool *nz_any, int *kmin0)
+{
+    bool nz = false;
+    int kmin = 0x7fffffff;
+    for (int k = (int)lane; k < m; k += 32) {
+        const int sv = s[k];
+        nz |= sv > 0;
+        if (sv == 0 && k < kmin) kmin = k;
+    }
+    *nz_any = __any_sync(FULL, nz);
+    *kmin0 = __reduce_min_sync(FULL, kmin);
+}
+
+__global__ void __launch_bounds__(256, 5) covers_kernel(const __grid_constant__ CoversArgs a)
 {
     extern __shared__ __align__(16) uint32_t lat_smem[];
     const Dims d = a.d;
@@ -285,13 +339,16 @@ __global__ void __launch_bounds__(256) covers_kernel(const __grid_constant__ Cov
     uint16_t *list = reinterpret_cast<uint16_t *>(rowsm + 64 * d.wm);
     const int chunks = (d.m + 31) >> 5;   // = wm
 
+    // One concept per claim, the next one claimed while this one runs: the concepts with large
+    // extents sit next to each other in the enumeration's output, and claims of several at a time
+    // gave some warps a run of them.
+    unsigned long long inext = 0;
+    if (lane == 0) inext = atomicAdd(&a.lc->next, 1ull);
     for (;;) {
-        unsigned long long i0 = 0;
-        if (lane == 0) i0 = atomicAdd(&a.lc->next, (unsigned long long)COVER_GRAB);
-        i0 = __shfl_sync(FULL, i0, 0);
-        if (i0 >= a.count) break;
-        const unsigned long long i1 = i0 + COVER_GRAB < a.count ? i0 + COVER_GRAB : a.count;
-        for (unsigned long long i = i0; i < i1; ++i) {
+        const unsigned long long i = __shfl_sync(FULL, inext, 0);
+        if (i >= a.count) break;
+        if (lane == 0) inext = atomicAdd(&a.lc->next, 1ull);
+        {
             // B: lane w holds word w
             const uint32_t Bw = (int)lane < d.wm ? a.intents[i * d.wm + lane] & valid_bits(lane, d.wm, d.m) : 0u;
 
@@ -321,30 +378,11 @@ __global__ void __launch_bounds__(256) covers_kernel(const __grid_constant__ Cov
             __syncwarp();
 
             int ne = 0;   // covers found for concept i (rows in eb)
+            bool nz_any = false;   // some C_k outside B is not empty
+            int kmin0 = 0;         // the smallest k outside B with C_k empty
             const bool small = objs <= 64;
             if (small) {
-                // object ids of A (at most 64; every non-zero word holds at least one object)
-                unsigned off = 0;
-                for (int j0 = 0; j0 < nnz; j0 += 32) {
-                    const int j = j0 + (int)lane;
-                    const uint32_t v = j < nnz ? Aw[j] : 0u;
-                    const unsigned c = __popc(v);
-                    unsigned pre = c;   // inclusive prefix sum of the popcounts
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const unsigned y = __shfl_up_sync(FULL, pre, o);
-                        if ((int)lane >= o) pre += y;
-                    }
-                    unsigned p = off + pre - c;
-                    uint32_t x = v;
-                    while (x) {
-                        const int b = __ffs(x) - 1;
-                        x &= x - 1u;
-                        ids[p++] = (uint32_t)(32 * Ai[j] + b);
-                    }
-                    off += __shfl_sync(FULL, pre, 31);
-                }
-                __syncwarp();
+                list_objects(Aw, Ai, nnz, ids, lane);   // object ids of A (at most 64)
                 // the rows of A's objects (processing order), then the restricted sets by attribute:
                 // R[k] bit o = object ids[o] has attribute k (inv maps a position back to its attribute)
                 for (int x = (int)lane; x < objs * d.wm; x += 32) {
@@ -367,6 +405,7 @@ __global__ void __launch_bounds__(256) covers_kernel(const __grid_constant__ Cov
                     if (k < d.m) s[k] = inB ? -1 : __popcll(R[k]);
                 }
                 __syncwarp();
+                empty_vote(s, d.m, lane, &nz_any, &kmin0);
                 // the covers: candidates k whose C_k is maximal among the C_k and that are the smallest
                 // attribute of their class (no other k2 has C_k inside C_k2 with more objects, or the
                 // same set and a smaller index). The k2 with C_k inside C_k2 are the attributes of
@@ -376,7 +415,9 @@ __global__ void __launch_bounds__(256) covers_kernel(const __grid_constant__ Cov
                     const int k = 32 * c + (int)lane;
                     const int sk = k < d.m ? s[k] : -1;
                     bool bad = sk < 0;
-                    if (!bad) {
+                    if (sk == 0) {
+                        bad = nz_any || k != kmin0;
+                    } else if (!bad) {
                         const unsigned long long Rk = R[k];
                         for (int t = 0; t < d.wm && !bad; ++t) {
                             uint32_t dk = valid_bits(t, d.wm, d.m);
@@ -424,7 +465,8 @@ __global__ void __launch_bounds__(256) covers_kernel(const __grid_constant__ Cov
                     }
                 }
             } else {
-                // supports, one attribute at a time, lanes over A's non-zero words
+                // supports, SUP_BATCH attributes per pass: lanes over A's non-zero words, each word of
+                // A read once per pass and the batch's column words gathered together
                 for (int c = 0; c < chunks; ++c) {
                     const int k = 32 * c + (int)lane;
                     if (k < d.m) s[k] = -1;
@@ -433,60 +475,145 @@ __global__ void __launch_bounds__(256) covers_kernel(const __grid_constant__ Cov
                 for (int c = 0; c < chunks; ++c) {
                     uint32_t cand = ~__shfl_sync(FULL, Bw, c) & valid_bits(c, d.wm, d.m);
                     while (cand) {
-                        const int k = 32 * c + __ffs(cand) - 1;
-                        cand &= cand - 1u;
-                        const uint32_t *col = a.cols + (size_t)k * d.wnp;
-                        unsigned cnt = 0;
-                        for (int j = (int)lane; j < nnz; j += 32) cnt += __popc(Aw[j] & __ldg(col + Ai[j]));
-                        cnt = __reduce_add_sync(FULL, cnt);
-                        if (lane == 0) s[k] = (int)cnt;
+                        int kk[SUP_BATCH];
+                        const uint32_t *colb[SUP_BATCH];
+#pragma unroll
+                        for (int u = 0; u < SUP_BATCH; ++u) {
+                            kk[u] = cand ? 32 * c + __ffs(cand) - 1 : -1;
+                            cand &= cand - 1u;
+                            colb[u] = a.cols + (size_t)(kk[u] < 0 ? kk[0] : kk[u]) * d.wnp;   // kk[0] >= 0
+                        }
+                        unsigned cnt[SUP_BATCH];
+#pragma unroll
+                        for (int u = 0; u < SUP_BATCH; ++u) cnt[u] = 0u;
+#pragma unroll 2
+                        for (int j = (int)lane; j < nnz; j += 32) {
+                            const uint32_t aw = Aw[j];
+                            const uint32_t ai = Ai[j];
+#pragma unroll
+                            for (int u = 0; u < SUP_BATCH; ++u) cnt[u] += __popc(aw & __ldg(colb[u] + ai));
+                        }
+#pragma unroll
+                        for (int u = 0; u < SUP_BATCH; ++u) {
+                            const unsigned t = __reduce_add_sync(FULL, cnt[u]);
+                            if (lane == 0 && kk[u] >= 0) s[kk[u]] = (int)t;
+                        }
                     }
                 }
                 __syncwarp();
-                // each candidate in turn: C_k's non-zero words compacted, then lanes take the k2 and
-                // test C_k inside column k2 on those words only
+                empty_vote(s, d.m, lane, &nz_any, &kmin0);
+                // each candidate k in turn. Only attributes k2 outside B with s_k2 >= s_k can hold C_k
+                // (C_k inside C_k2 gives |C_k| <= |C_k2|); with none, C_k is maximal, the smallest of
+                // its class, and its cover's intent is B + {k}. Otherwise C_k's non-zero words are
+                // compacted and lanes take the k2 and test C_k inside column k2 on those words only,
+                // the warp reading the compacted words together and gathering SCAN_BATCH of them at a time.
                 for (int c = 0; c < chunks; ++c) {
                     uint32_t cand = ~__shfl_sync(FULL, Bw, c) & valid_bits(c, d.wm, d.m);
                     while (cand) {
                         const int k = 32 * c + __ffs(cand) - 1;
                         cand &= cand - 1u;
                         const int sk = s[k];
-                        const uint32_t *col = a.cols + (size_t)k * d.wnp;
-                        int cnz = 0;
-                        for (int j0 = 0; j0 < nnz; j0 += 32) {
-                            const int j = j0 + (int)lane;
-                            const uint32_t v = j < nnz ? Aw[j] & __ldg(col + Ai[j]) : 0u;
-                            const unsigned nzb = __ballot_sync(FULL, v != 0u);
-                            if (v) {
-                                const int p = cnz + __popc(nzb & ((1u << lane) - 1u));
-                                Cv[p] = v;
-                                Ci[p] = Ai[j];
-                            }
-                            cnz += __popc(nzb);
-                        }
-                        __syncwarp();
-                        bool bad = false;
                         uint32_t Dw = Bw;
-                        for (int c2 = 0; c2 < chunks && !bad; ++c2) {
-                            const int k2 = 32 * c2 + (int)lane;
-                            bool in = false;
-                            if (k2 < d.m && k2 != k && s[k2] >= sk) {   // s < 0 for attributes of B
-                                const uint32_t *col2 = a.cols + (size_t)k2 * d.wnp;
-                                in = true;
-                                for (int j = 0; j < cnz; ++j) {
-                                    if (Cv[j] & ~__ldg(col2 + Ci[j])) {
-                                        in = false;
-                                        break;
-                                    }
-                                }
-                                if (in && (s[k2] > sk || k2 < k)) bad = true;
+                        bool any_holder = false;
+                        if (sk == 0) {
+                            if (nz_any || k != kmin0) continue;
+                            Dw = (int)lane < d.wm ? valid_bits(lane, d.wm, d.m) : 0u;   // the bottom: M
+                        } else {
+                            for (int c2 = 0; c2 < chunks; ++c2) {
+                                const int k2 = 32 * c2 + (int)lane;
+                                any_holder |= k2 < d.m && k2 != k && s[k2] >= sk;   // s < 0 for attributes of B
                             }
-                            bad = __any_sync(FULL, bad);
-                            const uint32_t word = __ballot_sync(FULL, in);
-                            if ((int)lane == c2) Dw |= word;
                         }
-                        __syncwarp();
-                        if (bad) continue;
+                        if (__any_sync(FULL, any_holder)) {
+                            const uint32_t *col = a.cols + (size_t)k * d.wnp;
+                            int cnz = 0;
+                            __syncwarp();
+                            for (int j0 = 0; j0 < nnz; j0 += 32 * COMPACT_U) {
+                                uint32_t v[COMPACT_U], wi[COMPACT_U];
+#pragma unroll
+                                for (int u = 0; u < COMPACT_U; ++u) {
+                                    const int j = j0 + 32 * u + (int)lane;
+                                    v[u] = j < nnz ? Aw[j] : 0u;   // A's listed words are non-zero
+                                    wi[u] = j < nnz ? Ai[j] : 0u;
+                                }
+#pragma unroll
+                                for (int u = 0; u < COMPACT_U; ++u) v[u] = v[u] ? v[u] & __ldg(col + wi[u]) : 0u;
+#pragma unroll
+                                for (int u = 0; u < COMPACT_U; ++u) {
+                                    const unsigned nzb = __ballot_sync(FULL, v[u] != 0u);
+                                    if (v[u]) {
+                                        const int p = cnz + __popc(nzb & ((1u << lane) - 1u));
+                                        Cv[p] = v[u];
+                                        Ci[p] = wi[u];
+                                    }
+                                    cnz += __popc(nzb);
+                                }
+                            }
+                            __syncwarp();
+                            bool bad = false;
+                            if (sk <= 64) {
+                                // D_k = C_k' (processing positions, lane t holds word t): the AND of
+                                // the rows of C_k's objects, at most two per lane; the k2 holding C_k
+                                // are the attributes of D_k outside B
+                                list_objects(Cv, Ci, cnz, ids, lane);
+                                const uint32_t o0 = (int)lane < sk ? ids[lane] : 0u;
+                                const uint32_t o1 = (int)lane + 32 < sk ? ids[lane + 32] : 0u;
+                                uint32_t Dp = 0u;
+#pragma unroll 4
+                                for (int t = 0; t < d.wm; ++t) {
+                                    uint32_t v = (int)lane < sk ? __ldg(a.rows + (size_t)o0 * d.wm + t) : FULL;
+                                    if ((int)lane + 32 < sk) v &= __ldg(a.rows + (size_t)o1 * d.wm + t);
+                                    v = __reduce_and_sync(FULL, v);
+                                    if ((int)lane == t) Dp = v;
+                                }
+                                for (int c2 = 0; c2 < chunks; ++c2) {
+                                    const int k2 = 32 * c2 + (int)lane;
+                                    const int p = k2 < d.m ? (a.perm ? a.perm[k2] : k2) : 0;
+                                    const uint32_t wd = __shfl_sync(FULL, Dp, p >> 5);
+                                    const bool held = k2 < d.m && k2 != k && s[k2] >= 0 && ((wd >> (p & 31)) & 1u);
+                                    if (held && (s[k2] > sk || k2 < k)) bad = true;
+                                    const uint32_t word = __ballot_sync(FULL, held);
+                                    if ((int)lane == c2) Dw |= word;
+                                }
+                                bad = __any_sync(FULL, bad);
+                            } else {
+                                for (int c2 = 0; c2 < chunks && !bad; ++c2) {
+                                    const int k2 = 32 * c2 + (int)lane;
+                                    bool held = k2 < d.m && k2 != k && s[k2] >= sk;
+                                    const uint32_t *col2 = a.cols + (size_t)(held ? k2 : 0) * d.wnp;
+                                    for (int j0 = 0; j0 < cnz && __any_sync(FULL, held); j0 += 32) {
+                                        const int jl = j0 + (int)lane;
+                                        const uint32_t myv = jl < cnz ? Cv[jl] : 0u;
+                                        const uint32_t myi = jl < cnz ? Ci[jl] : 0u;
+                                        int u0 = 0;
+                                        if (j0 == 0) {
+                                            // most k2 miss C_k on its first word: test that word alone
+                                            const uint32_t cv = __shfl_sync(FULL, myv, 0);
+                                            const uint32_t ci = __shfl_sync(FULL, myi, 0);
+                                            if (held && (cv & ~__ldg(col2 + ci))) held = false;
+                                            u0 = 1;
+                                        }
+                                        for (; u0 < 32 && j0 + u0 < cnz && __any_sync(FULL, held); u0 += SCAN_BATCH) {
+                                            uint32_t viol = 0u;
+#pragma unroll
+                                            for (int u = 0; u < SCAN_BATCH; ++u) {
+                                                const int src = u0 + u;
+                                                const uint32_t cv = __shfl_sync(FULL, myv, src & 31);
+                                                const uint32_t ci = __shfl_sync(FULL, myi, src & 31);
+                                                if (held && src < 32 && cv) viol |= cv & ~__ldg(col2 + ci);
+                                            }
+                                            held = held && viol == 0u;
+                                        }
+                                    }
+                                    if (held && (s[k2] > sk || k2 < k)) bad = true;
+                                    bad = __any_sync(FULL, bad);
+                                    const uint32_t word = __ballot_sync(FULL, held);
+                                    if ((int)lane == c2) Dw |= word;
+                                }
+                            }
+                            __syncwarp();
+                            if (bad) continue;
+                        }
                         if ((int)lane == (k >> 5)) Dw |= 1u << (k & 31);
                         const long long row = find_intent(a, Dw, lane);
                         if (row < 0) {

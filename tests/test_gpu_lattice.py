@@ -40,7 +40,8 @@ def chain(n):
 
 
 # shapes straddle the word boundaries of objects and attributes and the 64-object switch of the
-# cover kernel (its extents of at most 64 objects are 64-bit masks, larger ones object bitmaps)
+# cover kernel (its extents of at most 64 objects are 64-bit masks, larger ones object bitmaps; the
+# cover cases of 2 100 and 5 000 objects give compacted sub-extents of more than 32 and 128 words)
 EXT_CASES = [(1, 1, 0.5, 0), (31, 7, 0.3, 1), (33, 31, 0.3, 2), (64, 65, 0.12, 3), (65, 20, 0.3, 4),
              (130, 64, 0.12, 5), (257, 45, 0.2, 6), (1500, 40, 0.12, 7), (600, 96, 0.12, 8), (40, 1000, 0.02, 9)]
 
@@ -109,7 +110,8 @@ def edge_set(e):
 COVER_CASES = [("contranominal", 10), ("identity", 40), ("chain", 33), ("random", (60, 12, 0.35, 5)),
                ("random", (100, 20, 0.2, 6)), ("random", (200, 40, 0.15, 7)), ("random", (64, 33, 0.3, 8)),
                ("random", (65, 70, 0.12, 9)), ("random", (300, 45, 0.1, 10)), ("random", (1000, 30, 0.1, 11)),
-               ("random", (40, 1000, 0.02, 9))]
+               ("random", (40, 1000, 0.02, 9)), ("random", (2100, 28, 0.1, 14)), ("random", (5000, 16, 0.15, 12)),
+               ("divisors", (5000, 24))]
 
 
 def cover_context(kind, arg):
@@ -119,6 +121,13 @@ def cover_context(kind, arg):
         return cx.identity(arg), arg, arg
     if kind == "chain":
         return chain(arg), arg, arg
+    if kind == "divisors":
+        # object o (1..n) has attribute a when a + 1 divides o: nested columns (the multiples of 4 lie
+        # inside the multiples of 2) spread over every word of the object bitmap, so containment tests
+        # of large extents run to the last word
+        n, m = arg
+        o = np.arange(1, n + 1)[:, None]
+        return cx.pack_rows(o % np.arange(2, m + 2)[None, :] == 0), n, m
     n, m, p, s = arg
     return cx.random_context(n, m, p, s), n, m
 
