@@ -671,15 +671,27 @@ size_t covers_smem_per_warp(const Dims &d) { return (size_t)covers_words_per_war
 
 int covers_shape(const Dims &d, uint64_t count, int sm_count, int *wpb, unsigned *blocks, size_t *smem)
 {
+    // Each warp holds its own shared memory, so the block size only decides how much of an SM's
+    // shared memory blocks can fill: take the size (at most 8 warps) with the most warps resident.
     const size_t per_warp = covers_smem_per_warp(d);
-    *wpb = (int)std::max<size_t>(1, std::min<size_t>(8, (200 * 1024) / per_warp));
-    *smem = per_warp * *wpb;
-    if (*smem > 227 * 1024) return (int)cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(covers_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)*smem);
+    const size_t limit = 227 * 1024;
+    if (per_warp > limit) return (int)cudaErrorInvalidValue;
+    const int wmax = (int)std::min<size_t>(8, limit / per_warp);
+    cudaError_t e =
+        cudaFuncSetAttribute(covers_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)(per_warp * wmax));
     if (e != cudaSuccess) return (int)e;
-    int per_sm = 1;
-    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, covers_kernel, *wpb * 32, *smem)) != cudaSuccess)
-        return (int)e;
+    int per_sm = 0, best = -1;
+    for (int w = wmax; w >= 1; --w) {
+        int b = 0;
+        if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, covers_kernel, w * 32, per_warp * w)) != cudaSuccess)
+            return (int)e;
+        if (b * w > best) {
+            best = b * w;
+            *wpb = w;
+            per_sm = b;
+        }
+    }
+    *smem = per_warp * *wpb;
     per_sm = std::max(1, per_sm);
     *blocks = (unsigned)std::max<unsigned long long>(
         1, std::min<unsigned long long>((std::max<uint64_t>(count, 1) + *wpb - 1) / *wpb,
