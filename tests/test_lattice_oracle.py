@@ -15,7 +15,10 @@ textbook contexts and against a pure-Python set enumeration on tiny contexts, ne
 - the rule the cover kernel computes (lower covers = the maximal distinct restrictions A & {k}',
   each with intent B plus the attributes giving the same set), restated with Python sets, equals
   the oracle's cover relation; and the oracle's two formulations (whole relation, one concept's
-  lower covers) agree on a thousand-concept lattice.
+  lower covers) agree on a thousand-concept lattice;
+- the facts behind the cover kernel's shortcuts hold in the oracle's relation: an empty restriction
+  is a cover's extent only when all restrictions are empty (the one cover is then the concept with
+  the empty extent), and the attributes holding a non-empty restriction are those its objects share.
 """
 import itertools
 
@@ -231,6 +234,38 @@ def test_maximal_restrictions_give_the_covers(n, m, p, seed):
     intents = oracle.cbo(rows, n, m)["intents"]
     assert covers_by_maximal_restrictions(rows, n, m, intents) == \
         sorted(map(tuple, lattice.cover_edges(intents, m).tolist()))
+
+
+@pytest.mark.parametrize("n,m,p,seed", [(20, 8, 0.4, 1), (40, 12, 0.3, 2), (70, 40, 0.2, 3), (30, 10, 0.05, 5)])
+def test_empty_restrictions_and_row_closures(n, m, p, seed):
+    """The two facts the cover kernel's shortcuts rest on, against the oracle's cover relation. An
+    empty C_k = A & {k}' is a lower cover's extent only when every C_k outside B is empty, and then
+    the concept's one lower cover has the empty extent. The attributes k2 outside B whose C_k2 holds
+    a non-empty C_k are exactly those common to all of C_k's objects."""
+    rows = cx.random_context(n, m, p, seed)
+    cells = cx.unpack_rows(rows, m)
+    intents = oracle.cbo(rows, n, m)["intents"]
+    sets = intent_sets(intents, m)
+    lower = {}
+    for i, j in lattice.cover_edges(intents, m).tolist():
+        lower.setdefault(i, []).append(j)
+    seen_all_empty = seen_some = 0
+    for i, b in enumerate(sets):
+        a = frozenset(o for o in range(n) if all(cells[o][x] for x in b))
+        c = {k: frozenset(o for o in a if cells[o][k]) for k in range(m) if k not in b}
+        cover_extents = [frozenset(o for o in range(n) if all(cells[o][x] for x in sets[j]))
+                         for j in lower.get(i, [])]
+        if c and all(not ck for ck in c.values()):
+            seen_all_empty += 1
+            assert cover_extents == [frozenset()]
+        elif c:
+            seen_some += 1
+            assert frozenset() not in cover_extents
+        for k, ck in c.items():
+            if ck:
+                common = {x for x in range(m) if all(cells[o][x] for o in ck)}
+                assert common - b == {k2 for k2, c2 in c.items() if ck <= c2}
+    assert seen_all_empty and seen_some
 
 
 def test_two_cover_formulations_agree_at_a_thousand_concepts():
